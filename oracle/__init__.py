@@ -1,0 +1,177 @@
+"""Python access to the CPU oracle (TEST INFRASTRUCTURE ONLY).
+
+The oracle is plain single-threaded C (oracle.c) restating the method from
+its pages.  Only tests, the smoke check and the benchmark's CPU-baseline leg
+may import this module; the CUDA library never does.  Arrays are numpy;
+bf16 data is passed as its uint16 bit pattern.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(HERE, "oracle.c")
+HDR = os.path.join(HERE, "oracle.h")
+LIB = os.path.join(HERE, "liboracle.so")
+
+BF16, FP32 = 0, 1
+GREEDY, SAMPLE = 0, 1
+STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
+STREAM_DRAFT, STREAM_ACCEPT, STREAM_RESID, STREAM_BONUS = 0, 1, 2, 3
+FLAG_TIER_UNCAPTURED = 2
+FLAG_INEXACT_MARKOV = 16
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (-O2 -ffp-contract=off, single-threaded)."""
+    newest = max(os.path.getmtime(SRC), os.path.getmtime(HDR))
+    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < newest:
+        tmp = LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11",
+                               "-fPIC", "-shared", "-o", tmp, SRC, "-lm"])
+        os.replace(tmp, LIB)
+    return LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = ctypes.CDLL(LIB)
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _dt(arr) -> int:
+    return BF16 if arr.dtype == np.uint16 else FP32
+
+
+def philox(ctr, key):
+    out = np.zeros(4, np.uint32)
+    lib().orc_philox4x32_10(_p(_c(ctr, np.uint32)), _p(_c(key, np.uint32)), _p(out))
+    return out
+
+
+def uniform(seed, cycle, stream, req, row, v) -> float:
+    f = lib().orc_uniform
+    f.restype = ctypes.c_double
+    return f(ctypes.c_uint64(seed), ctypes.c_uint64(cycle), ctypes.c_int(stream),
+             ctypes.c_uint32(req), ctypes.c_uint32(row), ctypes.c_uint32(v))
+
+
+def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0, req_ids=None):
+    """L [R,B,V] (uint16 bf16 bits or float32), U [V,r], W [r,V] uint16."""
+    R, B, V = L.shape
+    r = U.shape[1]
+    L = np.ascontiguousarray(L)
+    tokens = np.zeros((R, B), np.int32)
+    logq = np.zeros((R, B), np.float64)
+    lse = np.zeros((R, B), np.float64)
+    margin = np.zeros((R, B), np.float64)
+    ids = None if req_ids is None else _c(req_ids, np.int32)
+    flags = lib().orc_draft_chain(
+        _p(L), _dt(L), _p(_c(U, np.uint16)), _p(_c(W, np.uint16)), _p(_c(anchor, np.int32)), _p(ids),
+        R, B, V, r, decode, ctypes.c_double(temperature), ctypes.c_uint64(seed), ctypes.c_uint64(cycle),
+        _p(tokens), _p(logq), _p(lse), _p(margin))
+    return dict(tokens=tokens, logq=logq, lse=lse, margin=margin, flags=flags)
+
+
+def draft_tree(L, U, W, anchor, k, P, N):
+    R, B, V = L.shape
+    r = U.shape[1]
+    L = np.ascontiguousarray(L)
+    S = N + 1
+    words = (S + 31) // 32
+    tok = np.zeros((R, S), np.int32)
+    parent = np.zeros((R, S), np.int32)
+    depth = np.zeros((R, S), np.int32)
+    score = np.zeros((R, S), np.float64)
+    mask = np.zeros((R, S, words), np.uint32)
+    n_nodes = np.zeros(R, np.int32)
+    margin = np.zeros(R, np.float64)
+    flags = lib().orc_draft_tree(
+        _p(L), _dt(L), _p(_c(U, np.uint16)), _p(_c(W, np.uint16)), _p(_c(anchor, np.int32)),
+        R, B, V, r, k, P, N, _p(tok), _p(parent), _p(depth), _p(score), _p(mask), _p(n_nodes), _p(margin))
+    return dict(tok=tok, parent=parent, depth=depth, score=score, mask=mask, n_nodes=n_nodes,
+                margin=margin, flags=flags)
+
+
+def schedule_budget(conf, cost):
+    R, g = conf.shape
+    survival = np.zeros((R, g), np.float32)
+    budget = np.zeros(R, np.int32)
+    expected = np.zeros(1, np.float64)
+    total = np.zeros(1, np.int32)
+    m_star = np.zeros(1, np.int32)
+    lib().orc_schedule_budget(_p(_c(conf, np.float32)), R, g, _p(_c(cost, np.float64)), _p(survival),
+                              _p(budget), _p(expected), _p(total), _p(m_star))
+    return dict(survival=survival, budget=budget, expected=float(expected[0]), total_tokens=int(total[0]),
+                m_star=int(m_star[0]))
+
+
+def pack_ragged(anchor, draft, budget, tiers):
+    R, g = draft.shape
+    tiers = _c(tiers, np.int32)
+    cap = max(int(tiers.max()) if tiers.size else 0, R * (g + 1))
+    cu = np.zeros(R + 1, np.int32)
+    ptok = np.full(cap, -7, np.int32)
+    preq = np.full(cap, -7, np.int32)
+    ppos = np.full(cap, -7, np.int32)
+    tier = np.zeros(1, np.int32)
+    flags = np.zeros(1, np.int32)
+    b = None if budget is None else _c(budget, np.int32)
+    rc = lib().orc_pack_ragged(_p(_c(anchor, np.int32)), _p(_c(draft, np.int32)), _p(b), R, g,
+                               _p(tiers), tiers.size, _p(cu), _p(ptok), _p(preq), _p(ppos), _p(tier), _p(flags))
+    if rc != 0:
+        raise ValueError("pack_ragged: budget out of range")
+    t = int(tier[0])
+    return dict(cu_seqlens=cu, packed_tok=ptok[:t], packed_req=preq[:t], packed_pos=ppos[:t], tier=t,
+                flags=int(flags[0]))
+
+
+def verify(mode, decode, target, cu_seqlens, anchor, draft, budget=None, logq=None, lse_q=None,
+           L=None, U=None, W=None, temperature=1.0, seed=0, cycle=0):
+    """target [rows, V] packed (uint16 bf16 bits or float32)."""
+    R, g = draft.shape
+    V = target.shape[-1]
+    target = np.ascontiguousarray(target)
+    accept = np.zeros(R, np.int32)
+    ceiling = np.zeros(R, np.int32)
+    out_tok = np.zeros((R, g + 1), np.int32)
+    n_out = np.zeros(R, np.int32)
+    margin = np.zeros(R, np.float64)
+    r = 0 if U is None else U.shape[1]
+    Lc = None if L is None else np.ascontiguousarray(L)
+    flags = lib().orc_verify(
+        mode, decode, ctypes.c_double(temperature), ctypes.c_uint64(seed), ctypes.c_uint64(cycle),
+        _p(target), _dt(target), _p(_c(cu_seqlens, np.int32)), _p(_c(anchor, np.int32)), _p(_c(draft, np.int32)),
+        _p(None if budget is None else _c(budget, np.int32)),
+        _p(None if logq is None else _c(logq, np.float64)), _p(None if lse_q is None else _c(lse_q, np.float64)),
+        _p(Lc), 0 if Lc is None else _dt(Lc), _p(None if U is None else _c(U, np.uint16)),
+        _p(None if W is None else _c(W, np.uint16)), r, R, g, V,
+        _p(accept), _p(ceiling), _p(out_tok), _p(n_out), _p(margin))
+    return dict(accept=accept, ceiling=ceiling, out_tok=out_tok, n_out=n_out, margin=margin, flags=flags)
+
+
+def verify_tree(target, tok, parent, n_nodes, B):
+    R, S, V = target.shape
+    target = np.ascontiguousarray(target)
+    accept = np.zeros(R, np.int32)
+    out_tok = np.zeros((R, B + 1), np.int32)
+    n_out = np.zeros(R, np.int32)
+    lib().orc_verify_tree(_p(target), _dt(target), _p(_c(tok, np.int32)), _p(_c(parent, np.int32)),
+                          _p(_c(n_nodes, np.int32)), R, S - 1, B, V, _p(accept), _p(out_tok), _p(n_out))
+    return dict(accept=accept, out_tok=out_tok, n_out=n_out)

@@ -1,0 +1,103 @@
+/*
+ * oracle.h - CPU oracle for the DSpark / PCTree speculative-decoding hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded C
+ * restatement of what the method computes, written from the pages that
+ * describe it.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline leg may load it.  It shares no code, header or table with the
+ * CUDA library (speculative_decoding_markov_gb300/csrc) and the library never
+ * calls it.
+ *
+ * Page keys used in the citations below:
+ *   [DSpark notes]  LayerX ML study-group notes 2026-06-30, "DSpark:
+ *                   Confidence-Scheduled Speculative Decoding with
+ *                   Semi-Autoregressive Generation", sections 1-9.
+ *   [PCTree]        Qiita article on PCTree (Parent-Conditioned Drafting
+ *                   Tree), section "a linear draft wastes everything after
+ *                   the first miss".
+ *   [SGLang]        winzheng.jp, "DSpark in SGLang", sections "SPS cost
+ *                   table", "three verify modes", "ragged verify".
+ *
+ * Conventions shared with the library's C-ABI (they are conventions of the
+ * interface, restated here independently):
+ *   - bf16 values are passed as raw uint16 bit patterns;
+ *   - L is [R, B, V] (request, draft position d-1, vocab), row-major;
+ *   - U is [V, r], W is [r, V], both bf16;
+ *   - the random numbers the method draws come from Philox4x32-10 (Salmon et
+ *     al., SC'11) keyed by (seed, cycle); see orc_uniform().
+ * Precision: the Markov product and every log/exp/ratio are in double; the
+ * combined logit z = L + Markov is an fp32 addition (the pages keep logits in
+ * the drafter's float type), so argmax decisions are taken on the same fp32
+ * values the kernel sees.  Survival products are fp32 multiplies, expected
+ * token counts fp64 sums.
+ */
+#ifndef SDM_ORACLE_H
+#define SDM_ORACLE_H
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_BF16 = 0, ORC_FP32 = 1 };
+enum { ORC_GREEDY = 0, ORC_SAMPLE = 1 };
+enum { ORC_STATIC = 0, ORC_COMPACT = 1, ORC_CAP_ACCEPT = 2 };
+enum { ORC_STREAM_DRAFT = 0, ORC_STREAM_ACCEPT = 1, ORC_STREAM_RESID = 2, ORC_STREAM_BONUS = 3 };
+/* flag bits returned through *flags */
+enum { ORC_FLAG_TIER_UNCAPTURED = 2, ORC_FLAG_INEXACT_MARKOV = 16 };
+
+/* Philox4x32-10 block function, straight from its published definition. */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+/* The uniform in (0,1) for (stream, request, row, vocab id v). */
+double orc_uniform(uint64_t seed, uint64_t cycle, int stream, uint32_t req, uint32_t row, uint32_t v);
+
+/* Markov-head chain draft.  req_ids (may be NULL = 0..R-1) gives the global
+ * request index used for the random counters, so a subset of requests can be
+ * drafted on its own.  logq, lse, margin may be NULL. */
+int orc_draft_chain(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
+                    const int32_t* anchor, const int32_t* req_ids, int R, int B, int V, int r,
+                    int decode, double temperature, uint64_t seed, uint64_t cycle,
+                    int32_t* tokens, double* logq, double* lse, double* margin);
+
+/* PCTree drafting.  Outputs hold N+1 slots per request (slot 0 = root);
+ * mask holds ceil((N+1)/32) words per node row.  margin[i] = smallest score
+ * gap at a prune or top-N boundary of request i (may be NULL). */
+int orc_draft_tree(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
+                   const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N,
+                   int32_t* tok, int32_t* parent, int32_t* depth, double* score,
+                   uint32_t* mask, int32_t* n_nodes, double* margin);
+
+/* Survival product and the throughput-maximising prefix budget. */
+int orc_schedule_budget(const float* conf, int R, int gamma, const double* cost,
+                        float* survival, int32_t* budget, double* expected,
+                        int32_t* total_tokens, int32_t* m_star);
+
+/* Ragged front-pack of the verify windows.  budget == NULL means the full
+ * block (n_i = gamma).  Packed arrays need max(tiers[-1], R*(gamma+1)) slots. */
+int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,
+                    int R, int gamma, const int32_t* tiers, int n_tiers,
+                    int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
+                    int32_t* packed_pos, int32_t* tier, int32_t* flags);
+
+/* Verification over packed target logits [rows, V].  budget is only read in
+ * cap-accept mode; logq/lse_q/L/U/W/r only in sample mode.  margin[i] = the
+ * smallest decision margin met for request i (may be NULL). */
+int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t cycle,
+               const void* target, int dtT, const int32_t* cu_seqlens,
+               const int32_t* anchor, const int32_t* draft, const int32_t* budget,
+               const double* logq, const double* lse_q,
+               const void* L, int dtL, const uint16_t* U, const uint16_t* W, int r,
+               int R, int gamma, int V,
+               int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+               double* margin);
+
+/* Greedy verification of a drafted tree: target is [R, N+1, V], one row per
+ * tree slot.  out_tok holds B+1 slots per request. */
+int orc_verify_tree(const void* target, int dtT, const int32_t* tok, const int32_t* parent,
+                    const int32_t* n_nodes, int R, int N, int B, int V,
+                    int32_t* accept, int32_t* out_tok, int32_t* n_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,591 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: known-answer
+vectors, the worked example of the DSpark notes' Figure 1, closed forms
+(losslessness: speculative greedy decoding equals target-only greedy
+decoding), brute force on tiny inputs, special cases that reduce to a library
+routine, and chi-square tests of the samplers.
+"""
+from __future__ import annotations
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy import special, stats
+
+import oracle
+from speculative_decoding_markov_gb300 import synthetic
+from speculative_decoding_markov_gb300.workloads import BF16, FP32
+from tests.helpers import (absolute_inputs, cycle_inputs, np_of, oracle_greedy_decode, small,
+                           target_only_greedy)
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---------------------------------------------------------------------------
+# Philox4x32-10 and the uniforms
+# ---------------------------------------------------------------------------
+def test_philox_known_answers():
+    rows = [l.split() for l in open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) if l.strip() and l[0] != "#"]
+    assert len(rows) == 3
+    for row in rows:
+        vals = [int(x, 16) for x in row]
+        out = oracle.philox(vals[0:4], vals[4:6])
+        assert [int(x) for x in out] == vals[6:10]
+
+
+def test_uniform_grid_and_moments():
+    us = np.array([oracle.uniform(7, 3, oracle.STREAM_DRAFT, i, 2, v) for i in range(40) for v in range(100)])
+    assert np.all(us > 0) and np.all(us < 1)
+    k = us * 2 ** 24
+    assert np.all(k == np.round(k)) and np.all(np.round(k) % 2 == 1)      # odd multiples of 2^-24
+    assert abs(us.mean() - 0.5) < 0.02 and abs(us.var() - 1 / 12) < 0.01
+    # the four words of one block serve v = 4c .. 4c+3; a new block for each field
+    assert oracle.uniform(1, 0, 0, 0, 0, 0) != oracle.uniform(1, 0, 0, 0, 0, 1)
+    assert oracle.uniform(1, 0, 0, 0, 0, 0) != oracle.uniform(1, 0, 1, 0, 0, 0)
+    assert oracle.uniform(1, 0, 0, 0, 0, 0) != oracle.uniform(1, 1, 0, 0, 0, 0)
+    assert oracle.uniform(1, 0, 0, 0, 0, 0) != oracle.uniform(2, 0, 0, 0, 0, 0)
+
+
+def test_uniform_uses_block_words_as_documented():
+    blk = oracle.philox([1, 5, (oracle.STREAM_RESID << 16) | 3, 9], [11, 0])
+    for w in range(4):
+        u = oracle.uniform(11, 9, oracle.STREAM_RESID, 5, 3, 4 + w)
+        assert u == (2 * (int(blk[w]) >> 9) + 1) / 2 ** 24
+
+
+# ---------------------------------------------------------------------------
+# Markov head and chain drafting
+# ---------------------------------------------------------------------------
+def _inputs(w, seed=0):
+    return synthetic.generate(w, seed=seed)
+
+
+def test_markov_product_exact_on_grid_and_flagged_off_grid():
+    w = small(R=2, B=3, V=40, r=64)
+    inp = _inputs(w)
+    res = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    assert res["flags"] & oracle.FLAG_INEXACT_MARKOV == 0
+    # a planted off-grid table (full-precision bf16 normals) must be caught
+    U = np_of(torch.randn(40, 64, generator=torch.Generator().manual_seed(1)).to(torch.bfloat16))
+    Wt = np_of(torch.randn(64, 40, generator=torch.Generator().manual_seed(2)).to(torch.bfloat16))
+    res = oracle.draft_chain(np_of(inp["L"]), U, Wt, np_of(inp["anchor"]))
+    assert res["flags"] & oracle.FLAG_INEXACT_MARKOV
+
+
+def test_chain_with_zero_markov_is_independent_argmax():
+    """W = 0 turns the semi-AR head into the parallel drafter: y_d = argmax L_d."""
+    for ldt in (FP32, BF16):
+        w = small(R=5, B=6, V=333, r=32, l_dtype=ldt)
+        inp = _inputs(w, seed=3)
+        Wz = np.zeros((32, 333), np.uint16)
+        res = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), Wz, np_of(inp["anchor"]))
+        ref = torch.argmax(inp["L"].float(), dim=-1).numpy()
+        np.testing.assert_array_equal(res["tokens"], ref)
+
+
+def test_chain_zero_noise_target_accepts_everything():
+    """sigma = 0 makes the target equal the drafter's logits: a correct chain
+    draft (right previous token, right W orientation, L added) is accepted in
+    full by greedy verification against the independent target stand-in."""
+    for ldt in (FP32, BF16):
+        w = small(R=6, B=7, V=97 * 8, r=64, l_dtype=ldt, target_dtype=FP32, sigma=(0.0,), l_std=1.0)
+        inp = _inputs(w, seed=5)
+        dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+        tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), FP32)
+        t_argmax = torch.argmax(tgt, dim=-1).numpy()
+        np.testing.assert_array_equal(t_argmax[:, :-1], dr["tokens"])
+        cu = np.arange(w.R + 1, dtype=np.int32) * (w.B + 1)
+        vr = oracle.verify(oracle.STATIC, oracle.GREEDY, np_of(tgt.reshape(-1, w.V)), cu, np_of(inp["anchor"]),
+                           dr["tokens"])
+        np.testing.assert_array_equal(vr["accept"], np.full(w.R, w.B))
+        np.testing.assert_array_equal(vr["out_tok"][:, -1], t_argmax[:, -1])
+
+
+def test_chain_markov_term_changes_the_draft():
+    """With a strong Markov term the draft follows z = L + U[y_{d-1}] W; the
+    target's argmax along that prefix (computed by the stand-in) agrees."""
+    w = small(R=4, B=5, V=64, r=64, l_std=0.05, sigma=(0.0,))
+    inp = _inputs(w, seed=9)
+    dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), FP32)
+    np.testing.assert_array_equal(torch.argmax(tgt, -1).numpy()[:, :-1], dr["tokens"])
+    # and it differs from the parallel drafter's choice somewhere
+    assert (dr["tokens"] != torch.argmax(inp["L"].float(), -1).numpy()).any()
+
+
+def test_argmax_ties_take_lowest_id():
+    V, r = 16, 8
+    L = np.zeros((1, 2, V), np.float32)
+    L[0, 0, [3, 9, 12]] = 2.0
+    L[0, 1, [0, 15]] = 1.0
+    U = np.zeros((V, r), np.uint16)
+    W = np.zeros((r, V), np.uint16)
+    res = oracle.draft_chain(L, U, W, np.array([5], np.int32))
+    assert res["tokens"].tolist() == [[3, 0]]
+    assert res["margin"][0, 0] == 0.0
+
+
+def test_chain_lse_and_logq_match_library_logsumexp():
+    """With W = 0, z = L: lse must equal scipy's logsumexp of L/T and
+    logq = L[y]/T - lse."""
+    w = small(R=3, B=4, V=200, r=16)
+    inp = _inputs(w, seed=2)
+    L = np_of(inp["L"])
+    Wz = np.zeros((16, 200), np.uint16)
+    for T in (1.0, 0.7):
+        res = oracle.draft_chain(L, np_of(inp["U"]), Wz, np_of(inp["anchor"]), decode=oracle.SAMPLE,
+                                 temperature=T, seed=4)
+        ref = special.logsumexp(L.astype(np.float64) / T, axis=-1)
+        np.testing.assert_allclose(res["lse"], ref, rtol=1e-13)
+        y = res["tokens"]
+        ly = np.take_along_axis(L.astype(np.float64), y[..., None], -1)[..., 0] / T
+        np.testing.assert_allclose(res["logq"], ly - ref, rtol=1e-12, atol=1e-13)
+
+
+def test_race_sampler_follows_softmax():
+    """The exponential race draws y ~ softmax(z/T): chi-square over many
+    independent requests (distinct counters) that share one logit row."""
+    V, n, T = 8, 1 << 15, 0.8
+    rng = np.random.default_rng(0)
+    row = rng.normal(0, 1.0, V).astype(np.float32)
+    L = np.broadcast_to(row, (n, 1, V)).copy()
+    U = np.zeros((V, 4), np.uint16)
+    W = np.zeros((4, V), np.uint16)
+    anchor = np.zeros(n, np.int32)
+    res = oracle.draft_chain(L, U, W, anchor, decode=oracle.SAMPLE, temperature=T, seed=123)
+    counts = np.bincount(res["tokens"][:, 0], minlength=V)
+    p = special.softmax(row.astype(np.float64) / T)
+    _, pval = stats.chisquare(counts, p * n)
+    assert pval > 1e-4
+
+
+# ---------------------------------------------------------------------------
+# scheduler
+# ---------------------------------------------------------------------------
+def test_scheduler_fig1_budget():
+    g = json.load(open(os.path.join(GOLDEN, "fig1_walkthrough.json")))
+    conf = np.array([g["confidences"]], np.float32)
+    cost = g["cost_a"] + g["cost_b"] * np.arange(1 * (len(g["confidences"]) + 1) + 1, dtype=np.float64)
+    sc = oracle.schedule_budget(conf, cost)
+    assert sc["budget"].tolist() == [g["expected_budget"]]
+    # survival is the running product
+    np.testing.assert_array_equal(sc["survival"][0], np.cumprod(conf[0], dtype=np.float32))
+
+
+def _objective(S, n, cost):
+    E = S.shape[0] + sum(float(S[i, :n[i]].astype(np.float64).sum()) for i in range(S.shape[0]))
+    N = S.shape[0] + int(sum(n))
+    return E / cost[N]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_scheduler_matches_brute_force(seed):
+    """Greedy over ranked survivals is the exact optimum of E/cost over every
+    allocation (n_1..n_R) in [0, gamma]^R (notes sec. 5.2)."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, 5))
+    g = int(rng.integers(1, 5))
+    conf = rng.uniform(0.05, 1.0, (R, g)).astype(np.float32)
+    a, b = float(rng.uniform(0.5, 3.0)), float(rng.uniform(0.01, 0.6))
+    cost = a + b * np.arange(R * (g + 1) + 1, dtype=np.float64)
+    sc = oracle.schedule_budget(conf, cost)
+    S = np.cumprod(conf, axis=1, dtype=np.float32)
+    best = max(_objective(S, n, cost) for n in itertools.product(range(g + 1), repeat=R))
+    got = _objective(S, sc["budget"], cost)
+    assert got == pytest.approx(best, rel=1e-15, abs=0)
+    assert sc["total_tokens"] == R + int(sc["budget"].sum())
+    assert sc["expected"] == R + sum(float(S[i, :sc["budget"][i]].astype(np.float64).sum()) for i in range(R))
+
+
+def test_scheduler_prefix_closed_and_unimodal():
+    rng = np.random.default_rng(7)
+    R, g = 64, 8
+    conf = rng.uniform(0.2, 1.0, (R, g)).astype(np.float32)
+    cost = 2.0 + 0.004 * np.arange(R * (g + 1) + 1)
+    sc = oracle.schedule_budget(conf, cost)
+    S = np.cumprod(conf, axis=1, dtype=np.float32)
+    # prefix-closed: every selected position k has all k' < k selected, and
+    # every selected survival is >= every unselected one
+    sel = np.array([[k < sc["budget"][i] for k in range(g)] for i in range(R)])
+    assert S[sel].min() >= S[~sel].max()
+    # f(m) over the ranked list rises then falls: early stop == global argmax
+    order = sorted(((float(S[i, k]), i, k) for i in range(R) for k in range(g)), key=lambda t: (-t[0], t[1], t[2]))
+    f = [(R + sum(o[0] for o in order[:m])) / cost[R + m] for m in range(len(order) + 1)]
+    m_star = int(np.argmax(f))
+    assert sc["m_star"] == m_star
+    assert all(f[m] <= f[m + 1] for m in range(m_star)) and all(f[m] >= f[m + 1] for m in range(m_star, len(f) - 1))
+
+
+# ---------------------------------------------------------------------------
+# ragged pack
+# ---------------------------------------------------------------------------
+def test_pack_round_trip_and_tier():
+    rng = np.random.default_rng(1)
+    R, g = 37, 8
+    anchor = rng.integers(0, 1000, R).astype(np.int32)
+    draft = rng.integers(0, 1000, (R, g)).astype(np.int32)
+    budget = rng.integers(0, g + 1, R).astype(np.int32)
+    tiers = np.array([64, 128, 256, 512], np.int32)
+    pk = oracle.pack_ragged(anchor, draft, budget, tiers)
+    cu = pk["cu_seqlens"]
+    np.testing.assert_array_equal(np.diff(cu), budget + 1)
+    T = int(cu[-1])
+    assert pk["tier"] == min(t for t in tiers if t >= T) and pk["flags"] == 0
+    for row in range(T):
+        i, p = pk["packed_req"][row], pk["packed_pos"][row]
+        assert cu[i] + p == row
+        assert pk["packed_tok"][row] == (anchor[i] if p == 0 else draft[i, p - 1])
+    assert np.all(pk["packed_tok"][T:] == -1) and np.all(pk["packed_req"][T:] == -1)
+    # static (budget = None) above every tier: uncaptured, tier = total
+    pk = oracle.pack_ragged(anchor, draft, None, tiers[:3])
+    assert pk["tier"] == R * (g + 1) and pk["flags"] & oracle.FLAG_TIER_UNCAPTURED
+
+
+def test_pack_empty_windows():
+    anchor = np.array([3, 4], np.int32)
+    draft = np.array([[1, 2], [5, 6]], np.int32)
+    pk = oracle.pack_ragged(anchor, draft, np.array([0, 0], np.int32), np.array([2, 4], np.int32))
+    assert pk["cu_seqlens"].tolist() == [0, 1, 2] and pk["tier"] == 2
+    assert pk["packed_tok"].tolist() == [3, 4]
+
+
+# ---------------------------------------------------------------------------
+# greedy verification
+# ---------------------------------------------------------------------------
+def _onehot_rows(ids, V, hi=5.0):
+    t = np.zeros((len(ids), V), np.float32)
+    for j, v in enumerate(ids):
+        t[j, v] = hi
+    return t
+
+
+def test_verify_fig1_walkthrough():
+    g = json.load(open(os.path.join(GOLDEN, "fig1_walkthrough.json")))
+    V = len(g["vocab"])
+    anchor = np.array([g["vocab"].index(g["anchor"])], np.int32)
+    draft = np.array([g["draft_ids"]], np.int32)
+    conf = np.array([g["confidences"]], np.float32)
+    cost = g["cost_a"] + g["cost_b"] * np.arange(len(g["confidences"]) + 2, dtype=np.float64)
+    sc = oracle.schedule_budget(conf, cost)
+    pk = oracle.pack_ragged(anchor, draft, sc["budget"], np.array([8], np.int32))
+    assert pk["packed_tok"][: pk["cu_seqlens"][-1]].tolist() == [3, 4, 5, 6]      # D E F G
+    target = _onehot_rows(g["target_argmax_ids"][: pk["cu_seqlens"][-1]], V)
+    target = np.concatenate([target, np.zeros((pk["tier"] - target.shape[0], V), np.float32)])
+    vr = oracle.verify(oracle.COMPACT, oracle.GREEDY, target, pk["cu_seqlens"], anchor, draft)
+    assert vr["accept"].tolist() == [g["expected_accept"]]
+    assert vr["out_tok"][0, : vr["n_out"][0]].tolist() == g["expected_commit_ids"]
+    assert vr["n_out"][0] == vr["accept"][0] + 1            # the bonus counts
+
+
+def test_verify_accept_is_first_mismatch_and_bonus_is_target_token():
+    rng = np.random.default_rng(3)
+    R, g, V = 50, 6, 12
+    anchor = rng.integers(0, V, R).astype(np.int32)
+    draft = rng.integers(0, V, (R, g)).astype(np.int32)
+    t_ids = draft.copy()
+    flip = rng.random((R, g)) < 0.3
+    t_ids[flip] = (t_ids[flip] + 1 + rng.integers(0, V - 1, flip.sum())) % V
+    bonus = rng.integers(0, V, R)
+    rows = np.concatenate([t_ids, bonus[:, None]], axis=1)
+    target = _onehot_rows(rows.reshape(-1), V)
+    cu = np.arange(R + 1, dtype=np.int32) * (g + 1)
+    vr = oracle.verify(oracle.STATIC, oracle.GREEDY, target, cu, anchor, draft)
+    for i in range(R):
+        mism = np.nonzero(draft[i] != rows[i, :g])[0]
+        a = int(mism[0]) if mism.size else g
+        assert vr["accept"][i] == a
+        assert vr["out_tok"][i, :a].tolist() == draft[i, :a].tolist()
+        assert vr["out_tok"][i, a] == rows[i, a]
+
+
+def test_greedy_speculative_decoding_equals_target_only_decoding():
+    """Lossless: the committed stream of speculative greedy decoding is the
+    target model's own greedy decode (PCTree article; notes sec. 1)."""
+    for ldt, tdt in ((FP32, FP32), (BF16, BF16)):
+        w = small(R=4, B=5, V=64, r=16, l_dtype=ldt, target_dtype=tdt, sigma=(0.3, 0.8), l_std=1.0)
+        cycles = 6
+        ab = absolute_inputs(w, positions=cycles * (w.B + 1) + w.B + 1, seed=11)
+        seqs, recs = oracle_greedy_decode(w, ab, cycles)
+        n = min(len(s) for s in seqs) - 1
+        ref = target_only_greedy(ab, n, tdt)
+        for i in range(w.R):
+            assert seqs[i][: n + 1] == ref[i].tolist()
+        acc = np.concatenate([r["verify"]["accept"] for r in recs])
+        assert acc.min() == 0 and acc.max() >= 2        # a mix of accepts and rejections
+
+
+def test_verify_modes_invariants():
+    """cap-accept commits exactly what compact commits and reports a ceiling
+    >= its accept; compact accept = min(static accept, n_i); static is compact
+    with n_i = gamma (DSpark in SGLang, three verify modes)."""
+    w = small(R=16, B=6, V=64, r=16, sigma=(0.2, 0.6, 1.2), target_dtype=BF16, l_dtype=BF16)
+    inp = _inputs(w, seed=21)
+    an = np_of(inp["anchor"])
+    dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), an)
+    sc = oracle.schedule_budget(np_of(inp["conf"]), synthetic.cost_table(w).numpy())
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    res = {}
+    for mode, budget in (("static", None), ("compact", sc["budget"]), ("cap", None)):
+        pk = oracle.pack_ragged(an, dr["tokens"], budget, np.array(w.tiers, np.int32))
+        packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+        om = {"static": oracle.STATIC, "compact": oracle.COMPACT, "cap": oracle.CAP_ACCEPT}[mode]
+        res[mode] = oracle.verify(om, oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an, dr["tokens"],
+                                  budget=sc["budget"])
+    np.testing.assert_array_equal(res["cap"]["out_tok"], res["compact"]["out_tok"])
+    np.testing.assert_array_equal(res["cap"]["n_out"], res["compact"]["n_out"])
+    assert np.all(res["cap"]["ceiling"] >= res["cap"]["accept"])
+    np.testing.assert_array_equal(res["cap"]["ceiling"], res["static"]["accept"])
+    np.testing.assert_array_equal(res["compact"]["accept"], np.minimum(res["static"]["accept"], sc["budget"]))
+
+
+# ---------------------------------------------------------------------------
+# rejection sampling
+# ---------------------------------------------------------------------------
+def _sample_cycle(w, inp, anchor, seed, cycle, mode=oracle.STATIC, budget=None):
+    U, W = np_of(inp["U"]), np_of(inp["W"])
+    dr = oracle.draft_chain(np_of(inp["L"]), U, W, anchor, decode=oracle.SAMPLE, temperature=w.temperature,
+                            seed=seed, cycle=cycle)
+    tgt = synthetic.chain_target(inp | {"anchor": torch.as_tensor(anchor)}, torch.as_tensor(dr["tokens"]),
+                                 w.target_dtype)
+    R = anchor.shape[0]
+    cu = np.arange(R + 1, dtype=np.int32) * (w.B + 1)
+    vr = oracle.verify(mode, oracle.SAMPLE, np_of(tgt.reshape(R * (w.B + 1), -1)), cu, anchor, dr["tokens"],
+                       budget=budget, logq=dr["logq"], lse_q=dr["lse"], L=np_of(inp["L"]), U=U, W=W,
+                       temperature=w.temperature, seed=seed, cycle=cycle)
+    return dr, tgt, vr
+
+
+@pytest.mark.parametrize("sigma", [0.3, 2.0])
+def test_rejection_sampling_first_token_follows_target(sigma):
+    """u < min(1, p/q) with residual resampling keeps the target distribution:
+    the first committed token ~ p_1(. | anchor) (chi-square, df = V-1)."""
+    n, V = 1 << 16, 8
+    w = small(R=n, B=3, V=V, r=4, sigma=(sigma,), l_std=1.0)
+    base = _inputs(small(R=1, B=3, V=V, r=4, sigma=(sigma,), l_std=1.0), seed=2)
+    inp = {k: (v.expand(n, *v.shape[1:]).contiguous() if k in ("L", "L_bonus", "eta", "anchor") else v)
+           for k, v in base.items()}
+    anchor = np.full(n, int(base["anchor"][0]), np.int32)
+    dr, tgt, vr = _sample_cycle(w, inp, anchor, seed=77, cycle=1)
+    p1 = torch.softmax(tgt[0, 0].double(), -1).numpy()
+    counts = np.bincount(vr["out_tok"][:, 0], minlength=V)
+    _, pval = stats.chisquare(counts, p1 * n)
+    assert pval > 1e-4
+    assert vr["accept"].min() == 0 and vr["accept"].max() == 3
+
+
+def test_rejection_sampling_pairs_follow_target():
+    """First two committed tokens ~ p_1(t1) p_2(t2 | t1) (df = V^2 - 1); a
+    second cycle from the committed anchor supplies t2 when the first cycle
+    commits one token only."""
+    n, V, B = 1 << 16, 8, 3
+    w = small(R=n, B=B, V=V, r=4, sigma=(0.8,), l_std=1.0)
+    ab1 = absolute_inputs(small(R=1, B=B, V=V, r=4, sigma=(0.8,), l_std=1.0), positions=2 * B + 2, seed=5)
+    ab = {k: (v.expand(n, *v.shape[1:]).contiguous() if k in ("L_abs", "eta_abs", "anchor", "conf_abs") else v)
+          for k, v in ab1.items()}
+    anchor = np.full(n, int(ab1["anchor"][0]), np.int32)
+    ci = cycle_inputs(ab, np.zeros(n, np.int64), B)
+    _, _, v1 = _sample_cycle(w, ci, anchor, seed=3, cycle=0)
+    t1 = v1["out_tok"][:, 0]
+    t2 = v1["out_tok"][:, 1].copy()
+    need = v1["n_out"] == 1
+    idx = np.nonzero(need)[0]
+    ci2 = cycle_inputs({k: (v[idx] if k in ("L_abs", "eta_abs", "conf_abs") else v) for k, v in ab.items()},
+                       np.ones(idx.size, np.int64), B)
+    _, _, v2 = _sample_cycle(w, ci2, t1[idx].astype(np.int32), seed=3, cycle=1)
+    t2[idx] = v2["out_tok"][:, 0]
+    # reference joint distribution from the stand-in target
+    one = {"L": ab1["L_abs"], "L_bonus": ab1["L_abs"][:, -1], "U": ab1["U"], "W": ab1["W"], "eta": ab1["eta_abs"]}
+    r1 = synthetic.target_rows(one, torch.tensor([0]), torch.tensor([0]), ab1["anchor"][:1], w.target_dtype)
+    p1 = torch.softmax(r1[0].double(), -1)
+    r2 = synthetic.target_rows(one, torch.zeros(V, dtype=torch.long), torch.ones(V, dtype=torch.long),
+                               torch.arange(V), w.target_dtype)
+    p2 = torch.softmax(r2.double(), -1)
+    joint = (p1.view(V, 1) * p2).numpy().reshape(-1)
+    counts = np.bincount(t1 * V + t2, minlength=V * V)
+    keep = joint * n >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    exp = np.append(joint[keep] * n, joint[~keep].sum() * n)
+    _, pval = stats.chisquare(obs, exp)
+    assert pval > 1e-4
+
+
+def test_rejection_sampling_equal_distributions_accept_everything():
+    w = small(R=40, B=5, V=64, r=16, sigma=(0.0,), l_std=1.5)
+    inp = _inputs(w, seed=8)
+    _, _, vr = _sample_cycle(w, inp, np_of(inp["anchor"]), seed=1, cycle=0)
+    np.testing.assert_array_equal(vr["accept"], np.full(w.R, w.B))
+
+
+def test_rejection_sampling_cap_accept_equals_compact():
+    w = small(R=64, B=6, V=32, r=16, sigma=(1.0,), l_std=1.0)
+    inp = _inputs(w, seed=4)
+    an = np_of(inp["anchor"])
+    budget = np.random.default_rng(0).integers(0, w.B + 1, w.R).astype(np.int32)
+    U, W = np_of(inp["U"]), np_of(inp["W"])
+    dr = oracle.draft_chain(np_of(inp["L"]), U, W, an, decode=oracle.SAMPLE, seed=9, cycle=2)
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    outs = {}
+    for mode, bud in (("compact", budget), ("cap", None)):
+        pk = oracle.pack_ragged(an, dr["tokens"], bud, np.array(w.tiers, np.int32))
+        packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+        om = oracle.COMPACT if mode == "compact" else oracle.CAP_ACCEPT
+        outs[mode] = oracle.verify(om, oracle.SAMPLE, np_of(packed), pk["cu_seqlens"], an, dr["tokens"],
+                                   budget=budget, logq=dr["logq"], lse_q=dr["lse"], L=np_of(inp["L"]), U=U, W=W,
+                                   seed=9, cycle=2)
+    np.testing.assert_array_equal(outs["cap"]["out_tok"], outs["compact"]["out_tok"])
+    assert np.all(outs["cap"]["ceiling"] >= outs["cap"]["accept"])
+    assert (outs["cap"]["ceiling"] > outs["cap"]["accept"]).any()
+
+
+# ---------------------------------------------------------------------------
+# PCTree
+# ---------------------------------------------------------------------------
+def test_tree_with_k1_is_the_chain():
+    """k = 1, N = B: every level keeps one child, the tree is the greedy chain."""
+    w = small(R=5, B=6, V=300, r=32, l_dtype=BF16)
+    inp = _inputs(w, seed=13)
+    args = (np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    ch = oracle.draft_chain(*args)
+    tr = oracle.draft_tree(*args, k=1, P=4, N=w.B)
+    np.testing.assert_array_equal(tr["tok"][:, 1:], ch["tokens"])
+    np.testing.assert_array_equal(tr["parent"][:, 1:], np.tile(np.arange(w.B), (w.R, 1)))
+    np.testing.assert_array_equal(tr["depth"][:, 1:], np.tile(np.arange(1, w.B + 1), (w.R, 1)))
+    assert np.all(tr["n_nodes"] == w.B + 1)
+
+
+def _all_paths(L, U, W, anchor, B):
+    """Brute force: every token path of length <= B with its score
+    sum log pi(v | parent) (dict path -> score)."""
+    V = L.shape[-1]
+    Lf = L.astype(np.float32) if L.dtype != np.uint16 else (L.astype(np.uint32) << 16).view(np.float32)
+    Uf = (U.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Wf = (W.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    out = {}
+
+    def rec(path, prev, s):
+        d = len(path) + 1
+        if d > B:
+            return
+        z = (Lf[d - 1] + (Uf[prev] @ Wf).astype(np.float32)).astype(np.float32)
+        lse = special.logsumexp(z.astype(np.float64))
+        for v in range(V):
+            p2 = path + (v,)
+            sc = s + (float(z[v]) - lse)
+            out[p2] = (sc, float(z[v]))
+            rec(p2, v, sc)
+
+    rec((), int(anchor), 0.0)
+    return out
+
+
+def _beam_reference(paths, V, B, k, P, N):
+    """Independent replay of PCTree's rules over the enumerated paths."""
+    frontier = [()]
+    pool = []
+    for d in range(1, B + 1):
+        cands = []
+        for slot, par in enumerate(frontier):
+            kids = sorted(range(V), key=lambda v: (-paths[par + (v,)][1], v))[:k]
+            for rank, v in enumerate(kids):
+                cands.append((paths[par + (v,)][0], slot, rank, par + (v,)))
+        cands.sort(key=lambda c: (-c[0], c[1], c[2]))
+        frontier = [c[3] for c in cands[:P]]
+        pool.extend((paths[f][0], d, len(pool), f) for f in frontier)
+    pool.sort(key=lambda t: (-t[0], t[1], t[2]))
+    return [t[3] for t in pool[:N]]
+
+
+def _tree_paths(tr, i):
+    out = []
+    for c in range(1, tr["n_nodes"][i]):
+        p, a = [], c
+        while a > 0:
+            p.append(int(tr["tok"][i, a]))
+            a = tr["parent"][i, a]
+        out.append(tuple(reversed(p)))
+    return out
+
+
+@pytest.mark.parametrize("V,B,k,P,N", [(5, 3, 2, 3, 6), (4, 3, 3, 4, 9), (6, 2, 2, 2, 3), (3, 3, 2, 8, 10)])
+def test_tree_matches_brute_force_beam(V, B, k, P, N):
+    w = small(R=3, B=B, V=V, r=8, l_std=1.0)
+    inp = _inputs(w, seed=V * 10 + B)
+    L, U, W, an = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"])
+    tr = oracle.draft_tree(L, U, W, an, k=k, P=P, N=N)
+    for i in range(w.R):
+        paths = _all_paths(L[i], U, W, an[i], B)
+        ref = _beam_reference(paths, V, B, k, P, N)
+        assert _tree_paths(tr, i) == ref
+        for c in range(1, tr["n_nodes"][i]):
+            assert tr["parent"][i, c] < c
+            assert tr["score"][i, c] == pytest.approx(paths[_tree_paths(tr, i)[c - 1]][0], abs=1e-12)
+
+
+def test_tree_without_pruning_maximises_path_mass():
+    """k = V and P >= V^B: the selected N nodes maximise sum exp(s) over all
+    ancestor-closed node sets of size N (top-N by path probability)."""
+    V, B, N = 3, 3, 4
+    w = small(R=2, B=B, V=V, r=8, l_std=1.2)
+    inp = _inputs(w, seed=1)
+    L, U, W, an = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"])
+    tr = oracle.draft_tree(L, U, W, an, k=V, P=V ** B, N=N)
+    for i in range(w.R):
+        paths = _all_paths(L[i], U, W, an[i], B)
+        nodes = list(paths)
+        best = -1.0
+        for sub in itertools.combinations(nodes, N):
+            ss = set(sub)
+            if all(p[:-1] in ss or len(p) == 1 for p in sub):
+                best = max(best, sum(math.exp(paths[p][0]) for p in sub))
+        got = sum(math.exp(paths[p][0]) for p in _tree_paths(tr, i))
+        assert got == pytest.approx(best, rel=1e-12)
+
+
+def test_tree_mask_is_ancestor_closure():
+    w = small(R=4, B=4, V=50, r=16)
+    inp = _inputs(w, seed=3)
+    tr = oracle.draft_tree(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]), k=3, P=4, N=10)
+    S = 11
+    for i in range(w.R):
+        for c in range(S):
+            bits = tr["mask"][i, c, 0]
+            if c >= tr["n_nodes"][i]:
+                assert bits == 0
+                continue
+            anc = set()
+            a = c
+            while a >= 0:
+                anc.add(a)
+                a = tr["parent"][i, a]
+            assert {j for j in range(S) if bits >> j & 1} == anc
+
+
+def test_tree_verify_walks_longest_accepted_path():
+    # hand-built tree: root(5) -> {1: tok 2, 2: tok 3}; 1 -> {3: tok 4}; 2 -> {4: tok 4}
+    V, B, N = 8, 3, 4
+    tok = np.array([[5, 2, 3, 4, 4]], np.int32)
+    parent = np.array([[-1, 0, 0, 1, 2]], np.int32)
+    n_nodes = np.array([5], np.int32)
+    # target argmax per slot: root -> 3 (accept slot 2), slot 2 -> 4 (accept slot 4), slot 4 -> 6 (bonus)
+    am = [3, 0, 4, 0, 6]
+    target = _onehot_rows(am, V).reshape(1, 5, V)
+    vr = oracle.verify_tree(target, tok, parent, n_nodes, B)
+    assert vr["accept"].tolist() == [2] and vr["out_tok"][0, :3].tolist() == [3, 4, 6]
+    # a chain-shaped tree verifies like the chain
+    w = small(R=6, B=5, V=64, r=16, sigma=(0.5,))
+    inp = _inputs(w, seed=6)
+    args = (np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    tr = oracle.draft_tree(*args, k=1, P=2, N=w.B)
+    tgt = synthetic.tree_target(inp, torch.as_tensor(tr["tok"]), torch.as_tensor(tr["depth"]),
+                                torch.as_tensor(tr["n_nodes"]), FP32)
+    vt = oracle.verify_tree(np_of(tgt), tr["tok"], tr["parent"], tr["n_nodes"], w.B)
+    cu = np.arange(w.R + 1, dtype=np.int32) * (w.B + 1)
+    vc = oracle.verify(oracle.STATIC, oracle.GREEDY, np_of(tgt.reshape(-1, w.V)), cu, args[3], tr["tok"][:, 1:])
+    np.testing.assert_array_equal(vt["accept"], vc["accept"])
+    np.testing.assert_array_equal(vt["out_tok"], vc["out_tok"])
