@@ -1,0 +1,491 @@
+#!/usr/bin/env python
+"""Benchmark of the DSpark hot path on one GB300: one step = one decode cycle
+(draft -> schedule -> pack -> verify) over a batch of synthetic inputs.
+
+Metric: committed tokens per second (accepted drafts + one bonus token per
+request) over the device time of draft + schedule + pack + verify; the
+target-model stand-in (a row gather of precomputed synthetic target logits
+into the packed buffer) sits between pack and verify and is not timed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) each rank runs an independent replica on its own GPU
+(the path shards by request; there is no data-path collective) and rank 0
+prints the aggregate.  --impl reference times the CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/s (draft+schedule+verify) at vocab 152K; % HBM roofline"
+UNIT = "tokens/s"
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_8b_chain")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("markov_gemm.cu", "device.cuh", "stream.cu", "internal.h"):
+        with open(os.path.join(ROOT, "speculative_decoding_markov_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(kernel)
+    if not e or e.get("source_hash") != kernel_source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+class Cycle:
+    """Preallocated buffers and the launch sequence of one decode cycle."""
+
+    def __init__(self, w, seed, device):
+        import torch
+
+        from speculative_decoding_markov_gb300 import binding as sdm
+        from speculative_decoding_markov_gb300 import synthetic
+
+        self.torch, self.sdm, self.synthetic = torch, sdm, synthetic
+        self.w = w
+        self.dev = device
+        self.inp = synthetic.generate(w, seed=seed, device=device)
+        R, B, V, r = w.R, w.B, w.V, w.r
+        self.sample = w.decode == "sample"
+        self.mode = {"compact": sdm.COMPACT, "static": sdm.STATIC, "cap_accept": sdm.CAP_ACCEPT}[w.modes[0]]
+        i32 = dict(dtype=torch.int32, device=device)
+        self.dr = dict(tokens=torch.empty((R, B), **i32), logq=torch.zeros((R, B), dtype=torch.float32, device=device),
+                       lse=torch.zeros((R, B), dtype=torch.float32, device=device))
+        self.sc = dict(survival=torch.empty((R, B), dtype=torch.float32, device=device), budget=torch.empty((R,), **i32),
+                       expected=torch.empty((1,), dtype=torch.float64, device=device),
+                       total_tokens=torch.empty((1,), **i32))
+        cap = sdm.pack_capacity(R, B, list(w.tiers))
+        self.cap = cap
+        self.pk = dict(cu_seqlens=torch.empty((R + 1,), **i32), packed_tok=torch.empty((cap,), **i32),
+                       packed_req=torch.empty((cap,), **i32), packed_pos=torch.empty((cap,), **i32),
+                       tier=torch.empty((1,), **i32))
+        tdt = synthetic.torch_dtype(w.target_dtype)
+        self.packed = torch.empty((cap, V), dtype=tdt, device=device)
+        self.vr = dict(accept=torch.empty((R,), **i32), ceiling=torch.empty((R,), **i32),
+                       out_tok=torch.empty((R, B + 1), **i32), n_out=torch.empty((R,), **i32))
+        self.ws_draft = sdm.workspace(sdm.OP_DRAFT_CHAIN, R, B, V, r, device=device)
+        self.ws_verify = sdm.workspace(sdm.OP_VERIFY, R, B, V, r, cap, device=device)
+        self.status = sdm.new_status(device)
+        # one untimed cycle fixes the drafted prefix; the stand-in target model
+        # then provides every window row along it
+        self.draft()
+        self.schedule_pack()
+        self.target = synthetic.chain_target(self.inp, self.dr["tokens"], w.target_dtype)
+        self.gather()
+        self.verify()
+        torch.cuda.synchronize()
+        assert int(self.status.item()) & ~sdm.DEV_TIER_UNCAPTURED == 0, f"device status {int(self.status.item())}"
+
+    # the four timed operations -------------------------------------------
+    def draft(self):
+        sdm, i = self.sdm, self.inp
+        sdm.draft_chain(i["L"], i["U"], i["W"], i["anchor"], decode=sdm.SAMPLE if self.sample else sdm.GREEDY,
+                        temperature=self.w.temperature, seed=0, cycle=0, out=self.dr, ws=self.ws_draft,
+                        dev_status=self.status)
+
+    def schedule_pack(self):
+        sdm, i = self.sdm, self.inp
+        sdm.schedule_budget(i["conf"], i["cost"], out=self.sc, dev_status=self.status)
+        budget = self.sc["budget"] if self.mode == sdm.COMPACT else None
+        sdm.pack_ragged(i["anchor"], self.dr["tokens"], budget, i["tiers"], out=self.pk, dev_status=self.status)
+
+    def gather(self):
+        self.synthetic.gather_packed(self.target, self.pk["packed_req"], self.pk["packed_pos"], out=self.packed)
+
+    def verify(self):
+        sdm, i = self.sdm, self.inp
+        kw = {}
+        if self.sample:
+            kw = dict(logq=self.dr["logq"], lse_q=self.dr["lse"], L=i["L"], U=i["U"], W=i["W"])
+        sdm.verify(self.mode, sdm.SAMPLE if self.sample else sdm.GREEDY, self.packed, self.pk["cu_seqlens"],
+                   i["anchor"], self.dr["tokens"], budget=self.sc["budget"], temperature=self.w.temperature,
+                   out=self.vr, ws=self.ws_verify, dev_status=self.status, **kw)
+
+    def launches_per_step(self):
+        verify = 5 if self.sample else 3
+        return (self.w.B + 2) + 1 + 1 + verify
+
+
+def run_ours(args, w, world, rank, local):
+    import torch
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    cyc = Cycle(w, seed=rank, device=dev)
+    R, B, V = w.R, w.B, w.V
+    committed = int(cyc.vr["n_out"].sum().item())
+    accepted = int(cyc.vr["accept"].sum().item())
+    windows = int(cyc.pk["cu_seqlens"][-1].item())          # sum of (n_i + 1) verified rows
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        flush.fill_(1)                                      # L2 flush, untimed
+        if ev:
+            ev[0].record(stream)
+        cyc.draft()
+        if ev:
+            ev[1].record(stream)
+        cyc.schedule_pack()
+        if ev:
+            ev[2].record(stream)
+        cyc.gather()                                        # target stand-in, untimed
+        if ev:
+            ev[3].record(stream)
+        cyc.verify()
+        if ev:
+            ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for k in range(args.steps):
+            step(events[k])
+        torch.cuda.synchronize()
+    barrier(world)
+    t_draft = sum(e[0].elapsed_time(e[1]) for e in events) / 1e3
+    t_sched = sum(e[1].elapsed_time(e[2]) for e in events) / 1e3
+    t_verify = sum(e[3].elapsed_time(e[4]) for e in events) / 1e3
+    t_total = t_draft + t_sched + t_verify
+    t_max = allreduce_max(t_total, world)
+    status = int(cyc.status.item())
+
+    # roofline of the dominant kernel (algorithmic bytes / measured time)
+    peak, peak_kind = measured_peaks()
+    s_l = 2 if w.l_dtype == 0 else 4
+    s_t = 2 if w.target_dtype == 0 else 4
+    draft_bytes = R * B * V * s_l + w.r * V * 2                 # L once + W once per cycle
+    verify_bytes = windows * V * s_t                            # verified window rows
+    if t_draft >= t_verify:
+        kname = "markov_gemm_kernel<chain>"
+        per_launch_s = t_draft / args.steps / B
+        achieved = draft_bytes / B / per_launch_s / 1e9
+        traffic = recorded_traffic(kname)
+    else:
+        kname = "row_stream_kernel<argmax>"
+        per_launch_s = t_verify / args.steps
+        achieved = verify_bytes / per_launch_s / 1e9
+        traffic = recorded_traffic(kname)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(cyc, args, committed)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        cpu = oracle_sample(w, cyc.inp, args.cpu_seconds)
+
+    clk = clocks.summary()
+    out = {
+        "metric": METRIC,
+        "value": committed * args.steps * world / t_max,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_max / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "R": R, "B": B, "V": V, "r": w.r, "decode": w.decode, "mode": w.modes[0],
+                   "parallelism": f"replicas{world}" if world > 1 else "single",
+                   "l2": "flushed by a 256 MB write before every step",
+                   "timed": "draft+schedule+pack+verify (CUDA events); target stand-in row gather excluded"},
+        "breakdown_ms_per_step": {"draft": t_draft / args.steps * 1e3, "schedule+pack": t_sched / args.steps * 1e3,
+                                  "verify": t_verify / args.steps * 1e3},
+        "tokens_per_step": {"committed": committed, "accepted_drafts": accepted, "verified_rows": windows},
+        "verified_rows_per_s": windows * args.steps * world / t_max,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
+                     "algorithmic_bytes": {"draft_per_cycle": draft_bytes, "verify_per_cycle": verify_bytes}},
+        "gpu_launches": cyc.launches_per_step() * args.steps,
+        "device_status": status,
+        "clocks": clk,
+    }
+    if e2e is not None:
+        out["e2e"] = e2e
+    if cpu is not None:
+        out["cpu_baseline"] = cpu
+    return out
+
+
+def run_e2e(cyc, args, committed):
+    """Same cycle through the C-ABI with host buffers: every step copies its
+    inputs (backbone logits, anchors, confidences, target logits) from pinned
+    host memory and reads the committed tokens back."""
+    import torch
+
+    i = cyc.inp
+    host = {k: i[k].cpu().pin_memory() for k in ("L", "anchor", "conf")}
+    host["target"] = cyc.target.cpu().pin_memory()
+    out_h = torch.empty_like(cyc.vr["out_tok"], device="cpu").pin_memory()
+    nout_h = torch.empty_like(cyc.vr["n_out"], device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 4 + nout_h.numel() * 4
+
+    def step():
+        i["L"].copy_(host["L"], non_blocking=True)
+        i["anchor"].copy_(host["anchor"], non_blocking=True)
+        i["conf"].copy_(host["conf"], non_blocking=True)
+        cyc.target.copy_(host["target"], non_blocking=True)
+        cyc.draft()
+        cyc.schedule_pack()
+        cyc.gather()
+        cyc.verify()
+        out_h.copy_(cyc.vr["out_tok"], non_blocking=True)
+        nout_h.copy_(cyc.vr["n_out"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(2, args.warmup)):
+        step()
+    k = max(3, args.steps // 2)
+    t0 = time.perf_counter()
+    for _ in range(k):
+        step()
+    dt = time.perf_counter() - t0
+    assert int(nout_h.sum()) == committed
+    return {"value": committed * k / dt, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": dt / k * 1e3}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_cycle(w, inp, idx, cycle_seed=0):
+    """One oracle cycle for the requests idx (schedule over all requests);
+    returns (seconds of oracle work, committed tokens)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from speculative_decoding_markov_gb300 import synthetic
+
+    def np_of(t):
+        t = t.detach().cpu().contiguous()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+
+    idx_t = torch.as_tensor(idx, dtype=torch.long, device=inp["L"].device)
+    sub = {k: inp[k].index_select(0, idx_t) for k in ("L", "L_bonus", "eta", "anchor")}
+    sub["U"], sub["W"] = inp["U"], inp["W"]
+    L, U, W = np_of(sub["L"]), np_of(inp["U"]), np_of(inp["W"])
+    an = np_of(sub["anchor"])
+    conf, cost, tiers = np_of(inp["conf"]), np_of(inp["cost"]), np_of(inp["tiers"])
+    sample = w.decode == "sample"
+    ids = np.asarray(idx, np.int32)
+    t0 = time.perf_counter()
+    dr = oracle.draft_chain(L, U, W, an, decode=oracle.SAMPLE if sample else oracle.GREEDY,
+                            temperature=w.temperature, seed=cycle_seed, req_ids=ids)
+    sc = oracle.schedule_budget(conf, cost)
+    budget = sc["budget"][ids]
+    static = w.modes[0] != "compact"
+    pk = oracle.pack_ragged(an, dr["tokens"], None if static else budget, tiers)
+    t1 = time.perf_counter()
+    tgt = synthetic.chain_target({k: v.cpu() for k, v in sub.items()}, torch.as_tensor(dr["tokens"]),
+                                 w.target_dtype)          # target stand-in: not timed
+    packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+    t2 = time.perf_counter()
+    mode = {"compact": oracle.COMPACT, "static": oracle.STATIC, "cap_accept": oracle.CAP_ACCEPT}[w.modes[0]]
+    kw = {}
+    if sample:
+        kw = dict(logq=dr["logq"], lse_q=dr["lse"], L=L, U=U, W=W, temperature=w.temperature, seed=cycle_seed)
+    vr = oracle.verify(mode, oracle.SAMPLE if sample else oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an,
+                       dr["tokens"], budget=budget, req_ids=ids, **kw)
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2), int(vr["n_out"].sum())
+
+
+def oracle_sample(w, inp, seconds):
+    """Oracle throughput on a bounded sample: requests are added one at a time
+    (each a full cycle: its draft, the schedule over all requests, its pack and
+    verify) until about `seconds` of oracle work."""
+    spent, toks, n = 0.0, 0, 0
+    while n < w.R and (spent < seconds or n < 2):
+        dt, c = oracle_cycle(w, inp, [n])
+        spent += dt
+        toks += c
+        n += 1
+    return {"value": toks / spent, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {w.R} requests of one cycle (one cycle each; schedule over all {w.R}), "
+                      f"{spent:.1f} s of single-threaded oracle work"}
+
+
+def run_reference(args, w):
+    import torch
+
+    from speculative_decoding_markov_gb300 import synthetic
+
+    inp = synthetic.generate(w, seed=0, device="cpu")
+    for _ in range(args.warmup):
+        oracle_cycle(w, inp, [0])
+    spent, toks = 0.0, 0
+    per = max(1, min(w.R, 2))
+    for k in range(args.steps):
+        idx = [(k * per + j) % w.R for j in range(per)]
+        dt, c = oracle_cycle(w, inp, idx)
+        spent += dt
+        toks += c
+    value = toks / spent
+    sample = f"{per} of {w.R} requests per step (schedule over all {w.R}), single-threaded oracle"
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": spent / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "R": w.R, "B": w.B, "V": w.V, "r": w.r, "decode": w.decode,
+                       "mode": w.modes[0]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    from speculative_decoding_markov_gb300.workloads import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, w)))
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    import __graft_entry__
+    __graft_entry__.build()
+    out = run_ours(args, w, world, rank, local)
+    if rank == 0:
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

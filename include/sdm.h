@@ -1,0 +1,246 @@
+/*
+ * sdm.h - C-ABI of the DSpark / PCTree speculative-decoding hot path on one
+ * GB300 GPU (sm_103a).
+ *
+ * Library: libsdm.so (speculative_decoding_markov_gb300/libsdm.so).
+ *
+ * One decode cycle of semi-autoregressive speculative decoding is
+ *   draft (Markov head, chain or PCTree)  ->  schedule (survival product and
+ *   throughput-maximising prefix budget)  ->  pack (ragged front-pack into a
+ *   captured tier)  ->  [target LLM forward: outside this library]  ->  verify.
+ *
+ * Sources, cited by page and section:
+ *   [DSpark notes]  LayerX ML study-group notes (2026-06-30), summary of
+ *                   "DSpark: Confidence-Scheduled Speculative Decoding with
+ *                   Semi-Autoregressive Generation", sections 1-9.
+ *   [PCTree]        Qiita article on PCTree (Parent-Conditioned Drafting Tree),
+ *                   section on tree drafting with the Markov head.
+ *   [SGLang]        "DSpark in SGLang" (winzheng.jp), sections on the SPS cost
+ *                   table, ragged verify and the three verify modes.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer unless the comment says
+ *     "host".  The caller owns every buffer; the library never allocates.
+ *     Scratch memory is the caller's `ws` buffer of at least
+ *     sdm_workspace_size(op, ...) bytes (256-byte aligned).
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  The return value reports
+ *     host-side validation and launch errors only.
+ *   - Conditions found on the device (out-of-range token ids, a verify window
+ *     that does not fit, a bounded wait that ran out, a packed total above
+ *     every tier) are OR-ed into *dev_status (device int32, SDM_DEV_* bits);
+ *     the caller reads it after synchronising.  No kernel traps.
+ *   - Layouts are row-major.  bf16 arrays are raw 16-bit patterns.
+ *     L is [R, B, V]: L[i, d-1, :] is the backbone logit row of draft
+ *     position d of request i.  U is [V, r], W is [r, V].
+ *   - Constraints: V % 8 == 0, r % 64 == 0 and r <= 256, L/U/W/target base
+ *     addresses 16-byte aligned.  Anything else returns SDM_ERR_UNSUPPORTED.
+ *   - Randomness (sampling only) is Philox4x32-10 with key (seed mod 2^32,
+ *     seed >> 32) and counter (v >> 2, request, stream << 16 | row,
+ *     cycle mod 2^32); word v & 3 gives u = (2 (w >> 9) + 1) 2^-24.  Streams:
+ *     0 draft, 1 accept test, 2 residual, 3 bonus.
+ *   - Ties: argmax and top-k prefer the lowest token id; the scheduler ranks
+ *     (survival desc, request asc, position asc); PCTree prunes by (score
+ *     desc, parent slot asc, child rank asc) and selects by (score desc,
+ *     depth asc, creation order asc).
+ *   - Calls are independent (no global state); results are deterministic.
+ */
+#ifndef SDM_H
+#define SDM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SDM_OK = 0,
+    SDM_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum */
+    SDM_ERR_UNSUPPORTED = 2,   /* shape or alignment outside the constraints */
+    SDM_ERR_TIER_OVERFLOW = 3, /* reserved: strict tier mode */
+    SDM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
+    SDM_ERR_WORKSPACE = 5      /* ws is NULL or smaller than required */
+} sdm_status;
+
+typedef enum { SDM_BF16 = 0, SDM_FP32 = 1 } sdm_dtype;
+typedef enum { SDM_GREEDY = 0, SDM_SAMPLE = 1 } sdm_decode;
+typedef enum { SDM_STATIC = 0, SDM_COMPACT = 1, SDM_CAP_ACCEPT = 2 } sdm_vmode;
+
+/* bits OR-ed into *dev_status */
+enum {
+    SDM_DEV_BAD_TOKEN = 1,        /* a token id outside [0, V) was read */
+    SDM_DEV_TIER_UNCAPTURED = 2,  /* packed total above every tier: tier = total */
+    SDM_DEV_TIMEOUT = 4,          /* a bounded pipeline wait ran out */
+    SDM_DEV_BAD_WINDOW = 8,       /* budget or cu_seqlens window outside [0, gamma] */
+    SDM_DEV_CAPACITY = 16         /* packed rows would exceed the given capacity */
+};
+
+/* Philox key material: key = seed, counter word 3 = cycle. */
+typedef struct {
+    uint64_t seed;
+    uint64_t cycle;
+} sdm_rng;
+
+/* Operation ids for sdm_workspace_size. */
+enum {
+    SDM_OP_DRAFT_CHAIN = 0,
+    SDM_OP_DRAFT_TREE = 1,
+    SDM_OP_SCHEDULE = 2,
+    SDM_OP_PACK = 3,
+    SDM_OP_VERIFY = 4,
+    SDM_OP_VERIFY_TREE = 5
+};
+
+/* Bytes of scratch the operation needs for these sizes (0 if none).  Pass the
+ * same sizes as the call; unused sizes may be 0.  For SDM_OP_VERIFY pass the
+ * packed row capacity as P. */
+size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int N);
+
+/*
+ * draft_chain: the Markov-head sequential stage ([DSpark notes] sec. 4,
+ * "Sequential stage" and "Markov head"; [PCTree] z_d = L_d + Markov(y_{d-1})).
+ * For d = 1..B, with y_0 = anchor:
+ *     z_d = fp32(L[i, d-1, :]) + U[y_{d-1}] . W          (fp32)
+ *     greedy:  y_d = argmax_v z_d[v]
+ *     sample:  y_d ~ softmax(z_d / T) by the exponential race
+ *              y_d = argmax_v (z_d[v]/T - ln(-ln u_v)), stream 0, row d;
+ *              lse[i, d-1] = log sum_v exp(z_d[v]/T);
+ *              logq[i, d-1] = z_d[y_d]/T - lse[i, d-1].
+ * In:  L [R, B, V] (dtL), U [V, r] bf16, W [r, V] bf16, anchor [R] int32.
+ * Out: tokens [R, B] int32; logq, lse [R, B] fp32 (sample only; may be NULL
+ *      when greedy).
+ * The product U[y] . W runs on the tcgen05 tensor cores (bf16 in, fp32
+ * accumulate in TMEM) and the +L / argmax / race is fused into its epilogue;
+ * z is never written to memory.
+ */
+sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                           const int32_t* anchor, int R, int B, int V, int r,
+                           sdm_decode decode, float temperature, sdm_rng rng,
+                           int32_t* tokens, float* logq, float* lse,
+                           void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * draft_tree: PCTree drafting ([PCTree]: per parent p, z_d(p) = L_d +
+ * Markov(p) for every frontier parent in one batched Markov call; local top-k
+ * per parent; path score s(c) = s(p) + log pi(v | p); top-P prune per level;
+ * global top-N selection within the verify budget; the tree is verified in one
+ * target forward with a tree-causal mask ([DSpark notes] JetSpec note: a node
+ * attends to its ancestors only)).
+ * Level 1 expands the root (token anchor[i], score 0); level d expands the
+ * <= P nodes kept at level d-1.  Scores use T = 1 and are fp32.
+ * Out (per request, N+1 slots; slot 0 = root, then the selected nodes in
+ * rank order so parent[c] < c; unused slots hold -1 / 0):
+ *   tok, parent, depth [R, N+1] int32; score [R, N+1] fp32;
+ *   mask [R, N+1, ceil((N+1)/32)] uint32, bit j of row c set iff slot j is c
+ *   or an ancestor of c; n_nodes [R] int32 (root included).
+ * Constraints: 1 <= k <= 8, 1 <= P, P*k <= 64, 128 % P == 0, N <= P*B.
+ */
+sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                          const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N,
+                          int32_t* tok, int32_t* parent, int32_t* depth, float* score,
+                          uint32_t* mask, int32_t* n_nodes,
+                          void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * schedule_budget: confidence survival and the hardware-aware prefix budget
+ * ([DSpark notes] sec. 5.1 and 5.2; [SGLang] "SPS cost table").
+ *   S[i, k] = S[i, k-1] * c[i, k]  (fp32, k = 1..gamma, S[i, 0] = 1)
+ *   Survivals >= 2^-18 are ranked (S desc, request asc, position asc); with
+ *   E(m) = R + sum of the top m and N(m) = R + m, the greedy adds the next
+ *   survival while E(m+1)/cost[N(m+1)] > E(m)/cost[N(m)] and stops at the
+ *   first that does not improve it.  budget[i] = request i's count in the
+ *   top m*.  Sums are exact in fp64.
+ * In:  conf [R, gamma] fp32 (post-sigmoid), cost [R*(gamma+1)+1] fp64 (step
+ *      cost by total verify tokens).
+ * Out: survival [R, gamma] fp32, budget [R] int32, expected [1] fp64 (E(m*)),
+ *      total_tokens [1] int32 (N(m*)).
+ * Constraint: R * gamma <= 8192.
+ */
+sdm_status sdm_schedule_budget(const float* conf, int R, int gamma, const double* cost,
+                               float* survival, int32_t* budget, double* expected,
+                               int32_t* total_tokens, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * pack_ragged: ragged front-pack of the verify windows ([SGLang] "ragged
+ * verify": windows are front-packed into a compact cu_seqlens buffer whose
+ * total is rounded up to the nearest captured tier).
+ *   n_i = budget[i] (budget == NULL: n_i = gamma, the static block)
+ *   cu_seqlens[0] = 0, cu_seqlens[i+1] = cu_seqlens[i] + n_i + 1
+ *   rows cu[i] .. cu[i] + n_i hold y_0 (anchor), y_1 .. y_{n_i}, with
+ *   packed_req = i and packed_pos = 0..n_i; rows total .. tier-1 hold -1.
+ *   tier = smallest tiers[q] >= total; above every tier: tier = total and
+ *   SDM_DEV_TIER_UNCAPTURED is set (the caller runs uncaptured).
+ * In:  anchor [R], draft [R, gamma], budget [R] or NULL, tiers [n_tiers]
+ *      int32 (device).
+ * Out: cu_seqlens [R+1], packed_tok/req/pos [capacity], tier [1] (device);
+ *      tier_host (host, may be NULL): if non-NULL it must be pinned host
+ *      memory and receives the tier by an async copy on `stream`.
+ * capacity >= max(max tier, R*(gamma+1)) guarantees every row fits; rows past
+ * capacity are dropped and SDM_DEV_CAPACITY is set.
+ */
+sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,
+                           int R, int gamma, const int32_t* tiers, int n_tiers,
+                           int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
+                           int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,
+                           int32_t* dev_status, void* stream);
+
+/*
+ * verify: fused verification over the packed target logits ([DSpark notes]
+ * sec. 1: left-to-right acceptance, discard after the first rejection, one
+ * bonus token; [SGLang] "three verify modes").
+ * Window of request i: w_i = cu[i+1] - cu[i] - 1 drafts, target rows
+ * cu[i] .. cu[i] + w_i; row p is the target's prediction after y_p.
+ *   greedy: t_p = argmax target row p; A = first p < w_i with y_{p+1} != t_p,
+ *           else w_i; commit a = A drafts and t_a.
+ *   sample: accept y_{p+1} iff u(stream 1, row p) < p_p(y)/q_p(y), with
+ *           p = softmax(target row / T) and q_p(y) = exp(logq[i, p]); at the
+ *           first rejection p = a, sample from max(0, p_a - q_a) where q_a is
+ *           recomputed from L, U, W and lse_q (stream 2, row a); if all
+ *           committed drafts pass, the bonus is drawn from p at row a
+ *           (stream 3).  The exponential race is the sampler throughout.
+ *   modes: STATIC (w_i = gamma, commit A), COMPACT (w_i = budget, commit A),
+ *          CAP_ACCEPT (w_i = gamma verified, commit a = min(A, budget[i]):
+ *          the same output as compact; ceiling = A).
+ * In:  target [rows, V] (dtT), cu_seqlens [R+1], anchor [R], draft [R, gamma];
+ *      budget [R] (CAP_ACCEPT only); logq, lse_q [R, gamma] fp32, L [R, gamma,
+ *      V], U, W, r (SAMPLE only, else may be NULL/0).  row_capacity = rows
+ *      allocated in target (an upper bound on cu[R]).
+ * Out: accept [R], ceiling [R] (may be NULL), out_tok [R, gamma+1] (-1
+ *      padded), n_out [R] = accept + 1.
+ */
+sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_rng rng,
+                      const void* target, sdm_dtype dtT, int row_capacity, const int32_t* cu_seqlens,
+                      const int32_t* anchor, const int32_t* draft, const int32_t* budget,
+                      const float* logq, const float* lse_q,
+                      const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, int r,
+                      int R, int gamma, int V,
+                      int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * verify_tree: greedy verification of a drafted tree in one target forward
+ * ([PCTree]; greedy only).  Walk from the root: t = argmax of the current
+ * slot's target row; move to the child whose token is t; stop when none is.
+ * accept = depth reached; out_tok = accepted tokens then t (bonus).
+ * In:  target [R, N+1, V] (dtT; slot c's row predicts c's child), tok, parent
+ *      [R, N+1], n_nodes [R].
+ * Out: accept [R], out_tok [R, B+1] (-1 padded), n_out [R].
+ */
+sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok,
+                           const int32_t* parent, const int32_t* n_nodes, int R, int N, int B, int V,
+                           int32_t* accept, int32_t* out_tok, int32_t* n_out,
+                           void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* sdm_status_str(sdm_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int sdm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDM_H */

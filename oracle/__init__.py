@@ -143,7 +143,7 @@ def pack_ragged(anchor, draft, budget, tiers):
 
 
 def verify(mode, decode, target, cu_seqlens, anchor, draft, budget=None, logq=None, lse_q=None,
-           L=None, U=None, W=None, temperature=1.0, seed=0, cycle=0):
+           L=None, U=None, W=None, temperature=1.0, seed=0, cycle=0, req_ids=None):
     """target [rows, V] packed (uint16 bf16 bits or float32)."""
     R, g = draft.shape
     V = target.shape[-1]
@@ -157,7 +157,7 @@ def verify(mode, decode, target, cu_seqlens, anchor, draft, budget=None, logq=No
     Lc = None if L is None else np.ascontiguousarray(L)
     flags = lib().orc_verify(
         mode, decode, ctypes.c_double(temperature), ctypes.c_uint64(seed), ctypes.c_uint64(cycle),
-        _p(target), _dt(target), _p(_c(cu_seqlens, np.int32)), _p(_c(anchor, np.int32)), _p(_c(draft, np.int32)),
+        _p(None if req_ids is None else _c(req_ids, np.int32)), _p(target), _dt(target), _p(_c(cu_seqlens, np.int32)), _p(_c(anchor, np.int32)), _p(_c(draft, np.int32)),
         _p(None if budget is None else _c(budget, np.int32)),
         _p(None if logq is None else _c(logq, np.float64)), _p(None if lse_q is None else _c(lse_q, np.float64)),
         _p(Lc), 0 if Lc is None else _dt(Lc), _p(None if U is None else _c(U, np.uint16)),

@@ -473,7 +473,7 @@ static double row_lse(const void* T, int dtT, size_t row, int V, double inv_t) {
 }
 
 int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t cycle,
-               const void* target, int dtT, const int32_t* cu_seqlens,
+               const int32_t* req_ids, const void* target, int dtT, const int32_t* cu_seqlens,
                const int32_t* anchor, const int32_t* draft, const int32_t* budget,
                const double* logq, const double* lse_q,
                const void* L, int dtL, const uint16_t* U, const uint16_t* W, int r,
@@ -485,6 +485,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
     double* M = (double*)malloc(sizeof(double) * (size_t)V);
     float* z = (float*)malloc(sizeof(float) * (size_t)V);
     for (int i = 0; i < R; ++i) {
+        uint32_t gid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
         size_t row0 = (size_t)cu_seqlens[i];
         int w = cu_seqlens[i + 1] - cu_seqlens[i] - 1;           /* drafts in the window */
         int cap = (mode == ORC_CAP_ACCEPT) ? budget[i] : w;       /* drafts that may commit */
@@ -513,7 +514,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
                 double lp = (double)load_elem(target, dtT, (row0 + (size_t)p) * (size_t)V + (size_t)y[p]) * inv_t
                             - row_lse(target, dtT, row0 + (size_t)p, V, inv_t);
                 double lq = logq[(size_t)i * gamma + (size_t)p];
-                double lu = log(orc_uniform(seed, cycle, ORC_STREAM_ACCEPT, (uint32_t)i, (uint32_t)p, 0u));
+                double lu = log(orc_uniform(seed, cycle, ORC_STREAM_ACCEPT, gid, (uint32_t)p, 0u));
                 double g = fabs(lu - (lp - lq));
                 if (g < min_gap) min_gap = g;
                 if (!(lu < lp - lq)) {
@@ -538,7 +539,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
                     double qv = exp((double)z[v] * inv_t - lq_row);
                     double wv = pv - qv;
                     if (!(wv > 0.0)) continue;
-                    double u = orc_uniform(seed, cycle, ORC_STREAM_RESID, (uint32_t)i, (uint32_t)row, (uint32_t)v);
+                    double u = orc_uniform(seed, cycle, ORC_STREAM_RESID, gid, (uint32_t)row, (uint32_t)v);
                     double key = log(wv) - log(race_exponential(u));
                     if (key > best) {
                         second = best;
@@ -551,7 +552,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
             } else {
                 /* every committed draft accepted: bonus token ~ p at row a */
                 for (int v = 0; v < V; ++v) {
-                    double u = orc_uniform(seed, cycle, ORC_STREAM_BONUS, (uint32_t)i, (uint32_t)row, (uint32_t)v);
+                    double u = orc_uniform(seed, cycle, ORC_STREAM_BONUS, gid, (uint32_t)row, (uint32_t)v);
                     double key = (double)load_elem(target, dtT, (row0 + (size_t)row) * (size_t)V + (size_t)v) * inv_t
                                  - log(race_exponential(u));
                     if (key > best) {

@@ -80,10 +80,11 @@ int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* 
                     int32_t* packed_pos, int32_t* tier, int32_t* flags);
 
 /* Verification over packed target logits [rows, V].  budget is only read in
- * cap-accept mode; logq/lse_q/L/U/W/r only in sample mode.  margin[i] = the
- * smallest decision margin met for request i (may be NULL). */
+ * cap-accept mode; logq/lse_q/L/U/W/r only in sample mode.  req_ids (may be
+ * NULL) maps local request i to the global request id of the random counters.
+ * margin[i] = the smallest decision margin met for request i (may be NULL). */
 int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t cycle,
-               const void* target, int dtT, const int32_t* cu_seqlens,
+               const int32_t* req_ids, const void* target, int dtT, const int32_t* cu_seqlens,
                const int32_t* anchor, const int32_t* draft, const int32_t* budget,
                const double* logq, const double* lse_q,
                const void* L, int dtL, const uint16_t* U, const uint16_t* W, int r,

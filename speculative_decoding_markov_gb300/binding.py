@@ -1,0 +1,250 @@
+"""Python binding of libsdm.so (ctypes): argument marshalling only.
+
+`sdm_*` are the raw C entry points (pointers and sizes).  The lower-case
+helpers take torch CUDA tensors, allocate outputs and the workspace with
+torch (device memory is all torch provides here), call the C entry point on
+the current stream and return the outputs.  Every computation happens in the
+library's CUDA kernels; there is no fallback: if libsdm.so is missing or no
+GPU is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsdm.so")
+
+BF16, FP32 = 0, 1
+GREEDY, SAMPLE = 0, 1
+STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
+OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE = range(6)
+DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY = 1, 2, 4, 8, 16
+
+EXPORTS = ("sdm_workspace_size", "sdm_draft_chain", "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged",
+           "sdm_verify", "sdm_verify_tree", "sdm_status_str", "sdm_version")
+
+
+class SdmRng(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64), ("cycle", ctypes.c_uint64)]
+
+
+_lib = None
+_VP, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+
+
+def _declare(lib):
+    lib.sdm_workspace_size.restype = _SZ
+    lib.sdm_workspace_size.argtypes = [_I] * 8
+    lib.sdm_status_str.restype = ctypes.c_char_p
+    lib.sdm_status_str.argtypes = [_I]
+    lib.sdm_version.restype = _I
+    lib.sdm_draft_chain.restype = _I
+    lib.sdm_draft_chain.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, SdmRng, _VP, _VP, _VP, _VP, _SZ,
+                                    _VP, _VP]
+    lib.sdm_draft_tree.restype = _I
+    lib.sdm_draft_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP,
+                                   _VP, _SZ, _VP, _VP]
+    lib.sdm_schedule_budget.restype = _I
+    lib.sdm_schedule_budget.argtypes = [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+    lib.sdm_pack_ragged.restype = _I
+    lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
+    lib.sdm_verify.restype = _I
+    lib.sdm_verify.argtypes = [_I, _I, _F, SdmRng, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I,
+                               _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+    lib.sdm_verify_tree.restype = _I
+    lib.sdm_verify_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+
+
+def load(path: str = LIB_PATH):
+    """Load libsdm.so (built by __graft_entry__.build / build.py); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libsdm.so not built at {path}: run speculative_decoding_markov_gb300.build")
+        lib = ctypes.CDLL(path)
+        _declare(lib)
+        _lib = lib
+    return _lib
+
+
+def lib():
+    return load()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(st: int, what: str):
+    if st != 0:
+        raise RuntimeError(f"{what}: {lib().sdm_status_str(st).decode()} (status {st})")
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("inputs must be contiguous CUDA tensors")
+
+
+def _u16(t):
+    """bf16 tensors are passed by pointer; this only checks the dtype."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError("U and W must be bf16")
+    return t
+
+
+def workspace(op, R, B=0, V=0, r=0, P=0, k=0, N=0, device="cuda"):
+    n = lib().sdm_workspace_size(op, R, B, V, r, P, k, N)
+    return torch.empty(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
+def new_status(device="cuda"):
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+# ---------------------------------------------------------------------------
+def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0, out=None, ws=None,
+                dev_status=None):
+    _need_cuda(L, U, W, anchor)
+    R, B, V = L.shape
+    r = U.shape[1]
+    dev = L.device
+    if out is None:
+        out = dict(tokens=torch.empty((R, B), dtype=torch.int32, device=dev),
+                   logq=torch.zeros((R, B), dtype=torch.float32, device=dev),
+                   lse=torch.zeros((R, B), dtype=torch.float32, device=dev))
+    ws = workspace(OP_DRAFT_CHAIN, R, B, V, r, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_draft_chain(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(anchor), R, B, V, r, decode,
+                               float(temperature), SdmRng(seed, cycle), _ptr(out["tokens"]), _ptr(out["logq"]),
+                               _ptr(out["lse"]), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_draft_chain")
+    out["dev_status"] = dev_status
+    return out
+
+
+def draft_tree(L, U, W, anchor, k, P, N, out=None, ws=None, dev_status=None):
+    _need_cuda(L, U, W, anchor)
+    R, B, V = L.shape
+    r = U.shape[1]
+    dev = L.device
+    S = N + 1
+    words = (S + 31) // 32
+    if out is None:
+        out = dict(tok=torch.empty((R, S), dtype=torch.int32, device=dev),
+                   parent=torch.empty((R, S), dtype=torch.int32, device=dev),
+                   depth=torch.empty((R, S), dtype=torch.int32, device=dev),
+                   score=torch.empty((R, S), dtype=torch.float32, device=dev),
+                   mask=torch.empty((R, S, words), dtype=torch.int32, device=dev),
+                   n_nodes=torch.empty((R,), dtype=torch.int32, device=dev))
+    ws = workspace(OP_DRAFT_TREE, R, B, V, r, P, k, N, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_draft_tree(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(anchor), R, B, V, r, k, P, N,
+                              _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["score"]),
+                              _ptr(out["mask"]), _ptr(out["n_nodes"]), _ptr(ws), ws.numel(), _ptr(dev_status),
+                              _stream())
+    _check(st, "sdm_draft_tree")
+    out["dev_status"] = dev_status
+    return out
+
+
+def schedule_budget(conf, cost, out=None, dev_status=None):
+    _need_cuda(conf, cost)
+    R, g = conf.shape
+    dev = conf.device
+    if out is None:
+        out = dict(survival=torch.empty((R, g), dtype=torch.float32, device=dev),
+                   budget=torch.empty((R,), dtype=torch.int32, device=dev),
+                   expected=torch.empty((1,), dtype=torch.float64, device=dev),
+                   total_tokens=torch.empty((1,), dtype=torch.int32, device=dev))
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_schedule_budget(_ptr(conf), R, g, _ptr(cost), _ptr(out["survival"]), _ptr(out["budget"]),
+                                   _ptr(out["expected"]), _ptr(out["total_tokens"]), None, 0, _ptr(dev_status),
+                                   _stream())
+    _check(st, "sdm_schedule_budget")
+    out["dev_status"] = dev_status
+    return out
+
+
+def pack_capacity(R, gamma, tiers) -> int:
+    return max(max(tiers) if len(tiers) else 0, R * (gamma + 1))
+
+
+def pack_ragged(anchor, draft, budget, tiers, capacity=None, out=None, dev_status=None, tier_host=None):
+    _need_cuda(anchor, draft, budget, tiers)
+    R, g = draft.shape
+    dev = draft.device
+    if out is None:
+        cap = capacity if capacity else pack_capacity(R, g, tiers.tolist())
+        out = dict(cu_seqlens=torch.empty((R + 1,), dtype=torch.int32, device=dev),
+                   packed_tok=torch.empty((cap,), dtype=torch.int32, device=dev),
+                   packed_req=torch.empty((cap,), dtype=torch.int32, device=dev),
+                   packed_pos=torch.empty((cap,), dtype=torch.int32, device=dev),
+                   tier=torch.empty((1,), dtype=torch.int32, device=dev))
+    cap = out["packed_tok"].numel()
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_pack_ragged(_ptr(anchor), _ptr(draft), _ptr(budget), R, g, _ptr(tiers), tiers.numel(),
+                               _ptr(out["cu_seqlens"]), _ptr(out["packed_tok"]), _ptr(out["packed_req"]),
+                               _ptr(out["packed_pos"]), cap, _ptr(out["tier"]), _ptr(tier_host), _ptr(dev_status),
+                               _stream())
+    _check(st, "sdm_pack_ragged")
+    out["dev_status"] = dev_status
+    return out
+
+
+def verify(mode, decode, target, cu_seqlens, anchor, draft, budget=None, logq=None, lse_q=None, L=None, U=None,
+           W=None, temperature=1.0, seed=0, cycle=0, out=None, ws=None, dev_status=None):
+    _need_cuda(target, cu_seqlens, anchor, draft, budget, logq, lse_q, L, U, W)
+    R, g = draft.shape
+    V = target.shape[-1]
+    rows = target.numel() // V
+    dev = target.device
+    r = 0 if U is None else U.shape[1]
+    if out is None:
+        out = dict(accept=torch.empty((R,), dtype=torch.int32, device=dev),
+                   ceiling=torch.empty((R,), dtype=torch.int32, device=dev),
+                   out_tok=torch.empty((R, g + 1), dtype=torch.int32, device=dev),
+                   n_out=torch.empty((R,), dtype=torch.int32, device=dev))
+    ws = workspace(OP_VERIFY, R, g, V, r, rows, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_verify(mode, decode, float(temperature), SdmRng(seed, cycle), _ptr(target), _dt(target), rows,
+                          _ptr(cu_seqlens), _ptr(anchor), _ptr(draft), _ptr(budget), _ptr(logq), _ptr(lse_q),
+                          _ptr(L), _dt(L) if L is not None else BF16, _ptr(U), _ptr(W), r, R, g, V,
+                          _ptr(out["accept"]), _ptr(out["ceiling"]), _ptr(out["out_tok"]), _ptr(out["n_out"]),
+                          _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_verify")
+    out["dev_status"] = dev_status
+    return out
+
+
+def verify_tree(target, tok, parent, n_nodes, B, out=None, ws=None, dev_status=None):
+    _need_cuda(target, tok, parent, n_nodes)
+    R, S, V = target.shape
+    dev = target.device
+    if out is None:
+        out = dict(accept=torch.empty((R,), dtype=torch.int32, device=dev),
+                   out_tok=torch.empty((R, B + 1), dtype=torch.int32, device=dev),
+                   n_out=torch.empty((R,), dtype=torch.int32, device=dev))
+    ws = workspace(OP_VERIFY_TREE, R, B, V, 0, 0, 0, S - 1, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_verify_tree(_ptr(target), _dt(target), _ptr(tok), _ptr(parent), _ptr(n_nodes), R, S - 1, B, V,
+                               _ptr(out["accept"]), _ptr(out["out_tok"]), _ptr(out["n_out"]), _ptr(ws), ws.numel(),
+                               _ptr(dev_status), _stream())
+    _check(st, "sdm_verify_tree")
+    out["dev_status"] = dev_status
+    return out

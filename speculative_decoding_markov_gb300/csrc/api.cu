@@ -1,0 +1,431 @@
+// api.cu - the extern "C" entry points of libsdm.so (declared in include/sdm.h):
+// argument validation, tensor-map encoding, workspace carving and the launch
+// sequence of each operation.  Every operation is enqueued on the caller's
+// stream and allocates nothing.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+using namespace sdm;
+
+constexpr int kMaxGx = 256;           // upper bound of vocab splits per GEMM launch
+constexpr int kChunkBf16 = 16384;     // ids per streaming work item (32 KB)
+constexpr int kChunkFp32 = 8192;
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Carver {
+    uint8_t* base;
+    size_t off = 0;
+    template <typename T>
+    T* take(size_t count) {
+        T* p = reinterpret_cast<T*>(base + off);
+        off = align256(off + count * sizeof(T));
+        return p;
+    }
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// W [r, V] bf16 as a 2-D map (V innermost), box 64 x r, 128-byte swizzle.
+bool map_w(CUtensorMap* m, const uint16_t* W, int r, int V) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(r)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(r)};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// L [R, B, V] as a 3-D map (V, B, R), box (128 bytes of V) x 1 x l_rows.
+bool map_l(CUtensorMap* m, const void* L, int fp32, int R, int B, int V, int l_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t es = fp32 ? 4 : 2;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(B), static_cast<cuuint64_t>(R)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(V) * es, static_cast<cuuint64_t>(V) * B * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(fp32 ? 32 : 64), 1, static_cast<cuuint32_t>(l_rows)};
+    cuuint32_t el[3] = {1, 1, 1};
+    return fn(m, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(L),
+              dims, strides, box, el, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int gemm_grid_x(int n_tiles, int grid_y) {
+    int gx = std::max(1, num_sms() / grid_y);
+    gx = std::min(gx, n_tiles);
+    return std::min(gx, kMaxGx);
+}
+
+inline bool vocab_ok(int V) { return V >= 8 && V % 8 == 0; }
+inline bool rank_ok(int r) { return r >= 64 && r <= 256 && r % 64 == 0; }
+inline int n_chunks_of(int V, int fp32) {
+    const int c = fp32 ? kChunkFp32 : kChunkBf16;
+    return (V + c - 1) / c;
+}
+
+#define SDM_CHECK_CUDA(x)                          \
+    do {                                           \
+        if ((x) != cudaSuccess) return SDM_ERR_CUDA; \
+    } while (0)
+
+size_t ws_chain(int R, int B) {
+    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(B) * R * kMaxGx * 8);
+}
+
+size_t ws_tree(int R, int B, int P) {
+    const size_t rows = static_cast<size_t>(R) * P;
+    const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
+    return align256(rows * kMaxGx * (2 + 2 * kMaxTopK) * 4) + 3 * align256(rows * 4) + align256(R * 4) +
+           4 * align256(pool * 4) + align256(R * 4);
+}
+
+size_t ws_verify(int R, int rows, int V) {
+    const int nc = n_chunks_of(V, 0) > n_chunks_of(V, 1) ? n_chunks_of(V, 0) : n_chunks_of(V, 1);
+    return align256(static_cast<size_t>(rows) * 8) + align256(static_cast<size_t>(rows) * nc * 8) +
+           6 * align256(static_cast<size_t>(R) * 4) + align256(static_cast<size_t>(R) * 8);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int N) {
+    (void)r;
+    (void)k;
+    if (R <= 0) return 0;
+    switch (op) {
+        case SDM_OP_DRAFT_CHAIN: return ws_chain(R, B);
+        case SDM_OP_DRAFT_TREE: return ws_tree(R, B, P);
+        case SDM_OP_VERIFY: return ws_verify(R, P, V);
+        case SDM_OP_VERIFY_TREE: return align256(static_cast<size_t>(R) * (N + 1) * 8);
+        default: return 0;
+    }
+}
+
+const char* sdm_status_str(sdm_status st) {
+    switch (st) {
+        case SDM_OK: return "ok";
+        case SDM_ERR_INVALID_ARG: return "invalid argument";
+        case SDM_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+        case SDM_ERR_TIER_OVERFLOW: return "packed total above every tier";
+        case SDM_ERR_CUDA: return "CUDA error";
+        case SDM_ERR_WORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+int sdm_version(void) { return 100; }
+
+sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                           const int32_t* anchor, int R, int B, int V, int r, sdm_decode decode, float temperature,
+                           sdm_rng rng, int32_t* tokens, float* logq, float* lse, void* ws, size_t ws_bytes,
+                           int32_t* dev_status, void* stream) {
+    if (!L || !U || !W || !anchor || !tokens || R <= 0 || B <= 0 || V <= 0 || r <= 0) return SDM_ERR_INVALID_ARG;
+    if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (decode != SDM_GREEDY && decode != SDM_SAMPLE) return SDM_ERR_INVALID_ARG;
+    if (decode == SDM_SAMPLE && !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_chain(R, B)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Carver c{static_cast<uint8_t*>(ws)};
+    auto* keys = c.take<unsigned long long>(static_cast<size_t>(B) * R);
+    auto* lse_part = c.take<float2>(static_cast<size_t>(B) * R * kMaxGx);
+
+    const int fp32 = dtL == SDM_FP32;
+    const int l_rows = std::min(R, kTileM);
+    CUtensorMap tmW, tmL;
+    if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
+    const int mode = decode == SDM_GREEDY ? MODE_CHAIN_GREEDY : MODE_CHAIN_SAMPLE;
+    const int n_tiles = (V + kTileN - 1) / kTileN;
+    const int gy = (R + kTileM - 1) / kTileM;
+    const int gx = gemm_grid_x(n_tiles, gy);
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = R;
+    p.R = R;
+    p.B = B;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = n_tiles;
+    p.l_fp32 = fp32;
+    p.l_rows = l_rows;
+    p.P = 1;
+    p.k = 1;
+    p.stages = gemm_pick_stages(r, l_rows, fp32, mode);
+    p.inv_t = decode == SDM_SAMPLE ? 1.0f / temperature : 1.0f;
+    p.rng_k0 = static_cast<uint32_t>(rng.seed);
+    p.rng_k1 = static_cast<uint32_t>(rng.seed >> 32);
+    p.rng_cycle = static_cast<uint32_t>(rng.cycle);
+    p.U = U;
+    p.anchor = anchor;
+    p.keys = keys;
+    p.lse_part = lse_part;
+    p.dev_status = dev_status;
+
+    SDM_CHECK_CUDA(launch_fill_u64(keys, static_cast<size_t>(B) * R, 0ull, s));
+    for (int d = 1; d <= B; ++d) {
+        p.d = d;
+        SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
+    }
+    SDM_CHECK_CUDA(launch_chain_finalize(keys, lse_part, gx, R, B, V, r, L, fp32, U, W, anchor, p.inv_t,
+                                         decode == SDM_SAMPLE, tokens, logq, lse, dev_status, s));
+    return SDM_OK;
+}
+
+sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                          const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N, int32_t* tok,
+                          int32_t* parent, int32_t* depth, float* score, uint32_t* mask, int32_t* n_nodes, void* ws,
+                          size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!L || !U || !W || !anchor || !tok || !parent || !depth || !score || !mask || !n_nodes) return SDM_ERR_INVALID_ARG;
+    if (R <= 0 || B <= 0 || V <= 0 || r <= 0 || k <= 0 || P <= 0 || N <= 0) return SDM_ERR_INVALID_ARG;
+    if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
+    if (k > kMaxTopK || k > V || P * k > 64 || kTileM % P != 0 || N > P * B) return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_tree(R, B, P)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t rows = static_cast<size_t>(R) * P;
+    const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
+    Carver c{static_cast<uint8_t*>(ws)};
+    float* tree_part = c.take<float>(rows * kMaxGx * (2 + 2 * kMaxTopK));
+    int32_t* front_tok = c.take<int32_t>(rows);
+    int32_t* front_node = c.take<int32_t>(rows);
+    float* front_score = c.take<float>(rows);
+    int32_t* n_front = c.take<int32_t>(R);
+    int32_t* pool_tok = c.take<int32_t>(pool);
+    int32_t* pool_parent = c.take<int32_t>(pool);
+    int32_t* pool_depth = c.take<int32_t>(pool);
+    float* pool_score = c.take<float>(pool);
+    int32_t* pool_n = c.take<int32_t>(R);
+
+    const int fp32 = dtL == SDM_FP32;
+    const int l_rows = std::min(kTileM / P, R);
+    CUtensorMap tmW, tmL;
+    if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
+    const int n_tiles = (V + kTileN - 1) / kTileN;
+    const int gy = static_cast<int>((rows + kTileM - 1) / kTileM);
+    const int gx = gemm_grid_x(n_tiles, gy);
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = static_cast<int>(rows);
+    p.R = R;
+    p.B = B;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = n_tiles;
+    p.l_fp32 = fp32;
+    p.l_rows = l_rows;
+    p.P = P;
+    p.k = k;
+    p.stages = gemm_pick_stages(r, l_rows, fp32, MODE_TREE);
+    p.inv_t = 1.0f;
+    p.U = U;
+    p.anchor = anchor;
+    p.front_tok = front_tok;
+    p.tree_part = tree_part;
+    p.dev_status = dev_status;
+
+    SDM_CHECK_CUDA(launch_tree_init(anchor, R, P, B, front_tok, front_node, front_score, n_front, pool_tok, pool_parent,
+                                    pool_depth, pool_score, pool_n, dev_status, s));
+    for (int d = 1; d <= B; ++d) {
+        p.d = d;
+        SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE, tmW, tmL, p, gx, gy, s));
+        SDM_CHECK_CUDA(launch_tree_merge(tree_part, gx, R, P, k, B, d, front_tok, front_node, front_score, n_front,
+                                         pool_tok, pool_parent, pool_depth, pool_score, pool_n, s));
+    }
+    SDM_CHECK_CUDA(launch_tree_finalize(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok, parent,
+                                        depth, score, mask, n_nodes, s));
+    return SDM_OK;
+}
+
+sdm_status sdm_schedule_budget(const float* conf, int R, int gamma, const double* cost, float* survival,
+                               int32_t* budget, double* expected, int32_t* total_tokens, void* ws, size_t ws_bytes,
+                               int32_t* dev_status, void* stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!conf || !cost || !survival || !budget || !expected || !total_tokens || R <= 0 || gamma <= 0)
+        return SDM_ERR_INVALID_ARG;
+    if (static_cast<long long>(R) * gamma > 8192) return SDM_ERR_UNSUPPORTED;
+    SDM_CHECK_CUDA(launch_schedule(conf, R, gamma, cost, survival, budget, expected, total_tokens, nullptr, dev_status,
+                                   static_cast<cudaStream_t>(stream)));
+    return SDM_OK;
+}
+
+sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
+                           const int32_t* tiers, int n_tiers, int32_t* cu_seqlens, int32_t* packed_tok,
+                           int32_t* packed_req, int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,
+                           int32_t* dev_status, void* stream) {
+    if (!anchor || !draft || !cu_seqlens || !packed_tok || !packed_req || !packed_pos || !tier) return SDM_ERR_INVALID_ARG;
+    if (R <= 0 || gamma < 0 || n_tiers < 0 || capacity <= 0 || (n_tiers > 0 && !tiers)) return SDM_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    SDM_CHECK_CUDA(launch_pack(anchor, draft, budget, R, gamma, tiers, n_tiers, cu_seqlens, packed_tok, packed_req,
+                               packed_pos, capacity, tier, dev_status, s));
+    if (tier_host) SDM_CHECK_CUDA(cudaMemcpyAsync(tier_host, tier, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+    return SDM_OK;
+}
+
+sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_rng rng, const void* target,
+                      sdm_dtype dtT, int row_capacity, const int32_t* cu_seqlens, const int32_t* anchor,
+                      const int32_t* draft, const int32_t* budget, const float* logq, const float* lse_q,
+                      const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, int r, int R, int gamma,
+                      int V, int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out, void* ws,
+                      size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!target || !cu_seqlens || !anchor || !draft || !accept || !out_tok || !n_out) return SDM_ERR_INVALID_ARG;
+    if (R <= 0 || gamma <= 0 || V <= 0 || row_capacity <= 0) return SDM_ERR_INVALID_ARG;
+    if (mode != SDM_STATIC && mode != SDM_COMPACT && mode != SDM_CAP_ACCEPT) return SDM_ERR_INVALID_ARG;
+    if (decode != SDM_GREEDY && decode != SDM_SAMPLE) return SDM_ERR_INVALID_ARG;
+    if (dtT != SDM_BF16 && dtT != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (mode == SDM_CAP_ACCEPT && !budget) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !aligned16(target)) return SDM_ERR_UNSUPPORTED;
+    if (decode == SDM_SAMPLE) {
+        if (!logq || !lse_q || !L || !U || !W || !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
+        if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+        if (!rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
+    }
+    if (!ws || ws_bytes < ws_verify(R, row_capacity, V)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int t_fp32 = dtT == SDM_FP32;
+    const int nchunk_max = std::max(n_chunks_of(V, 0), n_chunks_of(V, 1));
+    Carver c{static_cast<uint8_t*>(ws)};
+    auto* row_keys = c.take<unsigned long long>(row_capacity);
+    auto* lse_part = c.take<float2>(static_cast<size_t>(row_capacity) * nchunk_max);
+    int32_t* res_tok = c.take<int32_t>(R);
+    int32_t* res_pos = c.take<int32_t>(R);
+    int32_t* res_trow = c.take<int32_t>(R);
+    float* res_lse_p = c.take<float>(R);
+    int32_t* bonus_row = c.take<int32_t>(R);
+    int32_t* bonus_pos = c.take<int32_t>(R);
+    auto* res_keys = c.take<unsigned long long>(R);
+
+    StreamParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.base = target;
+    sp.fp32 = t_fp32;
+    sp.V = V;
+    sp.chunk = t_fp32 ? kChunkFp32 : kChunkBf16;
+    sp.n_chunks = n_chunks_of(V, t_fp32);
+    sp.count = cu_seqlens + R;
+    sp.n_items = row_capacity;
+    sp.inv_t = decode == SDM_SAMPLE ? 1.0f / temperature : 1.0f;
+
+    if (decode == SDM_GREEDY) {
+        sp.keys = row_keys;
+        SDM_CHECK_CUDA(launch_fill_u64(row_keys, row_capacity, 0ull, s));
+        SDM_CHECK_CUDA(launch_stream(STREAM_ARGMAX, sp, row_capacity, s));
+        SDM_CHECK_CUDA(launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, row_keys, R, gamma, V, accept,
+                                                     ceiling, out_tok, n_out, dev_status, s));
+        return SDM_OK;
+    }
+    // rejection sampling
+    const uint32_t k0 = static_cast<uint32_t>(rng.seed), k1 = static_cast<uint32_t>(rng.seed >> 32);
+    const uint32_t cyc = static_cast<uint32_t>(rng.cycle);
+    sp.part = lse_part;
+    SDM_CHECK_CUDA(launch_stream(STREAM_LSE, sp, row_capacity, s));
+    SDM_CHECK_CUDA(launch_verify_sample_scan(mode, cu_seqlens, anchor, draft, budget, logq, target, t_fp32, V, lse_part,
+                                             sp.n_chunks, sp.inv_t, k0, k1, cyc, R, gamma, accept, ceiling, res_tok,
+                                             res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, res_keys, dev_status,
+                                             s));
+    // residual rows: recompute q with the Markov head, race over max(0, p - q)
+    CUtensorMap tmW;
+    if (!map_w(&tmW, W, r, V)) return SDM_ERR_CUDA;
+    const int n_tiles = (V + kTileN - 1) / kTileN;
+    const int gy = (R + kTileM - 1) / kTileM;
+    const int gx = gemm_grid_x(n_tiles, gy);
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = R;
+    p.R = R;
+    p.B = gamma;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = n_tiles;
+    p.l_fp32 = dtL == SDM_FP32;
+    p.l_rows = 1;
+    p.P = 1;
+    p.k = 1;
+    p.d = 1;
+    p.stages = gemm_pick_stages(r, 1, p.l_fp32, MODE_RESID);
+    p.inv_t = sp.inv_t;
+    p.rng_k0 = k0;
+    p.rng_k1 = k1;
+    p.rng_cycle = cyc;
+    p.U = U;
+    p.res_tok = res_tok;
+    p.res_pos = res_pos;
+    p.res_trow = res_trow;
+    p.res_lse_p = res_lse_p;
+    p.lse_q = lse_q;
+    p.L = L;
+    p.target = target;
+    p.t_fp32 = t_fp32;
+    p.gamma = gamma;
+    p.res_keys = res_keys;
+    p.dev_status = dev_status;
+    SDM_CHECK_CUDA(launch_markov_gemm(MODE_RESID, tmW, tmW, p, gx, gy, s));
+    // bonus rows: race over p
+    StreamParams bp = sp;
+    bp.count = nullptr;
+    bp.n_items = R;
+    bp.row_of = bonus_row;
+    bp.race_row = bonus_pos;
+    bp.keys = res_keys;
+    bp.part = nullptr;
+    bp.rng_k0 = k0;
+    bp.rng_k1 = k1;
+    bp.rng_cycle = cyc;
+    SDM_CHECK_CUDA(launch_stream(STREAM_BONUS_RACE, bp, R, s));
+    SDM_CHECK_CUDA(launch_verify_sample_finalize(draft, accept, res_keys, R, gamma, V, out_tok, n_out, dev_status, s));
+    return SDM_OK;
+}
+
+sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok, const int32_t* parent,
+                           const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept, int32_t* out_tok,
+                           int32_t* n_out, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!target || !tok || !parent || !n_nodes || !accept || !out_tok || !n_out) return SDM_ERR_INVALID_ARG;
+    if (R <= 0 || N < 0 || B <= 0 || V <= 0) return SDM_ERR_INVALID_ARG;
+    if (dtT != SDM_BF16 && dtT != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !aligned16(target)) return SDM_ERR_UNSUPPORTED;
+    const size_t rows = static_cast<size_t>(R) * (N + 1);
+    if (!ws || ws_bytes < align256(rows * 8)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto* row_keys = static_cast<unsigned long long*>(ws);
+    StreamParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.base = target;
+    sp.fp32 = dtT == SDM_FP32;
+    sp.V = V;
+    sp.chunk = sp.fp32 ? kChunkFp32 : kChunkBf16;
+    sp.n_chunks = n_chunks_of(V, sp.fp32);
+    sp.n_items = static_cast<int>(rows);
+    sp.keys = row_keys;
+    sp.inv_t = 1.0f;
+    SDM_CHECK_CUDA(launch_fill_u64(row_keys, rows, 0ull, s));
+    SDM_CHECK_CUDA(launch_stream(STREAM_ARGMAX, sp, static_cast<int>(rows), s));
+    SDM_CHECK_CUDA(launch_tree_verify_walk(row_keys, tok, parent, n_nodes, R, N, B, V, accept, out_tok, n_out,
+                                           dev_status, s));
+    return SDM_OK;
+}
+
+}  // extern "C"

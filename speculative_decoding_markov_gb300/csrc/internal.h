@@ -1,0 +1,143 @@
+// internal.h - launch parameters and launcher declarations shared by the
+// kernel translation units and the C-ABI layer (api.cu).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/sdm.h"
+
+namespace sdm {
+
+// ---------------------------------------------------------------------------
+// Markov GEMM (tcgen05): one CTA = one 128-row M tile x a contiguous range of
+// 64-wide vocab tiles; K = r (<= 256, multiple of 64).
+// ---------------------------------------------------------------------------
+constexpr int kTileM = 128;        // GEMM rows per CTA (TMEM lanes)
+constexpr int kTileN = 64;         // vocab ids per tile (one 128-byte bf16 swizzle span)
+constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kMaxTopK = 8;
+
+enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3 };
+
+struct GemmParams {
+    int rows;            // GEMM rows in use
+    int R, B, V, r;
+    int n_tiles;         // ceil(V / 64)
+    int stages;          // smem pipeline depth
+    int l_fp32;          // L element type: 0 bf16, 1 fp32
+    int l_rows;          // L rows per M tile in the TMA box (chain: min(R,128); tree: 128/P)
+    int P;               // tree: GEMM rows per request (frontier slots)
+    int k;               // tree: local top-k
+    int d;               // 1-based draft position / tree level
+    float inv_t;         // 1 / temperature
+    uint32_t rng_k0, rng_k1, rng_cycle;
+    const uint16_t* U;   // [V, r]
+    const int32_t* anchor;
+    // chain
+    unsigned long long* keys;   // [B][R] argmax / race keys
+    float2* lse_part;           // [B][R][gridDim.x]
+    // tree
+    const int32_t* front_tok;   // [R][P] frontier tokens (-1: empty slot)
+    float* tree_part;           // [rows][gridDim.x][2 + 2 * kMaxTopK]
+    // residual (sample verify): one GEMM row per request
+    const int32_t* res_tok;     // [R] previous token of the rejected position, -1: none
+    const int32_t* res_pos;     // [R] rejected window position j (L row j, stream row j)
+    const int32_t* res_trow;    // [R] packed target row of position j
+    const float* res_lse_p;     // [R] log-sum-exp of target row j / T
+    const float* lse_q;         // [R, gamma] draft log-sum-exp
+    const void* L;              // [R, gamma, V] (residual reads rows directly)
+    const void* target;         // packed target rows
+    int t_fp32;                 // target element type
+    int gamma;
+    unsigned long long* res_keys;   // [R]
+    int32_t* dev_status;
+};
+
+size_t gemm_smem_bytes(int r, int l_rows, int l_fp32, int stages, int mode);
+int gemm_pick_stages(int r, int l_rows, int l_fp32, int mode);
+cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p,
+                               int grid_x, int grid_y, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Vocab-row streaming kernels (argmax / log-sum-exp / race over target rows)
+// ---------------------------------------------------------------------------
+enum StreamOp { STREAM_ARGMAX = 0, STREAM_LSE = 1, STREAM_BONUS_RACE = 2 };
+
+struct StreamParams {
+    const void* base;       // row r starts at base + r * V elements
+    int fp32;               // element type
+    int V;
+    int chunk;              // elements per work item (multiple of 8)
+    int n_chunks;           // chunks per row
+    int n_items;            // rows (items) when count == NULL
+    const int32_t* count;   // device item count (e.g. cu_seqlens + R), may be NULL
+    const int32_t* row_of;  // item -> row index (NULL: identity; < 0: skip)
+    float inv_t;
+    unsigned long long* keys;   // ARGMAX / BONUS: [n_items]
+    float2* part;               // LSE: [n_items][n_chunks]
+    // bonus race
+    uint32_t rng_k0, rng_k1, rng_cycle;
+    const int32_t* race_row;    // item -> Philox row (window position)
+};
+
+cudaError_t launch_stream(int op, const StreamParams& p, int max_items, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// small kernels
+// ---------------------------------------------------------------------------
+cudaError_t launch_fill_u64(unsigned long long* p, size_t n, unsigned long long v, cudaStream_t s);
+
+cudaError_t launch_chain_finalize(const unsigned long long* keys, const float2* lse_part, int gx, int R, int B, int V,
+                                  int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
+                                  const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
+                                  float* lse, int32_t* dev_status, cudaStream_t s);
+
+cudaError_t launch_schedule(const float* conf, int R, int gamma, const double* cost, float* survival,
+                            int32_t* budget, double* expected, int32_t* total_tokens, unsigned long long* ws_keys,
+                            int32_t* dev_status, cudaStream_t s);
+
+cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
+                        const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
+                        int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s);
+
+cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
+                                          const unsigned long long* row_keys, int R, int gamma, int V,
+                                          int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+                                          int32_t* dev_status, cudaStream_t s);
+
+// Sample verify, step 2: per request, merge row LSE partials, run the
+// left-to-right accept tests and choose the final row (residual or bonus).
+cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t* anchor, const int32_t* draft,
+                                      const int32_t* budget, const float* logq, const void* target, int t_fp32,
+                                      int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
+                                      uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
+                                      int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
+                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
+                                      unsigned long long* res_keys, int32_t* dev_status, cudaStream_t s);
+
+cudaError_t launch_verify_sample_finalize(const int32_t* draft, const int32_t* accept,
+                                          const unsigned long long* res_keys, int R, int gamma, int V,
+                                          int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s);
+
+// PCTree
+cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
+                             float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
+                             int32_t* pool_depth, float* pool_score, int32_t* pool_n, int32_t* dev_status,
+                             cudaStream_t s);
+cudaError_t launch_tree_merge(const float* tree_part, int gx, int R, int P, int k, int B, int d, int32_t* front_tok,
+                              int32_t* front_node, float* front_score, int32_t* n_front, int32_t* pool_tok,
+                              int32_t* pool_parent, int32_t* pool_depth, float* pool_score, int32_t* pool_n,
+                              cudaStream_t s);
+cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool_tok, const int32_t* pool_parent,
+                                 const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
+                                 int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
+                                 int32_t* n_nodes, cudaStream_t s);
+cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, const int32_t* tok, const int32_t* parent,
+                                    const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
+                                    int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace sdm

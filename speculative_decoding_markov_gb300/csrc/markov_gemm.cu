@@ -1,0 +1,559 @@
+// markov_gemm.cu - the Markov-head projection on the 5th-generation tensor
+// cores, with the vocab-wide reductions fused into the epilogue.
+//
+// One launch computes, for a set of GEMM rows m (requests, or PCTree
+// (request, frontier slot) pairs), the logits
+//     z[m, v] = L[row(m), v] + (U[tok(m)] . W)[v]          v in [0, V)
+// and reduces them over the vocabulary without writing z anywhere:
+//   MODE_CHAIN_GREEDY  argmax_v z                       (DSpark notes sec. 4)
+//   MODE_CHAIN_SAMPLE  exponential race on z / T + log-sum-exp partials
+//   MODE_TREE          log-sum-exp partials + local top-k by z  (PCTree)
+//   MODE_RESID         race over max(0, p - q) at a rejected position
+//
+// Data path (one CTA = 128 GEMM rows x a contiguous range of 64-wide vocab
+// tiles, K = r):
+//   * all threads gather the 128 rows U[tok(m)] (bf16, K-major) into shared
+//     memory once, in the 128-byte swizzled layout tcgen05 reads;
+//   * warp 0 streams W tiles [r x 64] (MN-major, TMA 2-D, 128-byte swizzle,
+//     L2 evict_last: W is re-read by every draft step) and the matching L tile
+//     [rows x 64] (TMA 3-D, evict_first) through an S-stage mbarrier ring;
+//   * warp 1 issues r/16 tcgen05.mma (M=128, N=64, K=16, bf16 -> fp32) per
+//     tile into one of two 64-column TMEM accumulators;
+//   * warps 2-5 drain the accumulator with tcgen05.ld (thread = GEMM row),
+//     add L and run the mode's reduction in registers; one result per row
+//     and CTA is written at the end.
+// The grid is (vocab splits) x (M tiles), one CTA per SM.
+#include "device.cuh"
+#include "internal.h"
+
+namespace sdm {
+namespace {
+
+constexpr int kEpiWarps = 4;
+constexpr int kSmemLimit = 232448;   // 227 KB opt-in per block
+
+struct SmemLayout {
+    uint32_t a_bytes, w_bytes, l_box_bytes, l_bytes, stage_bytes, bar_off, total;
+};
+
+__host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32, int stages, int mode) {
+    SmemLayout s;
+    s.a_bytes = static_cast<uint32_t>(kTileM) * static_cast<uint32_t>(r) * 2u;
+    s.w_bytes = static_cast<uint32_t>(r) * 128u;
+    s.l_box_bytes = (static_cast<uint32_t>(l_rows) * 128u + 1023u) & ~1023u;
+    s.l_bytes = (mode == MODE_RESID) ? 0u : s.l_box_bytes * (l_fp32 ? 2u : 1u);
+    s.stage_bytes = s.w_bytes + s.l_bytes;
+    s.bar_off = s.a_bytes + static_cast<uint32_t>(stages) * s.stage_bytes;
+    s.total = s.bar_off + static_cast<uint32_t>(2 * stages + 4) * 8u + 16u + 1024u;
+    return s;
+}
+
+__device__ __forceinline__ void fail_timeout(const GemmParams& p) { set_status(p.dev_status, SDM_DEV_TIMEOUT); }
+
+// Token whose U row feeds GEMM row `grow`; -1 for an unused row.
+template <int MODE>
+__device__ __forceinline__ int gemm_row_token(const GemmParams& p, int grow) {
+    int t = -1;
+    if (MODE == MODE_CHAIN_GREEDY || MODE == MODE_CHAIN_SAMPLE) {
+        if (grow >= p.R) return -1;
+        t = (p.d == 1) ? p.anchor[grow] : static_cast<int>(key_token(p.keys[static_cast<size_t>(p.d - 2) * p.R + grow]));
+    } else if (MODE == MODE_TREE) {
+        if (grow >= p.rows) return -1;
+        t = p.front_tok[grow];
+        if (t < 0) return -1;
+    } else {
+        if (grow >= p.R) return -1;
+        t = p.res_tok[grow];
+        if (t < 0) return -1;
+    }
+    if (t < 0 || t >= p.V) {
+        set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+        return -1;
+    }
+    return t;
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+// The 32 L values of columns [32h, 32h + 32) of the staged tile, box row lr.
+__device__ __forceinline__ void load_l32(const uint8_t* sl, uint32_t l_box_bytes, int l_fp32, int lr, int h,
+                                         float (&out)[32]) {
+    if (!l_fp32) {
+        const uint8_t* rowp = sl + lr * 128;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int chunk = h * 4 + c;
+            const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((chunk ^ (lr & 7)) << 4));
+            out[c * 8 + 0] = bf_lo(v.x);
+            out[c * 8 + 1] = bf_hi(v.x);
+            out[c * 8 + 2] = bf_lo(v.y);
+            out[c * 8 + 3] = bf_hi(v.y);
+            out[c * 8 + 4] = bf_lo(v.z);
+            out[c * 8 + 5] = bf_hi(v.z);
+            out[c * 8 + 6] = bf_lo(v.w);
+            out[c * 8 + 7] = bf_hi(v.w);
+        }
+    } else {
+        const uint8_t* rowp = sl + h * l_box_bytes + lr * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const float4 v = *reinterpret_cast<const float4*>(rowp + ((c ^ (lr & 7)) << 4));
+            out[c * 4 + 0] = v.x;
+            out[c * 4 + 1] = v.y;
+            out[c * 4 + 2] = v.z;
+            out[c * 4 + 3] = v.w;
+        }
+    }
+}
+
+// 32 consecutive elements of a global row (bf16 or fp32) starting at v0;
+// entries at or past V read as 0 (callers mask them).
+__device__ __forceinline__ void load_g32(const void* base, int fp32, size_t off, int v0, int V, float (&out)[32]) {
+    if (!fp32) {
+        const uint16_t* p = static_cast<const uint16_t*>(base) + off;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (v0 + c * 8 < V) v = __ldg(reinterpret_cast<const uint4*>(p + v0 + c * 8));
+            out[c * 8 + 0] = bf_lo(v.x);
+            out[c * 8 + 1] = bf_hi(v.x);
+            out[c * 8 + 2] = bf_lo(v.y);
+            out[c * 8 + 3] = bf_hi(v.y);
+            out[c * 8 + 4] = bf_lo(v.z);
+            out[c * 8 + 5] = bf_hi(v.z);
+            out[c * 8 + 6] = bf_lo(v.w);
+            out[c * 8 + 7] = bf_hi(v.w);
+        }
+    } else {
+        const float* p = static_cast<const float*>(base) + off;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (v0 + c * 4 < V) v = __ldg(reinterpret_cast<const float4*>(p + v0 + c * 4));
+            out[c * 4 + 0] = v.x;
+            out[c * 4 + 1] = v.y;
+            out[c * 4 + 2] = v.z;
+            out[c * 4 + 3] = v.w;
+        }
+    }
+}
+
+// Per-row epilogue state of each mode.
+template <int MODE>
+struct Epi;
+
+template <>
+struct Epi<MODE_CHAIN_GREEDY> {
+    bool valid;
+    float best;
+    uint32_t best_v;
+    __device__ void init(const GemmParams& p, int grow) {
+        valid = grow < p.R;
+        best = -INFINITY;
+        best_v = 0;
+    }
+    __device__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
+                            const uint32_t (&acc)[32]) {
+        if (!valid) return;
+        float lv[32];
+        load_l32(sl, lbb, p.l_fp32, lrow, h, lv);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float z = lv[j] + __uint_as_float(acc[j]);     // fp32(L) + Markov, one rounding
+            if (z > best && vbase + j < p.V) {                   // strict: the lowest id keeps ties
+                best = z;
+                best_v = static_cast<uint32_t>(vbase + j);
+            }
+        }
+    }
+    __device__ void flush(const GemmParams& p, int grow) {
+        if (valid) atomicMax(&p.keys[static_cast<size_t>(p.d - 1) * p.R + grow], argmax_key(best, best_v));
+    }
+};
+
+template <>
+struct Epi<MODE_CHAIN_SAMPLE> {
+    bool valid;
+    float best;
+    uint32_t best_v;
+    float m, s;
+    RngKey key;
+    __device__ void init(const GemmParams& p, int grow) {
+        valid = grow < p.R;
+        best = -INFINITY;
+        best_v = 0;
+        m = -INFINITY;
+        s = 0.f;
+        key = RngKey{p.rng_k0, p.rng_k1, p.rng_cycle};
+    }
+    __device__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
+                            const uint32_t (&acc)[32]) {
+        if (!valid) return;
+        float lv[32];
+        load_l32(sl, lbb, p.l_fp32, lrow, h, lv);
+        const int grow = lrow + blockIdx.y * kTileM;
+        float zt[32];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            zt[j] = (lv[j] + __uint_as_float(acc[j])) * p.inv_t;
+            if (vbase + j < p.V) mx = fmaxf(mx, zt[j]);
+        }
+        if (mx > m) {
+            s *= __expf(m - mx);
+            m = mx;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int v4 = vbase + c * 4;
+            if (v4 >= p.V) break;
+            const U4 blk = philox_block(key, 0u, static_cast<uint32_t>(grow), static_cast<uint32_t>(p.d),
+                                        static_cast<uint32_t>(v4) >> 2);
+            const uint32_t w[4] = {blk.x, blk.y, blk.z, blk.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float z = zt[c * 4 + q];
+                s += __expf(z - m);
+                const float k = z - race_log_exp(word_to_uniform(w[q]));
+                if (k > best) {
+                    best = k;
+                    best_v = static_cast<uint32_t>(v4 + q);
+                }
+            }
+        }
+    }
+    __device__ void flush(const GemmParams& p, int grow) {
+        if (!valid) return;
+        const size_t o = static_cast<size_t>(p.d - 1) * p.R + grow;
+        atomicMax(&p.keys[o], argmax_key(best, best_v));
+        p.lse_part[o * gridDim.x + blockIdx.x] = make_float2(m, s);
+    }
+};
+
+template <>
+struct Epi<MODE_TREE> {
+    bool valid;
+    float m, s;
+    float tv[kMaxTopK];
+    uint32_t ti[kMaxTopK];
+    __device__ void init(const GemmParams& p, int grow) {
+        valid = grow < p.rows && p.front_tok[grow] >= 0;
+        m = -INFINITY;
+        s = 0.f;
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q) {
+            tv[q] = -INFINITY;
+            ti[q] = 0xffffffffu;
+        }
+    }
+    __device__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
+                            const uint32_t (&acc)[32]) {
+        if (!valid) return;
+        float lv[32];
+        load_l32(sl, lbb, p.l_fp32, lrow / p.P, h, lv);
+        float z[32];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            z[j] = lv[j] + __uint_as_float(acc[j]);
+            if (vbase + j < p.V) mx = fmaxf(mx, z[j]);
+        }
+        if (mx > m) {
+            s *= __expf(m - mx);
+            m = mx;
+        }
+        const int k = p.k;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (vbase + j >= p.V) break;
+            s += __expf(z[j] - m);
+            if (z[j] > tv[k - 1]) {
+                float cz = z[j];
+                uint32_t cv = static_cast<uint32_t>(vbase + j);
+#pragma unroll
+                for (int q = 0; q < kMaxTopK; ++q) {
+                    if (q < k && cz > tv[q]) {     // strict: earlier (lower id) ties stay ahead
+                        const float tz = tv[q];
+                        const uint32_t tiv = ti[q];
+                        tv[q] = cz;
+                        ti[q] = cv;
+                        cz = tz;
+                        cv = tiv;
+                    }
+                }
+            }
+        }
+    }
+    __device__ void flush(const GemmParams& p, int grow) {
+        if (!valid) return;
+        float* rec = p.tree_part + (static_cast<size_t>(grow) * gridDim.x + blockIdx.x) * (2 + 2 * kMaxTopK);
+        rec[0] = m;
+        rec[1] = s;
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q) {
+            rec[2 + q] = tv[q];
+            rec[2 + kMaxTopK + q] = __uint_as_float(ti[q]);
+        }
+    }
+};
+
+template <>
+struct Epi<MODE_RESID> {
+    bool valid;
+    float best;
+    uint32_t best_v;
+    int jpos;
+    size_t l_off, t_off;
+    float lse_q, lse_p;
+    RngKey key;
+    __device__ void init(const GemmParams& p, int grow) {
+        valid = grow < p.R && p.res_tok[grow] >= 0;
+        best = -INFINITY;
+        best_v = 0;
+        key = RngKey{p.rng_k0, p.rng_k1, p.rng_cycle};
+        if (valid) {
+            jpos = p.res_pos[grow];
+            l_off = (static_cast<size_t>(grow) * p.gamma + jpos) * static_cast<size_t>(p.V);
+            t_off = static_cast<size_t>(p.res_trow[grow]) * static_cast<size_t>(p.V);
+            lse_q = p.lse_q[static_cast<size_t>(grow) * p.gamma + jpos];
+            lse_p = p.res_lse_p[grow];
+        }
+    }
+    __device__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int lrow, int vbase, int,
+                            const uint32_t (&acc)[32]) {
+        if (!valid) return;
+        const int grow = lrow + blockIdx.y * kTileM;
+        float lv[32], tv[32];
+        load_g32(p.L, p.l_fp32, l_off, vbase, p.V, lv);
+        load_g32(p.target, p.t_fp32, t_off, vbase, p.V, tv);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int v4 = vbase + c * 4;
+            if (v4 >= p.V) break;
+            const U4 blk = philox_block(key, 2u, static_cast<uint32_t>(grow), static_cast<uint32_t>(jpos),
+                                        static_cast<uint32_t>(v4) >> 2);
+            const uint32_t w[4] = {blk.x, blk.y, blk.z, blk.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = c * 4 + q;
+                const float lq = (lv[j] + __uint_as_float(acc[j])) * p.inv_t - lse_q;   // log q_v
+                const float lp = tv[j] * p.inv_t - lse_p;                                 // log p_v
+                if (lp > lq) {
+                    // log(p - q) = log p + log(1 - q/p)
+                    const float k = lp + log1pf(-__expf(lq - lp)) - race_log_exp(word_to_uniform(w[q]));
+                    if (k > best) {
+                        best = k;
+                        best_v = static_cast<uint32_t>(v4 + q);
+                    }
+                }
+            }
+        }
+    }
+    __device__ void flush(const GemmParams& p, int grow) {
+        if (valid) atomicMax(&p.res_keys[grow], argmax_key(best, best_v));
+    }
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    markov_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmL,
+                       const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.stages, MODE);
+    uint8_t* sA = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
+    uint64_t* empty = full + p.stages;
+    uint64_t* tfull = empty + p.stages;
+    uint64_t* tempty = tfull + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row0 = blockIdx.y * kTileM;
+    const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
+    const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
+    const int nt = t_end - t_begin;
+
+    // 1. gather A = U[tok(m)] for the 128 rows (K-major, 128-byte swizzle:
+    //    16-byte chunk c of row m in K block kb sits at chunk c ^ (m & 7)).
+    const int kchunks = p.r >> 3;
+    for (int rr = warp; rr < kTileM; rr += kGemmThreads / 32) {
+        const int tok = gemm_row_token<MODE>(p, row0 + rr);
+        const uint16_t* src = p.U + static_cast<size_t>(tok < 0 ? 0 : tok) * p.r;
+        for (int q = lane; q < kchunks; q += 32) {
+            uint8_t* dst = sA + (q >> 3) * (kTileM * 128) + rr * 128 + (((q & 7) ^ (rr & 7)) << 4);
+            cp_async_16(dst, src + q * 8, tok < 0 ? 0u : 16u);
+        }
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1 + kEpiWarps);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], kEpiWarps);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        if (MODE != MODE_RESID) tma_prefetch_desc(&tmL);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 2 * kTileN);
+        tmem_relinquish();
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // 2. producer: W tile + L tile per vocab tile
+        if (lane == 0 && nt > 0) {
+            const uint64_t pol_w = policy_evict_last();
+            const uint64_t pol_l = policy_evict_first();
+            const uint32_t tx =
+                lay.w_bytes + (MODE == MODE_RESID ? 0u : static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u));
+            const int lrow0 = (MODE == MODE_TREE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
+            for (int i = 0; i < nt; ++i) {
+                const int s = i % p.stages;
+                if (i >= p.stages && !mbar_wait(&empty[s], ((i / p.stages) - 1) & 1)) {
+                    fail_timeout(p);
+                    break;
+                }
+                uint8_t* st = smem + lay.a_bytes + s * lay.stage_bytes;
+                mbar_arrive_expect_tx(&full[s], tx);
+                const int v0 = (t_begin + i) * kTileN;
+                tma_load_2d(st, &tmW, &full[s], v0, 0, pol_w);
+                if (MODE != MODE_RESID) {
+                    uint8_t* sl = st + lay.w_bytes;
+                    tma_load_3d(sl, &tmL, &full[s], v0, p.d - 1, lrow0, pol_l);
+                    if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &full[s], v0 + 32, p.d - 1, lrow0, pol_l);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // 3. MMA issuer: D[128 x 64] = A[128 x r] * W_tile[r x 64]
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
+            const uint32_t a_addr = smem_u32(sA);
+            const int ksteps = p.r >> 4;
+            for (int i = 0; i < nt; ++i) {
+                const int s = i % p.stages;
+                const int b = i & 1;
+                if (!mbar_wait(&full[s], (i / p.stages) & 1)) {
+                    fail_timeout(p);
+                    break;
+                }
+                if (i >= 2 && !mbar_wait(&tempty[b], ((i >> 1) - 1) & 1)) {
+                    fail_timeout(p);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t w_addr = smem_u32(smem + lay.a_bytes + s * lay.stage_bytes);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    const uint64_t ad =
+                        smem_desc_sw128(a_addr + (ks >> 2) * (kTileM * 128) + (ks & 3) * 32, 16, 1024);
+                    // N = 64 is one swizzle span, so the MN-atom offset is never
+                    // applied; it is set equal to the K-group stride (1024 B).
+                    const uint64_t bd = smem_desc_sw128(w_addr + ks * 2048, 1024, 1024);
+                    mma_bf16(d_tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&empty[s]);
+                mma_commit(&tfull[b]);
+            }
+        }
+        __syncwarp();
+    } else {
+        // 4. epilogue: thread = GEMM row (TMEM lane), 64 columns per tile
+        const int q = warp & 3;
+        const int lrow = q * 32 + lane;
+        const int grow = row0 + lrow;
+        Epi<MODE> st;
+        st.init(p, grow);
+        const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        for (int i = 0; i < nt; ++i) {
+            const int s = i % p.stages;
+            const int b = i & 1;
+            bool ok = mbar_wait(&tfull[b], (i >> 1) & 1);
+            if (ok) ok = mbar_wait(&full[s], (i / p.stages) & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) fail_timeout(p);
+                break;
+            }
+            tc_fence_after();
+            const uint8_t* sl = smem + lay.a_bytes + s * lay.stage_bytes + lay.w_bytes;
+            const int v0 = (t_begin + i) * kTileN;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint32_t acc[32];
+                tmem_ld32(lane_addr + static_cast<uint32_t>(b * kTileN + h * 32), acc);
+                tmem_ld_wait();
+                st.consume(p, sl, lay.l_box_bytes, lrow, v0 + h * 32, h, acc);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&tempty[b]);
+                mbar_arrive(&empty[s]);
+            }
+        }
+        st.flush(p, grow);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 2 * kTileN);
+    }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p, int gx, int gy,
+                        cudaStream_t s) {
+    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.stages, MODE);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemLimit);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    markov_gemm_kernel<MODE><<<dim3(gx, gy), kGemmThreads, lay.total, s>>>(tmW, tmL, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes(int r, int l_rows, int l_fp32, int stages, int mode) {
+    return make_layout(r, l_rows, l_fp32, stages, mode).total;
+}
+
+int gemm_pick_stages(int r, int l_rows, int l_fp32, int mode) {
+    int st = 4;
+    while (st > 1 && make_layout(r, l_rows, l_fp32, st, mode).total > static_cast<uint32_t>(kSmemLimit)) --st;
+    return st;
+}
+
+cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p,
+                               int grid_x, int grid_y, cudaStream_t s) {
+    switch (mode) {
+        case MODE_CHAIN_GREEDY: return launch_mode<MODE_CHAIN_GREEDY>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_CHAIN_SAMPLE: return launch_mode<MODE_CHAIN_SAMPLE>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TREE: return launch_mode<MODE_TREE>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_RESID: return launch_mode<MODE_RESID>(tmW, tmL, p, grid_x, grid_y, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sdm

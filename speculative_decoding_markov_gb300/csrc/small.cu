@@ -1,0 +1,762 @@
+// small.cu - the latency-bound kernels of the cycle: chain finalisation,
+// the prefix scheduler, the ragged pack, the per-request verification scans,
+// and PCTree's per-level merge/prune and final top-N selection.
+#include "device.cuh"
+#include "internal.h"
+
+namespace sdm {
+namespace {
+
+__device__ __forceinline__ float load_elem(const void* base, int fp32, size_t idx) {
+    if (fp32) return static_cast<const float*>(base)[idx];
+    return bf16_bits_to_float(static_cast<const uint16_t*>(base)[idx]);
+}
+
+// ---------------------------------------------------------------------------
+__global__ void fill_u64_kernel(unsigned long long* p, size_t n, unsigned long long v) {
+    for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<size_t>(gridDim.x) * blockDim.x)
+        p[i] = v;
+}
+
+// ---------------------------------------------------------------------------
+// chain finalize: tokens from the argmax keys; for sampling, merge the
+// log-sum-exp partials in a fixed order and form log q(y_d).
+// ---------------------------------------------------------------------------
+__global__ void chain_finalize_kernel(const unsigned long long* keys, const float2* lse_part, int gx, int R, int B,
+                                      int V, int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
+                                      const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
+                                      float* lse, int32_t* dev_status) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= R * B) return;
+    const int i = idx / B, d = idx % B + 1;
+    const size_t o = static_cast<size_t>(d - 1) * R + i;
+    int y = static_cast<int>(key_token(keys[o]));
+    if (y < 0 || y >= V) {
+        set_status(dev_status, SDM_DEV_BAD_TOKEN);
+        y = 0;
+    }
+    tokens[static_cast<size_t>(i) * B + d - 1] = y;
+    if (!sample) return;
+    Lse acc{-INFINITY, 0.f};
+    for (int c = 0; c < gx; ++c) {
+        const float2 pc = lse_part[o * gx + c];
+        acc = lse_merge(acc, Lse{pc.x, pc.y});
+    }
+    const float l = acc.m + logf(acc.s);
+    int prev = (d == 1) ? anchor[i] : static_cast<int>(key_token(keys[o - R]));
+    if (prev < 0 || prev >= V) prev = 0;
+    // z_d[y] = L + U[prev] . W[:, y]; exact in fp32 on the 2^-8 grid tables
+    float m = 0.f;
+    for (int j = 0; j < r; ++j)
+        m += bf16_bits_to_float(U[static_cast<size_t>(prev) * r + j]) * bf16_bits_to_float(W[static_cast<size_t>(j) * V + y]);
+    const float z = load_elem(L, l_fp32, (static_cast<size_t>(i) * B + (d - 1)) * V + y) + m;
+    if (lse) lse[static_cast<size_t>(i) * B + d - 1] = l;
+    if (logq) logq[static_cast<size_t>(i) * B + d - 1] = z * inv_t - l;
+}
+
+// ---------------------------------------------------------------------------
+// scheduler: one CTA
+// ---------------------------------------------------------------------------
+constexpr int kSchedThreads = 1024;
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* conf, int R, int gamma,
+                                                                 const double* cost, float* survival,
+                                                                 int32_t* budget, double* expected,
+                                                                 int32_t* total_tokens, int n_pad) {
+    extern __shared__ unsigned long long sk[];              // n_pad sort keys
+    unsigned long long* part = sk + n_pad;                   // kSchedThreads partial sums
+    int* cnt = reinterpret_cast<int*>(part + kSchedThreads);  // R counters
+    __shared__ int m_star;
+    __shared__ int n_cand;
+    const int tid = threadIdx.x;
+    const int n = R * gamma;
+    const float floor_s = 1.0f / 262144.0f;                 // 2^-18
+
+    // survival S_{i,k} = S_{i,k-1} c_{i,k}, fp32, left to right
+    for (int i = tid; i < R; i += kSchedThreads) {
+        float s = 1.0f;
+        for (int k = 0; k < gamma; ++k) {
+            s = __fmul_rn(s, conf[static_cast<size_t>(i) * gamma + k]);
+            survival[static_cast<size_t>(i) * gamma + k] = s;
+            const uint32_t id = static_cast<uint32_t>(i * gamma + k);
+            sk[i * gamma + k] = (s >= floor_s) ? ((static_cast<unsigned long long>(__float_as_uint(s)) << 32) | ~id) : 0ull;
+        }
+        cnt[i] = 0;
+    }
+    for (int t = n + tid; t < n_pad; t += kSchedThreads) sk[t] = 0ull;
+    if (tid == 0) {
+        m_star = 0x7fffffff;
+        n_cand = 0;
+    }
+    __syncthreads();
+    // bitonic sort, descending (S desc, then request asc, position asc)
+    for (int size = 2; size <= n_pad; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < n_pad; t += kSchedThreads) {
+                const int u = t ^ stride;
+                if (u > t) {
+                    const bool desc = (t & size) == 0;
+                    const unsigned long long a = sk[t], b = sk[u];
+                    if (desc ? (a < b) : (a > b)) {
+                        sk[t] = b;
+                        sk[u] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // number of ranked survivals
+    for (int t = tid; t < n_pad; t += kSchedThreads)
+        if (sk[t] != 0ull && (t + 1 == n_pad || sk[t + 1] == 0ull)) n_cand = t + 1;
+    __syncthreads();
+    const int M = n_cand;
+    // exact prefix sums: a survival >= 2^-18 is an integer multiple of 2^-41
+    const int per = (n_pad + kSchedThreads - 1) / kSchedThreads;
+    unsigned long long local = 0;
+    for (int q = 0; q < per; ++q) {
+        const int t = tid * per + q;
+        if (t < M) local += static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[t] >> 32)), 41));
+    }
+    part[tid] = local;
+    __syncthreads();
+    if (tid == 0) {   // exclusive scan over the thread partials (1024 adds)
+        unsigned long long run = 0;
+        for (int q = 0; q < kSchedThreads; ++q) {
+            const unsigned long long v = part[q];
+            part[q] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    // f(m) = E(m) / cost[R + m]; the greedy stops at the first m whose next
+    // survival does not raise f strictly.
+    {
+        unsigned long long run = part[tid];
+        const double two_m41 = 4.547473508864641e-13;   // 2^-41
+        const unsigned long long base = static_cast<unsigned long long>(R) << 41;
+        for (int q = 0; q < per; ++q) {
+            const int m = tid * per + q;              // E(m) uses the first m survivals
+            if (m >= M) break;
+            const unsigned long long s_int =
+                static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[m] >> 32)), 41));
+            const double e0 = static_cast<double>(base + run) * two_m41;
+            const double e1 = static_cast<double>(base + run + s_int) * two_m41;
+            const double f0 = __ddiv_rn(e0, cost[R + m]);
+            const double f1 = __ddiv_rn(e1, cost[R + m + 1]);
+            if (!(f1 > f0)) atomicMin(&m_star, m);
+            run += s_int;
+        }
+    }
+    __syncthreads();
+    const int ms = (m_star == 0x7fffffff) ? M : m_star;
+    for (int t = tid; t < ms; t += kSchedThreads) {
+        const uint32_t id = ~static_cast<uint32_t>(sk[t] & 0xffffffffull);
+        atomicAdd(&cnt[id / gamma], 1);
+    }
+    __syncthreads();
+    for (int i = tid; i < R; i += kSchedThreads) budget[i] = cnt[i];
+    if (tid == 0) {
+        unsigned long long sum = 0;
+        for (int t = 0; t < ms; ++t)
+            sum += static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[t] >> 32)), 41));
+        *expected = static_cast<double>((static_cast<unsigned long long>(R) << 41) + sum) * 4.547473508864641e-13;
+        *total_tokens = R + ms;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// ragged pack: one CTA
+// ---------------------------------------------------------------------------
+constexpr int kPackThreads = 1024;
+
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* anchor, const int32_t* draft,
+                                                            const int32_t* budget, int R, int gamma,
+                                                            const int32_t* tiers, int n_tiers, int32_t* cu,
+                                                            int32_t* ptok, int32_t* preq, int32_t* ppos,
+                                                            int capacity, int32_t* tier, int32_t* dev_status) {
+    __shared__ int warp_sum[32];
+    __shared__ int s_total, s_tier;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int carry = 0;
+    // exclusive scan of (n_i + 1), 1024 requests per pass
+    for (int base = 0; base < R; base += kPackThreads) {
+        const int i = base + tid;
+        int n = 0;
+        if (i < R) {
+            n = budget ? budget[i] : gamma;
+            if (n < 0 || n > gamma) {
+                set_status(dev_status, SDM_DEV_BAD_WINDOW);
+                n = n < 0 ? 0 : gamma;
+            }
+        }
+        const int len = (i < R) ? n + 1 : 0;
+        int x = len;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sum[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int w = warp_sum[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sum[lane] = w;
+        }
+        __syncthreads();
+        const int incl = x + (warp > 0 ? warp_sum[warp - 1] : 0) + carry;
+        const int start = incl - len;
+        if (i < R) {
+            cu[i] = start;
+            for (int p = 0; p <= n; ++p) {
+                const int row = start + p;
+                if (row >= capacity) {
+                    set_status(dev_status, SDM_DEV_CAPACITY);
+                    break;
+                }
+                ptok[row] = (p == 0) ? anchor[i] : draft[static_cast<size_t>(i) * gamma + p - 1];
+                preq[row] = i;
+                ppos[row] = p;
+            }
+        }
+        const int chunk_total = warp_sum[31];
+        __syncthreads();
+        carry += chunk_total;
+    }
+    if (tid == 0) {
+        cu[R] = carry;
+        int t = -1;
+        for (int q = 0; q < n_tiers; ++q)
+            if (tiers[q] >= carry && (t < 0 || tiers[q] < t)) t = tiers[q];
+        if (t < 0) {
+            t = carry;
+            set_status(dev_status, SDM_DEV_TIER_UNCAPTURED);
+        }
+        s_total = carry;
+        s_tier = t;
+        *tier = t;
+    }
+    __syncthreads();
+    const int end = s_tier < capacity ? s_tier : capacity;
+    for (int row = s_total + tid; row < end; row += kPackThreads) {
+        ptok[row] = -1;
+        preq[row] = -1;
+        ppos[row] = -1;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// greedy verification: first mismatch per request
+// ---------------------------------------------------------------------------
+__global__ void verify_greedy_finalize_kernel(int mode, const int32_t* cu, const int32_t* draft,
+                                              const int32_t* budget, const unsigned long long* row_keys, int R,
+                                              int gamma, int V, int32_t* accept, int32_t* ceiling,
+                                              int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R) return;
+    const int row0 = cu[i];
+    int w = cu[i + 1] - row0 - 1;
+    if (w < 0 || w > gamma) {
+        set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        w = w < 0 ? 0 : gamma;
+    }
+    int cap = w;
+    if (mode == SDM_CAP_ACCEPT) {
+        cap = budget[i];
+        if (cap < 0 || cap > w) {
+            set_status(dev_status, SDM_DEV_BAD_WINDOW);
+            cap = cap < 0 ? 0 : w;
+        }
+    }
+    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    int A = w;
+    for (int p = 0; p < w; ++p) {
+        if (y[p] != static_cast<int>(key_token(row_keys[row0 + p]))) {
+            A = p;
+            break;
+        }
+    }
+    const int a = A < cap ? A : cap;
+    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
+    for (int p = 0; p < a; ++p) o[p] = y[p];
+    int t = static_cast<int>(key_token(row_keys[row0 + a]));
+    if (t < 0 || t >= V) {
+        set_status(dev_status, SDM_DEV_BAD_TOKEN);
+        t = 0;
+    }
+    o[a] = t;
+    for (int p = a + 1; p <= gamma; ++p) o[p] = -1;
+    accept[i] = a;
+    n_out[i] = a + 1;
+    if (ceiling) ceiling[i] = A;
+}
+
+// ---------------------------------------------------------------------------
+// rejection sampling: accept scan per request
+// ---------------------------------------------------------------------------
+__global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int32_t* anchor, const int32_t* draft,
+                                          const int32_t* budget, const float* logq, const void* target, int t_fp32,
+                                          int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
+                                          uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
+                                          int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
+                                          float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
+                                          unsigned long long* res_keys, int32_t* dev_status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R) return;
+    const RngKey rk{k0, k1, cycle};
+    const int row0 = cu[i];
+    int w = cu[i + 1] - row0 - 1;
+    if (w < 0 || w > gamma) {
+        set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        w = w < 0 ? 0 : gamma;
+    }
+    int cap = w;
+    if (mode == SDM_CAP_ACCEPT) {
+        cap = budget[i];
+        if (cap < 0 || cap > w) {
+            set_status(dev_status, SDM_DEV_BAD_WINDOW);
+            cap = cap < 0 ? 0 : w;
+        }
+    }
+    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    auto row_lse = [&](int p) {
+        Lse acc{-INFINITY, 0.f};
+        const float2* pp = lse_part + static_cast<size_t>(row0 + p) * n_chunks;
+        for (int c = 0; c < n_chunks; ++c) acc = lse_merge(acc, Lse{pp[c].x, pp[c].y});
+        return acc.m + logf(acc.s);
+    };
+    int A = w;
+    for (int p = 0; p < w; ++p) {
+        int yp = y[p];
+        if (yp < 0 || yp >= V) {
+            set_status(dev_status, SDM_DEV_BAD_TOKEN);
+            yp = 0;
+        }
+        const float lp = load_elem(target, t_fp32, static_cast<size_t>(row0 + p) * V + yp) * inv_t - row_lse(p);
+        const float lq = logq[static_cast<size_t>(i) * gamma + p];
+        const float u = uniform_at(rk, 1u, static_cast<uint32_t>(i), static_cast<uint32_t>(p), 0u);
+        if (!(logf(u) < lp - lq)) {   // accept iff u < p(y) / q(y)
+            A = p;
+            break;
+        }
+    }
+    const int a = A < cap ? A : cap;
+    accept[i] = a;
+    if (ceiling) ceiling[i] = A;
+    res_keys[i] = 0ull;
+    if (A < cap) {   // rejected at row a: residual from max(0, p - q)
+        res_tok[i] = (a == 0) ? anchor[i] : y[a - 1];
+        res_pos[i] = a;
+        res_trow[i] = row0 + a;
+        res_lse_p[i] = row_lse(a);
+        bonus_row[i] = -1;
+        bonus_pos[i] = 0;
+    } else {         // every committed draft passed: bonus from p at row a
+        res_tok[i] = -1;
+        res_pos[i] = 0;
+        res_trow[i] = 0;
+        res_lse_p[i] = 0.f;
+        bonus_row[i] = row0 + a;
+        bonus_pos[i] = a;
+    }
+}
+
+__global__ void verify_sample_finalize_kernel(const int32_t* draft, const int32_t* accept,
+                                              const unsigned long long* res_keys, int R, int gamma, int V,
+                                              int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R) return;
+    const int a = accept[i];
+    int t = static_cast<int>(key_token(res_keys[i]));
+    if (t < 0 || t >= V) {
+        set_status(dev_status, SDM_DEV_BAD_TOKEN);
+        t = 0;
+    }
+    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
+    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    for (int p = 0; p < a; ++p) o[p] = y[p];
+    o[a] = t;
+    for (int p = a + 1; p <= gamma; ++p) o[p] = -1;
+    n_out[i] = a + 1;
+}
+
+// ---------------------------------------------------------------------------
+// PCTree
+// ---------------------------------------------------------------------------
+__global__ void tree_init_kernel(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
+                                 float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
+                                 int32_t* pool_depth, float* pool_score, int32_t* pool_n, int32_t* dev_status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R) return;
+    const int pool_cap = 1 + P * B;
+    const size_t pb = static_cast<size_t>(i) * pool_cap;
+    pool_tok[pb] = anchor[i];
+    pool_parent[pb] = -1;
+    pool_depth[pb] = 0;
+    pool_score[pb] = 0.f;
+    pool_n[i] = 1;
+    for (int s = 0; s < P; ++s) {
+        front_tok[static_cast<size_t>(i) * P + s] = (s == 0) ? anchor[i] : -1;
+        front_node[static_cast<size_t>(i) * P + s] = (s == 0) ? 0 : -1;
+        front_score[static_cast<size_t>(i) * P + s] = 0.f;
+    }
+    n_front[i] = 1;
+}
+
+struct Cand {
+    float s;
+    int slot, rank, tok;
+};
+
+__device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
+    if (a.s != b.s) return a.s > b.s;
+    if (a.slot != b.slot) return a.slot < b.slot;
+    return a.rank < b.rank;
+}
+
+// One CTA per request, one warp per frontier slot.
+__global__ void tree_merge_kernel(const float* tree_part, int gx, int R, int P, int k, int B, int d,
+                                  int32_t* front_tok, int32_t* front_node, float* front_score, int32_t* n_front,
+                                  int32_t* pool_tok, int32_t* pool_parent, int32_t* pool_depth, float* pool_score,
+                                  int32_t* pool_n) {
+    extern __shared__ float tm_smem[];
+    float* lane_z = tm_smem;                                          // [P][32][k]
+    uint32_t* lane_id = reinterpret_cast<uint32_t*>(lane_z + P * 32 * k);
+    Cand* cand = reinterpret_cast<Cand*>(lane_id + P * 32 * k);      // [P * k]
+    const int i = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nf = n_front[i];
+    constexpr int REC = 2 + 2 * kMaxTopK;
+    if (warp < nf) {
+        const int grow = i * P + warp;
+        // lane-local merge over the vocab splits c = lane, lane + 32, ...
+        Lse acc{-INFINITY, 0.f};
+        float tz[kMaxTopK];
+        uint32_t ti[kMaxTopK];
+#pragma unroll
+        for (int q = 0; q < kMaxTopK; ++q) {
+            tz[q] = -INFINITY;
+            ti[q] = 0xffffffffu;
+        }
+        for (int c = lane; c < gx; c += 32) {
+            const float* rec = tree_part + (static_cast<size_t>(grow) * gx + c) * REC;
+            acc = lse_merge(acc, Lse{rec[0], rec[1]});
+            for (int q = 0; q < k; ++q) {
+                float cz = rec[2 + q];
+                uint32_t cv = __float_as_uint(rec[2 + kMaxTopK + q]);
+#pragma unroll
+                for (int e = 0; e < kMaxTopK; ++e) {
+                    if (e < k && (cz > tz[e] || (cz == tz[e] && cv < ti[e]))) {
+                        const float oz = tz[e];
+                        const uint32_t ov = ti[e];
+                        tz[e] = cz;
+                        ti[e] = cv;
+                        cz = oz;
+                        cv = ov;
+                    }
+                }
+            }
+        }
+        acc = warp_lse(acc);
+        for (int q = 0; q < k; ++q) {
+            lane_z[(warp * 32 + lane) * k + q] = tz[q];
+            lane_id[(warp * 32 + lane) * k + q] = ti[q];
+        }
+        __syncwarp();
+        if (lane == 0) {
+            float bz[kMaxTopK];
+            uint32_t bi[kMaxTopK];
+            for (int q = 0; q < kMaxTopK; ++q) {
+                bz[q] = -INFINITY;
+                bi[q] = 0xffffffffu;
+            }
+            for (int e = 0; e < 32 * k; ++e) {
+                float cz = lane_z[warp * 32 * k + e];
+                uint32_t cv = lane_id[warp * 32 * k + e];
+                for (int q = 0; q < k; ++q) {
+                    if (cz > bz[q] || (cz == bz[q] && cv < bi[q])) {
+                        const float oz = bz[q];
+                        const uint32_t ov = bi[q];
+                        bz[q] = cz;
+                        bi[q] = cv;
+                        cz = oz;
+                        cv = ov;
+                    }
+                }
+            }
+            const float lse = acc.m + logf(acc.s);
+            const float sp = front_score[static_cast<size_t>(i) * P + warp];
+            for (int q = 0; q < k; ++q)   // s(c) = s(p) + log pi(v | p)
+                cand[warp * k + q] = Cand{sp + (bz[q] - lse), warp, q, static_cast<int>(bi[q])};
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int nc = nf * k;
+        // insertion sort by (s desc, slot asc, rank asc), keep P
+        for (int a = 1; a < nc; ++a) {
+            const Cand t = cand[a];
+            int b = a;
+            while (b > 0 && cand_before(t, cand[b - 1])) {
+                cand[b] = cand[b - 1];
+                --b;
+            }
+            cand[b] = t;
+        }
+        const int keep = nc < P ? nc : P;
+        const int pool_cap = 1 + P * B;
+        const size_t pb = static_cast<size_t>(i) * pool_cap;
+        int np = pool_n[i];
+        int parent_node[64];
+        for (int c = 0; c < nf && c < 64; ++c) parent_node[c] = front_node[static_cast<size_t>(i) * P + c];
+        for (int c = 0; c < keep; ++c) {
+            pool_tok[pb + np] = cand[c].tok;
+            pool_parent[pb + np] = parent_node[cand[c].slot];
+            pool_depth[pb + np] = d;
+            pool_score[pb + np] = cand[c].s;
+            front_tok[static_cast<size_t>(i) * P + c] = cand[c].tok;
+            front_node[static_cast<size_t>(i) * P + c] = np;
+            front_score[static_cast<size_t>(i) * P + c] = cand[c].s;
+            ++np;
+        }
+        for (int c = keep; c < P; ++c) {
+            front_tok[static_cast<size_t>(i) * P + c] = -1;
+            front_node[static_cast<size_t>(i) * P + c] = -1;
+        }
+        n_front[i] = keep;
+        pool_n[i] = np;
+    }
+}
+
+// One CTA per request: rank the pool by (score desc, depth asc, creation asc),
+// keep the top N, emit root + nodes in rank order and the tree-causal mask.
+__global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* pool_tok, const int32_t* pool_parent,
+                                     const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
+                                     int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
+                                     int32_t* n_nodes) {
+    extern __shared__ int tf_smem[];
+    const int pool_cap = 1 + P * B;
+    int* slot_of = tf_smem;               // pool index -> output slot (-1: not selected)
+    int* node_at = slot_of + pool_cap;    // output slot -> pool index
+    const int i = blockIdx.x;
+    const size_t pb = static_cast<size_t>(i) * pool_cap;
+    const int np = pool_n[i];
+    const int S = N + 1;
+    const int take = (np - 1) < N ? (np - 1) : N;
+    for (int j = threadIdx.x; j < pool_cap; j += blockDim.x) slot_of[j] = -1;
+    __syncthreads();
+    for (int j = 1 + threadIdx.x; j < np; j += blockDim.x) {
+        const float sj = pool_score[pb + j];
+        const int dj = pool_depth[pb + j];
+        int rank = 0;
+        for (int q = 1; q < np; ++q) {
+            if (q == j) continue;
+            const float sq = pool_score[pb + q];
+            const int dq = pool_depth[pb + q];
+            if (sq > sj || (sq == sj && (dq < dj || (dq == dj && q < j)))) ++rank;
+        }
+        if (rank < take) {
+            slot_of[j] = rank + 1;
+            node_at[rank + 1] = j;
+        }
+    }
+    if (threadIdx.x == 0) {
+        slot_of[0] = 0;
+        node_at[0] = 0;
+    }
+    __syncthreads();
+    const size_t ob = static_cast<size_t>(i) * S;
+    const int words = (S + 31) / 32;
+    for (int c = threadIdx.x; c < S; c += blockDim.x) {
+        uint32_t* mrow = mask + (ob + c) * words;
+        for (int w = 0; w < words; ++w) mrow[w] = 0u;
+        if (c <= take) {
+            const int j = node_at[c];
+            tok[ob + c] = pool_tok[pb + j];
+            const int pj = pool_parent[pb + j];
+            parent[ob + c] = (c == 0) ? -1 : slot_of[pj];
+            depth[ob + c] = pool_depth[pb + j];
+            score[ob + c] = (c == 0) ? 0.f : pool_score[pb + j];
+            for (int a = j; a >= 0; a = pool_parent[pb + a]) {
+                const int sa = slot_of[a];
+                if (sa >= 0) mrow[sa >> 5] |= 1u << (sa & 31);
+            }
+        } else {
+            tok[ob + c] = -1;
+            parent[ob + c] = -1;
+            depth[ob + c] = -1;
+            score[ob + c] = 0.f;
+        }
+    }
+    if (threadIdx.x == 0) n_nodes[i] = take + 1;
+}
+
+__global__ void tree_verify_walk_kernel(const unsigned long long* row_keys, const int32_t* tok, const int32_t* parent,
+                                        const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
+                                        int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= R) return;
+    const int S = N + 1;
+    const size_t base = static_cast<size_t>(i) * S;
+    int32_t* o = out_tok + static_cast<size_t>(i) * (B + 1);
+    int nn = n_nodes[i];
+    if (nn < 1 || nn > S) {
+        set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        nn = nn < 1 ? 1 : S;
+    }
+    int cur = 0, a = 0;
+    for (;;) {
+        int t = static_cast<int>(key_token(row_keys[base + cur]));
+        if (t < 0 || t >= V) {
+            set_status(dev_status, SDM_DEV_BAD_TOKEN);
+            t = 0;
+        }
+        int next = -1;
+        for (int c = 1; c < nn; ++c)
+            if (parent[base + c] == cur && tok[base + c] == t) {
+                next = c;
+                break;
+            }
+        o[a] = t;
+        if (next < 0 || a >= B) break;
+        ++a;
+        cur = next;
+    }
+    for (int p = a + 1; p <= B; ++p) o[p] = -1;
+    accept[i] = a;
+    n_out[i] = a + 1;
+}
+
+inline int blocks_for(long long n, int t) { return static_cast<int>((n + t - 1) / t); }
+
+}  // namespace
+
+cudaError_t launch_fill_u64(unsigned long long* p, size_t n, unsigned long long v, cudaStream_t s) {
+    if (n == 0) return cudaSuccess;
+    const int grid = static_cast<int>(n / 256 + 1 < 1024 ? n / 256 + 1 : 1024);
+    fill_u64_kernel<<<grid, 256, 0, s>>>(p, n, v);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chain_finalize(const unsigned long long* keys, const float2* lse_part, int gx, int R, int B, int V,
+                                  int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
+                                  const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
+                                  float* lse, int32_t* dev_status, cudaStream_t s) {
+    chain_finalize_kernel<<<blocks_for(static_cast<long long>(R) * B, 128), 128, 0, s>>>(
+        keys, lse_part, gx, R, B, V, r, L, l_fp32, U, W, anchor, inv_t, sample, tokens, logq, lse, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const float* conf, int R, int gamma, const double* cost, float* survival,
+                            int32_t* budget, double* expected, int32_t* total_tokens, unsigned long long*,
+                            int32_t* dev_status, cudaStream_t s) {
+    (void)dev_status;
+    int n_pad = 1;
+    while (n_pad < R * gamma) n_pad <<= 1;
+    const size_t smem = static_cast<size_t>(n_pad) * 8 + kSchedThreads * 8 + static_cast<size_t>(R) * 4;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    schedule_kernel<<<1, kSchedThreads, smem, s>>>(conf, R, gamma, cost, survival, budget, expected, total_tokens,
+                                                   n_pad);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
+                        const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
+                        int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s) {
+    pack_kernel<<<1, kPackThreads, 0, s>>>(anchor, draft, budget, R, gamma, tiers, n_tiers, cu, ptok, preq, ppos,
+                                           capacity, tier, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
+                                          const unsigned long long* row_keys, int R, int gamma, int V,
+                                          int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+                                          int32_t* dev_status, cudaStream_t s) {
+    verify_greedy_finalize_kernel<<<blocks_for(R, 128), 128, 0, s>>>(mode, cu, draft, budget, row_keys, R, gamma, V,
+                                                                      accept, ceiling, out_tok, n_out, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t* anchor, const int32_t* draft,
+                                      const int32_t* budget, const float* logq, const void* target, int t_fp32,
+                                      int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
+                                      uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
+                                      int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
+                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
+                                      unsigned long long* res_keys, int32_t* dev_status, cudaStream_t s) {
+    verify_sample_scan_kernel<<<blocks_for(R, 64), 64, 0, s>>>(
+        mode, cu, anchor, draft, budget, logq, target, t_fp32, V, lse_part, n_chunks, inv_t, k0, k1, cycle, R, gamma,
+        accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, res_keys, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_verify_sample_finalize(const int32_t* draft, const int32_t* accept,
+                                          const unsigned long long* res_keys, int R, int gamma, int V,
+                                          int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s) {
+    verify_sample_finalize_kernel<<<blocks_for(R, 128), 128, 0, s>>>(draft, accept, res_keys, R, gamma, V, out_tok,
+                                                                      n_out, dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
+                             float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
+                             int32_t* pool_depth, float* pool_score, int32_t* pool_n, int32_t* dev_status,
+                             cudaStream_t s) {
+    tree_init_kernel<<<blocks_for(R, 128), 128, 0, s>>>(anchor, R, P, B, front_tok, front_node, front_score, n_front,
+                                                        pool_tok, pool_parent, pool_depth, pool_score, pool_n,
+                                                        dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_merge(const float* tree_part, int gx, int R, int P, int k, int B, int d, int32_t* front_tok,
+                              int32_t* front_node, float* front_score, int32_t* n_front, int32_t* pool_tok,
+                              int32_t* pool_parent, int32_t* pool_depth, float* pool_score, int32_t* pool_n,
+                              cudaStream_t s) {
+    const size_t smem = static_cast<size_t>(P) * 32 * k * 8 + static_cast<size_t>(P) * k * sizeof(Cand);
+    tree_merge_kernel<<<R, P * 32, smem, s>>>(tree_part, gx, R, P, k, B, d, front_tok, front_node, front_score,
+                                              n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool_tok, const int32_t* pool_parent,
+                                 const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
+                                 int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
+                                 int32_t* n_nodes, cudaStream_t s) {
+    const int pool_cap = 1 + P * B;
+    const size_t smem = static_cast<size_t>(pool_cap) * 4 + static_cast<size_t>(N + 1) * 4;
+    tree_finalize_kernel<<<R, 128, smem, s>>>(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok,
+                                              parent, depth, score, mask, n_nodes);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, const int32_t* tok, const int32_t* parent,
+                                    const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
+                                    int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s) {
+    tree_verify_walk_kernel<<<blocks_for(R, 64), 64, 0, s>>>(row_keys, tok, parent, n_nodes, R, N, B, V, accept,
+                                                             out_tok, n_out, dev_status);
+    return cudaGetLastError();
+}
+
+int num_sms() {
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 148;
+    }
+    return n;
+}
+
+}  // namespace sdm

@@ -1,0 +1,103 @@
+"""The C-ABI library builds for sm_103a, loads, exports every symbol that
+include/sdm.h declares, and rejects bad arguments on the host (no GPU needed:
+these paths return before any CUDA call)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_markov_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdm_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_operations():
+    names = declared_functions()
+    for op in ("sdm_draft_chain", "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify"):
+        assert op in names
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.sdm_status_str(0) == b"ok"
+    assert lib.sdm_status_str(5) == b"workspace missing or too small"
+    assert lib.sdm_version() >= 100
+
+
+def test_workspace_sizes_are_host_computable(lib):
+    assert lib.sdm_workspace_size(binding.OP_DRAFT_CHAIN, 64, 7, 151936, 256, 0, 0, 0) > 0
+    assert lib.sdm_workspace_size(binding.OP_DRAFT_TREE, 32, 16, 151936, 256, 8, 4, 64) > 0
+    assert lib.sdm_workspace_size(binding.OP_VERIFY, 64, 7, 151936, 256, 512, 0, 0) >= 512 * 8
+    assert lib.sdm_workspace_size(binding.OP_VERIFY_TREE, 32, 16, 151936, 0, 0, 0, 64) >= 32 * 65 * 8
+    assert lib.sdm_workspace_size(binding.OP_SCHEDULE, 64, 7, 0, 0, 0, 0, 0) == 0
+
+
+FAKE = ctypes.c_void_p(0x1000)   # never dereferenced: validation fails first
+
+
+def _chain(lib, **kw):
+    a = dict(L=FAKE, dtL=0, U=FAKE, W=FAKE, anchor=FAKE, R=4, B=7, V=1024, r=64, dec=0, T=1.0, tokens=FAKE,
+             ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.sdm_draft_chain(a["L"], a["dtL"], a["U"], a["W"], a["anchor"], a["R"], a["B"], a["V"], a["r"],
+                               a["dec"], a["T"], binding.SdmRng(0, 0), a["tokens"], None, None, a["ws"],
+                               a["ws_bytes"], None, None)
+
+
+def test_draft_chain_host_validation(lib):
+    assert _chain(lib, L=None) == 1
+    assert _chain(lib, R=0) == 1
+    assert _chain(lib, dtL=7) == 1
+    assert _chain(lib, dec=1, T=0.0) == 1
+    assert _chain(lib, V=1001) == 2            # V % 8 != 0
+    assert _chain(lib, r=96) == 2              # r % 64 != 0
+    assert _chain(lib, r=512) == 2             # r > 256
+    assert _chain(lib, L=ctypes.c_void_p(0x1004)) == 2   # misaligned base
+    assert _chain(lib, ws=None) == 5
+    assert _chain(lib, ws_bytes=16) == 5
+
+
+def test_tree_and_verify_host_validation(lib):
+    f = lib.sdm_draft_tree
+    args = [FAKE, 0, FAKE, FAKE, FAKE, 32, 16, 1024, 64, 4, 8, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30,
+            None, None]
+    bad_k = list(args)
+    bad_k[9] = 9                                # k > 8
+    assert f(*bad_k) == 2
+    bad_p = list(args)
+    bad_p[10] = 3                               # 128 % P != 0
+    assert f(*bad_p) == 2
+    bad_n = list(args)
+    bad_n[11] = 8 * 16 + 1                      # N > P * B
+    assert f(*bad_n) == 2
+    v = lib.sdm_verify
+    vargs = [2, 0, 1.0, binding.SdmRng(0, 0), FAKE, 0, 64, FAKE, FAKE, FAKE, None, None, None, None, 0, None, None, 0,
+             4, 7, 1024, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None, None]
+    assert v(*vargs) == 1                       # cap-accept without a budget
+    vargs[0] = 1
+    vargs[1] = 1                                # sample without logq / L / U / W
+    assert v(*vargs) == 1
+    assert lib.sdm_schedule_budget(FAKE, 2000, 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None, None) == 2
+    assert lib.sdm_pack_ragged(FAKE, FAKE, None, 4, 7, None, 2, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None, None,
+                               None) == 1       # tiers missing

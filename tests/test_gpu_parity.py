@@ -1,0 +1,322 @@
+"""GPU parity: every C-ABI operation against the CPU oracle on the same seeded
+inputs.
+
+Integer results (token ids, accept lengths, budgets, packed offsets, tree
+indices, masks) must match bit for bit; fp32 log-prob sums and scores within
+1e-5 relative (|gpu - oracle| <= 1e-5 * max(1, |oracle|)).  Sampling and tree
+pruning decide integers from exp/log values that the kernel computes in fp32
+and the oracle in fp64: a mismatch there is only tolerated when the oracle's
+decision margin is below 1e-5 (a tie-zone event, reported), and none is
+expected at these seeds.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_markov_gb300 import binding as sdm
+from speculative_decoding_markov_gb300 import synthetic
+from speculative_decoding_markov_gb300.workloads import BF16, FP32, WORKLOADS
+from tests.helpers import np_of, small
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TIE = 1e-5
+FTOL = 1e-5
+
+
+def dev(t):
+    return t.to(DEV).contiguous()
+
+
+def host(t):
+    return t.detach().cpu().numpy()
+
+
+def close(gpu, ref, tol=FTOL):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    return np.abs(gpu - ref) <= tol * np.maximum(1.0, np.abs(ref))
+
+
+def compare_sequences(gpu_tok, orc_tok, orc_margin, what):
+    """Exact per-request comparison up to a tie-zone flip (then the rest of
+    that request depends on a different prefix and is not compared)."""
+    events = 0
+    for i in range(orc_tok.shape[0]):
+        mism = np.nonzero(gpu_tok[i] != orc_tok[i])[0]
+        if mism.size:
+            d = int(mism[0])
+            assert orc_margin[i, d] < TIE, f"{what}: request {i} position {d} differs at margin {orc_margin[i, d]}"
+            events += 1
+    return events
+
+
+# ---------------------------------------------------------------------------
+# draft_chain
+# ---------------------------------------------------------------------------
+CHAIN_CASES = [
+    dict(R=4, B=7, V=1024, r=64, l_dtype=FP32),          # tiny chain workload shape
+    dict(R=64, B=4, V=1000, r=256, l_dtype=BF16),        # ragged vocab tail (15 tiles + 40)
+    dict(R=200, B=3, V=520, r=128, l_dtype=BF16),        # two M tiles, ragged rows
+    dict(R=1, B=2, V=8, r=64, l_dtype=FP32),             # smallest shapes
+    dict(R=130, B=2, V=4160, r=64, l_dtype=FP32),
+]
+
+
+@pytest.mark.parametrize("case", CHAIN_CASES, ids=lambda c: f"R{c['R']}B{c['B']}V{c['V']}r{c['r']}")
+def test_draft_chain_greedy(case):
+    w = small(sigma=(0.5,), **case)
+    inp = synthetic.generate(w, seed=case["R"] + case["V"])
+    ref = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    assert ref["flags"] == 0
+    out = sdm.draft_chain(dev(inp["L"]), dev(inp["U"]), dev(inp["W"]), dev(inp["anchor"]))
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0
+    np.testing.assert_array_equal(host(out["tokens"]), ref["tokens"])
+
+
+@pytest.mark.parametrize("case,T", [(dict(R=40, B=5, V=2056, r=64, l_dtype=BF16), 0.7),
+                                    (dict(R=150, B=2, V=512, r=128, l_dtype=FP32), 1.3),
+                                    (dict(R=3, B=3, V=8, r=64, l_dtype=FP32), 1.0)])
+def test_draft_chain_sample(case, T):
+    w = small(sigma=(0.5,), **case)
+    inp = synthetic.generate(w, seed=7)
+    ref = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]),
+                             decode=oracle.SAMPLE, temperature=T, seed=99, cycle=5)
+    out = sdm.draft_chain(dev(inp["L"]), dev(inp["U"]), dev(inp["W"]), dev(inp["anchor"]), decode=sdm.SAMPLE,
+                          temperature=T, seed=99, cycle=5)
+    torch.cuda.synchronize()
+    tok = host(out["tokens"])
+    events = compare_sequences(tok, ref["tokens"], ref["margin"], "sample chain")
+    assert events == 0
+    assert close(host(out["lse"]), ref["lse"]).all()
+    assert close(host(out["logq"]), ref["logq"]).all()
+
+
+def test_draft_chain_is_deterministic():
+    w = small(R=96, B=3, V=4096, r=256, l_dtype=BF16, sigma=(0.5,))
+    inp = {k: dev(v) for k, v in synthetic.generate(w, seed=3).items()}
+    a = sdm.draft_chain(inp["L"], inp["U"], inp["W"], inp["anchor"], decode=sdm.SAMPLE, seed=1)
+    b = sdm.draft_chain(inp["L"], inp["U"], inp["W"], inp["anchor"], decode=sdm.SAMPLE, seed=1)
+    torch.cuda.synchronize()
+    for key in ("tokens", "logq", "lse"):
+        assert torch.equal(a[key], b[key])
+
+
+def test_draft_chain_flags_bad_anchor_without_faulting():
+    w = small(R=8, B=2, V=512, r=64, sigma=(0.5,))
+    inp = synthetic.generate(w, seed=1)
+    anchor = inp["anchor"].clone()
+    anchor[3] = w.V + 17
+    out = sdm.draft_chain(dev(inp["L"]), dev(inp["U"]), dev(inp["W"]), dev(anchor))
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) & sdm.DEV_BAD_TOKEN
+    ok = [i for i in range(w.R) if i != 3]
+    ref = oracle.draft_chain(np_of(inp["L"][ok]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"][ok]))
+    np.testing.assert_array_equal(host(out["tokens"])[ok], ref["tokens"])
+
+
+# ---------------------------------------------------------------------------
+# schedule_budget
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("R,g,seed", [(1, 1, 0), (5, 7, 1), (64, 7, 2), (256, 8, 3), (512, 16, 4), (33, 16, 5)])
+def test_schedule_budget(R, g, seed):
+    rng = np.random.default_rng(seed)
+    conf = rng.uniform(0.02, 1.0, (R, g)).astype(np.float32)
+    conf[rng.random((R, g)) < 0.1] = 1.0                  # exact ties in S
+    a, b = float(rng.uniform(0.5, 3.0)), float(rng.uniform(0.001, 0.2))
+    cost = a + b * np.arange(R * (g + 1) + 1, dtype=np.float64)
+    ref = oracle.schedule_budget(conf, cost)
+    out = sdm.schedule_budget(dev(torch.from_numpy(conf)), dev(torch.from_numpy(cost)))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(out["survival"]).view(np.uint32), ref["survival"].view(np.uint32))
+    np.testing.assert_array_equal(host(out["budget"]), ref["budget"])
+    if R * (g + 1) < 4096:                                 # fp64 sums exact in any order
+        assert float(host(out["expected"])[0]) == ref["expected"]
+    else:
+        assert close(host(out["expected"]), [ref["expected"]], 1e-12).all()
+    assert int(host(out["total_tokens"])[0]) == ref["total_tokens"]
+
+
+def test_schedule_flushes_tiny_survivals_and_breaks_ties_by_request():
+    R, g = 6, 5
+    conf = np.full((R, g), 0.5, np.float32)
+    conf[2] = 0.01                                         # S falls below 2^-18 by k = 3
+    cost = 1.0 + 0.0001 * np.arange(R * (g + 1) + 1)
+    ref = oracle.schedule_budget(conf, cost)
+    out = sdm.schedule_budget(dev(torch.from_numpy(conf)), dev(torch.from_numpy(cost)))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(out["budget"]), ref["budget"])
+    assert ref["budget"][2] <= 2
+
+
+# ---------------------------------------------------------------------------
+# pack_ragged
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("R,g,seed,static", [(1, 1, 0, False), (37, 8, 1, False), (256, 8, 2, False),
+                                             (256, 8, 3, True), (1500, 2, 4, False)])
+def test_pack_ragged(R, g, seed, static):
+    rng = np.random.default_rng(seed)
+    anchor = rng.integers(0, 5000, R).astype(np.int32)
+    draft = rng.integers(0, 5000, (R, g)).astype(np.int32)
+    budget = rng.integers(0, g + 1, R).astype(np.int32)
+    budget[: max(1, R // 5)] = 0
+    tiers = np.array([64, 128, 256, 512, 1024, 2048], np.int32)
+    ref = oracle.pack_ragged(anchor, draft, None if static else budget, tiers)
+    out = sdm.pack_ragged(dev(torch.from_numpy(anchor)), dev(torch.from_numpy(draft)),
+                          None if static else dev(torch.from_numpy(budget)), dev(torch.from_numpy(tiers)))
+    torch.cuda.synchronize()
+    t = ref["tier"]
+    assert int(host(out["tier"])[0]) == t
+    np.testing.assert_array_equal(host(out["cu_seqlens"]), ref["cu_seqlens"])
+    for k in ("packed_tok", "packed_req", "packed_pos"):
+        np.testing.assert_array_equal(host(out[k])[:t], ref[k])
+    flag = int(out["dev_status"].item()) & sdm.DEV_TIER_UNCAPTURED
+    assert bool(flag) == bool(ref["flags"] & oracle.FLAG_TIER_UNCAPTURED)
+
+
+# ---------------------------------------------------------------------------
+# verify (greedy, all modes) on oracle-drafted inputs
+# ---------------------------------------------------------------------------
+def _oracle_chain_pipeline(w, seed, mode):
+    inp = synthetic.generate(w, seed=seed)
+    an = np_of(inp["anchor"])
+    dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), an)
+    sc = oracle.schedule_budget(np_of(inp["conf"]), synthetic.cost_table(w).numpy())
+    budget = sc["budget"]
+    pk = oracle.pack_ragged(an, dr["tokens"], budget if mode == "compact" else None, np.array(w.tiers, np.int32))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+    return inp, dr, budget, pk, packed
+
+
+@pytest.mark.parametrize("mode", ["static", "compact", "cap_accept"])
+@pytest.mark.parametrize("case", [dict(R=16, B=6, V=2048, r=64, l_dtype=BF16, target_dtype=BF16),
+                                  dict(R=5, B=7, V=1024, r=64, l_dtype=FP32, target_dtype=FP32),
+                                  dict(R=70, B=3, V=40008, r=64, l_dtype=BF16, target_dtype=BF16)],
+                         ids=lambda c: f"R{c['R']}V{c['V']}")
+def test_verify_greedy(mode, case):
+    w = small(sigma=(0.1, 0.6, 1.5), class_mix="alternate", **case)
+    inp, dr, budget, pk, packed = _oracle_chain_pipeline(w, 11, mode)
+    om = {"static": oracle.STATIC, "compact": oracle.COMPACT, "cap_accept": oracle.CAP_ACCEPT}[mode]
+    an = np_of(inp["anchor"])
+    ref = oracle.verify(om, oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an, dr["tokens"], budget=budget)
+    gm = {"static": sdm.STATIC, "compact": sdm.COMPACT, "cap_accept": sdm.CAP_ACCEPT}[mode]
+    out = sdm.verify(gm, sdm.GREEDY, dev(packed), dev(torch.from_numpy(pk["cu_seqlens"])), dev(inp["anchor"]),
+                     dev(torch.from_numpy(dr["tokens"])), budget=dev(torch.from_numpy(budget)))
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0
+    for k in ("accept", "out_tok", "n_out"):
+        np.testing.assert_array_equal(host(out[k]), ref[k])
+    if mode == "cap_accept":
+        np.testing.assert_array_equal(host(out["ceiling"]), ref["ceiling"])
+
+
+def test_verify_greedy_empty_windows():
+    """Budget 0 for every request: the window is the root only; the commit is
+    the target token at row 0."""
+    w = small(R=9, B=4, V=1024, r=64, l_dtype=BF16, target_dtype=BF16)
+    inp = synthetic.generate(w, seed=2)
+    an = np_of(inp["anchor"])
+    dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), an)
+    budget = np.zeros(w.R, np.int32)
+    pk = oracle.pack_ragged(an, dr["tokens"], budget, np.array([16], np.int32))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+    ref = oracle.verify(oracle.COMPACT, oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an, dr["tokens"])
+    out = sdm.verify(sdm.COMPACT, sdm.GREEDY, dev(packed), dev(torch.from_numpy(pk["cu_seqlens"])),
+                     dev(inp["anchor"]), dev(torch.from_numpy(dr["tokens"])))
+    torch.cuda.synchronize()
+    assert np.all(ref["accept"] == 0)
+    np.testing.assert_array_equal(host(out["out_tok"]), ref["out_tok"])
+
+
+# ---------------------------------------------------------------------------
+# verify (rejection sampling)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("mode", ["static", "compact", "cap_accept"])
+@pytest.mark.parametrize("case,T", [(dict(R=48, B=5, V=2048, r=64, l_dtype=BF16, target_dtype=FP32), 1.0),
+                                    (dict(R=20, B=4, V=1000, r=128, l_dtype=FP32, target_dtype=BF16), 0.8)],
+                         ids=["bf16L_fp32T", "fp32L_bf16T"])
+def test_verify_sample(mode, case, T):
+    w = small(sigma=(0.3, 1.0), class_mix="alternate", temperature=T, **case)
+    inp = synthetic.generate(w, seed=21)
+    an = np_of(inp["anchor"])
+    U, W = np_of(inp["U"]), np_of(inp["W"])
+    dr = oracle.draft_chain(np_of(inp["L"]), U, W, an, decode=oracle.SAMPLE, temperature=T, seed=5, cycle=3)
+    logq32 = dr["logq"].astype(np.float32)
+    lse32 = dr["lse"].astype(np.float32)
+    budget = np.random.default_rng(1).integers(0, w.B + 1, w.R).astype(np.int32)
+    pk = oracle.pack_ragged(an, dr["tokens"], budget if mode == "compact" else None, np.array(w.tiers, np.int32))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+    om = {"static": oracle.STATIC, "compact": oracle.COMPACT, "cap_accept": oracle.CAP_ACCEPT}[mode]
+    ref = oracle.verify(om, oracle.SAMPLE, np_of(packed), pk["cu_seqlens"], an, dr["tokens"], budget=budget,
+                        logq=logq32.astype(np.float64), lse_q=lse32.astype(np.float64), L=np_of(inp["L"]), U=U, W=W,
+                        temperature=T, seed=5, cycle=3)
+    gm = {"static": sdm.STATIC, "compact": sdm.COMPACT, "cap_accept": sdm.CAP_ACCEPT}[mode]
+    out = sdm.verify(gm, sdm.SAMPLE, dev(packed), dev(torch.from_numpy(pk["cu_seqlens"])), dev(inp["anchor"]),
+                     dev(torch.from_numpy(dr["tokens"])), budget=dev(torch.from_numpy(budget)),
+                     logq=dev(torch.from_numpy(logq32)), lse_q=dev(torch.from_numpy(lse32)), L=dev(inp["L"]),
+                     U=dev(inp["U"]), W=dev(inp["W"]), temperature=T, seed=5, cycle=3)
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0
+    diff = np.nonzero((host(out["out_tok"]) != ref["out_tok"]).any(axis=1) | (host(out["accept"]) != ref["accept"]))[0]
+    for i in diff:
+        assert ref["margin"][i] < TIE, f"request {i} differs at margin {ref['margin'][i]}"
+    assert diff.size == 0
+    if mode == "cap_accept":
+        np.testing.assert_array_equal(host(out["ceiling"]), ref["ceiling"])
+
+
+# ---------------------------------------------------------------------------
+# PCTree
+# ---------------------------------------------------------------------------
+TREE_CASES = [dict(R=4, B=4, V=1000, r=64, k=4, P=8, N=16),
+              dict(R=3, B=3, V=64, r=64, k=2, P=4, N=6),
+              dict(R=20, B=5, V=2048, r=128, k=4, P=8, N=32),     # 160 GEMM rows: two M tiles
+              dict(R=2, B=6, V=520, r=64, k=1, P=2, N=6)]         # k = 1: the chain
+
+
+@pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"R{c['R']}B{c['B']}k{c['k']}P{c['P']}N{c['N']}")
+def test_draft_tree(case):
+    w = small(R=case["R"], B=case["B"], V=case["V"], r=case["r"], l_dtype=BF16, sigma=(0.5,), l_std=2.0)
+    inp = synthetic.generate(w, seed=case["V"])
+    args = (np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    ref = oracle.draft_tree(*args, k=case["k"], P=case["P"], N=case["N"])
+    out = sdm.draft_tree(dev(inp["L"]), dev(inp["U"]), dev(inp["W"]), dev(inp["anchor"]), case["k"], case["P"],
+                         case["N"])
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0
+    for i in range(w.R):
+        same = all(np.array_equal(host(out[k])[i], ref[k][i]) for k in ("tok", "parent", "depth"))
+        if not same:
+            assert ref["margin"][i] < TIE, f"request {i} tree differs at margin {ref['margin'][i]}"
+            continue
+        assert host(out["n_nodes"])[i] == ref["n_nodes"][i]
+        np.testing.assert_array_equal(host(out["mask"])[i].view(np.uint32), ref["mask"][i])
+        assert close(host(out["score"])[i], ref["score"][i]).all()
+    if case["k"] == 1:
+        ch = oracle.draft_chain(*args)
+        np.testing.assert_array_equal(host(out["tok"])[:, 1:], ch["tokens"])
+
+
+def test_verify_tree():
+    case = dict(R=6, B=4, V=2048, r=64, k=3, P=4, N=12)
+    w = small(R=case["R"], B=case["B"], V=case["V"], r=case["r"], l_dtype=BF16, target_dtype=BF16, sigma=(0.4,),
+              l_std=2.0)
+    inp = synthetic.generate(w, seed=4)
+    args = (np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    tr = oracle.draft_tree(*args, k=case["k"], P=case["P"], N=case["N"])
+    tgt = synthetic.tree_target(inp, torch.as_tensor(tr["tok"]), torch.as_tensor(tr["depth"]),
+                                torch.as_tensor(tr["n_nodes"]), w.target_dtype)
+    ref = oracle.verify_tree(np_of(tgt), tr["tok"], tr["parent"], tr["n_nodes"], w.B)
+    out = sdm.verify_tree(dev(tgt), dev(torch.from_numpy(tr["tok"])), dev(torch.from_numpy(tr["parent"])),
+                          dev(torch.from_numpy(tr["n_nodes"])), w.B)
+    torch.cuda.synchronize()
+    for k in ("accept", "out_tok", "n_out"):
+        np.testing.assert_array_equal(host(out[k]), ref[k])
+    assert ref["accept"].max() >= 1
