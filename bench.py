@@ -36,8 +36,9 @@ FLUSH_BYTES = 256 << 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--no-graphs", action="store_true", help="launch eagerly instead of replaying CUDA graphs")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_8b_chain")
     ap.add_argument("--no-e2e", action="store_true")
@@ -87,7 +88,7 @@ def recorded_traffic(kernel: str):
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled during the timed region."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
@@ -99,7 +100,8 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)                    # let the sampler start before the work
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -116,25 +118,31 @@ class ClockSampler:
             self.lines = [l for l in out.splitlines() if l.strip()]
         return False
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and active throttle reasons of the samples taken
+        between wall-clock times t0 and t1 (all samples if fewer than 3 fall
+        inside)."""
+        import datetime
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        rows = []
         for line in getattr(self, "lines", []):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 7:
+            if len(parts) < 8:
                 continue
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:8]))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[3:7]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if t0 is not None and t0 <= r[0] <= t1]
+        window = "timed region"
+        if len(inside) < 3:
+            inside, window = rows, "warm-up and timed region"
+        if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = sorted({n for r in inside for n, v in zip(names, r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
 
 
 # ---------------------------------------------------------------------------
@@ -174,6 +182,9 @@ class Cycle:
         self.ws_draft = sdm.workspace(sdm.OP_DRAFT_CHAIN, R, B, V, r, device=device)
         self.ws_verify = sdm.workspace(sdm.OP_VERIFY, R, B, V, r, cap, device=device)
         self.status = sdm.new_status(device)
+        # greedy drafting uses the Markov head's prepared tables, built once
+        # per weights (model-load time, outside the timed cycle)
+        self.prepared = None if self.sample else sdm.markov_prepare(self.inp["U"], self.inp["W"])
         # one untimed cycle fixes the drafted prefix; the stand-in target model
         # then provides every window row along it
         self.draft()
@@ -189,7 +200,7 @@ class Cycle:
         sdm, i = self.sdm, self.inp
         sdm.draft_chain(i["L"], i["U"], i["W"], i["anchor"], decode=sdm.SAMPLE if self.sample else sdm.GREEDY,
                         temperature=self.w.temperature, seed=0, cycle=0, out=self.dr, ws=self.ws_draft,
-                        dev_status=self.status)
+                        dev_status=self.status, prepared=self.prepared)
 
     def schedule_pack(self):
         sdm, i = self.sdm, self.inp
@@ -210,8 +221,22 @@ class Cycle:
                    out=self.vr, ws=self.ws_verify, dev_status=self.status, **kw)
 
     def launches_per_step(self):
-        verify = 5 if self.sample else 3
-        return (self.w.B + 2) + 1 + 1 + verify
+        draft = 2 if self.prepared is not None else self.w.B + 2
+        verify = 5 if self.sample else 2
+        return draft + 1 + 1 + verify
+
+    def capture(self):
+        """CUDA graphs of the two timed segments (the stand-in gather between
+        them stays outside)."""
+        torch = self.torch
+        self.g_draft = torch.cuda.CUDAGraph()
+        self.g_verify = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.g_draft):
+            self.draft()
+            self.schedule_pack()
+        with torch.cuda.graph(self.g_verify):
+            self.verify()
+        torch.cuda.synchronize()
 
 
 def run_ours(args, w, world, rank, local):
@@ -227,37 +252,66 @@ def run_ours(args, w, world, rank, local):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
+    graphs = not args.no_graphs
+    if graphs:
+        cyc.capture()
+
+    def run_draft():
+        if graphs:
+            cyc.g_draft.replay()
+        else:
+            cyc.draft()
+            cyc.schedule_pack()
+
+    def run_verify():
+        if graphs:
+            cyc.g_verify.replay()
+        else:
+            cyc.verify()
+
     def step(ev=None):
         flush.fill_(1)                                      # L2 flush, untimed
         if ev:
             ev[0].record(stream)
-        cyc.draft()
+        run_draft()                                         # draft + schedule + pack
         if ev:
             ev[1].record(stream)
-        cyc.schedule_pack()
-        if ev:
-            ev[2].record(stream)
         cyc.gather()                                        # target stand-in, untimed
         if ev:
-            ev[3].record(stream)
-        cyc.verify()
+            ev[2].record(stream)
+        run_verify()
         if ev:
-            ev[4].record(stream)
+            ev[3].record(stream)
 
+    # draft-only events on a separate eager run give the draft / schedule split
+    ev_split = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     for _ in range(args.warmup):
         step()
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
+        w0 = time.time()
         for k in range(args.steps):
             step(events[k])
         torch.cuda.synchronize()
+        w1 = time.time()
     barrier(world)
-    t_draft = sum(e[0].elapsed_time(e[1]) for e in events) / 1e3
-    t_sched = sum(e[1].elapsed_time(e[2]) for e in events) / 1e3
-    t_verify = sum(e[3].elapsed_time(e[4]) for e in events) / 1e3
-    t_total = t_draft + t_sched + t_verify
+    # one eager cycle split into draft and schedule+pack (reported only)
+    flush.fill_(1)
+    ev_split[0].record(stream)
+    cyc.draft()
+    ev_split[1].record(stream)
+    cyc.schedule_pack()
+    ev_split[2].record(stream)
+    torch.cuda.synchronize()
+    split_draft = ev_split[0].elapsed_time(ev_split[1])
+    split_sched = ev_split[1].elapsed_time(ev_split[2])
+    t_front = sum(e[0].elapsed_time(e[1]) for e in events) / 1e3       # draft + schedule + pack
+    t_verify = sum(e[2].elapsed_time(e[3]) for e in events) / 1e3
+    t_total = t_front + t_verify
+    # the draft's share of the front segment, from the eager split cycle
+    t_draft = t_front * split_draft / max(split_draft + split_sched, 1e-9)
     t_max = allreduce_max(t_total, world)
     status = int(cyc.status.item())
 
@@ -265,12 +319,20 @@ def run_ours(args, w, world, rank, local):
     peak, peak_kind = measured_peaks()
     s_l = 2 if w.l_dtype == 0 else 4
     s_t = 2 if w.target_dtype == 0 else 4
-    draft_bytes = R * B * V * s_l + w.r * V * 2                 # L once + W once per cycle
+    # algorithmic bytes: the pruned greedy chain must read every element of L
+    # once (the few W^T rows it scores are not counted); the dense chain reads
+    # L once and W once per cycle
+    draft_bytes = R * B * V * s_l + (0 if cyc.prepared is not None else w.r * V * 2)
     verify_bytes = windows * V * s_t                            # verified window rows
     if t_draft >= t_verify:
-        kname = "markov_gemm_kernel<chain>"
-        per_launch_s = t_draft / args.steps / B
-        achieved = draft_bytes / B / per_launch_s / 1e9
+        if cyc.prepared is not None:
+            kname = "chain_scan_kernel+chain_pick_kernel"
+            per_launch_s = t_draft / args.steps
+            achieved = draft_bytes / per_launch_s / 1e9
+        else:
+            kname = "markov_gemm_kernel<chain>"
+            per_launch_s = t_draft / args.steps / B
+            achieved = draft_bytes / B / per_launch_s / 1e9
         traffic = recorded_traffic(kname)
     else:
         kname = "row_stream_kernel<argmax>"
@@ -286,7 +348,7 @@ def run_ours(args, w, world, rank, local):
     if not args.no_cpu_baseline and rank == 0 and world == 1:
         cpu = oracle_sample(w, cyc.inp, args.cpu_seconds)
 
-    clk = clocks.summary()
+    clk = clocks.summary(w0, w1)
     out = {
         "metric": METRIC,
         "value": committed * args.steps * world / t_max,
@@ -304,8 +366,10 @@ def run_ours(args, w, world, rank, local):
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed by a 256 MB write before every step",
                    "timed": "draft+schedule+pack+verify (CUDA events); target stand-in row gather excluded"},
-        "breakdown_ms_per_step": {"draft": t_draft / args.steps * 1e3, "schedule+pack": t_sched / args.steps * 1e3,
-                                  "verify": t_verify / args.steps * 1e3},
+        "breakdown_ms_per_step": {"draft+schedule+pack": t_front / args.steps * 1e3,
+                                  "verify": t_verify / args.steps * 1e3,
+                                  "eager_split_ms": {"draft": split_draft, "schedule+pack": split_sched}},
+        "graphs": graphs,
         "tokens_per_step": {"committed": committed, "accepted_drafts": accepted, "verified_rows": windows},
         "verified_rows_per_s": windows * args.steps * world / t_max,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -336,22 +400,30 @@ def run_e2e(cyc, args, committed):
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * 4 + nout_h.numel() * 4
 
+    graphs = hasattr(cyc, "g_draft")
+
     def step():
         i["L"].copy_(host["L"], non_blocking=True)
         i["anchor"].copy_(host["anchor"], non_blocking=True)
         i["conf"].copy_(host["conf"], non_blocking=True)
         cyc.target.copy_(host["target"], non_blocking=True)
-        cyc.draft()
-        cyc.schedule_pack()
+        if graphs:
+            cyc.g_draft.replay()
+        else:
+            cyc.draft()
+            cyc.schedule_pack()
         cyc.gather()
-        cyc.verify()
+        if graphs:
+            cyc.g_verify.replay()
+        else:
+            cyc.verify()
         out_h.copy_(cyc.vr["out_tok"], non_blocking=True)
         nout_h.copy_(cyc.vr["n_out"], non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
-    for _ in range(max(2, args.warmup)):
+    for _ in range(3):
         step()
-    k = max(3, args.steps // 2)
+    k = max(3, min(50, args.steps // 4))
     t0 = time.perf_counter()
     for _ in range(k):
         step()

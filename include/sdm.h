@@ -99,6 +99,19 @@ enum {
 size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int N);
 
 /*
+ * markov_prepare: tables derived once from the Markov head (U, W), for the
+ * greedy chain (no counterpart on the pages; a layout step, like packing a
+ * weight matrix at load time).  Fills `prepared` (device, at least
+ * sdm_markov_prepared_size(V, r) bytes, 256-byte aligned) with
+ *   W^T [V, r] bf16, u_norm [V] fp32 = |U[v]|_2 and n_max fp32 =
+ *   max_v |W[:, v]|_2, norms accumulated in fp64 and rounded up.
+ * Enqueued on `stream`; valid until U or W change.
+ */
+size_t sdm_markov_prepared_size(int V, int r);
+sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, void* prepared,
+                              size_t prepared_bytes, void* stream);
+
+/*
  * draft_chain: the Markov-head sequential stage ([DSpark notes] sec. 4,
  * "Sequential stage" and "Markov head"; [PCTree] z_d = L_d + Markov(y_{d-1})).
  * For d = 1..B, with y_0 = anchor:
@@ -108,15 +121,23 @@ size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int 
  *              y_d = argmax_v (z_d[v]/T - ln(-ln u_v)), stream 0, row d;
  *              lse[i, d-1] = log sum_v exp(z_d[v]/T);
  *              logq[i, d-1] = z_d[y_d]/T - lse[i, d-1].
- * In:  L [R, B, V] (dtL), U [V, r] bf16, W [r, V] bf16, anchor [R] int32.
+ * In:  L [R, B, V] (dtL), U [V, r] bf16, W [r, V] bf16, anchor [R] int32;
+ *      prepared: NULL, or the tables sdm_markov_prepare built from U and W.
  * Out: tokens [R, B] int32; logq, lse [R, B] fp32 (sample only; may be NULL
  *      when greedy).
- * The product U[y] . W runs on the tcgen05 tensor cores (bf16 in, fp32
- * accumulate in TMEM) and the +L / argmax / race is fused into its epilogue;
- * z is never written to memory.
+ * Sampling (and greedy without prepared tables): the product U[y] . W runs on
+ * the tcgen05 tensor cores (bf16 in, fp32 accumulate in TMEM) and the +L /
+ * argmax / race is fused into its epilogue; z is never written to memory.
+ * Greedy with prepared tables: since |U[y] . W[:, v]| <= |U[y]| max_v |W[:, v]|
+ * = C(y), only ids with L[v] >= max L - 2 C(y) can win.  One HBM-bound pass
+ * over all of L lists those ids for every (request, step) with the worst-case
+ * C, then one CTA per request walks the B steps scoring only listed ids
+ * exactly (from W^T).  L is read once and the result is the same argmax bit
+ * for bit.  Needs B <= 64 and V <= 64 * 16384 (bf16 L) or 64 * 8192 (fp32 L),
+ * else SDM_ERR_UNSUPPORTED.
  */
 sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
-                           const int32_t* anchor, int R, int B, int V, int r,
+                           const void* prepared, const int32_t* anchor, int R, int B, int V, int r,
                            sdm_decode decode, float temperature, sdm_rng rng,
                            int32_t* tokens, float* logq, float* lse,
                            void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
@@ -170,7 +191,7 @@ sdm_status sdm_schedule_budget(const float* conf, int R, int gamma, const double
  *   n_i = budget[i] (budget == NULL: n_i = gamma, the static block)
  *   cu_seqlens[0] = 0, cu_seqlens[i+1] = cu_seqlens[i] + n_i + 1
  *   rows cu[i] .. cu[i] + n_i hold y_0 (anchor), y_1 .. y_{n_i}, with
- *   packed_req = i and packed_pos = 0..n_i; rows total .. tier-1 hold -1.
+ *   packed_req = i and packed_pos = 0..n_i; rows total .. capacity-1 hold -1.
  *   tier = smallest tiers[q] >= total; above every tier: tier = total and
  *   SDM_DEV_TIER_UNCAPTURED is set (the caller runs uncaptured).
  * In:  anchor [R], draft [R, gamma], budget [R] or NULL, tiers [n_tiers]

@@ -23,8 +23,9 @@ STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
 OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE = range(6)
 DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY = 1, 2, 4, 8, 16
 
-EXPORTS = ("sdm_workspace_size", "sdm_draft_chain", "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged",
-           "sdm_verify", "sdm_verify_tree", "sdm_status_str", "sdm_version")
+EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
+           "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
+           "sdm_status_str", "sdm_version")
 
 
 class SdmRng(ctypes.Structure):
@@ -41,9 +42,13 @@ def _declare(lib):
     lib.sdm_status_str.restype = ctypes.c_char_p
     lib.sdm_status_str.argtypes = [_I]
     lib.sdm_version.restype = _I
+    lib.sdm_markov_prepared_size.restype = _SZ
+    lib.sdm_markov_prepared_size.argtypes = [_I, _I]
+    lib.sdm_markov_prepare.restype = _I
+    lib.sdm_markov_prepare.argtypes = [_VP, _VP, _I, _I, _VP, _SZ, _VP]
     lib.sdm_draft_chain.restype = _I
-    lib.sdm_draft_chain.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, SdmRng, _VP, _VP, _VP, _VP, _SZ,
-                                    _VP, _VP]
+    lib.sdm_draft_chain.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, SdmRng, _VP, _VP, _VP, _VP,
+                                    _SZ, _VP, _VP]
     lib.sdm_draft_tree.restype = _I
     lib.sdm_draft_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP,
                                    _VP, _SZ, _VP, _VP]
@@ -118,8 +123,20 @@ def new_status(device="cuda"):
 
 
 # ---------------------------------------------------------------------------
+def markov_prepare(U, W, out=None):
+    """Prepared tables of the Markov head (W^T, row norms) for greedy drafting."""
+    _need_cuda(U, W)
+    V, r = U.shape
+    n = lib().sdm_markov_prepared_size(V, r)
+    if out is None:
+        out = torch.empty(int(n), dtype=torch.uint8, device=U.device)
+    st = lib().sdm_markov_prepare(_ptr(_u16(U)), _ptr(_u16(W)), V, r, _ptr(out), out.numel(), _stream())
+    _check(st, "sdm_markov_prepare")
+    return out
+
+
 def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0, out=None, ws=None,
-                dev_status=None):
+                dev_status=None, prepared=None):
     _need_cuda(L, U, W, anchor)
     R, B, V = L.shape
     r = U.shape[1]
@@ -130,7 +147,8 @@ def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0
                    lse=torch.zeros((R, B), dtype=torch.float32, device=dev))
     ws = workspace(OP_DRAFT_CHAIN, R, B, V, r, device=dev) if ws is None else ws
     dev_status = new_status(dev) if dev_status is None else dev_status
-    st = lib().sdm_draft_chain(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(anchor), R, B, V, r, decode,
+    st = lib().sdm_draft_chain(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(prepared), _ptr(anchor), R, B, V,
+                               r, decode,
                                float(temperature), SdmRng(seed, cycle), _ptr(out["tokens"]), _ptr(out["logq"]),
                                _ptr(out["lse"]), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
     _check(st, "sdm_draft_chain")

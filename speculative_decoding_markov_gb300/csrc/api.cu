@@ -89,20 +89,28 @@ inline int n_chunks_of(int V, int fp32) {
         if ((x) != cudaSuccess) return SDM_ERR_CUDA; \
     } while (0)
 
-size_t ws_chain(int R, int B) {
-    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(B) * R * kMaxGx * 8);
+size_t ws_chain_dense(int R, int B) {
+    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(B) * R * kMaxGx * 2 * 8);
 }
+
+// candidate lists of the pruned greedy chain (sized for the larger fp32 split)
+size_t ws_chain_pruned(int R, int B, int V) {
+    const size_t segs = static_cast<size_t>(R) * B * pruned_chunks(V, 1);
+    return align256(segs * kSegCap * 8) + align256(segs * 4) + align256(segs * 4);
+}
+
+size_t ws_chain(int R, int B, int V) { return std::max(ws_chain_dense(R, B), ws_chain_pruned(R, B, V)); }
 
 size_t ws_tree(int R, int B, int P) {
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
-    return align256(rows * kMaxGx * (2 + 2 * kMaxTopK) * 4) + 3 * align256(rows * 4) + align256(R * 4) +
+    return align256(rows * kMaxGx * 2 * (2 + 2 * kMaxTopK) * 4) + 3 * align256(rows * 4) + align256(R * 4) +
            4 * align256(pool * 4) + align256(R * 4);
 }
 
 size_t ws_verify(int R, int rows, int V) {
     const int nc = n_chunks_of(V, 0) > n_chunks_of(V, 1) ? n_chunks_of(V, 0) : n_chunks_of(V, 1);
-    return align256(static_cast<size_t>(rows) * 8) + align256(static_cast<size_t>(rows) * nc * 8) +
+    return align256(static_cast<size_t>(rows) * nc * 8) + align256(static_cast<size_t>(rows) * nc * 8) +
            6 * align256(static_cast<size_t>(R) * 4) + align256(static_cast<size_t>(R) * 8);
 }
 
@@ -115,10 +123,11 @@ size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int 
     (void)k;
     if (R <= 0) return 0;
     switch (op) {
-        case SDM_OP_DRAFT_CHAIN: return ws_chain(R, B);
+        case SDM_OP_DRAFT_CHAIN: return ws_chain(R, B, V);
         case SDM_OP_DRAFT_TREE: return ws_tree(R, B, P);
         case SDM_OP_VERIFY: return ws_verify(R, P, V);
-        case SDM_OP_VERIFY_TREE: return align256(static_cast<size_t>(R) * (N + 1) * 8);
+        case SDM_OP_VERIFY_TREE:
+            return align256(static_cast<size_t>(R) * (N + 1) * 8 * std::max(n_chunks_of(V, 0), n_chunks_of(V, 1)));
         default: return 0;
     }
 }
@@ -137,20 +146,71 @@ const char* sdm_status_str(sdm_status st) {
 
 int sdm_version(void) { return 100; }
 
+size_t sdm_markov_prepared_size(int V, int r) {
+    if (V <= 0 || r <= 0) return 0;
+    return align256(static_cast<size_t>(V) * r * 2) + align256(static_cast<size_t>(V) * 4) + 2 * 256;
+}
+
+sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, void* prepared,
+                              size_t prepared_bytes, void* stream) {
+    if (!U || !W || !prepared || V <= 0 || r <= 0) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(U) || !aligned16(W) || !aligned16(prepared))
+        return SDM_ERR_UNSUPPORTED;
+    if (prepared_bytes < sdm_markov_prepared_size(V, r)) return SDM_ERR_WORKSPACE;
+    Carver c{static_cast<uint8_t*>(prepared)};
+    uint16_t* Wt = c.take<uint16_t>(static_cast<size_t>(V) * r);
+    float* u_norm = c.take<float>(V);
+    float* n_max = c.take<float>(1);
+    float* u_max = c.take<float>(1);
+    SDM_CHECK_CUDA(launch_markov_prepare(U, W, V, r, Wt, u_norm, n_max, u_max, static_cast<cudaStream_t>(stream)));
+    return SDM_OK;
+}
+
 sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
-                           const int32_t* anchor, int R, int B, int V, int r, sdm_decode decode, float temperature,
-                           sdm_rng rng, int32_t* tokens, float* logq, float* lse, void* ws, size_t ws_bytes,
-                           int32_t* dev_status, void* stream) {
+                           const void* prepared, const int32_t* anchor, int R, int B, int V, int r,
+                           sdm_decode decode, float temperature, sdm_rng rng, int32_t* tokens, float* logq,
+                           float* lse, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
     if (!L || !U || !W || !anchor || !tokens || R <= 0 || B <= 0 || V <= 0 || r <= 0) return SDM_ERR_INVALID_ARG;
     if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
     if (decode != SDM_GREEDY && decode != SDM_SAMPLE) return SDM_ERR_INVALID_ARG;
     if (decode == SDM_SAMPLE && !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
     if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
-    if (!ws || ws_bytes < ws_chain(R, B)) return SDM_ERR_WORKSPACE;
+    if (!ws || ws_bytes < ws_chain(R, B, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (decode == SDM_GREEDY && prepared) {
+        // greedy by bound pruning: one cluster per request, all B steps in one launch
+        if (!aligned16(prepared)) return SDM_ERR_UNSUPPORTED;
+        const int n_chunks = pruned_chunks(V, dtL == SDM_FP32);
+        if (B > kMaxPickSteps || n_chunks > kMaxPickChunks) return SDM_ERR_UNSUPPORTED;
+        Carver pc{static_cast<uint8_t*>(const_cast<void*>(prepared))};
+        PrunedParams pp;
+        std::memset(&pp, 0, sizeof pp);
+        pp.L = L;
+        pp.l_fp32 = dtL == SDM_FP32;
+        pp.R = R;
+        pp.B = B;
+        pp.V = V;
+        pp.r = r;
+        pp.n_chunks = n_chunks;
+        pp.anchor = anchor;
+        pp.U = U;
+        pp.Wt = pc.take<uint16_t>(static_cast<size_t>(V) * r);
+        pp.u_norm = pc.take<float>(V);
+        pp.n_max = pc.take<float>(1);
+        pp.u_max = pc.take<float>(1);
+        Carver wc{static_cast<uint8_t*>(ws)};
+        const size_t segs = static_cast<size_t>(R) * B * n_chunks;
+        pp.cand = wc.take<uint2>(segs * kSegCap);
+        pp.cand_n = wc.take<int32_t>(segs);
+        pp.cmax = wc.take<float>(segs);
+        pp.tokens = tokens;
+        pp.dev_status = dev_status;
+        SDM_CHECK_CUDA(launch_chain_pruned(pp, s));
+        return SDM_OK;
+    }
     Carver c{static_cast<uint8_t*>(ws)};
     auto* keys = c.take<unsigned long long>(static_cast<size_t>(B) * R);
-    auto* lse_part = c.take<float2>(static_cast<size_t>(B) * R * kMaxGx);
+    auto* lse_part = c.take<float2>(static_cast<size_t>(B) * R * kMaxGx * 2);
 
     const int fp32 = dtL == SDM_FP32;
     const int l_rows = std::min(R, kTileM);
@@ -189,7 +249,7 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
         p.d = d;
         SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
     }
-    SDM_CHECK_CUDA(launch_chain_finalize(keys, lse_part, gx, R, B, V, r, L, fp32, U, W, anchor, p.inv_t,
+    SDM_CHECK_CUDA(launch_chain_finalize(keys, lse_part, 2 * gx, R, B, V, r, L, fp32, U, W, anchor, p.inv_t,
                                          decode == SDM_SAMPLE, tokens, logq, lse, dev_status, s));
     return SDM_OK;
 }
@@ -208,7 +268,7 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
     Carver c{static_cast<uint8_t*>(ws)};
-    float* tree_part = c.take<float>(rows * kMaxGx * (2 + 2 * kMaxTopK));
+    float* tree_part = c.take<float>(rows * kMaxGx * 2 * (2 + 2 * kMaxTopK));
     int32_t* front_tok = c.take<int32_t>(rows);
     int32_t* front_node = c.take<int32_t>(rows);
     float* front_score = c.take<float>(rows);
@@ -252,7 +312,7 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     for (int d = 1; d <= B; ++d) {
         p.d = d;
         SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE, tmW, tmL, p, gx, gy, s));
-        SDM_CHECK_CUDA(launch_tree_merge(tree_part, gx, R, P, k, B, d, front_tok, front_node, front_score, n_front,
+        SDM_CHECK_CUDA(launch_tree_merge(tree_part, 2 * gx, R, P, k, B, d, front_tok, front_node, front_score, n_front,
                                          pool_tok, pool_parent, pool_depth, pool_score, pool_n, s));
     }
     SDM_CHECK_CUDA(launch_tree_finalize(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok, parent,
@@ -309,7 +369,7 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     const int t_fp32 = dtT == SDM_FP32;
     const int nchunk_max = std::max(n_chunks_of(V, 0), n_chunks_of(V, 1));
     Carver c{static_cast<uint8_t*>(ws)};
-    auto* row_keys = c.take<unsigned long long>(row_capacity);
+    auto* row_keys = c.take<unsigned long long>(static_cast<size_t>(row_capacity) * nchunk_max);
     auto* lse_part = c.take<float2>(static_cast<size_t>(row_capacity) * nchunk_max);
     int32_t* res_tok = c.take<int32_t>(R);
     int32_t* res_pos = c.take<int32_t>(R);
@@ -332,9 +392,8 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
 
     if (decode == SDM_GREEDY) {
         sp.keys = row_keys;
-        SDM_CHECK_CUDA(launch_fill_u64(row_keys, row_capacity, 0ull, s));
         SDM_CHECK_CUDA(launch_stream(STREAM_ARGMAX, sp, row_capacity, s));
-        SDM_CHECK_CUDA(launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, row_keys, R, gamma, V, accept,
+        SDM_CHECK_CUDA(launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, row_keys, sp.n_chunks, R, gamma, V, accept,
                                                      ceiling, out_tok, n_out, dev_status, s));
         return SDM_OK;
     }
@@ -408,7 +467,8 @@ sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok
     if (dtT != SDM_BF16 && dtT != SDM_FP32) return SDM_ERR_INVALID_ARG;
     if (!vocab_ok(V) || !aligned16(target)) return SDM_ERR_UNSUPPORTED;
     const size_t rows = static_cast<size_t>(R) * (N + 1);
-    if (!ws || ws_bytes < align256(rows * 8)) return SDM_ERR_WORKSPACE;
+    const int nck = n_chunks_of(V, dtT == SDM_FP32);
+    if (!ws || ws_bytes < align256(rows * 8 * nck)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     auto* row_keys = static_cast<unsigned long long*>(ws);
     StreamParams sp;
@@ -421,9 +481,8 @@ sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok
     sp.n_items = static_cast<int>(rows);
     sp.keys = row_keys;
     sp.inv_t = 1.0f;
-    SDM_CHECK_CUDA(launch_fill_u64(row_keys, rows, 0ull, s));
     SDM_CHECK_CUDA(launch_stream(STREAM_ARGMAX, sp, static_cast<int>(rows), s));
-    SDM_CHECK_CUDA(launch_tree_verify_walk(row_keys, tok, parent, n_nodes, R, N, B, V, accept, out_tok, n_out,
+    SDM_CHECK_CUDA(launch_tree_verify_walk(row_keys, sp.n_chunks, tok, parent, n_nodes, R, N, B, V, accept, out_tok, n_out,
                                            dev_status, s));
     return SDM_OK;
 }

@@ -50,6 +50,12 @@ __device__ __forceinline__ uint32_t key_token(unsigned long long key) {
     return ~static_cast<uint32_t>(key & 0xffffffffull);
 }
 
+// The value an argmax key was built from (-0 comes back as +0).
+__device__ __forceinline__ float key_value(unsigned long long key) {
+    const uint32_t o = static_cast<uint32_t>(key >> 32);
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+}
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) {
     return a > b ? a : b;
 }

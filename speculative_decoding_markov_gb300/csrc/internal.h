@@ -16,7 +16,7 @@ namespace sdm {
 // ---------------------------------------------------------------------------
 constexpr int kTileM = 128;        // GEMM rows per CTA (TMEM lanes)
 constexpr int kTileN = 64;         // vocab ids per tile (one 128-byte bf16 swizzle span)
-constexpr int kGemmThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int kGemmThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int kMaxTopK = 8;
 
 enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3 };
@@ -37,10 +37,10 @@ struct GemmParams {
     const int32_t* anchor;
     // chain
     unsigned long long* keys;   // [B][R] argmax / race keys
-    float2* lse_part;           // [B][R][gridDim.x]
+    float2* lse_part;           // [B][R][gridDim.x][2] (one per column half)
     // tree
     const int32_t* front_tok;   // [R][P] frontier tokens (-1: empty slot)
-    float* tree_part;           // [rows][gridDim.x][2 + 2 * kMaxTopK]
+    float* tree_part;           // [rows][gridDim.x][2][2 + 2 * kMaxTopK]
     // residual (sample verify): one GEMM row per request
     const int32_t* res_tok;     // [R] previous token of the rejected position, -1: none
     const int32_t* res_pos;     // [R] rejected window position j (L row j, stream row j)
@@ -75,7 +75,7 @@ struct StreamParams {
     const int32_t* count;   // device item count (e.g. cu_seqlens + R), may be NULL
     const int32_t* row_of;  // item -> row index (NULL: identity; < 0: skip)
     float inv_t;
-    unsigned long long* keys;   // ARGMAX / BONUS: [n_items]
+    unsigned long long* keys;   // ARGMAX: [n_items][n_chunks] partial keys; BONUS: [n_items] (atomic max)
     float2* part;               // LSE: [n_items][n_chunks]
     // bonus race
     uint32_t rng_k0, rng_k1, rng_cycle;
@@ -103,7 +103,7 @@ cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32
                         int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s);
 
 cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
-                                          const unsigned long long* row_keys, int R, int gamma, int V,
+                                          const unsigned long long* row_keys, int n_chunks, int R, int gamma, int V,
                                           int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
                                           int32_t* dev_status, cudaStream_t s);
 
@@ -134,9 +134,40 @@ cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool
                                  const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
                                  int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
                                  int32_t* n_nodes, cudaStream_t s);
-cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, const int32_t* tok, const int32_t* parent,
+cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, int n_chunks, const int32_t* tok, const int32_t* parent,
                                     const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
                                     int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Greedy chain by bound pruning (one cluster of CTAs per request)
+// ---------------------------------------------------------------------------
+constexpr int kChunkBytes = 32 * 1024;         // bytes of a row of L per scan work item
+constexpr int kSegCap = 512;                   // listed ids per chunk
+constexpr int kMaxPickSteps = 64;              // B limit of the pruned chain
+constexpr int kMaxPickChunks = 64;             // chunks-per-row limit of the pruned chain
+
+struct PrunedParams {
+    const void* L;
+    int l_fp32;
+    int R, B, V, r;
+    int n_chunks;           // scan work items per row
+    const int32_t* anchor;
+    const uint16_t* U;      // [V, r]
+    const uint16_t* Wt;     // [V, r] (prepared)
+    const float* u_norm;    // [V] |U[v]|_2 rounded up (prepared)
+    const float* n_max;     // [1] max_v |W[:, v]|_2 rounded up (prepared)
+    const float* u_max;     // [1] max_v |U[v]|_2 rounded up (prepared)
+    uint2* cand;            // [R * B][n_chunks][kSegCap] listed (id, L bits)
+    int32_t* cand_n;        // [R * B][n_chunks] list lengths (true counts)
+    float* cmax;            // [R * B][n_chunks] chunk maxima
+    int32_t* tokens;        // [R, B]
+    int32_t* dev_status;
+};
+
+int pruned_chunks(int V, int l_fp32);
+cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s);
+cudaError_t launch_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, uint16_t* Wt, float* u_norm,
+                                  float* n_max, float* u_max, cudaStream_t s);
 
 int num_sms();
 

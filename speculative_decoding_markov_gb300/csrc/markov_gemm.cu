@@ -29,7 +29,7 @@
 namespace sdm {
 namespace {
 
-constexpr int kEpiWarps = 4;
+constexpr int kEpiWarps = 8;   // two per TMEM sub-partition: one per 32-column half
 constexpr int kSmemLimit = 232448;   // 227 KB opt-in per block
 
 struct SmemLayout {
@@ -143,31 +143,61 @@ __device__ __forceinline__ void load_g32(const void* base, int fp32, size_t off,
 template <int MODE>
 struct Epi;
 
+// Maximum of 32 values as a balanced tree (no serial dependency chain).
+__device__ __forceinline__ float max32(const float (&z)[32]) {
+    float t[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) t[j] = fmaxf(z[j], z[j + 16]);
+#pragma unroll
+    for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+        for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+    return t[0];
+}
+
+// Lowest j with z[j] == m (m is one of the z).
+__device__ __forceinline__ int first_index_of(const float (&z)[32], float m) {
+    int jj = 31;
+#pragma unroll
+    for (int j = 31; j >= 0; --j)
+        if (z[j] == m) jj = j;
+    return jj;
+}
+
+__device__ __forceinline__ void mask_tail(float (&z)[32], int vbase, int V) {
+    if (vbase + 32 > V) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (vbase + j >= V) z[j] = -INFINITY;
+    }
+}
+
 template <>
 struct Epi<MODE_CHAIN_GREEDY> {
     bool valid;
+    int half;
     float best;
     uint32_t best_v;
-    __device__ void init(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R;
         best = -INFINITY;
         best_v = 0;
     }
-    __device__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
                             const uint32_t (&acc)[32]) {
         if (!valid) return;
-        float lv[32];
-        load_l32(sl, lbb, p.l_fp32, lrow, h, lv);
+        float z[32];
+        load_l32(sl, lbb, p.l_fp32, lrow, h, z);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float z = lv[j] + __uint_as_float(acc[j]);     // fp32(L) + Markov, one rounding
-            if (z > best && vbase + j < p.V) {                   // strict: the lowest id keeps ties
-                best = z;
-                best_v = static_cast<uint32_t>(vbase + j);
-            }
+        for (int j = 0; j < 32; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
+        mask_tail(z, vbase, p.V);
+        const float m = max32(z);
+        if (m > best) {   // strict: an earlier (lower) id keeps a tie
+            best = m;
+            best_v = static_cast<uint32_t>(vbase + first_index_of(z, m));
         }
     }
-    __device__ void flush(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
         if (valid) atomicMax(&p.keys[static_cast<size_t>(p.d - 1) * p.R + grow], argmax_key(best, best_v));
     }
 };
@@ -175,11 +205,12 @@ struct Epi<MODE_CHAIN_GREEDY> {
 template <>
 struct Epi<MODE_CHAIN_SAMPLE> {
     bool valid;
+    int half;
     float best;
     uint32_t best_v;
     float m, s;
     RngKey key;
-    __device__ void init(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R;
         best = -INFINITY;
         best_v = 0;
@@ -187,7 +218,7 @@ struct Epi<MODE_CHAIN_SAMPLE> {
         s = 0.f;
         key = RngKey{p.rng_k0, p.rng_k1, p.rng_cycle};
     }
-    __device__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
                             const uint32_t (&acc)[32]) {
         if (!valid) return;
         float lv[32];
@@ -223,57 +254,68 @@ struct Epi<MODE_CHAIN_SAMPLE> {
             }
         }
     }
-    __device__ void flush(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
         if (!valid) return;
         const size_t o = static_cast<size_t>(p.d - 1) * p.R + grow;
         atomicMax(&p.keys[o], argmax_key(best, best_v));
-        p.lse_part[o * gridDim.x + blockIdx.x] = make_float2(m, s);
+        p.lse_part[(o * gridDim.x + blockIdx.x) * 2 + half] = make_float2(m, s);
     }
 };
 
 template <>
 struct Epi<MODE_TREE> {
     bool valid;
+    int half;
     float m, s;
+    float thresh;                 // current k-th best z (entry to the top-k)
     float tv[kMaxTopK];
     uint32_t ti[kMaxTopK];
-    __device__ void init(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.rows && p.front_tok[grow] >= 0;
         m = -INFINITY;
         s = 0.f;
+        thresh = -INFINITY;
 #pragma unroll
         for (int q = 0; q < kMaxTopK; ++q) {
             tv[q] = -INFINITY;
             ti[q] = 0xffffffffu;
         }
     }
-    __device__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
                             const uint32_t (&acc)[32]) {
         if (!valid) return;
-        float lv[32];
-        load_l32(sl, lbb, p.l_fp32, lrow / p.P, h, lv);
         float z[32];
-        float mx = -INFINITY;
+        load_l32(sl, lbb, p.l_fp32, lrow / p.P, h, z);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            z[j] = lv[j] + __uint_as_float(acc[j]);
-            if (vbase + j < p.V) mx = fmaxf(mx, z[j]);
-        }
+        for (int j = 0; j < 32; ++j) z[j] = z[j] + __uint_as_float(acc[j]);
+        mask_tail(z, vbase, p.V);
+        const float mx = max32(z);
         if (mx > m) {
             s *= __expf(m - mx);
             m = mx;
         }
-        const int k = p.k;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (vbase + j >= p.V) break;
-            s += __expf(z[j] - m);
-            if (z[j] > tv[k - 1]) {
-                float cz = z[j];
+        for (int j = 0; j < 32; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
+        s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        // The kernel keeps a sorted top-8 (value desc, lower id first); its first
+        // k entries are the top-k for any k <= 8.
+        if (mx > thresh) {   // some entry enters the top-8 (rare once it has filled)
+            uint32_t cand = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cand |= (z[j] > thresh ? 1u : 0u) << j;
+            while (cand) {
+                const int j = __ffs(cand) - 1;   // ascending ids: earlier ties stay ahead
+                cand &= cand - 1;
+                float cz = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj)
+                    if (jj == j) cz = z[jj];
+                if (!(cz > thresh)) continue;
                 uint32_t cv = static_cast<uint32_t>(vbase + j);
 #pragma unroll
                 for (int q = 0; q < kMaxTopK; ++q) {
-                    if (q < k && cz > tv[q]) {     // strict: earlier (lower id) ties stay ahead
+                    if (cz > tv[q]) {   // strict: earlier (lower id) ties stay ahead
                         const float tz = tv[q];
                         const uint32_t tiv = ti[q];
                         tv[q] = cz;
@@ -282,12 +324,13 @@ struct Epi<MODE_TREE> {
                         cv = tiv;
                     }
                 }
+                thresh = tv[kMaxTopK - 1];
             }
         }
     }
-    __device__ void flush(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
         if (!valid) return;
-        float* rec = p.tree_part + (static_cast<size_t>(grow) * gridDim.x + blockIdx.x) * (2 + 2 * kMaxTopK);
+        float* rec = p.tree_part + ((static_cast<size_t>(grow) * gridDim.x + blockIdx.x) * 2 + half) * (2 + 2 * kMaxTopK);
         rec[0] = m;
         rec[1] = s;
 #pragma unroll
@@ -301,13 +344,14 @@ struct Epi<MODE_TREE> {
 template <>
 struct Epi<MODE_RESID> {
     bool valid;
+    int half;
     float best;
     uint32_t best_v;
     int jpos;
     size_t l_off, t_off;
     float lse_q, lse_p;
     RngKey key;
-    __device__ void init(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R && p.res_tok[grow] >= 0;
         best = -INFINITY;
         best_v = 0;
@@ -320,7 +364,7 @@ struct Epi<MODE_RESID> {
             lse_p = p.res_lse_p[grow];
         }
     }
-    __device__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int lrow, int vbase, int,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int lrow, int vbase, int,
                             const uint32_t (&acc)[32]) {
         if (!valid) return;
         const int grow = lrow + blockIdx.y * kTileM;
@@ -350,7 +394,7 @@ struct Epi<MODE_RESID> {
             }
         }
     }
-    __device__ void flush(const GemmParams& p, int grow) {
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
         if (valid) atomicMax(&p.res_keys[grow], argmax_key(best, best_v));
     }
 };
@@ -372,9 +416,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row0 = blockIdx.y * kTileM;
-    const int t_begin = static_cast<int>((static_cast<long long>(blockIdx.x) * p.n_tiles) / gridDim.x);
-    const int t_end = static_cast<int>((static_cast<long long>(blockIdx.x + 1) * p.n_tiles) / gridDim.x);
-    const int nt = t_end - t_begin;
+    // vocab tiles are dealt round-robin (tile = blockIdx.x + i * gridDim.x) so
+    // that concurrently running CTAs read neighbouring 128-byte segments of
+    // every W and L row
+    const int nt = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
     // 1. gather A = U[tok(m)] for the 128 rows (K-major, 128-byte swizzle:
     //    16-byte chunk c of row m in K block kb sits at chunk c ^ (m & 7)).
@@ -429,7 +474,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
                 uint8_t* st = smem + lay.a_bytes + s * lay.stage_bytes;
                 mbar_arrive_expect_tx(&full[s], tx);
-                const int v0 = (t_begin + i) * kTileN;
+                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
                 tma_load_2d(st, &tmW, &full[s], v0, 0, pol_w);
                 if (MODE != MODE_RESID) {
                     uint8_t* sl = st + lay.w_bytes;
@@ -473,12 +518,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         __syncwarp();
     } else {
-        // 4. epilogue: thread = GEMM row (TMEM lane), 64 columns per tile
+        // 4. epilogue: thread = GEMM row (TMEM lane of its sub-partition
+        //    warp % 4); warps 2-5 take columns 0-31 of every tile, 6-9 32-63
         const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
         const int lrow = q * 32 + lane;
         const int grow = row0 + lrow;
         Epi<MODE> st;
         st.init(p, grow);
+        st.half = h;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         for (int i = 0; i < nt; ++i) {
             const int s = i % p.stages;
@@ -492,14 +540,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             tc_fence_after();
             const uint8_t* sl = smem + lay.a_bytes + s * lay.stage_bytes + lay.w_bytes;
-            const int v0 = (t_begin + i) * kTileN;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                uint32_t acc[32];
-                tmem_ld32(lane_addr + static_cast<uint32_t>(b * kTileN + h * 32), acc);
-                tmem_ld_wait();
-                st.consume(p, sl, lay.l_box_bytes, lrow, v0 + h * 32, h, acc);
-            }
+            const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+            uint32_t acc[32];
+            tmem_ld32(lane_addr + static_cast<uint32_t>(b * kTileN + h * 32), acc);
+            tmem_ld_wait();
+            st.consume(p, sl, lay.l_box_bytes, lrow, v0 + h * 32, h, acc);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {

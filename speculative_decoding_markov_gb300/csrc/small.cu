@@ -91,20 +91,42 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
     }
     __syncthreads();
     // bitonic sort, descending (S desc, then request asc, position asc)
-    for (int size = 2; size <= n_pad; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = tid; t < n_pad; t += kSchedThreads) {
-                const int u = t ^ stride;
-                if (u > t) {
-                    const bool desc = (t & size) == 0;
-                    const unsigned long long a = sk[t], b = sk[u];
-                    if (desc ? (a < b) : (a > b)) {
-                        sk[t] = b;
-                        sk[u] = a;
+    if (n_pad <= kSchedThreads) {
+        // one key per thread: partners closer than a warp swap by shuffle
+        unsigned long long key = tid < n_pad ? sk[tid] : 0ull;
+        for (int size = 2; size <= n_pad; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                unsigned long long other;
+                if (stride >= 32) {
+                    if (tid < n_pad) sk[tid] = key;
+                    __syncthreads();
+                    other = tid < n_pad ? sk[tid ^ stride] : 0ull;
+                    __syncthreads();
+                } else {
+                    other = __shfl_xor_sync(0xffffffffu, key, stride);
+                }
+                const bool desc = (tid & size) == 0, lower = (tid & stride) == 0;
+                key = (desc == lower) ? umax64(key, other) : (key < other ? key : other);
+            }
+        }
+        if (tid < n_pad) sk[tid] = key;
+        __syncthreads();
+    } else {
+        for (int size = 2; size <= n_pad; size <<= 1) {
+            for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                for (int t = tid; t < n_pad; t += kSchedThreads) {
+                    const int u = t ^ stride;
+                    if (u > t) {
+                        const bool desc = (t & size) == 0;
+                        const unsigned long long a = sk[t], b = sk[u];
+                        if (desc ? (a < b) : (a > b)) {
+                            sk[t] = b;
+                            sk[u] = a;
+                        }
                     }
                 }
+                __syncthreads();
             }
-            __syncthreads();
         }
     }
     // number of ranked survivals
@@ -119,15 +141,31 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
         const int t = tid * per + q;
         if (t < M) local += static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[t] >> 32)), 41));
     }
-    part[tid] = local;
-    __syncthreads();
-    if (tid == 0) {   // exclusive scan over the thread partials (1024 adds)
-        unsigned long long run = 0;
-        for (int q = 0; q < kSchedThreads; ++q) {
-            const unsigned long long v = part[q];
-            part[q] = run;
-            run += v;
+    // exclusive block scan of the thread partials (warp shuffles, then the
+    // 32 warp totals by warp 0); integer adds are exact in any order
+    {
+        const int lane = tid & 31, warp = tid >> 5;
+        unsigned long long x = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
         }
+        if (lane == 31) part[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long wv = part[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, wv, o);
+                if (lane >= o) wv += y;
+            }
+            part[lane] = wv;
+        }
+        __syncthreads();
+        const unsigned long long before = (warp > 0 ? part[warp - 1] : 0ull) + x - local;
+        __syncthreads();
+        part[tid] = before;
     }
     __syncthreads();
     // f(m) = E(m) / cost[R + m]; the greedy stops at the first m whose next
@@ -158,8 +196,10 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
     __syncthreads();
     for (int i = tid; i < R; i += kSchedThreads) budget[i] = cnt[i];
     if (tid == 0) {
-        unsigned long long sum = 0;
-        for (int t = 0; t < ms; ++t)
+        // prefix at m*: the owning thread's exclusive prefix plus its first entries
+        const int owner = ms / per < kSchedThreads ? ms / per : kSchedThreads - 1;
+        unsigned long long sum = part[owner];
+        for (int t = owner * per; t < ms; ++t)
             sum += static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[t] >> 32)), 41));
         *expected = static_cast<double>((static_cast<unsigned long long>(R) << 41) + sum) * 4.547473508864641e-13;
         *total_tokens = R + ms;
@@ -243,58 +283,77 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
         *tier = t;
     }
     __syncthreads();
-    const int end = s_tier < capacity ? s_tier : capacity;
-    for (int row = s_total + tid; row < end; row += kPackThreads) {
+    // every row past the packed total (the tier padding and the rest of the
+    // buffer) holds -1, so a consumer may read the whole buffer safely
+    for (int row = s_total + tid; row < capacity; row += kPackThreads) {
         ptok[row] = -1;
         preq[row] = -1;
         ppos[row] = -1;
     }
 }
 
+// Argmax token of a row from its per-chunk partial keys.
+__device__ __forceinline__ int row_token(const unsigned long long* part, size_t row, int n_chunks) {
+    unsigned long long k = 0;
+    for (int c = 0; c < n_chunks; ++c) k = umax64(k, part[row * n_chunks + c]);
+    return static_cast<int>(key_token(k));
+}
+
 // ---------------------------------------------------------------------------
 // greedy verification: first mismatch per request
 // ---------------------------------------------------------------------------
 __global__ void verify_greedy_finalize_kernel(int mode, const int32_t* cu, const int32_t* draft,
-                                              const int32_t* budget, const unsigned long long* row_keys, int R,
-                                              int gamma, int V, int32_t* accept, int32_t* ceiling,
+                                              const int32_t* budget, const unsigned long long* row_keys, int n_chunks,
+                                              int R, int gamma, int V, int32_t* accept, int32_t* ceiling,
                                               int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    // one warp per request: lane p resolves window rows p, p + 32, ...
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     if (i >= R) return;
     const int row0 = cu[i];
     int w = cu[i + 1] - row0 - 1;
     if (w < 0 || w > gamma) {
-        set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
         w = w < 0 ? 0 : gamma;
     }
     int cap = w;
     if (mode == SDM_CAP_ACCEPT) {
         cap = budget[i];
         if (cap < 0 || cap > w) {
-            set_status(dev_status, SDM_DEV_BAD_WINDOW);
+            if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
             cap = cap < 0 ? 0 : w;
         }
     }
     const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
+    // A = first p < w with y_{p+1} != argmax of row p, else w
     int A = w;
-    for (int p = 0; p < w; ++p) {
-        if (y[p] != static_cast<int>(key_token(row_keys[row0 + p]))) {
-            A = p;
-            break;
-        }
+    for (int base = 0; base < w && A == w; base += 32) {
+        const int p = base + lane;
+        const bool mism = p < w && y[p] != row_token(row_keys, static_cast<size_t>(row0 + p), n_chunks);
+        const unsigned bal = __ballot_sync(0xffffffffu, mism);
+        if (bal) A = base + __ffs(bal) - 1;
     }
     const int a = A < cap ? A : cap;
-    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
-    for (int p = 0; p < a; ++p) o[p] = y[p];
-    int t = static_cast<int>(key_token(row_keys[row0 + a]));
-    if (t < 0 || t >= V) {
-        set_status(dev_status, SDM_DEV_BAD_TOKEN);
-        t = 0;
+    for (int p = lane; p <= gamma; p += 32) {
+        if (p < a) {
+            o[p] = y[p];
+        } else if (p == a) {
+            int t = row_token(row_keys, static_cast<size_t>(row0 + a), n_chunks);
+            if (t < 0 || t >= V) {
+                set_status(dev_status, SDM_DEV_BAD_TOKEN);
+                t = 0;
+            }
+            o[p] = t;
+        } else {
+            o[p] = -1;
+        }
     }
-    o[a] = t;
-    for (int p = a + 1; p <= gamma; ++p) o[p] = -1;
-    accept[i] = a;
-    n_out[i] = a + 1;
-    if (ceiling) ceiling[i] = A;
+    if (lane == 0) {
+        accept[i] = a;
+        n_out[i] = a + 1;
+        if (ceiling) ceiling[i] = A;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -597,7 +656,8 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
     if (threadIdx.x == 0) n_nodes[i] = take + 1;
 }
 
-__global__ void tree_verify_walk_kernel(const unsigned long long* row_keys, const int32_t* tok, const int32_t* parent,
+__global__ void tree_verify_walk_kernel(const unsigned long long* row_keys, int n_chunks, const int32_t* tok,
+                                        const int32_t* parent,
                                         const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
                                         int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
@@ -612,7 +672,7 @@ __global__ void tree_verify_walk_kernel(const unsigned long long* row_keys, cons
     }
     int cur = 0, a = 0;
     for (;;) {
-        int t = static_cast<int>(key_token(row_keys[base + cur]));
+        int t = row_token(row_keys, base + cur, n_chunks);
         if (t < 0 || t >= V) {
             set_status(dev_status, SDM_DEV_BAD_TOKEN);
             t = 0;
@@ -680,10 +740,11 @@ cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32
 }
 
 cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
-                                          const unsigned long long* row_keys, int R, int gamma, int V,
+                                          const unsigned long long* row_keys, int n_chunks, int R, int gamma, int V,
                                           int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
                                           int32_t* dev_status, cudaStream_t s) {
-    verify_greedy_finalize_kernel<<<blocks_for(R, 128), 128, 0, s>>>(mode, cu, draft, budget, row_keys, R, gamma, V,
+    verify_greedy_finalize_kernel<<<blocks_for(static_cast<long long>(R) * 32, 128), 128, 0, s>>>(
+        mode, cu, draft, budget, row_keys, n_chunks, R, gamma, V,
                                                                       accept, ceiling, out_tok, n_out, dev_status);
     return cudaGetLastError();
 }
@@ -740,10 +801,10 @@ cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool
     return cudaGetLastError();
 }
 
-cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, const int32_t* tok, const int32_t* parent,
+cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, int n_chunks, const int32_t* tok, const int32_t* parent,
                                     const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
                                     int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s) {
-    tree_verify_walk_kernel<<<blocks_for(R, 64), 64, 0, s>>>(row_keys, tok, parent, n_nodes, R, N, B, V, accept,
+    tree_verify_walk_kernel<<<blocks_for(R, 64), 64, 0, s>>>(row_keys, n_chunks, tok, parent, n_nodes, R, N, B, V, accept,
                                                              out_tok, n_out, dev_status);
     return cudaGetLastError();
 }

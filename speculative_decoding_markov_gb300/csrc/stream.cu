@@ -136,7 +136,10 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
             if (threadIdx.x == 0) {
                 unsigned long long acc = red_key[0];
                 for (int q = 1; q < kThreads / 32; ++q) acc = umax64(acc, red_key[q]);
-                atomicMax(&p.keys[item], acc);
+                if (OP == STREAM_ARGMAX)
+                    p.keys[static_cast<size_t>(item) * p.n_chunks + chunk] = acc;   // one partial per chunk
+                else
+                    atomicMax(&p.keys[item], acc);
             }
             __syncthreads();
         }

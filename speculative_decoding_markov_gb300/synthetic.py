@@ -174,10 +174,11 @@ def gather_packed(target: torch.Tensor, packed_req: torch.Tensor, packed_pos: to
     """Stand-in for the target forward over the packed verify buffer.
 
     Copies row (packed_req[j], packed_pos[j]) of target [R, B+1, V] into packed
-    row j; padding rows (req = -1) receive row 0.
+    row j; padding rows (req = -1) receive row 0.  Indices are clamped into
+    range, so a buffer with unwritten tail entries cannot index out of bounds.
     """
     R, S, V = target.shape
-    idx = (packed_req.long().clamp(min=0) * S + packed_pos.long().clamp(min=0))
+    idx = packed_req.long().clamp(0, R - 1) * S + packed_pos.long().clamp(0, S - 1)
     flat = target.view(R * S, V)
     if out is None:
         return flat.index_select(0, idx)

@@ -60,7 +60,7 @@ def _chain(lib, **kw):
     a = dict(L=FAKE, dtL=0, U=FAKE, W=FAKE, anchor=FAKE, R=4, B=7, V=1024, r=64, dec=0, T=1.0, tokens=FAKE,
              ws=FAKE, ws_bytes=1 << 30)
     a.update(kw)
-    return lib.sdm_draft_chain(a["L"], a["dtL"], a["U"], a["W"], a["anchor"], a["R"], a["B"], a["V"], a["r"],
+    return lib.sdm_draft_chain(a["L"], a["dtL"], a["U"], a["W"], None, a["anchor"], a["R"], a["B"], a["V"], a["r"],
                                a["dec"], a["T"], binding.SdmRng(0, 0), a["tokens"], None, None, a["ws"],
                                a["ws_bytes"], None, None)
 
@@ -76,6 +76,13 @@ def test_draft_chain_host_validation(lib):
     assert _chain(lib, L=ctypes.c_void_p(0x1004)) == 2   # misaligned base
     assert _chain(lib, ws=None) == 5
     assert _chain(lib, ws_bytes=16) == 5
+
+
+def test_prepare_host_validation(lib):
+    assert lib.sdm_markov_prepared_size(151936, 256) >= 151936 * 256 * 2 + 151936 * 4
+    assert lib.sdm_markov_prepare(None, FAKE, 1024, 64, FAKE, 1 << 30, None) == 1
+    assert lib.sdm_markov_prepare(FAKE, FAKE, 1020, 64, FAKE, 1 << 30, None) == 2
+    assert lib.sdm_markov_prepare(FAKE, FAKE, 1024, 64, FAKE, 16, None) == 5
 
 
 def test_tree_and_verify_host_validation(lib):

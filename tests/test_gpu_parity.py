@@ -78,6 +78,71 @@ def test_draft_chain_greedy(case):
     np.testing.assert_array_equal(host(out["tokens"]), ref["tokens"])
 
 
+@pytest.mark.parametrize("case", CHAIN_CASES + [dict(R=3, B=4, V=151936, r=256, l_dtype=BF16),
+                                                dict(R=2, B=3, V=50000, r=64, l_dtype=FP32)],
+                         ids=lambda c: f"R{c['R']}B{c['B']}V{c['V']}r{c['r']}")
+def test_draft_chain_greedy_prepared(case):
+    """The bound-pruned greedy chain (prepared tables) against the oracle and
+    bit for bit against the dense tensor-core path."""
+    w = small(sigma=(0.5,), **case)
+    inp = synthetic.generate(w, seed=case["R"] * 7 + case["V"])
+    d = {k: dev(v) for k, v in inp.items()}
+    prep = sdm.markov_prepare(d["U"], d["W"])
+    pr = sdm.draft_chain(d["L"], d["U"], d["W"], d["anchor"], prepared=prep)
+    dn = sdm.draft_chain(d["L"], d["U"], d["W"], d["anchor"])
+    torch.cuda.synchronize()
+    assert int(pr["dev_status"].item()) == 0
+    ref = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    np.testing.assert_array_equal(host(pr["tokens"]), ref["tokens"])
+    assert torch.equal(pr["tokens"], dn["tokens"])
+
+
+def test_markov_prepare_tables():
+    w = small(R=1, B=1, V=1000, r=128, sigma=(0.5,))
+    inp = synthetic.generate(w, seed=2)
+    prep = sdm.markov_prepare(dev(inp["U"]), dev(inp["W"]))
+    torch.cuda.synchronize()
+    raw = prep.cpu()
+    V, r = w.V, w.r
+    wt = raw[: V * r * 2].view(torch.bfloat16).view(V, r)
+    assert torch.equal(wt, inp["W"].t().contiguous())
+    off = (V * r * 2 + 255) // 256 * 256
+    u_norm = raw[off: off + V * 4].view(torch.float32)
+    off2 = off + (V * 4 + 255) // 256 * 256
+    n_max = raw[off2: off2 + 4].view(torch.float32)
+    u_max = raw[off2 + 256: off2 + 260].view(torch.float32)
+    u_ref = inp["U"].double().norm(dim=1)
+    assert float(u_max) >= float(u_ref.max()) and float(u_max) <= float(u_ref.max()) * (1 + 1e-6)
+    assert torch.all(u_norm.double() >= u_ref) and torch.all(u_norm.double() <= u_ref * (1 + 1e-6) + 1e-30)
+    w_ref = inp["W"].double().norm(dim=0).max()
+    assert float(n_max) >= float(w_ref) and float(n_max) <= float(w_ref) * (1 + 1e-6)
+
+
+@pytest.mark.parametrize("kind", ["all_equal", "outlier", "ties", "wide_markov"])
+def test_draft_chain_prepared_adversarial(kind):
+    """Inputs that defeat the pruning bound (every id a candidate: many batches),
+    exact ties (lowest id wins) and a dominant Markov term."""
+    R, B, V, r = 3, 3, 8192, 64
+    w = small(R=R, B=B, V=V, r=r, l_dtype=BF16, sigma=(0.5,))
+    inp = synthetic.generate(w, seed=9)
+    L = inp["L"].clone()
+    if kind == "all_equal":
+        L[:] = 0.5
+    elif kind == "outlier":
+        L[:, :, 4321] = 50.0
+    elif kind == "ties":
+        L = torch.round(L.float() * 2).to(torch.bfloat16) / 2          # many exact ties
+    elif kind == "wide_markov":
+        L = (L.float() * 0.01).to(torch.bfloat16)                      # the Markov term decides
+    d = {k: dev(v) for k, v in inp.items()}
+    d["L"] = dev(L)
+    prep = sdm.markov_prepare(d["U"], d["W"])
+    pr = sdm.draft_chain(d["L"], d["U"], d["W"], d["anchor"], prepared=prep)
+    torch.cuda.synchronize()
+    ref = oracle.draft_chain(np_of(L), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    np.testing.assert_array_equal(host(pr["tokens"]), ref["tokens"])
+
+
 @pytest.mark.parametrize("case,T", [(dict(R=40, B=5, V=2056, r=64, l_dtype=BF16), 0.7),
                                     (dict(R=150, B=2, V=512, r=128, l_dtype=FP32), 1.3),
                                     (dict(R=3, B=3, V=8, r=64, l_dtype=FP32), 1.0)])
