@@ -255,6 +255,29 @@ sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok
                            int32_t* accept, int32_t* out_tok, int32_t* n_out,
                            void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/*
+ * verify_greedy_static: greedy verification (as sdm_verify with SDM_GREEDY)
+ * that allocates nothing and takes no workspace.  The pages have no
+ * counterpart; this entry point exists for callers that cannot hand the
+ * library scratch memory: a server that reserved all device memory up front,
+ * a framework whose allocator must account for every byte, or a latency-bound
+ * loop that cannot afford the device synchronisation of cudaMalloc/cudaFree.
+ * Scratch: a fixed 1 MiB array in the library's own device memory (every GPU
+ * that loads libsdm.so holds it until the process exits); row_capacity *
+ * ceil(V / 16384) (bf16 target) or row_capacity * ceil(V / 8192) (fp32) must
+ * be <= 131072, else SDM_ERR_WORKSPACE and nothing is launched.
+ * The first call on a device looks the array's device address up (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  All calls share the one array and each call fully rewrites what it
+ * reads, so nothing carries over between calls, but calls that overlap on the
+ * GPU (concurrent streams) race on it: serialise them.
+ * Arguments and outputs are those of sdm_verify.
+ */
+sdm_status sdm_verify_greedy_static(sdm_vmode mode, const void* target, sdm_dtype dtT, int row_capacity,
+                                    const int32_t* cu_seqlens, const int32_t* draft, const int32_t* budget,
+                                    int R, int gamma, int V, int32_t* accept, int32_t* ceiling,
+                                    int32_t* out_tok, int32_t* n_out, int32_t* dev_status, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* sdm_status_str(sdm_status status);
 

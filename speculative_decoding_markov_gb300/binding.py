@@ -25,7 +25,7 @@ DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY = 
 
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
-           "sdm_status_str", "sdm_version")
+           "sdm_verify_greedy_static", "sdm_status_str", "sdm_version")
 
 
 class SdmRng(ctypes.Structure):
@@ -59,6 +59,8 @@ def _declare(lib):
     lib.sdm_verify.restype = _I
     lib.sdm_verify.argtypes = [_I, _I, _F, SdmRng, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I,
                                _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+    lib.sdm_verify_greedy_static.restype = _I
+    lib.sdm_verify_greedy_static.argtypes = [_I, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_verify_tree.restype = _I
     lib.sdm_verify_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
 
