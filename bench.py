@@ -312,7 +312,7 @@ def run_ours(args, w, world, rank, local):
     t_total = t_front + t_verify
     # the draft's share of the front segment, from the eager split cycle
     t_draft = t_front * split_draft / max(split_draft + split_sched, 1e-9)
-    t_max = allreduce_max(t_total, world)
+    t_max, units = merge_ranks(t_total, [committed * args.steps, windows * args.steps], world)
     status = int(cyc.status.item())
 
     # roofline of the dominant kernel (algorithmic bytes / measured time)
@@ -351,7 +351,7 @@ def run_ours(args, w, world, rank, local):
     clk = clocks.summary(w0, w1)
     out = {
         "metric": METRIC,
-        "value": committed * args.steps * world / t_max,
+        "value": units[0] / t_max,
         "unit": UNIT,
         "n_gpus": world,
         "steps": args.steps,
@@ -371,7 +371,7 @@ def run_ours(args, w, world, rank, local):
                                   "eager_split_ms": {"draft": split_draft, "schedule+pack": split_sched}},
         "graphs": graphs,
         "tokens_per_step": {"committed": committed, "accepted_drafts": accepted, "verified_rows": windows},
-        "verified_rows_per_s": windows * args.steps * world / t_max,
+        "verified_rows_per_s": units[1] / t_max,
         "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
                      "algorithmic_bytes": {"draft_per_cycle": draft_bytes, "verify_per_cycle": verify_bytes}},
@@ -527,14 +527,19 @@ def barrier(world):
         dist.barrier()
 
 
-def allreduce_max(x, world):
+def merge_ranks(t_local, units_local, world):
+    """Whole-job figures of independent replicas: the slowest rank's timed
+    seconds and the units (tokens, rows) summed over all ranks.  Host scalars
+    only; the replicas exchange no data."""
     if world == 1:
-        return x
+        return t_local, list(units_local)
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64)
+    t = torch.tensor([t_local], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
+    u = torch.tensor(list(units_local), dtype=torch.float64)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), [float(x) for x in u.tolist()]
 
 
 def main():

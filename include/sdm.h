@@ -100,16 +100,25 @@ size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int 
 
 /*
  * markov_prepare: tables derived once from the Markov head (U, W), for the
- * greedy chain (no counterpart on the pages; a layout step, like packing a
- * weight matrix at load time).  Fills `prepared` (device, at least
- * sdm_markov_prepared_size(V, r) bytes, 256-byte aligned) with
- *   W^T [V, r] bf16, u_norm [V] fp32 = |U[v]|_2 and n_max fp32 =
- *   max_v |W[:, v]|_2, norms accumulated in fp64 and rounded up.
- * Enqueued on `stream`; valid until U or W change.
+ * greedy chain (no counterpart on the pages; a weight-preparation step, like
+ * packing a weight matrix at load time).  Fills `prepared` (device, at least
+ * sdm_markov_prepared_size(V, r) bytes, 256-byte aligned) with, in order,
+ * each array starting on a 256-byte boundary:
+ *   W^T [V, r] bf16;
+ *   c [V] fp32: c(y) bounds |U[y] . W[:, v]| over every v, for the exact
+ *     product and for any fp32 evaluation of it:
+ *       c(y) = A(y) (1 + 2^-10) + 4 r 2^-24 |U[y]|_2 max_v |W[:, v]|_2 + 2^-20
+ *     rounded up, A(y) = max_v |U[y] . W[:, v]| accumulated in fp32 by the
+ *     tensor cores (one V x V x r product, about 12 TFLOP at V = 151,936,
+ *     r = 256; nothing of it is stored);
+ *   |U[v]|_2 [V] fp32 (fp64 accumulation, rounded up); A [V] (scratch);
+ *   c_max = max_y c(y), max_v |W[:, v]|_2, max_v |U[v]|_2 (fp32 each).
+ * A pipeline wait that runs out sets SDM_DEV_TIMEOUT in *dev_status (may be
+ * NULL).  Enqueued on `stream`; valid until U or W change.
  */
 size_t sdm_markov_prepared_size(int V, int r);
 sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, void* prepared,
-                              size_t prepared_bytes, void* stream);
+                              size_t prepared_bytes, int32_t* dev_status, void* stream);
 
 /*
  * draft_chain: the Markov-head sequential stage ([DSpark notes] sec. 4,
@@ -128,13 +137,14 @@ sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r
  * Sampling (and greedy without prepared tables): the product U[y] . W runs on
  * the tcgen05 tensor cores (bf16 in, fp32 accumulate in TMEM) and the +L /
  * argmax / race is fused into its epilogue; z is never written to memory.
- * Greedy with prepared tables: since |U[y] . W[:, v]| <= |U[y]| max_v |W[:, v]|
- * = C(y), only ids with L[v] >= max L - 2 C(y) can win.  One HBM-bound pass
- * over all of L lists those ids for every (request, step) with the worst-case
- * C, then one CTA per request walks the B steps scoring only listed ids
- * exactly (from W^T).  L is read once and the result is the same argmax bit
- * for bit.  Needs B <= 64 and V <= 64 * 16384 (bf16 L) or 64 * 8192 (fp32 L),
- * else SDM_ERR_UNSUPPORTED.
+ * Greedy with prepared tables: since |U[y] . W[:, v]| <= c(y) for every v,
+ * only ids with L[v] >= max L - 2 c(y) can win.  One HBM-bound pass over all
+ * of L lists those ids for every (request, step) with the worst case c_max,
+ * then one CTA per request stages the listed rows of W^T and U in shared
+ * memory and walks the B steps, scoring exactly the ids that the previous
+ * token's c(y) leaves.  L is read once and the result is the same argmax bit
+ * for bit.  Needs B <= 64, V <= 64 * 16384 (bf16 L) or 64 * 8192 (fp32 L) and
+ * R * B * ceil(V / 16384 or 8192) <= 2^30, else SDM_ERR_UNSUPPORTED.
  */
 sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
                            const void* prepared, const int32_t* anchor, int R, int B, int V, int r,

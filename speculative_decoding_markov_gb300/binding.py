@@ -45,7 +45,7 @@ def _declare(lib):
     lib.sdm_markov_prepared_size.restype = _SZ
     lib.sdm_markov_prepared_size.argtypes = [_I, _I]
     lib.sdm_markov_prepare.restype = _I
-    lib.sdm_markov_prepare.argtypes = [_VP, _VP, _I, _I, _VP, _SZ, _VP]
+    lib.sdm_markov_prepare.argtypes = [_VP, _VP, _I, _I, _VP, _SZ, _VP, _VP]
     lib.sdm_draft_chain.restype = _I
     lib.sdm_draft_chain.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, SdmRng, _VP, _VP, _VP, _VP,
                                     _SZ, _VP, _VP]
@@ -125,14 +125,16 @@ def new_status(device="cuda"):
 
 
 # ---------------------------------------------------------------------------
-def markov_prepare(U, W, out=None):
-    """Prepared tables of the Markov head (W^T, row norms) for greedy drafting."""
+def markov_prepare(U, W, out=None, dev_status=None):
+    """Prepared tables of the Markov head (W^T, per-token bounds of the Markov
+    term) for greedy drafting."""
     _need_cuda(U, W)
     V, r = U.shape
     n = lib().sdm_markov_prepared_size(V, r)
     if out is None:
         out = torch.empty(int(n), dtype=torch.uint8, device=U.device)
-    st = lib().sdm_markov_prepare(_ptr(_u16(U)), _ptr(_u16(W)), V, r, _ptr(out), out.numel(), _stream())
+    st = lib().sdm_markov_prepare(_ptr(_u16(U)), _ptr(_u16(W)), V, r, _ptr(out), out.numel(), _ptr(dev_status),
+                                  _stream())
     _check(st, "sdm_markov_prepare")
     return out
 

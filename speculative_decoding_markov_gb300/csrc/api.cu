@@ -148,21 +148,50 @@ int sdm_version(void) { return 100; }
 
 size_t sdm_markov_prepared_size(int V, int r) {
     if (V <= 0 || r <= 0) return 0;
-    return align256(static_cast<size_t>(V) * r * 2) + align256(static_cast<size_t>(V) * 4) + 2 * 256;
+    return align256(static_cast<size_t>(V) * r * 2) + 3 * align256(static_cast<size_t>(V) * 4) + 3 * 256;
 }
 
 sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, void* prepared,
-                              size_t prepared_bytes, void* stream) {
+                              size_t prepared_bytes, int32_t* dev_status, void* stream) {
     if (!U || !W || !prepared || V <= 0 || r <= 0) return SDM_ERR_INVALID_ARG;
     if (!vocab_ok(V) || !rank_ok(r) || !aligned16(U) || !aligned16(W) || !aligned16(prepared))
         return SDM_ERR_UNSUPPORTED;
     if (prepared_bytes < sdm_markov_prepared_size(V, r)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     Carver c{static_cast<uint8_t*>(prepared)};
     uint16_t* Wt = c.take<uint16_t>(static_cast<size_t>(V) * r);
+    float* c_bound = c.take<float>(V);
     float* u_norm = c.take<float>(V);
+    unsigned int* absmax = c.take<unsigned int>(V);
+    float* c_max = c.take<float>(1);
     float* n_max = c.take<float>(1);
     float* u_max = c.take<float>(1);
-    SDM_CHECK_CUDA(launch_markov_prepare(U, W, V, r, Wt, u_norm, n_max, u_max, static_cast<cudaStream_t>(stream)));
+    SDM_CHECK_CUDA(launch_markov_prepare(U, W, V, r, Wt, u_norm, n_max, u_max, absmax, s));
+    // A(y) = max_v |U[y] . W[:, v]| for every token y: the Markov GEMM with
+    // GEMM row y = token y and an absolute-maximum epilogue
+    CUtensorMap tmW;
+    if (!map_w(&tmW, W, r, V)) return SDM_ERR_CUDA;
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = V;
+    p.R = V;
+    p.B = 1;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = (V + kTileN - 1) / kTileN;
+    p.l_rows = 1;
+    p.P = 1;
+    p.k = 1;
+    p.d = 1;
+    p.inv_t = 1.0f;
+    p.stages = gemm_pick_stages(r, 1, 0, MODE_ABSMAX);
+    p.U = U;
+    p.absmax_bits = absmax;
+    p.dev_status = dev_status;
+    const int gy = (V + kTileM - 1) / kTileM;
+    const int gx = gemm_grid_x(p.n_tiles, gy);
+    SDM_CHECK_CUDA(launch_markov_gemm(MODE_ABSMAX, tmW, tmW, p, gx, gy, s));
+    SDM_CHECK_CUDA(launch_markov_bounds(absmax, u_norm, n_max, V, r, c_bound, c_max, s));
     return SDM_OK;
 }
 
@@ -178,10 +207,11 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
     if (!ws || ws_bytes < ws_chain(R, B, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode == SDM_GREEDY && prepared) {
-        // greedy by bound pruning: one cluster per request, all B steps in one launch
+        // greedy by bound pruning: one scan of L, then one CTA per request walks the B steps
         if (!aligned16(prepared)) return SDM_ERR_UNSUPPORTED;
         const int n_chunks = pruned_chunks(V, dtL == SDM_FP32);
-        if (B > kMaxPickSteps || n_chunks > kMaxPickChunks) return SDM_ERR_UNSUPPORTED;
+        if (B > kMaxPickSteps || n_chunks > kMaxPickChunks || static_cast<long long>(R) * B * n_chunks > (1LL << 30))
+            return SDM_ERR_UNSUPPORTED;
         Carver pc{static_cast<uint8_t*>(const_cast<void*>(prepared))};
         PrunedParams pp;
         std::memset(&pp, 0, sizeof pp);
@@ -195,9 +225,10 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
         pp.anchor = anchor;
         pp.U = U;
         pp.Wt = pc.take<uint16_t>(static_cast<size_t>(V) * r);
-        pp.u_norm = pc.take<float>(V);
-        pp.n_max = pc.take<float>(1);
-        pp.u_max = pc.take<float>(1);
+        pp.c_bound = pc.take<float>(V);
+        pc.take<float>(V);           // |U[v]|
+        pc.take<unsigned int>(V);    // A(v)
+        pp.c_max = pc.take<float>(1);
         Carver wc{static_cast<uint8_t*>(ws)};
         const size_t segs = static_cast<size_t>(R) * B * n_chunks;
         pp.cand = wc.take<uint2>(segs * kSegCap);

@@ -1,32 +1,32 @@
 // chain_pruned.cu - the greedy Markov-head chain without the dense projection.
 //
 // Greedy drafting needs y_d = argmax_v z_d[v], z_d = fp32(L_d) + U[y_{d-1}] W.
-// The Markov term is bounded: |U[y] . W[:, v]| <= |U[y]|_2 |W[:, v]|_2 <= C(y)
-// with C(y) = u_norm[y] * n_max from the prepared tables (Cauchy-Schwarz), so
-// no id with L_d[v] < max_v L_d[v] - 2 C(y) can be the argmax.  Only the
-// threshold depends on the previous token, and C(y) <= C_max = u_max * n_max,
-// which splits the chain into two launches:
+// The Markov term of a previous token y is bounded over the whole vocabulary:
+// |U[y] . W[:, v]| <= c(y) for every v, with c(y) from the prepared tables
+// (the exact maximum max_v |U[y] . W[:, v]|, formed once on the tensor cores,
+// plus slack for rounding).  So no id with L_d[v] < max_v L_d[v] - 2 c(y) can
+// be the argmax.  Only that threshold depends on the previous token, and
+// c(y) <= c_max = max_y c(y), which splits the chain into two launches:
 //
 //   chain_scan_kernel  (every (request, step) row in parallel, HBM-bound)
-//     a cluster of CTAs per row copies the row L_d into shared memory (bulk
-//     TMA), reduces its maximum over the cluster through distributed shared
-//     memory and lists every id with L_d[v] >= max - 2 C_max.  L is read from
-//     HBM exactly once.
+//     a persistent grid walks 32 KB chunks of the rows of L; each CTA holds
+//     its chunk in registers, reduces the chunk maximum m_c and lists every
+//     id with L >= m_c - 2 c_max.  L is read from HBM exactly once.
 //   chain_pick_kernel  (one CTA per request, the B dependent steps)
-//     step d keeps the listed ids with L_d[v] >= max - 2 C(y_{d-1}) and scores
-//     them exactly, z = L + U[y_{d-1}] . W^T[v] (fp32, from the prepared W^T,
-//     whose rows were prefetched into L2), then takes the (z desc, id asc)
-//     winner.  A row whose list overflowed is rescanned in full.
+//     keeps the listed ids with L >= max_v L_d - 2 c_max (the ids any
+//     previous token can need), copies their W^T rows and U rows into shared
+//     memory, then walks the steps: step d scores the ids with
+//     L >= max - 2 c(y_{d-1}) exactly, z = L + U[y_{d-1}] . W^T[v] (fp32), and
+//     takes the (z desc, id asc) winner; one barrier per step.  Steps whose
+//     lists overflowed, or that do not fit in shared memory, score from global
+//     memory (a full-row scan when a list overflowed).
 //
 // The result equals the dense argmax bit for bit: the kept set contains every
 // id that can reach the maximum and the kept ids are scored exactly.
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "device.cuh"
 #include "internal.h"
-
-namespace cg = cooperative_groups;
 
 namespace sdm {
 namespace {
@@ -69,19 +69,9 @@ __device__ __forceinline__ void fold_max(const uint4& x, uint4& acc) {
     }
 }
 
-template <int FP32>
-__device__ __forceinline__ float vec_max(const uint4& x) {
-    float v[FP32 ? 4 : 8];
-    unpack<FP32>(x, v);
-    float m = v[0];
-#pragma unroll
-    for (int q = 1; q < (FP32 ? 4 : 8); ++q) m = fmaxf(m, v[q]);
-    return m;
-}
-
 // Maximum of one 16-byte vector: a packed bf16x2 tree, two conversions at the end.
 template <int FP32>
-__device__ __forceinline__ float vec_max_packed(const uint4& x) {
+__device__ __forceinline__ float vec_max(const uint4& x) {
     if (FP32)
         return fmaxf(fmaxf(__uint_as_float(x.x), __uint_as_float(x.y)), fmaxf(__uint_as_float(x.z), __uint_as_float(x.w)));
     __nv_bfloat162 w[4];
@@ -92,12 +82,13 @@ __device__ __forceinline__ float vec_max_packed(const uint4& x) {
     return fmaxf(__uint_as_float(b << 16), __uint_as_float(b & 0xffff0000u));
 }
 
+// Start of row (request `row`, step d) of L at id v.
 __device__ __forceinline__ const uint8_t* row_ptr(const PrunedParams& p, int row, int d, int v) {
     const size_t esz = p.l_fp32 ? 4 : 2;
     return static_cast<const uint8_t*>(p.L) + ((static_cast<size_t>(row) * p.B + (d - 1)) * p.V + v) * esz;
 }
 
-// Bulk (non-tensor) TMA copy global -> shared, completing on an mbarrier.
+// Bulk (non-tensor) copy global -> shared, completing on an mbarrier.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                      smem_u32(dst)),
@@ -105,15 +96,8 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                  : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
-// The bound C on |Markov(prev)| with slack for the fp32 rounding of the
-// product, and the candidate threshold below a row maximum m.
-__device__ __forceinline__ float bound_c(float norm_u, float n_max) {
-    return norm_u * n_max * 1.0009765625f + 9.5367431640625e-7f;
-}
+// The candidate threshold below a row maximum m for a Markov bound c, with
+// slack for the fp32 rounding of fp32(L) + Markov.
 __device__ __forceinline__ float threshold(float m, float c) {
     return m - 2.0f * c - fabsf(m) * 9.765625e-4f - 9.5367431640625e-7f;
 }
@@ -121,38 +105,44 @@ __device__ __forceinline__ float threshold(float m, float c) {
 // ---------------------------------------------------------------------------
 // A: candidate lists of every (request, step, chunk)
 // ---------------------------------------------------------------------------
-// Work item = kChunkIds consecutive ids of one row L_d (32 KB); a persistent
-// grid walks the items.  Each thread holds 8 16-byte vectors of the chunk in
+// Work item = kChunkBytes of one row L_d; row-major items, a persistent grid
+// strides over them.  Each thread holds 8 16-byte vectors of the chunk in
 // registers, the chunk maximum m_c is reduced over the CTA, and every id with
-// L >= m_c - 2 C_max is listed.  m_c <= max_v L_d[v] and C(y) <= C_max, so the
-// list holds every id the exact step can need.
+// L >= m_c - 2 c_max is listed.  m_c <= max_v L_d[v] and c(y) <= c_max, so
+// the list holds every id an exact step can need.
 template <int FP32>
-__global__ void __launch_bounds__(kThreads) chain_scan_kernel(const PrunedParams p) {
+__global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedParams p) {
     constexpr int VEC = FP32 ? 4 : 8;
+    constexpr int ESZ = FP32 ? 4 : 2;
     constexpr int VPT = kChunkBytes / 16 / kThreads;        // vectors per thread
+    constexpr int CHUNK_IDS = kChunkBytes / ESZ;
     __shared__ float s_wmax[kWarps];
     __shared__ int s_cnt;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int chunk_ids = kChunkBytes / (FP32 ? 4 : 2);
-    const long long items = static_cast<long long>(p.R) * p.B * p.n_chunks;
-    const float cmax = bound_c(*p.u_max, *p.n_max);
-    for (long long it = blockIdx.x; it < items; it += gridDim.x) {
-        const int rs = static_cast<int>(it / p.n_chunks);
-        const int c = static_cast<int>(it % p.n_chunks);
-        const int row = rs / p.B, d = rs % p.B + 1;
-        const int v0 = c * chunk_ids;
-        const int n_vec = (min(p.V, v0 + chunk_ids) - v0) / VEC;
-        const uint4* src = reinterpret_cast<const uint4*>(row_ptr(p, row, d, v0));
-        {   // this CTA's next item starts moving from HBM into L2 now
-            const long long nx = it + gridDim.x;
-            if (nx < items) {
-                const int nrs = static_cast<int>(nx / p.n_chunks), nc = static_cast<int>(nx % p.n_chunks);
-                const int nv0 = nc * chunk_ids;
-                const int nbytes = (min(p.V, nv0 + chunk_ids) - nv0) * (FP32 ? 4 : 2);
-                const char* nsrc = reinterpret_cast<const char*>(row_ptr(p, nrs / p.B, nrs % p.B + 1, nv0));
-                for (int off = threadIdx.x * 128; off < nbytes; off += kThreads * 128)
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(nsrc + off));
-            }
+    const int nc = p.n_chunks;
+    const int items = p.R * p.B * nc;       // <= 2^30 (checked by the host)
+    const float cmax = *p.c_max;
+    // item it = rs * nc + c, rs = request * B + (d - 1): walk (rs, c) by the
+    // grid stride without dividing per item
+    int it = blockIdx.x;
+    int rs = it / nc, c = it - rs * nc;
+    const int srs = gridDim.x / nc, sc = gridDim.x - srs * nc;
+    const uint8_t* L = static_cast<const uint8_t*>(p.L);
+    while (it < items) {
+        int nrs = rs + srs, ncc = c + sc;
+        if (ncc >= nc) {
+            ncc -= nc;
+            ++nrs;
+        }
+        const int v0 = c * CHUNK_IDS;
+        const int n_vec = (min(p.V, v0 + CHUNK_IDS) - v0) / VEC;
+        const uint4* src = reinterpret_cast<const uint4*>(L + (static_cast<size_t>(rs) * p.V + v0) * ESZ);
+        if (it + static_cast<int>(gridDim.x) < items) {   // this CTA's next item starts moving into L2 now
+            const int nv0 = ncc * CHUNK_IDS;
+            const int nbytes = (min(p.V, nv0 + CHUNK_IDS) - nv0) * ESZ;
+            const char* nsrc = reinterpret_cast<const char*>(L + (static_cast<size_t>(nrs) * p.V + nv0) * ESZ);
+            for (int off = threadIdx.x * 128; off < nbytes; off += kThreads * 128)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(nsrc + off));
         }
         uint4 x[VPT];
 #pragma unroll
@@ -175,12 +165,12 @@ __global__ void __launch_bounds__(kThreads) chain_scan_kernel(const PrunedParams
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) mc = fmaxf(mc, s_wmax[w]);
         const float T = threshold(mc, cmax);
-        const size_t seg = static_cast<size_t>(rs) * p.n_chunks + c;
-        uint2* out = p.cand + seg * kSegCap;
-        if (tmax >= T) {
+        const int seg = rs * nc + c;
+        uint2* out = p.cand + static_cast<size_t>(seg) * kSegCap;
+        if (tmax >= T) {   // only threads holding a candidate
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                if (vec_max_packed<FP32>(x[k]) < T) continue;
+                if (vec_max<FP32>(x[k]) < T) continue;
                 float v[VEC];
                 unpack<FP32>(x[k], v);
                 const int i = threadIdx.x + k * kThreads;
@@ -199,19 +189,69 @@ __global__ void __launch_bounds__(kThreads) chain_scan_kernel(const PrunedParams
             p.cand_n[seg] = s_cnt;        // the true count: above kSegCap the list is incomplete
             p.cmax[seg] = mc;
         }
+        it += gridDim.x;
+        rs = nrs;
+        c = ncc;
     }
 }
 
 // ---------------------------------------------------------------------------
 // B: the B dependent steps of each request
 // ---------------------------------------------------------------------------
-constexpr int kGroup = 8;       // candidates a warp scores per round
-constexpr int kPickCap = 1024;  // ids staged per step (more: the full-row path)
-constexpr int kStageEntries = 16384;   // listed ids of one request held in shared memory
+constexpr int kGroup = 8;              // candidates a warp scores per round (global path)
+constexpr int kPickCap = 1024;         // ids per scoring batch of the global path
+constexpr int kListCap = 4096;         // listed ids of one request held in shared memory
+constexpr int kRowCapMax = 192;        // staged candidates (W^T row + U row each)
+constexpr int kPickSmem = 200 * 1024;  // dynamic shared memory of the pick kernel
 
-// Warp-cooperative exact scores of the staged ids: lanes hold 8 of r; a warp
-// scores kGroup ids per round with all their W^T row loads in flight.
-__device__ __forceinline__ unsigned long long score_staged(const PrunedParams& p, const uint2* ids, int n,
+struct PickLayout {
+    uint32_t cm, cn, soff, st_key, st_c, st_w, st_u, total;
+    int cap;
+};
+
+__host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
+
+__host__ __device__ inline PickLayout pick_layout(int B, int nc, int r) {
+    PickLayout l;
+    const uint32_t nseg = static_cast<uint32_t>(B) * static_cast<uint32_t>(nc);
+    l.cm = kListCap * 8u;
+    l.cn = al16(l.cm + nseg * 4u);
+    l.soff = al16(l.cn + nseg * 4u);
+    const uint32_t fixed = al16(l.soff + (nseg + 1u) * 4u);
+    const uint32_t per = 8u + 4u + 4u * static_cast<uint32_t>(r);   // key, bound, W^T row, U row
+    int cap = static_cast<int>((kPickSmem - fixed - 64u) / per);
+    cap = cap < kRowCapMax ? cap : kRowCapMax;
+    l.cap = cap;
+    l.st_key = fixed;
+    l.st_c = al16(l.st_key + static_cast<uint32_t>(cap) * 8u);
+    l.st_w = al16(l.st_c + static_cast<uint32_t>(cap) * 4u);
+    l.st_u = l.st_w + static_cast<uint32_t>(cap) * 2u * r;
+    l.total = l.st_u + static_cast<uint32_t>(cap) * 2u * r;
+    return l;
+}
+
+// U row slice of a lane: elements [8 lane, 8 lane + 8) of a row that may sit
+// in shared or global memory (generic address); zero past r.
+__device__ __forceinline__ void load_ub(const uint16_t* urow, int lane, int r, float (&ub)[8]) {
+    const uint4 u = lane * 8 < r ? *reinterpret_cast<const uint4*>(urow + lane * 8) : make_uint4(0, 0, 0, 0);
+    unpack<0>(u, ub);
+}
+
+// U[y] . w for the lane slices, summed over the warp (every lane gets the sum).
+__device__ __forceinline__ float warp_dot(const uint4& w, const float (&ub)[8]) {
+    float a[8];
+    unpack<0>(w, a);
+    float acc = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc = fmaf(a[q], ub[q], acc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    return acc;
+}
+
+// Global path: warp-cooperative exact scores of staged ids; a warp scores
+// kGroup ids per round with all their W^T row loads in flight.
+__device__ __forceinline__ unsigned long long score_global(const PrunedParams& p, const uint2* ids, int n,
                                                            const float (&ub)[8], int warp, int lane) {
     unsigned long long best = 0ull;
     for (int c0 = warp * kGroup; c0 < n; c0 += kWarps * kGroup) {
@@ -224,30 +264,14 @@ __device__ __forceinline__ unsigned long long score_staged(const PrunedParams& p
             wv[j] = ok ? __ldg(reinterpret_cast<const uint4*>(p.Wt + static_cast<size_t>(cd[j].x) * p.r) + lane)
                        : make_uint4(0, 0, 0, 0);
         }
-        float acc[kGroup];
 #pragma unroll
         for (int j = 0; j < kGroup; ++j) {
-            float a[8];
-            unpack<0>(wv[j], a);
-            acc[j] = 0.f;
-#pragma unroll
-            for (int q = 0; q < 8; ++q) acc[j] = fmaf(a[q], ub[q], acc[j]);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int j = 0; j < kGroup; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
-#pragma unroll
-        for (int j = 0; j < kGroup; ++j)
+            const float dot = warp_dot(wv[j], ub);
             if (cd[j].x < static_cast<uint32_t>(p.V))
-                best = umax64(best, argmax_key(__uint_as_float(cd[j].y) + acc[j], cd[j].x));   // fp32(L) + Markov
+                best = umax64(best, argmax_key(__uint_as_float(cd[j].y) + dot, cd[j].x));   // fp32(L) + Markov
+        }
     }
     return best;
-}
-
-__device__ __forceinline__ void prefetch_row_l2(const uint16_t* base, uint32_t v, int r) {
-    const char* a = reinterpret_cast<const char*>(base + static_cast<size_t>(v) * r);
-    for (int off = 0; off < r * 2; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(a + off));
 }
 
 template <int FP32>
@@ -255,27 +279,41 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     constexpr int VEC = FP32 ? 4 : 8;
     const int row = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nc = p.n_chunks, B = p.B, r = p.r;
+    const int nseg = B * nc;
+    const PickLayout lay = pick_layout(B, nc, r);
     extern __shared__ __align__(16) uint8_t s_dyn[];
-    const int nc = p.n_chunks;
-    const int nseg = p.B * nc;
-    uint2* s_list = reinterpret_cast<uint2*>(s_dyn);               // [kStageEntries] all lists, packed
-    float* s_cm = reinterpret_cast<float*>(s_list + kStageEntries); // [B][nc] chunk maxima
-    int* s_cn = reinterpret_cast<int*>(s_cm + nseg);               // [B][nc] list lengths
-    int* s_soff = s_cn + nseg;                                     // [B * nc + 1] packed offsets
+    uint2* s_list = reinterpret_cast<uint2*>(s_dyn);              // [kListCap] all lists, packed
+    float* s_cm = reinterpret_cast<float*>(s_dyn + lay.cm);        // [B][nc] chunk maxima
+    int* s_cn = reinterpret_cast<int*>(s_dyn + lay.cn);            // [B][nc] list lengths
+    int* s_soff = reinterpret_cast<int*>(s_dyn + lay.soff);        // [B * nc + 1] packed list offsets
+    uint2* st_key = reinterpret_cast<uint2*>(s_dyn + lay.st_key);  // [cap] staged (id, L bits)
+    float* st_c = reinterpret_cast<float*>(s_dyn + lay.st_c);      // [cap] c(id)
+    uint16_t* st_w = reinterpret_cast<uint16_t*>(s_dyn + lay.st_w);   // [cap][r] W^T rows
+    uint16_t* st_u = reinterpret_cast<uint16_t*>(s_dyn + lay.st_u);   // [cap][r] U rows
     __shared__ __align__(8) uint64_t s_bar;
-    __shared__ int s_staged;
-    __shared__ uint4 s_u[32];
-    __shared__ uint2 s_cand[kPickCap];       // this step's ids with L >= max - 2C
-    __shared__ uint2 s_ids[kPickCap];        // the ids of one scoring round
+    __shared__ __align__(16) uint16_t s_u0[256];                   // U[anchor]
     __shared__ float s_lmax[kMaxPickSteps];
-    __shared__ int s_off[kMaxPickChunks + 1];
-    __shared__ int s_n, s_m, s_over, s_prev;
+    __shared__ int s_scnt[kMaxPickSteps];                          // staged ids of each step
+    __shared__ int s_sbeg[kMaxPickSteps + 1];                      // their first slot (-1: not staged)
+    __shared__ int s_over[kMaxPickSteps];                          // a list of the step overflowed
+    __shared__ int s_lists_in_smem;
+    __shared__ unsigned long long s_wbest[2][kWarps];
+    __shared__ int s_wslot[2][kWarps];
+    __shared__ uint2 s_ids[kPickCap];
+    __shared__ int s_m;
     __shared__ unsigned long long s_best;
-    const float n_max = *p.n_max;
-    const float cmax = bound_c(*p.u_max, n_max);
-    const size_t seg0 = static_cast<size_t>(row) * nseg;
+    const float cmax = *p.c_max;
+    const int seg0 = row * nseg;
 
-    // chunk maxima and list lengths of every step, once
+    int prev = p.anchor[row];
+    if (prev < 0 || prev >= p.V) {
+        if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+        prev = 0;
+    }
+    // 1. U[anchor] (async), chunk maxima and list lengths of every step
+    if (threadIdx.x * 8 < r) cp_async_16(s_u0 + threadIdx.x * 8, p.U + static_cast<size_t>(prev) * r + threadIdx.x * 8, 16u);
+    float cprev = p.c_bound[prev];
     if (threadIdx.x == 0) {
         mbar_init(&s_bar, 1);
         fence_mbar_init();
@@ -285,26 +323,56 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
         s_cn[i] = p.cand_n[seg0 + i];
     }
     __syncthreads();
-    // every list of this request into shared memory by bulk copies (each
-    // list padded to an even length so that copies are 16-byte multiples)
-    if (threadIdx.x == 0) {
+    // 2. warp 0: packed list offsets (lists padded to even lengths so that the
+    //    bulk copies are 16-byte multiples) and the copies; the other warps:
+    //    row maxima and overflow flags of every step
+    if (warp == 0) {
         int run = 0;
-        for (int i = 0; i < nseg; ++i) {
-            s_soff[i] = run;
-            run += (min(s_cn[i], kSegCap) + 1) & ~1;
+        for (int i0 = 0; i0 < nseg; i0 += 32) {
+            const int i = i0 + lane;
+            const int n = i < nseg ? (min(s_cn[i], kSegCap) + 1) & ~1 : 0;
+            int x = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (i < nseg) s_soff[i] = run + x - n;
+            run += __shfl_sync(0xffffffffu, x, 31);
         }
-        s_soff[nseg] = run;
-        s_staged = run <= kStageEntries;
-        if (s_staged && run > 0) {
-            mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(run) * 8u);
-            for (int i = 0; i < nseg; ++i) {
-                const uint32_t n = static_cast<uint32_t>(s_soff[i + 1] - s_soff[i]) * 8u;
-                if (n) bulk_load(s_list + s_soff[i], p.cand + (seg0 + i) * kSegCap, n, &s_bar);
+        if (lane == 0) {
+            s_soff[nseg] = run;
+            const int fits = run <= kListCap;
+            s_lists_in_smem = fits;
+            if (fits && run > 0) {
+                mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(run) * 8u);
+                for (int i = 0; i < nseg; ++i) {
+                    const int n = (min(s_cn[i], kSegCap) + 1) & ~1;
+                    if (n) bulk_load(s_list + s_soff[i], p.cand + static_cast<size_t>(seg0 + i) * kSegCap,
+                                     static_cast<uint32_t>(n) * 8u, &s_bar);
+                }
+            }
+        }
+    } else {
+        for (int d = warp - 1; d < B; d += kWarps - 1) {
+            float m = -INFINITY;
+            int over = 0;
+            for (int c = lane; c < nc; c += 32) {
+                m = fmaxf(m, s_cm[d * nc + c]);
+                over |= s_cn[d * nc + c] > kSegCap;
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            over = __any_sync(0xffffffffu, over);
+            if (lane == 0) {
+                s_lmax[d] = m;
+                s_over[d] = over;
             }
         }
     }
     __syncthreads();
-    if (s_staged && s_soff[nseg] > 0) {
+    const bool lists_in_smem = s_lists_in_smem;
+    if (lists_in_smem && s_soff[nseg] > 0) {
         const bool ok = mbar_wait(&s_bar, 0);
         if (!__syncthreads_and(ok) && threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_TIMEOUT);
         for (int i = threadIdx.x; i < nseg; i += kThreads) {   // the padding slot is not an id
@@ -313,149 +381,179 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
         }
         __syncthreads();
     }
-    for (int d = warp; d < p.B; d += kWarps) {
-        float m = -INFINITY;
-        for (int c = lane; c < nc; c += 32) m = fmaxf(m, s_cm[d * nc + c]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) s_lmax[d] = m;
-    }
-    __syncthreads();
-    // the likely winners of every step (L >= max - C_max): their W^T rows, and
-    // their U rows for the next step, into L2
-    if (s_staged) {
-        for (int d = 0; d < p.B; ++d) {
-            const float cut = s_lmax[d] - cmax;
-            for (int t = s_soff[d * nc] + threadIdx.x; t < s_soff[(d + 1) * nc]; t += kThreads) {
-                const uint2 en = s_list[t];
-                if (en.x >= static_cast<uint32_t>(p.V) || __uint_as_float(en.y) < cut) continue;
-                prefetch_row_l2(p.Wt, en.x, p.r);
-                if (d + 1 < p.B) prefetch_row_l2(p.U, en.x, p.r);
+    // 3. stage, step by step, the listed ids with L >= max - 2 c_max: count
+    //    (warp per step), assign slots in step order, compact, then copy their
+    //    W^T rows, U rows (steps < B: the next step's possible previous token)
+    //    and bounds into shared memory
+    if (lists_in_smem) {
+        for (int d = warp; d < B; d += kWarps) {
+            const float t = threshold(s_lmax[d], cmax);
+            int cnt = 0;
+            for (int e = s_soff[d * nc] + lane; e < s_soff[(d + 1) * nc]; e += 32) {
+                const uint2 en = s_list[e];
+                cnt += en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= t;
             }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+            if (lane == 0) s_scnt[d] = cnt;
         }
-    }
-    int prev = p.anchor[row];
-    if (prev < 0 || prev >= p.V) {
-        if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
-        prev = 0;
-    }
-    for (int d = 1; d <= p.B; ++d) {
-        const int ds = (d - 1) * nc;
-        if (warp == 0 && lane * 8 < p.r)
-            s_u[lane] = __ldg(reinterpret_cast<const uint4*>(p.U + static_cast<size_t>(prev) * p.r) + lane);
-        if (warp == 1) {   // list offsets of this step (exclusive scan over the chunks)
-            int over = 0, run = 0;
-            for (int c0 = 0; c0 < nc; c0 += 32) {
-                const int c = c0 + lane;
-                const int n = c < nc ? s_cn[ds + c] : 0;
-                over |= __any_sync(0xffffffffu, n > kSegCap);
-                int x = n;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += y;
-                }
-                if (c < nc) s_off[c] = run + x - n;
-                run += __shfl_sync(0xffffffffu, x, 31);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int run = 0;
+            for (int d = 0; d < B; ++d) {
+                const bool fits = !s_over[d] && run + s_scnt[d] <= lay.cap;
+                s_sbeg[d] = fits ? run : -1;
+                if (fits) run += s_scnt[d];
             }
-            if (lane == 0) {
-                s_off[nc] = run;
-                s_over = over;
-                s_n = 0;
-                s_best = 0ull;
+            s_sbeg[B] = run;
+        }
+        __syncthreads();
+        for (int d = warp; d < B; d += kWarps) {
+            if (s_sbeg[d] < 0) continue;
+            const float t = threshold(s_lmax[d], cmax);
+            int base = s_sbeg[d];
+            for (int e0 = s_soff[d * nc]; e0 < s_soff[(d + 1) * nc]; e0 += 32) {
+                const int e = e0 + lane;
+                uint2 en = make_uint2(0xffffffffu, 0u);
+                if (e < s_soff[(d + 1) * nc]) en = s_list[e];
+                const bool keep = en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= t;
+                const unsigned bal = __ballot_sync(0xffffffffu, keep);
+                if (keep) st_key[base + __popc(bal & ((1u << lane) - 1u))] = en;
+                base += __popc(bal);
             }
         }
         __syncthreads();
-        const float C = bound_c(p.u_norm[prev], n_max);
+        const int n_st = s_sbeg[B];
+        const int cpr = r >> 3;   // 16-byte pieces per row
+        for (int i = threadIdx.x; i < n_st * cpr; i += kThreads) {
+            const int j = i / cpr, q = i - j * cpr;
+            const uint32_t v = st_key[j].x;
+            cp_async_16(st_w + static_cast<size_t>(j) * r + q * 8, p.Wt + static_cast<size_t>(v) * r + q * 8, 16u);
+            cp_async_16(st_u + static_cast<size_t>(j) * r + q * 8, p.U + static_cast<size_t>(v) * r + q * 8, 16u);
+        }
+        for (int j = threadIdx.x; j < n_st; j += kThreads) st_c[j] = p.c_bound[st_key[j].x];
+    } else {
+        for (int d = threadIdx.x; d <= B; d += kThreads) s_sbeg[d] = d < B ? -1 : 0;
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // 4. the steps
+    const uint16_t* urow = s_u0;   // U[y_{d-1}]: shared (staged) or global
+    for (int d = 1; d <= B; ++d) {
+        const int ds = (d - 1) * nc;
         const float lmax = s_lmax[d - 1];
-        const float tall = threshold(lmax, C);   // every id that can win has L >= tall
-        // stage this step's ids with L >= tall (from the lists, or from the row)
-        int m = 0;
-        if (!s_over) {
-            if (s_staged) {
-                for (int t = s_soff[ds] + threadIdx.x; t < s_soff[ds + nc]; t += kThreads) {
-                    const uint2 en = s_list[t];
-                    if (en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= tall) {
-                        const int slot = atomicAdd(&s_n, 1);
-                        if (slot < kPickCap) s_cand[slot] = en;
+        const float tall = threshold(lmax, cprev);   // every id that can win has L >= tall
+        float ub[8];
+        load_ub(urow, lane, r, ub);
+        const int par = d & 1;
+        const int sb = s_sbeg[d - 1];
+        unsigned long long win;
+        int win_slot = -1;
+        if (sb >= 0) {
+            // staged: each warp scores its share of the step's staged ids
+            unsigned long long best = 0ull;
+            int bslot = -1;
+            const int n = s_scnt[d - 1];
+            for (int j = sb + warp; j < sb + n; j += kWarps) {
+                const uint2 en = st_key[j];
+                const float lv = __uint_as_float(en.y);
+                if (lv < tall) continue;   // warp-uniform
+                const uint4 w = lane * 8 < r ? *reinterpret_cast<const uint4*>(st_w + static_cast<size_t>(j) * r + lane * 8)
+                                             : make_uint4(0, 0, 0, 0);
+                const unsigned long long k = argmax_key(lv + warp_dot(w, ub), en.x);
+                if (k > best) {
+                    best = k;
+                    bslot = j;
+                }
+            }
+            if (lane == 0) {
+                s_wbest[par][warp] = best;
+                s_wslot[par][warp] = bslot;
+            }
+            __syncthreads();
+            win = s_wbest[par][0];
+            win_slot = s_wslot[par][0];
+#pragma unroll
+            for (int w = 1; w < kWarps; ++w) {
+                const unsigned long long k = s_wbest[par][w];
+                if (k > win) {
+                    win = k;
+                    win_slot = s_wslot[par][w];
+                }
+            }
+        } else {
+            // global path
+            if (threadIdx.x == 0) s_best = 0ull;
+            if (!s_over[d - 1]) {
+                // the step's list entries in windows of kPickCap, ids with L >= tall scored
+                const int e_beg = lists_in_smem ? s_soff[ds] : 0;
+                int e_end;
+                if (lists_in_smem) {
+                    e_end = s_soff[ds + nc];
+                } else {
+                    e_end = 0;
+                    for (int c = 0; c < nc; ++c) e_end += min(s_cn[ds + c], kSegCap);
+                }
+                for (int w0 = e_beg; w0 < e_end; w0 += kPickCap) {
+                    if (threadIdx.x == 0) s_m = 0;
+                    __syncthreads();
+                    for (int e = w0 + threadIdx.x; e < min(e_end, w0 + kPickCap); e += kThreads) {
+                        uint2 en;
+                        if (lists_in_smem) {
+                            en = s_list[e];
+                        } else {   // entry e of the step's lists, chunk by chunk
+                            int c = 0, off = e;
+                            while (off >= min(s_cn[ds + c], kSegCap)) off -= min(s_cn[ds + c++], kSegCap);
+                            en = p.cand[static_cast<size_t>(seg0 + ds + c) * kSegCap + off];
+                        }
+                        if (en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= tall)
+                            s_ids[atomicAdd(&s_m, 1)] = en;
                     }
+                    __syncthreads();
+                    const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
+                    if (lane == 0 && b) atomicMax(&s_best, b);
+                    __syncthreads();
                 }
             } else {
-                const int total = s_off[nc];
-                for (int t = threadIdx.x; t < total; t += kThreads) {
-                    int c = 0;
-                    while (s_off[c + 1] <= t) ++c;
-                    const uint2 en = p.cand[(seg0 + ds + c) * kSegCap + (t - s_off[c])];
-                    if (__uint_as_float(en.y) >= tall) {
-                        const int slot = atomicAdd(&s_n, 1);
-                        if (slot < kPickCap) s_cand[slot] = en;
+                // a list overflowed: scan the whole row in batches (exact for any input)
+                const uint4* src = reinterpret_cast<const uint4*>(row_ptr(p, row, d, 0));
+                const int nv = p.V / VEC;
+                for (int c0 = 0; c0 < nv; c0 += kPickCap / VEC) {
+                    if (threadIdx.x == 0) s_m = 0;
+                    __syncthreads();
+                    for (int i = c0 + threadIdx.x; i < min(nv, c0 + kPickCap / VEC); i += kThreads) {
+                        float v[VEC];
+                        unpack<FP32>(__ldg(src + i), v);
+#pragma unroll
+                        for (int q = 0; q < VEC; ++q)
+                            if (v[q] >= tall)
+                                s_ids[atomicAdd(&s_m, 1)] = make_uint2(static_cast<uint32_t>(i * VEC + q), __float_as_uint(v[q]));
                     }
+                    __syncthreads();
+                    const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
+                    if (lane == 0 && b) atomicMax(&s_best, b);
+                    __syncthreads();
                 }
             }
             __syncthreads();
-            m = s_n;
-            if (m > kPickCap) {
-                if (threadIdx.x == 0) s_over = 1;
-                __syncthreads();
-            }
+            win = s_best;
         }
-        float ub[8];
-        unpack<0>(lane * 8 < p.r ? s_u[lane] : make_uint4(0, 0, 0, 0), ub);
-        if (!s_over) {
-            // Any id that can reach the maximum z* has L >= z* - C.  Round 1
-            // scores the staged ids with L >= max - C (z* >= their best z1);
-            // round 2 those with z1 - C <= L < max - C.
-            float lo = threshold(lmax, 0.5f * C), hi = INFINITY;
-            for (int round = 0; round < 2; ++round) {
-                if (threadIdx.x == 0) s_m = 0;
-                __syncthreads();
-                for (int t = threadIdx.x; t < m; t += kThreads) {
-                    const float lv = __uint_as_float(s_cand[t].y);
-                    if (lv >= lo && lv < hi) s_ids[atomicAdd(&s_m, 1)] = s_cand[t];
-                }
-                __syncthreads();
-                unsigned long long b = score_staged(p, s_ids, s_m, ub, warp, lane);
-                b = warp_max_u64(b);
-                if (lane == 0 && b) atomicMax(&s_best, b);
-                __syncthreads();
-                const unsigned long long k = s_best;
-                hi = lo;
-                lo = threshold(k ? key_value(k) : -INFINITY, 0.5f * C);
-                if (!(lo < hi)) break;
-            }
+        int y = static_cast<int>(key_token(win));
+        if (win == 0ull || y < 0 || y >= p.V) {
+            if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+            y = 0;
+            win_slot = -1;
+        }
+        if (threadIdx.x == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
+        if (d == B) break;
+        if (win_slot >= 0) {   // the winner's U row and bound were staged with it
+            urow = st_u + static_cast<size_t>(win_slot) * r;
+            cprev = st_c[win_slot];
         } else {
-            // a list overflowed: scan the whole row in batches (exact for any input)
-            const uint4* src = reinterpret_cast<const uint4*>(row_ptr(p, row, d, 0));
-            const int nv = p.V / VEC;
-            for (int c0 = 0; c0 < nv; c0 += kPickCap / VEC) {
-                if (threadIdx.x == 0) s_m = 0;
-                __syncthreads();
-                for (int i = c0 + threadIdx.x; i < min(nv, c0 + kPickCap / VEC); i += kThreads) {
-                    float v[VEC];
-                    unpack<FP32>(__ldg(src + i), v);
-#pragma unroll
-                    for (int q = 0; q < VEC; ++q)
-                        if (v[q] >= tall)
-                            s_ids[atomicAdd(&s_m, 1)] = make_uint2(static_cast<uint32_t>(i * VEC + q), __float_as_uint(v[q]));
-                }
-                __syncthreads();
-                unsigned long long b = score_staged(p, s_ids, s_m, ub, warp, lane);
-                b = warp_max_u64(b);
-                if (lane == 0 && b) atomicMax(&s_best, b);
-                __syncthreads();
-            }
+            urow = p.U + static_cast<size_t>(y) * r;
+            cprev = p.c_bound[y];
         }
-        if (threadIdx.x == 0) {
-            int y = static_cast<int>(key_token(s_best));
-            if (y < 0 || y >= p.V) {
-                set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
-                y = 0;
-            }
-            p.tokens[static_cast<size_t>(row) * p.B + (d - 1)] = y;
-            s_prev = y;
-        }
-        __syncthreads();
-        prev = s_prev;
     }
 }
 
@@ -498,6 +596,22 @@ __global__ void row_norm_kernel(const uint16_t* T, int V, int r, float* out, uns
     }
 }
 
+// c(y) = A(y) (1 + 2^-10) + 4 r 2^-24 |U[y]| max_v |W[:, v]| + 2^-20, rounded
+// up, where A(y) = max_v |U[y] . W[:, v]| as the tensor cores accumulated it.
+// Any fp32 evaluation of a dot product of length r differs from the exact
+// one by at most about r 2^-24 |U[y]| |W[:, v]|, so 4 r 2^-24 |U| max|W|
+// covers both the tensor-core maximum and the pick kernel's own dot products.
+__global__ void bounds_kernel(const unsigned int* absmax_bits, const float* u_norm, const float* n_max, int V, int r,
+                              float* c_bound, unsigned int* c_max_bits) {
+    const int y = blockIdx.x * blockDim.x + threadIdx.x;
+    if (y >= V) return;
+    const double a = static_cast<double>(__uint_as_float(absmax_bits[y]));
+    const double slack = 4.0 * r * 5.9604644775390625e-8 * static_cast<double>(u_norm[y]) * static_cast<double>(*n_max);
+    const float c = __double2float_ru(a * (1.0 + 9.765625e-4) + slack + 9.5367431640625e-7);
+    c_bound[y] = c;
+    atomicMax(c_max_bits, __float_as_uint(c));
+}
+
 }  // namespace
 
 int pruned_chunks(int V, int l_fp32) {
@@ -507,6 +621,7 @@ int pruned_chunks(int V, int l_fp32) {
 
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
     const long long items = static_cast<long long>(p.R) * p.B * p.n_chunks;
+    if (items > (1LL << 30)) return cudaErrorInvalidValue;
     const int grid = static_cast<int>(items < 8LL * num_sms() ? items : 8LL * num_sms());
     if (p.l_fp32)
         chain_scan_kernel<1><<<grid, kThreads, 0, s>>>(p);
@@ -514,36 +629,46 @@ cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
         chain_scan_kernel<0><<<grid, kThreads, 0, s>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const size_t smem = static_cast<size_t>(kStageEntries) * 8 + static_cast<size_t>(p.B) * p.n_chunks * 12 + 16;
+    const PickLayout lay = pick_layout(p.B, p.n_chunks, p.r);
+    if (lay.cap < 1) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(chain_pick_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
+        e = cudaFuncSetAttribute(chain_pick_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPickSmem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(chain_pick_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            e = cudaFuncSetAttribute(chain_pick_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPickSmem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
     if (p.l_fp32)
-        chain_pick_kernel<1><<<p.R, kThreads, smem, s>>>(p);
+        chain_pick_kernel<1><<<p.R, kThreads, lay.total, s>>>(p);
     else
-        chain_pick_kernel<0><<<p.R, kThreads, smem, s>>>(p);
+        chain_pick_kernel<0><<<p.R, kThreads, lay.total, s>>>(p);
     return cudaGetLastError();
 }
 
 cudaError_t launch_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, uint16_t* Wt, float* u_norm,
-                                  float* n_max, float* u_max, cudaStream_t s) {
+                                  float* n_max, float* u_max, unsigned int* absmax_bits, cudaStream_t s) {
     transpose_kernel<<<dim3((V + 31) / 32, (r + 31) / 32), dim3(32, 8), 0, s>>>(W, r, V, Wt);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(n_max, 0, sizeof(float), s);
     if (e == cudaSuccess) e = cudaMemsetAsync(u_max, 0, sizeof(float), s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(absmax_bits, 0, static_cast<size_t>(V) * sizeof(unsigned int), s);
     if (e != cudaSuccess) return e;
     const int blocks = (V * 32 + 255) / 256;
     row_norm_kernel<<<blocks, 256, 0, s>>>(U, V, r, u_norm, reinterpret_cast<unsigned int*>(u_max));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     row_norm_kernel<<<blocks, 256, 0, s>>>(Wt, V, r, nullptr, reinterpret_cast<unsigned int*>(n_max));
+    return cudaGetLastError();
+}
+
+cudaError_t launch_markov_bounds(const unsigned int* absmax_bits, const float* u_norm, const float* n_max, int V,
+                                 int r, float* c_bound, float* c_max, cudaStream_t s) {
+    cudaError_t e = cudaMemsetAsync(c_max, 0, sizeof(float), s);
+    if (e != cudaSuccess) return e;
+    bounds_kernel<<<(V + 255) / 256, 256, 0, s>>>(absmax_bits, u_norm, n_max, V, r, c_bound,
+                                                  reinterpret_cast<unsigned int*>(c_max));
     return cudaGetLastError();
 }
 

@@ -19,7 +19,10 @@ constexpr int kTileN = 64;         // vocab ids per tile (one 128-byte bf16 swiz
 constexpr int kGemmThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
 constexpr int kMaxTopK = 8;
 
-enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3 };
+enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3, MODE_ABSMAX = 4 };
+
+// Modes that stage a tile of L beside each W tile.
+__host__ __device__ constexpr bool mode_reads_l(int mode) { return mode != MODE_RESID && mode != MODE_ABSMAX; }
 
 struct GemmParams {
     int rows;            // GEMM rows in use
@@ -52,6 +55,8 @@ struct GemmParams {
     int t_fp32;                 // target element type
     int gamma;
     unsigned long long* res_keys;   // [R]
+    // absmax (prepared tables): GEMM row m = token m
+    unsigned int* absmax_bits;      // [rows] max_v |U[m] . W[:, v]| as fp32 bits (atomic max)
     int32_t* dev_status;
 };
 
@@ -139,7 +144,8 @@ cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, int n_ch
                                     int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
-// Greedy chain by bound pruning (one cluster of CTAs per request)
+// Greedy chain by bound pruning: a scan of every row of L, then one CTA per
+// request walks the B steps
 // ---------------------------------------------------------------------------
 constexpr int kChunkBytes = 32 * 1024;         // bytes of a row of L per scan work item
 constexpr int kSegCap = 512;                   // listed ids per chunk
@@ -154,9 +160,8 @@ struct PrunedParams {
     const int32_t* anchor;
     const uint16_t* U;      // [V, r]
     const uint16_t* Wt;     // [V, r] (prepared)
-    const float* u_norm;    // [V] |U[v]|_2 rounded up (prepared)
-    const float* n_max;     // [1] max_v |W[:, v]|_2 rounded up (prepared)
-    const float* u_max;     // [1] max_v |U[v]|_2 rounded up (prepared)
+    const float* c_bound;   // [V] bound on |Markov(y)| over the vocabulary (prepared)
+    const float* c_max;     // [1] max_y c_bound[y] (prepared)
     uint2* cand;            // [R * B][n_chunks][kSegCap] listed (id, L bits)
     int32_t* cand_n;        // [R * B][n_chunks] list lengths (true counts)
     float* cmax;            // [R * B][n_chunks] chunk maxima
@@ -166,8 +171,12 @@ struct PrunedParams {
 
 int pruned_chunks(int V, int l_fp32);
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s);
+// Prepared tables, step 1: W^T, |U[v]|, max |W[:, v]| and max |U[v]|; zeroes
+// absmax_bits for the absmax GEMM.  Step 2 (after that GEMM): the bounds.
 cudaError_t launch_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, uint16_t* Wt, float* u_norm,
-                                  float* n_max, float* u_max, cudaStream_t s);
+                                  float* n_max, float* u_max, unsigned int* absmax_bits, cudaStream_t s);
+cudaError_t launch_markov_bounds(const unsigned int* absmax_bits, const float* u_norm, const float* n_max, int V,
+                                 int r, float* c_bound, float* c_max, cudaStream_t s);
 
 int num_sms();
 

@@ -9,6 +9,8 @@
 //   MODE_CHAIN_SAMPLE  exponential race on z / T + log-sum-exp partials
 //   MODE_TREE          log-sum-exp partials + local top-k by z  (PCTree)
 //   MODE_RESID         race over max(0, p - q) at a rejected position
+//   MODE_ABSMAX        max_v |U[m] . W[:, v]| for m = 0..V-1, no L (the
+//                      per-token bound of the pruned greedy chain)
 //
 // Data path (one CTA = 128 GEMM rows x a contiguous range of 64-wide vocab
 // tiles, K = r):
@@ -19,10 +21,12 @@
 //     [rows x 64] (TMA 3-D, evict_first) through an S-stage mbarrier ring;
 //   * warp 1 issues r/16 tcgen05.mma (M=128, N=64, K=16, bf16 -> fp32) per
 //     tile into one of two 64-column TMEM accumulators;
-//   * warps 2-5 drain the accumulator with tcgen05.ld (thread = GEMM row),
-//     add L and run the mode's reduction in registers; one result per row
-//     and CTA is written at the end.
-// The grid is (vocab splits) x (M tiles), one CTA per SM.
+//   * warps 2-9 drain the accumulator with tcgen05.ld (thread = GEMM row;
+//     warps 2-5 take columns 0-31 of every tile, warps 6-9 columns 32-63),
+//     add L and run the mode's reduction in registers; one result per row,
+//     CTA and column half is written at the end.
+// The grid is (vocab splits) x (M tiles), one CTA per SM; vocab tiles are
+// dealt to the splits round-robin.
 #include "device.cuh"
 #include "internal.h"
 
@@ -41,7 +45,7 @@ __host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32,
     s.a_bytes = static_cast<uint32_t>(kTileM) * static_cast<uint32_t>(r) * 2u;
     s.w_bytes = static_cast<uint32_t>(r) * 128u;
     s.l_box_bytes = (static_cast<uint32_t>(l_rows) * 128u + 1023u) & ~1023u;
-    s.l_bytes = (mode == MODE_RESID) ? 0u : s.l_box_bytes * (l_fp32 ? 2u : 1u);
+    s.l_bytes = mode_reads_l(mode) ? s.l_box_bytes * (l_fp32 ? 2u : 1u) : 0u;
     s.stage_bytes = s.w_bytes + s.l_bytes;
     s.bar_off = s.a_bytes + static_cast<uint32_t>(stages) * s.stage_bytes;
     s.total = s.bar_off + static_cast<uint32_t>(2 * stages + 4) * 8u + 16u + 1024u;
@@ -61,6 +65,8 @@ __device__ __forceinline__ int gemm_row_token(const GemmParams& p, int grow) {
         if (grow >= p.rows) return -1;
         t = p.front_tok[grow];
         if (t < 0) return -1;
+    } else if (MODE == MODE_ABSMAX) {
+        return grow < p.rows ? grow : -1;
     } else {
         if (grow >= p.R) return -1;
         t = p.res_tok[grow];
@@ -399,6 +405,35 @@ struct Epi<MODE_RESID> {
     }
 };
 
+template <>
+struct Epi<MODE_ABSMAX> {
+    bool valid;
+    int half;
+    float best;
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
+        valid = grow < p.rows;
+        best = 0.f;
+    }
+    // Columns past V hold 0 (the W tile's out-of-range fill), which never
+    // raises a maximum of absolute values.
+    __device__ __forceinline__ void consume(const GemmParams&, const uint8_t*, uint32_t, int, int, int,
+                                            const uint32_t (&acc)[32]) {
+        float t[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            t[j] = fmaxf(fabsf(__uint_as_float(acc[j])), fabsf(__uint_as_float(acc[j + 16])));
+#pragma unroll
+        for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+        best = fmaxf(best, t[0]);
+    }
+    // the bits of non-negative floats order like their values
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
+        if (valid) atomicMax(&p.absmax_bits[grow], __float_as_uint(best));
+    }
+};
+
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     markov_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmL,
@@ -445,7 +480,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmW);
-        if (MODE != MODE_RESID) tma_prefetch_desc(&tmL);
+        if (mode_reads_l(MODE)) tma_prefetch_desc(&tmL);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 2 * kTileN);
@@ -464,7 +499,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t pol_w = policy_evict_last();
             const uint64_t pol_l = policy_evict_first();
             const uint32_t tx =
-                lay.w_bytes + (MODE == MODE_RESID ? 0u : static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u));
+                lay.w_bytes + (mode_reads_l(MODE) ? static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u) : 0u);
             const int lrow0 = (MODE == MODE_TREE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
             for (int i = 0; i < nt; ++i) {
                 const int s = i % p.stages;
@@ -476,7 +511,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 mbar_arrive_expect_tx(&full[s], tx);
                 const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
                 tma_load_2d(st, &tmW, &full[s], v0, 0, pol_w);
-                if (MODE != MODE_RESID) {
+                if (mode_reads_l(MODE)) {
                     uint8_t* sl = st + lay.w_bytes;
                     tma_load_3d(sl, &tmL, &full[s], v0, p.d - 1, lrow0, pol_l);
                     if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &full[s], v0 + 32, p.d - 1, lrow0, pol_l);
@@ -597,6 +632,7 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
         case MODE_CHAIN_SAMPLE: return launch_mode<MODE_CHAIN_SAMPLE>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TREE: return launch_mode<MODE_TREE>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_RESID: return launch_mode<MODE_RESID>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_ABSMAX: return launch_mode<MODE_ABSMAX>(tmW, tmL, p, grid_x, grid_y, s);
         default: return cudaErrorInvalidValue;
     }
 }

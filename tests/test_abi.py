@@ -79,10 +79,10 @@ def test_draft_chain_host_validation(lib):
 
 
 def test_prepare_host_validation(lib):
-    assert lib.sdm_markov_prepared_size(151936, 256) >= 151936 * 256 * 2 + 151936 * 4
-    assert lib.sdm_markov_prepare(None, FAKE, 1024, 64, FAKE, 1 << 30, None) == 1
-    assert lib.sdm_markov_prepare(FAKE, FAKE, 1020, 64, FAKE, 1 << 30, None) == 2
-    assert lib.sdm_markov_prepare(FAKE, FAKE, 1024, 64, FAKE, 16, None) == 5
+    assert lib.sdm_markov_prepared_size(151936, 256) >= 151936 * 256 * 2 + 3 * 151936 * 4
+    assert lib.sdm_markov_prepare(None, FAKE, 1024, 64, FAKE, 1 << 30, None, None) == 1
+    assert lib.sdm_markov_prepare(FAKE, FAKE, 1020, 64, FAKE, 1 << 30, None, None) == 2
+    assert lib.sdm_markov_prepare(FAKE, FAKE, 1024, 64, FAKE, 16, None, None) == 5
 
 
 def test_tree_and_verify_host_validation(lib):

@@ -97,32 +97,73 @@ def test_draft_chain_greedy_prepared(case):
     assert torch.equal(pr["tokens"], dn["tokens"])
 
 
+def _prepared_views(raw, V, r):
+    """The arrays of the prepared-tables buffer (each on a 256-byte boundary)."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    out, off = {}, 0
+    for name, n, dt in (("wt", V * r * 2, torch.bfloat16), ("c", V * 4, torch.float32),
+                        ("u_norm", V * 4, torch.float32), ("absmax", V * 4, torch.float32),
+                        ("c_max", 4, torch.float32), ("n_max", 4, torch.float32), ("u_max", 4, torch.float32)):
+        out[name] = raw[off: off + n].view(dt)
+        off += up(n)
+    out["wt"] = out["wt"].view(V, r)
+    return out
+
+
+def _check_bounds(c, U, W, ys, u_norm, n_max, r):
+    """c(y) bounds max_v |U[y] . W[:, v]| (exact, fp64) from above, and by no
+    more than the stated slack."""
+    exact = (U[ys].double() @ W.double()).abs().max(dim=1).values
+    slack = 4 * r * 2.0 ** -24 * u_norm[ys].double() * float(n_max) + 2.0 ** -20
+    cy = c[ys].double()
+    assert torch.all(cy >= exact), "bound below the exact maximum"
+    assert torch.all(cy <= exact * (1 + 2.0 ** -10) * (1 + 1e-6) + slack + 1e-7), "bound looser than stated"
+
+
 def test_markov_prepare_tables():
     w = small(R=1, B=1, V=1000, r=128, sigma=(0.5,))
     inp = synthetic.generate(w, seed=2)
     prep = sdm.markov_prepare(dev(inp["U"]), dev(inp["W"]))
     torch.cuda.synchronize()
-    raw = prep.cpu()
     V, r = w.V, w.r
-    wt = raw[: V * r * 2].view(torch.bfloat16).view(V, r)
-    assert torch.equal(wt, inp["W"].t().contiguous())
-    off = (V * r * 2 + 255) // 256 * 256
-    u_norm = raw[off: off + V * 4].view(torch.float32)
-    off2 = off + (V * 4 + 255) // 256 * 256
-    n_max = raw[off2: off2 + 4].view(torch.float32)
-    u_max = raw[off2 + 256: off2 + 260].view(torch.float32)
+    t = _prepared_views(prep.cpu(), V, r)
+    assert torch.equal(t["wt"], inp["W"].t().contiguous())
     u_ref = inp["U"].double().norm(dim=1)
-    assert float(u_max) >= float(u_ref.max()) and float(u_max) <= float(u_ref.max()) * (1 + 1e-6)
-    assert torch.all(u_norm.double() >= u_ref) and torch.all(u_norm.double() <= u_ref * (1 + 1e-6) + 1e-30)
+    assert float(t["u_max"]) >= float(u_ref.max()) and float(t["u_max"]) <= float(u_ref.max()) * (1 + 1e-6)
+    assert torch.all(t["u_norm"].double() >= u_ref) and torch.all(t["u_norm"].double() <= u_ref * (1 + 1e-6) + 1e-30)
     w_ref = inp["W"].double().norm(dim=0).max()
-    assert float(n_max) >= float(w_ref) and float(n_max) <= float(w_ref) * (1 + 1e-6)
+    assert float(t["n_max"]) >= float(w_ref) and float(t["n_max"]) <= float(w_ref) * (1 + 1e-6)
+    _check_bounds(t["c"], inp["U"], inp["W"], torch.arange(V), t["u_norm"], t["n_max"], r)
+    assert float(t["c_max"]) == float(t["c"].max())
 
 
-@pytest.mark.parametrize("kind", ["all_equal", "outlier", "ties", "wide_markov"])
+def test_markov_prepare_bounds_full_vocab():
+    """The absolute-maximum GEMM at the 152K vocabulary (1187 M tiles, every
+    vocab tile): sampled tokens, and c_max against the sampled maxima."""
+    w = small(R=1, B=1, V=151936, r=256, sigma=(0.5,))
+    inp = synthetic.generate(w, seed=4)
+    prep = sdm.markov_prepare(dev(inp["U"]), dev(inp["W"]))
+    torch.cuda.synchronize()
+    t = _prepared_views(prep.cpu(), w.V, w.r)
+    g = torch.Generator().manual_seed(1)
+    ys = torch.cat([torch.randint(0, w.V, (96,), generator=g), torch.tensor([0, 127, 128, w.V - 1])])
+    _check_bounds(t["c"], inp["U"], inp["W"], ys, t["u_norm"], t["n_max"], w.r)
+    assert float(t["c_max"]) == float(t["c"].max())
+    assert float(t["c_max"]) < float(t["u_max"]) * float(t["n_max"])   # tighter than Cauchy-Schwarz
+
+
+@pytest.mark.parametrize("kind", ["all_equal", "outlier", "ties", "wide_markov", "crowded", "crowded_long"])
 def test_draft_chain_prepared_adversarial(kind):
     """Inputs that defeat the pruning bound (every id a candidate: many batches),
-    exact ties (lowest id wins) and a dominant Markov term."""
+    exact ties (lowest id wins), a dominant Markov term, and crowded rows whose
+    candidates overflow the shared-memory staging (later steps score from
+    global memory; with 64 steps the lists themselves stay in global memory)."""
     R, B, V, r = 3, 3, 8192, 64
+    if kind == "crowded":
+        B = 24
+    elif kind == "crowded_long":
+        R, B = 2, 64
     w = small(R=R, B=B, V=V, r=r, l_dtype=BF16, sigma=(0.5,))
     inp = synthetic.generate(w, seed=9)
     L = inp["L"].clone()
@@ -134,6 +175,8 @@ def test_draft_chain_prepared_adversarial(kind):
         L = torch.round(L.float() * 2).to(torch.bfloat16) / 2          # many exact ties
     elif kind == "wide_markov":
         L = (L.float() * 0.01).to(torch.bfloat16)                      # the Markov term decides
+    else:
+        L = (L.float() * 0.3).to(torch.bfloat16)                       # ~60 candidates per step
     d = {k: dev(v) for k, v in inp.items()}
     d["L"] = dev(L)
     prep = sdm.markov_prepare(d["U"], d["W"])
