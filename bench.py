@@ -55,19 +55,23 @@ def dist_env():
 
 
 def measured_peaks():
+    """(HBM GB/s, dense bf16 TFLOP/s sustained, source): the measured copy
+    bandwidth and GEMM throughput of this GPU, else the fallback figures."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops_sustained", d.get("bf16_tflops", 1700.0))), "measured"
+    return 6800.0, 1700.0, "fallback"
 
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("markov_gemm.cu", "device.cuh", "stream.cu", "internal.h"):
-        with open(os.path.join(ROOT, "speculative_decoding_markov_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    csrc = os.path.join(ROOT, "speculative_decoding_markov_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -163,8 +167,15 @@ class Cycle:
         self.inp = synthetic.generate(w, seed=seed, device=device)
         R, B, V, r = w.R, w.B, w.V, w.r
         self.sample = w.decode == "sample"
-        self.mode = {"compact": sdm.COMPACT, "static": sdm.STATIC, "cap_accept": sdm.CAP_ACCEPT}[w.modes[0]]
+        self.tree = w.decode == "tree"
         i32 = dict(dtype=torch.int32, device=device)
+        self.status = sdm.new_status(device)
+        self.side = torch.cuda.Stream(device=device)
+        self.prepared = None
+        if self.tree:
+            self._init_tree(R, B, V, r, i32)
+            return
+        self.mode = {"compact": sdm.COMPACT, "static": sdm.STATIC, "cap_accept": sdm.CAP_ACCEPT}[w.modes[0]]
         self.dr = dict(tokens=torch.empty((R, B), **i32), logq=torch.zeros((R, B), dtype=torch.float32, device=device),
                        lse=torch.zeros((R, B), dtype=torch.float32, device=device))
         self.sc = dict(survival=torch.empty((R, B), dtype=torch.float32, device=device), budget=torch.empty((R,), **i32),
@@ -181,7 +192,6 @@ class Cycle:
                        out_tok=torch.empty((R, B + 1), **i32), n_out=torch.empty((R,), **i32))
         self.ws_draft = sdm.workspace(sdm.OP_DRAFT_CHAIN, R, B, V, r, device=device)
         self.ws_verify = sdm.workspace(sdm.OP_VERIFY, R, B, V, r, cap, device=device)
-        self.status = sdm.new_status(device)
         # greedy drafting uses the Markov head's prepared tables, built once
         # per weights (model-load time, outside the timed cycle)
         self.prepared = None if self.sample else sdm.markov_prepare(self.inp["U"], self.inp["W"])
@@ -195,24 +205,85 @@ class Cycle:
         torch.cuda.synchronize()
         assert int(self.status.item()) & ~sdm.DEV_TIER_UNCAPTURED == 0, f"device status {int(self.status.item())}"
 
+    def _init_tree(self, R, B, V, r, i32):
+        """PCTree cycle: tree draft (batched frontier, per-level prune, global
+        top-N) and greedy verification of every tree slot."""
+        torch, sdm, w = self.torch, self.sdm, self.w
+        S = w.N + 1
+        dev = self.dev
+        self.tr = dict(tok=torch.empty((R, S), **i32), parent=torch.empty((R, S), **i32),
+                       depth=torch.empty((R, S), **i32), score=torch.empty((R, S), dtype=torch.float32, device=dev),
+                       mask=torch.empty((R, S, (S + 31) // 32), **i32), n_nodes=torch.empty((R,), **i32))
+        self.vr = dict(accept=torch.empty((R,), **i32), out_tok=torch.empty((R, B + 1), **i32),
+                       n_out=torch.empty((R,), **i32))
+        self.ws_draft = sdm.workspace(sdm.OP_DRAFT_TREE, R, B, V, r, w.P, w.k, w.N, device=dev)
+        self.ws_verify = sdm.workspace(sdm.OP_VERIFY_TREE, R, B, V, 0, 0, 0, w.N, device=dev)
+        self.draft()
+        self.target = self.synthetic.tree_target(self.inp, self.tr["tok"], self.tr["depth"], self.tr["n_nodes"],
+                                                 w.target_dtype)
+        self.verify()
+        torch.cuda.synchronize()
+        assert int(self.status.item()) == 0, f"device status {int(self.status.item())}"
+
+    def verified_rows(self):
+        if self.tree:
+            return int(self.tr["n_nodes"].sum().item())
+        return int(self.pk["cu_seqlens"][-1].item())
+
     # the four timed operations -------------------------------------------
     def draft(self):
         sdm, i = self.sdm, self.inp
+        if self.tree:
+            w = self.w
+            sdm.draft_tree(i["L"], i["U"], i["W"], i["anchor"], w.k, w.P, w.N, out=self.tr, ws=self.ws_draft,
+                           dev_status=self.status)
+            return
         sdm.draft_chain(i["L"], i["U"], i["W"], i["anchor"], decode=sdm.SAMPLE if self.sample else sdm.GREEDY,
                         temperature=self.w.temperature, seed=0, cycle=0, out=self.dr, ws=self.ws_draft,
                         dev_status=self.status, prepared=self.prepared)
 
-    def schedule_pack(self):
+    def schedule(self):
         sdm, i = self.sdm, self.inp
         sdm.schedule_budget(i["conf"], i["cost"], out=self.sc, dev_status=self.status)
+
+    def pack(self):
+        sdm, i = self.sdm, self.inp
         budget = self.sc["budget"] if self.mode == sdm.COMPACT else None
         sdm.pack_ragged(i["anchor"], self.dr["tokens"], budget, i["tiers"], out=self.pk, dev_status=self.status)
 
+    def schedule_pack(self):
+        if self.tree:    # the tree's node budget is its global top-N
+            return
+        self.schedule()
+        self.pack()
+
+    def front(self):
+        """Draft, schedule and pack.  The budget needs only the confidences,
+        so the scheduler runs on a side stream while the draft runs; the
+        pack joins both."""
+        if self.tree:
+            self.draft()
+            return
+        torch = self.torch
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)
+        with torch.cuda.stream(self.side):
+            self.schedule()
+        self.draft()
+        main.wait_stream(self.side)
+        self.pack()
+
     def gather(self):
+        if self.tree:    # the target rows of every tree slot are resident
+            return
         self.synthetic.gather_packed(self.target, self.pk["packed_req"], self.pk["packed_pos"], out=self.packed)
 
     def verify(self):
         sdm, i = self.sdm, self.inp
+        if self.tree:
+            sdm.verify_tree(self.target, self.tr["tok"], self.tr["parent"], self.tr["n_nodes"], self.w.B, out=self.vr,
+                            ws=self.ws_verify, dev_status=self.status)
+            return
         kw = {}
         if self.sample:
             kw = dict(logq=self.dr["logq"], lse_q=self.dr["lse"], L=i["L"], U=i["U"], W=i["W"])
@@ -221,6 +292,8 @@ class Cycle:
                    out=self.vr, ws=self.ws_verify, dev_status=self.status, **kw)
 
     def launches_per_step(self):
+        if self.tree:
+            return (2 * self.w.B + 2) + 2
         draft = 2 if self.prepared is not None else self.w.B + 2
         verify = 5 if self.sample else 2
         return draft + 1 + 1 + verify
@@ -232,8 +305,7 @@ class Cycle:
         self.g_draft = torch.cuda.CUDAGraph()
         self.g_verify = torch.cuda.CUDAGraph()
         with torch.cuda.graph(self.g_draft):
-            self.draft()
-            self.schedule_pack()
+            self.front()
         with torch.cuda.graph(self.g_verify):
             self.verify()
         torch.cuda.synchronize()
@@ -248,7 +320,7 @@ def run_ours(args, w, world, rank, local):
     R, B, V = w.R, w.B, w.V
     committed = int(cyc.vr["n_out"].sum().item())
     accepted = int(cyc.vr["accept"].sum().item())
-    windows = int(cyc.pk["cu_seqlens"][-1].item())          # sum of (n_i + 1) verified rows
+    windows = cyc.verified_rows()                            # target rows verified per cycle
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -260,8 +332,7 @@ def run_ours(args, w, world, rank, local):
         if graphs:
             cyc.g_draft.replay()
         else:
-            cyc.draft()
-            cyc.schedule_pack()
+            cyc.front()
 
     def run_verify():
         if graphs:
@@ -315,30 +386,35 @@ def run_ours(args, w, world, rank, local):
     t_max, units = merge_ranks(t_total, [committed * args.steps, windows * args.steps], world)
     status = int(cyc.status.item())
 
-    # roofline of the dominant kernel (algorithmic bytes / measured time)
-    peak, peak_kind = measured_peaks()
+    # roofline of the dominant kernel (algorithmic bytes or flops / measured time)
+    hbm_peak, tc_peak, peak_kind = measured_peaks()
     s_l = 2 if w.l_dtype == 0 else 4
     s_t = 2 if w.target_dtype == 0 else 4
-    # algorithmic bytes: the pruned greedy chain must read every element of L
-    # once (the few W^T rows it scores are not counted); the dense chain reads
-    # L once and W once per cycle
-    draft_bytes = R * B * V * s_l + (0 if cyc.prepared is not None else w.r * V * 2)
-    verify_bytes = windows * V * s_t                            # verified window rows
-    if t_draft >= t_verify:
-        if cyc.prepared is not None:
-            kname = "chain_scan_kernel+chain_pick_kernel"
-            per_launch_s = t_draft / args.steps
-            achieved = draft_bytes / per_launch_s / 1e9
-        else:
-            kname = "markov_gemm_kernel<chain>"
-            per_launch_s = t_draft / args.steps / B
-            achieved = draft_bytes / B / per_launch_s / 1e9
-        traffic = recorded_traffic(kname)
+    verify_bytes = windows * V * s_t                            # every verified target row once
+    if cyc.tree:
+        # one tensor-core launch per level: 2 * (R * P rows) * r * V flops
+        draft_alg, draft_launches, bound = 2.0 * R * w.P * w.r * V, B, "tensor"
+        dname = "markov_gemm_kernel<tree>"
+    elif cyc.prepared is not None:
+        # the pruned greedy chain must read every element of L once (the few
+        # W^T rows it scores are not counted)
+        draft_alg, draft_launches, bound = float(R * B * V * s_l), 1, "hbm"
+        dname = "chain_scan_kernel+chain_pick_kernel"
     else:
-        kname = "row_stream_kernel<argmax>"
+        # one launch per step: that step's rows of L and all of W
+        draft_alg, draft_launches, bound = float(R * V * s_l + w.r * V * 2), B, "hbm"
+        dname = "markov_gemm_kernel<chain>"
+    if t_draft >= t_verify:
+        kname = dname
+        per_launch_s = t_draft / args.steps / draft_launches
+        achieved = draft_alg / per_launch_s / (1e12 if bound == "tensor" else 1e9)
+    else:
+        kname, bound = "row_stream_kernel<argmax>", "hbm"
         per_launch_s = t_verify / args.steps
         achieved = verify_bytes / per_launch_s / 1e9
-        traffic = recorded_traffic(kname)
+    peak, unit = (tc_peak, "TFLOP/s") if bound == "tensor" else (hbm_peak, "GB/s")
+    traffic = recorded_traffic(kname)
+    draft_bytes = R * B * V * s_l
 
     e2e = None
     if not args.no_e2e:
@@ -372,9 +448,11 @@ def run_ours(args, w, world, rank, local):
         "graphs": graphs,
         "tokens_per_step": {"committed": committed, "accepted_drafts": accepted, "verified_rows": windows},
         "verified_rows_per_s": units[1] / t_max,
-        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved, "peak": peak, "unit": "GB/s",
+        "roofline": {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes": {"draft_per_cycle": draft_bytes, "verify_per_cycle": verify_bytes}},
+                     "algorithmic": {"draft_per_launch": draft_alg, "draft_launches_per_cycle": draft_launches,
+                                     "draft_unit": "flop" if cyc.tree else "byte",
+                                     "verify_bytes_per_cycle": verify_bytes, "L_bytes_per_cycle": draft_bytes}},
         "gpu_launches": cyc.launches_per_step() * args.steps,
         "device_status": status,
         "clocks": clk,
@@ -410,8 +488,7 @@ def run_e2e(cyc, args, committed):
         if graphs:
             cyc.g_draft.replay()
         else:
-            cyc.draft()
-            cyc.schedule_pack()
+            cyc.front()
         cyc.gather()
         if graphs:
             cyc.g_verify.replay()
@@ -454,6 +531,17 @@ def oracle_cycle(w, inp, idx, cycle_seed=0):
     sub["U"], sub["W"] = inp["U"], inp["W"]
     L, U, W = np_of(sub["L"]), np_of(inp["U"]), np_of(inp["W"])
     an = np_of(sub["anchor"])
+    if w.decode == "tree":
+        t0 = time.perf_counter()
+        tr = oracle.draft_tree(L, U, W, an, w.k, w.P, w.N)
+        t1 = time.perf_counter()
+        tgt = synthetic.tree_target({k: v.cpu() for k, v in sub.items()}, torch.as_tensor(tr["tok"]),
+                                    torch.as_tensor(tr["depth"]), torch.as_tensor(tr["n_nodes"]),
+                                    w.target_dtype)       # target stand-in: not timed
+        t2 = time.perf_counter()
+        vt = oracle.verify_tree(np_of(tgt), tr["tok"], tr["parent"], tr["n_nodes"], w.B)
+        t3 = time.perf_counter()
+        return (t1 - t0) + (t3 - t2), int(vt["n_out"].sum())
     conf, cost, tiers = np_of(inp["conf"]), np_of(inp["cost"]), np_of(inp["tiers"])
     sample = w.decode == "sample"
     ids = np.asarray(idx, np.int32)

@@ -166,7 +166,8 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
  *   tok, parent, depth [R, N+1] int32; score [R, N+1] fp32;
  *   mask [R, N+1, ceil((N+1)/32)] uint32, bit j of row c set iff slot j is c
  *   or an ancestor of c; n_nodes [R] int32 (root included).
- * Constraints: 1 <= k <= 8, 1 <= P, P*k <= 64, 128 % P == 0, N <= P*B.
+ * Constraints: 1 <= k <= 8, 1 <= P, P*k <= 64, 128 % P == 0, N <= P*B,
+ * P*B + 1 <= 8192 (else SDM_ERR_UNSUPPORTED).
  */
 sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
                           const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N,
@@ -259,6 +260,8 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
  * In:  target [R, N+1, V] (dtT; slot c's row predicts c's child), tok, parent
  *      [R, N+1], n_nodes [R].
  * Out: accept [R], out_tok [R, B+1] (-1 padded), n_out [R].
+ * When several children carry t, the lowest slot is taken.  N < 16384, else
+ * SDM_ERR_UNSUPPORTED.
  */
 sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok,
                            const int32_t* parent, const int32_t* n_nodes, int R, int N, int B, int V,

@@ -90,7 +90,7 @@ inline int n_chunks_of(int V, int fp32) {
     } while (0)
 
 size_t ws_chain_dense(int R, int B) {
-    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(B) * R * kMaxGx * 2 * 8);
+    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(B) * R * kMaxGx * kColGroups * 8);
 }
 
 // candidate lists of the pruned greedy chain (sized for the larger fp32 split)
@@ -104,7 +104,7 @@ size_t ws_chain(int R, int B, int V) { return std::max(ws_chain_dense(R, B), ws_
 size_t ws_tree(int R, int B, int P) {
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
-    return align256(rows * kMaxGx * 2 * (2 + 2 * kMaxTopK) * 4) + 3 * align256(rows * 4) + align256(R * 4) +
+    return align256(rows * kMaxGx * kColGroups * (2 + 2 * kMaxTopK) * 4) + 3 * align256(rows * 4) + align256(R * 4) +
            4 * align256(pool * 4) + align256(R * 4);
 }
 
@@ -241,7 +241,7 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
     }
     Carver c{static_cast<uint8_t*>(ws)};
     auto* keys = c.take<unsigned long long>(static_cast<size_t>(B) * R);
-    auto* lse_part = c.take<float2>(static_cast<size_t>(B) * R * kMaxGx * 2);
+    auto* lse_part = c.take<float2>(static_cast<size_t>(B) * R * kMaxGx * kColGroups);
 
     const int fp32 = dtL == SDM_FP32;
     const int l_rows = std::min(R, kTileM);
@@ -280,7 +280,7 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
         p.d = d;
         SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
     }
-    SDM_CHECK_CUDA(launch_chain_finalize(keys, lse_part, 2 * gx, R, B, V, r, L, fp32, U, W, anchor, p.inv_t,
+    SDM_CHECK_CUDA(launch_chain_finalize(keys, lse_part, kColGroups * gx, R, B, V, r, L, fp32, U, W, anchor, p.inv_t,
                                          decode == SDM_SAMPLE, tokens, logq, lse, dev_status, s));
     return SDM_OK;
 }
@@ -294,12 +294,13 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
     if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
     if (k > kMaxTopK || k > V || P * k > 64 || kTileM % P != 0 || N > P * B) return SDM_ERR_UNSUPPORTED;
+    if (static_cast<long long>(P) * B + 1 > 8192) return SDM_ERR_UNSUPPORTED;   // the pool is ranked in shared memory
     if (!ws || ws_bytes < ws_tree(R, B, P)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
     Carver c{static_cast<uint8_t*>(ws)};
-    float* tree_part = c.take<float>(rows * kMaxGx * 2 * (2 + 2 * kMaxTopK));
+    float* tree_part = c.take<float>(rows * kMaxGx * kColGroups * (2 + 2 * kMaxTopK));
     int32_t* front_tok = c.take<int32_t>(rows);
     int32_t* front_node = c.take<int32_t>(rows);
     float* front_score = c.take<float>(rows);
@@ -343,7 +344,7 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     for (int d = 1; d <= B; ++d) {
         p.d = d;
         SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE, tmW, tmL, p, gx, gy, s));
-        SDM_CHECK_CUDA(launch_tree_merge(tree_part, 2 * gx, R, P, k, B, d, front_tok, front_node, front_score, n_front,
+        SDM_CHECK_CUDA(launch_tree_merge(tree_part, kColGroups * gx, R, P, k, B, d, front_tok, front_node, front_score, n_front,
                                          pool_tok, pool_parent, pool_depth, pool_score, pool_n, s));
     }
     SDM_CHECK_CUDA(launch_tree_finalize(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok, parent,
@@ -495,6 +496,7 @@ sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok
                            int32_t* n_out, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
     if (!target || !tok || !parent || !n_nodes || !accept || !out_tok || !n_out) return SDM_ERR_INVALID_ARG;
     if (R <= 0 || N < 0 || B <= 0 || V <= 0) return SDM_ERR_INVALID_ARG;
+    if (N >= 16384) return SDM_ERR_UNSUPPORTED;   // the tree is walked in shared memory
     if (dtT != SDM_BF16 && dtT != SDM_FP32) return SDM_ERR_INVALID_ARG;
     if (!vocab_ok(V) || !aligned16(target)) return SDM_ERR_UNSUPPORTED;
     const size_t rows = static_cast<size_t>(R) * (N + 1);

@@ -13,13 +13,14 @@
 //     its chunk in registers, reduces the chunk maximum m_c and lists every
 //     id with L >= m_c - 2 c_max.  L is read from HBM exactly once.
 //   chain_pick_kernel  (one CTA per request, the B dependent steps)
-//     keeps the listed ids with L >= max_v L_d - 2 c_max (the ids any
-//     previous token can need), copies their W^T rows and U rows into shared
-//     memory, then walks the steps: step d scores the ids with
-//     L >= max - 2 c(y_{d-1}) exactly, z = L + U[y_{d-1}] . W^T[v] (fp32), and
-//     takes the (z desc, id asc) winner; one barrier per step.  Steps whose
-//     lists overflowed, or that do not fit in shared memory, score from global
-//     memory (a full-row scan when a list overflowed).
+//     one warp per step keeps the listed ids with L >= max_v L_d - 2 c_max
+//     (the ids any previous token can need) and copies their W^T rows and U
+//     rows into shared memory; then the CTA walks the steps: step d scores
+//     the ids with L >= max - 2 c(y_{d-1}) exactly,
+//     z = L + U[y_{d-1}] . W^T[v] (fp32), and takes the (z desc, id asc)
+//     winner; one warp walks these steps with no block barrier.  Steps whose
+//     lists overflowed, or whose ids do not fit in shared memory, score from
+//     global memory with every warp (a full-row scan when a list overflowed).
 //
 // The result equals the dense argmax bit for bit: the kept set contains every
 // id that can reach the maximum and the kept ids are scored exactly.
@@ -88,14 +89,6 @@ __device__ __forceinline__ const uint8_t* row_ptr(const PrunedParams& p, int row
     return static_cast<const uint8_t*>(p.L) + ((static_cast<size_t>(row) * p.B + (d - 1)) * p.V + v) * esz;
 }
 
-// Bulk (non-tensor) copy global -> shared, completing on an mbarrier.
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
-
 // The candidate threshold below a row maximum m for a Markov bound c, with
 // slack for the fp32 rounding of fp32(L) + Markov.
 __device__ __forceinline__ float threshold(float m, float c) {
@@ -118,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
     constexpr int CHUNK_IDS = kChunkBytes / ESZ;
     __shared__ float s_wmax[kWarps];
     __shared__ int s_cnt;
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nc = p.n_chunks;
     const int items = p.R * p.B * nc;       // <= 2^30 (checked by the host)
@@ -200,33 +195,31 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
 // ---------------------------------------------------------------------------
 constexpr int kGroup = 8;              // candidates a warp scores per round (global path)
 constexpr int kPickCap = 1024;         // ids per scoring batch of the global path
-constexpr int kListCap = 4096;         // listed ids of one request held in shared memory
-constexpr int kRowCapMax = 192;        // staged candidates (W^T row + U row each)
+constexpr int kRowCapMax = 256;        // staged candidates (W^T row + U row each)
 constexpr int kPickSmem = 200 * 1024;  // dynamic shared memory of the pick kernel
 
 struct PickLayout {
-    uint32_t cm, cn, soff, st_key, st_c, st_w, st_u, total;
+    uint32_t st_key, st_c, st_w, st_u, total;
     int cap;
 };
 
 __host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
 
+// Dynamic shared memory: list prefix sums [B][nc + 1], then a pool of cap
+// staged candidates shared by the steps: (id, L) keys, bounds c(id), W^T rows
+// and U rows.
 __host__ __device__ inline PickLayout pick_layout(int B, int nc, int r) {
     PickLayout l;
-    const uint32_t nseg = static_cast<uint32_t>(B) * static_cast<uint32_t>(nc);
-    l.cm = kListCap * 8u;
-    l.cn = al16(l.cm + nseg * 4u);
-    l.soff = al16(l.cn + nseg * 4u);
-    const uint32_t fixed = al16(l.soff + (nseg + 1u) * 4u);
-    const uint32_t per = 8u + 4u + 4u * static_cast<uint32_t>(r);   // key, bound, W^T row, U row
+    const uint32_t fixed = al16(static_cast<uint32_t>(B) * static_cast<uint32_t>(nc + 1) * 4u);
+    const uint32_t per = 8u + 4u + 4u * static_cast<uint32_t>(r);
     int cap = static_cast<int>((kPickSmem - fixed - 64u) / per);
     cap = cap < kRowCapMax ? cap : kRowCapMax;
     l.cap = cap;
     l.st_key = fixed;
-    l.st_c = al16(l.st_key + static_cast<uint32_t>(cap) * 8u);
-    l.st_w = al16(l.st_c + static_cast<uint32_t>(cap) * 4u);
-    l.st_u = l.st_w + static_cast<uint32_t>(cap) * 2u * r;
-    l.total = l.st_u + static_cast<uint32_t>(cap) * 2u * r;
+    l.st_c = al16(l.st_key + static_cast<uint32_t>(l.cap) * 8u);
+    l.st_w = al16(l.st_c + static_cast<uint32_t>(l.cap) * 4u);
+    l.st_u = l.st_w + static_cast<uint32_t>(l.cap) * 2u * r;
+    l.total = l.st_u + static_cast<uint32_t>(l.cap) * 2u * r;
     return l;
 }
 
@@ -274,286 +267,304 @@ __device__ __forceinline__ unsigned long long score_global(const PrunedParams& p
     return best;
 }
 
+// Segment holding entry t of a step's concatenated lists: the largest c with
+// pref[c] <= t (pref[0] = 0 <= t < pref[nc]).
+__device__ __forceinline__ int segment_of(const int* pref, int nc, int t) {
+    int lo = 0, hi = nc - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (pref[mid] <= t)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 template <int FP32>
 __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedParams p) {
     constexpr int VEC = FP32 ? 4 : 8;
+    constexpr int kBatch = 4;   // list entries a lane loads at once (second round)
+    constexpr int kHead = 32;   // entries of each list loaded with its length
+    pdl_wait();
+    pdl_trigger();
     const int row = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nc = p.n_chunks, B = p.B, r = p.r;
-    const int nseg = B * nc;
     const PickLayout lay = pick_layout(B, nc, r);
     extern __shared__ __align__(16) uint8_t s_dyn[];
-    uint2* s_list = reinterpret_cast<uint2*>(s_dyn);              // [kListCap] all lists, packed
-    float* s_cm = reinterpret_cast<float*>(s_dyn + lay.cm);        // [B][nc] chunk maxima
-    int* s_cn = reinterpret_cast<int*>(s_dyn + lay.cn);            // [B][nc] list lengths
-    int* s_soff = reinterpret_cast<int*>(s_dyn + lay.soff);        // [B * nc + 1] packed list offsets
+    int* s_pref = reinterpret_cast<int*>(s_dyn);                   // [B][nc + 1] list prefix sums
     uint2* st_key = reinterpret_cast<uint2*>(s_dyn + lay.st_key);  // [cap] staged (id, L bits)
-    float* st_c = reinterpret_cast<float*>(s_dyn + lay.st_c);      // [cap] c(id)
-    uint16_t* st_w = reinterpret_cast<uint16_t*>(s_dyn + lay.st_w);   // [cap][r] W^T rows
-    uint16_t* st_u = reinterpret_cast<uint16_t*>(s_dyn + lay.st_u);   // [cap][r] U rows
-    __shared__ __align__(8) uint64_t s_bar;
+    float* st_c = reinterpret_cast<float*>(s_dyn + lay.st_c);      // c(id)
+    uint16_t* st_w = reinterpret_cast<uint16_t*>(s_dyn + lay.st_w);   // W^T rows
+    uint16_t* st_u = reinterpret_cast<uint16_t*>(s_dyn + lay.st_u);   // U rows
     __shared__ __align__(16) uint16_t s_u0[256];                   // U[anchor]
     __shared__ float s_lmax[kMaxPickSteps];
     __shared__ int s_scnt[kMaxPickSteps];                          // staged ids of each step
-    __shared__ int s_sbeg[kMaxPickSteps + 1];                      // their first slot (-1: not staged)
+    __shared__ int s_sbeg[kMaxPickSteps];                          // their first pool slot
+    __shared__ int s_alloc;                                        // pool slots handed out
+    __shared__ int s_staged[kMaxPickSteps];                        // the step scores from shared memory
     __shared__ int s_over[kMaxPickSteps];                          // a list of the step overflowed
-    __shared__ int s_lists_in_smem;
-    __shared__ unsigned long long s_wbest[2][kWarps];
-    __shared__ int s_wslot[2][kWarps];
+    __shared__ const uint16_t* s_urow;
+    __shared__ float s_cprev;
     __shared__ uint2 s_ids[kPickCap];
     __shared__ int s_m;
-    __shared__ unsigned long long s_best;
+    __shared__ unsigned long long s_best[2];
     const float cmax = *p.c_max;
-    const int seg0 = row * nseg;
+    const int seg0 = row * B * nc;
 
     int prev = p.anchor[row];
     if (prev < 0 || prev >= p.V) {
         if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
         prev = 0;
     }
-    // 1. U[anchor] (async), chunk maxima and list lengths of every step
     if (threadIdx.x * 8 < r) cp_async_16(s_u0 + threadIdx.x * 8, p.U + static_cast<size_t>(prev) * r + threadIdx.x * 8, 16u);
     float cprev = p.c_bound[prev];
-    if (threadIdx.x == 0) {
-        mbar_init(&s_bar, 1);
-        fence_mbar_init();
-    }
-    for (int i = threadIdx.x; i < nseg; i += kThreads) {
-        s_cm[i] = p.cmax[seg0 + i];
-        s_cn[i] = p.cand_n[seg0 + i];
-    }
+    if (threadIdx.x == 0) s_alloc = 0;
     __syncthreads();
-    // 2. warp 0: packed list offsets (lists padded to even lengths so that the
-    //    bulk copies are 16-byte multiples) and the copies; the other warps:
-    //    row maxima and overflow flags of every step
-    if (warp == 0) {
-        int run = 0;
-        for (int i0 = 0; i0 < nseg; i0 += 32) {
-            const int i = i0 + lane;
-            const int n = i < nseg ? (min(s_cn[i], kSegCap) + 1) & ~1 : 0;
+
+    // One warp per step (lane = chunk): the chunk maxima, the list lengths
+    // and, in the same round of loads, the head of every list; the listed
+    // ids with L >= max - 2 c_max (those any previous token can need) are
+    // compacted, then their W^T rows, U rows and bounds copied into shared
+    // memory.  Lists longer than their loaded head take a second round.
+    for (int d = warp; d < B; d += kWarps) {
+        const int sg = seg0 + d * nc;
+        int* pref = s_pref + d * (nc + 1);
+        float m = -INFINITY;
+        int over = 0, spill = 0, run = 0;
+        uint2 head[kHead];
+        int cn0 = 0;
+        for (int c0 = 0; c0 < nc; c0 += 32) {
+            const int c = c0 + lane;
+            int n = 0;
+            if (c < nc) {
+                m = fmaxf(m, p.cmax[sg + c]);
+                const int cn = p.cand_n[sg + c];
+                if (c0 == 0) {
+                    cn0 = cn;
+                    const uint4* h = reinterpret_cast<const uint4*>(p.cand + static_cast<size_t>(sg + c) * kSegCap);
+#pragma unroll
+                    for (int q = 0; q < kHead / 2; ++q) {
+                        const uint4 v = h[q];
+                        head[2 * q] = make_uint2(v.x, v.y);
+                        head[2 * q + 1] = make_uint2(v.z, v.w);
+                    }
+                }
+                over |= cn > kSegCap;
+                spill |= cn > kHead;
+                n = min(cn, kSegCap);
+            }
             int x = n;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += y;
             }
-            if (i < nseg) s_soff[i] = run + x - n;
+            if (c < nc) pref[c] = run + x - n;
             run += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (lane == 0) {
-            s_soff[nseg] = run;
-            const int fits = run <= kListCap;
-            s_lists_in_smem = fits;
-            if (fits && run > 0) {
-                mbar_arrive_expect_tx(&s_bar, static_cast<uint32_t>(run) * 8u);
-                for (int i = 0; i < nseg; ++i) {
-                    const int n = (min(s_cn[i], kSegCap) + 1) & ~1;
-                    if (n) bulk_load(s_list + s_soff[i], p.cand + static_cast<size_t>(seg0 + i) * kSegCap,
-                                     static_cast<uint32_t>(n) * 8u, &s_bar);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        over = __any_sync(0xffffffffu, over);
+        spill = __any_sync(0xffffffffu, spill) || nc > 32;
+        __syncwarp();
+        if (lane == 0) pref[nc] = run;
+        const float t_all = threshold(m, cmax);
+        // two passes over the same ids: count, take a range of the pool,
+        // then write (a step whose ids do not fit scores from global memory)
+        int kept = 0, off = 0;
+        bool fits = !over;
+        for (int pass = 0; pass < 2 && fits; ++pass) {
+            int pos0 = 0;
+            if (!spill) {
+                // every list fits in its head: compact from registers
+#pragma unroll
+                for (int e = 0; e < kHead; ++e) {
+                    const bool keep = lane < nc && e < cn0 && head[e].x < static_cast<uint32_t>(p.V) &&
+                                      __uint_as_float(head[e].y) >= t_all;
+                    const unsigned bal = __ballot_sync(0xffffffffu, keep);
+                    if (pass == 1 && keep) st_key[off + pos0 + __popc(bal & ((1u << lane) - 1u))] = head[e];
+                    pos0 += __popc(bal);
+                }
+            } else {
+                for (int t0 = 0; t0 < run; t0 += 32 * kBatch) {
+                    uint2 en[kBatch];
+#pragma unroll
+                    for (int q = 0; q < kBatch; ++q) {   // independent loads, all in flight
+                        const int t = t0 + q * 32 + lane;
+                        en[q] = make_uint2(0xffffffffu, 0u);
+                        if (t < run) {
+                            const int c = segment_of(pref, nc, t);
+                            en[q] = p.cand[static_cast<size_t>(sg + c) * kSegCap + (t - pref[c])];
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kBatch; ++q) {
+                        const bool keep = en[q].x < static_cast<uint32_t>(p.V) && __uint_as_float(en[q].y) >= t_all;
+                        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+                        if (pass == 1 && keep) st_key[off + pos0 + __popc(bal & ((1u << lane) - 1u))] = en[q];
+                        pos0 += __popc(bal);
+                    }
                 }
             }
-        }
-    } else {
-        for (int d = warp - 1; d < B; d += kWarps - 1) {
-            float m = -INFINITY;
-            int over = 0;
-            for (int c = lane; c < nc; c += 32) {
-                m = fmaxf(m, s_cm[d * nc + c]);
-                over |= s_cn[d * nc + c] > kSegCap;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            over = __any_sync(0xffffffffu, over);
-            if (lane == 0) {
-                s_lmax[d] = m;
-                s_over[d] = over;
+            if (pass == 0) {
+                kept = pos0;
+                int o = 0;
+                if (lane == 0) o = atomicAdd(&s_alloc, kept);
+                off = __shfl_sync(0xffffffffu, o, 0);
+                fits = off + kept <= lay.cap;
             }
         }
-    }
-    __syncthreads();
-    const bool lists_in_smem = s_lists_in_smem;
-    if (lists_in_smem && s_soff[nseg] > 0) {
-        const bool ok = mbar_wait(&s_bar, 0);
-        if (!__syncthreads_and(ok) && threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_TIMEOUT);
-        for (int i = threadIdx.x; i < nseg; i += kThreads) {   // the padding slot is not an id
-            const int n = min(s_cn[i], kSegCap);
-            if (s_soff[i] + n < s_soff[i + 1]) s_list[s_soff[i] + n] = make_uint2(0xffffffffu, 0u);
-        }
-        __syncthreads();
-    }
-    // 3. stage, step by step, the listed ids with L >= max - 2 c_max: count
-    //    (warp per step), assign slots in step order, compact, then copy their
-    //    W^T rows, U rows (steps < B: the next step's possible previous token)
-    //    and bounds into shared memory
-    if (lists_in_smem) {
-        for (int d = warp; d < B; d += kWarps) {
-            const float t = threshold(s_lmax[d], cmax);
-            int cnt = 0;
-            for (int e = s_soff[d * nc] + lane; e < s_soff[(d + 1) * nc]; e += 32) {
-                const uint2 en = s_list[e];
-                cnt += en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= t;
+        __syncwarp();
+        if (fits) {
+            for (int j = 0; j < kept; ++j) {
+                const uint32_t v = st_key[off + j].x;
+                const int slot = off + j;
+                if (lane * 8 < r) {
+                    cp_async_16(st_w + static_cast<size_t>(slot) * r + lane * 8, p.Wt + static_cast<size_t>(v) * r + lane * 8, 16u);
+                    cp_async_16(st_u + static_cast<size_t>(slot) * r + lane * 8, p.U + static_cast<size_t>(v) * r + lane * 8, 16u);
+                }
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-            if (lane == 0) s_scnt[d] = cnt;
+            for (int j = lane; j < kept; j += 32) st_c[off + j] = p.c_bound[st_key[off + j].x];
         }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int run = 0;
-            for (int d = 0; d < B; ++d) {
-                const bool fits = !s_over[d] && run + s_scnt[d] <= lay.cap;
-                s_sbeg[d] = fits ? run : -1;
-                if (fits) run += s_scnt[d];
-            }
-            s_sbeg[B] = run;
+        if (lane == 0) {
+            s_lmax[d] = m;
+            s_over[d] = over;
+            s_scnt[d] = kept;
+            s_sbeg[d] = off;
+            s_staged[d] = fits;
         }
-        __syncthreads();
-        for (int d = warp; d < B; d += kWarps) {
-            if (s_sbeg[d] < 0) continue;
-            const float t = threshold(s_lmax[d], cmax);
-            int base = s_sbeg[d];
-            for (int e0 = s_soff[d * nc]; e0 < s_soff[(d + 1) * nc]; e0 += 32) {
-                const int e = e0 + lane;
-                uint2 en = make_uint2(0xffffffffu, 0u);
-                if (e < s_soff[(d + 1) * nc]) en = s_list[e];
-                const bool keep = en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= t;
-                const unsigned bal = __ballot_sync(0xffffffffu, keep);
-                if (keep) st_key[base + __popc(bal & ((1u << lane) - 1u))] = en;
-                base += __popc(bal);
-            }
-        }
-        __syncthreads();
-        const int n_st = s_sbeg[B];
-        const int cpr = r >> 3;   // 16-byte pieces per row
-        for (int i = threadIdx.x; i < n_st * cpr; i += kThreads) {
-            const int j = i / cpr, q = i - j * cpr;
-            const uint32_t v = st_key[j].x;
-            cp_async_16(st_w + static_cast<size_t>(j) * r + q * 8, p.Wt + static_cast<size_t>(v) * r + q * 8, 16u);
-            cp_async_16(st_u + static_cast<size_t>(j) * r + q * 8, p.U + static_cast<size_t>(v) * r + q * 8, 16u);
-        }
-        for (int j = threadIdx.x; j < n_st; j += kThreads) st_c[j] = p.c_bound[st_key[j].x];
-    } else {
-        for (int d = threadIdx.x; d <= B; d += kThreads) s_sbeg[d] = d < B ? -1 : 0;
     }
     cp_async_wait_all();
     __syncthreads();
 
-    // 4. the steps
+    // The steps.  A staged step is warp 0's alone (its ids, rows and bounds
+    // are in shared memory; no block barrier); the other warps join only for
+    // a step on the global path, where warp 0 hands over its state.
     const uint16_t* urow = s_u0;   // U[y_{d-1}]: shared (staged) or global
     for (int d = 1; d <= B; ++d) {
-        const int ds = (d - 1) * nc;
         const float lmax = s_lmax[d - 1];
-        const float tall = threshold(lmax, cprev);   // every id that can win has L >= tall
-        float ub[8];
-        load_ub(urow, lane, r, ub);
-        const int par = d & 1;
-        const int sb = s_sbeg[d - 1];
-        unsigned long long win;
-        int win_slot = -1;
-        if (sb >= 0) {
-            // staged: each warp scores its share of the step's staged ids
+        if (s_staged[d - 1]) {
+            if (warp != 0) continue;
+            const float tall = threshold(lmax, cprev);   // every id that can win has L >= tall
+            float ub[8];
+            load_ub(urow, lane, r, ub);
+            const int sb = s_sbeg[d - 1];
+            const int n = s_scnt[d - 1];
             unsigned long long best = 0ull;
             int bslot = -1;
-            const int n = s_scnt[d - 1];
-            for (int j = sb + warp; j < sb + n; j += kWarps) {
-                const uint2 en = st_key[j];
-                const float lv = __uint_as_float(en.y);
-                if (lv < tall) continue;   // warp-uniform
-                const uint4 w = lane * 8 < r ? *reinterpret_cast<const uint4*>(st_w + static_cast<size_t>(j) * r + lane * 8)
-                                             : make_uint4(0, 0, 0, 0);
-                const unsigned long long k = argmax_key(lv + warp_dot(w, ub), en.x);
-                if (k > best) {
-                    best = k;
-                    bslot = j;
-                }
-            }
-            if (lane == 0) {
-                s_wbest[par][warp] = best;
-                s_wslot[par][warp] = bslot;
-            }
-            __syncthreads();
-            win = s_wbest[par][0];
-            win_slot = s_wslot[par][0];
+            for (int j0 = 0; j0 < n; j0 += kGroup) {
+                uint2 en[kGroup];
+                float acc[kGroup];
 #pragma unroll
-            for (int w = 1; w < kWarps; ++w) {
-                const unsigned long long k = s_wbest[par][w];
-                if (k > win) {
-                    win = k;
-                    win_slot = s_wslot[par][w];
+                for (int jj = 0; jj < kGroup; ++jj) {   // all row loads first, then the sums
+                    const int j = j0 + jj;
+                    en[jj] = j < n ? st_key[sb + j] : make_uint2(0xffffffffu, 0u);
+                    const bool ok = j < n && __uint_as_float(en[jj].y) >= tall && lane * 8 < r;
+                    const uint4 w = ok ? *reinterpret_cast<const uint4*>(st_w + static_cast<size_t>(sb + j) * r + lane * 8)
+                                       : make_uint4(0, 0, 0, 0);
+                    float a[8];
+                    unpack<0>(w, a);
+                    acc[jj] = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) acc[jj] = fmaf(a[q], ub[q], acc[jj]);
                 }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+                    for (int jj = 0; jj < kGroup; ++jj) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], o);
+#pragma unroll
+                for (int jj = 0; jj < kGroup; ++jj) {
+                    const float lv = __uint_as_float(en[jj].y);
+                    if (j0 + jj < n && lv >= tall) {
+                        const unsigned long long k = argmax_key(lv + acc[jj], en[jj].x);   // fp32(L) + Markov
+                        if (k > best) {
+                            best = k;
+                            bslot = sb + j0 + jj;
+                        }
+                    }
+                }
+            }
+            int y = static_cast<int>(key_token(best));
+            if (best == 0ull || y < 0 || y >= p.V) {
+                if (lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+                y = 0;
+                bslot = -1;
+            }
+            if (lane == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
+            if (bslot >= 0) {   // the winner's U row and bound were staged with it
+                urow = st_u + static_cast<size_t>(bslot) * r;
+                cprev = st_c[bslot];
+            } else {
+                urow = p.U + static_cast<size_t>(y) * r;
+                cprev = p.c_bound[y];
+            }
+            continue;
+        }
+        // global path: every warp, warp 0's state first
+        const int par = d & 1;
+        if (threadIdx.x == 0) {
+            s_urow = urow;
+            s_cprev = cprev;
+            s_best[par] = 0ull;
+        }
+        __syncthreads();
+        urow = s_urow;
+        cprev = s_cprev;
+        const int ds = (d - 1) * nc;
+        const float tall = threshold(lmax, cprev);
+        float ub[8];
+        load_ub(urow, lane, r, ub);
+        if (!s_over[d - 1]) {
+            // the step's list entries in windows of kPickCap; ids with L >= tall scored
+            const int* pref = s_pref + (d - 1) * (nc + 1);
+            const int total = pref[nc];
+            for (int w0 = 0; w0 < total; w0 += kPickCap) {
+                if (threadIdx.x == 0) s_m = 0;
+                __syncthreads();
+                for (int t = w0 + threadIdx.x; t < min(total, w0 + kPickCap); t += kThreads) {
+                    const int c = segment_of(pref, nc, t);
+                    const uint2 en = p.cand[static_cast<size_t>(seg0 + ds + c) * kSegCap + (t - pref[c])];
+                    if (en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= tall)
+                        s_ids[atomicAdd(&s_m, 1)] = en;
+                }
+                __syncthreads();
+                const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
+                if (lane == 0 && b) atomicMax(&s_best[par], b);
+                __syncthreads();
             }
         } else {
-            // global path
-            if (threadIdx.x == 0) s_best = 0ull;
-            if (!s_over[d - 1]) {
-                // the step's list entries in windows of kPickCap, ids with L >= tall scored
-                const int e_beg = lists_in_smem ? s_soff[ds] : 0;
-                int e_end;
-                if (lists_in_smem) {
-                    e_end = s_soff[ds + nc];
-                } else {
-                    e_end = 0;
-                    for (int c = 0; c < nc; ++c) e_end += min(s_cn[ds + c], kSegCap);
-                }
-                for (int w0 = e_beg; w0 < e_end; w0 += kPickCap) {
-                    if (threadIdx.x == 0) s_m = 0;
-                    __syncthreads();
-                    for (int e = w0 + threadIdx.x; e < min(e_end, w0 + kPickCap); e += kThreads) {
-                        uint2 en;
-                        if (lists_in_smem) {
-                            en = s_list[e];
-                        } else {   // entry e of the step's lists, chunk by chunk
-                            int c = 0, off = e;
-                            while (off >= min(s_cn[ds + c], kSegCap)) off -= min(s_cn[ds + c++], kSegCap);
-                            en = p.cand[static_cast<size_t>(seg0 + ds + c) * kSegCap + off];
-                        }
-                        if (en.x < static_cast<uint32_t>(p.V) && __uint_as_float(en.y) >= tall)
-                            s_ids[atomicAdd(&s_m, 1)] = en;
-                    }
-                    __syncthreads();
-                    const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
-                    if (lane == 0 && b) atomicMax(&s_best, b);
-                    __syncthreads();
-                }
-            } else {
-                // a list overflowed: scan the whole row in batches (exact for any input)
-                const uint4* src = reinterpret_cast<const uint4*>(row_ptr(p, row, d, 0));
-                const int nv = p.V / VEC;
-                for (int c0 = 0; c0 < nv; c0 += kPickCap / VEC) {
-                    if (threadIdx.x == 0) s_m = 0;
-                    __syncthreads();
-                    for (int i = c0 + threadIdx.x; i < min(nv, c0 + kPickCap / VEC); i += kThreads) {
-                        float v[VEC];
-                        unpack<FP32>(__ldg(src + i), v);
+            // a list overflowed: scan the whole row in batches (exact for any input)
+            const uint4* src = reinterpret_cast<const uint4*>(row_ptr(p, row, d, 0));
+            const int nv = p.V / VEC;
+            for (int c0 = 0; c0 < nv; c0 += kPickCap / VEC) {
+                if (threadIdx.x == 0) s_m = 0;
+                __syncthreads();
+                for (int i = c0 + threadIdx.x; i < min(nv, c0 + kPickCap / VEC); i += kThreads) {
+                    float v[VEC];
+                    unpack<FP32>(__ldg(src + i), v);
 #pragma unroll
-                        for (int q = 0; q < VEC; ++q)
-                            if (v[q] >= tall)
-                                s_ids[atomicAdd(&s_m, 1)] = make_uint2(static_cast<uint32_t>(i * VEC + q), __float_as_uint(v[q]));
-                    }
-                    __syncthreads();
-                    const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
-                    if (lane == 0 && b) atomicMax(&s_best, b);
-                    __syncthreads();
+                    for (int q = 0; q < VEC; ++q)
+                        if (v[q] >= tall)
+                            s_ids[atomicAdd(&s_m, 1)] = make_uint2(static_cast<uint32_t>(i * VEC + q), __float_as_uint(v[q]));
                 }
+                __syncthreads();
+                const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
+                if (lane == 0 && b) atomicMax(&s_best[par], b);
+                __syncthreads();
             }
-            __syncthreads();
-            win = s_best;
         }
+        __syncthreads();
+        const unsigned long long win = s_best[par];
         int y = static_cast<int>(key_token(win));
         if (win == 0ull || y < 0 || y >= p.V) {
             if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
             y = 0;
-            win_slot = -1;
         }
         if (threadIdx.x == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
-        if (d == B) break;
-        if (win_slot >= 0) {   // the winner's U row and bound were staged with it
-            urow = st_u + static_cast<size_t>(win_slot) * r;
-            cprev = st_c[win_slot];
-        } else {
-            urow = p.U + static_cast<size_t>(y) * r;
-            cprev = p.c_bound[y];
-        }
+        urow = p.U + static_cast<size_t>(y) * r;
+        cprev = p.c_bound[y];
     }
 }
 
@@ -622,12 +633,11 @@ int pruned_chunks(int V, int l_fp32) {
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
     const long long items = static_cast<long long>(p.R) * p.B * p.n_chunks;
     if (items > (1LL << 30)) return cudaErrorInvalidValue;
+    // two CTAs per resident slot: a CTA that finishes early is replaced, which
+    // evens out the tail better than one wave of equal shares
     const int grid = static_cast<int>(items < 8LL * num_sms() ? items : 8LL * num_sms());
-    if (p.l_fp32)
-        chain_scan_kernel<1><<<grid, kThreads, 0, s>>>(p);
-    else
-        chain_scan_kernel<0><<<grid, kThreads, 0, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = p.l_fp32 ? launch_pdl(chain_scan_kernel<1>, dim3(grid), dim3(kThreads), 0, s, p)
+                             : launch_pdl(chain_scan_kernel<0>, dim3(grid), dim3(kThreads), 0, s, p);
     if (e != cudaSuccess) return e;
     const PickLayout lay = pick_layout(p.B, p.n_chunks, p.r);
     if (lay.cap < 1) return cudaErrorInvalidValue;
@@ -639,11 +649,8 @@ cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    if (p.l_fp32)
-        chain_pick_kernel<1><<<p.R, kThreads, lay.total, s>>>(p);
-    else
-        chain_pick_kernel<0><<<p.R, kThreads, lay.total, s>>>(p);
-    return cudaGetLastError();
+    return p.l_fp32 ? launch_pdl(chain_pick_kernel<1>, dim3(p.R), dim3(kThreads), lay.total, s, p)
+                    : launch_pdl(chain_pick_kernel<0>, dim3(p.R), dim3(kThreads), lay.total, s, p);
 }
 
 cudaError_t launch_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, uint16_t* Wt, float* u_norm,

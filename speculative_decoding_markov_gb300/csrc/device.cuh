@@ -92,6 +92,15 @@ __device__ __forceinline__ void set_status(int32_t* dev_status, int bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may become resident before the previous kernel in the stream
+// has finished; pdl_wait() returns once that grid has completed and its
+// memory operations are visible (immediately when there is none).  Kernels
+// call it before touching global memory, then pdl_trigger() so that the next
+// kernel can start its own launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon et al., SC'11) and the uniforms of the C-ABI
 // ---------------------------------------------------------------------------
@@ -116,6 +125,16 @@ __device__ __forceinline__ U4 philox10(U4 c, uint32_t k0, uint32_t k1) {
 // Uniform (2 (w >> 9) + 1) 2^-24 in (0, 1), exact in fp32.
 __device__ __forceinline__ float word_to_uniform(uint32_t w) {
     return static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-8f;
+}
+
+// 1 - u for the same word, exact.  Race filter: the key z_v - ln E_v,
+// E_v = -ln u_v, can beat a running best b only if E_v < exp(z_v - b); since
+// -ln u >= 1 - u, an element with 1 - u >= 2 exp(z_v - b) is ruled out
+// without a logarithm (the factor 2 leaves a margin of ln 2 in the key, far
+// above the rounding of the logarithms), so the winner is the same as with
+// every key formed.
+__device__ __forceinline__ float one_minus_uniform(uint32_t w) {
+    return __uint2float_rn(16777215u - 2u * (w >> 9)) * 5.9604644775390625e-8f;
 }
 
 struct RngKey {
@@ -287,6 +306,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
           "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
           "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 

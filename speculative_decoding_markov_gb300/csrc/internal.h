@@ -10,13 +10,34 @@
 
 namespace sdm {
 
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor in the stream drains, and waits for it in pdl_wait().
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // Markov GEMM (tcgen05): one CTA = one 128-row M tile x a contiguous range of
 // 64-wide vocab tiles; K = r (<= 256, multiple of 64).
 // ---------------------------------------------------------------------------
 constexpr int kTileM = 128;        // GEMM rows per CTA (TMEM lanes)
 constexpr int kTileN = 64;         // vocab ids per tile (one 128-byte bf16 swizzle span)
-constexpr int kGemmThreads = 320;  // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kColGroups = 4;      // epilogue column groups per tile (16 columns each)
+constexpr int kEpiCols = kTileN / kColGroups;
+constexpr int kEpiWarps = 4 * kColGroups;          // four TMEM sub-partitions x column groups
+constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA, warps 2.. epilogue
 constexpr int kMaxTopK = 8;
 
 enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3, MODE_ABSMAX = 4 };
@@ -40,10 +61,10 @@ struct GemmParams {
     const int32_t* anchor;
     // chain
     unsigned long long* keys;   // [B][R] argmax / race keys
-    float2* lse_part;           // [B][R][gridDim.x][2] (one per column half)
+    float2* lse_part;           // [B][R][gridDim.x][kColGroups]
     // tree
     const int32_t* front_tok;   // [R][P] frontier tokens (-1: empty slot)
-    float* tree_part;           // [rows][gridDim.x][2][2 + 2 * kMaxTopK]
+    float* tree_part;           // [rows][gridDim.x][kColGroups][2 + 2 * kMaxTopK]
     // residual (sample verify): one GEMM row per request
     const int32_t* res_tok;     // [R] previous token of the rejected position, -1: none
     const int32_t* res_pos;     // [R] rejected window position j (L row j, stream row j)

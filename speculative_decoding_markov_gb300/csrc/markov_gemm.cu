@@ -21,10 +21,10 @@
 //     [rows x 64] (TMA 3-D, evict_first) through an S-stage mbarrier ring;
 //   * warp 1 issues r/16 tcgen05.mma (M=128, N=64, K=16, bf16 -> fp32) per
 //     tile into one of two 64-column TMEM accumulators;
-//   * warps 2-9 drain the accumulator with tcgen05.ld (thread = GEMM row;
-//     warps 2-5 take columns 0-31 of every tile, warps 6-9 columns 32-63),
-//     add L and run the mode's reduction in registers; one result per row,
-//     CTA and column half is written at the end.
+//   * warps 2-17 drain the accumulator with tcgen05.ld (thread = GEMM row of
+//     its TMEM sub-partition; four warps per sub-partition, one per 16-column
+//     group of every tile), add L and run the mode's reduction in registers;
+//     one result per row, CTA and column group is written at the end.
 // The grid is (vocab splits) x (M tiles), one CTA per SM; vocab tiles are
 // dealt to the splits round-robin.
 #include "device.cuh"
@@ -33,7 +33,6 @@
 namespace sdm {
 namespace {
 
-constexpr int kEpiWarps = 8;   // two per TMEM sub-partition: one per 32-column half
 constexpr int kSmemLimit = 232448;   // 227 KB opt-in per block
 
 struct SmemLayout {
@@ -82,14 +81,17 @@ __device__ __forceinline__ int gemm_row_token(const GemmParams& p, int grow) {
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
-// The 32 L values of columns [32h, 32h + 32) of the staged tile, box row lr.
-__device__ __forceinline__ void load_l32(const uint8_t* sl, uint32_t l_box_bytes, int l_fp32, int lr, int h,
-                                         float (&out)[32]) {
+constexpr int C = kEpiCols;   // columns per epilogue thread and tile
+
+// The C L values of column group g of the staged tile, box row lr (128-byte
+// swizzle: 16-byte chunk c of a row sits at c ^ (lr & 7)).
+__device__ __forceinline__ void load_l(const uint8_t* sl, uint32_t l_box_bytes, int l_fp32, int lr, int g,
+                                       float (&out)[C]) {
     if (!l_fp32) {
         const uint8_t* rowp = sl + lr * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const int chunk = h * 4 + c;
+        for (int c = 0; c < C / 8; ++c) {
+            const int chunk = g * (C / 8) + c;
             const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((chunk ^ (lr & 7)) << 4));
             out[c * 8 + 0] = bf_lo(v.x);
             out[c * 8 + 1] = bf_hi(v.x);
@@ -100,11 +102,13 @@ __device__ __forceinline__ void load_l32(const uint8_t* sl, uint32_t l_box_bytes
             out[c * 8 + 6] = bf_lo(v.w);
             out[c * 8 + 7] = bf_hi(v.w);
         }
-    } else {
-        const uint8_t* rowp = sl + h * l_box_bytes + lr * 128;
+    } else {   // two boxes of 32 fp32 columns
+        const int col0 = g * C;
+        const uint8_t* rowp = sl + (col0 >> 5) * l_box_bytes + lr * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const float4 v = *reinterpret_cast<const float4*>(rowp + ((c ^ (lr & 7)) << 4));
+        for (int c = 0; c < C / 4; ++c) {
+            const int chunk = ((col0 & 31) >> 2) + c;
+            const float4 v = *reinterpret_cast<const float4*>(rowp + ((chunk ^ (lr & 7)) << 4));
             out[c * 4 + 0] = v.x;
             out[c * 4 + 1] = v.y;
             out[c * 4 + 2] = v.z;
@@ -113,13 +117,13 @@ __device__ __forceinline__ void load_l32(const uint8_t* sl, uint32_t l_box_bytes
     }
 }
 
-// 32 consecutive elements of a global row (bf16 or fp32) starting at v0;
+// C consecutive elements of a global row (bf16 or fp32) starting at v0;
 // entries at or past V read as 0 (callers mask them).
-__device__ __forceinline__ void load_g32(const void* base, int fp32, size_t off, int v0, int V, float (&out)[32]) {
+__device__ __forceinline__ void load_g(const void* base, int fp32, size_t off, int v0, int V, float (&out)[C]) {
     if (!fp32) {
         const uint16_t* p = static_cast<const uint16_t*>(base) + off;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < C / 8; ++c) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (v0 + c * 8 < V) v = __ldg(reinterpret_cast<const uint4*>(p + v0 + c * 8));
             out[c * 8 + 0] = bf_lo(v.x);
@@ -134,7 +138,7 @@ __device__ __forceinline__ void load_g32(const void* base, int fp32, size_t off,
     } else {
         const float* p = static_cast<const float*>(base) + off;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < C / 4; ++c) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
             if (v0 + c * 4 < V) v = __ldg(reinterpret_cast<const float4*>(p + v0 + c * 4));
             out[c * 4 + 0] = v.x;
@@ -149,31 +153,31 @@ __device__ __forceinline__ void load_g32(const void* base, int fp32, size_t off,
 template <int MODE>
 struct Epi;
 
-// Maximum of 32 values as a balanced tree (no serial dependency chain).
-__device__ __forceinline__ float max32(const float (&z)[32]) {
-    float t[16];
+// Maximum of C values as a balanced tree (no serial dependency chain).
+__device__ __forceinline__ float maxc(const float (&z)[C]) {
+    float t[C / 2];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) t[j] = fmaxf(z[j], z[j + 16]);
+    for (int j = 0; j < C / 2; ++j) t[j] = fmaxf(z[j], z[j + C / 2]);
 #pragma unroll
-    for (int w = 8; w > 0; w >>= 1)
+    for (int w = C / 4; w > 0; w >>= 1)
 #pragma unroll
         for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
     return t[0];
 }
 
 // Lowest j with z[j] == m (m is one of the z).
-__device__ __forceinline__ int first_index_of(const float (&z)[32], float m) {
-    int jj = 31;
+__device__ __forceinline__ int first_index_of(const float (&z)[C], float m) {
+    int jj = C - 1;
 #pragma unroll
-    for (int j = 31; j >= 0; --j)
+    for (int j = C - 1; j >= 0; --j)
         if (z[j] == m) jj = j;
     return jj;
 }
 
-__device__ __forceinline__ void mask_tail(float (&z)[32], int vbase, int V) {
-    if (vbase + 32 > V) {
+__device__ __forceinline__ void mask_tail(float (&z)[C], int vbase, int V) {
+    if (vbase + C > V) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < C; ++j)
             if (vbase + j >= V) z[j] = -INFINITY;
     }
 }
@@ -181,7 +185,7 @@ __device__ __forceinline__ void mask_tail(float (&z)[32], int vbase, int V) {
 template <>
 struct Epi<MODE_CHAIN_GREEDY> {
     bool valid;
-    int half;
+    int group;
     float best;
     uint32_t best_v;
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
@@ -189,15 +193,15 @@ struct Epi<MODE_CHAIN_GREEDY> {
         best = -INFINITY;
         best_v = 0;
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
-                            const uint32_t (&acc)[32]) {
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+                                            int g, const uint32_t (&acc)[C]) {
         if (!valid) return;
-        float z[32];
-        load_l32(sl, lbb, p.l_fp32, lrow, h, z);
+        float z[C];
+        load_l(sl, lbb, p.l_fp32, lrow, g, z);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
+        for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
         mask_tail(z, vbase, p.V);
-        const float m = max32(z);
+        const float m = maxc(z);
         if (m > best) {   // strict: an earlier (lower) id keeps a tie
             best = m;
             best_v = static_cast<uint32_t>(vbase + first_index_of(z, m));
@@ -208,13 +212,17 @@ struct Epi<MODE_CHAIN_GREEDY> {
     }
 };
 
+// Race filter (see one_minus_uniform): exp(z_v - b) is formed as
+// exp(z_v - m) exp(m - b) with m the running maximum of z, the first factor
+// being the log-sum-exp term already at hand.
 template <>
 struct Epi<MODE_CHAIN_SAMPLE> {
     bool valid;
-    int half;
+    int group;
     float best;
     uint32_t best_v;
     float m, s;
+    float g2;     // 2 exp(m - best): an element passes the race filter if 1 - u < exp(z - m) g2
     RngKey key;
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R;
@@ -222,40 +230,49 @@ struct Epi<MODE_CHAIN_SAMPLE> {
         best_v = 0;
         m = -INFINITY;
         s = 0.f;
+        g2 = INFINITY;
         key = RngKey{p.rng_k0, p.rng_k1, p.rng_cycle};
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
-                            const uint32_t (&acc)[32]) {
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+                                            int g, const uint32_t (&acc)[C]) {
         if (!valid) return;
-        float lv[32];
-        load_l32(sl, lbb, p.l_fp32, lrow, h, lv);
+        float lv[C];
+        load_l(sl, lbb, p.l_fp32, lrow, g, lv);
         const int grow = lrow + blockIdx.y * kTileM;
-        float zt[32];
+        float zt[C];
         float mx = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < C; ++j) {
             zt[j] = (lv[j] + __uint_as_float(acc[j])) * p.inv_t;
             if (vbase + j < p.V) mx = fmaxf(mx, zt[j]);
         }
         if (mx > m) {
             s *= __expf(m - mx);
             m = mx;
+            g2 = 2.0f * __expf(m - best);
         }
+        U4 blk[C / 4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < C / 4; ++c)   // independent blocks: their rounds interleave
+            blk[c] = philox_block(key, 0u, static_cast<uint32_t>(grow), static_cast<uint32_t>(p.d),
+                                  static_cast<uint32_t>(vbase + c * 4) >> 2);
+#pragma unroll
+        for (int c = 0; c < C / 4; ++c) {
             const int v4 = vbase + c * 4;
             if (v4 >= p.V) break;
-            const U4 blk = philox_block(key, 0u, static_cast<uint32_t>(grow), static_cast<uint32_t>(p.d),
-                                        static_cast<uint32_t>(v4) >> 2);
-            const uint32_t w[4] = {blk.x, blk.y, blk.z, blk.w};
+            const uint32_t w[4] = {blk[c].x, blk[c].y, blk[c].z, blk[c].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const float z = zt[c * 4 + q];
-                s += __expf(z - m);
-                const float k = z - race_log_exp(word_to_uniform(w[q]));
-                if (k > best) {
-                    best = k;
-                    best_v = static_cast<uint32_t>(v4 + q);
+                const float e = __expf(z - m);
+                s += e;
+                if (one_minus_uniform(w[q]) < e * g2) {   // else the key cannot beat best
+                    const float k = z - race_log_exp(word_to_uniform(w[q]));
+                    if (k > best) {
+                        best = k;
+                        best_v = static_cast<uint32_t>(v4 + q);
+                        g2 = 2.0f * __expf(m - best);
+                    }
                 }
             }
         }
@@ -264,16 +281,16 @@ struct Epi<MODE_CHAIN_SAMPLE> {
         if (!valid) return;
         const size_t o = static_cast<size_t>(p.d - 1) * p.R + grow;
         atomicMax(&p.keys[o], argmax_key(best, best_v));
-        p.lse_part[(o * gridDim.x + blockIdx.x) * 2 + half] = make_float2(m, s);
+        p.lse_part[(o * gridDim.x + blockIdx.x) * kColGroups + group] = make_float2(m, s);
     }
 };
 
 template <>
 struct Epi<MODE_TREE> {
     bool valid;
-    int half;
+    int group;
     float m, s;
-    float thresh;                 // current k-th best z (entry to the top-k)
+    float thresh;                 // current 8th best z (entry to the top-8)
     float tv[kMaxTopK];
     uint32_t ti[kMaxTopK];
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
@@ -287,36 +304,29 @@ struct Epi<MODE_TREE> {
             ti[q] = 0xffffffffu;
         }
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase, int h,
-                            const uint32_t (&acc)[32]) {
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+                                            int g, const uint32_t (&acc)[C]) {
         if (!valid) return;
-        float z[32];
-        load_l32(sl, lbb, p.l_fp32, lrow / p.P, h, z);
+        float z[C];
+        load_l(sl, lbb, p.l_fp32, lrow / p.P, g, z);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) z[j] = z[j] + __uint_as_float(acc[j]);
+        for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);
         mask_tail(z, vbase, p.V);
-        const float mx = max32(z);
+        const float mx = maxc(z);
         if (mx > m) {
             s *= __expf(m - mx);
             m = mx;
         }
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < 32; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
+        for (int j = 0; j < C; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
         s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         // The kernel keeps a sorted top-8 (value desc, lower id first); its first
         // k entries are the top-k for any k <= 8.
         if (mx > thresh) {   // some entry enters the top-8 (rare once it has filled)
-            uint32_t cand = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cand |= (z[j] > thresh ? 1u : 0u) << j;
-            while (cand) {
-                const int j = __ffs(cand) - 1;   // ascending ids: earlier ties stay ahead
-                cand &= cand - 1;
-                float cz = 0.f;
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj)
-                    if (jj == j) cz = z[jj];
+            for (int j = 0; j < C; ++j) {   // ascending ids: earlier ties stay ahead
+                float cz = z[j];
                 if (!(cz > thresh)) continue;
                 uint32_t cv = static_cast<uint32_t>(vbase + j);
 #pragma unroll
@@ -336,7 +346,8 @@ struct Epi<MODE_TREE> {
     }
     __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
         if (!valid) return;
-        float* rec = p.tree_part + ((static_cast<size_t>(grow) * gridDim.x + blockIdx.x) * 2 + half) * (2 + 2 * kMaxTopK);
+        float* rec = p.tree_part +
+                     ((static_cast<size_t>(grow) * gridDim.x + blockIdx.x) * kColGroups + group) * (2 + 2 * kMaxTopK);
         rec[0] = m;
         rec[1] = s;
 #pragma unroll
@@ -350,7 +361,7 @@ struct Epi<MODE_TREE> {
 template <>
 struct Epi<MODE_RESID> {
     bool valid;
-    int half;
+    int group;
     float best;
     uint32_t best_v;
     int jpos;
@@ -371,14 +382,14 @@ struct Epi<MODE_RESID> {
         }
     }
     __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int lrow, int vbase, int,
-                            const uint32_t (&acc)[32]) {
+                                            const uint32_t (&acc)[C]) {
         if (!valid) return;
         const int grow = lrow + blockIdx.y * kTileM;
-        float lv[32], tv[32];
-        load_g32(p.L, p.l_fp32, l_off, vbase, p.V, lv);
-        load_g32(p.target, p.t_fp32, t_off, vbase, p.V, tv);
+        float lv[C], tv[C];
+        load_g(p.L, p.l_fp32, l_off, vbase, p.V, lv);
+        load_g(p.target, p.t_fp32, t_off, vbase, p.V, tv);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < C / 4; ++c) {
             const int v4 = vbase + c * 4;
             if (v4 >= p.V) break;
             const U4 blk = philox_block(key, 2u, static_cast<uint32_t>(grow), static_cast<uint32_t>(jpos),
@@ -389,7 +400,9 @@ struct Epi<MODE_RESID> {
                 const int j = c * 4 + q;
                 const float lq = (lv[j] + __uint_as_float(acc[j])) * p.inv_t - lse_q;   // log q_v
                 const float lp = tv[j] * p.inv_t - lse_p;                                 // log p_v
-                if (lp > lq) {
+                // race filter with p - q <= p: the key cannot beat best
+                // unless 1 - u < 2 exp(log p - best)
+                if (lp > lq && one_minus_uniform(w[q]) < 2.0f * __expf(lp - best)) {
                     // log(p - q) = log p + log(1 - q/p)
                     const float k = lp + log1pf(-__expf(lq - lp)) - race_log_exp(word_to_uniform(w[q]));
                     if (k > best) {
@@ -408,7 +421,7 @@ struct Epi<MODE_RESID> {
 template <>
 struct Epi<MODE_ABSMAX> {
     bool valid;
-    int half;
+    int group;
     float best;
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.rows;
@@ -417,13 +430,13 @@ struct Epi<MODE_ABSMAX> {
     // Columns past V hold 0 (the W tile's out-of-range fill), which never
     // raises a maximum of absolute values.
     __device__ __forceinline__ void consume(const GemmParams&, const uint8_t*, uint32_t, int, int, int,
-                                            const uint32_t (&acc)[32]) {
-        float t[16];
+                                            const uint32_t (&acc)[C]) {
+        float t[C / 2];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            t[j] = fmaxf(fabsf(__uint_as_float(acc[j])), fabsf(__uint_as_float(acc[j + 16])));
+        for (int j = 0; j < C / 2; ++j)
+            t[j] = fmaxf(fabsf(__uint_as_float(acc[j])), fabsf(__uint_as_float(acc[j + C / 2])));
 #pragma unroll
-        for (int w = 8; w > 0; w >>= 1)
+        for (int w = C / 4; w > 0; w >>= 1)
 #pragma unroll
             for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
         best = fmaxf(best, t[0]);
@@ -554,14 +567,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
     } else {
         // 4. epilogue: thread = GEMM row (TMEM lane of its sub-partition
-        //    warp % 4); warps 2-5 take columns 0-31 of every tile, 6-9 32-63
+        //    warp % 4); column group g = (warp - 2) / 4 takes columns
+        //    [16 g, 16 g + 16) of every tile
         const int q = warp & 3;
-        const int h = (warp - 2) >> 2;
+        const int g = (warp - 2) >> 2;
         const int lrow = q * 32 + lane;
         const int grow = row0 + lrow;
         Epi<MODE> st;
         st.init(p, grow);
-        st.half = h;
+        st.group = g;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         for (int i = 0; i < nt; ++i) {
             const int s = i % p.stages;
@@ -576,10 +590,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             tc_fence_after();
             const uint8_t* sl = smem + lay.a_bytes + s * lay.stage_bytes + lay.w_bytes;
             const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
-            uint32_t acc[32];
-            tmem_ld32(lane_addr + static_cast<uint32_t>(b * kTileN + h * 32), acc);
+            uint32_t acc[C];
+            tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + g * C), acc);
             tmem_ld_wait();
-            st.consume(p, sl, lay.l_box_bytes, lrow, v0 + h * 32, h, acc);
+            st.consume(p, sl, lay.l_box_bytes, lrow, v0 + g * C, g, acc);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {

@@ -58,7 +58,7 @@ __global__ void chain_finalize_kernel(const unsigned long long* keys, const floa
 // ---------------------------------------------------------------------------
 // scheduler: one CTA
 // ---------------------------------------------------------------------------
-constexpr int kSchedThreads = 1024;
+constexpr int kSchedThreads = 1024;   // most threads; a launch uses min(1024, max(64, n_pad))
 
 __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* conf, int R, int gamma,
                                                                  const double* cost, float* survival,
@@ -67,31 +67,40 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
     extern __shared__ unsigned long long sk[];              // n_pad sort keys
     unsigned long long* part = sk + n_pad;                   // kSchedThreads partial sums
     int* cnt = reinterpret_cast<int*>(part + kSchedThreads);  // R counters
+    float* s_surv = reinterpret_cast<float*>(cnt + R);       // R * gamma confidences, then survivals
+    float* fq = s_surv + R * gamma;                          // n_pad + 1 fp32 screens of f(m)
     __shared__ int m_star;
     __shared__ int n_cand;
-    const int tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, nt = blockDim.x;
     const int n = R * gamma;
     const float floor_s = 1.0f / 262144.0f;                 // 2^-18
 
-    // survival S_{i,k} = S_{i,k-1} c_{i,k}, fp32, left to right
-    for (int i = tid; i < R; i += kSchedThreads) {
-        float s = 1.0f;
-        for (int k = 0; k < gamma; ++k) {
-            s = __fmul_rn(s, conf[static_cast<size_t>(i) * gamma + k]);
-            survival[static_cast<size_t>(i) * gamma + k] = s;
-            const uint32_t id = static_cast<uint32_t>(i * gamma + k);
-            sk[i * gamma + k] = (s >= floor_s) ? ((static_cast<unsigned long long>(__float_as_uint(s)) << 32) | ~id) : 0ull;
-        }
-        cnt[i] = 0;
-    }
-    for (int t = n + tid; t < n_pad; t += kSchedThreads) sk[t] = 0ull;
+    // all confidences in one coalesced pass (no dependent global loads below)
+    for (int t = tid; t < n; t += nt) s_surv[t] = conf[t];
+    for (int i = tid; i < R; i += nt) cnt[i] = 0;
+    for (int t = n + tid; t < n_pad; t += nt) sk[t] = 0ull;
     if (tid == 0) {
         m_star = 0x7fffffff;
         n_cand = 0;
     }
     __syncthreads();
+    // survival S_{i,k} = S_{i,k-1} c_{i,k}, fp32, left to right
+    for (int i = tid; i < R; i += nt) {
+        float s = 1.0f;
+        for (int k = 0; k < gamma; ++k) {
+            const int t = i * gamma + k;
+            s = __fmul_rn(s, s_surv[t]);
+            s_surv[t] = s;
+            sk[t] = (s >= floor_s) ? ((static_cast<unsigned long long>(__float_as_uint(s)) << 32) | ~static_cast<uint32_t>(t))
+                                   : 0ull;
+        }
+    }
+    __syncthreads();
+    for (int t = tid; t < n; t += nt) survival[t] = s_surv[t];
     // bitonic sort, descending (S desc, then request asc, position asc)
-    if (n_pad <= kSchedThreads) {
+    if (n_pad <= nt) {
         // one key per thread: partners closer than a warp swap by shuffle
         unsigned long long key = tid < n_pad ? sk[tid] : 0ull;
         for (int size = 2; size <= n_pad; size <<= 1) {
@@ -114,7 +123,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
     } else {
         for (int size = 2; size <= n_pad; size <<= 1) {
             for (int stride = size >> 1; stride > 0; stride >>= 1) {
-                for (int t = tid; t < n_pad; t += kSchedThreads) {
+                for (int t = tid; t < n_pad; t += nt) {
                     const int u = t ^ stride;
                     if (u > t) {
                         const bool desc = (t & size) == 0;
@@ -130,12 +139,12 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
         }
     }
     // number of ranked survivals
-    for (int t = tid; t < n_pad; t += kSchedThreads)
+    for (int t = tid; t < n_pad; t += nt)
         if (sk[t] != 0ull && (t + 1 == n_pad || sk[t + 1] == 0ull)) n_cand = t + 1;
     __syncthreads();
     const int M = n_cand;
     // exact prefix sums: a survival >= 2^-18 is an integer multiple of 2^-41
-    const int per = (n_pad + kSchedThreads - 1) / kSchedThreads;
+    const int per = (n_pad + nt - 1) / nt;
     unsigned long long local = 0;
     for (int q = 0; q < per; ++q) {
         const int t = tid * per + q;
@@ -153,8 +162,8 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
         }
         if (lane == 31) part[warp] = x;
         __syncthreads();
-        if (warp == 0) {
-            unsigned long long wv = part[lane];
+        if (warp == 0) {   // lanes past the last warp hold 0
+            unsigned long long wv = lane < (nt >> 5) ? part[lane] : 0ull;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const unsigned long long y = __shfl_up_sync(0xffffffffu, wv, o);
@@ -169,35 +178,60 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
     }
     __syncthreads();
     // f(m) = E(m) / cost[R + m]; the greedy stops at the first m whose next
-    // survival does not raise f strictly.
+    // survival does not raise f strictly (compared as fp64 quotients).  Each
+    // f(m) is first formed in fp32 (relative error < 2^-22); when two
+    // neighbours differ by more than 2^-20 relative, the fp64 quotients
+    // order the same way, and only closer pairs are divided in fp64 (fp64
+    // throughput is low on this part).
+    const double two_m41 = 4.547473508864641e-13;   // 2^-41
+    const unsigned long long base = static_cast<unsigned long long>(R) << 41;
+    auto f32_of = [&](unsigned long long e_int, int m) {
+        return __fdiv_rn(__ull2float_rn(e_int) * 4.547473508864641e-13f, __double2float_rn(cost[R + m]));
+    };
     {
         unsigned long long run = part[tid];
-        const double two_m41 = 4.547473508864641e-13;   // 2^-41
-        const unsigned long long base = static_cast<unsigned long long>(R) << 41;
         for (int q = 0; q < per; ++q) {
             const int m = tid * per + q;              // E(m) uses the first m survivals
             if (m >= M) break;
+            fq[m] = f32_of(base + run, m);
+            run += static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[m] >> 32)), 41));
+            if (m == M - 1) fq[M] = f32_of(base + run, M);
+        }
+    }
+    __syncthreads();
+    {
+        unsigned long long run = part[tid];
+        for (int q = 0; q < per; ++q) {
+            const int m = tid * per + q;
+            if (m >= M) break;
             const unsigned long long s_int =
                 static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[m] >> 32)), 41));
-            const double e0 = static_cast<double>(base + run) * two_m41;
-            const double e1 = static_cast<double>(base + run + s_int) * two_m41;
-            const double f0 = __ddiv_rn(e0, cost[R + m]);
-            const double f1 = __ddiv_rn(e1, cost[R + m + 1]);
-            if (!(f1 > f0)) atomicMin(&m_star, m);
+            const float g0 = fq[m], g1 = fq[m + 1];
+            bool up;
+            if (g1 > g0 * 1.00000095367431640625f) {
+                up = true;
+            } else if (g1 < g0 * 0.99999904632568359375f) {
+                up = false;
+            } else {
+                const double f0 = __ddiv_rn(static_cast<double>(base + run) * two_m41, cost[R + m]);
+                const double f1 = __ddiv_rn(static_cast<double>(base + run + s_int) * two_m41, cost[R + m + 1]);
+                up = f1 > f0;
+            }
+            if (!up) atomicMin(&m_star, m);
             run += s_int;
         }
     }
     __syncthreads();
     const int ms = (m_star == 0x7fffffff) ? M : m_star;
-    for (int t = tid; t < ms; t += kSchedThreads) {
+    for (int t = tid; t < ms; t += nt) {
         const uint32_t id = ~static_cast<uint32_t>(sk[t] & 0xffffffffull);
         atomicAdd(&cnt[id / gamma], 1);
     }
     __syncthreads();
-    for (int i = tid; i < R; i += kSchedThreads) budget[i] = cnt[i];
+    for (int i = tid; i < R; i += nt) budget[i] = cnt[i];
     if (tid == 0) {
         // prefix at m*: the owning thread's exclusive prefix plus its first entries
-        const int owner = ms / per < kSchedThreads ? ms / per : kSchedThreads - 1;
+        const int owner = ms / per < nt ? ms / per : nt - 1;
         unsigned long long sum = part[owner];
         for (int t = owner * per; t < ms; ++t)
             sum += static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(sk[t] >> 32)), 41));
@@ -209,7 +243,7 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
 // ---------------------------------------------------------------------------
 // ragged pack: one CTA
 // ---------------------------------------------------------------------------
-constexpr int kPackThreads = 1024;
+constexpr int kPackThreads = 256;
 
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* anchor, const int32_t* draft,
                                                             const int32_t* budget, int R, int gamma,
@@ -218,9 +252,12 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
                                                             int capacity, int32_t* tier, int32_t* dev_status) {
     __shared__ int warp_sum[32];
     __shared__ int s_total, s_tier;
+    __shared__ int s_start[kPackThreads], s_n[kPackThreads];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     int carry = 0;
-    // exclusive scan of (n_i + 1), 1024 requests per pass
+    // exclusive scan of (n_i + 1), kPackThreads requests per pass
     for (int base = 0; base < R; base += kPackThreads) {
         const int i = base + tid;
         int n = 0;
@@ -240,8 +277,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
         }
         if (lane == 31) warp_sum[warp] = x;
         __syncthreads();
-        if (warp == 0) {
-            int w = warp_sum[lane];
+        if (warp == 0) {   // lanes past the last warp hold 0
+            int w = lane < kPackThreads / 32 ? warp_sum[lane] : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int y = __shfl_up_sync(0xffffffffu, w, o);
@@ -252,29 +289,42 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
         __syncthreads();
         const int incl = x + (warp > 0 ? warp_sum[warp - 1] : 0) + carry;
         const int start = incl - len;
-        if (i < R) {
-            cu[i] = start;
-            for (int p = 0; p <= n; ++p) {
-                const int row = start + p;
-                if (row >= capacity) {
-                    set_status(dev_status, SDM_DEV_CAPACITY);
-                    break;
-                }
-                ptok[row] = (p == 0) ? anchor[i] : draft[static_cast<size_t>(i) * gamma + p - 1];
-                preq[row] = i;
-                ppos[row] = p;
+        if (i < R) cu[i] = start;
+        s_start[tid] = start;
+        s_n[tid] = (i < R) ? n : -1;
+        __syncthreads();
+        // one (request, position) pair per thread: the loads are independent
+        const int per = gamma + 1;
+        const int chunk_r = min(kPackThreads, R - base);
+        for (int idx = tid; idx < chunk_r * per; idx += kPackThreads) {
+            const int il = idx / per, p = idx - il * per;
+            if (p > s_n[il]) continue;
+            const int row = s_start[il] + p;
+            if (row < 0 || row >= capacity) {
+                set_status(dev_status, SDM_DEV_CAPACITY);
+                continue;
             }
+            const int ig = base + il;
+            ptok[row] = (p == 0) ? anchor[ig] : draft[static_cast<size_t>(ig) * gamma + p - 1];
+            preq[row] = ig;
+            ppos[row] = p;
         }
-        const int chunk_total = warp_sum[31];
+        const int chunk_total = warp_sum[kPackThreads / 32 - 1];
         __syncthreads();
         carry += chunk_total;
     }
+    // the smallest tier that holds the total (the tiers are read in parallel)
+    if (tid == 0) s_tier = 0x7fffffff;
+    __syncthreads();
+    for (int q = tid; q < n_tiers; q += kPackThreads) {
+        const int tq = tiers[q];
+        if (tq >= carry) atomicMin(&s_tier, tq);
+    }
+    __syncthreads();
     if (tid == 0) {
         cu[R] = carry;
-        int t = -1;
-        for (int q = 0; q < n_tiers; ++q)
-            if (tiers[q] >= carry && (t < 0 || tiers[q] < t)) t = tiers[q];
-        if (t < 0) {
+        int t = s_tier;
+        if (t == 0x7fffffff) {
             t = carry;
             set_status(dev_status, SDM_DEV_TIER_UNCAPTURED);
         }
@@ -292,11 +342,19 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
     }
 }
 
-// Argmax token of a row from its per-chunk partial keys.
+// Argmax token of a row from its per-chunk partial keys (eight loads in
+// flight at a time).
 __device__ __forceinline__ int row_token(const unsigned long long* part, size_t row, int n_chunks) {
-    unsigned long long k = 0;
-    for (int c = 0; c < n_chunks; ++c) k = umax64(k, part[row * n_chunks + c]);
-    return static_cast<int>(key_token(k));
+    const unsigned long long* q = part + row * n_chunks;
+    unsigned long long k[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (c0 + j < n_chunks) k[j] = umax64(k[j], q[c0 + j]);
+    }
+#pragma unroll
+    for (int j = 1; j < 8; ++j) k[0] = umax64(k[0], k[j]);
+    return static_cast<int>(key_token(k[0]));
 }
 
 // ---------------------------------------------------------------------------
@@ -307,6 +365,8 @@ __global__ void verify_greedy_finalize_kernel(int mode, const int32_t* cu, const
                                               int R, int gamma, int V, int32_t* accept, int32_t* ceiling,
                                               int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
     // one warp per request: lane p resolves window rows p, p + 32, ...
+    pdl_wait();
+    pdl_trigger();
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= R) return;
@@ -479,22 +539,25 @@ __device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
     return a.rank < b.rank;
 }
 
-// One CTA per request, one warp per frontier slot.
+// One CTA per request, one warp per frontier slot.  Each lane merges its
+// share of the vocab-split records (log-sum-exp and a sorted top-k); the warp
+// then takes its top-k in k rounds of a warp argmax over the lanes' heads;
+// finally the nf * k children are ranked in parallel and the best P kept.
 __global__ void tree_merge_kernel(const float* tree_part, int gx, int R, int P, int k, int B, int d,
                                   int32_t* front_tok, int32_t* front_node, float* front_score, int32_t* n_front,
                                   int32_t* pool_tok, int32_t* pool_parent, int32_t* pool_depth, float* pool_score,
                                   int32_t* pool_n) {
     extern __shared__ float tm_smem[];
-    float* lane_z = tm_smem;                                          // [P][32][k]
-    uint32_t* lane_id = reinterpret_cast<uint32_t*>(lane_z + P * 32 * k);
-    Cand* cand = reinterpret_cast<Cand*>(lane_id + P * 32 * k);      // [P * k]
+    Cand* cand = reinterpret_cast<Cand*>(tm_smem);                   // [P * k] children
+    Cand* sorted = cand + P * k;                                     // [P * k] in rank order
+    int* parent_node = reinterpret_cast<int*>(sorted + P * k);       // [P]
     const int i = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nf = n_front[i];
     constexpr int REC = 2 + 2 * kMaxTopK;
+    if (warp < P) parent_node[warp] = front_node[static_cast<size_t>(i) * P + warp];
     if (warp < nf) {
         const int grow = i * P + warp;
-        // lane-local merge over the vocab splits c = lane, lane + 32, ...
         Lse acc{-INFINITY, 0.f};
         float tz[kMaxTopK];
         uint32_t ti[kMaxTopK];
@@ -505,10 +568,19 @@ __global__ void tree_merge_kernel(const float* tree_part, int gx, int R, int P, 
         }
         for (int c = lane; c < gx; c += 32) {
             const float* rec = tree_part + (static_cast<size_t>(grow) * gx + c) * REC;
+            float rz[kMaxTopK];
+            uint32_t rv[kMaxTopK];
+#pragma unroll
+            for (int q = 0; q < kMaxTopK; ++q) {   // loads first
+                rz[q] = q < k ? rec[2 + q] : -INFINITY;
+                rv[q] = q < k ? __float_as_uint(rec[2 + kMaxTopK + q]) : 0xffffffffu;
+            }
             acc = lse_merge(acc, Lse{rec[0], rec[1]});
-            for (int q = 0; q < k; ++q) {
-                float cz = rec[2 + q];
-                uint32_t cv = __float_as_uint(rec[2 + kMaxTopK + q]);
+#pragma unroll
+            for (int q = 0; q < kMaxTopK; ++q) {
+                if (q >= k) break;
+                float cz = rz[q];
+                uint32_t cv = rv[q];
 #pragma unroll
                 for (int e = 0; e < kMaxTopK; ++e) {
                     if (e < k && (cz > tz[e] || (cz == tz[e] && cv < ti[e]))) {
@@ -523,78 +595,66 @@ __global__ void tree_merge_kernel(const float* tree_part, int gx, int R, int P, 
             }
         }
         acc = warp_lse(acc);
+        const float lse = acc.m + logf(acc.s);
+        const float sp = front_score[static_cast<size_t>(i) * P + warp];
+        // k rounds: the best head over the lanes is popped by its lane (ids
+        // are distinct across lanes, so exactly one lane matches)
         for (int q = 0; q < k; ++q) {
-            lane_z[(warp * 32 + lane) * k + q] = tz[q];
-            lane_id[(warp * 32 + lane) * k + q] = ti[q];
-        }
-        __syncwarp();
-        if (lane == 0) {
-            float bz[kMaxTopK];
-            uint32_t bi[kMaxTopK];
-            for (int q = 0; q < kMaxTopK; ++q) {
-                bz[q] = -INFINITY;
-                bi[q] = 0xffffffffu;
-            }
-            for (int e = 0; e < 32 * k; ++e) {
-                float cz = lane_z[warp * 32 * k + e];
-                uint32_t cv = lane_id[warp * 32 * k + e];
-                for (int q = 0; q < k; ++q) {
-                    if (cz > bz[q] || (cz == bz[q] && cv < bi[q])) {
-                        const float oz = bz[q];
-                        const uint32_t ov = bi[q];
-                        bz[q] = cz;
-                        bi[q] = cv;
-                        cz = oz;
-                        cv = ov;
-                    }
+            const unsigned long long mine = argmax_key(tz[0], ti[0]);
+            const unsigned long long best = warp_max_u64(mine);
+            if (mine == best) {
+#pragma unroll
+                for (int e = 0; e + 1 < kMaxTopK; ++e) {
+                    tz[e] = tz[e + 1];
+                    ti[e] = ti[e + 1];
                 }
+                tz[kMaxTopK - 1] = -INFINITY;
+                ti[kMaxTopK - 1] = 0xffffffffu;
             }
-            const float lse = acc.m + logf(acc.s);
-            const float sp = front_score[static_cast<size_t>(i) * P + warp];
-            for (int q = 0; q < k; ++q)   // s(c) = s(p) + log pi(v | p)
-                cand[warp * k + q] = Cand{sp + (bz[q] - lse), warp, q, static_cast<int>(bi[q])};
+            if (lane == 0)   // s(c) = s(p) + log pi(v | p)
+                cand[warp * k + q] = Cand{sp + (key_value(best) - lse), warp, q, static_cast<int>(key_token(best))};
+        }
+    }
+    __syncthreads();
+    // rank of every child by (s desc, slot asc, rank asc): a strict total order
+    const int nc = nf * k;
+    for (int t = threadIdx.x; t < nc; t += blockDim.x) {
+        const Cand me = cand[t];
+        int rk = 0;
+        for (int u = 0; u < nc; ++u) rk += cand_before(cand[u], me) ? 1 : 0;
+        sorted[rk] = me;
+    }
+    __syncthreads();
+    const int keep = nc < P ? nc : P;
+    const int pool_cap = 1 + P * B;
+    const size_t pb = static_cast<size_t>(i) * pool_cap;
+    const int np = pool_n[i];
+    for (int c = threadIdx.x; c < P; c += blockDim.x) {
+        const size_t fo = static_cast<size_t>(i) * P + c;
+        if (c < keep) {
+            const Cand cd = sorted[c];
+            pool_tok[pb + np + c] = cd.tok;
+            pool_parent[pb + np + c] = parent_node[cd.slot];
+            pool_depth[pb + np + c] = d;
+            pool_score[pb + np + c] = cd.s;
+            front_tok[fo] = cd.tok;
+            front_node[fo] = np + c;
+            front_score[fo] = cd.s;
+        } else {
+            front_tok[fo] = -1;
+            front_node[fo] = -1;
         }
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int nc = nf * k;
-        // insertion sort by (s desc, slot asc, rank asc), keep P
-        for (int a = 1; a < nc; ++a) {
-            const Cand t = cand[a];
-            int b = a;
-            while (b > 0 && cand_before(t, cand[b - 1])) {
-                cand[b] = cand[b - 1];
-                --b;
-            }
-            cand[b] = t;
-        }
-        const int keep = nc < P ? nc : P;
-        const int pool_cap = 1 + P * B;
-        const size_t pb = static_cast<size_t>(i) * pool_cap;
-        int np = pool_n[i];
-        int parent_node[64];
-        for (int c = 0; c < nf && c < 64; ++c) parent_node[c] = front_node[static_cast<size_t>(i) * P + c];
-        for (int c = 0; c < keep; ++c) {
-            pool_tok[pb + np] = cand[c].tok;
-            pool_parent[pb + np] = parent_node[cand[c].slot];
-            pool_depth[pb + np] = d;
-            pool_score[pb + np] = cand[c].s;
-            front_tok[static_cast<size_t>(i) * P + c] = cand[c].tok;
-            front_node[static_cast<size_t>(i) * P + c] = np;
-            front_score[static_cast<size_t>(i) * P + c] = cand[c].s;
-            ++np;
-        }
-        for (int c = keep; c < P; ++c) {
-            front_tok[static_cast<size_t>(i) * P + c] = -1;
-            front_node[static_cast<size_t>(i) * P + c] = -1;
-        }
         n_front[i] = keep;
-        pool_n[i] = np;
+        pool_n[i] = np + keep;
     }
 }
 
 // One CTA per request: rank the pool by (score desc, depth asc, creation asc),
 // keep the top N, emit root + nodes in rank order and the tree-causal mask.
+// The pool is staged in shared memory first.
 __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* pool_tok, const int32_t* pool_parent,
                                      const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
                                      int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
@@ -603,22 +663,31 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
     const int pool_cap = 1 + P * B;
     int* slot_of = tf_smem;               // pool index -> output slot (-1: not selected)
     int* node_at = slot_of + pool_cap;    // output slot -> pool index
+    int* s_par = node_at + (N + 1);       // pool parents
+    int* s_dep = s_par + pool_cap;        // pool depths
+    float* s_sc = reinterpret_cast<float*>(s_dep + pool_cap);   // pool scores
     const int i = blockIdx.x;
     const size_t pb = static_cast<size_t>(i) * pool_cap;
     const int np = pool_n[i];
     const int S = N + 1;
     const int take = (np - 1) < N ? (np - 1) : N;
-    for (int j = threadIdx.x; j < pool_cap; j += blockDim.x) slot_of[j] = -1;
+    for (int j = threadIdx.x; j < pool_cap; j += blockDim.x) {
+        slot_of[j] = -1;
+        if (j < np) {
+            s_par[j] = pool_parent[pb + j];
+            s_dep[j] = pool_depth[pb + j];
+            s_sc[j] = pool_score[pb + j];
+        }
+    }
     __syncthreads();
     for (int j = 1 + threadIdx.x; j < np; j += blockDim.x) {
-        const float sj = pool_score[pb + j];
-        const int dj = pool_depth[pb + j];
+        const float sj = s_sc[j];
+        const int dj = s_dep[j];
         int rank = 0;
         for (int q = 1; q < np; ++q) {
-            if (q == j) continue;
-            const float sq = pool_score[pb + q];
-            const int dq = pool_depth[pb + q];
-            if (sq > sj || (sq == sj && (dq < dj || (dq == dj && q < j)))) ++rank;
+            const float sq = s_sc[q];
+            const int dq = s_dep[q];
+            rank += (q != j && (sq > sj || (sq == sj && (dq < dj || (dq == dj && q < j))))) ? 1 : 0;
         }
         if (rank < take) {
             slot_of[j] = rank + 1;
@@ -634,63 +703,87 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
     const int words = (S + 31) / 32;
     for (int c = threadIdx.x; c < S; c += blockDim.x) {
         uint32_t* mrow = mask + (ob + c) * words;
-        for (int w = 0; w < words; ++w) mrow[w] = 0u;
         if (c <= take) {
             const int j = node_at[c];
             tok[ob + c] = pool_tok[pb + j];
-            const int pj = pool_parent[pb + j];
-            parent[ob + c] = (c == 0) ? -1 : slot_of[pj];
-            depth[ob + c] = pool_depth[pb + j];
-            score[ob + c] = (c == 0) ? 0.f : pool_score[pb + j];
-            for (int a = j; a >= 0; a = pool_parent[pb + a]) {
-                const int sa = slot_of[a];
-                if (sa >= 0) mrow[sa >> 5] |= 1u << (sa & 31);
+            parent[ob + c] = (c == 0) ? -1 : slot_of[s_par[j]];
+            depth[ob + c] = s_dep[j];
+            score[ob + c] = (c == 0) ? 0.f : s_sc[j];
+            for (int w = 0; w < words; ++w) {   // bit sa of the row: ancestors (and the node) in word w
+                uint32_t bits = 0u;
+                for (int a = j; a >= 0; a = (a == 0 ? -1 : s_par[a])) {
+                    const int sa = slot_of[a];
+                    if (sa >= 0 && (sa >> 5) == w) bits |= 1u << (sa & 31);
+                }
+                mrow[w] = bits;
             }
         } else {
             tok[ob + c] = -1;
             parent[ob + c] = -1;
             depth[ob + c] = -1;
             score[ob + c] = 0.f;
+            for (int w = 0; w < words; ++w) mrow[w] = 0u;
         }
     }
     if (threadIdx.x == 0) n_nodes[i] = take + 1;
 }
 
+// One warp per request: the tree (parents, tokens) and the target argmax of
+// every slot are staged in shared memory, then the walk follows, from the
+// root, the child whose token is the target's choice (lowest slot first).
 __global__ void tree_verify_walk_kernel(const unsigned long long* row_keys, int n_chunks, const int32_t* tok,
-                                        const int32_t* parent,
-                                        const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
-                                        int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= R) return;
+                                        const int32_t* parent, const int32_t* n_nodes, int R, int N, int B, int V,
+                                        int32_t* accept, int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
+    extern __shared__ int tw_smem[];
+    pdl_wait();
+    pdl_trigger();
     const int S = N + 1;
+    int* s_par = tw_smem;
+    int* s_tok = s_par + S;
+    int* s_rt = s_tok + S;
+    const int i = blockIdx.x;
+    const int lane = threadIdx.x;
     const size_t base = static_cast<size_t>(i) * S;
     int32_t* o = out_tok + static_cast<size_t>(i) * (B + 1);
     int nn = n_nodes[i];
     if (nn < 1 || nn > S) {
-        set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
         nn = nn < 1 ? 1 : S;
     }
-    int cur = 0, a = 0;
-    for (;;) {
-        int t = row_token(row_keys, base + cur, n_chunks);
+    for (int c = lane; c < nn; c += 32) {
+        s_par[c] = parent[base + c];
+        s_tok[c] = tok[base + c];
+        int t = row_token(row_keys, base + c, n_chunks);
         if (t < 0 || t >= V) {
             set_status(dev_status, SDM_DEV_BAD_TOKEN);
             t = 0;
         }
+        s_rt[c] = t;
+    }
+    __syncwarp();
+    int cur = 0, a = 0;
+    for (;;) {
+        const int t = s_rt[cur];
         int next = -1;
-        for (int c = 1; c < nn; ++c)
-            if (parent[base + c] == cur && tok[base + c] == t) {
-                next = c;
+        for (int c0 = 1; c0 < nn; c0 += 32) {
+            const int c = c0 + lane;
+            const bool hit = c < nn && s_par[c] == cur && s_tok[c] == t;
+            const unsigned bal = __ballot_sync(0xffffffffu, hit);
+            if (bal) {
+                next = c0 + __ffs(bal) - 1;
                 break;
             }
-        o[a] = t;
+        }
+        if (lane == 0) o[a] = t;
         if (next < 0 || a >= B) break;
         ++a;
         cur = next;
     }
-    for (int p = a + 1; p <= B; ++p) o[p] = -1;
-    accept[i] = a;
-    n_out[i] = a + 1;
+    for (int p = a + 1 + lane; p <= B; p += 32) o[p] = -1;
+    if (lane == 0) {
+        accept[i] = a;
+        n_out[i] = a + 1;
+    }
 }
 
 inline int blocks_for(long long n, int t) { return static_cast<int>((n + t - 1) / t); }
@@ -719,34 +812,33 @@ cudaError_t launch_schedule(const float* conf, int R, int gamma, const double* c
     (void)dev_status;
     int n_pad = 1;
     while (n_pad < R * gamma) n_pad <<= 1;
-    const size_t smem = static_cast<size_t>(n_pad) * 8 + kSchedThreads * 8 + static_cast<size_t>(R) * 4;
+    const size_t smem = static_cast<size_t>(n_pad) * 8 + kSchedThreads * 8 + static_cast<size_t>(R) * 4 +
+                        static_cast<size_t>(R) * gamma * 4 + (static_cast<size_t>(n_pad) + 1) * 4;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(schedule_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    schedule_kernel<<<1, kSchedThreads, smem, s>>>(conf, R, gamma, cost, survival, budget, expected, total_tokens,
-                                                   n_pad);
-    return cudaGetLastError();
+    const int nt = n_pad < 64 ? 64 : (n_pad > kSchedThreads ? kSchedThreads : n_pad);
+    return launch_pdl(schedule_kernel, dim3(1), dim3(nt), smem, s, conf, R, gamma, cost, survival, budget,
+                      expected, total_tokens, n_pad);
 }
 
 cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
                         const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
                         int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s) {
-    pack_kernel<<<1, kPackThreads, 0, s>>>(anchor, draft, budget, R, gamma, tiers, n_tiers, cu, ptok, preq, ppos,
-                                           capacity, tier, dev_status);
-    return cudaGetLastError();
+    return launch_pdl(pack_kernel, dim3(1), dim3(kPackThreads), 0, s, anchor, draft, budget, R, gamma, tiers, n_tiers,
+                      cu, ptok, preq, ppos, capacity, tier, dev_status);
 }
 
 cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
                                           const unsigned long long* row_keys, int n_chunks, int R, int gamma, int V,
                                           int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
                                           int32_t* dev_status, cudaStream_t s) {
-    verify_greedy_finalize_kernel<<<blocks_for(static_cast<long long>(R) * 32, 128), 128, 0, s>>>(
-        mode, cu, draft, budget, row_keys, n_chunks, R, gamma, V,
-                                                                      accept, ceiling, out_tok, n_out, dev_status);
-    return cudaGetLastError();
+    return launch_pdl(verify_greedy_finalize_kernel, dim3(blocks_for(static_cast<long long>(R) * 32, 128)), dim3(128),
+                      0, s, mode, cu, draft, budget, row_keys, n_chunks, R, gamma, V, accept, ceiling, out_tok, n_out,
+                      dev_status);
 }
 
 cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t* anchor, const int32_t* draft,
@@ -784,7 +876,7 @@ cudaError_t launch_tree_merge(const float* tree_part, int gx, int R, int P, int 
                               int32_t* front_node, float* front_score, int32_t* n_front, int32_t* pool_tok,
                               int32_t* pool_parent, int32_t* pool_depth, float* pool_score, int32_t* pool_n,
                               cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(P) * 32 * k * 8 + static_cast<size_t>(P) * k * sizeof(Cand);
+    const size_t smem = 2 * static_cast<size_t>(P) * k * sizeof(Cand) + static_cast<size_t>(P) * 4;
     tree_merge_kernel<<<R, P * 32, smem, s>>>(tree_part, gx, R, P, k, B, d, front_tok, front_node, front_score,
                                               n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n);
     return cudaGetLastError();
@@ -795,7 +887,14 @@ cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool
                                  int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
                                  int32_t* n_nodes, cudaStream_t s) {
     const int pool_cap = 1 + P * B;
-    const size_t smem = static_cast<size_t>(pool_cap) * 4 + static_cast<size_t>(N + 1) * 4;
+    const size_t smem = static_cast<size_t>(pool_cap) * 16 + static_cast<size_t>(N + 1) * 4;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(tree_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
     tree_finalize_kernel<<<R, 128, smem, s>>>(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok,
                                               parent, depth, score, mask, n_nodes);
     return cudaGetLastError();
@@ -804,9 +903,16 @@ cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool
 cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, int n_chunks, const int32_t* tok, const int32_t* parent,
                                     const int32_t* n_nodes, int R, int N, int B, int V, int32_t* accept,
                                     int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s) {
-    tree_verify_walk_kernel<<<blocks_for(R, 64), 64, 0, s>>>(row_keys, n_chunks, tok, parent, n_nodes, R, N, B, V, accept,
-                                                             out_tok, n_out, dev_status);
-    return cudaGetLastError();
+    const size_t smem = static_cast<size_t>(N + 1) * 12;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(tree_verify_walk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             200 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    return launch_pdl(tree_verify_walk_kernel, dim3(R), dim3(32), smem, s, row_keys, n_chunks, tok, parent, n_nodes, R,
+                      N, B, V, accept, out_tok, n_out, dev_status);
 }
 
 int num_sms() {

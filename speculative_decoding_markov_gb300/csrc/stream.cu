@@ -50,6 +50,8 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
     constexpr int VEC = FP32 ? 4 : 8;
     __shared__ unsigned long long red_key[kThreads / 32];
     __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
+    pdl_wait();
+    pdl_trigger();
     const int n_items = p.count ? *p.count : p.n_items;
     const long long total = static_cast<long long>(n_items) * p.n_chunks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,8 +111,11 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
                         const U4 blk = philox_block(rk, 3u, static_cast<uint32_t>(item), race_row, (v0 >> 2) + b);
                         const uint32_t wd[4] = {blk.x, blk.y, blk.z, blk.w};
 #pragma unroll
-                        for (int q = 0; q < 4; ++q)
-                            am.add(val[b * 4 + q] * p.inv_t - race_log_exp(word_to_uniform(wd[q])), v0 + b * 4 + q);
+                        for (int q = 0; q < 4; ++q) {
+                            const float z = val[b * 4 + q] * p.inv_t;
+                            if (one_minus_uniform(wd[q]) < 2.0f * __expf(z - am.best))   // race filter
+                                am.add(z - race_log_exp(word_to_uniform(wd[q])), v0 + b * 4 + q);
+                        }
                     }
                 }
             }
@@ -151,11 +156,8 @@ cudaError_t launch_op(const StreamParams& p, int max_items, cudaStream_t s) {
     const long long work = static_cast<long long>(max_items) * p.n_chunks;
     if (work <= 0) return cudaSuccess;
     const int grid = static_cast<int>(work < 8LL * num_sms() ? work : 8LL * num_sms());
-    if (p.fp32)
-        row_stream_kernel<OP, 1><<<grid, kThreads, 0, s>>>(p);
-    else
-        row_stream_kernel<OP, 0><<<grid, kThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    return p.fp32 ? launch_pdl(row_stream_kernel<OP, 1>, dim3(grid), dim3(kThreads), 0, s, p)
+                  : launch_pdl(row_stream_kernel<OP, 0>, dim3(grid), dim3(kThreads), 0, s, p);
 }
 
 }  // namespace

@@ -98,6 +98,11 @@ def test_tree_and_verify_host_validation(lib):
     bad_n = list(args)
     bad_n[11] = 8 * 16 + 1                      # N > P * B
     assert f(*bad_n) == 2
+    big_pool = list(args)
+    big_pool[6], big_pool[10], big_pool[9] = 128, 64, 1   # P * B + 1 > 8192 (pool ranked in shared memory)
+    assert f(*big_pool) == 2
+    vt = lib.sdm_verify_tree
+    assert vt(FAKE, 0, FAKE, FAKE, FAKE, 4, 16384, 7, 1024, FAKE, FAKE, FAKE, FAKE, 1 << 30, None, None) == 2
     v = lib.sdm_verify
     vargs = [2, 0, 1.0, binding.SdmRng(0, 0), FAKE, 0, 64, FAKE, FAKE, FAKE, None, None, None, None, 0, None, None, 0,
              4, 7, 1024, FAKE, None, FAKE, FAKE, FAKE, 1 << 30, None, None]
