@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kListHead = 32;   // list entries the pick kernel loads with the list length
 
 template <int FP32>
 __device__ __forceinline__ void unpack(const uint4& x, float (&v)[FP32 ? 4 : 8]) {
@@ -110,7 +111,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
     constexpr int VPT = kChunkBytes / 16 / kThreads;        // vectors per thread
     constexpr int CHUNK_IDS = kChunkBytes / ESZ;
     __shared__ float s_wmax[kWarps];
-    __shared__ int s_cnt;
+    __shared__ int s_cnt[2];   // by item parity: a slot is reset two items after its last read
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
     int rs = it / nc, c = it - rs * nc;
     const int srs = gridDim.x / nc, sc = gridDim.x - srs * nc;
     const uint8_t* L = static_cast<const uint8_t*>(p.L);
-    while (it < items) {
+    for (int par = 0; it < items; par ^= 1) {
         int nrs = rs + srs, ncc = c + sc;
         if (ncc >= nc) {
             ncc -= nc;
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         if (lane == 0) s_wmax[warp] = m;
-        if (threadIdx.x == 0) s_cnt = 0;
+        if (threadIdx.x == 0) s_cnt[par] = 0;
         __syncthreads();
         float mc = s_wmax[0];
 #pragma unroll
@@ -172,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) {
                     if (v[q] >= T) {
-                        const int slot = atomicAdd(&s_cnt, 1);
+                        const int slot = atomicAdd(&s_cnt[par], 1);
                         if (slot < kSegCap)
                             out[slot] = make_uint2(static_cast<uint32_t>(v0 + i * VEC + q), __float_as_uint(v[q]));
                     }
@@ -180,10 +181,14 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
             }
         }
         __syncthreads();
+        const int cnt = s_cnt[par];
         if (threadIdx.x == 0) {
-            p.cand_n[seg] = s_cnt;        // the true count: above kSegCap the list is incomplete
+            p.cand_n[seg] = cnt;          // the true count: above kSegCap the list is incomplete
             p.cmax[seg] = mc;
         }
+        // the head of the list (kListHead entries) is always written, so that
+        // the pick kernel's speculative head loads hit L2
+        if (threadIdx.x >= cnt && threadIdx.x < kListHead) out[threadIdx.x] = make_uint2(0xffffffffu, 0u);
         it += gridDim.x;
         rs = nrs;
         c = ncc;
@@ -195,31 +200,38 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
 // ---------------------------------------------------------------------------
 constexpr int kGroup = 8;              // candidates a warp scores per round (global path)
 constexpr int kPickCap = 1024;         // ids per scoring batch of the global path
-constexpr int kRowCapMax = 256;        // staged candidates (W^T row + U row each)
+constexpr int kRowCapMax = 160;        // staged candidates (W^T row + U row each)
 constexpr int kPickSmem = 200 * 1024;  // dynamic shared memory of the pick kernel
+constexpr uint32_t kZBytes = 48 * 1024;   // pair scores
 
 struct PickLayout {
-    uint32_t st_key, st_c, st_w, st_u, total;
-    int cap;
+    uint32_t st_key, st_c, st_w, st_u, z, total;
+    int cap, rs, zcap;   // staged candidates, row stride (elements), pair scores
 };
 
 __host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
 
-// Dynamic shared memory: list prefix sums [B][nc + 1], then a pool of cap
-// staged candidates shared by the steps: (id, L) keys, bounds c(id), W^T rows
-// and U rows.
+// Dynamic shared memory: list prefix sums [B][nc + 1]; a pool of cap staged
+// candidates shared by the steps: (id, L) keys, bounds c(id), W^T rows and U
+// rows (plus U[anchor] as row cap), rows padded by 16 bytes so that the
+// tensor-core fragment loads of eight rows fall in distinct banks; then the
+// pair scores z[d][prev][cand].
 __host__ __device__ inline PickLayout pick_layout(int B, int nc, int r) {
     PickLayout l;
+    l.rs = r + 8;
     const uint32_t fixed = al16(static_cast<uint32_t>(B) * static_cast<uint32_t>(nc + 1) * 4u);
-    const uint32_t per = 8u + 4u + 4u * static_cast<uint32_t>(r);
-    int cap = static_cast<int>((kPickSmem - fixed - 64u) / per);
+    const uint32_t row = 2u * static_cast<uint32_t>(l.rs);
+    const uint32_t per = 8u + 4u + 2u * row;
+    int cap = static_cast<int>((kPickSmem - fixed - kZBytes - row - 64u) / per);
     cap = cap < kRowCapMax ? cap : kRowCapMax;
     l.cap = cap;
     l.st_key = fixed;
-    l.st_c = al16(l.st_key + static_cast<uint32_t>(l.cap) * 8u);
-    l.st_w = al16(l.st_c + static_cast<uint32_t>(l.cap) * 4u);
-    l.st_u = l.st_w + static_cast<uint32_t>(l.cap) * 2u * r;
-    l.total = l.st_u + static_cast<uint32_t>(l.cap) * 2u * r;
+    l.st_c = al16(l.st_key + static_cast<uint32_t>(cap) * 8u);
+    l.st_w = al16(l.st_c + static_cast<uint32_t>(cap) * 4u);
+    l.st_u = l.st_w + static_cast<uint32_t>(cap) * row;
+    l.z = l.st_u + static_cast<uint32_t>(cap + 1) * row;
+    l.zcap = static_cast<int>(kZBytes / 4u);
+    l.total = l.z + kZBytes;
     return l;
 }
 
@@ -281,30 +293,50 @@ __device__ __forceinline__ int segment_of(const int* pref, int nc, int t) {
     return lo;
 }
 
+__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// D += A B for one m16n8k16 tile: bf16 inputs, fp32 accumulation (the
+// register layouts of A, B and D are those the PTX ISA gives for this shape).
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 template <int FP32>
 __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedParams p) {
     constexpr int VEC = FP32 ? 4 : 8;
     constexpr int kBatch = 4;   // list entries a lane loads at once (second round)
-    constexpr int kHead = 32;   // entries of each list loaded with its length
+    constexpr int kHead = kListHead;
     pdl_wait();
     pdl_trigger();
     const int row = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nc = p.n_chunks, B = p.B, r = p.r;
     const PickLayout lay = pick_layout(B, nc, r);
+    const int RS = lay.rs;
     extern __shared__ __align__(16) uint8_t s_dyn[];
     int* s_pref = reinterpret_cast<int*>(s_dyn);                   // [B][nc + 1] list prefix sums
     uint2* st_key = reinterpret_cast<uint2*>(s_dyn + lay.st_key);  // [cap] staged (id, L bits)
     float* st_c = reinterpret_cast<float*>(s_dyn + lay.st_c);      // c(id)
-    uint16_t* st_w = reinterpret_cast<uint16_t*>(s_dyn + lay.st_w);   // W^T rows
-    uint16_t* st_u = reinterpret_cast<uint16_t*>(s_dyn + lay.st_u);   // U rows
-    __shared__ __align__(16) uint16_t s_u0[256];                   // U[anchor]
+    uint16_t* st_w = reinterpret_cast<uint16_t*>(s_dyn + lay.st_w);   // [cap][RS] W^T rows
+    uint16_t* st_u = reinterpret_cast<uint16_t*>(s_dyn + lay.st_u);   // [cap + 1][RS] U rows, U[anchor] last
+    float* s_z = reinterpret_cast<float*>(s_dyn + lay.z);             // pair scores
+    uint16_t* u_anchor = st_u + static_cast<size_t>(lay.cap) * RS;
     __shared__ float s_lmax[kMaxPickSteps];
     __shared__ int s_scnt[kMaxPickSteps];                          // staged ids of each step
     __shared__ int s_sbeg[kMaxPickSteps];                          // their first pool slot
-    __shared__ int s_alloc;                                        // pool slots handed out
-    __shared__ int s_staged[kMaxPickSteps];                        // the step scores from shared memory
+    __shared__ int s_staged[kMaxPickSteps];                        // the step's ids sit in the pool
     __shared__ int s_over[kMaxPickSteps];                          // a list of the step overflowed
+    __shared__ int s_zoff[kMaxPickSteps + 1];                      // pair-score offset (-1: no pair scores)
+    __shared__ int s_toff[kMaxPickSteps + 1];                      // first tensor tile of each step
+    __shared__ int s_aoff[kMaxPickSteps + 1];                      // first winner-table row of each step
+    __shared__ int s_arg[kRowCapMax + 1];                          // winner slot of every pair-score row
+    __shared__ int s_alloc;                                        // pool slots handed out
+    __shared__ float s_cprev0;
     __shared__ const uint16_t* s_urow;
     __shared__ float s_cprev;
     __shared__ uint2 s_ids[kPickCap];
@@ -312,14 +344,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     __shared__ unsigned long long s_best[2];
     const float cmax = *p.c_max;
     const int seg0 = row * B * nc;
-
-    int prev = p.anchor[row];
-    if (prev < 0 || prev >= p.V) {
-        if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
-        prev = 0;
-    }
-    if (threadIdx.x * 8 < r) cp_async_16(s_u0 + threadIdx.x * 8, p.U + static_cast<size_t>(prev) * r + threadIdx.x * 8, 16u);
-    float cprev = p.c_bound[prev];
     if (threadIdx.x == 0) s_alloc = 0;
     __syncthreads();
 
@@ -422,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
                 const uint32_t v = st_key[off + j].x;
                 const int slot = off + j;
                 if (lane * 8 < r) {
-                    cp_async_16(st_w + static_cast<size_t>(slot) * r + lane * 8, p.Wt + static_cast<size_t>(v) * r + lane * 8, 16u);
-                    cp_async_16(st_u + static_cast<size_t>(slot) * r + lane * 8, p.U + static_cast<size_t>(v) * r + lane * 8, 16u);
+                    cp_async_16(st_w + static_cast<size_t>(slot) * RS + lane * 8, p.Wt + static_cast<size_t>(v) * r + lane * 8, 16u);
+                    cp_async_16(st_u + static_cast<size_t>(slot) * RS + lane * 8, p.U + static_cast<size_t>(v) * r + lane * 8, 16u);
                 }
             }
             for (int j = lane; j < kept; j += 32) st_c[off + j] = p.c_bound[st_key[off + j].x];
@@ -436,69 +460,204 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
             s_staged[d] = fits;
         }
     }
+    // the anchor: U[anchor] as the pool's last U row, and its bound
+    if (warp == kWarps - 1) {
+        int a = p.anchor[row];
+        if (a < 0 || a >= p.V) {
+            if (lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+            a = 0;
+        }
+        if (lane * 8 < r) cp_async_16(u_anchor + lane * 8, p.U + static_cast<size_t>(a) * r + lane * 8, 16u);
+        if (lane == 0) s_cprev0 = p.c_bound[a];
+    }
     cp_async_wait_all();
     __syncthreads();
 
-    // The steps.  A staged step is warp 0's alone (its ids, rows and bounds
-    // are in shared memory; no block barrier); the other warps join only for
-    // a step on the global path, where warp 0 hands over its state.
-    const uint16_t* urow = s_u0;   // U[y_{d-1}]: shared (staged) or global
+    // Pair scores: for every step d whose ids are staged and whose possible
+    // previous tokens are too (the anchor for d = 1, the staged ids of d - 1
+    // otherwise), z[d][p][j] = L_j + U[p] . W^T[j] for all pairs, as 16 x 8
+    // tensor-core tiles (mma.sync, bf16 in, fp32 accumulate) spread over the
+    // warps.  The chain below then only looks scores up.
+    if (threadIdx.x == 0) {
+        int zo = 0, to = 0, ao = 0;
+        for (int d = 0; d < B; ++d) {
+            const bool prev_ok = d == 0 || s_staged[d - 1];
+            const int np = d == 0 ? 1 : s_scnt[d - 1];
+            const int nq = s_scnt[d];
+            const int need = np * nq;
+            s_toff[d] = to;
+            s_aoff[d] = ao;
+            if (s_staged[d] && prev_ok && nq > 0 && np > 0 && zo + need <= lay.zcap && ao + np <= kRowCapMax + 1) {
+                s_zoff[d] = zo;
+                zo += need;
+                to += ((np + 15) >> 4) * ((nq + 7) >> 3);
+                ao += np;
+            } else {
+                s_zoff[d] = -1;
+            }
+        }
+        s_toff[B] = to;
+        s_aoff[B] = ao;
+    }
+    __syncthreads();
+    {
+        const int gid = lane >> 2, tig = lane & 3;
+        const int n_tiles = s_toff[B];
+        for (int t = warp; t < n_tiles; t += kWarps) {
+            int d = 0;
+            while (s_toff[d + 1] <= t) ++d;
+            const int np = d == 0 ? 1 : s_scnt[d - 1];
+            const int nq = s_scnt[d];
+            const int tq = (nq + 7) >> 3;
+            const int lt = t - s_toff[d];
+            const int p0 = (lt / tq) * 16, j0 = (lt % tq) * 8;
+            const uint16_t* ubase = d == 0 ? u_anchor : st_u + static_cast<size_t>(s_sbeg[d - 1]) * RS;
+            const uint16_t* ua = ubase + static_cast<size_t>(min(p0 + gid, np - 1)) * RS + tig * 2;
+            const uint16_t* ub = ubase + static_cast<size_t>(min(p0 + gid + 8, np - 1)) * RS + tig * 2;
+            const uint16_t* wb = st_w + static_cast<size_t>(s_sbeg[d] + min(j0 + gid, nq - 1)) * RS + tig * 2;
+            // two independent accumulator chains (even and odd k-steps), r % 64 == 0
+            float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k0 = 0; k0 < r; k0 += 32) {
+                mma_16816(acc, lds32(ua + k0), lds32(ub + k0), lds32(ua + k0 + 8), lds32(ub + k0 + 8), lds32(wb + k0),
+                          lds32(wb + k0 + 8));
+                mma_16816(acc2, lds32(ua + k0 + 16), lds32(ub + k0 + 16), lds32(ua + k0 + 24), lds32(ub + k0 + 24),
+                          lds32(wb + k0 + 16), lds32(wb + k0 + 24));
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
+            float* z = s_z + s_zoff[d];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int pp = p0 + gid + (e >> 1) * 8;
+                const int jj = j0 + tig * 2 + (e & 1);
+                if (pp < np && jj < nq)   // fp32(L) + Markov, one rounding
+                    z[pp * nq + jj] = __uint_as_float(st_key[s_sbeg[d] + jj].y) + acc[e];
+            }
+        }
+    }
+    __syncthreads();
+    // every pair-score row reduced to its (z desc, id asc) winner, in parallel
+    for (int t = threadIdx.x; t < s_aoff[B]; t += kThreads) {
+        int d = 0;
+        while (s_aoff[d + 1] <= t) ++d;
+        const int nq = s_scnt[d];
+        const int sb = s_sbeg[d];
+        const float* zr = s_z + s_zoff[d] + (t - s_aoff[d]) * nq;
+        unsigned long long best = 0ull;
+        int bj = 0;
+        for (int j = 0; j < nq; ++j) {
+            const unsigned long long k = argmax_key(zr[j], st_key[sb + j].x);
+            if (k > best) {
+                best = k;
+                bj = j;
+            }
+        }
+        s_arg[t] = sb + bj;
+    }
+    __syncthreads();
+
+    // The chain.  A step with pair scores is a table lookup (the winner for
+    // the previous token's row).  A staged step without them scores from
+    // shared memory; either is warp 0's alone.  A step on the global path
+    // uses every warp, warp 0 handing over its state first.
+    if (s_aoff[B] > 0 && s_zoff[B - 1] >= 0) {
+        // fast path: every step has pair scores (then every step is staged) -
+        // one thread walks the winner table, the warp writes the tokens
+        bool all = true;
+        for (int d = 0; d < B; ++d) all = all && s_zoff[d] >= 0;
+        if (all) {
+            if (warp == 0) {
+                int tokv = 0;
+                if (lane == 0) {
+                    int pidx = 0;
+                    for (int d = 0; d < B; ++d) {
+                        const int bslot = s_arg[s_aoff[d] + pidx];
+                        pidx = bslot - s_sbeg[d];
+                        s_ids[d].x = st_key[bslot].x;
+                    }
+                }
+                __syncwarp();
+                for (int d = lane; d < B; d += 32) {
+                    tokv = static_cast<int>(s_ids[d].x);
+                    if (tokv < 0 || tokv >= p.V) {
+                        set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+                        tokv = 0;
+                    }
+                    p.tokens[static_cast<size_t>(row) * B + d] = tokv;
+                }
+            }
+            return;
+        }
+    }
+    const uint16_t* urow = u_anchor;   // U[y_{d-1}]: shared (staged) or global
+    float cprev = s_cprev0;
+    int pidx = 0;                      // index of y_{d-1} among the previous step's staged ids (-1: none)
     for (int d = 1; d <= B; ++d) {
         const float lmax = s_lmax[d - 1];
         if (s_staged[d - 1]) {
             if (warp != 0) continue;
-            const float tall = threshold(lmax, cprev);   // every id that can win has L >= tall
-            float ub[8];
-            load_ub(urow, lane, r, ub);
             const int sb = s_sbeg[d - 1];
             const int n = s_scnt[d - 1];
-            unsigned long long best = 0ull;
+            uint32_t bid = 0xffffffffu;
             int bslot = -1;
-            for (int j0 = 0; j0 < n; j0 += kGroup) {
-                uint2 en[kGroup];
-                float acc[kGroup];
+            if (s_zoff[d - 1] >= 0 && pidx >= 0) {
+                bslot = s_arg[s_aoff[d - 1] + pidx];
+                bid = st_key[bslot].x;
+            } else {
+                // staged, no pair scores: score the staged ids against U[y_{d-1}]
+                const float tall = threshold(lmax, cprev);   // every id that can win has L >= tall
+                float ubv[8];
+                load_ub(urow, lane, r, ubv);
+                unsigned long long best = 0ull;
+                for (int j0 = 0; j0 < n; j0 += kGroup) {
+                    uint2 en[kGroup];
+                    float acc[kGroup];
 #pragma unroll
-                for (int jj = 0; jj < kGroup; ++jj) {   // all row loads first, then the sums
-                    const int j = j0 + jj;
-                    en[jj] = j < n ? st_key[sb + j] : make_uint2(0xffffffffu, 0u);
-                    const bool ok = j < n && __uint_as_float(en[jj].y) >= tall && lane * 8 < r;
-                    const uint4 w = ok ? *reinterpret_cast<const uint4*>(st_w + static_cast<size_t>(sb + j) * r + lane * 8)
-                                       : make_uint4(0, 0, 0, 0);
-                    float a[8];
-                    unpack<0>(w, a);
-                    acc[jj] = 0.f;
+                    for (int jj = 0; jj < kGroup; ++jj) {   // all row loads first, then the sums
+                        const int j = j0 + jj;
+                        en[jj] = j < n ? st_key[sb + j] : make_uint2(0xffffffffu, 0u);
+                        const bool ok = j < n && __uint_as_float(en[jj].y) >= tall && lane * 8 < r;
+                        const uint4 wv = ok ? *reinterpret_cast<const uint4*>(st_w + static_cast<size_t>(sb + j) * RS + lane * 8)
+                                            : make_uint4(0, 0, 0, 0);
+                        float a[8];
+                        unpack<0>(wv, a);
+                        acc[jj] = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) acc[jj] = fmaf(a[q], ub[q], acc[jj]);
-                }
+                        for (int q = 0; q < 8; ++q) acc[jj] = fmaf(a[q], ubv[q], acc[jj]);
+                    }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
+                    for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-                    for (int jj = 0; jj < kGroup; ++jj) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], o);
+                        for (int jj = 0; jj < kGroup; ++jj) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], o);
 #pragma unroll
-                for (int jj = 0; jj < kGroup; ++jj) {
-                    const float lv = __uint_as_float(en[jj].y);
-                    if (j0 + jj < n && lv >= tall) {
-                        const unsigned long long k = argmax_key(lv + acc[jj], en[jj].x);   // fp32(L) + Markov
-                        if (k > best) {
-                            best = k;
-                            bslot = sb + j0 + jj;
+                    for (int jj = 0; jj < kGroup; ++jj) {
+                        const float lv = __uint_as_float(en[jj].y);
+                        if (j0 + jj < n && lv >= tall) {
+                            const unsigned long long k = argmax_key(lv + acc[jj], en[jj].x);   // fp32(L) + Markov
+                            if (k > best) {
+                                best = k;
+                                bslot = sb + j0 + jj;
+                            }
                         }
                     }
                 }
+                bid = key_token(best);
             }
-            int y = static_cast<int>(key_token(best));
-            if (best == 0ull || y < 0 || y >= p.V) {
+            int y = static_cast<int>(bid);
+            if (bslot < 0 || y < 0 || y >= p.V) {
                 if (lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
                 y = 0;
                 bslot = -1;
             }
             if (lane == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
             if (bslot >= 0) {   // the winner's U row and bound were staged with it
-                urow = st_u + static_cast<size_t>(bslot) * r;
+                urow = st_u + static_cast<size_t>(bslot) * RS;
                 cprev = st_c[bslot];
+                pidx = bslot - sb;
             } else {
                 urow = p.U + static_cast<size_t>(y) * r;
                 cprev = p.c_bound[y];
+                pidx = -1;
             }
             continue;
         }
@@ -514,8 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
         cprev = s_cprev;
         const int ds = (d - 1) * nc;
         const float tall = threshold(lmax, cprev);
-        float ub[8];
-        load_ub(urow, lane, r, ub);
+        float ubv[8];
+        load_ub(urow, lane, r, ubv);
         if (!s_over[d - 1]) {
             // the step's list entries in windows of kPickCap; ids with L >= tall scored
             const int* pref = s_pref + (d - 1) * (nc + 1);
@@ -530,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
                         s_ids[atomicAdd(&s_m, 1)] = en;
                 }
                 __syncthreads();
-                const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
+                const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ubv, warp, lane));
                 if (lane == 0 && b) atomicMax(&s_best[par], b);
                 __syncthreads();
             }
@@ -550,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
                             s_ids[atomicAdd(&s_m, 1)] = make_uint2(static_cast<uint32_t>(i * VEC + q), __float_as_uint(v[q]));
                 }
                 __syncthreads();
-                const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ub, warp, lane));
+                const unsigned long long b = warp_max_u64(score_global(p, s_ids, s_m, ubv, warp, lane));
                 if (lane == 0 && b) atomicMax(&s_best[par], b);
                 __syncthreads();
             }
@@ -565,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
         if (threadIdx.x == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
         urow = p.U + static_cast<size_t>(y) * r;
         cprev = p.c_bound[y];
+        pidx = -1;
     }
 }
 

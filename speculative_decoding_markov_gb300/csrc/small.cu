@@ -27,32 +27,39 @@ __global__ void chain_finalize_kernel(const unsigned long long* keys, const floa
                                       int V, int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
                                       const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
                                       float* lse, int32_t* dev_status) {
-    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+    // one warp per (request, step): lanes share the partials and the dot product
+    const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     if (idx >= R * B) return;
     const int i = idx / B, d = idx % B + 1;
     const size_t o = static_cast<size_t>(d - 1) * R + i;
     int y = static_cast<int>(key_token(keys[o]));
     if (y < 0 || y >= V) {
-        set_status(dev_status, SDM_DEV_BAD_TOKEN);
+        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_TOKEN);
         y = 0;
     }
-    tokens[static_cast<size_t>(i) * B + d - 1] = y;
+    if (lane == 0) tokens[static_cast<size_t>(i) * B + d - 1] = y;
     if (!sample) return;
     Lse acc{-INFINITY, 0.f};
-    for (int c = 0; c < gx; ++c) {
+    for (int c = lane; c < gx; c += 32) {
         const float2 pc = lse_part[o * gx + c];
         acc = lse_merge(acc, Lse{pc.x, pc.y});
     }
+    acc = warp_lse(acc);
     const float l = acc.m + logf(acc.s);
     int prev = (d == 1) ? anchor[i] : static_cast<int>(key_token(keys[o - R]));
     if (prev < 0 || prev >= V) prev = 0;
     // z_d[y] = L + U[prev] . W[:, y]; exact in fp32 on the 2^-8 grid tables
     float m = 0.f;
-    for (int j = 0; j < r; ++j)
+    for (int j = lane; j < r; j += 32)
         m += bf16_bits_to_float(U[static_cast<size_t>(prev) * r + j]) * bf16_bits_to_float(W[static_cast<size_t>(j) * V + y]);
-    const float z = load_elem(L, l_fp32, (static_cast<size_t>(i) * B + (d - 1)) * V + y) + m;
-    if (lse) lse[static_cast<size_t>(i) * B + d - 1] = l;
-    if (logq) logq[static_cast<size_t>(i) * B + d - 1] = z * inv_t - l;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) m += __shfl_xor_sync(0xffffffffu, m, s);
+    if (lane == 0) {
+        const float z = load_elem(L, l_fp32, (static_cast<size_t>(i) * B + (d - 1)) * V + y) + m;
+        if (lse) lse[static_cast<size_t>(i) * B + d - 1] = l;
+        if (logq) logq[static_cast<size_t>(i) * B + d - 1] = z * inv_t - l;
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -426,20 +433,23 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
                                           int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
                                           float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
                                           unsigned long long* res_keys, int32_t* dev_status) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    // one warp per request; lane p runs the accept test of window row p (all
+    // rows at once, each from its own partials), the first failure wins
+    const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
     if (i >= R) return;
     const RngKey rk{k0, k1, cycle};
     const int row0 = cu[i];
     int w = cu[i + 1] - row0 - 1;
     if (w < 0 || w > gamma) {
-        set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
         w = w < 0 ? 0 : gamma;
     }
     int cap = w;
     if (mode == SDM_CAP_ACCEPT) {
         cap = budget[i];
         if (cap < 0 || cap > w) {
-            set_status(dev_status, SDM_DEV_BAD_WINDOW);
+            if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
             cap = cap < 0 ? 0 : w;
         }
     }
@@ -451,20 +461,24 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
         return acc.m + logf(acc.s);
     };
     int A = w;
-    for (int p = 0; p < w; ++p) {
-        int yp = y[p];
-        if (yp < 0 || yp >= V) {
-            set_status(dev_status, SDM_DEV_BAD_TOKEN);
-            yp = 0;
+    for (int p0 = 0; p0 < w && A == w; p0 += 32) {
+        const int p = p0 + lane;
+        bool reject = false;
+        if (p < w) {
+            int yp = y[p];
+            if (yp < 0 || yp >= V) {
+                set_status(dev_status, SDM_DEV_BAD_TOKEN);
+                yp = 0;
+            }
+            const float lp = load_elem(target, t_fp32, static_cast<size_t>(row0 + p) * V + yp) * inv_t - row_lse(p);
+            const float lq = logq[static_cast<size_t>(i) * gamma + p];
+            const float u = uniform_at(rk, 1u, static_cast<uint32_t>(i), static_cast<uint32_t>(p), 0u);
+            reject = !(logf(u) < lp - lq);   // accept iff u < p(y) / q(y)
         }
-        const float lp = load_elem(target, t_fp32, static_cast<size_t>(row0 + p) * V + yp) * inv_t - row_lse(p);
-        const float lq = logq[static_cast<size_t>(i) * gamma + p];
-        const float u = uniform_at(rk, 1u, static_cast<uint32_t>(i), static_cast<uint32_t>(p), 0u);
-        if (!(logf(u) < lp - lq)) {   // accept iff u < p(y) / q(y)
-            A = p;
-            break;
-        }
+        const unsigned bal = __ballot_sync(0xffffffffu, reject);
+        if (bal) A = p0 + __ffs(bal) - 1;
     }
+    if (lane != 0) return;
     const int a = A < cap ? A : cap;
     accept[i] = a;
     if (ceiling) ceiling[i] = A;
@@ -801,7 +815,7 @@ cudaError_t launch_chain_finalize(const unsigned long long* keys, const float2* 
                                   int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
                                   const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
                                   float* lse, int32_t* dev_status, cudaStream_t s) {
-    chain_finalize_kernel<<<blocks_for(static_cast<long long>(R) * B, 128), 128, 0, s>>>(
+    chain_finalize_kernel<<<blocks_for(static_cast<long long>(R) * B * 32, 128), 128, 0, s>>>(
         keys, lse_part, gx, R, B, V, r, L, l_fp32, U, W, anchor, inv_t, sample, tokens, logq, lse, dev_status);
     return cudaGetLastError();
 }
@@ -848,7 +862,7 @@ cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t
                                       int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
                                       float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
                                       unsigned long long* res_keys, int32_t* dev_status, cudaStream_t s) {
-    verify_sample_scan_kernel<<<blocks_for(R, 64), 64, 0, s>>>(
+    verify_sample_scan_kernel<<<blocks_for(static_cast<long long>(R) * 32, 128), 128, 0, s>>>(
         mode, cu, anchor, draft, budget, logq, target, t_fp32, V, lse_part, n_chunks, inv_t, k0, k1, cycle, R, gamma,
         accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, res_keys, dev_status);
     return cudaGetLastError();
