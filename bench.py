@@ -381,8 +381,24 @@ def run_ours(args, w, world, rank, local):
     t_front = sum(e[0].elapsed_time(e[1]) for e in events) / 1e3       # draft + schedule + pack
     t_verify = sum(e[2].elapsed_time(e[3]) for e in events) / 1e3
     t_total = t_front + t_verify
-    # the draft's share of the front segment, from the eager split cycle
-    t_draft = t_front * split_draft / max(split_draft + split_sched, 1e-9)
+    # the draft alone (for the roofline of its kernels): its own graph, the
+    # same L2 flush before every launch, CUDA events on the stream
+    n_draft = max(20, min(200, args.steps))
+    g_only = None
+    if graphs:
+        g_only = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_only):
+            cyc.draft()
+    ev_d = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_draft)]
+    for k in range(n_draft + 3):
+        flush.fill_(1)
+        if k >= 3:
+            ev_d[k - 3][0].record(stream)
+        g_only.replay() if g_only is not None else cyc.draft()
+        if k >= 3:
+            ev_d[k - 3][1].record(stream)
+    torch.cuda.synchronize()
+    t_draft = sum(e[0].elapsed_time(e[1]) for e in ev_d) / 1e3 / n_draft * args.steps   # seconds per args.steps
     t_max, units = merge_ranks(t_total, [committed * args.steps, windows * args.steps], world)
     status = int(cyc.status.item())
 
@@ -444,6 +460,7 @@ def run_ours(args, w, world, rank, local):
                    "timed": "draft+schedule+pack+verify (CUDA events); target stand-in row gather excluded"},
         "breakdown_ms_per_step": {"draft+schedule+pack": t_front / args.steps * 1e3,
                                   "verify": t_verify / args.steps * 1e3,
+                                  "draft_alone": t_draft / args.steps * 1e3,
                                   "eager_split_ms": {"draft": split_draft, "schedule+pack": split_sched}},
         "graphs": graphs,
         "tokens_per_step": {"committed": committed, "accepted_drafts": accepted, "verified_rows": windows},

@@ -101,9 +101,11 @@ __device__ __forceinline__ float threshold(float m, float c) {
 // ---------------------------------------------------------------------------
 // Work item = kChunkBytes of one row L_d; row-major items, a persistent grid
 // strides over them.  Each thread holds 8 16-byte vectors of the chunk in
-// registers, the chunk maximum m_c is reduced over the CTA, and every id with
-// L >= m_c - 2 c_max is listed.  m_c <= max_v L_d[v] and c(y) <= c_max, so
-// the list holds every id an exact step can need.
+// registers (all eight loads in flight at once; an explicit L2 prefetch of the
+// next item measured slower on this part), the chunk maximum m_c is reduced
+// over the CTA, and every id with L >= m_c - 2 c_max is listed.
+// m_c <= max_v L_d[v] and c(y) <= c_max, so the list holds every id an exact
+// step can need.
 template <int FP32>
 __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedParams p) {
     constexpr int VEC = FP32 ? 4 : 8;
@@ -133,13 +135,6 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
         const int v0 = c * CHUNK_IDS;
         const int n_vec = (min(p.V, v0 + CHUNK_IDS) - v0) / VEC;
         const uint4* src = reinterpret_cast<const uint4*>(L + (static_cast<size_t>(rs) * p.V + v0) * ESZ);
-        if (it + static_cast<int>(gridDim.x) < items) {   // this CTA's next item starts moving into L2 now
-            const int nv0 = ncc * CHUNK_IDS;
-            const int nbytes = (min(p.V, nv0 + CHUNK_IDS) - nv0) * ESZ;
-            const char* nsrc = reinterpret_cast<const char*>(L + (static_cast<size_t>(nrs) * p.V + nv0) * ESZ);
-            for (int off = threadIdx.x * 128; off < nbytes; off += kThreads * 128)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(nsrc + off));
-        }
         uint4 x[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -200,13 +195,12 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
 // ---------------------------------------------------------------------------
 constexpr int kGroup = 8;              // candidates a warp scores per round (global path)
 constexpr int kPickCap = 1024;         // ids per scoring batch of the global path
-constexpr int kRowCapMax = 160;        // staged candidates (W^T row + U row each)
+constexpr int kRowCapMax = 192;        // staged candidates (W^T row + U row each); < 256
 constexpr int kPickSmem = 200 * 1024;  // dynamic shared memory of the pick kernel
-constexpr uint32_t kZBytes = 48 * 1024;   // pair scores
 
 struct PickLayout {
-    uint32_t st_key, st_c, st_w, st_u, z, total;
-    int cap, rs, zcap;   // staged candidates, row stride (elements), pair scores
+    uint32_t st_key, st_c, st_w, st_u, total;
+    int cap, rs;   // staged candidates, row stride (elements)
 };
 
 __host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; }
@@ -214,24 +208,21 @@ __host__ __device__ inline uint32_t al16(uint32_t x) { return (x + 15u) & ~15u; 
 // Dynamic shared memory: list prefix sums [B][nc + 1]; a pool of cap staged
 // candidates shared by the steps: (id, L) keys, bounds c(id), W^T rows and U
 // rows (plus U[anchor] as row cap), rows padded by 16 bytes so that the
-// tensor-core fragment loads of eight rows fall in distinct banks; then the
-// pair scores z[d][prev][cand].
+// tensor-core fragment loads of eight rows fall in distinct banks.
 __host__ __device__ inline PickLayout pick_layout(int B, int nc, int r) {
     PickLayout l;
     l.rs = r + 8;
     const uint32_t fixed = al16(static_cast<uint32_t>(B) * static_cast<uint32_t>(nc + 1) * 4u);
     const uint32_t row = 2u * static_cast<uint32_t>(l.rs);
     const uint32_t per = 8u + 4u + 2u * row;
-    int cap = static_cast<int>((kPickSmem - fixed - kZBytes - row - 64u) / per);
+    int cap = static_cast<int>((kPickSmem - fixed - row - 64u) / per);
     cap = cap < kRowCapMax ? cap : kRowCapMax;
     l.cap = cap;
     l.st_key = fixed;
     l.st_c = al16(l.st_key + static_cast<uint32_t>(cap) * 8u);
     l.st_w = al16(l.st_c + static_cast<uint32_t>(cap) * 4u);
     l.st_u = l.st_w + static_cast<uint32_t>(cap) * row;
-    l.z = l.st_u + static_cast<uint32_t>(cap + 1) * row;
-    l.zcap = static_cast<int>(kZBytes / 4u);
-    l.total = l.z + kZBytes;
+    l.total = l.st_u + static_cast<uint32_t>(cap + 1) * row;
     return l;
 }
 
@@ -293,7 +284,17 @@ __device__ __forceinline__ int segment_of(const int* pref, int nc, int t) {
     return lo;
 }
 
-__device__ __forceinline__ uint32_t lds32(const uint16_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+// Four (x4) or two (x2) 8 x 8 bf16 matrices from shared memory, one 16-byte
+// row address per lane (lanes 8m..8m+7 address matrix m); thread t receives
+// row t / 4, elements 2 (t % 4) and 2 (t % 4) + 1 of each matrix.
+__device__ __forceinline__ void ldmatrix_x4(const uint16_t* p, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldmatrix_x2(const uint16_t* p, uint32_t& r0, uint32_t& r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(smem_u32(p)));
+}
 
 // D += A B for one m16n8k16 tile: bf16 inputs, fp32 accumulation (the
 // register layouts of A, B and D are those the PTX ISA gives for this shape).
@@ -324,17 +325,16 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     float* st_c = reinterpret_cast<float*>(s_dyn + lay.st_c);      // c(id)
     uint16_t* st_w = reinterpret_cast<uint16_t*>(s_dyn + lay.st_w);   // [cap][RS] W^T rows
     uint16_t* st_u = reinterpret_cast<uint16_t*>(s_dyn + lay.st_u);   // [cap + 1][RS] U rows, U[anchor] last
-    float* s_z = reinterpret_cast<float*>(s_dyn + lay.z);             // pair scores
     uint16_t* u_anchor = st_u + static_cast<size_t>(lay.cap) * RS;
     __shared__ float s_lmax[kMaxPickSteps];
     __shared__ int s_scnt[kMaxPickSteps];                          // staged ids of each step
     __shared__ int s_sbeg[kMaxPickSteps];                          // their first pool slot
     __shared__ int s_staged[kMaxPickSteps];                        // the step's ids sit in the pool
     __shared__ int s_over[kMaxPickSteps];                          // a list of the step overflowed
-    __shared__ int s_zoff[kMaxPickSteps + 1];                      // pair-score offset (-1: no pair scores)
+    __shared__ int s_paired[kMaxPickSteps];                        // the step has pair scores
     __shared__ int s_toff[kMaxPickSteps + 1];                      // first tensor tile of each step
     __shared__ int s_aoff[kMaxPickSteps + 1];                      // first winner-table row of each step
-    __shared__ int s_arg[kRowCapMax + 1];                          // winner slot of every pair-score row
+    __shared__ unsigned long long s_rowkey[kRowCapMax + 1];        // winner key of every pair-score row
     __shared__ int s_alloc;                                        // pool slots handed out
     __shared__ float s_cprev0;
     __shared__ const uint16_t* s_urow;
@@ -345,6 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     const float cmax = *p.c_max;
     const int seg0 = row * B * nc;
     if (threadIdx.x == 0) s_alloc = 0;
+    for (int t = threadIdx.x; t <= kRowCapMax; t += kThreads) s_rowkey[t] = 0ull;
     __syncthreads();
 
     // One warp per step (lane = chunk): the chunk maxima, the list lengths
@@ -395,23 +396,42 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
         __syncwarp();
         if (lane == 0) pref[nc] = run;
         const float t_all = threshold(m, cmax);
-        // two passes over the same ids: count, take a range of the pool,
-        // then write (a step whose ids do not fit scores from global memory)
+        // count, take a range of the pool, then write (a step whose ids do not
+        // fit scores from global memory)
         int kept = 0, off = 0;
         bool fits = !over;
-        for (int pass = 0; pass < 2 && fits; ++pass) {
-            int pos0 = 0;
-            if (!spill) {
-                // every list fits in its head: compact from registers
+        if (fits && !spill) {
+            // every list fits in its head: a keep mask per lane, a warp prefix
+            // sum of the counts, then each lane writes its own entries
+            uint32_t mask = 0u;
 #pragma unroll
-                for (int e = 0; e < kHead; ++e) {
-                    const bool keep = lane < nc && e < cn0 && head[e].x < static_cast<uint32_t>(p.V) &&
-                                      __uint_as_float(head[e].y) >= t_all;
-                    const unsigned bal = __ballot_sync(0xffffffffu, keep);
-                    if (pass == 1 && keep) st_key[off + pos0 + __popc(bal & ((1u << lane) - 1u))] = head[e];
-                    pos0 += __popc(bal);
-                }
-            } else {
+            for (int e = 0; e < kHead; ++e) {
+                const bool keep = lane < nc && e < cn0 && head[e].x < static_cast<uint32_t>(p.V) &&
+                                  __uint_as_float(head[e].y) >= t_all;
+                mask |= keep ? (1u << e) : 0u;
+            }
+            const int cnt = __popc(mask);
+            int x = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            kept = __shfl_sync(0xffffffffu, x, 31);
+            int o0 = 0;
+            if (lane == 0) o0 = atomicAdd(&s_alloc, kept);
+            off = __shfl_sync(0xffffffffu, o0, 0);
+            fits = off + kept <= lay.cap;
+            if (fits) {
+                int pos = off + x - cnt;
+#pragma unroll
+                for (int e = 0; e < kHead; ++e)
+                    if (mask & (1u << e)) st_key[pos++] = head[e];
+            }
+        }
+        for (int pass = 0; pass < 2 && fits && spill; ++pass) {
+            int pos0 = 0;
+            {
                 for (int t0 = 0; t0 < run; t0 += 32 * kBatch) {
                     uint2 en[kBatch];
 #pragma unroll
@@ -478,26 +498,47 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     // otherwise), z[d][p][j] = L_j + U[p] . W^T[j] for all pairs, as 16 x 8
     // tensor-core tiles (mma.sync, bf16 in, fp32 accumulate) spread over the
     // warps.  The chain below then only looks scores up.
-    if (threadIdx.x == 0) {
-        int zo = 0, to = 0, ao = 0;
-        for (int d = 0; d < B; ++d) {
-            const bool prev_ok = d == 0 || s_staged[d - 1];
-            const int np = d == 0 ? 1 : s_scnt[d - 1];
-            const int nq = s_scnt[d];
-            const int need = np * nq;
-            s_toff[d] = to;
-            s_aoff[d] = ao;
-            if (s_staged[d] && prev_ok && nq > 0 && np > 0 && zo + need <= lay.zcap && ao + np <= kRowCapMax + 1) {
-                s_zoff[d] = zo;
-                zo += need;
-                to += ((np + 15) >> 4) * ((nq + 7) >> 3);
-                ao += np;
-            } else {
-                s_zoff[d] = -1;
+    if (warp == 0) {
+        // per step (lane = step): whether it gets pair scores, its tiles and
+        // winner rows as exclusive prefix sums.  The winner rows always fit:
+        // they number 1 + (staged ids) <= cap + 1.
+        int trun = 0, arun = 0;
+        for (int d0 = 0; d0 < B; d0 += 32) {
+            const int d = d0 + lane;
+            int tiles = 0, rows = 0;
+            bool ok = false;
+            if (d < B) {
+                const bool prev_ok = d == 0 || s_staged[d - 1];
+                const int np = d == 0 ? 1 : s_scnt[d - 1];
+                const int nq = s_scnt[d];
+                ok = s_staged[d] && prev_ok && nq > 0 && np > 0;
+                if (ok) {
+                    tiles = ((np + 15) >> 4) * ((nq + 7) >> 3);
+                    rows = np;
+                }
             }
+            int xt = tiles, xa = rows;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int yt = __shfl_up_sync(0xffffffffu, xt, o);
+                const int ya = __shfl_up_sync(0xffffffffu, xa, o);
+                if (lane >= o) {
+                    xt += yt;
+                    xa += ya;
+                }
+            }
+            if (d < B) {
+                s_paired[d] = ok;
+                s_toff[d] = trun + xt - tiles;
+                s_aoff[d] = arun + xa - rows;
+            }
+            trun += __shfl_sync(0xffffffffu, xt, 31);
+            arun += __shfl_sync(0xffffffffu, xa, 31);
         }
-        s_toff[B] = to;
-        s_aoff[B] = ao;
+        if (lane == 0) {
+            s_toff[B] = trun;
+            s_aoff[B] = arun;
+        }
     }
     __syncthreads();
     {
@@ -512,73 +553,72 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
             const int lt = t - s_toff[d];
             const int p0 = (lt / tq) * 16, j0 = (lt % tq) * 8;
             const uint16_t* ubase = d == 0 ? u_anchor : st_u + static_cast<size_t>(s_sbeg[d - 1]) * RS;
-            const uint16_t* ua = ubase + static_cast<size_t>(min(p0 + gid, np - 1)) * RS + tig * 2;
-            const uint16_t* ub = ubase + static_cast<size_t>(min(p0 + gid + 8, np - 1)) * RS + tig * 2;
-            const uint16_t* wb = st_w + static_cast<size_t>(s_sbeg[d] + min(j0 + gid, nq - 1)) * RS + tig * 2;
+            // ldmatrix addresses: A (16 x 16) as matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15),
+            // B (16 x 8, the W^T rows of 8 candidates) as (k 0-7 | 8-15); rows past the set repeat its last row
+            const int arow = min(p0 + (lane & 7) + ((lane >> 3) & 1) * 8, np - 1);
+            const uint16_t* ua = ubase + static_cast<size_t>(arow) * RS + (lane >> 4) * 8;
+            const int brow = min(j0 + (lane & 7), nq - 1);
+            const uint16_t* wb = st_w + static_cast<size_t>(s_sbeg[d] + brow) * RS + ((lane >> 3) & 1) * 8;
             // two independent accumulator chains (even and odd k-steps), r % 64 == 0
             float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
             for (int k0 = 0; k0 < r; k0 += 32) {
-                mma_16816(acc, lds32(ua + k0), lds32(ub + k0), lds32(ua + k0 + 8), lds32(ub + k0 + 8), lds32(wb + k0),
-                          lds32(wb + k0 + 8));
-                mma_16816(acc2, lds32(ua + k0 + 16), lds32(ub + k0 + 16), lds32(ua + k0 + 24), lds32(ub + k0 + 24),
-                          lds32(wb + k0 + 16), lds32(wb + k0 + 24));
+                uint32_t a0, a1, a2, a3, b0, b1, c0, c1, c2, c3, e0, e1;
+                ldmatrix_x4(ua + k0, a0, a1, a2, a3);
+                ldmatrix_x2(wb + k0, b0, b1);
+                ldmatrix_x4(ua + k0 + 16, c0, c1, c2, c3);
+                ldmatrix_x2(wb + k0 + 16, e0, e1);
+                mma_16816(acc, a0, a1, a2, a3, b0, b1);
+                mma_16816(acc2, c0, c1, c2, c3, e0, e1);
             }
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[e] += acc2[e];
-            float* z = s_z + s_zoff[d];
+            // z = fp32(L) + Markov (one rounding); the winner of each row is
+            // kept as a key ordered by (z desc, id asc) whose low byte is the
+            // candidate's index in the step: ids < 2^24, at most 256 per step
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int pp = p0 + gid + (e >> 1) * 8;
-                const int jj = j0 + tig * 2 + (e & 1);
-                if (pp < np && jj < nq)   // fp32(L) + Markov, one rounding
-                    z[pp * nq + jj] = __uint_as_float(st_key[s_sbeg[d] + jj].y) + acc[e];
+            for (int h = 0; h < 2; ++h) {
+                const int pp = p0 + gid + h * 8;
+                unsigned long long best = 0ull;
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int jj = j0 + tig * 2 + e;
+                    if (jj < nq) {
+                        const uint2 en = st_key[s_sbeg[d] + jj];
+                        const float z = __uint_as_float(en.y) + acc[h * 2 + e];
+                        const unsigned long long k = (static_cast<unsigned long long>(ordered_bits(z)) << 32) |
+                                                     ((0xffffffu - en.x) << 8) | static_cast<uint32_t>(jj);
+                        best = umax64(best, k);
+                    }
+                }
+                best = umax64(best, __shfl_xor_sync(0xffffffffu, best, 1));
+                best = umax64(best, __shfl_xor_sync(0xffffffffu, best, 2));
+                if (tig == 0 && pp < np && best) atomicMax(&s_rowkey[s_aoff[d] + pp], best);
             }
         }
     }
     __syncthreads();
-    // every pair-score row reduced to its (z desc, id asc) winner, in parallel
-    for (int t = threadIdx.x; t < s_aoff[B]; t += kThreads) {
-        int d = 0;
-        while (s_aoff[d + 1] <= t) ++d;
-        const int nq = s_scnt[d];
-        const int sb = s_sbeg[d];
-        const float* zr = s_z + s_zoff[d] + (t - s_aoff[d]) * nq;
-        unsigned long long best = 0ull;
-        int bj = 0;
-        for (int j = 0; j < nq; ++j) {
-            const unsigned long long k = argmax_key(zr[j], st_key[sb + j].x);
-            if (k > best) {
-                best = k;
-                bj = j;
-            }
-        }
-        s_arg[t] = sb + bj;
-    }
-    __syncthreads();
-
     // The chain.  A step with pair scores is a table lookup (the winner for
     // the previous token's row).  A staged step without them scores from
     // shared memory; either is warp 0's alone.  A step on the global path
     // uses every warp, warp 0 handing over its state first.
-    if (s_aoff[B] > 0 && s_zoff[B - 1] >= 0) {
+    if (s_aoff[B] > 0 && s_paired[B - 1]) {
         // fast path: every step has pair scores (then every step is staged) -
         // one thread walks the winner table, the warp writes the tokens
         bool all = true;
-        for (int d = 0; d < B; ++d) all = all && s_zoff[d] >= 0;
+        for (int d = 0; d < B; ++d) all = all && s_paired[d];
         if (all) {
             if (warp == 0) {
                 int tokv = 0;
                 if (lane == 0) {
                     int pidx = 0;
                     for (int d = 0; d < B; ++d) {
-                        const int bslot = s_arg[s_aoff[d] + pidx];
-                        pidx = bslot - s_sbeg[d];
-                        s_ids[d].x = st_key[bslot].x;
+                        pidx = static_cast<int>(s_rowkey[s_aoff[d] + pidx] & 0xffu);
+                        s_ids[d].x = static_cast<uint32_t>(s_sbeg[d] + pidx);
                     }
                 }
                 __syncwarp();
                 for (int d = lane; d < B; d += 32) {
-                    tokv = static_cast<int>(s_ids[d].x);
+                    tokv = static_cast<int>(st_key[s_ids[d].x].x);
                     if (tokv < 0 || tokv >= p.V) {
                         set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
                         tokv = 0;
@@ -600,8 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
             const int n = s_scnt[d - 1];
             uint32_t bid = 0xffffffffu;
             int bslot = -1;
-            if (s_zoff[d - 1] >= 0 && pidx >= 0) {
-                bslot = s_arg[s_aoff[d - 1] + pidx];
+            if (s_paired[d - 1] && pidx >= 0) {
+                bslot = sb + static_cast<int>(s_rowkey[s_aoff[d - 1] + pidx] & 0xffu);
                 bid = st_key[bslot].x;
             } else {
                 // staged, no pair scores: score the staged ids against U[y_{d-1}]
