@@ -76,17 +76,18 @@ def kernel_source_hash():
 
 
 def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from the committed ncu summary profiles/traffic.txt (one line per kernel:
+    name, source hash, bytes), if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        d = json.load(f)
-    e = d.get(kernel)
-    if not e or e.get("source_hash") != kernel_source_hash():
-        return None
-    return e.get("bytes_per_launch")
+        for line in f:
+            parts = line.split()
+            if len(parts) == 3 and not line.startswith("#") and parts[0] == kernel:
+                return int(parts[2]) if parts[1] == kernel_source_hash() else None
+    return None
 
 
 class ClockSampler:

@@ -290,7 +290,7 @@ struct Epi<MODE_TREE> {
     bool valid;
     int group;
     float m, s;
-    float thresh;                 // current 8th best z (entry to the top-8)
+    float thresh;                 // current k-th best z (entry to the top-k)
     float tv[kMaxTopK];
     uint32_t ti[kMaxTopK];
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
@@ -321,17 +321,25 @@ struct Epi<MODE_TREE> {
 #pragma unroll
         for (int j = 0; j < C; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
         s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        // The kernel keeps a sorted top-8 (value desc, lower id first); its first
-        // k entries are the top-k for any k <= 8.
-        if (mx > thresh) {   // some entry enters the top-8 (rare once it has filled)
+        // A sorted top-k (value desc, lower id first; k <= 8 slots in use).
+        // Only the columns above the current k-th best are inserted, one set
+        // bit at a time (rare once the list has filled).
+        if (mx > thresh) {
+            uint32_t cm = 0u;
 #pragma unroll
-            for (int j = 0; j < C; ++j) {   // ascending ids: earlier ties stay ahead
-                float cz = z[j];
+            for (int j = 0; j < C; ++j) cm |= (z[j] > thresh ? 1u : 0u) << j;
+            while (cm) {
+                const int j = __ffs(cm) - 1;   // ascending ids: earlier ties stay ahead
+                cm &= cm - 1u;
+                float cz = z[0];
+#pragma unroll
+                for (int jj = 1; jj < C; ++jj)
+                    if (jj == j) cz = z[jj];
                 if (!(cz > thresh)) continue;
                 uint32_t cv = static_cast<uint32_t>(vbase + j);
 #pragma unroll
                 for (int q = 0; q < kMaxTopK; ++q) {
-                    if (cz > tv[q]) {   // strict: earlier (lower id) ties stay ahead
+                    if (q < p.k && cz > tv[q]) {   // strict: earlier (lower id) ties stay ahead
                         const float tz = tv[q];
                         const uint32_t tiv = ti[q];
                         tv[q] = cz;
@@ -340,7 +348,9 @@ struct Epi<MODE_TREE> {
                         cv = tiv;
                     }
                 }
-                thresh = tv[kMaxTopK - 1];
+#pragma unroll
+                for (int q = 0; q < kMaxTopK; ++q)
+                    if (q == p.k - 1) thresh = tv[q];
             }
         }
     }

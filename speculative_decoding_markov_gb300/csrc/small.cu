@@ -547,8 +547,12 @@ struct Cand {
     int slot, rank, tok;
 };
 
+// (s desc, slot asc, rank asc), with s compared through its order-preserving
+// bits: a strict total order even when a score is NaN, so that parallel ranks
+// form a permutation.
 __device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
-    if (a.s != b.s) return a.s > b.s;
+    const uint32_t oa = ordered_bits(a.s), ob = ordered_bits(b.s);
+    if (oa != ob) return oa > ob;
     if (a.slot != b.slot) return a.slot < b.slot;
     return a.rank < b.rank;
 }
@@ -694,12 +698,14 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
         }
     }
     __syncthreads();
+    // ranks by (score desc, depth asc, creation asc); scores compared through
+    // their order-preserving bits, a strict total order even for NaN
     for (int j = 1 + threadIdx.x; j < np; j += blockDim.x) {
-        const float sj = s_sc[j];
+        const uint32_t sj = ordered_bits(s_sc[j]);
         const int dj = s_dep[j];
         int rank = 0;
         for (int q = 1; q < np; ++q) {
-            const float sq = s_sc[q];
+            const uint32_t sq = ordered_bits(s_sc[q]);
             const int dq = s_dep[q];
             rank += (q != j && (sq > sj || (sq == sj && (dq < dj || (dq == dj && q < j))))) ? 1 : 0;
         }
