@@ -65,13 +65,20 @@ def measured_peaks():
     return 6800.0, 1700.0, "fallback"
 
 
-def kernel_source_hash():
+KERNEL_SOURCES = {   # the files whose text fixes each reported kernel's code
+    "chain_scan_kernel+chain_pick_kernel": ("chain_pruned.cu", "device.cuh", "internal.h"),
+    "markov_gemm_kernel<chain>": ("markov_gemm.cu", "device.cuh", "internal.h"),
+    "markov_gemm_kernel<tree>": ("markov_gemm.cu", "device.cuh", "internal.h"),
+    "row_stream_kernel<argmax>": ("stream.cu", "device.cuh", "internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str = "chain_scan_kernel+chain_pick_kernel"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_markov_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in KERNEL_SOURCES.get(kernel, ()):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
@@ -86,7 +93,7 @@ def recorded_traffic(kernel: str):
         for line in f:
             parts = line.split()
             if len(parts) == 3 and not line.startswith("#") and parts[0] == kernel:
-                return int(parts[2]) if parts[1] == kernel_source_hash() else None
+                return int(parts[2]) if parts[1] == kernel_source_hash(kernel) else None
     return None
 
 
