@@ -19,8 +19,10 @@
 //   * warp 0 streams W tiles [r x 64] (MN-major, TMA 2-D, 128-byte swizzle,
 //     L2 evict_last: W is re-read by every draft step) and the matching L tile
 //     [rows x 64] (TMA 3-D, evict_first) through an S-stage mbarrier ring;
-//   * warp 1 issues r/16 tcgen05.mma (M=128, N=64, K=16, bf16 -> fp32) per
-//     tile into one of two 64-column TMEM accumulators;
+//   * warp 1 first copies A into tensor memory (tcgen05.cp, r/16 blocks of
+//     128 rows x 16 bf16), then issues r/16 tcgen05.mma (M=128, N=64, K=16,
+//     bf16 -> fp32, A from tensor memory, B from shared memory) per tile into
+//     one of two 64-column TMEM accumulators, with precomputed descriptors;
 //   * warps 2-17 drain the accumulator with tcgen05.ld (thread = GEMM row of
 //     its TMEM sub-partition; four warps per sub-partition, one per 16-column
 //     group of every tile), add L and run the mode's reduction in registers;
@@ -34,6 +36,10 @@ namespace sdm {
 namespace {
 
 constexpr int kSmemLimit = 232448;   // 227 KB opt-in per block
+// Tensor memory: two 64-column fp32 accumulators, then A (128 rows x r bf16,
+// two per 32-bit column: r / 2 <= 128 columns).
+constexpr int kTmemA = 2 * kTileN;
+constexpr int kTmemCols = 256;
 
 struct SmemLayout {
     uint32_t a_bytes, w_bytes, l_box_bytes, l_bytes, stage_bytes, bar_off, total;
@@ -506,7 +512,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (mode_reads_l(MODE)) tma_prefetch_desc(&tmL);
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 2 * kTileN);
+        tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     cp_async_wait_all();
@@ -546,8 +552,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // 3. MMA issuer: D[128 x 64] = A[128 x r] * W_tile[r x 64]
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
-            const uint32_t a_addr = smem_u32(sA);
+            // Descriptors are formed once and advanced by adding the k-step's
+            // offset to their 14-bit start-address field (address >> 4; every
+            // shared address here is below 256 KB, so the field cannot carry):
+            // A steps 32 bytes within a 128-byte swizzle row and 128 x 128
+            // bytes per K block of 64; B steps 16 rows of 128 bytes.
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const int ksteps = p.r >> 4;
+            // A into tensor memory once: every MMA then reads only its B tile
+            // from shared memory
+            const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA);
+            for (int ks = 0; ks < ksteps; ++ks)
+                tmem_cp_128x256b(a_tmem + static_cast<uint32_t>(ks * 8),
+                                 a_desc0 + static_cast<uint64_t>((ks >> 2) * ((kTileM * 128) >> 4) + (ks & 3) * 2));
             for (int i = 0; i < nt; ++i) {
                 const int s = i % p.stages;
                 const int b = i & 1;
@@ -560,15 +577,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t w_addr = smem_u32(smem + lay.a_bytes + s * lay.stage_bytes);
+                // N = 64 is one swizzle span, so the MN-atom offset is never
+                // applied; it is set equal to the K-group stride (1024 B).
+                const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + lay.a_bytes + s * lay.stage_bytes), 1024, 1024);
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
+#pragma unroll 4
                 for (int ks = 0; ks < ksteps; ++ks) {
-                    const uint64_t ad =
-                        smem_desc_sw128(a_addr + (ks >> 2) * (kTileM * 128) + (ks & 3) * 32, 16, 1024);
-                    // N = 64 is one swizzle span, so the MN-atom offset is never
-                    // applied; it is set equal to the K-group stride (1024 B).
-                    const uint64_t bd = smem_desc_sw128(w_addr + ks * 2048, 1024, 1024);
-                    mma_bf16(d_tmem, ad, bd, idesc, ks > 0 ? 1u : 0u);
+                    const uint64_t bd = b_desc0 + static_cast<uint64_t>(ks * (2048 >> 4));
+                    mma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>(ks * 8), bd, idesc, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&empty[s]);
                 mma_commit(&tfull[b]);
@@ -618,7 +634,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, 2 * kTileN);
+        tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 
