@@ -74,8 +74,31 @@ double orc_uniform(uint64_t seed, uint64_t cycle, int stream, uint32_t req, uint
     return (double)(2u * (word >> 9) + 1u) / 16777216.0;
 }
 
-/* Exponential variate E = -ln u of the exponential race. */
-static double race_exponential(double u) { return -log(u); }
+/* Categorical draw by the inverse CDF in index order (the pages leave the
+ * sampler open; this is the plain textbook one): the smallest v with
+ * w[0] + ... + w[v] > u S, S = sum of the nonnegative weights w, one uniform
+ * u per draw.  *margin = the distance from u S to the nearer cumulative bound
+ * around v, relative to S (how far u is from changing the draw). */
+static int icdf_draw(const double* w, int V, double u, double* margin) {
+    double S = 0.0;
+    for (int v = 0; v < V; ++v) S += w[v];
+    const double t = u * S;
+    double c = 0.0;
+    int last = -1;
+    for (int v = 0; v < V; ++v) {
+        if (!(w[v] > 0.0)) continue;
+        last = v;
+        const double c1 = c + w[v];
+        if (c1 > t) {
+            const double a = t - c, b = c1 - t;
+            if (margin) *margin = (a < b ? a : b) / S;
+            return v;
+        }
+        c = c1;
+    }
+    if (margin) *margin = 0.0;   /* u S at or above the rounded total: the last positive weight */
+    return last < 0 ? 0 : last;
+}
 
 /* ------------------------------------------------------------------ */
 /* Markov head: Markov(y) = U[y] . W, rank r  ([DSpark notes] sec. 4,    */
@@ -139,6 +162,7 @@ int orc_draft_chain(const void* L, int dtL, const uint16_t* U, const uint16_t* W
                     int32_t* tokens, double* logq, double* lse, double* margin) {
     int flags = 0;
     double* M = (double*)malloc(sizeof(double) * (size_t)V);
+    double* wts = (double*)malloc(sizeof(double) * (size_t)V);
     float* z = (float*)malloc(sizeof(float) * (size_t)V);
     double inv_t = 1.0 / temperature;
     for (int i = 0; i < R; ++i) {
@@ -157,22 +181,14 @@ int orc_draft_chain(const void* L, int dtL, const uint16_t* U, const uint16_t* W
                 if (logq) logq[o] = 0.0;
                 if (lse) lse[o] = 0.0;
             } else {
-                /* y_d ~ softmax(z_d / T) by the exponential race:
-                 * y = argmax_v z_v/T - ln E_v with E_v ~ Exp(1) i.i.d. */
-                double best = -INFINITY, second = -INFINITY;
-                y = 0;
-                for (int v = 0; v < V; ++v) {
-                    double u = orc_uniform(seed, cycle, ORC_STREAM_DRAFT, gid, (uint32_t)d, (uint32_t)v);
-                    double key = (double)z[v] * inv_t - log(race_exponential(u));
-                    if (key > best) {
-                        second = best;
-                        best = key;
-                        y = v;
-                    } else if (key > second) {
-                        second = key;
-                    }
-                }
-                gap = best - second;
+                /* y_d ~ softmax(z_d / T): inverse CDF in vocabulary order,
+                 * one uniform (stream 0, row d) */
+                double zmax = -INFINITY;
+                for (int v = 0; v < V; ++v)
+                    if ((double)z[v] * inv_t > zmax) zmax = (double)z[v] * inv_t;
+                for (int v = 0; v < V; ++v) wts[v] = exp((double)z[v] * inv_t - zmax);
+                double u = orc_uniform(seed, cycle, ORC_STREAM_DRAFT, gid, (uint32_t)d, 0u);
+                y = icdf_draw(wts, V, u, &gap);
                 double l = logsumexp_scaled(z, V, inv_t);
                 if (lse) lse[o] = l;
                 if (logq) logq[o] = (double)z[y] * inv_t - l;     /* log q_d(y_d) */
@@ -183,6 +199,7 @@ int orc_draft_chain(const void* L, int dtL, const uint16_t* U, const uint16_t* W
         }
     }
     free(M);
+    free(wts);
     free(z);
     return flags;
 }
@@ -483,6 +500,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
     int flags = 0;
     double inv_t = 1.0 / temperature;
     double* M = (double*)malloc(sizeof(double) * (size_t)V);
+    double* wts = (double*)malloc(sizeof(double) * (size_t)V);
     float* z = (float*)malloc(sizeof(float) * (size_t)V);
     for (int i = 0; i < R; ++i) {
         uint32_t gid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
@@ -525,11 +543,11 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
             a = A < cap ? A : cap;
             int row = a;
             double lse_p = row_lse(target, dtT, row0 + (size_t)row, V, inv_t);
-            double best = -INFINITY, second = -INFINITY;
-            last = -1;
+            double gap = INFINITY;
             if (A < cap) {
                 /* rejected at row a = A: resample from max(0, p - q), with q
-                 * recomputed from the Markov head at that position */
+                 * recomputed from the Markov head at that position (inverse
+                 * CDF, one uniform: stream 2, row a) */
                 int prev = row == 0 ? anchor[i] : y[row - 1];
                 if (markov_row(U, W, prev, r, V, M)) flags |= ORC_FLAG_INEXACT_MARKOV;
                 combine_logits(L, dtL, ((size_t)i * gamma + (size_t)row) * V, M, V, z);
@@ -538,33 +556,17 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
                     double pv = exp((double)load_elem(target, dtT, (row0 + (size_t)row) * (size_t)V + (size_t)v) * inv_t - lse_p);
                     double qv = exp((double)z[v] * inv_t - lq_row);
                     double wv = pv - qv;
-                    if (!(wv > 0.0)) continue;
-                    double u = orc_uniform(seed, cycle, ORC_STREAM_RESID, gid, (uint32_t)row, (uint32_t)v);
-                    double key = log(wv) - log(race_exponential(u));
-                    if (key > best) {
-                        second = best;
-                        best = key;
-                        last = v;
-                    } else if (key > second) {
-                        second = key;
-                    }
+                    wts[v] = wv > 0.0 ? wv : 0.0;
                 }
+                last = icdf_draw(wts, V, orc_uniform(seed, cycle, ORC_STREAM_RESID, gid, (uint32_t)row, 0u), &gap);
             } else {
-                /* every committed draft accepted: bonus token ~ p at row a */
-                for (int v = 0; v < V; ++v) {
-                    double u = orc_uniform(seed, cycle, ORC_STREAM_BONUS, gid, (uint32_t)row, (uint32_t)v);
-                    double key = (double)load_elem(target, dtT, (row0 + (size_t)row) * (size_t)V + (size_t)v) * inv_t
-                                 - log(race_exponential(u));
-                    if (key > best) {
-                        second = best;
-                        best = key;
-                        last = v;
-                    } else if (key > second) {
-                        second = key;
-                    }
-                }
+                /* every committed draft accepted: bonus token ~ p at row a
+                 * (inverse CDF, stream 3, row a) */
+                for (int v = 0; v < V; ++v)
+                    wts[v] = exp((double)load_elem(target, dtT, (row0 + (size_t)row) * (size_t)V + (size_t)v) * inv_t - lse_p);
+                last = icdf_draw(wts, V, orc_uniform(seed, cycle, ORC_STREAM_BONUS, gid, (uint32_t)row, 0u), &gap);
             }
-            if (best - second < min_gap) min_gap = best - second;
+            if (gap < min_gap) min_gap = gap;
         }
         size_t ob = (size_t)i * (size_t)(gamma + 1);
         for (int p = 0; p < a; ++p) out_tok[ob + (size_t)p] = y[p];
@@ -576,6 +578,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
         if (margin) margin[i] = min_gap;
     }
     free(M);
+    free(wts);
     free(z);
     return flags;
 }

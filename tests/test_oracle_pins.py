@@ -148,8 +148,31 @@ def test_chain_lse_and_logq_match_library_logsumexp():
         np.testing.assert_allclose(res["logq"], ly - ref, rtol=1e-12, atol=1e-13)
 
 
-def test_race_sampler_follows_softmax():
-    """The exponential race draws y ~ softmax(z/T): chi-square over many
+def test_sampler_is_inverse_cdf_of_its_uniform():
+    """Each sampled draft token is the inverse CDF of softmax(z/T) in
+    vocabulary order at the one uniform of (stream 0, request, row d):
+    numpy's searchsorted over the cumulative probabilities gives the same id,
+    and the reported margin is the distance of u to the nearer bound."""
+    V, R, B, T = 50, 40, 3, 0.7
+    rng = np.random.default_rng(11)
+    L = rng.normal(0, 1.5, (R, B, V)).astype(np.float32)
+    U = np.zeros((V, 4), np.uint16)
+    W = np.zeros((4, V), np.uint16)
+    anchor = np.zeros(R, np.int32)
+    res = oracle.draft_chain(L, U, W, anchor, decode=oracle.SAMPLE, temperature=T, seed=5, cycle=3)
+    for i in range(R):
+        for d in range(B):
+            p = special.softmax(L[i, d].astype(np.float64) / T)
+            c = np.cumsum(p)
+            u = oracle.uniform(5, 3, oracle.STREAM_DRAFT, i, d + 1, 0)   # rows count drafts from 1
+            y = int(np.searchsorted(c, u, side="right"))
+            assert res["tokens"][i, d] == y
+            lo = c[y - 1] if y else 0.0
+            np.testing.assert_allclose(res["margin"][i, d], min(u - lo, c[y] - u), rtol=1e-9, atol=1e-14)
+
+
+def test_sampler_follows_softmax():
+    """The inverse-CDF sampler draws y ~ softmax(z/T): chi-square over many
     independent requests (distinct counters) that share one logit row."""
     V, n, T = 8, 1 << 15, 0.8
     rng = np.random.default_rng(0)
@@ -418,8 +441,45 @@ def test_rejection_sampling_pairs_follow_target():
 def test_rejection_sampling_equal_distributions_accept_everything():
     w = small(R=40, B=5, V=64, r=16, sigma=(0.0,), l_std=1.5)
     inp = _inputs(w, seed=8)
-    _, _, vr = _sample_cycle(w, inp, np_of(inp["anchor"]), seed=1, cycle=0)
+    _, tgt, vr = _sample_cycle(w, inp, np_of(inp["anchor"]), seed=1, cycle=0)
     np.testing.assert_array_equal(vr["accept"], np.full(w.R, w.B))
+    # the bonus token is the inverse CDF of p at row B, one uniform of stream 3
+    for i in range(w.R):
+        c = np.cumsum(special.softmax(tgt[i, w.B].double().numpy() / w.temperature))
+        u = oracle.uniform(1, 0, oracle.STREAM_BONUS, i, w.B, 0)
+        assert vr["out_tok"][i, w.B] == int(np.searchsorted(c, u, side="right"))
+
+
+def test_residual_and_bonus_are_inverse_cdf_draws():
+    """With the Markov term zero, q_d = softmax(L_d/T).  Where request i stops
+    at row a < B the committed token is the inverse CDF of max(0, p_a - q_a)
+    (normalised) at the uniform of (stream 2, i, a); where every draft is
+    accepted it is the inverse CDF of p_B at (stream 3, i, B)."""
+    R, B, V, T = 300, 3, 12, 0.9
+    rng = np.random.default_rng(21)
+    L = rng.normal(0, 1.0, (R, B, V)).astype(np.float32)
+    U = np.zeros((V, 4), np.uint16)
+    W = np.zeros((4, V), np.uint16)
+    anchor = rng.integers(0, V, R).astype(np.int32)
+    dr = oracle.draft_chain(L, U, W, anchor, decode=oracle.SAMPLE, temperature=T, seed=6, cycle=1)
+    tgt = (L[:, np.r_[0:B, B - 1]] + rng.normal(0, 0.7, (R, B + 1, V))).astype(np.float32)
+    cu = np.arange(R + 1, dtype=np.int32) * (B + 1)
+    vr = oracle.verify(oracle.STATIC, oracle.SAMPLE, tgt.reshape(-1, V), cu, anchor, dr["tokens"],
+                       logq=dr["logq"], lse_q=dr["lse"], L=L, U=U, W=W, temperature=T, seed=6, cycle=1)
+    seen = set()
+    for i in range(R):
+        a = int(vr["accept"][i])
+        p = special.softmax(tgt[i, a].astype(np.float64) / T)
+        if a < B:
+            w_ = np.maximum(p - special.softmax(L[i, a].astype(np.float64) / T), 0.0)
+            u = oracle.uniform(6, 1, oracle.STREAM_RESID, i, a, 0)
+        else:
+            w_ = p
+            u = oracle.uniform(6, 1, oracle.STREAM_BONUS, i, a, 0)
+        c = np.cumsum(w_)
+        assert vr["out_tok"][i, a] == int(np.searchsorted(c, u * c[-1], side="right"))
+        seen.add(a)
+    assert seen == set(range(B + 1))
 
 
 def test_rejection_sampling_cap_accept_equals_compact():
