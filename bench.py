@@ -67,7 +67,7 @@ def measured_peaks():
 
 KERNEL_SOURCES = {   # the files whose text fixes each reported kernel's code
     "chain_scan_kernel+chain_pick_kernel": ("chain_pruned.cu", "device.cuh", "internal.h"),
-    "markov_gemm_kernel<chain>": ("markov_gemm.cu", "device.cuh", "internal.h"),
+    "markov_gemm_kernel<sample>+draft_select_kernel": ("markov_gemm.cu", "select.cu", "device.cuh", "internal.h"),
     "markov_gemm_kernel<tree>": ("markov_gemm.cu", "device.cuh", "internal.h"),
     "row_stream_kernel<argmax>": ("stream.cu", "device.cuh", "internal.h"),
 }
@@ -425,9 +425,10 @@ def run_ours(args, w, world, rank, local):
         draft_alg, draft_launches, bound = float(R * B * V * s_l), 1, "hbm"
         dname = "chain_scan_kernel+chain_pick_kernel"
     else:
-        # one launch per step: that step's rows of L and all of W
+        # one GEMM + one inverse-CDF select per step: that step's rows of L
+        # and all of W
         draft_alg, draft_launches, bound = float(R * V * s_l + w.r * V * 2), B, "hbm"
-        dname = "markov_gemm_kernel<chain>"
+        dname = "markov_gemm_kernel<sample>+draft_select_kernel"
     if t_draft >= t_verify:
         kname = dname
         per_launch_s = t_draft / args.steps / draft_launches

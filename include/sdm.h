@@ -36,9 +36,10 @@
  *   - Constraints: V % 8 == 0, r % 64 == 0 and r <= 256, L/U/W/target base
  *     addresses 16-byte aligned.  Anything else returns SDM_ERR_UNSUPPORTED.
  *   - Randomness (sampling only) is Philox4x32-10 with key (seed mod 2^32,
- *     seed >> 32) and counter (v >> 2, request, stream << 16 | row,
- *     cycle mod 2^32); word v & 3 gives u = (2 (w >> 9) + 1) 2^-24.  Streams:
- *     0 draft, 1 accept test, 2 residual, 3 bonus.
+ *     seed >> 32) and counter (0, request, stream << 16 | row,
+ *     cycle mod 2^32); its word 0, w, gives u = (2 (w >> 9) + 1) 2^-24, one
+ *     uniform per decision.  Streams: 0 draft, 1 accept test, 2 residual,
+ *     3 bonus.
  *   - Ties: argmax and top-k prefer the lowest token id; the scheduler ranks
  *     (survival desc, request asc, position asc); PCTree prunes by (score
  *     desc, parent slot asc, child rank asc) and selects by (score desc,
@@ -126,8 +127,9 @@ sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r
  * For d = 1..B, with y_0 = anchor:
  *     z_d = fp32(L[i, d-1, :]) + U[y_{d-1}] . W          (fp32)
  *     greedy:  y_d = argmax_v z_d[v]
- *     sample:  y_d ~ softmax(z_d / T) by the exponential race
- *              y_d = argmax_v (z_d[v]/T - ln(-ln u_v)), stream 0, row d;
+ *     sample:  y_d ~ softmax(z_d / T) by the inverse CDF in vocabulary
+ *              order: the smallest v with sum_{j<=v} exp(z_d[j]/T) > u S,
+ *              S the sum over all j, u = the uniform of (stream 0, row d);
  *              lse[i, d-1] = log sum_v exp(z_d[v]/T);
  *              logq[i, d-1] = z_d[y_d]/T - lse[i, d-1].
  * In:  L [R, B, V] (dtL), U [V, r] bf16, W [r, V] bf16, anchor [R] int32;
@@ -136,7 +138,10 @@ sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r
  *      when greedy).
  * Sampling (and greedy without prepared tables): the product U[y] . W runs on
  * the tcgen05 tensor cores (bf16 in, fp32 accumulate in TMEM) and the +L /
- * argmax / race is fused into its epilogue; z is never written to memory.
+ * argmax (greedy) or per-16-column (max, sum of exp) records (sampling) are
+ * fused into its epilogue; z is never written to memory.  A sampled step
+ * then walks the records of each request to the block holding u S and
+ * recomputes that block's 16 logits to find the id.
  * Greedy with prepared tables: since |U[y] . W[:, v]| <= c(y) for every v,
  * only ids with L[v] >= max L - 2 c(y) can win.  One HBM-bound pass over all
  * of L lists those ids for every (request, step) with the worst case c_max,
@@ -232,7 +237,10 @@ sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const in
  *           first rejection p = a, sample from max(0, p_a - q_a) where q_a is
  *           recomputed from L, U, W and lse_q (stream 2, row a); if all
  *           committed drafts pass, the bonus is drawn from p at row a
- *           (stream 3).  The exponential race is the sampler throughout.
+ *           (stream 3).  Every draw is the inverse CDF in vocabulary order
+ *           with one uniform (word 0 of the Philox block of its stream and
+ *           row; the row of a draft is d, of an accept test, residual or
+ *           bonus the window position).
  *   modes: STATIC (w_i = gamma, commit A), COMPACT (w_i = budget, commit A),
  *          CAP_ACCEPT (w_i = gamma verified, commit a = min(A, budget[i]):
  *          the same output as compact; ceiling = A).

@@ -89,8 +89,12 @@ inline int n_chunks_of(int V, int fp32) {
         if ((x) != cudaSuccess) return SDM_ERR_CUDA; \
     } while (0)
 
-size_t ws_chain_dense(int R, int B) {
-    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(B) * R * kMaxGx * kColGroups * 8);
+inline int n_blocks16(int V) { return (V + 15) / 16; }
+
+// greedy: argmax keys [B][R]; sampling: one (m, s) record per request and
+// 16-column block, reused by every step
+size_t ws_chain_dense(int R, int B, int V) {
+    return align256(static_cast<size_t>(B) * R * 8) + align256(static_cast<size_t>(R) * n_blocks16(V) * 8);
 }
 
 // candidate lists of the pruned greedy chain (sized for the larger fp32 split)
@@ -99,7 +103,7 @@ size_t ws_chain_pruned(int R, int B, int V) {
     return align256(segs * kSegCap * 8) + align256(segs * 4) + align256(segs * 4);
 }
 
-size_t ws_chain(int R, int B, int V) { return std::max(ws_chain_dense(R, B), ws_chain_pruned(R, B, V)); }
+size_t ws_chain(int R, int B, int V) { return std::max(ws_chain_dense(R, B, V), ws_chain_pruned(R, B, V)); }
 
 size_t ws_tree(int R, int B, int P) {
     const size_t rows = static_cast<size_t>(R) * P;
@@ -111,7 +115,7 @@ size_t ws_tree(int R, int B, int P) {
 size_t ws_verify(int R, int rows, int V) {
     const int nc = n_chunks_of(V, 0) > n_chunks_of(V, 1) ? n_chunks_of(V, 0) : n_chunks_of(V, 1);
     return align256(static_cast<size_t>(rows) * nc * 8) + align256(static_cast<size_t>(rows) * nc * 8) +
-           6 * align256(static_cast<size_t>(R) * 4) + align256(static_cast<size_t>(R) * 8);
+           6 * align256(static_cast<size_t>(R) * 4) + align256(static_cast<size_t>(R) * n_blocks16(V) * 8);
 }
 
 }  // namespace
@@ -241,7 +245,8 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
     }
     Carver c{static_cast<uint8_t*>(ws)};
     auto* keys = c.take<unsigned long long>(static_cast<size_t>(B) * R);
-    auto* lse_part = c.take<float2>(static_cast<size_t>(B) * R * kMaxGx * kColGroups);
+    const int nb = n_blocks16(V);
+    auto* blk = c.take<float2>(static_cast<size_t>(R) * nb);
 
     const int fp32 = dtL == SDM_FP32;
     const int l_rows = std::min(R, kTileM);
@@ -266,22 +271,52 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
     p.k = 1;
     p.stages = gemm_pick_stages(r, l_rows, fp32, mode);
     p.inv_t = decode == SDM_SAMPLE ? 1.0f / temperature : 1.0f;
-    p.rng_k0 = static_cast<uint32_t>(rng.seed);
-    p.rng_k1 = static_cast<uint32_t>(rng.seed >> 32);
-    p.rng_cycle = static_cast<uint32_t>(rng.cycle);
     p.U = U;
     p.anchor = anchor;
     p.keys = keys;
-    p.lse_part = lse_part;
+    p.tok_in = tokens;
+    p.blk = blk;
+    p.nb = nb;
     p.dev_status = dev_status;
 
-    SDM_CHECK_CUDA(launch_fill_u64(keys, static_cast<size_t>(B) * R, 0ull, s));
+    if (decode == SDM_GREEDY) {
+        SDM_CHECK_CUDA(launch_fill_u64(keys, static_cast<size_t>(B) * R, 0ull, s));
+        for (int d = 1; d <= B; ++d) {
+            p.d = d;
+            SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
+        }
+        SDM_CHECK_CUDA(launch_chain_finalize(keys, R, B, V, tokens, dev_status, s));
+        return SDM_OK;
+    }
+    // sampling: per step the GEMM writes the block records, then one CTA per
+    // request draws y_d by the inverse CDF (the next step's GEMM reads it)
+    DraftSelectParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.blk = blk;
+    sp.nb = nb;
+    sp.R = R;
+    sp.B = B;
+    sp.V = V;
+    sp.r = r;
+    sp.L = L;
+    sp.l_fp32 = fp32;
+    sp.U = U;
+    sp.W = W;
+    sp.anchor = anchor;
+    sp.inv_t = p.inv_t;
+    sp.k0 = static_cast<uint32_t>(rng.seed);
+    sp.k1 = static_cast<uint32_t>(rng.seed >> 32);
+    sp.cycle = static_cast<uint32_t>(rng.cycle);
+    sp.tokens = tokens;
+    sp.logq = logq;
+    sp.lse = lse;
+    sp.dev_status = dev_status;
     for (int d = 1; d <= B; ++d) {
         p.d = d;
+        sp.d = d;
         SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
+        SDM_CHECK_CUDA(launch_draft_select(sp, s));
     }
-    SDM_CHECK_CUDA(launch_chain_finalize(keys, lse_part, kColGroups * gx, R, B, V, r, L, fp32, U, W, anchor, p.inv_t,
-                                         decode == SDM_SAMPLE, tokens, logq, lse, dev_status, s));
     return SDM_OK;
 }
 
@@ -409,7 +444,8 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     float* res_lse_p = c.take<float>(R);
     int32_t* bonus_row = c.take<int32_t>(R);
     int32_t* bonus_pos = c.take<int32_t>(R);
-    auto* res_keys = c.take<unsigned long long>(R);
+    const int nb = n_blocks16(V);
+    auto* blk = c.take<float2>(static_cast<size_t>(R) * nb);
 
     StreamParams sp;
     std::memset(&sp, 0, sizeof sp);
@@ -436,9 +472,8 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     SDM_CHECK_CUDA(launch_stream(STREAM_LSE, sp, row_capacity, s));
     SDM_CHECK_CUDA(launch_verify_sample_scan(mode, cu_seqlens, anchor, draft, budget, logq, target, t_fp32, V, lse_part,
                                              sp.n_chunks, sp.inv_t, k0, k1, cyc, R, gamma, accept, ceiling, res_tok,
-                                             res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, res_keys, dev_status,
-                                             s));
-    // residual rows: recompute q with the Markov head, race over max(0, p - q)
+                                             res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, dev_status, s));
+    // residual rows: recompute q with the Markov head; records of max(0, p - q)
     CUtensorMap tmW;
     if (!map_w(&tmW, W, r, V)) return SDM_ERR_CUDA;
     const int n_tiles = (V + kTileN - 1) / kTileN;
@@ -459,9 +494,6 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     p.d = 1;
     p.stages = gemm_pick_stages(r, 1, p.l_fp32, MODE_RESID);
     p.inv_t = sp.inv_t;
-    p.rng_k0 = k0;
-    p.rng_k1 = k1;
-    p.rng_cycle = cyc;
     p.U = U;
     p.res_tok = res_tok;
     p.res_pos = res_pos;
@@ -472,22 +504,45 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     p.target = target;
     p.t_fp32 = t_fp32;
     p.gamma = gamma;
-    p.res_keys = res_keys;
+    p.blk = blk;
+    p.nb = nb;
     p.dev_status = dev_status;
     SDM_CHECK_CUDA(launch_markov_gemm(MODE_RESID, tmW, tmW, p, gx, gy, s));
-    // bonus rows: race over p
-    StreamParams bp = sp;
-    bp.count = nullptr;
-    bp.n_items = R;
-    bp.row_of = bonus_row;
-    bp.race_row = bonus_pos;
-    bp.keys = res_keys;
-    bp.part = nullptr;
-    bp.rng_k0 = k0;
-    bp.rng_k1 = k1;
-    bp.rng_cycle = cyc;
-    SDM_CHECK_CUDA(launch_stream(STREAM_BONUS_RACE, bp, R, s));
-    SDM_CHECK_CUDA(launch_verify_sample_finalize(draft, accept, res_keys, R, gamma, V, out_tok, n_out, dev_status, s));
+    // the residual or bonus draw of every request, then the committed tokens
+    ResampleParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    rp.blk = blk;
+    rp.nb = nb;
+    rp.res_tok = res_tok;
+    rp.res_pos = res_pos;
+    rp.res_trow = res_trow;
+    rp.res_lse_p = res_lse_p;
+    rp.lse_q = lse_q;
+    rp.L = L;
+    rp.l_fp32 = p.l_fp32;
+    rp.U = U;
+    rp.W = W;
+    rp.r = r;
+    rp.bonus_row = bonus_row;
+    rp.bonus_pos = bonus_pos;
+    rp.lse_part = lse_part;
+    rp.n_chunks = sp.n_chunks;
+    rp.chunk = sp.chunk;
+    rp.target = target;
+    rp.t_fp32 = t_fp32;
+    rp.R = R;
+    rp.gamma = gamma;
+    rp.V = V;
+    rp.inv_t = sp.inv_t;
+    rp.k0 = k0;
+    rp.k1 = k1;
+    rp.cycle = cyc;
+    rp.draft = draft;
+    rp.accept = accept;
+    rp.out_tok = out_tok;
+    rp.n_out = n_out;
+    rp.dev_status = dev_status;
+    SDM_CHECK_CUDA(launch_resample(rp, s));
     return SDM_OK;
 }
 

@@ -127,16 +127,6 @@ __device__ __forceinline__ float word_to_uniform(uint32_t w) {
     return static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-8f;
 }
 
-// 1 - u for the same word, exact.  Race filter: the key z_v - ln E_v,
-// E_v = -ln u_v, can beat a running best b only if E_v < exp(z_v - b); since
-// -ln u >= 1 - u, an element with 1 - u >= 2 exp(z_v - b) is ruled out
-// without a logarithm (the factor 2 leaves a margin of ln 2 in the key, far
-// above the rounding of the logarithms), so the winner is the same as with
-// every key formed.
-__device__ __forceinline__ float one_minus_uniform(uint32_t w) {
-    return __uint2float_rn(16777215u - 2u * (w >> 9)) * 5.9604644775390625e-8f;
-}
-
 struct RngKey {
     uint32_t k0, k1, cycle;
 };
@@ -154,13 +144,6 @@ __device__ __forceinline__ float uniform_at(RngKey k, uint32_t stream, uint32_t 
     U4 b = philox_block(k, stream, req, row, v >> 2);
     uint32_t w = (v & 3u) == 0 ? b.x : (v & 3u) == 1 ? b.y : (v & 3u) == 2 ? b.z : b.w;
     return word_to_uniform(w);
-}
-
-// ln E for the exponential race, E = -ln u.  For u > 1/2 the complement is
-// taken through log1p so that E keeps full relative precision near u = 1.
-__device__ __forceinline__ float race_log_exp(float u) {
-    float e = (u > 0.5f) ? -log1pf(u - 1.0f) : -__logf(u);
-    return __logf(e);
 }
 
 // ---------------------------------------------------------------------------

@@ -56,12 +56,14 @@ struct GemmParams {
     int k;               // tree: local top-k
     int d;               // 1-based draft position / tree level
     float inv_t;         // 1 / temperature
-    uint32_t rng_k0, rng_k1, rng_cycle;
     const uint16_t* U;   // [V, r]
     const int32_t* anchor;
     // chain
-    unsigned long long* keys;   // [B][R] argmax / race keys
-    float2* lse_part;           // [B][R][gridDim.x][kColGroups]
+    unsigned long long* keys;   // greedy: [B][R] argmax keys
+    const int32_t* tok_in;      // sample: [R, B] tokens drawn so far (step d reads column d - 2)
+    // sampling and residual: one (m, s) record per GEMM row and 16-column block
+    float2* blk;                // [rows][nb]
+    int nb;                     // ceil(V / 16)
     // tree
     const int32_t* front_tok;   // [R][P] frontier tokens (-1: empty slot)
     float* tree_part;           // [rows][gridDim.x][kColGroups][2 + 2 * kMaxTopK]
@@ -75,7 +77,6 @@ struct GemmParams {
     const void* target;         // packed target rows
     int t_fp32;                 // target element type
     int gamma;
-    unsigned long long* res_keys;   // [R]
     // absmax (prepared tables): GEMM row m = token m
     unsigned int* absmax_bits;      // [rows] max_v |U[m] . W[:, v]| as fp32 bits (atomic max)
     int32_t* dev_status;
@@ -87,9 +88,9 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
                                int grid_x, int grid_y, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
-// Vocab-row streaming kernels (argmax / log-sum-exp / race over target rows)
+// Vocab-row streaming kernels (argmax / log-sum-exp partials over target rows)
 // ---------------------------------------------------------------------------
-enum StreamOp { STREAM_ARGMAX = 0, STREAM_LSE = 1, STREAM_BONUS_RACE = 2 };
+enum StreamOp { STREAM_ARGMAX = 0, STREAM_LSE = 1 };
 
 struct StreamParams {
     const void* base;       // row r starts at base + r * V elements
@@ -101,11 +102,8 @@ struct StreamParams {
     const int32_t* count;   // device item count (e.g. cu_seqlens + R), may be NULL
     const int32_t* row_of;  // item -> row index (NULL: identity; < 0: skip)
     float inv_t;
-    unsigned long long* keys;   // ARGMAX: [n_items][n_chunks] partial keys; BONUS: [n_items] (atomic max)
-    float2* part;               // LSE: [n_items][n_chunks]
-    // bonus race
-    uint32_t rng_k0, rng_k1, rng_cycle;
-    const int32_t* race_row;    // item -> Philox row (window position)
+    unsigned long long* keys;   // ARGMAX: [n_items][n_chunks] partial keys
+    float2* part;               // LSE: [n_items][n_chunks] (max, sum of exp(x - max)) of x = row / T
 };
 
 cudaError_t launch_stream(int op, const StreamParams& p, int max_items, cudaStream_t s);
@@ -115,10 +113,9 @@ cudaError_t launch_stream(int op, const StreamParams& p, int max_items, cudaStre
 // ---------------------------------------------------------------------------
 cudaError_t launch_fill_u64(unsigned long long* p, size_t n, unsigned long long v, cudaStream_t s);
 
-cudaError_t launch_chain_finalize(const unsigned long long* keys, const float2* lse_part, int gx, int R, int B, int V,
-                                  int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
-                                  const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
-                                  float* lse, int32_t* dev_status, cudaStream_t s);
+// greedy chain: tokens from the argmax keys [B][R]
+cudaError_t launch_chain_finalize(const unsigned long long* keys, int R, int B, int V, int32_t* tokens,
+                                  int32_t* dev_status, cudaStream_t s);
 
 cudaError_t launch_schedule(const float* conf, int R, int gamma, const double* cost, float* survival,
                             int32_t* budget, double* expected, int32_t* total_tokens, unsigned long long* ws_keys,
@@ -140,12 +137,63 @@ cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t
                                       int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
                                       uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
                                       int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
-                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
-                                      unsigned long long* res_keys, int32_t* dev_status, cudaStream_t s);
+                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int32_t* dev_status,
+                                      cudaStream_t s);
 
-cudaError_t launch_verify_sample_finalize(const int32_t* draft, const int32_t* accept,
-                                          const unsigned long long* res_keys, int R, int gamma, int V,
-                                          int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s);
+// ---------------------------------------------------------------------------
+// Inverse-CDF draws (select.cu).  A draw walks a row's (m, s) records, whose
+// weights are s exp(m - max m), to the record holding u S, then recomputes
+// the record's elements to find the id.
+// ---------------------------------------------------------------------------
+struct DraftSelectParams {
+    const float2* blk;       // [R][nb] records of step d (MODE_CHAIN_SAMPLE)
+    int nb;
+    int R, B, V, r, d;       // d: 1-based draft position
+    const void* L;           // [R, B, V]
+    int l_fp32;
+    const uint16_t* U;       // [V, r]
+    const uint16_t* W;       // [r, V]
+    const int32_t* anchor;
+    float inv_t;
+    uint32_t k0, k1, cycle;  // Philox key and cycle
+    int32_t* tokens;         // [R, B]
+    float* logq;             // [R, B] or NULL
+    float* lse;              // [R, B] or NULL
+    int32_t* dev_status;
+};
+cudaError_t launch_draft_select(const DraftSelectParams& p, cudaStream_t s);
+
+struct ResampleParams {
+    // residual rows (res_tok >= 0): records of MODE_RESID
+    const float2* blk;       // [R][nb]
+    int nb;
+    const int32_t* res_tok;  // [R] token before the rejected position, -1: none
+    const int32_t* res_pos;  // [R] rejected window position a
+    const int32_t* res_trow; // [R] packed target row of position a
+    const float* res_lse_p;  // [R]
+    const float* lse_q;      // [R, gamma]
+    const void* L;           // [R, gamma, V]
+    int l_fp32;
+    const uint16_t* U;
+    const uint16_t* W;
+    int r;
+    // bonus rows (bonus_row >= 0): chunk log-sum-exp partials of the target row
+    const int32_t* bonus_row;
+    const int32_t* bonus_pos;
+    const float2* lse_part;  // [rows][n_chunks]
+    int n_chunks, chunk;
+    const void* target;
+    int t_fp32;
+    int R, gamma, V;
+    float inv_t;
+    uint32_t k0, k1, cycle;
+    const int32_t* draft;    // [R, gamma]
+    const int32_t* accept;   // [R]
+    int32_t* out_tok;        // [R, gamma + 1]
+    int32_t* n_out;          // [R]
+    int32_t* dev_status;
+};
+cudaError_t launch_resample(const ResampleParams& p, cudaStream_t s);
 
 // PCTree
 cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,

@@ -6,9 +6,12 @@
 //     z[m, v] = L[row(m), v] + (U[tok(m)] . W)[v]          v in [0, V)
 // and reduces them over the vocabulary without writing z anywhere:
 //   MODE_CHAIN_GREEDY  argmax_v z                       (DSpark notes sec. 4)
-//   MODE_CHAIN_SAMPLE  exponential race on z / T + log-sum-exp partials
+//   MODE_CHAIN_SAMPLE  per 16-column block: max of z / T and the sum of
+//                      exp(z / T - max) (the records an inverse-CDF draw
+//                      walks; the draw itself is select.cu's)
 //   MODE_TREE          log-sum-exp partials + local top-k by z  (PCTree)
-//   MODE_RESID         race over max(0, p - q) at a rejected position
+//   MODE_RESID         per 16-column block: the sum of max(0, p - q) at a
+//                      rejected position
 //   MODE_ABSMAX        max_v |U[m] . W[:, v]| for m = 0..V-1, no L (the
 //                      per-token bound of the pruned greedy chain)
 //
@@ -26,7 +29,8 @@
 //   * warps 2-17 drain the accumulator with tcgen05.ld (thread = GEMM row of
 //     its TMEM sub-partition; four warps per sub-partition, one per 16-column
 //     group of every tile), add L and run the mode's reduction in registers;
-//     one result per row, CTA and column group is written at the end.
+//     one result per row, CTA and column group is written at the end (the
+//     sampling modes write one record per row and 16-column block instead).
 // The grid is (vocab splits) x (M tiles), one CTA per SM; vocab tiles are
 // dealt to the splits round-robin.
 #include "device.cuh"
@@ -63,9 +67,12 @@ __device__ __forceinline__ void fail_timeout(const GemmParams& p) { set_status(p
 template <int MODE>
 __device__ __forceinline__ int gemm_row_token(const GemmParams& p, int grow) {
     int t = -1;
-    if (MODE == MODE_CHAIN_GREEDY || MODE == MODE_CHAIN_SAMPLE) {
+    if (MODE == MODE_CHAIN_GREEDY) {
         if (grow >= p.R) return -1;
         t = (p.d == 1) ? p.anchor[grow] : static_cast<int>(key_token(p.keys[static_cast<size_t>(p.d - 2) * p.R + grow]));
+    } else if (MODE == MODE_CHAIN_SAMPLE) {
+        if (grow >= p.R) return -1;
+        t = (p.d == 1) ? p.anchor[grow] : p.tok_in[static_cast<size_t>(grow) * p.B + (p.d - 2)];
     } else if (MODE == MODE_TREE) {
         if (grow >= p.rows) return -1;
         t = p.front_tok[grow];
@@ -218,77 +225,31 @@ struct Epi<MODE_CHAIN_GREEDY> {
     }
 };
 
-// Race filter (see one_minus_uniform): exp(z_v - b) is formed as
-// exp(z_v - m) exp(m - b) with m the running maximum of z, the first factor
-// being the log-sum-exp term already at hand.
+// Block record (m, s) of the 16 columns: m = max z / T, s = sum exp(z / T - m).
 template <>
 struct Epi<MODE_CHAIN_SAMPLE> {
     bool valid;
     int group;
-    float best;
-    uint32_t best_v;
-    float m, s;
-    float g2;     // 2 exp(m - best): an element passes the race filter if 1 - u < exp(z - m) g2
-    RngKey key;
+    float2* rec;   // this row's records [nb]
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R;
-        best = -INFINITY;
-        best_v = 0;
-        m = -INFINITY;
-        s = 0.f;
-        g2 = INFINITY;
-        key = RngKey{p.rng_k0, p.rng_k1, p.rng_cycle};
+        rec = p.blk + static_cast<size_t>(valid ? grow : 0) * p.nb;
     }
     __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
                                             int g, const uint32_t (&acc)[C]) {
-        if (!valid) return;
-        float lv[C];
-        load_l(sl, lbb, p.l_fp32, lrow, g, lv);
-        const int grow = lrow + blockIdx.y * kTileM;
-        float zt[C];
-        float mx = -INFINITY;
+        if (!valid || vbase >= p.V) return;
+        float z[C];
+        load_l(sl, lbb, p.l_fp32, lrow, g, z);
 #pragma unroll
-        for (int j = 0; j < C; ++j) {
-            zt[j] = (lv[j] + __uint_as_float(acc[j])) * p.inv_t;
-            if (vbase + j < p.V) mx = fmaxf(mx, zt[j]);
-        }
-        if (mx > m) {
-            s *= __expf(m - mx);
-            m = mx;
-            g2 = 2.0f * __expf(m - best);
-        }
-        U4 blk[C / 4];
+        for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * p.inv_t;
+        mask_tail(z, vbase, p.V);
+        const float m = maxc(z);
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < C / 4; ++c)   // independent blocks: their rounds interleave
-            blk[c] = philox_block(key, 0u, static_cast<uint32_t>(grow), static_cast<uint32_t>(p.d),
-                                  static_cast<uint32_t>(vbase + c * 4) >> 2);
-#pragma unroll
-        for (int c = 0; c < C / 4; ++c) {
-            const int v4 = vbase + c * 4;
-            if (v4 >= p.V) break;
-            const uint32_t w[4] = {blk[c].x, blk[c].y, blk[c].z, blk[c].w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float z = zt[c * 4 + q];
-                const float e = __expf(z - m);
-                s += e;
-                if (one_minus_uniform(w[q]) < e * g2) {   // else the key cannot beat best
-                    const float k = z - race_log_exp(word_to_uniform(w[q]));
-                    if (k > best) {
-                        best = k;
-                        best_v = static_cast<uint32_t>(v4 + q);
-                        g2 = 2.0f * __expf(m - best);
-                    }
-                }
-            }
-        }
+        for (int j = 0; j < C; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
+        rec[vbase / C] = make_float2(m, (ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
-    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
-        if (!valid) return;
-        const size_t o = static_cast<size_t>(p.d - 1) * p.R + grow;
-        atomicMax(&p.keys[o], argmax_key(best, best_v));
-        p.lse_part[(o * gridDim.x + blockIdx.x) * kColGroups + group] = make_float2(m, s);
-    }
+    __device__ __forceinline__ void flush(const GemmParams&, int) {}
 };
 
 template <>
@@ -374,64 +335,43 @@ struct Epi<MODE_TREE> {
     }
 };
 
+// Block record (0, s) of the 16 columns: s = sum max(0, p_v - q_v) with
+// p_v = exp(target / T - lse_p), q_v = exp(z / T - lse_q).
 template <>
 struct Epi<MODE_RESID> {
     bool valid;
     int group;
-    float best;
-    uint32_t best_v;
-    int jpos;
     size_t l_off, t_off;
     float lse_q, lse_p;
-    RngKey key;
+    float2* rec;
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R && p.res_tok[grow] >= 0;
-        best = -INFINITY;
-        best_v = 0;
-        key = RngKey{p.rng_k0, p.rng_k1, p.rng_cycle};
+        rec = p.blk + static_cast<size_t>(grow < p.R ? grow : 0) * p.nb;
         if (valid) {
-            jpos = p.res_pos[grow];
+            const int jpos = p.res_pos[grow];
             l_off = (static_cast<size_t>(grow) * p.gamma + jpos) * static_cast<size_t>(p.V);
             t_off = static_cast<size_t>(p.res_trow[grow]) * static_cast<size_t>(p.V);
             lse_q = p.lse_q[static_cast<size_t>(grow) * p.gamma + jpos];
             lse_p = p.res_lse_p[grow];
         }
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int lrow, int vbase, int,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int vbase, int,
                                             const uint32_t (&acc)[C]) {
-        if (!valid) return;
-        const int grow = lrow + blockIdx.y * kTileM;
+        if (!valid || vbase >= p.V) return;
         float lv[C], tv[C];
         load_g(p.L, p.l_fp32, l_off, vbase, p.V, lv);
         load_g(p.target, p.t_fp32, t_off, vbase, p.V, tv);
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < C / 4; ++c) {
-            const int v4 = vbase + c * 4;
-            if (v4 >= p.V) break;
-            const U4 blk = philox_block(key, 2u, static_cast<uint32_t>(grow), static_cast<uint32_t>(jpos),
-                                        static_cast<uint32_t>(v4) >> 2);
-            const uint32_t w[4] = {blk.x, blk.y, blk.z, blk.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = c * 4 + q;
-                const float lq = (lv[j] + __uint_as_float(acc[j])) * p.inv_t - lse_q;   // log q_v
-                const float lp = tv[j] * p.inv_t - lse_p;                                 // log p_v
-                // race filter with p - q <= p: the key cannot beat best
-                // unless 1 - u < 2 exp(log p - best)
-                if (lp > lq && one_minus_uniform(w[q]) < 2.0f * __expf(lp - best)) {
-                    // log(p - q) = log p + log(1 - q/p)
-                    const float k = lp + log1pf(-__expf(lq - lp)) - race_log_exp(word_to_uniform(w[q]));
-                    if (k > best) {
-                        best = k;
-                        best_v = static_cast<uint32_t>(v4 + q);
-                    }
-                }
-            }
+        for (int j = 0; j < C; ++j) {
+            const float q = __expf((lv[j] + __uint_as_float(acc[j])) * p.inv_t - lse_q);
+            const float pv = __expf(tv[j] * p.inv_t - lse_p);
+            const float w = (vbase + j < p.V) ? fmaxf(pv - q, 0.f) : 0.f;
+            ps[j & 3] += w;
         }
+        rec[vbase / C] = make_float2(0.f, (ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
-    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
-        if (valid) atomicMax(&p.res_keys[grow], argmax_key(best, best_v));
-    }
+    __device__ __forceinline__ void flush(const GemmParams&, int) {}
 };
 
 template <>
@@ -485,17 +425,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     // every W and L row
     const int nt = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
-    // 1. gather A = U[tok(m)] for the 128 rows (K-major, 128-byte swizzle:
-    //    16-byte chunk c of row m in K block kb sits at chunk c ^ (m & 7)).
-    const int kchunks = p.r >> 3;
-    for (int rr = warp; rr < kTileM; rr += kGemmThreads / 32) {
-        const int tok = gemm_row_token<MODE>(p, row0 + rr);
-        const uint16_t* src = p.U + static_cast<size_t>(tok < 0 ? 0 : tok) * p.r;
-        for (int q = lane; q < kchunks; q += 32) {
-            uint8_t* dst = sA + (q >> 3) * (kTileM * 128) + rr * 128 + (((q & 7) ^ (rr & 7)) << 4);
-            cp_async_16(dst, src + q * 8, tok < 0 ? 0u : 16u);
-        }
-    }
+    // set-up that reads nothing the previous kernel in the stream writes
     if (threadIdx.x == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&full[s], 1);
@@ -510,6 +440,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmW);
         if (mode_reads_l(MODE)) tma_prefetch_desc(&tmL);
+    }
+    pdl_wait();   // tokens (and every buffer this launch writes) belong to the previous kernel until here
+    pdl_trigger();
+
+    // 1. gather A = U[tok(m)] for the 128 rows (K-major, 128-byte swizzle:
+    //    16-byte chunk c of row m in K block kb sits at chunk c ^ (m & 7)).
+    const int kchunks = p.r >> 3;
+    for (int rr = warp; rr < kTileM; rr += kGemmThreads / 32) {
+        const int tok = gemm_row_token<MODE>(p, row0 + rr);
+        const uint16_t* src = p.U + static_cast<size_t>(tok < 0 ? 0 : tok) * p.r;
+        for (int q = lane; q < kchunks; q += 32) {
+            uint8_t* dst = sA + (q >> 3) * (kTileM * 128) + rr * 128 + (((q & 7) ^ (rr & 7)) << 4);
+            cp_async_16(dst, src + q * 8, tok < 0 ? 0u : 16u);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
@@ -649,8 +593,7 @@ cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const Ge
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    markov_gemm_kernel<MODE><<<dim3(gx, gy), kGemmThreads, lay.total, s>>>(tmW, tmL, p);
-    return cudaGetLastError();
+    return launch_pdl(markov_gemm_kernel<MODE>, dim3(gx, gy), dim3(kGemmThreads), lay.total, s, tmW, tmL, p);
 }
 
 }  // namespace

@@ -1,4 +1,4 @@
-// small.cu - the latency-bound kernels of the cycle: chain finalisation,
+// small.cu - the latency-bound kernels of the cycle: greedy chain finalisation,
 // the prefix scheduler, the ragged pack, the per-request verification scans,
 // and PCTree's per-level merge/prune and final top-N selection.
 #include "device.cuh"
@@ -20,46 +20,19 @@ __global__ void fill_u64_kernel(unsigned long long* p, size_t n, unsigned long l
 }
 
 // ---------------------------------------------------------------------------
-// chain finalize: tokens from the argmax keys; for sampling, merge the
-// log-sum-exp partials in a fixed order and form log q(y_d).
+// greedy chain finalize: tokens [R, B] from the argmax keys [B][R]
 // ---------------------------------------------------------------------------
-__global__ void chain_finalize_kernel(const unsigned long long* keys, const float2* lse_part, int gx, int R, int B,
-                                      int V, int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
-                                      const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
-                                      float* lse, int32_t* dev_status) {
-    // one warp per (request, step): lanes share the partials and the dot product
-    const int idx = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
+__global__ void chain_finalize_kernel(const unsigned long long* keys, int R, int B, int V, int32_t* tokens,
+                                      int32_t* dev_status) {
+    const int idx = blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= R * B) return;
     const int i = idx / B, d = idx % B + 1;
-    const size_t o = static_cast<size_t>(d - 1) * R + i;
-    int y = static_cast<int>(key_token(keys[o]));
+    int y = static_cast<int>(key_token(keys[static_cast<size_t>(d - 1) * R + i]));
     if (y < 0 || y >= V) {
-        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_TOKEN);
+        set_status(dev_status, SDM_DEV_BAD_TOKEN);
         y = 0;
     }
-    if (lane == 0) tokens[static_cast<size_t>(i) * B + d - 1] = y;
-    if (!sample) return;
-    Lse acc{-INFINITY, 0.f};
-    for (int c = lane; c < gx; c += 32) {
-        const float2 pc = lse_part[o * gx + c];
-        acc = lse_merge(acc, Lse{pc.x, pc.y});
-    }
-    acc = warp_lse(acc);
-    const float l = acc.m + logf(acc.s);
-    int prev = (d == 1) ? anchor[i] : static_cast<int>(key_token(keys[o - R]));
-    if (prev < 0 || prev >= V) prev = 0;
-    // z_d[y] = L + U[prev] . W[:, y]; exact in fp32 on the 2^-8 grid tables
-    float m = 0.f;
-    for (int j = lane; j < r; j += 32)
-        m += bf16_bits_to_float(U[static_cast<size_t>(prev) * r + j]) * bf16_bits_to_float(W[static_cast<size_t>(j) * V + y]);
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) m += __shfl_xor_sync(0xffffffffu, m, s);
-    if (lane == 0) {
-        const float z = load_elem(L, l_fp32, (static_cast<size_t>(i) * B + (d - 1)) * V + y) + m;
-        if (lse) lse[static_cast<size_t>(i) * B + d - 1] = l;
-        if (logq) logq[static_cast<size_t>(i) * B + d - 1] = z * inv_t - l;
-    }
+    tokens[idx] = y;
 }
 
 // ---------------------------------------------------------------------------
@@ -432,7 +405,7 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
                                           uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
                                           int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
                                           float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
-                                          unsigned long long* res_keys, int32_t* dev_status) {
+                                          int32_t* dev_status) {
     // one warp per request; lane p runs the accept test of window row p (all
     // rows at once, each from its own partials), the first failure wins
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -482,7 +455,6 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
     const int a = A < cap ? A : cap;
     accept[i] = a;
     if (ceiling) ceiling[i] = A;
-    res_keys[i] = 0ull;
     if (A < cap) {   // rejected at row a: residual from max(0, p - q)
         res_tok[i] = (a == 0) ? anchor[i] : y[a - 1];
         res_pos[i] = a;
@@ -498,25 +470,6 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
         bonus_row[i] = row0 + a;
         bonus_pos[i] = a;
     }
-}
-
-__global__ void verify_sample_finalize_kernel(const int32_t* draft, const int32_t* accept,
-                                              const unsigned long long* res_keys, int R, int gamma, int V,
-                                              int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= R) return;
-    const int a = accept[i];
-    int t = static_cast<int>(key_token(res_keys[i]));
-    if (t < 0 || t >= V) {
-        set_status(dev_status, SDM_DEV_BAD_TOKEN);
-        t = 0;
-    }
-    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
-    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
-    for (int p = 0; p < a; ++p) o[p] = y[p];
-    o[a] = t;
-    for (int p = a + 1; p <= gamma; ++p) o[p] = -1;
-    n_out[i] = a + 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -817,12 +770,10 @@ cudaError_t launch_fill_u64(unsigned long long* p, size_t n, unsigned long long 
     return cudaGetLastError();
 }
 
-cudaError_t launch_chain_finalize(const unsigned long long* keys, const float2* lse_part, int gx, int R, int B, int V,
-                                  int r, const void* L, int l_fp32, const uint16_t* U, const uint16_t* W,
-                                  const int32_t* anchor, float inv_t, int sample, int32_t* tokens, float* logq,
-                                  float* lse, int32_t* dev_status, cudaStream_t s) {
-    chain_finalize_kernel<<<blocks_for(static_cast<long long>(R) * B * 32, 128), 128, 0, s>>>(
-        keys, lse_part, gx, R, B, V, r, L, l_fp32, U, W, anchor, inv_t, sample, tokens, logq, lse, dev_status);
+cudaError_t launch_chain_finalize(const unsigned long long* keys, int R, int B, int V, int32_t* tokens,
+                                  int32_t* dev_status, cudaStream_t s) {
+    chain_finalize_kernel<<<blocks_for(static_cast<long long>(R) * B, 128), 128, 0, s>>>(keys, R, B, V, tokens,
+                                                                                         dev_status);
     return cudaGetLastError();
 }
 
@@ -866,19 +817,11 @@ cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t
                                       int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
                                       uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
                                       int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
-                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
-                                      unsigned long long* res_keys, int32_t* dev_status, cudaStream_t s) {
+                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int32_t* dev_status,
+                                      cudaStream_t s) {
     verify_sample_scan_kernel<<<blocks_for(static_cast<long long>(R) * 32, 128), 128, 0, s>>>(
         mode, cu, anchor, draft, budget, logq, target, t_fp32, V, lse_part, n_chunks, inv_t, k0, k1, cycle, R, gamma,
-        accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, res_keys, dev_status);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_verify_sample_finalize(const int32_t* draft, const int32_t* accept,
-                                          const unsigned long long* res_keys, int R, int gamma, int V,
-                                          int32_t* out_tok, int32_t* n_out, int32_t* dev_status, cudaStream_t s) {
-    verify_sample_finalize_kernel<<<blocks_for(R, 128), 128, 0, s>>>(draft, accept, res_keys, R, gamma, V, out_tok,
-                                                                      n_out, dev_status);
+        accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, dev_status);
     return cudaGetLastError();
 }
 

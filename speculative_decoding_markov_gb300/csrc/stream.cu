@@ -1,7 +1,7 @@
 // stream.cu - HBM-bound reductions over vocab rows of the packed target
-// logits: argmax (greedy verification, PCTree verification), log-sum-exp
-// partials (rejection sampling), and the exponential race that draws the
-// bonus token from p.
+// logits: argmax (greedy verification, PCTree verification) and log-sum-exp
+// partials per chunk (rejection sampling: the normaliser of p, and the chunk
+// weights the bonus draw walks).
 //
 // Work item = (row, chunk of `chunk` ids).  A persistent grid of CTAs walks
 // the items; each thread streams 16-byte vectors (8 bf16 or 4 fp32) with four
@@ -55,7 +55,6 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
     const int n_items = p.count ? *p.count : p.n_items;
     const long long total = static_cast<long long>(n_items) * p.n_chunks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const RngKey rk{p.rng_k0, p.rng_k1, p.rng_cycle};
 
     for (long long w = blockIdx.x; w < total; w += gridDim.x) {
         const int item = static_cast<int>(w / p.n_chunks);
@@ -68,7 +67,6 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
         const size_t esz = FP32 ? 4 : 2;
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.base) +
                                                           (static_cast<size_t>(row) * p.V + v_begin) * esz);
-        const uint32_t race_row = (OP == STREAM_BONUS_RACE) ? static_cast<uint32_t>(p.race_row[item]) : 0u;
 
         Argmax am;
         OnlineLse ls;
@@ -101,22 +99,10 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
                 if (OP == STREAM_ARGMAX) {
 #pragma unroll
                     for (int q = 0; q < VEC; ++q) am.add(val[q], v0 + q);
-                } else if (OP == STREAM_LSE) {
+                } else {
 #pragma unroll
                     for (int q = 0; q < VEC; ++q) val[q] *= p.inv_t;
                     ls.add(val);
-                } else {
-#pragma unroll
-                    for (int b = 0; b < VEC / 4; ++b) {
-                        const U4 blk = philox_block(rk, 3u, static_cast<uint32_t>(item), race_row, (v0 >> 2) + b);
-                        const uint32_t wd[4] = {blk.x, blk.y, blk.z, blk.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float z = val[b * 4 + q] * p.inv_t;
-                            if (one_minus_uniform(wd[q]) < 2.0f * __expf(z - am.best))   // race filter
-                                am.add(z - race_log_exp(word_to_uniform(wd[q])), v0 + b * 4 + q);
-                        }
-                    }
                 }
             }
         }
@@ -141,10 +127,7 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
             if (threadIdx.x == 0) {
                 unsigned long long acc = red_key[0];
                 for (int q = 1; q < kThreads / 32; ++q) acc = umax64(acc, red_key[q]);
-                if (OP == STREAM_ARGMAX)
-                    p.keys[static_cast<size_t>(item) * p.n_chunks + chunk] = acc;   // one partial per chunk
-                else
-                    atomicMax(&p.keys[item], acc);
+                p.keys[static_cast<size_t>(item) * p.n_chunks + chunk] = acc;   // one partial per chunk
             }
             __syncthreads();
         }
@@ -166,7 +149,6 @@ cudaError_t launch_stream(int op, const StreamParams& p, int max_items, cudaStre
     switch (op) {
         case STREAM_ARGMAX: return launch_op<STREAM_ARGMAX>(p, max_items, s);
         case STREAM_LSE: return launch_op<STREAM_LSE>(p, max_items, s);
-        case STREAM_BONUS_RACE: return launch_op<STREAM_BONUS_RACE>(p, max_items, s);
         default: return cudaErrorInvalidValue;
     }
 }
