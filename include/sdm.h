@@ -171,8 +171,12 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
  *   tok, parent, depth [R, N+1] int32; score [R, N+1] fp32;
  *   mask [R, N+1, ceil((N+1)/32)] uint32, bit j of row c set iff slot j is c
  *   or an ancestor of c; n_nodes [R] int32 (root included).
+ * Each level runs the tcgen05 GEMM for every frontier row with per-16-column
+ * (max, sum of exp) records in its epilogue; the row's top-k ids lie in the
+ * k blocks with the largest maxima, so one CTA per row ranks the records,
+ * recomputes the logits of its 2k best blocks and ranks those.
  * Constraints: 1 <= k <= 8, 1 <= P, P*k <= 64, 128 % P == 0, N <= P*B,
- * P*B + 1 <= 8192 (else SDM_ERR_UNSUPPORTED).
+ * P*B + 1 <= 8192, V <= 524288 (else SDM_ERR_UNSUPPORTED).
  */
 sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
                           const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N,

@@ -44,13 +44,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// W [r, V] bf16 as a 2-D map (V innermost), box 64 x r, 128-byte swizzle.
+// W [r, V] bf16 as a 2-D map (V innermost), box 64 ids x 64 K rows, 128-byte swizzle.
 bool map_w(CUtensorMap* m, const uint16_t* W, int r, int V) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(V), static_cast<cuuint64_t>(r)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(V) * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(r)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBoxN), 64u};
     cuuint32_t es[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(W), dims, strides, box, es,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -89,7 +89,9 @@ inline int n_chunks_of(int V, int fp32) {
         if ((x) != cudaSuccess) return SDM_ERR_CUDA; \
     } while (0)
 
-inline int n_blocks16(int V) { return (V + 15) / 16; }
+// Row stride of the (m, s) records, one per 16-column block: rounded up to an
+// even count so that every row starts on a 16-byte boundary (bulk copies).
+inline int n_blocks16(int V) { return (((V + 15) / 16) + 1) & ~1; }
 
 // greedy: argmax keys [B][R]; sampling: one (m, s) record per request and
 // 16-column block, reused by every step
@@ -105,11 +107,12 @@ size_t ws_chain_pruned(int R, int B, int V) {
 
 size_t ws_chain(int R, int B, int V) { return std::max(ws_chain_dense(R, B, V), ws_chain_pruned(R, B, V)); }
 
-size_t ws_tree(int R, int B, int P) {
+// block records [rows][nb], per-row top-k and log-sum-exp, frontier and pool
+size_t ws_tree(int R, int B, int P, int V) {
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
-    return align256(rows * kMaxGx * kColGroups * (2 + 2 * kMaxTopK) * 4) + 3 * align256(rows * 4) + align256(R * 4) +
-           4 * align256(pool * 4) + align256(R * 4);
+    return align256(rows * n_blocks16(V) * 8) + align256(rows * kMaxTopK * 8) + align256(rows * 4) +
+           3 * align256(rows * 4) + align256(R * 4) + 4 * align256(pool * 4) + align256(R * 4);
 }
 
 size_t ws_verify(int R, int rows, int V) {
@@ -128,7 +131,7 @@ size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int 
     if (R <= 0) return 0;
     switch (op) {
         case SDM_OP_DRAFT_CHAIN: return ws_chain(R, B, V);
-        case SDM_OP_DRAFT_TREE: return ws_tree(R, B, P);
+        case SDM_OP_DRAFT_TREE: return ws_tree(R, B, P, V);
         case SDM_OP_VERIFY: return ws_verify(R, P, V);
         case SDM_OP_VERIFY_TREE:
             return align256(static_cast<size_t>(R) * (N + 1) * 8 * std::max(n_chunks_of(V, 0), n_chunks_of(V, 1)));
@@ -188,7 +191,7 @@ sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r
     p.k = 1;
     p.d = 1;
     p.inv_t = 1.0f;
-    p.stages = gemm_pick_stages(r, 1, 0, MODE_ABSMAX);
+    gemm_pick_stages(p, MODE_ABSMAX);
     p.U = U;
     p.absmax_bits = absmax;
     p.dev_status = dev_status;
@@ -269,7 +272,7 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
     p.l_rows = l_rows;
     p.P = 1;
     p.k = 1;
-    p.stages = gemm_pick_stages(r, l_rows, fp32, mode);
+    gemm_pick_stages(p, mode);
     p.inv_t = decode == SDM_SAMPLE ? 1.0f / temperature : 1.0f;
     p.U = U;
     p.anchor = anchor;
@@ -330,12 +333,16 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
     if (k > kMaxTopK || k > V || P * k > 64 || kTileM % P != 0 || N > P * B) return SDM_ERR_UNSUPPORTED;
     if (static_cast<long long>(P) * B + 1 > 8192) return SDM_ERR_UNSUPPORTED;   // the pool is ranked in shared memory
-    if (!ws || ws_bytes < ws_tree(R, B, P)) return SDM_ERR_WORKSPACE;
+    if (V > 16 * 32768) return SDM_ERR_UNSUPPORTED;   // the per-row candidate list of the level select
+    if (!ws || ws_bytes < ws_tree(R, B, P, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
     Carver c{static_cast<uint8_t*>(ws)};
-    float* tree_part = c.take<float>(rows * kMaxGx * kColGroups * (2 + 2 * kMaxTopK));
+    const int nb = n_blocks16(V);
+    auto* blk = c.take<float2>(rows * nb);
+    auto* row_top = c.take<float2>(rows * kMaxTopK);
+    float* row_lse = c.take<float>(rows);
     int32_t* front_tok = c.take<int32_t>(rows);
     int32_t* front_node = c.take<int32_t>(rows);
     float* front_score = c.take<float>(rows);
@@ -366,20 +373,41 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     p.l_rows = l_rows;
     p.P = P;
     p.k = k;
-    p.stages = gemm_pick_stages(r, l_rows, fp32, MODE_TREE);
+    gemm_pick_stages(p, MODE_TREE);
     p.inv_t = 1.0f;
     p.U = U;
     p.anchor = anchor;
     p.front_tok = front_tok;
-    p.tree_part = tree_part;
+    p.blk = blk;
+    p.nb = nb;
     p.dev_status = dev_status;
+    TreeSelectParams tp;
+    std::memset(&tp, 0, sizeof tp);
+    tp.blk = blk;
+    tp.nb = nb;
+    tp.rows = static_cast<int>(rows);
+    tp.P = P;
+    tp.B = B;
+    tp.V = V;
+    tp.r = r;
+    tp.k = k;
+    tp.front_tok = front_tok;
+    tp.L = L;
+    tp.l_fp32 = fp32;
+    tp.U = U;
+    tp.W = W;
+    tp.row_top = row_top;
+    tp.row_lse = row_lse;
+    tp.dev_status = dev_status;
 
     SDM_CHECK_CUDA(launch_tree_init(anchor, R, P, B, front_tok, front_node, front_score, n_front, pool_tok, pool_parent,
                                     pool_depth, pool_score, pool_n, dev_status, s));
     for (int d = 1; d <= B; ++d) {
         p.d = d;
+        tp.d = d;
         SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE, tmW, tmL, p, gx, gy, s));
-        SDM_CHECK_CUDA(launch_tree_merge(tree_part, kColGroups * gx, R, P, k, B, d, front_tok, front_node, front_score, n_front,
+        SDM_CHECK_CUDA(launch_tree_select(tp, s));
+        SDM_CHECK_CUDA(launch_tree_merge(row_top, row_lse, R, P, k, B, d, front_tok, front_node, front_score, n_front,
                                          pool_tok, pool_parent, pool_depth, pool_score, pool_n, s));
     }
     SDM_CHECK_CUDA(launch_tree_finalize(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok, parent,
@@ -492,7 +520,7 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     p.P = 1;
     p.k = 1;
     p.d = 1;
-    p.stages = gemm_pick_stages(r, 1, p.l_fp32, MODE_RESID);
+    gemm_pick_stages(p, MODE_RESID);
     p.inv_t = sp.inv_t;
     p.U = U;
     p.res_tok = res_tok;

@@ -122,6 +122,14 @@ __device__ __forceinline__ U4 philox10(U4 c, uint32_t k0, uint32_t k1) {
     return c;
 }
 
+// 2^x by the SFU (ex2.approx: relative error below 2^-22 over the normal
+// range, flushes subnormal results to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Uniform (2 (w >> 9) + 1) 2^-24 in (0, 1), exact in fp32.
 __device__ __forceinline__ float word_to_uniform(uint32_t w) {
     return static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-8f;
@@ -230,6 +238,15 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
 // ---------------------------------------------------------------------------
 // cp.async (16-byte global -> shared, zero-filled when src_bytes == 0)
 // ---------------------------------------------------------------------------
+// Untiled bulk copy global -> shared memory of this CTA: both addresses
+// 16-byte aligned, bytes a multiple of 16; completion counted on bar.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
                  : "memory");

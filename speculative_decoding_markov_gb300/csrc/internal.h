@@ -29,15 +29,16 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 // ---------------------------------------------------------------------------
-// Markov GEMM (tcgen05): one CTA = one 128-row M tile x a contiguous range of
-// 64-wide vocab tiles; K = r (<= 256, multiple of 64).
+// Markov GEMM (tcgen05): one CTA = one 128-row M tile x a round-robin set of
+// 128-wide vocab tiles; K = r (<= 256, multiple of 64).
 // ---------------------------------------------------------------------------
 constexpr int kTileM = 128;        // GEMM rows per CTA (TMEM lanes)
-constexpr int kTileN = 64;         // vocab ids per tile (one 128-byte bf16 swizzle span)
-constexpr int kColGroups = 4;      // epilogue column groups per tile (16 columns each)
-constexpr int kEpiCols = kTileN / kColGroups;
+constexpr int kTileN = 128;        // vocab ids per tile = N of one tcgen05.mma
+constexpr int kBoxN = 64;          // vocab ids per TMA box (one 128-byte bf16 swizzle span)
+constexpr int kColGroups = 4;      // epilogue column groups per box (16 columns each)
+constexpr int kEpiCols = kBoxN / kColGroups;
 constexpr int kEpiWarps = 4 * kColGroups;          // four TMEM sub-partitions x column groups
-constexpr int kGemmThreads = 64 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA, warps 2.. epilogue
+constexpr int kGemmThreads = 96 + 32 * kEpiWarps;  // warp 0 W loads, warp 1 MMA, warp 2 L loads, warps 3.. epilogue
 constexpr int kMaxTopK = 8;
 
 enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3, MODE_ABSMAX = 4 };
@@ -49,7 +50,8 @@ struct GemmParams {
     int rows;            // GEMM rows in use
     int R, B, V, r;
     int n_tiles;         // ceil(V / 64)
-    int stages;          // smem pipeline depth
+    int w_stages;        // W ring depth (64 K rows x 128 ids per stage)
+    int l_stages;        // L ring depth (one 64-id box per stage)
     int l_fp32;          // L element type: 0 bf16, 1 fp32
     int l_rows;          // L rows per M tile in the TMA box (chain: min(R,128); tree: 128/P)
     int P;               // tree: GEMM rows per request (frontier slots)
@@ -66,7 +68,6 @@ struct GemmParams {
     int nb;                     // ceil(V / 16)
     // tree
     const int32_t* front_tok;   // [R][P] frontier tokens (-1: empty slot)
-    float* tree_part;           // [rows][gridDim.x][kColGroups][2 + 2 * kMaxTopK]
     // residual (sample verify): one GEMM row per request
     const int32_t* res_tok;     // [R] previous token of the rejected position, -1: none
     const int32_t* res_pos;     // [R] rejected window position j (L row j, stream row j)
@@ -82,8 +83,8 @@ struct GemmParams {
     int32_t* dev_status;
 };
 
-size_t gemm_smem_bytes(int r, int l_rows, int l_fp32, int stages, int mode);
-int gemm_pick_stages(int r, int l_rows, int l_fp32, int mode);
+// Ring depths for the launch shape (written into p.w_stages / p.l_stages).
+void gemm_pick_stages(GemmParams& p, int mode);
 cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p,
                                int grid_x, int grid_y, cudaStream_t s);
 
@@ -195,15 +196,31 @@ struct ResampleParams {
 };
 cudaError_t launch_resample(const ResampleParams& p, cudaStream_t s);
 
+// PCTree level: per frontier row, log-sum-exp and the top-k children by z.
+struct TreeSelectParams {
+    const float2* blk;       // [rows][nb] records of this level (MODE_TREE)
+    int nb;
+    int rows, P, B, V, r, k, d;
+    const int32_t* front_tok;   // [rows], -1: empty slot
+    const void* L;              // [R, B, V]
+    int l_fp32;
+    const uint16_t* U;
+    const uint16_t* W;
+    float2* row_top;            // [rows][kMaxTopK] (z, id bits) in rank order
+    float* row_lse;             // [rows]
+    int32_t* dev_status;
+};
+cudaError_t launch_tree_select(const TreeSelectParams& p, cudaStream_t s);
+
 // PCTree
 cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
                              float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
                              int32_t* pool_depth, float* pool_score, int32_t* pool_n, int32_t* dev_status,
                              cudaStream_t s);
-cudaError_t launch_tree_merge(const float* tree_part, int gx, int R, int P, int k, int B, int d, int32_t* front_tok,
-                              int32_t* front_node, float* front_score, int32_t* n_front, int32_t* pool_tok,
-                              int32_t* pool_parent, int32_t* pool_depth, float* pool_score, int32_t* pool_n,
-                              cudaStream_t s);
+cudaError_t launch_tree_merge(const float2* row_top, const float* row_lse, int R, int P, int k, int B, int d,
+                              int32_t* front_tok, int32_t* front_node, float* front_score, int32_t* n_front,
+                              int32_t* pool_tok, int32_t* pool_parent, int32_t* pool_depth, float* pool_score,
+                              int32_t* pool_n, cudaStream_t s);
 cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool_tok, const int32_t* pool_parent,
                                  const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
                                  int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,

@@ -9,7 +9,8 @@
 //   MODE_CHAIN_SAMPLE  per 16-column block: max of z / T and the sum of
 //                      exp(z / T - max) (the records an inverse-CDF draw
 //                      walks; the draw itself is select.cu's)
-//   MODE_TREE          log-sum-exp partials + local top-k by z  (PCTree)
+//   MODE_TREE          the same block records of z (PCTree frontier rows;
+//                      the top-k children come from select.cu)
 //   MODE_RESID         per 16-column block: the sum of max(0, p - q) at a
 //                      rejected position
 //   MODE_ABSMAX        max_v |U[m] . W[:, v]| for m = 0..V-1, no L (the
@@ -40,24 +41,34 @@ namespace sdm {
 namespace {
 
 constexpr int kSmemLimit = 232448;   // 227 KB opt-in per block
-// Tensor memory: two 64-column fp32 accumulators, then A (128 rows x r bf16,
-// two per 32-bit column: r / 2 <= 128 columns).
+constexpr uint32_t kWStageBytes = 64u * kTileN * 2u;   // 64 K rows x 128 ids bf16 = two 64 x 64 boxes
+constexpr uint32_t kWBoxBytes = 64u * kBoxN * 2u;      // 8 KB
+constexpr int kMaxWStages = 12;
+constexpr int kMaxLStages = 4;
+// Tensor memory: two 128-column fp32 accumulators, then A (128 rows x r
+// bf16, two per 32-bit column: r / 2 <= 128 columns).
 constexpr int kTmemA = 2 * kTileN;
-constexpr int kTmemCols = 256;
+constexpr int kTmemCols = 512;
 
+// Shared memory: the W ring (stage = K block kb of 64 rows x the tile's two
+// 64-id boxes), then the L ring (stage = one 64-id box of the tile's L rows),
+// then the barriers.  A (128 rows x r, K-major, 128-byte swizzle) is gathered
+// into the last r / 64 W stages and copied to tensor memory before those
+// stages are first loaded.
 struct SmemLayout {
-    uint32_t a_bytes, w_bytes, l_box_bytes, l_bytes, stage_bytes, bar_off, total;
+    uint32_t a_off, l_off, l_box_bytes, l_stage_bytes, bar_off, total;
 };
 
-__host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32, int stages, int mode) {
+__host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32, int w_stages, int l_stages,
+                                                  int mode) {
     SmemLayout s;
-    s.a_bytes = static_cast<uint32_t>(kTileM) * static_cast<uint32_t>(r) * 2u;
-    s.w_bytes = static_cast<uint32_t>(r) * 128u;
+    const uint32_t w_bytes = static_cast<uint32_t>(w_stages) * kWStageBytes;
+    s.a_off = w_bytes - static_cast<uint32_t>(kTileM) * static_cast<uint32_t>(r) * 2u;
+    s.l_off = w_bytes;
     s.l_box_bytes = (static_cast<uint32_t>(l_rows) * 128u + 1023u) & ~1023u;
-    s.l_bytes = mode_reads_l(mode) ? s.l_box_bytes * (l_fp32 ? 2u : 1u) : 0u;
-    s.stage_bytes = s.w_bytes + s.l_bytes;
-    s.bar_off = s.a_bytes + static_cast<uint32_t>(stages) * s.stage_bytes;
-    s.total = s.bar_off + static_cast<uint32_t>(2 * stages + 4) * 8u + 16u + 1024u;
+    s.l_stage_bytes = mode_reads_l(mode) ? s.l_box_bytes * (l_fp32 ? 2u : 1u) : 0u;
+    s.bar_off = s.l_off + static_cast<uint32_t>(l_stages) * s.l_stage_bytes;
+    s.total = s.bar_off + static_cast<uint32_t>(2 * w_stages + 2 * l_stages + 5) * 8u + 16u + 1024u;
     return s;
 }
 
@@ -225,14 +236,20 @@ struct Epi<MODE_CHAIN_GREEDY> {
     }
 };
 
-// Block record (m, s) of the 16 columns: m = max z / T, s = sum exp(z / T - m).
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Block record (m, s) of the 16 columns: m = max z / T, s = sum exp(z / T - m),
+// formed in base 2 (x = z log2(e) / T, s = sum 2^(x - max x)).
 template <>
 struct Epi<MODE_CHAIN_SAMPLE> {
     bool valid;
     int group;
+    float sc;      // log2(e) / T
     float2* rec;   // this row's records [nb]
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.R;
+        sc = p.inv_t * kLog2e;
         rec = p.blk + static_cast<size_t>(valid ? grow : 0) * p.nb;
     }
     __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
@@ -241,98 +258,43 @@ struct Epi<MODE_CHAIN_SAMPLE> {
         float z[C];
         load_l(sl, lbb, p.l_fp32, lrow, g, z);
 #pragma unroll
-        for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * p.inv_t;
+        for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * sc;
         mask_tail(z, vbase, p.V);
         const float m = maxc(z);
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < C; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
-        rec[vbase / C] = make_float2(m, (ps[0] + ps[1]) + (ps[2] + ps[3]));
+        for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(z[j] - m);   // 2^-inf = 0 on the tail
+        rec[vbase / C] = make_float2(m * kLn2, (ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
     __device__ __forceinline__ void flush(const GemmParams&, int) {}
 };
 
+// Block record (m, s) of the 16 columns of a frontier row: m = max z,
+// s = sum exp(z - m) (base 2 inside, as for sampling with T = 1).
 template <>
 struct Epi<MODE_TREE> {
     bool valid;
     int group;
-    float m, s;
-    float thresh;                 // current k-th best z (entry to the top-k)
-    float tv[kMaxTopK];
-    uint32_t ti[kMaxTopK];
+    float2* rec;
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = grow < p.rows && p.front_tok[grow] >= 0;
-        m = -INFINITY;
-        s = 0.f;
-        thresh = -INFINITY;
-#pragma unroll
-        for (int q = 0; q < kMaxTopK; ++q) {
-            tv[q] = -INFINITY;
-            ti[q] = 0xffffffffu;
-        }
+        rec = p.blk + static_cast<size_t>(grow < p.rows ? grow : 0) * p.nb;
     }
     __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
                                             int g, const uint32_t (&acc)[C]) {
-        if (!valid) return;
+        if (!valid || vbase >= p.V) return;
         float z[C];
         load_l(sl, lbb, p.l_fp32, lrow / p.P, g, z);
 #pragma unroll
-        for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);
+        for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * kLog2e;
         mask_tail(z, vbase, p.V);
-        const float mx = maxc(z);
-        if (mx > m) {
-            s *= __expf(m - mx);
-            m = mx;
-        }
+        const float m = maxc(z);
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int j = 0; j < C; ++j) ps[j & 3] += __expf(z[j] - m);   // exp(-inf) = 0 on the tail
-        s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-        // A sorted top-k (value desc, lower id first; k <= 8 slots in use).
-        // Only the columns above the current k-th best are inserted, one set
-        // bit at a time (rare once the list has filled).
-        if (mx > thresh) {
-            uint32_t cm = 0u;
-#pragma unroll
-            for (int j = 0; j < C; ++j) cm |= (z[j] > thresh ? 1u : 0u) << j;
-            while (cm) {
-                const int j = __ffs(cm) - 1;   // ascending ids: earlier ties stay ahead
-                cm &= cm - 1u;
-                float cz = z[0];
-#pragma unroll
-                for (int jj = 1; jj < C; ++jj)
-                    if (jj == j) cz = z[jj];
-                if (!(cz > thresh)) continue;
-                uint32_t cv = static_cast<uint32_t>(vbase + j);
-#pragma unroll
-                for (int q = 0; q < kMaxTopK; ++q) {
-                    if (q < p.k && cz > tv[q]) {   // strict: earlier (lower id) ties stay ahead
-                        const float tz = tv[q];
-                        const uint32_t tiv = ti[q];
-                        tv[q] = cz;
-                        ti[q] = cv;
-                        cz = tz;
-                        cv = tiv;
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < kMaxTopK; ++q)
-                    if (q == p.k - 1) thresh = tv[q];
-            }
-        }
+        for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(z[j] - m);
+        rec[vbase / C] = make_float2(m * kLn2, (ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
-    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
-        if (!valid) return;
-        float* rec = p.tree_part +
-                     ((static_cast<size_t>(grow) * gridDim.x + blockIdx.x) * kColGroups + group) * (2 + 2 * kMaxTopK);
-        rec[0] = m;
-        rec[1] = s;
-#pragma unroll
-        for (int q = 0; q < kMaxTopK; ++q) {
-            rec[2 + q] = tv[q];
-            rec[2 + kMaxTopK + q] = __uint_as_float(ti[q]);
-        }
-    }
+    __device__ __forceinline__ void flush(const GemmParams&, int) {}
 };
 
 // Block record (0, s) of the 16 columns: s = sum max(0, p_v - q_v) with
@@ -409,32 +371,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                        const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.stages, MODE);
-    uint8_t* sA = smem;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
-    uint64_t* empty = full + p.stages;
-    uint64_t* tfull = empty + p.stages;
+    const int SW = p.w_stages, SL = p.l_stages;
+    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, SW, SL, MODE);
+    uint8_t* sA = smem + lay.a_off;
+    uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
+    uint64_t* wempty = wfull + SW;
+    uint64_t* lfull = wempty + SW;
+    uint64_t* lempty = lfull + SL;
+    uint64_t* tfull = lempty + SL;
     uint64_t* tempty = tfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+    uint64_t* a_done = tempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_done + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row0 = blockIdx.y * kTileM;
+    const int KB = p.r >> 6;   // K blocks of 64 per tile
     // vocab tiles are dealt round-robin (tile = blockIdx.x + i * gridDim.x) so
-    // that concurrently running CTAs read neighbouring 128-byte segments of
-    // every W and L row
+    // that concurrently running CTAs read neighbouring segments of every W and
+    // L row
     const int nt = (p.n_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
 
     // set-up that reads nothing the previous kernel in the stream writes
     if (threadIdx.x == 0) {
-        for (int s = 0; s < p.stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + kEpiWarps);
+        for (int s = 0; s < SW; ++s) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], 1);
+        }
+        for (int s = 0; s < SL; ++s) {
+            mbar_init(&lfull[s], 1);
+            mbar_init(&lempty[s], kEpiWarps);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], kEpiWarps);
         }
+        mbar_init(a_done, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -467,108 +439,162 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
-        // 2. producer: W tile + L tile per vocab tile
+        // 2a. W producer: per tile, KB stages of [64 K rows x 128 ids] (two
+        //     64 x 64 boxes); a stage is free again once its MMAs complete.
+        //     Stages at or above a_first hold A until it is in tensor memory.
         if (lane == 0 && nt > 0) {
             const uint64_t pol_w = policy_evict_last();
-            const uint64_t pol_l = policy_evict_first();
-            const uint32_t tx =
-                lay.w_bytes + (mode_reads_l(MODE) ? static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u) : 0u);
-            const int lrow0 = (MODE == MODE_TREE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
+            const int a_first = SW - KB;
+            bool a_free = false;
+            int s = 0, lap = 0;   // ring slot and how many times the ring has wrapped
             for (int i = 0; i < nt; ++i) {
-                const int s = i % p.stages;
-                if (i >= p.stages && !mbar_wait(&empty[s], ((i / p.stages) - 1) & 1)) {
+                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+                bool ok = true;
+                for (int kb = 0; kb < KB && ok; ++kb, s = (s + 1 == SW) ? (++lap, 0) : s + 1) {
+                    if (lap > 0) {
+                        ok = mbar_wait(&wempty[s], (lap - 1) & 1);
+                    } else if (s >= a_first && !a_free) {
+                        ok = mbar_wait(a_done, 0);
+                        a_free = true;
+                    }
+                    if (!ok) break;
+                    uint8_t* st = smem + static_cast<uint32_t>(s) * kWStageBytes;
+                    mbar_arrive_expect_tx(&wfull[s], kWStageBytes);
+                    tma_load_2d(st, &tmW, &wfull[s], v0, kb * 64, pol_w);
+                    tma_load_2d(st + kWBoxBytes, &tmW, &wfull[s], v0 + kBoxN, kb * 64, pol_w);
+                }
+                if (!ok) {
                     fail_timeout(p);
                     break;
-                }
-                uint8_t* st = smem + lay.a_bytes + s * lay.stage_bytes;
-                mbar_arrive_expect_tx(&full[s], tx);
-                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
-                tma_load_2d(st, &tmW, &full[s], v0, 0, pol_w);
-                if (mode_reads_l(MODE)) {
-                    uint8_t* sl = st + lay.w_bytes;
-                    tma_load_3d(sl, &tmL, &full[s], v0, p.d - 1, lrow0, pol_l);
-                    if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &full[s], v0 + 32, p.d - 1, lrow0, pol_l);
                 }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // 3. MMA issuer: D[128 x 64] = A[128 x r] * W_tile[r x 64]
+        // 3. MMA issuer: A into tensor memory once, then per tile
+        //    D[128 x 128] = sum over K blocks of A_kb * W_kb, four K = 16
+        //    steps per stage, N = 128 per instruction
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
             // Descriptors are formed once and advanced by adding the k-step's
             // offset to their 14-bit start-address field (address >> 4; every
             // shared address here is below 256 KB, so the field cannot carry):
             // A steps 32 bytes within a 128-byte swizzle row and 128 x 128
-            // bytes per K block of 64; B steps 16 rows of 128 bytes.
+            // bytes per K block of 64; B steps 16 rows of 128 bytes, and its
+            // second 64-id box (the MN-atom stride) is kWBoxBytes further.
             const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
             const int ksteps = p.r >> 4;
-            // A into tensor memory once: every MMA then reads only its B tile
-            // from shared memory
             const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA);
             for (int ks = 0; ks < ksteps; ++ks)
                 tmem_cp_128x256b(a_tmem + static_cast<uint32_t>(ks * 8),
                                  a_desc0 + static_cast<uint64_t>((ks >> 2) * ((kTileM * 128) >> 4) + (ks & 3) * 2));
-            for (int i = 0; i < nt; ++i) {
-                const int s = i % p.stages;
+            mma_commit(a_done);   // the A stages may be loaded once the copy has read them
+            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem), kWBoxBytes, 1024);
+            bool ok = true;
+            int s = 0, lap = 0;
+            for (int i = 0; i < nt && ok; ++i) {
                 const int b = i & 1;
-                if (!mbar_wait(&full[s], (i / p.stages) & 1)) {
-                    fail_timeout(p);
-                    break;
-                }
                 if (i >= 2 && !mbar_wait(&tempty[b], ((i >> 1) - 1) & 1)) {
-                    fail_timeout(p);
+                    ok = false;
                     break;
                 }
                 tc_fence_after();
-                // N = 64 is one swizzle span, so the MN-atom offset is never
-                // applied; it is set equal to the K-group stride (1024 B).
-                const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + lay.a_bytes + s * lay.stage_bytes), 1024, 1024);
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
-#pragma unroll 4
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    const uint64_t bd = b_desc0 + static_cast<uint64_t>(ks * (2048 >> 4));
-                    mma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>(ks * 8), bd, idesc, ks > 0 ? 1u : 0u);
+                for (int kb = 0; kb < KB; ++kb, s = (s + 1 == SW) ? (++lap, 0) : s + 1) {
+                    if (!mbar_wait(&wfull[s], lap & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        mma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>((kb * 4 + j) * 8),
+                                    bd0 + static_cast<uint64_t>(j * (2048 >> 4)), idesc, (kb | j) ? 1u : 0u);
+                    mma_commit(&wempty[s]);
                 }
-                mma_commit(&empty[s]);
-                mma_commit(&tfull[b]);
+                if (ok) mma_commit(&tfull[b]);
             }
+            if (!ok) fail_timeout(p);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // 2b. L producer: the tile's two 64-id boxes of L rows, one stage each
+        if (mode_reads_l(MODE) && lane == 0 && nt > 0) {
+            const uint64_t pol_l = policy_evict_first();
+            const int lrow0 = (MODE == MODE_TREE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
+            bool ok = true;
+            int t = 0, lap = 0;
+            for (int i = 0; i < nt && ok; ++i) {
+                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+                for (int h = 0; h < 2; ++h, t = (t + 1 == SL) ? (++lap, 0) : t + 1) {
+                    if (lap > 0 && !mbar_wait(&lempty[t], (lap - 1) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(t) * lay.l_stage_bytes;
+                    mbar_arrive_expect_tx(&lfull[t], static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u));
+                    const int vb = v0 + h * kBoxN;
+                    tma_load_3d(sl, &tmL, &lfull[t], vb, p.d - 1, lrow0, pol_l);
+                    if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &lfull[t], vb + 32, p.d - 1, lrow0, pol_l);
+                }
+            }
+            if (!ok) fail_timeout(p);
         }
         __syncwarp();
     } else {
         // 4. epilogue: thread = GEMM row (TMEM lane of its sub-partition
-        //    warp % 4); column group g = (warp - 2) / 4 takes columns
-        //    [16 g, 16 g + 16) of every tile
+        //    warp % 4); column group g = (warp - 3) / 4 takes columns
+        //    [16 g, 16 g + 16) of both 64-id boxes of every tile
         const int q = warp & 3;
-        const int g = (warp - 2) >> 2;
+        const int g = (warp - 3) >> 2;
         const int lrow = q * 32 + lane;
         const int grow = row0 + lrow;
         Epi<MODE> st;
         st.init(p, grow);
         st.group = g;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+        int t = 0, lap = 0;   // L ring slot and wraps
         for (int i = 0; i < nt; ++i) {
-            const int s = i % p.stages;
             const int b = i & 1;
             bool ok = mbar_wait(&tfull[b], (i >> 1) & 1);
-            if (ok) ok = mbar_wait(&full[s], (i / p.stages) & 1);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) fail_timeout(p);
                 break;
             }
             tc_fence_after();
-            const uint8_t* sl = smem + lay.a_bytes + s * lay.stage_bytes + lay.w_bytes;
-            const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
-            uint32_t acc[C];
-            tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + g * C), acc);
+            // both 16-column slices of the tile into registers, then the
+            // accumulator goes back to the MMA warp before any arithmetic
+            uint32_t acc[2][C];
+            tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + g * C), acc[0]);
+            tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + kBoxN + g * C), acc[1]);
             tmem_ld_wait();
-            st.consume(p, sl, lay.l_box_bytes, lrow, v0 + g * C, g, acc);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&tempty[b]);
-                mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&tempty[b]);
+            const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                if (mode_reads_l(MODE)) {
+                    bool lok = mbar_wait(&lfull[t], lap & 1);
+                    lok = __all_sync(0xffffffffu, lok);
+                    if (!lok) {
+                        ok = false;
+                        break;
+                    }
+                }
+                const uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(t) * lay.l_stage_bytes;
+                st.consume(p, sl, lay.l_box_bytes, lrow, v0 + h * kBoxN + g * C, g, acc[h]);
+                if (mode_reads_l(MODE)) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&lempty[t]);
+                    t = (t + 1 == SL) ? (++lap, 0) : t + 1;
+                }
+            }
+            if (!ok) {
+                if (lane == 0) fail_timeout(p);
+                break;
             }
         }
         st.flush(p, grow);
@@ -585,7 +611,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p, int gx, int gy,
                         cudaStream_t s) {
-    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.stages, MODE);
+    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.w_stages, p.l_stages, MODE);
+    if (lay.total > static_cast<uint32_t>(kSmemLimit) || p.w_stages < (p.r >> 6) + 1) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -598,14 +625,16 @@ cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const Ge
 
 }  // namespace
 
-size_t gemm_smem_bytes(int r, int l_rows, int l_fp32, int stages, int mode) {
-    return make_layout(r, l_rows, l_fp32, stages, mode).total;
-}
-
-int gemm_pick_stages(int r, int l_rows, int l_fp32, int mode) {
-    int st = 4;
-    while (st > 1 && make_layout(r, l_rows, l_fp32, st, mode).total > static_cast<uint32_t>(kSmemLimit)) --st;
-    return st;
+void gemm_pick_stages(GemmParams& p, int mode) {
+    // L: two tiles ahead (one for fp32 boxes of 32 KB), W: the rest, at most 12
+    const SmemLayout one = make_layout(p.r, p.l_rows, p.l_fp32, 0, 1, mode);
+    const int l_stages = !mode_reads_l(mode) ? 0 : (one.l_stage_bytes > 16384u ? 3 : kMaxLStages);
+    int w_stages = kMaxWStages;
+    while (w_stages > 1 &&
+           make_layout(p.r, p.l_rows, p.l_fp32, w_stages, l_stages, mode).total > static_cast<uint32_t>(kSmemLimit))
+        --w_stages;
+    p.w_stages = w_stages;
+    p.l_stages = l_stages;
 }
 
 cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p,

@@ -510,11 +510,10 @@ __device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
     return a.rank < b.rank;
 }
 
-// One CTA per request, one warp per frontier slot.  Each lane merges its
-// share of the vocab-split records (log-sum-exp and a sorted top-k); the warp
-// then takes its top-k in k rounds of a warp argmax over the lanes' heads;
-// finally the nf * k children are ranked in parallel and the best P kept.
-__global__ void tree_merge_kernel(const float* tree_part, int gx, int R, int P, int k, int B, int d,
+// One CTA per request: the children of every frontier slot (its top-k by z,
+// from the level's select kernel) get s(c) = s(p) + z - lse; they are ranked
+// in parallel and the best P kept.
+__global__ void tree_merge_kernel(const float2* row_top, const float* row_lse, int R, int P, int k, int B, int d,
                                   int32_t* front_tok, int32_t* front_node, float* front_score, int32_t* n_front,
                                   int32_t* pool_tok, int32_t* pool_parent, int32_t* pool_depth, float* pool_score,
                                   int32_t* pool_n) {
@@ -522,69 +521,17 @@ __global__ void tree_merge_kernel(const float* tree_part, int gx, int R, int P, 
     Cand* cand = reinterpret_cast<Cand*>(tm_smem);                   // [P * k] children
     Cand* sorted = cand + P * k;                                     // [P * k] in rank order
     int* parent_node = reinterpret_cast<int*>(sorted + P * k);       // [P]
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nf = n_front[i];
-    constexpr int REC = 2 + 2 * kMaxTopK;
-    if (warp < P) parent_node[warp] = front_node[static_cast<size_t>(i) * P + warp];
-    if (warp < nf) {
-        const int grow = i * P + warp;
-        Lse acc{-INFINITY, 0.f};
-        float tz[kMaxTopK];
-        uint32_t ti[kMaxTopK];
-#pragma unroll
-        for (int q = 0; q < kMaxTopK; ++q) {
-            tz[q] = -INFINITY;
-            ti[q] = 0xffffffffu;
-        }
-        for (int c = lane; c < gx; c += 32) {
-            const float* rec = tree_part + (static_cast<size_t>(grow) * gx + c) * REC;
-            float rz[kMaxTopK];
-            uint32_t rv[kMaxTopK];
-#pragma unroll
-            for (int q = 0; q < kMaxTopK; ++q) {   // loads first
-                rz[q] = q < k ? rec[2 + q] : -INFINITY;
-                rv[q] = q < k ? __float_as_uint(rec[2 + kMaxTopK + q]) : 0xffffffffu;
-            }
-            acc = lse_merge(acc, Lse{rec[0], rec[1]});
-#pragma unroll
-            for (int q = 0; q < kMaxTopK; ++q) {
-                if (q >= k) break;
-                float cz = rz[q];
-                uint32_t cv = rv[q];
-#pragma unroll
-                for (int e = 0; e < kMaxTopK; ++e) {
-                    if (e < k && (cz > tz[e] || (cz == tz[e] && cv < ti[e]))) {
-                        const float oz = tz[e];
-                        const uint32_t ov = ti[e];
-                        tz[e] = cz;
-                        ti[e] = cv;
-                        cz = oz;
-                        cv = ov;
-                    }
-                }
-            }
-        }
-        acc = warp_lse(acc);
-        const float lse = acc.m + logf(acc.s);
-        const float sp = front_score[static_cast<size_t>(i) * P + warp];
-        // k rounds: the best head over the lanes is popped by its lane (ids
-        // are distinct across lanes, so exactly one lane matches)
-        for (int q = 0; q < k; ++q) {
-            const unsigned long long mine = argmax_key(tz[0], ti[0]);
-            const unsigned long long best = warp_max_u64(mine);
-            if (mine == best) {
-#pragma unroll
-                for (int e = 0; e + 1 < kMaxTopK; ++e) {
-                    tz[e] = tz[e + 1];
-                    ti[e] = ti[e + 1];
-                }
-                tz[kMaxTopK - 1] = -INFINITY;
-                ti[kMaxTopK - 1] = 0xffffffffu;
-            }
-            if (lane == 0)   // s(c) = s(p) + log pi(v | p)
-                cand[warp * k + q] = Cand{sp + (key_value(best) - lse), warp, q, static_cast<int>(key_token(best))};
-        }
+    for (int f = threadIdx.x; f < P; f += blockDim.x) parent_node[f] = front_node[static_cast<size_t>(i) * P + f];
+    for (int t = threadIdx.x; t < nf * k; t += blockDim.x) {
+        const int f = t / k, q = t % k;
+        const size_t grow = static_cast<size_t>(i) * P + f;
+        const float2 e = row_top[grow * kMaxTopK + q];
+        // s(c) = s(p) + log pi(v | p)
+        cand[t] = Cand{front_score[grow] + (e.x - row_lse[grow]), f, q, __float_as_int(e.y)};
     }
     __syncthreads();
     // rank of every child by (s desc, slot asc, rank asc): a strict total order
@@ -835,14 +782,13 @@ cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_tree_merge(const float* tree_part, int gx, int R, int P, int k, int B, int d, int32_t* front_tok,
-                              int32_t* front_node, float* front_score, int32_t* n_front, int32_t* pool_tok,
-                              int32_t* pool_parent, int32_t* pool_depth, float* pool_score, int32_t* pool_n,
-                              cudaStream_t s) {
+cudaError_t launch_tree_merge(const float2* row_top, const float* row_lse, int R, int P, int k, int B, int d,
+                              int32_t* front_tok, int32_t* front_node, float* front_score, int32_t* n_front,
+                              int32_t* pool_tok, int32_t* pool_parent, int32_t* pool_depth, float* pool_score,
+                              int32_t* pool_n, cudaStream_t s) {
     const size_t smem = 2 * static_cast<size_t>(P) * k * sizeof(Cand) + static_cast<size_t>(P) * 4;
-    tree_merge_kernel<<<R, P * 32, smem, s>>>(tree_part, gx, R, P, k, B, d, front_tok, front_node, front_score,
-                                              n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n);
-    return cudaGetLastError();
+    return launch_pdl(tree_merge_kernel, dim3(R), dim3(128), smem, s, row_top, row_lse, R, P, k, B, d, front_tok,
+                      front_node, front_score, n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n);
 }
 
 cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool_tok, const int32_t* pool_parent,
