@@ -44,7 +44,7 @@ constexpr int kSmemLimit = 232448;   // 227 KB opt-in per block
 constexpr uint32_t kWStageBytes = 64u * kTileN * 2u;   // 64 K rows x 128 ids bf16 = two 64 x 64 boxes
 constexpr uint32_t kWBoxBytes = 64u * kBoxN * 2u;      // 8 KB
 constexpr int kMaxWStages = 12;
-constexpr int kMaxLStages = 4;
+constexpr int kMaxLStages = 6;
 // Tensor memory: two 128-column fp32 accumulators, then A (128 rows x r
 // bf16, two per 32-bit column: r / 2 <= 128 columns).
 constexpr int kTmemA = 2 * kTileN;
@@ -63,7 +63,9 @@ __host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32,
                                                   int mode) {
     SmemLayout s;
     const uint32_t w_bytes = static_cast<uint32_t>(w_stages) * kWStageBytes;
-    s.a_off = w_bytes - static_cast<uint32_t>(kTileM) * static_cast<uint32_t>(r) * 2u;
+    // A fills the last tile slot (KB = r / 64 stages of 16 KB = 128 x r x 2 bytes)
+    const int kb = r >> 6;
+    s.a_off = static_cast<uint32_t>((w_stages / kb - 1) * kb) * kWStageBytes;
     s.l_off = w_bytes;
     s.l_box_bytes = (static_cast<uint32_t>(l_rows) * 128u + 1023u) & ~1023u;
     s.l_stage_bytes = mode_reads_l(mode) ? s.l_box_bytes * (l_fp32 ? 2u : 1u) : 0u;
@@ -375,8 +377,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, SW, SL, MODE);
     uint8_t* sA = smem + lay.a_off;
     uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
-    uint64_t* wempty = wfull + SW;
-    uint64_t* lfull = wempty + SW;
+    uint64_t* wdone = wfull + SW;   // per tile slot: the slot's last tile has completed
+    uint64_t* lfull = wdone + SW;
     uint64_t* lempty = lfull + SL;
     uint64_t* tfull = lempty + SL;
     uint64_t* tempty = tfull + 2;
@@ -387,6 +389,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int lane = threadIdx.x & 31;
     const int row0 = blockIdx.y * kTileM;
     const int KB = p.r >> 6;   // K blocks of 64 per tile
+    const int NTS = SW / KB;   // W tile slots: tile i takes stages (i % NTS) * KB .. + KB - 1
     // vocab tiles are dealt round-robin (tile = blockIdx.x + i * gridDim.x) so
     // that concurrently running CTAs read neighbouring segments of every W and
     // L row
@@ -396,7 +399,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < SW; ++s) {
             mbar_init(&wfull[s], 1);
-            mbar_init(&wempty[s], 1);
+            mbar_init(&wdone[s], 1);
         }
         for (int s = 0; s < SL; ++s) {
             mbar_init(&lfull[s], 1);
@@ -440,83 +443,76 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (warp == 0) {
         // 2a. W producer: per tile, KB stages of [64 K rows x 128 ids] (two
-        //     64 x 64 boxes); a stage is free again once its MMAs complete.
-        //     Stages at or above a_first hold A until it is in tensor memory.
+        //     64 x 64 boxes) in the tile's slot.  A slot is free again once
+        //     its last tile's MMAs have completed: the first epilogue warp
+        //     arrives on wdone[slot] when it sees that tile's accumulator
+        //     full, so the MMA warp commits once per tile (a commit waits for
+        //     the MMA pipe to drain; one per stage would cost KB drains per
+        //     tile).  The last slot holds A until it is in tensor memory.
         if (lane == 0 && nt > 0) {
             const uint64_t pol_w = policy_evict_last();
-            const int a_first = SW - KB;
-            bool a_free = false;
-            int s = 0, lap = 0;   // ring slot and how many times the ring has wrapped
-            for (int i = 0; i < nt; ++i) {
+            bool ok = true;
+            for (int i = 0; i < nt && ok; ++i) {
+                const int slot = i % NTS;
+                if (i >= NTS) ok = mbar_wait(&wdone[slot], ((i / NTS) - 1) & 1);
+                else if (slot == NTS - 1) ok = mbar_wait(a_done, 0);
+                if (!ok) break;
                 const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
-                bool ok = true;
-                for (int kb = 0; kb < KB && ok; ++kb, s = (s + 1 == SW) ? (++lap, 0) : s + 1) {
-                    if (lap > 0) {
-                        ok = mbar_wait(&wempty[s], (lap - 1) & 1);
-                    } else if (s >= a_first && !a_free) {
-                        ok = mbar_wait(a_done, 0);
-                        a_free = true;
-                    }
-                    if (!ok) break;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int s = slot * KB + kb;
                     uint8_t* st = smem + static_cast<uint32_t>(s) * kWStageBytes;
                     mbar_arrive_expect_tx(&wfull[s], kWStageBytes);
                     tma_load_2d(st, &tmW, &wfull[s], v0, kb * 64, pol_w);
                     tma_load_2d(st + kWBoxBytes, &tmW, &wfull[s], v0 + kBoxN, kb * 64, pol_w);
                 }
-                if (!ok) {
-                    fail_timeout(p);
-                    break;
-                }
             }
+            if (!ok) fail_timeout(p);
         }
         __syncwarp();
     } else if (warp == 1) {
         // 3. MMA issuer: A into tensor memory once, then per tile
         //    D[128 x 128] = sum over K blocks of A_kb * W_kb, four K = 16
-        //    steps per stage, N = 128 per instruction
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
-            // Descriptors are formed once and advanced by adding the k-step's
-            // offset to their 14-bit start-address field (address >> 4; every
-            // shared address here is below 256 KB, so the field cannot carry):
-            // A steps 32 bytes within a 128-byte swizzle row and 128 x 128
-            // bytes per K block of 64; B steps 16 rows of 128 bytes, and its
-            // second 64-id box (the MN-atom stride) is kWBoxBytes further.
-            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
-            const int ksteps = p.r >> 4;
-            const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA);
-            for (int ks = 0; ks < ksteps; ++ks)
-                tmem_cp_128x256b(a_tmem + static_cast<uint32_t>(ks * 8),
-                                 a_desc0 + static_cast<uint64_t>((ks >> 2) * ((kTileM * 128) >> 4) + (ks & 3) * 2));
-            mma_commit(a_done);   // the A stages may be loaded once the copy has read them
-            const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem), kWBoxBytes, 1024);
-            bool ok = true;
-            int s = 0, lap = 0;
-            for (int i = 0; i < nt && ok; ++i) {
-                const int b = i & 1;
-                if (i >= 2 && !mbar_wait(&tempty[b], ((i >> 1) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
+        //    steps per stage, N = 128 per instruction.  The whole warp runs
+        //    the loop and waits; each tcgen05 instruction is issued by the
+        //    lane elect.sync picks.
+        const uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, true);
+        // Descriptors are formed once and advanced by adding the k-step's
+        // offset to their 14-bit start-address field (address >> 4; every
+        // shared address here is below 256 KB, so the field cannot carry):
+        // A steps 32 bytes within a 128-byte swizzle row and 128 x 128
+        // bytes per K block of 64; B steps 16 rows of 128 bytes, and its
+        // second 64-id box (the MN-atom stride) is kWBoxBytes further.
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
+        const int ksteps = p.r >> 4;
+        const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA);
+        for (int ks = 0; ks < ksteps; ++ks)
+            tmem_cp_128x256b_warp(a_tmem + static_cast<uint32_t>(ks * 8),
+                                  a_desc0 + static_cast<uint64_t>((ks >> 2) * ((kTileM * 128) >> 4) + (ks & 3) * 2));
+        mma_commit_warp(a_done);   // the A stages may be loaded once the copy has read them
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem), kWBoxBytes, 1024);
+        bool ok = true;
+        for (int i = 0; i < nt && ok; ++i) {
+            const int b = i & 1;
+            if (i >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[b], ((i >> 1) - 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
+            const int slot = i % NTS;
+            const uint32_t par = static_cast<uint32_t>(i / NTS) & 1u;
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = slot * KB + kb;
+                ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par));
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
-                for (int kb = 0; kb < KB; ++kb, s = (s + 1 == SW) ? (++lap, 0) : s + 1) {
-                    if (!mbar_wait(&wfull[s], lap & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
+                const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        mma_bf16_ts(d_tmem, a_tmem + static_cast<uint32_t>((kb * 4 + j) * 8),
-                                    bd0 + static_cast<uint64_t>(j * (2048 >> 4)), idesc, (kb | j) ? 1u : 0u);
-                    mma_commit(&wempty[s]);
-                }
-                if (ok) mma_commit(&tfull[b]);
+                for (int j = 0; j < 4; ++j)
+                    mma_bf16_ts_warp(d_tmem, a_tmem + static_cast<uint32_t>((kb * 4 + j) * 8),
+                                     bd0 + static_cast<uint64_t>(j * (2048 >> 4)), idesc, (kb | j) ? 1u : 0u);
             }
-            if (!ok) fail_timeout(p);
+            if (ok) mma_commit_warp(&tfull[b]);
         }
+        if (!ok && lane == 0) fail_timeout(p);
         __syncwarp();
     } else if (warp == 2) {
         // 2b. L producer: the tile's two 64-id boxes of L rows, one stage each
@@ -563,6 +559,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 if (lane == 0) fail_timeout(p);
                 break;
             }
+            if (warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);   // the tile's W stages are free
             tc_fence_after();
             // both 16-column slices of the tile into registers, then the
             // accumulator goes back to the MMA warp before any arithmetic
@@ -612,7 +609,7 @@ template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p, int gx, int gy,
                         cudaStream_t s) {
     const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.w_stages, p.l_stages, MODE);
-    if (lay.total > static_cast<uint32_t>(kSmemLimit) || p.w_stages < (p.r >> 6) + 1) return cudaErrorInvalidValue;
+    if (lay.total > static_cast<uint32_t>(kSmemLimit) || p.w_stages < 2 * (p.r >> 6)) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -626,15 +623,20 @@ cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const Ge
 }  // namespace
 
 void gemm_pick_stages(GemmParams& p, int mode) {
-    // L: two tiles ahead (one for fp32 boxes of 32 KB), W: the rest, at most 12
-    const SmemLayout one = make_layout(p.r, p.l_rows, p.l_fp32, 0, 1, mode);
-    const int l_stages = !mode_reads_l(mode) ? 0 : (one.l_stage_bytes > 16384u ? 3 : kMaxLStages);
-    int w_stages = kMaxWStages;
-    while (w_stages > 1 &&
-           make_layout(p.r, p.l_rows, p.l_fp32, w_stages, l_stages, mode).total > static_cast<uint32_t>(kSmemLimit))
-        --w_stages;
-    p.w_stages = w_stages;
-    p.l_stages = l_stages;
+    // W in whole tile slots (r / 64 stages each), at least two; then as many
+    // L boxes as fit up to kMaxLStages (three tiles ahead: L comes from HBM
+    // in scattered rows); then more W slots with what is left.
+    const int kb = p.r >> 6;
+    const auto fits = [&](int ws, int ls) {
+        return make_layout(p.r, p.l_rows, p.l_fp32, ws, ls, mode).total <= static_cast<uint32_t>(kSmemLimit);
+    };
+    int ws = 2 * kb, ls = 0;
+    if (mode_reads_l(mode))
+        for (ls = kMaxLStages; ls > 2 && !fits(ws, ls); --ls) {
+        }
+    while (ws + kb <= kMaxWStages && fits(ws + kb, ls)) ws += kb;
+    p.w_stages = ws;
+    p.l_stages = ls;
 }
 
 cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p,
