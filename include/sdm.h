@@ -141,7 +141,8 @@ sdm_status sdm_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r
  * argmax (greedy) or per-16-column (max, sum of exp) records (sampling) are
  * fused into its epilogue; z is never written to memory.  A sampled step
  * then walks the records of each request to the block holding u S and
- * recomputes that block's 16 logits to find the id.
+ * recomputes that block's 16 logits to find the id (V <= 524288, else
+ * SDM_ERR_UNSUPPORTED).
  * Greedy with prepared tables: since |U[y] . W[:, v]| <= c(y) for every v,
  * only ids with L[v] >= max L - 2 c(y) can win.  One HBM-bound pass over all
  * of L lists those ids for every (request, step) with the worst case c_max,
@@ -244,7 +245,8 @@ sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const in
  *           (stream 3).  Every draw is the inverse CDF in vocabulary order
  *           with one uniform (word 0 of the Philox block of its stream and
  *           row; the row of a draft is d, of an accept test, residual or
- *           bonus the window position).
+ *           bonus the window position).  Sampling needs V <= 524288 (else
+ *           SDM_ERR_UNSUPPORTED).
  *   modes: STATIC (w_i = gamma, commit A), COMPACT (w_i = budget, commit A),
  *          CAP_ACCEPT (w_i = gamma verified, commit a = min(A, budget[i]):
  *          the same output as compact; ceiling = A).

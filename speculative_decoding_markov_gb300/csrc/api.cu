@@ -15,7 +15,7 @@ using namespace sdm;
 constexpr int kMaxGx = 256;           // upper bound of vocab splits per GEMM launch
 constexpr int kChunkBf16 = 16384;     // ids per streaming work item (32 KB)
 constexpr int kChunkFp32 = 8192;
-
+constexpr int kMaxSampleV = 524288;   // 32768 records of 16 ids: the select kernels' chunk tables
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Carver {
@@ -211,6 +211,7 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
     if (decode != SDM_GREEDY && decode != SDM_SAMPLE) return SDM_ERR_INVALID_ARG;
     if (decode == SDM_SAMPLE && !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
     if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
+    if (decode == SDM_SAMPLE && V > kMaxSampleV) return SDM_ERR_UNSUPPORTED;   // the draw's chunk table
     if (!ws || ws_bytes < ws_chain(R, B, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (decode == SDM_GREEDY && prepared) {
@@ -333,7 +334,7 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
     if (k > kMaxTopK || k > V || P * k > 64 || kTileM % P != 0 || N > P * B) return SDM_ERR_UNSUPPORTED;
     if (static_cast<long long>(P) * B + 1 > 8192) return SDM_ERR_UNSUPPORTED;   // the pool is ranked in shared memory
-    if (V > 16 * 32768) return SDM_ERR_UNSUPPORTED;   // the per-row candidate list of the level select
+    if (V > kMaxSampleV) return SDM_ERR_UNSUPPORTED;   // the per-row chunk and candidate tables of the level select
     if (!ws || ws_bytes < ws_tree(R, B, P, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t rows = static_cast<size_t>(R) * P;
@@ -458,6 +459,7 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
         if (!logq || !lse_q || !L || !U || !W || !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
         if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
         if (!rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
+        if (V > kMaxSampleV) return SDM_ERR_UNSUPPORTED;
     }
     if (!ws || ws_bytes < ws_verify(R, row_capacity, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

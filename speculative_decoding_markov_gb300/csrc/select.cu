@@ -38,7 +38,9 @@ constexpr uint32_t kBulkChunk = 32768;    // bytes per bulk copy instruction
 constexpr int kMaxChunks = 1024;          // chunk sums of the walk kept in shared memory
 
 struct SelShared {
-    float csum[kMaxChunks];
+    float csum[kMaxChunks];   // chunk sums of block_walk; chunk sums of the record walk
+    float cmax[kMaxChunks];   // chunk maxima of the record walk
+    float wmx[kSelWarps];
     float wsum[kSelWarps];
     float wmax[kSelWarps];
     uint64_t bar;
@@ -194,24 +196,107 @@ __device__ float block_walk(int n, float f, WFn wfn, SelShared& sh) {
     return S;
 }
 
-// Block-wide maximum of the records' m over n records (warp ranges, 32 at a time).
-__device__ __forceinline__ float records_max(const float2* rec, int n, SelShared& sh) {
-    int lo, hi;
-    warp_range(n, &lo, &hi);
-    float m = -INFINITY;
-#pragma unroll 8
-    for (int b = lo + (threadIdx.x & 31); b < hi; b += 32) {
-        const float2 r = rec[b];
-        if (r.y > 0.f) m = fmaxf(m, r.x);
+// The (max, sum) pair of the 32 records of chunk c (records past n count as
+// empty): sixteen 16-byte loads, issued in a lane-rotated order so that the
+// lanes of a warp, which read sixteen different chunks, spread over the banks.
+// rec is 16-byte aligned and holds at least n rounded up to even records.
+__device__ __forceinline__ void chunk_pair(const float2* rec, int n, int c, float* cm, float* cs) {
+    const int lane = threadIdx.x & 31;
+    const float4* q = reinterpret_cast<const float4*>(rec + c * 32);
+    float4 v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int jj = (j + lane) & 15;
+        v[j] = (c * 32 + 2 * jj < n) ? q[jj] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        if (c * 32 + 2 * jj + 1 >= n) v[j].w = 0.f;   // odd n: the second record of the last pair is padding
     }
-    return block_max(m, sh);
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (v[j].y > 0.f) m = fmaxf(m, v[j].x);
+        if (v[j].w > 0.f) m = fmaxf(m, v[j].z);
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if (v[j].y > 0.f) s += v[j].y * __expf(v[j].x - m);
+        if (v[j].w > 0.f) s += v[j].w * __expf(v[j].z - m);
+    }
+    *cm = m;
+    *cs = s;
 }
 
-// Levels 1 and 2 over n (m, s) records; returns S, *M_out = the scale M.
-__device__ __forceinline__ float walk_records(const float2* rec, int n, float u, SelShared& sh, float* M_out) {
-    const float M = records_max(rec, n, sh);
+// Levels 1-3 over n (m, s) records: every lane condenses one 32-record chunk
+// to a (max, sum) pair (chunk pairs in shared memory), the warps' pairs give
+// the scale M and the weights; the warp holding u S walks its chunks, then the
+// chosen chunk's records.  sh.part / sh.part_frac as for block_walk; returns
+// S, *M_out = M.
+__device__ float walk_records(const float2* rec, int n, float u, SelShared& sh, float* M_out) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nch = (n + 31) / 32;
+    const int cpw = (nch + kSelWarps - 1) / kSelWarps;
+    const int c0 = min(nch, warp * cpw), c1 = min(nch, c0 + cpw);
+    Lse acc{-INFINITY, 0.f};
+    for (int cb = c0; cb < c1; cb += 32) {
+        const int c = cb + lane;
+        float cm = -INFINITY, cs = 0.f;
+        if (c < c1) {
+            chunk_pair(rec, n, c, &cm, &cs);
+            sh.cmax[c] = cm;
+            sh.csum[c] = cs;
+        }
+        if (cs > 0.f) acc = lse_merge(acc, Lse{cm, cs});
+    }
+    acc = warp_lse(acc);
+    if (lane == 0) {
+        sh.wmx[warp] = acc.m;
+        sh.wsum[warp] = acc.s;
+    }
+    __syncthreads();
+    float M = -INFINITY;
+#pragma unroll
+    for (int q = 0; q < kSelWarps; ++q)
+        if (sh.wsum[q] > 0.f) M = fmaxf(M, sh.wmx[q]);
+    float wq[kSelWarps], S = 0.f;
+#pragma unroll
+    for (int q = 0; q < kSelWarps; ++q) {
+        wq[q] = sh.wsum[q] > 0.f ? sh.wsum[q] * __expf(sh.wmx[q] - M) : 0.f;
+        S += wq[q];
+    }
+    const float T = u * S;
+    int owner = -1;
+    float excl = 0.f, run = 0.f, wo = 0.f;
+#pragma unroll
+    for (int q = 0; q < kSelWarps; ++q) {
+        if (wq[q] > 0.f && run <= T) {
+            owner = q;
+            excl = run;
+            wo = wq[q];
+        }
+        run += wq[q];
+    }
+    if (owner < 0) {
+        if (threadIdx.x == 0) {
+            sh.part = -1;
+            sh.part_frac = 0.f;
+        }
+    } else if (warp == owner) {
+        const float fw = clamp_frac((T - excl) / wo);
+        float fc;
+        const int c = warp_pick(c0, c1, fw,
+                                [&](int q) { return sh.csum[q] > 0.f ? sh.csum[q] * __expf(sh.cmax[q] - M) : 0.f; },
+                                &fc);
+        int pick = -1;
+        float pf = 0.f;
+        if (c >= 0) pick = warp_pick(c * 32, min(n, c * 32 + 32), fc, [&](int b) { return rec_weight(rec[b], M); }, &pf);
+        if (lane == 0) {
+            sh.part = pick;
+            sh.part_frac = pf;
+        }
+    }
+    __syncthreads();
     *M_out = M;
-    return block_walk(n, u, [&](int b) { return rec_weight(rec[b], M); }, sh);
+    return S;
 }
 
 // Copies bytes (a multiple of 16, 16-byte aligned source) to dst with bulk
@@ -390,8 +475,14 @@ __global__ void __launch_bounds__(kSelThreads) resample_kernel(const ResamplePar
         // bonus: chunk partials of target row / T, then the chunk's ids
         const int row = p.bonus_row[i];
         const float u = uniform_at(rk, 3u, static_cast<uint32_t>(i), static_cast<uint32_t>(p.bonus_pos[i]), 0u);
-        float M;
-        walk_records(p.lse_part + static_cast<size_t>(row) * p.n_chunks, p.n_chunks, u, sh, &M);
+        {   // a few chunk records in global memory, not 16-byte aligned: scalar loads
+            const float2* lp = p.lse_part + static_cast<size_t>(row) * p.n_chunks;
+            float m = -INFINITY;
+            for (int b = tid; b < p.n_chunks; b += kSelThreads)
+                if (lp[b].y > 0.f) m = fmaxf(m, lp[b].x);
+            const float M = block_max(m, sh);
+            block_walk(p.n_chunks, u, [&](int b) { return rec_weight(lp[b], M); }, sh);
+        }
         const int c = sh.part;
         if (c >= 0) {
             const float mc = p.lse_part[static_cast<size_t>(row) * p.n_chunks + c].x;
