@@ -76,6 +76,7 @@ def test_draft_chain_host_validation(lib):
     assert _chain(lib, L=ctypes.c_void_p(0x1004)) == 2   # misaligned base
     assert _chain(lib, ws=None) == 5
     assert _chain(lib, ws_bytes=16) == 5
+    assert _chain(lib, dec=1, V=524288 + 8) == 2   # sampling: the draw's chunk table holds 32768 records
 
 
 def test_prepare_host_validation(lib):
@@ -101,6 +102,9 @@ def test_tree_and_verify_host_validation(lib):
     big_pool = list(args)
     big_pool[6], big_pool[10], big_pool[9] = 128, 64, 1   # P * B + 1 > 8192 (pool ranked in shared memory)
     assert f(*big_pool) == 2
+    big_v = list(args)
+    big_v[7] = 524288 + 8                       # V beyond the level select's chunk and candidate tables
+    assert f(*big_v) == 2
     vt = lib.sdm_verify_tree
     assert vt(FAKE, 0, FAKE, FAKE, FAKE, 4, 16384, 7, 1024, FAKE, FAKE, FAKE, FAKE, 1 << 30, None, None) == 2
     v = lib.sdm_verify
