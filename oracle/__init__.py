@@ -122,6 +122,21 @@ def schedule_budget(conf, cost):
                 m_star=int(m_star[0]))
 
 
+def schedule_dynamic(conf, conf_stale, cost):
+    R, g = conf.shape
+    assert conf_stale.shape == (R, g)
+    survival = np.zeros((R, g), np.float32)
+    budget = np.zeros(R, np.int32)
+    expected = np.zeros(1, np.float64)
+    total = np.zeros(1, np.int32)
+    capacity = np.zeros(1, np.int32)
+    lib().orc_schedule_dynamic(_p(_c(conf, np.float32)), _p(_c(conf_stale, np.float32)), R, g,
+                               _p(_c(cost, np.float64)), _p(survival), _p(budget), _p(expected), _p(total),
+                               _p(capacity))
+    return dict(survival=survival, budget=budget, expected=float(expected[0]), total_tokens=int(total[0]),
+                capacity=int(capacity[0]))
+
+
 def pack_ragged(anchor, draft, budget, tiers):
     R, g = draft.shape
     tiers = _c(tiers, np.int32)

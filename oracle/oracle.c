@@ -422,6 +422,62 @@ int orc_schedule_budget(const float* conf, int R, int gamma, const double* cost,
 }
 
 /* ------------------------------------------------------------------ */
+/* schedule_dynamic ([DSpark notes] sec. 9.2: the production scheduler)  */
+/* ------------------------------------------------------------------ */
+/* Ranked survivals of conf (the S_{i,k} products, those >= 2^-18) into e,
+ * written to surv when not NULL; returns how many. */
+static int ranked_survivals(const float* conf, int R, int gamma, float* surv, surv_entry* e) {
+    const float floor_s = 1.0f / 262144.0f;
+    int n = 0;
+    for (int i = 0; i < R; ++i) {
+        float s = 1.0f;
+        for (int k = 1; k <= gamma; ++k) {
+            s = s * conf[(size_t)i * gamma + (size_t)(k - 1)];
+            if (surv) surv[(size_t)i * gamma + (size_t)(k - 1)] = s;
+            if (s >= floor_s) e[n++] = (surv_entry){s, i, k};
+        }
+    }
+    qsort(e, (size_t)n, sizeof(surv_entry), surv_cmp);
+    return n;
+}
+
+int orc_schedule_dynamic(const float* conf, const float* conf_stale, int R, int gamma, const double* cost,
+                         float* survival, int32_t* budget, double* expected, int32_t* total_tokens,
+                         int32_t* capacity) {
+    surv_entry* e = (surv_entry*)malloc(sizeof(surv_entry) * (size_t)R * (size_t)gamma + 1);
+    /* 1. the verify capacity K from the confidences of two steps before: the
+     *    global argmax over every m of E'(m) / cost[R + m], no early stop
+     *    (the table may step), the smallest m on ties */
+    int n_stale = ranked_survivals(conf_stale, R, gamma, NULL, e);
+    double E = (double)R;
+    double best = E / cost[R];
+    int K = 0;
+    for (int m = 1; m <= n_stale; ++m) {
+        E += (double)e[m - 1].s;
+        double f = E / cost[R + m];
+        if (f > best) {
+            best = f;
+            K = m;
+        }
+    }
+    /* 2. this step's candidates ranked by their current survivals; the top K
+     *    (all of them if fewer) are verified */
+    int n_now = ranked_survivals(conf, R, gamma, survival, e);
+    int take = K < n_now ? K : n_now;
+    for (int i = 0; i < R; ++i) budget[i] = 0;
+    double En = (double)R;
+    for (int c = 0; c < take; ++c) {
+        budget[e[c].req] += 1;
+        En += (double)e[c].s;
+    }
+    *expected = En;
+    *total_tokens = R + take;
+    *capacity = K;
+    free(e);
+    return 0;
+}
+
+/* ------------------------------------------------------------------ */
 /* pack_ragged ([SGLang] "ragged verify")                               */
 /* ------------------------------------------------------------------ */
 int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,

@@ -72,6 +72,14 @@ int orc_schedule_budget(const float* conf, int R, int gamma, const double* cost,
                         float* survival, int32_t* budget, double* expected,
                         int32_t* total_tokens, int32_t* m_star);
 
+/* The production scheduler: capacity K = the global argmax over m of
+ * E'(m) / cost[R + m] on the survivals of conf_stale (the confidences of two
+ * steps before), then the top K of the current survivals (all if fewer).
+ * survival = the current products; capacity = K. */
+int orc_schedule_dynamic(const float* conf, const float* conf_stale, int R, int gamma, const double* cost,
+                         float* survival, int32_t* budget, double* expected, int32_t* total_tokens,
+                         int32_t* capacity);
+
 /* Ragged front-pack of the verify windows.  budget == NULL means the full
  * block (n_i = gamma).  Packed arrays need max(tiers[-1], R*(gamma+1)) slots. */
 int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,

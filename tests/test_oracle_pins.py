@@ -246,6 +246,86 @@ def test_scheduler_prefix_closed_and_unimodal():
 
 
 # ---------------------------------------------------------------------------
+# production scheduler (stale capacity, global search, current ranking)
+# ---------------------------------------------------------------------------
+def _cost_from(table, R, g):
+    cost = np.zeros(R * (g + 1) + 1, np.float64)
+    for n, c in table.items():
+        cost[int(n)] = c
+    cost[:R] = cost[R]
+    return cost
+
+
+def test_dynamic_scheduler_cliff_fixture():
+    """The hand-worked example: the stepped table makes f fall after the
+    first token, the early-stopping scheduler verifies nothing, the global
+    search over the stale survivals finds K = 4, and the current ranking
+    spends it on request 1."""
+    g = json.load(open(os.path.join(GOLDEN, "sps_cliff_dynamic_scheduler.json")))
+    R, gam = g["R"], g["gamma"]
+    cost = _cost_from(g["cost_by_tokens"], R, gam)
+    stale = np.array(g["conf_stale"], np.float32)
+    now = np.array(g["conf_now"], np.float32)
+    sd = oracle.schedule_dynamic(now, stale, cost)
+    assert sd["capacity"] == g["expected_capacity"]
+    assert sd["budget"].tolist() == g["expected_budget"]
+    assert sd["total_tokens"] == g["expected_total_tokens"]
+    assert abs(sd["expected"] - g["expected_E"]) < 1e-6
+    assert oracle.schedule_budget(stale, cost)["m_star"] == g["expected_capacity_with_early_stop"]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_dynamic_scheduler_equals_greedy_on_additive_tables(seed):
+    """With current == stale confidences and an additive table (f rises then
+    falls), the global search and the early-stopping greedy agree."""
+    rng = np.random.default_rng(100 + seed)
+    R, g = int(rng.integers(1, 40)), int(rng.integers(1, 9))
+    conf = rng.uniform(0.1, 1.0, (R, g)).astype(np.float32)
+    cost = float(rng.uniform(0.5, 3.0)) + float(rng.uniform(0.001, 0.5)) * np.arange(R * (g + 1) + 1)
+    sd = oracle.schedule_dynamic(conf, conf, cost)
+    sb = oracle.schedule_budget(conf, cost)
+    np.testing.assert_array_equal(sd["budget"], sb["budget"])
+    assert sd["capacity"] == sb["m_star"] and sd["expected"] == sb["expected"]
+    np.testing.assert_array_equal(sd["survival"], sb["survival"])
+
+
+def _allocations(R, g):
+    return itertools.product(range(g + 1), repeat=R)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_dynamic_scheduler_matches_brute_force(seed):
+    """Over every allocation (n_1..n_R) in [0, gamma]^R: the capacity's value
+    E'(K)/cost[R + K] on the stale survivals is the best any allocation
+    reaches (stepped table), and among the allocations of the verified size
+    none carries more current survival than the selection."""
+    rng = np.random.default_rng(seed)
+    R, g = int(rng.integers(1, 5)), int(rng.integers(1, 5))
+    stale = rng.uniform(0.05, 1.0, (R, g)).astype(np.float32)
+    now = rng.uniform(0.05, 1.0, (R, g)).astype(np.float32)
+    tiers = np.sort(rng.choice(np.arange(R, R * (g + 1) + 1), size=min(3, R * g + 1), replace=False))
+    N = np.arange(R * (g + 1) + 1)
+    tier_of = np.array([tiers[np.searchsorted(tiers, n)] if n <= tiers[-1] else n for n in N])
+    cost = float(rng.uniform(0.5, 2.0)) + float(rng.uniform(0.05, 0.6)) * tier_of.astype(np.float64)
+    sd = oracle.schedule_dynamic(now, stale, cost)
+    Ss = np.cumprod(stale, axis=1, dtype=np.float32).astype(np.float64)
+    Sn = np.cumprod(now, axis=1, dtype=np.float32).astype(np.float64)
+
+    def value(S, n):
+        return R + sum(S[i, :n[i]].sum() for i in range(R))
+
+    best = max(value(Ss, n) / cost[R + sum(n)] for n in _allocations(R, g))
+    K = sd["capacity"]
+    top_stale = sorted(Ss.reshape(-1), reverse=True)[:K]
+    assert abs((R + sum(top_stale)) / cost[R + K] - best) <= 1e-12 * best
+    size = sd["total_tokens"] - R
+    assert size == min(K, R * g)
+    best_now = max(value(Sn, n) for n in _allocations(R, g) if sum(n) == size)
+    assert abs(sd["expected"] - best_now) <= 1e-12 * best_now
+    assert int(sd["budget"].sum()) == size
+
+
+# ---------------------------------------------------------------------------
 # ragged pack
 # ---------------------------------------------------------------------------
 def test_pack_round_trip_and_tier():
