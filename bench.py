@@ -44,6 +44,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
+    ap.add_argument("--scheduler", default="budget", choices=["budget", "dynamic"],
+                    help="budget: the early-stopping scheduler on the additive table; dynamic: the production "
+                         "scheduler (capacity from the confidences of two steps before, global search over the "
+                         "tier-stepped table)")
     return ap.parse_args()
 
 
@@ -163,7 +167,7 @@ class ClockSampler:
 class Cycle:
     """Preallocated buffers and the launch sequence of one decode cycle."""
 
-    def __init__(self, w, seed, device):
+    def __init__(self, w, seed, device, dynamic=False):
         import torch
 
         from speculative_decoding_markov_gb300 import binding as sdm
@@ -176,6 +180,7 @@ class Cycle:
         R, B, V, r = w.R, w.B, w.V, w.r
         self.sample = w.decode == "sample"
         self.tree = w.decode == "tree"
+        self.dynamic = dynamic
         i32 = dict(dtype=torch.int32, device=device)
         self.status = sdm.new_status(device)
         self.side = torch.cuda.Stream(device=device)
@@ -188,7 +193,7 @@ class Cycle:
                        lse=torch.zeros((R, B), dtype=torch.float32, device=device))
         self.sc = dict(survival=torch.empty((R, B), dtype=torch.float32, device=device), budget=torch.empty((R,), **i32),
                        expected=torch.empty((1,), dtype=torch.float64, device=device),
-                       total_tokens=torch.empty((1,), **i32))
+                       total_tokens=torch.empty((1,), **i32), capacity=torch.empty((1,), **i32))
         cap = sdm.pack_capacity(R, B, list(w.tiers))
         self.cap = cap
         self.pk = dict(cu_seqlens=torch.empty((R + 1,), **i32), packed_tok=torch.empty((cap,), **i32),
@@ -252,7 +257,10 @@ class Cycle:
 
     def schedule(self):
         sdm, i = self.sdm, self.inp
-        sdm.schedule_budget(i["conf"], i["cost"], out=self.sc, dev_status=self.status)
+        if self.dynamic:
+            sdm.schedule_dynamic(i["conf"], i["conf_stale"], i["cost_tiered"], out=self.sc, dev_status=self.status)
+        else:
+            sdm.schedule_budget(i["conf"], i["cost"], out=self.sc, dev_status=self.status)
 
     def pack(self):
         sdm, i = self.sdm, self.inp
@@ -324,7 +332,8 @@ def run_ours(args, w, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    cyc = Cycle(w, seed=rank, device=dev)
+    dynamic = args.scheduler == "dynamic"
+    cyc = Cycle(w, seed=rank, device=dev, dynamic=dynamic)
     R, B, V = w.R, w.B, w.V
     committed = int(cyc.vr["n_out"].sum().item())
     accepted = int(cyc.vr["accept"].sum().item())
@@ -447,7 +456,7 @@ def run_ours(args, w, world, rank, local):
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        cpu = oracle_sample(w, cyc.inp, args.cpu_seconds)
+        cpu = oracle_sample(w, cyc.inp, args.cpu_seconds, dynamic)
 
     clk = clocks.summary(w0, w1)
     out = {
@@ -464,6 +473,7 @@ def run_ours(args, w, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "R": R, "B": B, "V": V, "r": w.r, "decode": w.decode, "mode": w.modes[0],
+                   "scheduler": None if cyc.tree else args.scheduler,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed by a 256 MB write before every step",
                    "timed": "draft+schedule+pack+verify (CUDA events); target stand-in row gather excluded"},
@@ -497,7 +507,8 @@ def run_e2e(cyc, args, committed):
     import torch
 
     i = cyc.inp
-    host = {k: i[k].cpu().pin_memory() for k in ("L", "anchor", "conf")}
+    keys = ("L", "anchor", "conf") + (("conf_stale",) if cyc.dynamic else ())
+    host = {k: i[k].cpu().pin_memory() for k in keys}
     host["target"] = cyc.target.cpu().pin_memory()
     out_h = torch.empty_like(cyc.vr["out_tok"], device="cpu").pin_memory()
     nout_h = torch.empty_like(cyc.vr["n_out"], device="cpu").pin_memory()
@@ -510,6 +521,8 @@ def run_e2e(cyc, args, committed):
         i["L"].copy_(host["L"], non_blocking=True)
         i["anchor"].copy_(host["anchor"], non_blocking=True)
         i["conf"].copy_(host["conf"], non_blocking=True)
+        if cyc.dynamic:
+            i["conf_stale"].copy_(host["conf_stale"], non_blocking=True)
         cyc.target.copy_(host["target"], non_blocking=True)
         if graphs:
             cyc.g_draft.replay()
@@ -539,7 +552,7 @@ def run_e2e(cyc, args, committed):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_cycle(w, inp, idx, cycle_seed=0):
+def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False):
     """One oracle cycle for the requests idx (schedule over all requests);
     returns (seconds of oracle work, committed tokens)."""
     import numpy as np
@@ -569,12 +582,17 @@ def oracle_cycle(w, inp, idx, cycle_seed=0):
         t3 = time.perf_counter()
         return (t1 - t0) + (t3 - t2), int(vt["n_out"].sum())
     conf, cost, tiers = np_of(inp["conf"]), np_of(inp["cost"]), np_of(inp["tiers"])
+    if dynamic:
+        stale, cost = np_of(inp["conf_stale"]), np_of(inp["cost_tiered"])
     sample = w.decode == "sample"
     ids = np.asarray(idx, np.int32)
     t0 = time.perf_counter()
     dr = oracle.draft_chain(L, U, W, an, decode=oracle.SAMPLE if sample else oracle.GREEDY,
                             temperature=w.temperature, seed=cycle_seed, req_ids=ids)
-    sc = oracle.schedule_budget(conf, cost)
+    if dynamic:
+        sc = oracle.schedule_dynamic(conf, stale, cost)
+    else:
+        sc = oracle.schedule_budget(conf, cost)
     budget = sc["budget"][ids]
     static = w.modes[0] != "compact"
     pk = oracle.pack_ragged(an, dr["tokens"], None if static else budget, tiers)
@@ -593,13 +611,13 @@ def oracle_cycle(w, inp, idx, cycle_seed=0):
     return (t1 - t0) + (t3 - t2), int(vr["n_out"].sum())
 
 
-def oracle_sample(w, inp, seconds):
+def oracle_sample(w, inp, seconds, dynamic=False):
     """Oracle throughput on a bounded sample: requests are added one at a time
     (each a full cycle: its draft, the schedule over all requests, its pack and
     verify) until about `seconds` of oracle work."""
     spent, toks, n = 0.0, 0, 0
     while n < w.R and (spent < seconds or n < 2):
-        dt, c = oracle_cycle(w, inp, [n])
+        dt, c = oracle_cycle(w, inp, [n], dynamic=dynamic)
         spent += dt
         toks += c
         n += 1
@@ -614,13 +632,14 @@ def run_reference(args, w):
     from speculative_decoding_markov_gb300 import synthetic
 
     inp = synthetic.generate(w, seed=0, device="cpu")
+    dynamic = args.scheduler == "dynamic" and w.decode != "tree"
     for _ in range(args.warmup):
-        oracle_cycle(w, inp, [0])
+        oracle_cycle(w, inp, [0], dynamic=dynamic)
     spent, toks = 0.0, 0
     per = max(1, min(w.R, 2))
     for k in range(args.steps):
         idx = [(k * per + j) % w.R for j in range(per)]
-        dt, c = oracle_cycle(w, inp, idx)
+        dt, c = oracle_cycle(w, inp, idx, dynamic=dynamic)
         spent += dt
         toks += c
     value = toks / spent
@@ -629,7 +648,7 @@ def run_reference(args, w):
             "ms_per_step": spent / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": w.name, "R": w.R, "B": w.B, "V": w.V, "r": w.r, "decode": w.decode,
-                       "mode": w.modes[0]},
+                       "mode": w.modes[0], "scheduler": None if w.decode == "tree" else args.scheduler},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

@@ -206,6 +206,32 @@ sdm_status sdm_schedule_budget(const float* conf, int R, int gamma, const double
                                int32_t* dev_status, void* stream);
 
 /*
+ * schedule_dynamic: the production scheduler ([DSpark notes] sec. 9.2,
+ * "scheduler adaptation on real hardware").  The step's batch capacity must
+ * be known before the step's own confidences are, so it comes from the
+ * confidences of two steps before; the step's candidates are still ranked by
+ * their own survivals (dynamic top-K); and because the capacity no longer
+ * depends on this step's tokens, the search over the cost table is global,
+ * which crosses the steps of a tiered table that an early stop would not.
+ *   S'[i, k], S[i, k]: the survival products of conf_stale and conf (fp32,
+ *   left to right), ranked as in schedule_budget (S desc, request asc,
+ *   position asc; values below 2^-18 are left out).
+ *   K = the m in 0 .. (ranked S') maximising E'(m) / cost[R + m], E'(m) =
+ *   R + sum of the top m of S' (exact fp64), the smallest m on ties.
+ *   budget[i] = request i's count in the top min(K, ranked S) of S.
+ * In:  conf, conf_stale [R, gamma] fp32 (post-sigmoid), cost
+ *      [R*(gamma+1)+1] fp64, every entry > 0 (it may step with the tier).
+ * Out: survival [R, gamma] fp32 (of conf), budget [R] int32, expected [1]
+ *      fp64 (R + the selected survivals), total_tokens [1] int32
+ *      (R + min(K, ranked S)), capacity [1] int32 (K).
+ * Constraint: R * gamma <= 8192.
+ */
+sdm_status sdm_schedule_dynamic(const float* conf, const float* conf_stale, int R, int gamma,
+                                const double* cost, float* survival, int32_t* budget,
+                                double* expected, int32_t* total_tokens, int32_t* capacity,
+                                int32_t* dev_status, void* stream);
+
+/*
  * pack_ragged: ragged front-pack of the verify windows ([SGLang] "ragged
  * verify": windows are front-packed into a compact cu_seqlens buffer whose
  * total is rounded up to the nearest captured tier).

@@ -25,7 +25,7 @@ DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY = 
 
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
-           "sdm_verify_greedy_static", "sdm_status_str", "sdm_version")
+           "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_status_str", "sdm_version")
 
 
 class SdmRng(ctypes.Structure):
@@ -54,6 +54,8 @@ def _declare(lib):
                                    _VP, _SZ, _VP, _VP]
     lib.sdm_schedule_budget.restype = _I
     lib.sdm_schedule_budget.argtypes = [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
+    lib.sdm_schedule_dynamic.restype = _I
+    lib.sdm_schedule_dynamic.argtypes = [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_pack_ragged.restype = _I
     lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
     lib.sdm_verify.restype = _I
@@ -199,6 +201,29 @@ def schedule_budget(conf, cost, out=None, dev_status=None):
                                    _ptr(out["expected"]), _ptr(out["total_tokens"]), None, 0, _ptr(dev_status),
                                    _stream())
     _check(st, "sdm_schedule_budget")
+    out["dev_status"] = dev_status
+    return out
+
+
+def schedule_dynamic(conf, conf_stale, cost, out=None, dev_status=None):
+    """The production scheduler: capacity from conf_stale (the confidences of
+    two steps before) by a global search over cost, then the top K of conf's
+    survivals."""
+    _need_cuda(conf, conf_stale, cost)
+    R, g = conf.shape
+    assert tuple(conf_stale.shape) == (R, g)
+    dev = conf.device
+    if out is None:
+        out = dict(survival=torch.empty((R, g), dtype=torch.float32, device=dev),
+                   budget=torch.empty((R,), dtype=torch.int32, device=dev),
+                   expected=torch.empty((1,), dtype=torch.float64, device=dev),
+                   total_tokens=torch.empty((1,), dtype=torch.int32, device=dev),
+                   capacity=torch.empty((1,), dtype=torch.int32, device=dev))
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_schedule_dynamic(_ptr(conf), _ptr(conf_stale), R, g, _ptr(cost), _ptr(out["survival"]),
+                                    _ptr(out["budget"]), _ptr(out["expected"]), _ptr(out["total_tokens"]),
+                                    _ptr(out["capacity"]), _ptr(dev_status), _stream())
+    _check(st, "sdm_schedule_dynamic")
     out["dev_status"] = dev_status
     return out
 

@@ -429,6 +429,19 @@ sdm_status sdm_schedule_budget(const float* conf, int R, int gamma, const double
     return SDM_OK;
 }
 
+sdm_status sdm_schedule_dynamic(const float* conf, const float* conf_stale, int R, int gamma, const double* cost,
+                                float* survival, int32_t* budget, double* expected, int32_t* total_tokens,
+                                int32_t* capacity, int32_t* dev_status, void* stream) {
+    (void)dev_status;
+    if (!conf || !conf_stale || !cost || !survival || !budget || !expected || !total_tokens || !capacity || R <= 0 ||
+        gamma <= 0)
+        return SDM_ERR_INVALID_ARG;
+    if (static_cast<long long>(R) * gamma > 8192) return SDM_ERR_UNSUPPORTED;
+    SDM_CHECK_CUDA(launch_schedule_dynamic(conf, conf_stale, R, gamma, cost, survival, budget, expected, total_tokens,
+                                           capacity, static_cast<cudaStream_t>(stream)));
+    return SDM_OK;
+}
+
 sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
                            const int32_t* tiers, int n_tiers, int32_t* cu_seqlens, int32_t* packed_tok,
                            int32_t* packed_req, int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,

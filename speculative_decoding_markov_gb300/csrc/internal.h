@@ -122,6 +122,10 @@ cudaError_t launch_schedule(const float* conf, int R, int gamma, const double* c
                             int32_t* budget, double* expected, int32_t* total_tokens, unsigned long long* ws_keys,
                             int32_t* dev_status, cudaStream_t s);
 
+cudaError_t launch_schedule_dynamic(const float* conf, const float* conf_stale, int R, int gamma, const double* cost,
+                                    float* survival, int32_t* budget, double* expected, int32_t* total_tokens,
+                                    int32_t* capacity, cudaStream_t s);
+
 cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
                         const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
                         int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s);

@@ -221,6 +221,166 @@ __global__ void __launch_bounds__(kSchedThreads) schedule_kernel(const float* co
 }
 
 // ---------------------------------------------------------------------------
+// production scheduler ([DSpark notes] sec. 9.2): capacity K from the
+// confidences of two steps before by a global search over the cost table,
+// then the top K of this step's survivals.  One CTA, the same survival keys,
+// floor and bitonic sort as schedule_kernel.
+// ---------------------------------------------------------------------------
+// Survivals of conf (fp32 products, left to right) as descending sort keys
+// (S bits, then ~(i * gamma + k): request asc, position asc), those below the
+// floor as 0; writes the survivals to surv_out when not NULL.  Returns the
+// number of keys above the floor (all threads).
+__device__ int ranked_keys(const float* conf, int R, int gamma, float* s_surv, unsigned long long* sk, int n_pad,
+                           float* surv_out, int* s_count) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int n = R * gamma;
+    const float floor_s = 1.0f / 262144.0f;
+    for (int t = tid; t < n; t += nt) s_surv[t] = conf[t];
+    for (int t = n + tid; t < n_pad; t += nt) sk[t] = 0ull;
+    if (tid == 0) *s_count = 0;
+    __syncthreads();
+    for (int i = tid; i < R; i += nt) {
+        float s = 1.0f;
+        for (int k = 0; k < gamma; ++k) {
+            const int t = i * gamma + k;
+            s = __fmul_rn(s, s_surv[t]);
+            s_surv[t] = s;
+            sk[t] = (s >= floor_s) ? ((static_cast<unsigned long long>(__float_as_uint(s)) << 32) | ~static_cast<uint32_t>(t))
+                                   : 0ull;
+        }
+    }
+    __syncthreads();
+    if (surv_out)
+        for (int t = tid; t < n; t += nt) surv_out[t] = s_surv[t];
+    for (int size = 2; size <= n_pad; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < n_pad; t += nt) {
+                const int u = t ^ stride;
+                if (u > t) {
+                    const bool desc = (t & size) == 0;
+                    const unsigned long long a = sk[t], b = sk[u];
+                    if (desc ? (a < b) : (a > b)) {
+                        sk[t] = b;
+                        sk[u] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int t = tid; t < n_pad; t += nt)
+        if (sk[t] != 0ull && (t + 1 == n_pad || sk[t + 1] == 0ull)) *s_count = t + 1;
+    __syncthreads();
+    return *s_count;
+}
+
+// A ranked survival as an exact integer (every survival >= 2^-18 is a
+// multiple of 2^-41).
+__device__ __forceinline__ unsigned long long surv_units(unsigned long long key) {
+    return static_cast<unsigned long long>(ldexpf(__uint_as_float(static_cast<uint32_t>(key >> 32)), 41));
+}
+
+__global__ void __launch_bounds__(kSchedThreads) schedule_dynamic_kernel(const float* conf, const float* conf_stale,
+                                                                         int R, int gamma, const double* cost,
+                                                                         float* survival, int32_t* budget,
+                                                                         double* expected, int32_t* total_tokens,
+                                                                         int32_t* capacity, int n_pad) {
+    extern __shared__ unsigned long long sk[];              // n_pad sort keys
+    unsigned long long* part = sk + n_pad;                   // kSchedThreads exclusive prefixes
+    int* cnt = reinterpret_cast<int*>(part + kSchedThreads);  // R counters
+    float* s_surv = reinterpret_cast<float*>(cnt + R);       // R * gamma confidences, then survivals
+    __shared__ int s_count;
+    __shared__ unsigned long long best_bits;
+    __shared__ int best_m;
+    __shared__ unsigned long long sum_units;
+    pdl_wait();
+    pdl_trigger();
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int per = (n_pad + 1 + nt - 1) / nt;   // m = 0 .. n_pad
+    // 1. capacity from the stale confidences: f(m) = E'(m) / cost[R + m] for
+    //    every m (E' exact in units of 2^-41, one IEEE fp64 division each, as
+    //    in the oracle), the largest f, the smallest m among equals
+    const int Ms = ranked_keys(conf_stale, R, gamma, s_surv, sk, n_pad, nullptr, &s_count);
+    unsigned long long local = 0;
+    for (int q = 0; q < per; ++q) {
+        const int t = tid * per + q;
+        if (t < Ms) local += surv_units(sk[t]);
+    }
+    {   // exclusive block scan of the thread partials (integer: exact in any order)
+        const int lane = tid & 31, warp = tid >> 5;
+        unsigned long long x = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) part[warp] = x;
+        if (tid == 0) {
+            best_bits = 0ull;
+            best_m = 0x7fffffff;
+            sum_units = 0ull;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long wv = lane < (nt >> 5) ? part[lane] : 0ull;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(0xffffffffu, wv, o);
+                if (lane >= o) wv += y;
+            }
+            part[lane] = wv;
+        }
+        __syncthreads();
+        const unsigned long long before = (warp > 0 ? part[warp - 1] : 0ull) + x - local;
+        __syncthreads();
+        part[tid] = before;
+    }
+    __syncthreads();
+    const double two_m41 = 4.547473508864641e-13;   // 2^-41
+    const unsigned long long base = static_cast<unsigned long long>(R) << 41;
+    double fbest = -1.0;
+    int mbest = 0x7fffffff;
+    {
+        unsigned long long run = part[tid];
+        for (int q = 0; q < per; ++q) {
+            const int m = tid * per + q;   // E'(m) uses the first m survivals
+            if (m > Ms) break;
+            const double f = __ddiv_rn(static_cast<double>(base + run) * two_m41, cost[R + m]);
+            if (f > fbest) {               // m rises: the first of equal values stays
+                fbest = f;
+                mbest = m;
+            }
+            if (m < Ms) run += surv_units(sk[m]);
+        }
+    }
+    if (mbest != 0x7fffffff) atomicMax(&best_bits, static_cast<unsigned long long>(__double_as_longlong(fbest)));
+    __syncthreads();   // (f > 0: the bits of positive doubles order like their values)
+    if (mbest != 0x7fffffff && static_cast<unsigned long long>(__double_as_longlong(fbest)) == best_bits)
+        atomicMin(&best_m, mbest);
+    __syncthreads();
+    const int K = best_m == 0x7fffffff ? 0 : best_m;
+    // 2. this step's survivals, ranked; the top min(K, available) are verified
+    const int Mn = ranked_keys(conf, R, gamma, s_surv, sk, n_pad, survival, &s_count);
+    const int take = K < Mn ? K : Mn;
+    for (int i = tid; i < R; i += nt) cnt[i] = 0;
+    __syncthreads();
+    unsigned long long mine = 0;
+    for (int t = tid; t < take; t += nt) {
+        const uint32_t id = ~static_cast<uint32_t>(sk[t] & 0xffffffffull);
+        atomicAdd(&cnt[id / gamma], 1);
+        mine += surv_units(sk[t]);
+    }
+    atomicAdd(&sum_units, mine);
+    __syncthreads();
+    for (int i = tid; i < R; i += nt) budget[i] = cnt[i];
+    if (tid == 0) {
+        *expected = static_cast<double>(base + sum_units) * two_m41;
+        *total_tokens = R + take;
+        *capacity = K;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // ragged pack: one CTA
 // ---------------------------------------------------------------------------
 constexpr int kPackThreads = 256;
@@ -741,6 +901,25 @@ cudaError_t launch_schedule(const float* conf, int R, int gamma, const double* c
     const int nt = n_pad < 64 ? 64 : (n_pad > kSchedThreads ? kSchedThreads : n_pad);
     return launch_pdl(schedule_kernel, dim3(1), dim3(nt), smem, s, conf, R, gamma, cost, survival, budget,
                       expected, total_tokens, n_pad);
+}
+
+cudaError_t launch_schedule_dynamic(const float* conf, const float* conf_stale, int R, int gamma, const double* cost,
+                                    float* survival, int32_t* budget, double* expected, int32_t* total_tokens,
+                                    int32_t* capacity, cudaStream_t s) {
+    int n_pad = 1;
+    while (n_pad < R * gamma) n_pad <<= 1;
+    const size_t smem = static_cast<size_t>(n_pad) * 8 + kSchedThreads * 8 + static_cast<size_t>(R) * 4 +
+                        static_cast<size_t>(R) * gamma * 4;
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e =
+            cudaFuncSetAttribute(schedule_dynamic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    const int nt = n_pad < 64 ? 64 : (n_pad > kSchedThreads ? kSchedThreads : n_pad);
+    return launch_pdl(schedule_dynamic_kernel, dim3(1), dim3(nt), smem, s, conf, conf_stale, R, gamma, cost, survival,
+                      budget, expected, total_tokens, capacity, n_pad);
 }
 
 cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,

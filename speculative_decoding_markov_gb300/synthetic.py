@@ -30,7 +30,7 @@ from .workloads import BF16, FP32, Workload
 _TORCH_DTYPE = {BF16: torch.bfloat16, FP32: torch.float32}
 
 # distinct generator streams per tensor (seed * 64 + stream)
-_S_L, _S_LB, _S_U, _S_W, _S_ANCHOR, _S_ETA, _S_CONF, _S_CLASS = range(16, 24)
+_S_L, _S_LB, _S_U, _S_W, _S_ANCHOR, _S_ETA, _S_CONF, _S_CLASS, _S_STALE = range(16, 25)
 
 
 def torch_dtype(code: int) -> torch.dtype:
@@ -81,6 +81,28 @@ def cost_table(w: Workload, R: int | None = None, B: int | None = None) -> torch
     return a + b * n
 
 
+def tiered_cost_table(w: Workload, R: int | None = None, B: int | None = None) -> torch.Tensor:
+    """The stepped form of the additive table: a + b tier(N), tier(N) = the
+    smallest captured tier >= N (N itself above every tier), the cost of the
+    graph a packed total actually replays (fp64)."""
+    R = w.R if R is None else R
+    B = w.B if B is None else B
+    a, b = w.cost
+    tiers = sorted(w.tiers)
+    n = torch.arange(R * (B + 1) + 1, dtype=torch.float64)
+    t = torch.tensor([next((x for x in tiers if x >= k), k) for k in range(R * (B + 1) + 1)], dtype=torch.float64)
+    return a + b * t if tiers else a + b * n
+
+
+def stale_confidences(conf: torch.Tensor, seed: int) -> torch.Tensor:
+    """Stand-in for the confidences of the same requests two steps before:
+    this step's, moved in logit space by N(0, 0.5) (fp32 [R, B])."""
+    x = torch.logit(conf.to(torch.float64).clamp(1e-6, 1 - 1e-6))
+    noise = torch.randn(conf.shape, generator=_gen(seed, _S_STALE, conf.device), device=conf.device,
+                        dtype=torch.float64) * 0.5
+    return torch.sigmoid(x + noise).to(torch.float32)
+
+
 def generate(w: Workload, seed: int = 0, device="cpu") -> dict:
     """All inputs of one decode cycle of workload w, on `device`."""
     R, B, V, r = w.R, w.B, w.V, w.r
@@ -96,6 +118,8 @@ def generate(w: Workload, seed: int = 0, device="cpu") -> dict:
     out = dict(L=L, L_bonus=L_bonus, U=U, W=W, anchor=anchor, sigma=sigma, eta=eta,
                cost=cost_table(w).to(device), tiers=torch.tensor(w.tiers, dtype=torch.int32, device=device))
     out["conf"] = confidences(w, out, seed, device)
+    out["conf_stale"] = stale_confidences(out["conf"], seed)
+    out["cost_tiered"] = tiered_cost_table(w).to(device)
     return out
 
 

@@ -115,5 +115,8 @@ def test_tree_and_verify_host_validation(lib):
     vargs[1] = 1                                # sample without logq / L / U / W
     assert v(*vargs) == 1
     assert lib.sdm_schedule_budget(FAKE, 2000, 8, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, None, None) == 2
+    sd = lib.sdm_schedule_dynamic
+    assert sd(FAKE, None, 4, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 1   # no stale confidences
+    assert sd(FAKE, FAKE, 2000, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 2   # R * gamma > 8192
     assert lib.sdm_pack_ragged(FAKE, FAKE, None, 4, 7, None, 2, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None, None,
                                None) == 1       # tiers missing

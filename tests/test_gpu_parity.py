@@ -261,6 +261,58 @@ def test_schedule_flushes_tiny_survivals_and_breaks_ties_by_request():
     assert ref["budget"][2] <= 2
 
 
+def _tiered_cost(R, g, rng):
+    """Step cost by total verify tokens: a + b * (the tier the total rounds up to)."""
+    tiers = np.array([64, 128, 256, 512, 1024, 2048, 4096], np.int64)
+    N = np.arange(R * (g + 1) + 1)
+    t = np.array([tiers[np.searchsorted(tiers, n)] if n <= tiers[-1] else n for n in N], np.float64)
+    return float(rng.uniform(0.5, 3.0)) + float(rng.uniform(0.001, 0.02)) * t
+
+
+@pytest.mark.parametrize("R,g,seed", [(1, 4, 0), (4, 7, 1), (64, 7, 2), (256, 8, 3), (450, 8, 4), (37, 3, 5)])
+def test_schedule_dynamic(R, g, seed):
+    """Capacity, budgets, survivals, E and N bit-exact against the oracle on a
+    tiered cost table (R * (gamma + 1) < 4096: fp64 sums exact in any order);
+    450 x 8 sorts 4096 keys, several per thread."""
+    rng = np.random.default_rng(seed)
+    now = rng.uniform(0.02, 1.0, (R, g)).astype(np.float32)
+    stale = np.clip(now + rng.normal(0, 0.2, (R, g)), 0.02, 1.0).astype(np.float32)
+    now[rng.random((R, g)) < 0.1] = 1.0                    # exact ties in S
+    cost = _tiered_cost(R, g, rng)
+    ref = oracle.schedule_dynamic(now, stale, cost)
+    out = sdm.schedule_dynamic(dev(torch.from_numpy(now)), dev(torch.from_numpy(stale)), dev(torch.from_numpy(cost)))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(out["survival"]).view(np.uint32), ref["survival"].view(np.uint32))
+    assert int(host(out["capacity"])[0]) == ref["capacity"]
+    np.testing.assert_array_equal(host(out["budget"]), ref["budget"])
+    assert float(host(out["expected"])[0]) == ref["expected"]
+    assert int(host(out["total_tokens"])[0]) == ref["total_tokens"]
+
+
+def test_schedule_dynamic_cliff_fixture_and_additive_agreement():
+    import json, os
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "sps_cliff_dynamic_scheduler.json")))
+    R, gam = g["R"], g["gamma"]
+    cost = np.zeros(R * (gam + 1) + 1, np.float64)
+    for n, c in g["cost_by_tokens"].items():
+        cost[int(n)] = c
+    cost[:R] = cost[R]
+    out = sdm.schedule_dynamic(dev(torch.tensor(g["conf_now"], dtype=torch.float32)),
+                               dev(torch.tensor(g["conf_stale"], dtype=torch.float32)), dev(torch.from_numpy(cost)))
+    torch.cuda.synchronize()
+    assert int(host(out["capacity"])[0]) == g["expected_capacity"]
+    assert host(out["budget"]).tolist() == g["expected_budget"]
+    assert int(host(out["total_tokens"])[0]) == g["expected_total_tokens"]
+    # equal confidences, additive table: the same budgets as the early-stopping scheduler
+    rng = np.random.default_rng(9)
+    conf = dev(torch.from_numpy(rng.uniform(0.05, 1.0, (128, 8)).astype(np.float32)))
+    add = dev(torch.from_numpy(2.0 + 0.004 * np.arange(128 * 9 + 1)))
+    a = sdm.schedule_dynamic(conf, conf, add)
+    b = sdm.schedule_budget(conf, add)
+    torch.cuda.synchronize()
+    assert torch.equal(a["budget"], b["budget"]) and torch.equal(a["expected"], b["expected"])
+
+
 # ---------------------------------------------------------------------------
 # pack_ragged
 # ---------------------------------------------------------------------------
