@@ -190,3 +190,35 @@ def verify_tree(target, tok, parent, n_nodes, B):
     lib().orc_verify_tree(_p(target), _dt(target), _p(_c(tok, np.int32)), _p(_c(parent, np.int32)),
                           _p(_c(n_nodes, np.int32)), R, S - 1, B, V, _p(accept), _p(out_tok), _p(n_out))
     return dict(accept=accept, out_tok=out_tok, n_out=n_out)
+
+
+def tv_label(target, cu_seqlens, anchor, draft, L, U, W, temperature=1.0):
+    """label [R, gamma] (float64): 1 - TV(q, p) per verified window row, -1 outside."""
+    R, g = draft.shape
+    V = target.shape[-1]
+    target = np.ascontiguousarray(target)
+    L = np.ascontiguousarray(L)
+    label = np.zeros((R, g), np.float64)
+    flags = lib().orc_tv_label(ctypes.c_double(temperature), _p(target), _dt(target), _p(_c(cu_seqlens, np.int32)),
+                               _p(_c(anchor, np.int32)), _p(_c(draft, np.int32)), _p(L), _dt(L),
+                               _p(_c(U, np.uint16)), _p(_c(W, np.uint16)), U.shape[1], R, g, V, _p(label))
+    return dict(label=label, flags=flags)
+
+
+def observe(conf, cu_seqlens, ceiling, cls, n_class, n_bins):
+    """Verify-cycle statistics (see orc_observe)."""
+    R, g = conf.shape
+    hist = np.zeros((n_class, g + 1), np.int32)
+    reached = np.zeros((n_class, g), np.int32)
+    hits = np.zeros((n_class, g), np.int32)
+    bin_n = np.zeros(n_bins, np.int32)
+    bin_hit = np.zeros(n_bins, np.int32)
+    bin_conf = np.zeros(n_bins, np.float64)
+    ece = np.zeros(1, np.float64)
+    rc = lib().orc_observe(_p(_c(conf, np.float32)), _p(_c(cu_seqlens, np.int32)), _p(_c(ceiling, np.int32)),
+                           _p(_c(cls, np.int32)), R, g, n_class, n_bins, _p(hist), _p(reached), _p(hits),
+                           _p(bin_n), _p(bin_hit), _p(bin_conf), _p(ece))
+    if rc != 0:
+        raise ValueError("class id out of range")
+    return dict(hist=hist, reached=reached, hits=hits, bin_n=bin_n, bin_hit=bin_hit, bin_conf=bin_conf,
+                ece=float(ece[0]))

@@ -672,3 +672,106 @@ int orc_verify_tree(const void* target, int dtT, const int32_t* tok, const int32
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Observability: the confidence head's soft label and the per-cycle    */
+/* statistics of verification ([DSpark notes] sec. 5.1, sec. 8.1;        */
+/* [SGLang] "observability").                                            */
+/* ------------------------------------------------------------------ */
+
+/* label[i, p] = sum_v min(q_v, p_v) = 1 - TV(q, p) for window row p < w_i,
+ * the chance that one token drafted from q survives the accept test against
+ * p ([DSpark notes] sec. 5.1: the soft acceptance label).  q is the draft's
+ * distribution at position p+1, softmax((L[i, p] + Markov(y_p)) / T) with
+ * y_0 the anchor, its log-sum-exp computed here in double; p is softmax of
+ * target row cu[i] + p over T.  Rows outside the window get -1. */
+int orc_tv_label(double temperature, const void* target, int dtT, const int32_t* cu_seqlens,
+                 const int32_t* anchor, const int32_t* draft, const void* L, int dtL,
+                 const uint16_t* U, const uint16_t* W, int r, int R, int gamma, int V, double* label) {
+    int flags = 0;
+    double inv_t = 1.0 / temperature;
+    double* M = (double*)malloc(sizeof(double) * (size_t)V);
+    float* z = (float*)malloc(sizeof(float) * (size_t)V);
+    for (int i = 0; i < R; ++i) {
+        int w = cu_seqlens[i + 1] - cu_seqlens[i] - 1;
+        for (int p = 0; p < gamma; ++p) {
+            double* out = label + (size_t)i * gamma + (size_t)p;
+            if (p >= w) {
+                *out = -1.0;
+                continue;
+            }
+            int prev = p == 0 ? anchor[i] : draft[(size_t)i * gamma + (size_t)(p - 1)];
+            if (markov_row(U, W, prev, r, V, M)) flags |= ORC_FLAG_INEXACT_MARKOV;
+            combine_logits(L, dtL, ((size_t)i * gamma + (size_t)p) * V, M, V, z);
+            double lq = logsumexp_scaled(z, V, inv_t);
+            size_t trow = (size_t)cu_seqlens[i] + (size_t)p;
+            double lp = row_lse(target, dtT, trow, V, inv_t);
+            double s = 0.0;
+            for (int v = 0; v < V; ++v) {
+                double qv = exp((double)z[v] * inv_t - lq);
+                double pv = exp((double)load_elem(target, dtT, trow * (size_t)V + (size_t)v) * inv_t - lp);
+                s += qv < pv ? qv : pv;
+            }
+            *out = s;
+        }
+    }
+    free(M);
+    free(z);
+    return flags;
+}
+
+/* Statistics of one verify cycle.  Position d = 1..gamma of request i is
+ * observed when every earlier draft was accepted and d was verified:
+ * d <= min(ceiling_i + 1, w_i); its outcome is hit = (d <= ceiling_i)
+ * ([DSpark notes] sec. 8.1 counts position d only where 1..d-1 were all
+ * accepted).  ceiling_i is the acceptance count of the whole verified window
+ * (cap-accept's ceiling; in the other modes the accepted count).
+ *   hist[c, k]      requests of class c whose ceiling is k (k = 0..gamma)
+ *   reached[c, d-1] observed positions d of class c; hits[c, d-1] their hits
+ *   calibration: confidence c clamped to [0, 1] (NaN as 0) falls in bin
+ *   floor(c * n_bins) (fp32 product), the top bin taking c = 1;
+ *   bin_n, bin_hit count observations and hits, bin_conf sums c;
+ *   ece = sum_b |bin_hit_b - bin_conf_b| / N, N = sum_b bin_n_b (0 if N = 0),
+ *   the expected calibration error with equal-width bins.
+ * Returns -1 when a class id is out of range, else 0. */
+int orc_observe(const float* conf, const int32_t* cu_seqlens, const int32_t* ceiling, const int32_t* cls,
+                int R, int gamma, int n_class, int n_bins,
+                int32_t* hist, int32_t* reached, int32_t* hits,
+                int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece) {
+    for (int k = 0; k < n_class * (gamma + 1); ++k) hist[k] = 0;
+    for (int k = 0; k < n_class * gamma; ++k) reached[k] = hits[k] = 0;
+    for (int b = 0; b < n_bins; ++b) {
+        bin_n[b] = bin_hit[b] = 0;
+        bin_conf[b] = 0.0;
+    }
+    for (int i = 0; i < R; ++i) {
+        int c = cls[i];
+        if (c < 0 || c >= n_class) return -1;
+        int w = cu_seqlens[i + 1] - cu_seqlens[i] - 1;
+        int A = ceiling[i];
+        hist[(size_t)c * (gamma + 1) + (size_t)A] += 1;
+        int last = A + 1 < w ? A + 1 : w;
+        for (int d = 1; d <= last; ++d) {
+            int hit = d <= A;
+            reached[(size_t)c * gamma + (size_t)(d - 1)] += 1;
+            hits[(size_t)c * gamma + (size_t)(d - 1)] += hit;
+            float x = conf[(size_t)i * gamma + (size_t)(d - 1)];
+            if (!(x > 0.0f)) x = 0.0f;
+            if (x > 1.0f) x = 1.0f;
+            float scaled = x * (float)n_bins;
+            int b = (int)floorf(scaled);
+            if (b > n_bins - 1) b = n_bins - 1;
+            bin_n[b] += 1;
+            bin_hit[b] += hit;
+            bin_conf[b] += (double)x;
+        }
+    }
+    long n = 0;
+    double e = 0.0;
+    for (int b = 0; b < n_bins; ++b) {
+        n += bin_n[b];
+        e += fabs((double)bin_hit[b] - bin_conf[b]);
+    }
+    *ece = n > 0 ? e / (double)n : 0.0;
+    return 0;
+}

@@ -106,6 +106,21 @@ int orc_verify_tree(const void* target, int dtT, const int32_t* tok, const int32
                     const int32_t* n_nodes, int R, int N, int B, int V,
                     int32_t* accept, int32_t* out_tok, int32_t* n_out);
 
+/* The confidence head's soft label 1 - TV(q, p) = sum_v min(q_v, p_v) for
+ * every verified window row (label [R, gamma], -1 outside the window); q is
+ * the draft's distribution at that position, p the target row's. */
+int orc_tv_label(double temperature, const void* target, int dtT, const int32_t* cu_seqlens,
+                 const int32_t* anchor, const int32_t* draft, const void* L, int dtL,
+                 const uint16_t* U, const uint16_t* W, int r, int R, int gamma, int V, double* label);
+
+/* Verify-cycle statistics: ceiling histogram per class [n_class, gamma+1],
+ * per-position observed / accepted counts [n_class, gamma], equal-width
+ * calibration bins of the confidences and their expected calibration error. */
+int orc_observe(const float* conf, const int32_t* cu_seqlens, const int32_t* ceiling, const int32_t* cls,
+                int R, int gamma, int n_class, int n_bins,
+                int32_t* hist, int32_t* reached, int32_t* hits,
+                int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece);
+
 #ifdef __cplusplus
 }
 #endif

@@ -729,3 +729,135 @@ def test_tree_verify_walks_longest_accepted_path():
     vc = oracle.verify(oracle.STATIC, oracle.GREEDY, np_of(tgt.reshape(-1, w.V)), cu, args[3], tr["tok"][:, 1:])
     np.testing.assert_array_equal(vt["accept"], vc["accept"])
     np.testing.assert_array_equal(vt["out_tok"], vc["out_tok"])
+
+
+# ---------------------------------------------------------------------------
+# observability: the soft label 1 - TV(q, p) and the verify-cycle statistics
+# ---------------------------------------------------------------------------
+def test_tv_label_is_the_first_accept_probability():
+    """Rejection sampling accepts y_1 ~ q_1 with probability sum_v min(q, p)
+    ([DSpark notes] sec. 5.1, the soft label); position 2 is accepted, given
+    y_1 was, with the label of row 1 along that y_1.  Both are checked
+    against the accept frequencies of the oracle's own verify."""
+    n, V, B = 1 << 15, 8, 3
+    w = small(R=n, B=B, V=V, r=4, sigma=(0.9,), l_std=1.0, temperature=1.3)
+    base = _inputs(small(R=1, B=B, V=V, r=4, sigma=(0.9,), l_std=1.0, temperature=1.3), seed=4)
+    inp = {k: (v.expand(n, *v.shape[1:]).contiguous() if k in ("L", "L_bonus", "eta", "anchor") else v)
+           for k, v in base.items()}
+    anchor = np.full(n, int(base["anchor"][0]), np.int32)
+    dr, tgt, vr = _sample_cycle(w, inp, anchor, seed=21, cycle=0)
+    cu = np.arange(n + 1, dtype=np.int32) * (B + 1)
+    lab = oracle.tv_label(np_of(tgt.reshape(n * (B + 1), -1)), cu, anchor, dr["tokens"], np_of(inp["L"]),
+                          np_of(inp["U"]), np_of(inp["W"]), temperature=w.temperature)["label"]
+    l0 = lab[0, 0]
+    assert np.all(lab[:, 0] == l0) and 0.05 < l0 < 0.95
+    f0 = np.mean(vr["accept"] >= 1)
+    assert abs(f0 - l0) < 4.5 * math.sqrt(l0 * (1 - l0) / n)
+    ok = vr["accept"] >= 1
+    m = int(ok.sum())
+    f1 = np.mean(vr["accept"][ok] >= 2)
+    e1 = lab[ok, 1].mean()
+    assert abs(f1 - e1) < 4.5 * math.sqrt(e1 * (1 - e1) / m)
+
+
+def test_tv_label_two_token_closed_form_and_equal_rows():
+    """V = 2: sum_v min(q_v, p_v) = 1 - |q_0 - p_0|; a target row equal to the
+    draft's logits (no noise) gives 1; rows outside the window get -1."""
+    w = small(R=6, B=4, V=2, r=4, sigma=(1.3,), l_std=1.2, temperature=0.7)
+    inp = _inputs(w, seed=9)
+    an = np_of(inp["anchor"])
+    L, U, W = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"])
+    toks = np.random.default_rng(3).integers(0, 2, size=(w.R, w.B)).astype(np.int32)
+    tgt = synthetic.chain_target(inp, torch.as_tensor(toks), w.target_dtype)
+    win = np.array([4, 0, 2, 4, 1, 3])
+    cu = np.zeros(w.R + 1, np.int32)
+    rows = []
+    for i in range(w.R):
+        cu[i + 1] = cu[i] + win[i] + 1
+        rows.append(np_of(tgt[i, : win[i] + 1]))
+    packed = np.concatenate(rows)
+    lab = oracle.tv_label(packed, cu, an, toks, L, U, W, temperature=w.temperature)["label"]
+    u = torch.from_numpy(U.view(np.int16)).view(torch.bfloat16).double().numpy()
+    wm = torch.from_numpy(W.view(np.int16)).view(torch.bfloat16).double().numpy()
+    for i in range(w.R):
+        for p in range(w.B):
+            if p >= win[i]:
+                assert lab[i, p] == -1.0
+                continue
+            prev = an[i] if p == 0 else toks[i, p - 1]
+            z = (L[i, p].astype(np.float32) + (u[prev] @ wm).astype(np.float32)).astype(np.float64) / w.temperature
+            q0 = 1.0 / (1.0 + math.exp(z[1] - z[0]))
+            t = tgt[i, p].double().numpy() / w.temperature
+            p0 = 1.0 / (1.0 + math.exp(t[1] - t[0]))
+            assert abs(lab[i, p] - (1.0 - abs(q0 - p0))) < 1e-12
+    # no target noise: p = q on every row
+    w0 = small(R=3, B=3, V=40, r=8, sigma=(0.0,), l_std=1.0)
+    inp0 = _inputs(w0, seed=2)
+    toks0 = np.random.default_rng(4).integers(0, 40, size=(3, 3)).astype(np.int32)
+    t0 = synthetic.chain_target(inp0, torch.as_tensor(toks0), w0.target_dtype)
+    cu0 = np.arange(4, dtype=np.int32) * 4
+    lab0 = oracle.tv_label(np_of(t0.reshape(12, -1)), cu0, np_of(inp0["anchor"]), toks0, np_of(inp0["L"]),
+                           np_of(inp0["U"]), np_of(inp0["W"]), temperature=w0.temperature)["label"]
+    np.testing.assert_allclose(lab0, 1.0, atol=1e-12)
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def test_observe_worked_example():
+    g = _load("observe_worked_example.json")
+    out = oracle.observe(np.array(g["conf"], np.float32), np.array(g["cu_seqlens"]), np.array(g["ceiling"]),
+                         np.array(g["cls"]), g["n_class"], g["n_bins"])
+    e = g["expected"]
+    for k in ("hist", "reached", "hits", "bin_n", "bin_hit"):
+        np.testing.assert_array_equal(out[k], np.array(e[k]), err_msg=k)
+    np.testing.assert_allclose(out["bin_conf"], e["bin_conf"], atol=1e-6)
+    assert abs(out["ece"] - e["ece"]) < 1e-6
+
+
+def test_observe_single_bin_edges_and_counts():
+    """One bin: ECE = |hits - sum conf| / N.  Confidence 1 and above fall in
+    the top bin, NaN and negatives in bin 0 as 0.  With full windows the
+    count reaching d+1 is the count of hits at d, and every class's
+    histogram sums to its requests."""
+    rng = np.random.default_rng(11)
+    R, g, nc = 300, 6, 3
+    conf = rng.random((R, g)).astype(np.float32)
+    conf[0, 0], conf[1, 0], conf[2, 0], conf[3, 0] = 1.0, np.nan, 1.7, -0.2
+    ceiling = rng.integers(0, g + 1, R).astype(np.int32)
+    ceiling[:4] = 0
+    cls = rng.integers(0, nc, R).astype(np.int32)
+    cu = np.arange(R + 1, dtype=np.int32) * (g + 1)
+    one = oracle.observe(conf, cu, ceiling, cls, nc, 1)
+    N = one["bin_n"][0]
+    assert N == one["reached"].sum() and one["bin_hit"][0] == one["hits"].sum()
+    x = np.nan_to_num(conf, nan=0.0).clip(0, 1)
+    obs = [(x[i, d - 1], d <= ceiling[i]) for i in range(R) for d in range(1, min(ceiling[i] + 1, g) + 1)]
+    assert len(obs) == N
+    assert abs(one["ece"] - abs(sum(h for _, h in obs) - sum(float(c) for c, _ in obs)) / N) < 1e-12
+    ten = oracle.observe(conf, cu, ceiling, cls, nc, 10)
+    assert ten["bin_n"][9] >= 2 and ten["bin_n"][0] >= 2                  # 1.0 and 1.7 on top; NaN, -0.2 at 0
+    np.testing.assert_array_equal(ten["reached"][:, 1:], ten["hits"][:, :-1])
+    np.testing.assert_array_equal(ten["hist"].sum(1), np.bincount(cls, minlength=nc))
+    with pytest.raises(ValueError):
+        oracle.observe(conf, cu, ceiling, np.full(R, nc, np.int32), nc, 4)
+
+
+def test_observe_calibrated_confidence_has_small_ece():
+    """Confidences equal to the true conditional accept probabilities (the
+    soft labels) are calibrated against the observed outcomes; cubing them
+    is not."""
+    n, V, B = 1 << 13, 6, 3
+    w = small(R=n, B=B, V=V, r=4, sigma=(1.0,), l_std=1.0)
+    inp = _inputs(w, seed=12)
+    an = np_of(inp["anchor"])
+    dr, tgt, vr = _sample_cycle(w, inp, an, seed=5, cycle=0)
+    cu = np.arange(n + 1, dtype=np.int32) * (B + 1)
+    lab = oracle.tv_label(np_of(tgt.reshape(n * (B + 1), -1)), cu, an, dr["tokens"], np_of(inp["L"]),
+                          np_of(inp["U"]), np_of(inp["W"]), temperature=w.temperature)["label"]
+    cls = np.zeros(n, np.int32)
+    good = oracle.observe(lab.astype(np.float32), cu, vr["ceiling"], cls, 1, 10)
+    bad = oracle.observe((lab ** 3).astype(np.float32), cu, vr["ceiling"], cls, 1, 10)
+    assert good["ece"] < 0.02 < 0.1 < bad["ece"]
