@@ -75,7 +75,8 @@ enum {
     SDM_DEV_TIER_UNCAPTURED = 2,  /* packed total above every tier: tier = total */
     SDM_DEV_TIMEOUT = 4,          /* a bounded pipeline wait ran out */
     SDM_DEV_BAD_WINDOW = 8,       /* budget or cu_seqlens window outside [0, gamma] */
-    SDM_DEV_CAPACITY = 16         /* packed rows would exceed the given capacity */
+    SDM_DEV_CAPACITY = 16,        /* packed rows would exceed the given capacity */
+    SDM_DEV_BAD_CLASS = 32        /* a request class id outside [0, n_class) */
 };
 
 /* Philox key material: key = seed, counter word 3 = cycle. */
@@ -91,12 +92,13 @@ enum {
     SDM_OP_SCHEDULE = 2,
     SDM_OP_PACK = 3,
     SDM_OP_VERIFY = 4,
-    SDM_OP_VERIFY_TREE = 5
+    SDM_OP_VERIFY_TREE = 5,
+    SDM_OP_TV_LABEL = 6
 };
 
 /* Bytes of scratch the operation needs for these sizes (0 if none).  Pass the
- * same sizes as the call; unused sizes may be 0.  For SDM_OP_VERIFY pass the
- * packed row capacity as P. */
+ * same sizes as the call; unused sizes may be 0.  For SDM_OP_VERIFY and
+ * SDM_OP_TV_LABEL pass the packed row capacity as P. */
 size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int N);
 
 /*
@@ -336,6 +338,67 @@ const char* sdm_status_str(sdm_status status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int sdm_version(void);
+
+/*
+ * tv_label: the confidence head's soft label for every verified draft position
+ * ([DSpark notes] sec. 5.1: the label is the single-token acceptance rate,
+ * fixed by the total-variation distance between the draft and target
+ * distributions):
+ *     label[i, p] = sum_v min(q_v, p_v) = 1 - TV(q, p)         for p < w_i
+ * with q = softmax((L[i, p] + U[y_p] . W) / T) the draft's distribution at
+ * position p+1 (y_0 = anchor[i], y_p = draft[i, p-1]) and p = softmax(target
+ * row cu[i] + p / T); w_i = cu[i+1] - cu[i] - 1.  label[i, p] = -1 for
+ * p >= w_i.
+ * In:  target [row_capacity, V] (dtT, the packed verify rows), cu_seqlens
+ *      [R+1], anchor [R], draft [R, gamma]; lse_q [R, gamma] fp32 = the
+ *      draft's log-sum-exp of (L + Markov) / T, as sampling drafts return it,
+ *      or NULL: computed here by one more pass over L; L [R, gamma, V] (dtL),
+ *      U [V, r], W [r, V] bf16, r in {64, 128, 192, 256}; temperature > 0 (1
+ *      for greedy drafts).  target, L, U, W 16-byte aligned; V % 8 == 0;
+ *      R gamma <= 2^22.
+ * Out: label [R, gamma] fp32 (device).  Arithmetic in fp32 (exp, sums over
+ *      16-column blocks, then over the vocabulary splits in a fixed order).
+ * ws:  sdm_workspace_size(SDM_OP_TV_LABEL, R, gamma, V, r, row_capacity, 0, 0).
+ * Device checks (OR-ed into *dev_status, the row keeps label -1): windows
+ * outside [0, gamma] SDM_DEV_BAD_WINDOW, target rows past row_capacity
+ * SDM_DEV_CAPACITY, previous tokens outside [0, V) SDM_DEV_BAD_TOKEN.
+ */
+sdm_status sdm_tv_label(float temperature, const void* target, sdm_dtype dtT, int row_capacity,
+                        const int32_t* cu_seqlens, const int32_t* anchor, const int32_t* draft, const float* lse_q,
+                        const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, int r, int R, int gamma,
+                        int V, float* label, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * observe: statistics of one verify cycle for offline analysis ([SGLang]
+ * "observability": the acceptance ceiling that cap-accept exposes, the
+ * per-request confidences and calibration metrics such as ECE; [DSpark
+ * notes] sec. 8.1: position d counts only where positions 1..d-1 were all
+ * accepted).  Position d = 1..gamma of request i is observed when
+ * d <= min(A_i + 1, w_i), A_i = ceiling[i], w_i = cu[i+1] - cu[i] - 1; its
+ * outcome is hit = (d <= A_i).
+ * In:  conf [R, gamma] fp32 (the confidences the scheduler ranked),
+ *      cu_seqlens [R+1] of the verify, ceiling [R] (sdm_verify's ceiling: the
+ *      acceptance count of the whole verified window), cls [R] class ids in
+ *      [0, n_class), n_bins >= 1.
+ * Out (device): hist [n_class, gamma+1] int32: requests per class and
+ *      ceiling; reached, hits [n_class, gamma] int32: observed positions and
+ *      their hits per class and position; bin_n, bin_hit [n_bins] int32 and
+ *      bin_conf [n_bins] fp64: per equal-width bin the observations, hits and
+ *      the sum of the confidences (c clamped to [0, 1], NaN as 0, in bin
+ *      floor(c n_bins) of an fp32 product, c = 1 in the top bin); ece [1]
+ *      fp64 = sum_b |bin_hit_b - bin_conf_b| / N, N = sum_b bin_n_b (0 when
+ *      N = 0).  bin_conf is summed by atomic adds: its last bits may differ
+ *      between runs; the counts are exact.
+ * Limits: 4 n_class (3 gamma + 1) + 16 n_bins <= 49152 bytes, else
+ *      SDM_ERR_UNSUPPORTED.
+ * Device checks: a class id outside [0, n_class) sets SDM_DEV_BAD_CLASS and
+ * the request is skipped; a window outside [0, gamma] or a ceiling outside
+ * [0, w_i] sets SDM_DEV_BAD_WINDOW and is clamped.
+ */
+sdm_status sdm_observe(const float* conf, const int32_t* cu_seqlens, const int32_t* ceiling, const int32_t* cls, int R,
+                       int gamma, int n_class, int n_bins, int32_t* hist, int32_t* reached, int32_t* hits,
+                       int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece, int32_t* dev_status,
+                       void* stream);
 
 #ifdef __cplusplus
 }

@@ -20,12 +20,13 @@ LIB_PATH = os.path.join(HERE, "libsdm.so")
 BF16, FP32 = 0, 1
 GREEDY, SAMPLE = 0, 1
 STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
-OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE = range(6)
-DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY = 1, 2, 4, 8, 16
+OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE, OP_TV_LABEL = range(7)
+DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY, DEV_BAD_CLASS = 1, 2, 4, 8, 16, 32
 
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
-           "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_status_str", "sdm_version")
+           "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_status_str",
+           "sdm_version")
 
 
 class SdmRng(ctypes.Structure):
@@ -63,6 +64,11 @@ def _declare(lib):
                                _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_verify_greedy_static.restype = _I
     lib.sdm_verify_greedy_static.argtypes = [_I, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]
+    lib.sdm_tv_label.restype = _I
+    lib.sdm_tv_label.argtypes = [_F, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _VP, _VP,
+                                 _SZ, _VP, _VP]
+    lib.sdm_observe.restype = _I
+    lib.sdm_observe.argtypes = [_VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_verify_tree.restype = _I
     lib.sdm_verify_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
 
@@ -275,6 +281,51 @@ def verify(mode, decode, target, cu_seqlens, anchor, draft, budget=None, logq=No
                           _ptr(out["accept"]), _ptr(out["ceiling"]), _ptr(out["out_tok"]), _ptr(out["n_out"]),
                           _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
     _check(st, "sdm_verify")
+    out["dev_status"] = dev_status
+    return out
+
+
+def tv_label(target, cu_seqlens, anchor, draft, L, U, W, lse_q=None, temperature=1.0, out=None, ws=None,
+             dev_status=None):
+    """Soft label 1 - TV(q, p) [R, gamma] of every verified window row (-1
+    past the window).  target holds the packed verify rows; lse_q (the
+    sampling draft's log-sum-exp) may be None."""
+    _need_cuda(target, cu_seqlens, anchor, draft, L, U, W, lse_q)
+    R, g = draft.shape
+    V = target.shape[-1]
+    rows = target.numel() // V
+    dev = target.device
+    r = U.shape[1]
+    if out is None:
+        out = torch.empty((R, g), dtype=torch.float32, device=dev)
+    ws = workspace(OP_TV_LABEL, R, g, V, r, rows, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_tv_label(float(temperature), _ptr(target), _dt(target), rows, _ptr(cu_seqlens), _ptr(anchor),
+                            _ptr(draft), _ptr(lse_q), _ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), r, R, g, V,
+                            _ptr(out), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_tv_label")
+    return out
+
+
+def observe(conf, cu_seqlens, ceiling, cls, n_class, n_bins, out=None, dev_status=None):
+    """Verify-cycle statistics: ceiling histograms per class, per-position
+    observed / accepted counts, calibration bins and their ECE."""
+    _need_cuda(conf, cu_seqlens, ceiling, cls)
+    R, g = conf.shape
+    dev = conf.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    if out is None:
+        out = dict(hist=torch.empty((n_class, g + 1), **i32), reached=torch.empty((n_class, g), **i32),
+                   hits=torch.empty((n_class, g), **i32), bin_n=torch.empty((n_bins,), **i32),
+                   bin_hit=torch.empty((n_bins,), **i32),
+                   bin_conf=torch.empty((n_bins,), dtype=torch.float64, device=dev),
+                   ece=torch.empty((1,), dtype=torch.float64, device=dev))
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_observe(_ptr(conf), _ptr(cu_seqlens), _ptr(ceiling), _ptr(cls), R, g, n_class, n_bins,
+                           _ptr(out["hist"]), _ptr(out["reached"]), _ptr(out["hits"]), _ptr(out["bin_n"]),
+                           _ptr(out["bin_hit"]), _ptr(out["bin_conf"]), _ptr(out["ece"]), _ptr(dev_status),
+                           _stream())
+    _check(st, "sdm_observe")
     out["dev_status"] = dev_status
     return out
 

@@ -121,6 +121,21 @@ size_t ws_verify(int R, int rows, int V) {
            6 * align256(static_cast<size_t>(R) * 4) + align256(static_cast<size_t>(R) * n_blocks16(V) * 8);
 }
 
+// soft label: target LSE partials, the row list, and one partial per listed
+// row, GEMM CTA column and column group
+int label_n_part(int R, int gamma, int V) {
+    const int rows = R * gamma;
+    const int gy = (rows + kTileM - 1) / kTileM;
+    return gemm_grid_x((V + kTileN - 1) / kTileN, gy) * kColGroups;
+}
+
+size_t ws_tv_label(int R, int gamma, int V, int row_capacity) {
+    const int nc = std::max(n_chunks_of(V, 0), n_chunks_of(V, 1));
+    const size_t slots = static_cast<size_t>(R) * gamma;
+    return align256(static_cast<size_t>(row_capacity) * nc * 8) + 6 * align256(slots * 4) +
+           align256(slots * label_n_part(R, gamma, V) * 8);
+}
+
 }  // namespace
 
 extern "C" {
@@ -133,6 +148,7 @@ size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int 
         case SDM_OP_DRAFT_CHAIN: return ws_chain(R, B, V);
         case SDM_OP_DRAFT_TREE: return ws_tree(R, B, P, V);
         case SDM_OP_VERIFY: return ws_verify(R, P, V);
+        case SDM_OP_TV_LABEL: return ws_tv_label(R, B, V, P);
         case SDM_OP_VERIFY_TREE:
             return align256(static_cast<size_t>(R) * (N + 1) * 8 * std::max(n_chunks_of(V, 0), n_chunks_of(V, 1)));
         default: return 0;
@@ -615,6 +631,108 @@ sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok
     SDM_CHECK_CUDA(launch_stream(STREAM_ARGMAX, sp, static_cast<int>(rows), s));
     SDM_CHECK_CUDA(launch_tree_verify_walk(row_keys, sp.n_chunks, tok, parent, n_nodes, R, N, B, V, accept, out_tok, n_out,
                                            dev_status, s));
+    return SDM_OK;
+}
+
+sdm_status sdm_tv_label(float temperature, const void* target, sdm_dtype dtT, int row_capacity,
+                        const int32_t* cu_seqlens, const int32_t* anchor, const int32_t* draft, const float* lse_q,
+                        const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, int r, int R, int gamma,
+                        int V, float* label, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!target || !cu_seqlens || !anchor || !draft || !L || !U || !W || !label) return SDM_ERR_INVALID_ARG;
+    if (R <= 0 || gamma <= 0 || V <= 0 || row_capacity <= 0 || !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
+    if ((dtT != SDM_BF16 && dtT != SDM_FP32) || (dtL != SDM_BF16 && dtL != SDM_FP32)) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(target) || !aligned16(L) || !aligned16(U) || !aligned16(W))
+        return SDM_ERR_UNSUPPORTED;
+    if (static_cast<long long>(R) * gamma > (1 << 22)) return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_tv_label(R, gamma, V, row_capacity)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int slots = R * gamma;
+    const int nchunk_max = std::max(n_chunks_of(V, 0), n_chunks_of(V, 1));
+    const int n_part = label_n_part(R, gamma, V);
+    Carver c{static_cast<uint8_t*>(ws)};
+    auto* lse_part = c.take<float2>(static_cast<size_t>(row_capacity) * nchunk_max);
+    int32_t* res_req = c.take<int32_t>(slots);
+    int32_t* res_pos = c.take<int32_t>(slots);
+    int32_t* res_tok = c.take<int32_t>(slots);
+    int32_t* res_trow = c.take<int32_t>(slots);
+    float* res_lse_p = c.take<float>(slots);
+    float* row_lse_q = c.take<float>(slots);
+    auto* part = c.take<float2>(static_cast<size_t>(slots) * n_part);
+
+    // log-sum-exp of every packed target row over T, in streaming partials
+    StreamParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.base = target;
+    sp.fp32 = dtT == SDM_FP32;
+    sp.V = V;
+    sp.chunk = sp.fp32 ? kChunkFp32 : kChunkBf16;
+    sp.n_chunks = n_chunks_of(V, sp.fp32);
+    sp.count = cu_seqlens + R;
+    sp.n_items = row_capacity;
+    sp.inv_t = 1.0f / temperature;
+    sp.part = lse_part;
+    SDM_CHECK_CUDA(launch_stream(STREAM_LSE, sp, row_capacity, s));
+    // every GEMM row unused until the row list names it
+    SDM_CHECK_CUDA(cudaMemsetAsync(res_tok, 0xFF, static_cast<size_t>(slots) * sizeof(int32_t), s));
+    SDM_CHECK_CUDA(launch_label_prep(cu_seqlens, anchor, draft, lse_q, lse_part, sp.n_chunks, R, gamma, V,
+                                     row_capacity, res_req, res_pos, res_tok, res_trow, res_lse_p, row_lse_q, label,
+                                     dev_status, s));
+    CUtensorMap tmW;
+    if (!map_w(&tmW, W, r, V)) return SDM_ERR_CUDA;
+    const int n_tiles = (V + kTileN - 1) / kTileN;
+    const int gy = (slots + kTileM - 1) / kTileM;
+    const int gx = gemm_grid_x(n_tiles, gy);
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = slots;
+    p.R = R;
+    p.B = gamma;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = n_tiles;
+    p.l_fp32 = dtL == SDM_FP32;
+    p.l_rows = 1;
+    p.P = 1;
+    p.k = 1;
+    p.d = 1;
+    p.inv_t = sp.inv_t;
+    p.U = U;
+    p.res_req = res_req;
+    p.res_tok = res_tok;
+    p.res_pos = res_pos;
+    p.res_trow = res_trow;
+    p.res_lse_p = res_lse_p;
+    p.row_lse_q = row_lse_q;
+    p.L = L;
+    p.target = target;
+    p.t_fp32 = sp.fp32;
+    p.gamma = gamma;
+    p.part = part;
+    p.n_part = n_part;
+    p.dev_status = dev_status;
+    if (!lse_q) {   // the draft's log-sum-exp, from one more pass over L
+        gemm_pick_stages(p, MODE_QLSE);
+        SDM_CHECK_CUDA(launch_markov_gemm(MODE_QLSE, tmW, tmW, p, gx, gy, s));
+        SDM_CHECK_CUDA(launch_label_lse_q(part, n_part, slots, res_tok, row_lse_q, s));
+    }
+    gemm_pick_stages(p, MODE_TVMIN);
+    SDM_CHECK_CUDA(launch_markov_gemm(MODE_TVMIN, tmW, tmW, p, gx, gy, s));
+    SDM_CHECK_CUDA(launch_label_finalize(part, n_part, slots, res_tok, res_req, res_pos, gamma, label, s));
+    return SDM_OK;
+}
+
+sdm_status sdm_observe(const float* conf, const int32_t* cu_seqlens, const int32_t* ceiling, const int32_t* cls, int R,
+                       int gamma, int n_class, int n_bins, int32_t* hist, int32_t* reached, int32_t* hits,
+                       int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece, int32_t* dev_status,
+                       void* stream) {
+    if (!conf || !cu_seqlens || !ceiling || !cls || !hist || !reached || !hits || !bin_n || !bin_hit || !bin_conf ||
+        !ece)
+        return SDM_ERR_INVALID_ARG;
+    if (R <= 0 || gamma <= 0 || n_class <= 0 || n_bins <= 0) return SDM_ERR_INVALID_ARG;
+    if (n_class > 4096 || n_bins > 4096 || gamma > 4096 || observe_smem_bytes(gamma, n_class, n_bins) > 49152)
+        return SDM_ERR_UNSUPPORTED;
+    SDM_CHECK_CUDA(launch_observe(conf, cu_seqlens, ceiling, cls, R, gamma, n_class, n_bins, hist, reached, hits,
+                                  bin_n, bin_hit, bin_conf, ece, dev_status, static_cast<cudaStream_t>(stream)));
     return SDM_OK;
 }
 

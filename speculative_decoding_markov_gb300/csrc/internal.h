@@ -41,10 +41,23 @@ constexpr int kEpiWarps = 4 * kColGroups;          // four TMEM sub-partitions x
 constexpr int kGemmThreads = 96 + 32 * kEpiWarps;  // warp 0 W loads, warp 1 MMA, warp 2 L loads, warps 3.. epilogue
 constexpr int kMaxTopK = 8;
 
-enum GemmMode { MODE_CHAIN_GREEDY = 0, MODE_CHAIN_SAMPLE = 1, MODE_TREE = 2, MODE_RESID = 3, MODE_ABSMAX = 4 };
+enum GemmMode {
+    MODE_CHAIN_GREEDY = 0,
+    MODE_CHAIN_SAMPLE = 1,
+    MODE_TREE = 2,
+    MODE_RESID = 3,
+    MODE_ABSMAX = 4,
+    MODE_QLSE = 5,    // soft label pass 1: log-sum-exp of the draft logits of listed rows
+    MODE_TVMIN = 6    // soft label pass 2: sum_v min(q_v, p_v) of listed rows
+};
 
-// Modes that stage a tile of L beside each W tile.
-__host__ __device__ constexpr bool mode_reads_l(int mode) { return mode != MODE_RESID && mode != MODE_ABSMAX; }
+// Modes that stage a tile of L beside each W tile (the others read their L
+// rows, if any, straight from global memory).
+__host__ __device__ constexpr bool mode_reads_l(int mode) {
+    return mode == MODE_CHAIN_GREEDY || mode == MODE_CHAIN_SAMPLE || mode == MODE_TREE;
+}
+// Modes whose GEMM rows come from an explicit row list (res_tok / res_req).
+__host__ __device__ constexpr bool mode_row_list(int mode) { return mode == MODE_QLSE || mode == MODE_TVMIN; }
 
 struct GemmParams {
     int rows;            // GEMM rows in use
@@ -78,6 +91,14 @@ struct GemmParams {
     const void* target;         // packed target rows
     int t_fp32;                 // target element type
     int gamma;
+    // soft label (row list): GEMM row g = window row res_pos[g] of request
+    // res_req[g] (previous token res_tok[g], -1: unused row; target row
+    // res_trow[g], target log-sum-exp res_lse_p[g], draft log-sum-exp
+    // row_lse_q[g]); one partial per row, CTA and column group in part
+    const int32_t* res_req;
+    const float* row_lse_q;
+    float2* part;               // [rows][n_part]
+    int n_part;                 // gridDim.x * kColGroups
     // absmax (prepared tables): GEMM row m = token m
     unsigned int* absmax_bits;      // [rows] max_v |U[m] . W[:, v]| as fp32 bits (atomic max)
     int32_t* dev_status;
@@ -99,8 +120,8 @@ struct StreamParams {
     int V;
     int chunk;              // elements per work item (multiple of 8)
     int n_chunks;           // chunks per row
-    int n_items;            // rows (items) when count == NULL
-    const int32_t* count;   // device item count (e.g. cu_seqlens + R), may be NULL
+    int n_items;            // rows (items) when count == NULL, else the rows the buffer holds
+    const int32_t* count;   // device item count (e.g. cu_seqlens + R), clamped to n_items; may be NULL
     const int32_t* row_of;  // item -> row index (NULL: identity; < 0: skip)
     float inv_t;
     unsigned long long* keys;   // ARGMAX: [n_items][n_chunks] partial keys
@@ -269,5 +290,24 @@ cudaError_t launch_markov_bounds(const unsigned int* absmax_bits, const float* u
                                  int r, float* c_bound, float* c_max, cudaStream_t s);
 
 int num_sms();
+
+// ---------------------------------------------------------------------------
+// Observability (observe.cu): the soft-label row list and reductions, and the
+// verify-cycle statistics
+// ---------------------------------------------------------------------------
+cudaError_t launch_label_prep(const int32_t* cu, const int32_t* anchor, const int32_t* draft, const float* lse_q,
+                              const float2* lse_part, int n_chunks, int R, int gamma, int V, int row_capacity,
+                              int32_t* res_req, int32_t* res_pos, int32_t* res_tok, int32_t* res_trow,
+                              float* res_lse_p, float* row_lse_q, float* label, int32_t* dev_status, cudaStream_t s);
+cudaError_t launch_label_lse_q(const float2* part, int n_part, int rows, const int32_t* res_tok, float* row_lse_q,
+                               cudaStream_t s);
+cudaError_t launch_label_finalize(const float2* part, int n_part, int rows, const int32_t* res_tok,
+                                  const int32_t* res_req, const int32_t* res_pos, int gamma, float* label,
+                                  cudaStream_t s);
+size_t observe_smem_bytes(int gamma, int n_class, int n_bins);
+cudaError_t launch_observe(const float* conf, const int32_t* cu, const int32_t* ceiling, const int32_t* cls, int R,
+                           int gamma, int n_class, int n_bins, int32_t* hist, int32_t* reached, int32_t* hits,
+                           int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece, int32_t* dev_status,
+                           cudaStream_t s);
 
 }  // namespace sdm

@@ -15,6 +15,11 @@
 //                      rejected position
 //   MODE_ABSMAX        max_v |U[m] . W[:, v]| for m = 0..V-1, no L (the
 //                      per-token bound of the pruned greedy chain)
+//   MODE_QLSE          log-sum-exp of z / T of listed (request, position)
+//                      rows, one partial (max, sum) per row, CTA and group
+//   MODE_TVMIN         sum_v min(q_v, p_v) of listed rows (the soft label
+//                      1 - TV, DSpark notes sec. 5.1), one partial sum per
+//                      row, CTA and column group
 //
 // Data path (one CTA = 128 GEMM rows x a contiguous range of 64-wide vocab
 // tiles, K = r):
@@ -92,6 +97,10 @@ __device__ __forceinline__ int gemm_row_token(const GemmParams& p, int grow) {
         if (t < 0) return -1;
     } else if (MODE == MODE_ABSMAX) {
         return grow < p.rows ? grow : -1;
+    } else if (mode_row_list(MODE)) {
+        if (grow >= p.rows) return -1;
+        t = p.res_tok[grow];
+        if (t < 0) return -1;
     } else {
         if (grow >= p.R) return -1;
         t = p.res_tok[grow];
@@ -336,6 +345,94 @@ struct Epi<MODE_RESID> {
         rec[vbase / C] = make_float2(0.f, (ps[0] + ps[1]) + (ps[2] + ps[3]));
     }
     __device__ __forceinline__ void flush(const GemmParams&, int) {}
+};
+
+// Listed row g: window row res_pos[g] of request res_req[g], its L row at
+// (request, position) and its target row res_trow[g].
+__device__ __forceinline__ bool list_row(const GemmParams& p, int grow, size_t& l_off, size_t& t_off) {
+    if (grow >= p.rows || p.res_tok[grow] < 0) return false;
+    const size_t req = static_cast<size_t>(p.res_req[grow]);
+    l_off = (req * p.gamma + static_cast<size_t>(p.res_pos[grow])) * static_cast<size_t>(p.V);
+    t_off = static_cast<size_t>(p.res_trow[grow]) * static_cast<size_t>(p.V);
+    return true;
+}
+
+__device__ __forceinline__ float2* part_slot(const GemmParams& p, int grow, int group) {
+    return p.part + static_cast<size_t>(grow) * p.n_part + blockIdx.x * kColGroups + group;
+}
+
+// Online (max, sum) of x = z log2(e) / T over every column this thread
+// consumes; the partial is (max x ln 2, sum 2^(x - max x)) = (max z / T, sum
+// exp(z / T - max)).  A thread that consumed nothing writes (-inf, 0).
+template <>
+struct Epi<MODE_QLSE> {
+    bool valid;
+    int group;
+    size_t l_off, t_off;
+    float sc, m, s;
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
+        valid = list_row(p, grow, l_off, t_off);
+        sc = p.inv_t * kLog2e;
+        m = -INFINITY;
+        s = 0.f;
+    }
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int vbase, int,
+                                            const uint32_t (&acc)[C]) {
+        if (!valid || vbase >= p.V) return;
+        float z[C];
+        load_g(p.L, p.l_fp32, l_off, vbase, p.V, z);
+#pragma unroll
+        for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * sc;
+        mask_tail(z, vbase, p.V);
+        const float mb = maxc(z);   // finite: column vbase < V
+        if (mb > m) {
+            s *= fast_exp2(m - mb);
+            m = mb;
+        }
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(z[j] - m);
+        s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    }
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
+        if (valid) *part_slot(p, grow, group) = make_float2(m * kLn2, s);
+    }
+};
+
+// Partial sum of min(q_v, p_v), q_v = exp(z / T - lse_q), p_v = exp(target /
+// T - lse_p), over every column this thread consumes.
+template <>
+struct Epi<MODE_TVMIN> {
+    bool valid;
+    int group;
+    size_t l_off, t_off;
+    float lse_q, lse_p, s;
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
+        valid = list_row(p, grow, l_off, t_off);
+        s = 0.f;
+        if (valid) {
+            lse_q = p.row_lse_q[grow];
+            lse_p = p.res_lse_p[grow];
+        }
+    }
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int vbase, int,
+                                            const uint32_t (&acc)[C]) {
+        if (!valid || vbase >= p.V) return;
+        float lv[C], tv[C];
+        load_g(p.L, p.l_fp32, l_off, vbase, p.V, lv);
+        load_g(p.target, p.t_fp32, t_off, vbase, p.V, tv);
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            const float q = __expf((lv[j] + __uint_as_float(acc[j])) * p.inv_t - lse_q);
+            const float pv = __expf(tv[j] * p.inv_t - lse_p);
+            ps[j & 3] += (vbase + j < p.V) ? fminf(pv, q) : 0.f;
+        }
+        s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    }
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
+        if (valid) *part_slot(p, grow, group) = make_float2(0.f, s);
+    }
 };
 
 template <>
@@ -647,6 +744,8 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
         case MODE_TREE: return launch_mode<MODE_TREE>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_RESID: return launch_mode<MODE_RESID>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_ABSMAX: return launch_mode<MODE_ABSMAX>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_QLSE: return launch_mode<MODE_QLSE>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TVMIN: return launch_mode<MODE_TVMIN>(tmW, tmL, p, grid_x, grid_y, s);
         default: return cudaErrorInvalidValue;
     }
 }

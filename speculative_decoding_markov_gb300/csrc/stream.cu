@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kThreads) row_stream_kernel(const StreamParams
     __shared__ float red_m[kThreads / 32], red_s[kThreads / 32];
     pdl_wait();
     pdl_trigger();
-    const int n_items = p.count ? *p.count : p.n_items;
+    const int n_items = p.count ? min(max(*p.count, 0), p.n_items) : p.n_items;   // never past the buffer
     const long long total = static_cast<long long>(n_items) * p.n_chunks;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 

@@ -120,3 +120,37 @@ def test_tree_and_verify_host_validation(lib):
     assert sd(FAKE, FAKE, 2000, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 2   # R * gamma > 8192
     assert lib.sdm_pack_ragged(FAKE, FAKE, None, 4, 7, None, 2, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None, None,
                                None) == 1       # tiers missing
+
+
+def test_observability_host_validation(lib):
+    # tv_label: workspace holds the target LSE partials, the row list and the GEMM partials
+    n = lib.sdm_workspace_size(binding.OP_TV_LABEL, 256, 16, 151936, 256, 4352, 0, 0)
+    assert n >= 4352 * 10 * 8 + 6 * 4096 * 4 + 4096 * 4 * 8
+    tv = lib.sdm_tv_label
+    a = [1.0, FAKE, 0, 64, FAKE, FAKE, FAKE, None, FAKE, 0, FAKE, FAKE, 64, 4, 7, 1024, FAKE, FAKE, 1 << 30, None, None]
+    bad = list(a)
+    bad[0] = 0.0                                # temperature must be positive
+    assert tv(*bad) == 1
+    bad = list(a)
+    bad[8] = None                               # L missing
+    assert tv(*bad) == 1
+    bad = list(a)
+    bad[15] = 1020                              # V % 8 != 0
+    assert tv(*bad) == 2
+    bad = list(a)
+    bad[12] = 96                                # r % 64 != 0
+    assert tv(*bad) == 2
+    bad = list(a)
+    bad[18] = 16                                # workspace too small
+    assert tv(*bad) == 5
+    ob = lib.sdm_observe
+    o = [FAKE, FAKE, FAKE, FAKE, 4, 7, 3, 10, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None]
+    bad = list(o)
+    bad[3] = None                               # class ids missing
+    assert ob(*bad) == 1
+    bad = list(o)
+    bad[7] = 0                                  # no bins
+    assert ob(*bad) == 1
+    bad = list(o)
+    bad[6], bad[5] = 1000, 16                   # counters beyond 48 KB of shared memory
+    assert ob(*bad) == 2
