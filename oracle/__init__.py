@@ -222,3 +222,23 @@ def observe(conf, cu_seqlens, ceiling, cls, n_class, n_bins):
         raise ValueError("class id out of range")
     return dict(hist=hist, reached=reached, hits=hits, bin_n=bin_n, bin_hit=bin_hit, bin_conf=bin_conf,
                 ece=float(ece[0]))
+
+
+def schedule_threshold(conf, tau):
+    R, g = conf.shape
+    budget = np.zeros(R, np.int32)
+    total = np.zeros(1, np.int32)
+    lib().orc_schedule_threshold(_p(_c(conf, np.float32)), R, g, ctypes.c_float(tau), _p(budget), _p(total))
+    return dict(budget=budget, total_tokens=int(total[0]))
+
+
+def threshold_sweep(conf, taus, ceiling=None):
+    R, g = conf.shape
+    taus = _c(taus, np.float32)
+    K = taus.size
+    drafts = np.zeros(K, np.int32)
+    accepted = np.zeros(K, np.int32)
+    expected = np.zeros(K, np.float64)
+    lib().orc_threshold_sweep(_p(_c(conf, np.float32)), _p(None if ceiling is None else _c(ceiling, np.int32)), R, g,
+                              _p(taus), K, _p(drafts), _p(accepted), _p(expected))
+    return dict(drafts=drafts, accepted=accepted, expected=expected)

@@ -775,3 +775,58 @@ int orc_observe(const float* conf, const int32_t* cu_seqlens, const int32_t* cei
     *ece = n > 0 ? e / (double)n : 0.0;
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* Fixed-threshold verify length and the threshold sweep                */
+/* ([DSpark notes] sec. 5.2: the conventional rule puts a fixed         */
+/* threshold on the confidences; sec. 8.3, Fig. 5: sweeping it,         */
+/* threshold 0 = verify the whole block)                                */
+/* ------------------------------------------------------------------ */
+
+/* n_i = the longest prefix of request i whose every confidence is >= tau
+ * (fp32 comparison; a NaN confidence ends the prefix). */
+static int threshold_len(const float* c, int gamma, float tau) {
+    int n = 0;
+    while (n < gamma && c[n] >= tau) ++n;
+    return n;
+}
+
+int orc_schedule_threshold(const float* conf, int R, int gamma, float tau, int32_t* budget, int32_t* total_tokens) {
+    int32_t total = R;   /* every request sends its root token */
+    for (int i = 0; i < R; ++i) {
+        budget[i] = threshold_len(conf + (size_t)i * gamma, gamma, tau);
+        total += budget[i];
+    }
+    *total_tokens = total;
+    return 0;
+}
+
+/* For every tau_k: drafts[k] = sum_i n_i(tau_k) verified drafts;
+ * accepted[k] = sum_i min(ceiling_i, n_i) (ceiling = what verifying the whole
+ * block accepts; -1 when ceiling is NULL); expected[k] = sum_i sum_{d <= n_i}
+ * S_{i,d}, the expected accepted drafts, with S_{i,d} the fp32 survival
+ * products.  The sum is exact: each S >= 2^-24 is a whole multiple of 2^-47
+ * and is added as an integer count of 2^-48; smaller survivals count 0. */
+int orc_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int gamma, const float* taus, int K,
+                        int32_t* drafts, int32_t* accepted, double* expected) {
+    const float tiny = 1.0f / 16777216.0f;   /* 2^-24 */
+    for (int k = 0; k < K; ++k) {
+        int32_t nd = 0, na = 0;
+        int64_t units = 0;                    /* multiples of 2^-48 */
+        for (int i = 0; i < R; ++i) {
+            const float* c = conf + (size_t)i * gamma;
+            int n = threshold_len(c, gamma, taus[k]);
+            float s = 1.0f;
+            for (int d = 0; d < n; ++d) {
+                s = s * c[d];
+                if (s >= tiny) units += (int64_t)ldexp((double)s, 48);
+            }
+            nd += n;
+            if (ceiling) na += ceiling[i] < n ? ceiling[i] : n;
+        }
+        drafts[k] = nd;
+        accepted[k] = ceiling ? na : -1;
+        expected[k] = ldexp((double)units, -48);
+    }
+    return 0;
+}

@@ -121,6 +121,16 @@ int orc_observe(const float* conf, const int32_t* cu_seqlens, const int32_t* cei
                 int32_t* hist, int32_t* reached, int32_t* hits,
                 int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece);
 
+/* Fixed-threshold verify length: n_i = the longest prefix with every
+ * confidence >= tau; total_tokens = R + sum n_i. */
+int orc_schedule_threshold(const float* conf, int R, int gamma, float tau, int32_t* budget, int32_t* total_tokens);
+
+/* Threshold sweep: per tau_k the verified drafts, the accepted drafts given
+ * the whole-block ceilings (ceiling may be NULL: accepted = -1) and the
+ * expected accepted drafts (exact sum of the survivals >= 2^-24). */
+int orc_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int gamma, const float* taus, int K,
+                        int32_t* drafts, int32_t* accepted, double* expected);
+
 #ifdef __cplusplus
 }
 #endif

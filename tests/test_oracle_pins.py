@@ -861,3 +861,77 @@ def test_observe_calibrated_confidence_has_small_ece():
     good = oracle.observe(lab.astype(np.float32), cu, vr["ceiling"], cls, 1, 10)
     bad = oracle.observe((lab ** 3).astype(np.float32), cu, vr["ceiling"], cls, 1, 10)
     assert good["ece"] < 0.02 < 0.1 < bad["ece"]
+
+
+# ---------------------------------------------------------------------------
+# fixed-threshold verify length and the threshold sweep
+# ---------------------------------------------------------------------------
+def test_threshold_worked_example():
+    g = _load("threshold_sweep_worked_example.json")
+    conf = np.array(g["conf"], np.float32)
+    out = oracle.threshold_sweep(conf, np.array(g["taus"], np.float32), np.array(g["ceiling"], np.int32))
+    e = g["expected"]
+    np.testing.assert_array_equal(out["drafts"], e["drafts"])
+    np.testing.assert_array_equal(out["accepted"], e["accepted"])
+    np.testing.assert_allclose(out["expected"], e["expected"], atol=1e-6)
+    one = oracle.schedule_threshold(conf, 0.5)
+    np.testing.assert_array_equal(one["budget"], e["budget_at_0.5"])
+    assert one["total_tokens"] == e["total_tokens_at_0.5"]
+    assert oracle.threshold_sweep(conf, [0.5])["accepted"][0] == -1       # no ceilings given
+
+
+def test_threshold_zero_verifies_the_whole_block_and_sweep_is_monotone():
+    """Threshold 0 is the fixed-length full verify (Fig. 5): every draft is
+    sent and what is accepted is the static verify's count; raising the
+    threshold never sends more drafts, and nothing above every confidence."""
+    w = small(R=30, B=6, V=64, r=16, sigma=(0.6, 1.6), class_mix="alternate")
+    inp = _inputs(w, seed=6)
+    an = np_of(inp["anchor"])
+    dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), an)
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    cu = np.arange(w.R + 1, dtype=np.int32) * (w.B + 1)
+    vr = oracle.verify(oracle.STATIC, oracle.GREEDY, np_of(tgt.reshape(w.R * (w.B + 1), -1)), cu, an, dr["tokens"])
+    conf = np_of(inp["conf"])
+    taus = np.linspace(0, 1, 21).astype(np.float32)
+    sw = oracle.threshold_sweep(conf, taus, vr["accept"])
+    assert sw["drafts"][0] == w.R * w.B and sw["accepted"][0] == vr["accept"].sum()
+    assert np.all(np.diff(sw["drafts"]) <= 0) and np.all(np.diff(sw["accepted"]) <= 0)
+    assert np.all(sw["accepted"] <= sw["drafts"]) and np.all(sw["expected"] <= sw["drafts"] + 1e-9)
+    top = oracle.threshold_sweep(conf, [np.nextafter(conf.max(), np.float32(2))], vr["accept"])
+    assert top["drafts"][0] == 0 and top["expected"][0] == 0.0
+    # the single-threshold budgets are the sweep's lengths, and compact
+    # verification with them commits min(ceiling, n) drafts
+    for tau in (0.3, 0.6):
+        b = oracle.schedule_threshold(conf, tau)["budget"]
+        assert b.sum() == oracle.threshold_sweep(conf, [tau])["drafts"][0]
+        pk = oracle.pack_ragged(an, dr["tokens"], b, np.array(w.tiers, np.int32))
+        packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"]))
+        vc = oracle.verify(oracle.COMPACT, oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an, dr["tokens"])
+        np.testing.assert_array_equal(vc["accept"], np.minimum(vr["accept"], b))
+
+
+def test_threshold_expected_matches_rejection_sampling():
+    """With each confidence the true accept probability of its drafted token,
+    min(1, p(y)/q(y)), the survivals are the chances of accepting every draft
+    up to d, so the expected accepted drafts at threshold 0 match what the
+    oracle's rejection-sampling verify accepts (CLT bound from the exact
+    variance of the accepted count)."""
+    n, V, B = 1 << 13, 8, 4
+    w = small(R=n, B=B, V=V, r=4, sigma=(0.8,), l_std=1.0)
+    base = _inputs(small(R=1, B=B, V=V, r=4, sigma=(0.8,), l_std=1.0), seed=14)
+    inp = {k: (v.expand(n, *v.shape[1:]).contiguous() if k in ("L", "L_bonus", "eta", "anchor") else v)
+           for k, v in base.items()}
+    anchor = np.full(n, int(base["anchor"][0]), np.int32)
+    dr, tgt, vr = _sample_cycle(w, inp, anchor, seed=8, cycle=2)
+    lp = torch.log_softmax(tgt[:, :B].double() / w.temperature, -1)
+    lp_y = lp.gather(-1, torch.as_tensor(dr["tokens"]).long().unsqueeze(-1)).squeeze(-1).numpy()
+    conf = np.minimum(1.0, np.exp(lp_y - dr["logq"])).astype(np.float32)
+    sw = oracle.threshold_sweep(conf, [0.0], vr["ceiling"])
+    S = np.cumprod(conf.astype(np.float64), axis=1)
+    var = 0.0
+    for i in range(n):      # A = sum_d 1[first d accepted]; E[1_d 1_e] = S_max(d, e)
+        s = S[i]
+        m2 = sum(s[max(d, e)] for d in range(B) for e in range(B))
+        var += m2 - s.sum() ** 2
+    assert abs(sw["accepted"][0] - sw["expected"][0]) < 4.5 * math.sqrt(var)
+    assert abs(sw["expected"][0] - S.sum()) < 1e-6 * S.sum()
