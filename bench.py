@@ -44,10 +44,18 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target length of the oracle sample")
-    ap.add_argument("--scheduler", default="budget", choices=["budget", "dynamic"],
-                    help="budget: the early-stopping scheduler on the additive table; dynamic: the production "
+    ap.add_argument("--scheduler", default="budget", choices=["budget", "dynamic", "threshold"],
+                    help="threshold: the conventional fixed confidence threshold (--tau); "
+                         "budget: the early-stopping scheduler on the additive table; dynamic: the production "
                          "scheduler (capacity from the confidences of two steps before, global search over the "
                          "tier-stepped table)")
+    ap.add_argument("--tau", type=float, default=0.5, help="confidence threshold of --scheduler threshold")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="run the workload with this many requests instead (smaller cases for profiler captures)")
+    ap.add_argument("--observe", action="store_true",
+                    help="add the fused observability pass to every verify: the soft label 1 - TV(q, p) of every "
+                         "verified row and the cycle statistics (ceiling histograms per class, per-position accept "
+                         "counts, calibration bins and ECE)")
     return ap.parse_args()
 
 
@@ -167,7 +175,7 @@ class ClockSampler:
 class Cycle:
     """Preallocated buffers and the launch sequence of one decode cycle."""
 
-    def __init__(self, w, seed, device, dynamic=False):
+    def __init__(self, w, seed, device, dynamic=False, observe=False, tau=None):
         import torch
 
         from speculative_decoding_markov_gb300 import binding as sdm
@@ -181,6 +189,8 @@ class Cycle:
         self.sample = w.decode == "sample"
         self.tree = w.decode == "tree"
         self.dynamic = dynamic
+        self.tau = tau
+        self.obs = observe and not self.tree
         i32 = dict(dtype=torch.int32, device=device)
         self.status = sdm.new_status(device)
         self.side = torch.cuda.Stream(device=device)
@@ -205,6 +215,18 @@ class Cycle:
                        out_tok=torch.empty((R, B + 1), **i32), n_out=torch.empty((R,), **i32))
         self.ws_draft = sdm.workspace(sdm.OP_DRAFT_CHAIN, R, B, V, r, device=device)
         self.ws_verify = sdm.workspace(sdm.OP_VERIFY, R, B, V, r, cap, device=device)
+        if self.obs:
+            self.n_class, self.n_bins = len(w.sigma), 10
+            self.cls = synthetic.request_class(w, seed).to(torch.int32).to(device)
+            self.label = torch.empty((R, B), dtype=torch.float32, device=device)
+            self.ws_label = sdm.workspace(sdm.OP_TV_LABEL, R, B, V, r, cap, device=device)
+            nc, nb = self.n_class, self.n_bins
+            self.st = dict(hist=torch.empty((nc, B + 1), **i32), reached=torch.empty((nc, B), **i32),
+                           hits=torch.empty((nc, B), **i32), bin_n=torch.empty((nb,), **i32),
+                           bin_hit=torch.empty((nb,), **i32),
+                           bin_conf=torch.empty((nb,), dtype=torch.float64, device=device),
+                           ece=torch.empty((1,), dtype=torch.float64, device=device))
+            self.side2 = torch.cuda.Stream(device=device)
         # greedy drafting uses the Markov head's prepared tables, built once
         # per weights (model-load time, outside the timed cycle)
         self.prepared = None if self.sample else sdm.markov_prepare(self.inp["U"], self.inp["W"])
@@ -257,7 +279,9 @@ class Cycle:
 
     def schedule(self):
         sdm, i = self.sdm, self.inp
-        if self.dynamic:
+        if self.tau is not None:
+            sdm.schedule_threshold(i["conf"], self.tau, out=self.sc, dev_status=self.status)
+        elif self.dynamic:
             sdm.schedule_dynamic(i["conf"], i["conf_stale"], i["cost_tiered"], out=self.sc, dev_status=self.status)
         else:
             sdm.schedule_budget(i["conf"], i["cost"], out=self.sc, dev_status=self.status)
@@ -303,15 +327,35 @@ class Cycle:
         kw = {}
         if self.sample:
             kw = dict(logq=self.dr["logq"], lse_q=self.dr["lse"], L=i["L"], U=i["U"], W=i["W"])
+        if self.obs:   # the soft labels need no verify output: they run beside it
+            main = self.torch.cuda.current_stream()
+            self.side2.wait_stream(main)
+            with self.torch.cuda.stream(self.side2):
+                self.tv_label()
         sdm.verify(self.mode, sdm.SAMPLE if self.sample else sdm.GREEDY, self.packed, self.pk["cu_seqlens"],
                    i["anchor"], self.dr["tokens"], budget=self.sc["budget"], temperature=self.w.temperature,
                    out=self.vr, ws=self.ws_verify, dev_status=self.status, **kw)
+        if self.obs:
+            self.stats()
+            main.wait_stream(self.side2)
+
+    def tv_label(self):
+        i = self.inp
+        self.sdm.tv_label(self.packed, self.pk["cu_seqlens"], i["anchor"], self.dr["tokens"], i["L"], i["U"], i["W"],
+                          lse_q=self.dr["lse"] if self.sample else None, temperature=self.w.temperature,
+                          out=self.label, ws=self.ws_label, dev_status=self.status)
+
+    def stats(self):
+        self.sdm.observe(self.inp["conf"], self.pk["cu_seqlens"], self.vr["ceiling"], self.cls, self.n_class,
+                         self.n_bins, out=self.st, dev_status=self.status)
 
     def launches_per_step(self):
         if self.tree:
             return (2 * self.w.B + 2) + 2
         draft = 2 if self.prepared is not None else self.w.B + 2
         verify = 5 if self.sample else 2
+        if self.obs:   # row stream, row list, [draft log-sum-exp pass + reduction], label pass + reduction, stats
+            verify += 5 if self.sample else 7
         return draft + 1 + 1 + verify
 
     def capture(self):
@@ -333,7 +377,8 @@ def run_ours(args, w, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dynamic = args.scheduler == "dynamic"
-    cyc = Cycle(w, seed=rank, device=dev, dynamic=dynamic)
+    tau = args.tau if args.scheduler == "threshold" else None
+    cyc = Cycle(w, seed=rank, device=dev, dynamic=dynamic, observe=args.observe, tau=tau)
     R, B, V = w.R, w.B, w.V
     committed = int(cyc.vr["n_out"].sum().item())
     accepted = int(cyc.vr["accept"].sum().item())
@@ -418,6 +463,7 @@ def run_ours(args, w, world, rank, local):
     t_draft = sum(e[0].elapsed_time(e[1]) for e in ev_d) / 1e3 / n_draft * args.steps   # seconds per args.steps
     t_max, units = merge_ranks(t_total, [committed * args.steps, windows * args.steps], world)
     status = int(cyc.status.item())
+    observe = observe_alone(cyc, flush, stream, graphs, max(20, min(200, args.steps))) if cyc.obs else None
 
     # roofline of the dominant kernel (algorithmic bytes or flops / measured time)
     hbm_peak, tc_peak, peak_kind = measured_peaks()
@@ -443,7 +489,15 @@ def run_ours(args, w, world, rank, local):
         per_launch_s = t_draft / args.steps / draft_launches
         achieved = draft_alg / per_launch_s / (1e12 if bound == "tensor" else 1e9)
     else:
-        kname, bound = "row_stream_kernel<argmax>", "hbm"
+        # the verify path: every verified target row once; sampling adds the
+        # residual pass (its L and target rows and W); the soft-label pass,
+        # when on, its own bytes
+        kname, bound = ("row_stream_kernel<lse>+residual" if cyc.sample else "row_stream_kernel<argmax>"), "hbm"
+        if cyc.sample:
+            verify_bytes += R * V * (s_l + s_t) + w.r * V * 2
+        if observe is not None:
+            kname += "+tv_label"
+            verify_bytes += observe["algorithmic_bytes"]
         per_launch_s = t_verify / args.steps
         achieved = verify_bytes / per_launch_s / 1e9
     peak, unit = (tc_peak, "TFLOP/s") if bound == "tensor" else (hbm_peak, "GB/s")
@@ -456,7 +510,7 @@ def run_ours(args, w, world, rank, local):
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        cpu = oracle_sample(w, cyc.inp, args.cpu_seconds, dynamic)
+        cpu = oracle_sample(w, cyc.inp, args.cpu_seconds, dynamic, cyc.obs, tau)
 
     clk = clocks.summary(w0, w1)
     out = {
@@ -473,7 +527,7 @@ def run_ours(args, w, world, rank, local):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": w.name, "R": R, "B": B, "V": V, "r": w.r, "decode": w.decode, "mode": w.modes[0],
-                   "scheduler": None if cyc.tree else args.scheduler,
+                   "scheduler": None if cyc.tree else args.scheduler, "tau": tau, "observe": cyc.obs,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed by a 256 MB write before every step",
                    "timed": "draft+schedule+pack+verify (CUDA events); target stand-in row gather excluded"},
@@ -495,9 +549,46 @@ def run_ours(args, w, world, rank, local):
     }
     if e2e is not None:
         out["e2e"] = e2e
+    if observe is not None:
+        observe["roofline_frac"] = observe["achieved_gbs"] / hbm_peak
+        out["observe"] = observe
     if cpu is not None:
         out["cpu_baseline"] = cpu
     return out
+
+
+def observe_alone(cyc, flush, stream, graphs, n):
+    """The soft-label pass on its own (graph replays after an L2 flush, CUDA
+    events on the stream) and what the last cycle's statistics say."""
+    import torch
+
+    w = cyc.w
+    g = None
+    if graphs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cyc.tv_label()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    for k in range(n + 3):
+        flush.fill_(1)
+        if k >= 3:
+            ev[k - 3][0].record(stream)
+        g.replay() if g is not None else cyc.tv_label()
+        if k >= 3:
+            ev[k - 3][1].record(stream)
+    torch.cuda.synchronize()
+    t = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3 / n
+    rows = int((cyc.label >= 0).sum().item())
+    s_l = 2 if w.l_dtype == 0 else 4
+    s_t = 2 if w.target_dtype == 0 else 4
+    passes = 1 if cyc.sample else 2                # the greedy draft returns no log-sum-exp
+    # per listed row: its target row twice (log-sum-exp stream, label pass),
+    # its L row once per GEMM pass; W once per GEMM pass
+    alg = rows * w.V * (2 * s_t + passes * s_l) + passes * w.r * w.V * 2
+    lab = cyc.label[cyc.label >= 0]
+    return {"label_ms": t * 1e3, "label_rows": rows, "algorithmic_bytes": alg, "achieved_gbs": alg / t / 1e9,
+            "mean_label": float(lab.mean().item()) if rows else None, "ece": float(cyc.st["ece"].item()),
+            "ceiling_hist": cyc.st["hist"].tolist(), "timed_in_verify": True}
 
 
 def run_e2e(cyc, args, committed):
@@ -552,7 +643,7 @@ def run_e2e(cyc, args, committed):
 # ---------------------------------------------------------------------------
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False):
+def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False, observe=False, tau=None):
     """One oracle cycle for the requests idx (schedule over all requests);
     returns (seconds of oracle work, committed tokens)."""
     import numpy as np
@@ -589,7 +680,9 @@ def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False):
     t0 = time.perf_counter()
     dr = oracle.draft_chain(L, U, W, an, decode=oracle.SAMPLE if sample else oracle.GREEDY,
                             temperature=w.temperature, seed=cycle_seed, req_ids=ids)
-    if dynamic:
+    if tau is not None:
+        sc = oracle.schedule_threshold(conf, tau)
+    elif dynamic:
         sc = oracle.schedule_dynamic(conf, stale, cost)
     else:
         sc = oracle.schedule_budget(conf, cost)
@@ -607,17 +700,21 @@ def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False):
         kw = dict(logq=dr["logq"], lse_q=dr["lse"], L=L, U=U, W=W, temperature=w.temperature, seed=cycle_seed)
     vr = oracle.verify(mode, oracle.SAMPLE if sample else oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an,
                        dr["tokens"], budget=budget, req_ids=ids, **kw)
+    if observe:
+        oracle.tv_label(np_of(packed), pk["cu_seqlens"], an, dr["tokens"], L, U, W, temperature=w.temperature)
+        cls = synthetic.request_class(w, 0).numpy().astype(np.int32)[ids]
+        oracle.observe(conf[ids], pk["cu_seqlens"], vr["ceiling"], cls, len(w.sigma), 10)
     t3 = time.perf_counter()
     return (t1 - t0) + (t3 - t2), int(vr["n_out"].sum())
 
 
-def oracle_sample(w, inp, seconds, dynamic=False):
+def oracle_sample(w, inp, seconds, dynamic=False, observe=False, tau=None):
     """Oracle throughput on a bounded sample: requests are added one at a time
     (each a full cycle: its draft, the schedule over all requests, its pack and
     verify) until about `seconds` of oracle work."""
     spent, toks, n = 0.0, 0, 0
     while n < w.R and (spent < seconds or n < 2):
-        dt, c = oracle_cycle(w, inp, [n], dynamic=dynamic)
+        dt, c = oracle_cycle(w, inp, [n], dynamic=dynamic, observe=observe, tau=tau)
         spent += dt
         toks += c
         n += 1
@@ -633,13 +730,15 @@ def run_reference(args, w):
 
     inp = synthetic.generate(w, seed=0, device="cpu")
     dynamic = args.scheduler == "dynamic" and w.decode != "tree"
+    observe = args.observe and w.decode != "tree"
+    tau = args.tau if args.scheduler == "threshold" and w.decode != "tree" else None
     for _ in range(args.warmup):
-        oracle_cycle(w, inp, [0], dynamic=dynamic)
+        oracle_cycle(w, inp, [0], dynamic=dynamic, observe=observe, tau=tau)
     spent, toks = 0.0, 0
     per = max(1, min(w.R, 2))
     for k in range(args.steps):
         idx = [(k * per + j) % w.R for j in range(per)]
-        dt, c = oracle_cycle(w, inp, idx, dynamic=dynamic)
+        dt, c = oracle_cycle(w, inp, idx, dynamic=dynamic, observe=observe, tau=tau)
         spent += dt
         toks += c
     value = toks / spent
@@ -648,7 +747,8 @@ def run_reference(args, w):
             "ms_per_step": spent / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": w.name, "R": w.R, "B": w.B, "V": w.V, "r": w.r, "decode": w.decode,
-                       "mode": w.modes[0], "scheduler": None if w.decode == "tree" else args.scheduler},
+                       "mode": w.modes[0], "scheduler": None if w.decode == "tree" else args.scheduler,
+                       "tau": tau, "observe": observe},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
@@ -680,6 +780,9 @@ def main():
     world, rank, local = dist_env()
     from speculative_decoding_markov_gb300.workloads import WORKLOADS
     w = WORKLOADS[args.workload]
+    if args.requests > 0:
+        from speculative_decoding_markov_gb300.workloads import scaled
+        w = scaled(w, R=args.requests)
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, w)))

@@ -340,6 +340,39 @@ const char* sdm_status_str(sdm_status status);
 int sdm_version(void);
 
 /*
+ * schedule_threshold: the conventional fixed-threshold verify length
+ * ([DSpark notes] sec. 5.2: a fixed threshold on the confidences decides how
+ * many drafts are verified; sec. 8.3, Fig. 5).  budget[i] = the longest
+ * prefix n such that conf[i, d] >= tau for every d < n (fp32 comparison; a
+ * NaN confidence ends the prefix); total_tokens = R + sum_i budget[i] (every
+ * request sends its root token).
+ * In:  conf [R, gamma] fp32 (device), tau.  R gamma <= 2^30.
+ * Out: budget [R] int32, total_tokens [1] int32 (device).
+ */
+sdm_status sdm_schedule_threshold(const float* conf, int R, int gamma, float tau, int32_t* budget,
+                                  int32_t* total_tokens, int32_t* dev_status, void* stream);
+
+/*
+ * threshold_sweep: the fixed-threshold rule at K thresholds at once
+ * ([DSpark notes] sec. 8.3, Fig. 5: threshold 0 verifies the whole block).
+ * With n_i(tau) as in schedule_threshold, for threshold k:
+ *   drafts[k]   = sum_i n_i(tau_k)                     drafts verified
+ *   accepted[k] = sum_i min(ceiling[i], n_i(tau_k))    drafts accepted, given
+ *                 the acceptance count of the whole block (sdm_verify's
+ *                 ceiling in CAP_ACCEPT or STATIC mode); -1 if ceiling NULL
+ *   expected[k] = sum_i sum_{d <= n_i} S_{i,d}         expected accepted drafts,
+ *                 S the fp32 running products of conf ([DSpark notes] sec.
+ *                 5.1), summed exactly: each S >= 2^-24 as an integer count
+ *                 of 2^-48, smaller survivals counted 0.
+ * In:  conf [R, gamma] fp32, ceiling [R] int32 or NULL, taus [K] fp32
+ *      (device).  R gamma <= 32768 (the exact sum stays below 2^63), K <= 65535.
+ * Out: drafts, accepted [K] int32, expected [K] fp64 (device).
+ */
+sdm_status sdm_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int gamma, const float* taus, int K,
+                               int32_t* drafts, int32_t* accepted, double* expected, int32_t* dev_status,
+                               void* stream);
+
+/*
  * tv_label: the confidence head's soft label for every verified draft position
  * ([DSpark notes] sec. 5.1: the label is the single-token acceptance rate,
  * fixed by the total-variation distance between the draft and target

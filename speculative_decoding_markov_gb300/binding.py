@@ -25,7 +25,8 @@ DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY, D
 
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
-           "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_status_str",
+           "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_schedule_threshold",
+           "sdm_threshold_sweep", "sdm_status_str",
            "sdm_version")
 
 
@@ -64,6 +65,10 @@ def _declare(lib):
                                _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_verify_greedy_static.restype = _I
     lib.sdm_verify_greedy_static.argtypes = [_I, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]
+    lib.sdm_schedule_threshold.restype = _I
+    lib.sdm_schedule_threshold.argtypes = [_VP, _I, _I, _F, _VP, _VP, _VP, _VP]
+    lib.sdm_threshold_sweep.restype = _I
+    lib.sdm_threshold_sweep.argtypes = [_VP, _VP, _I, _I, _VP, _I, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_tv_label.restype = _I
     lib.sdm_tv_label.argtypes = [_F, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I, _I, _I, _I, _VP, _VP,
                                  _SZ, _VP, _VP]
@@ -231,6 +236,40 @@ def schedule_dynamic(conf, conf_stale, cost, out=None, dev_status=None):
                                     _ptr(out["capacity"]), _ptr(dev_status), _stream())
     _check(st, "sdm_schedule_dynamic")
     out["dev_status"] = dev_status
+    return out
+
+
+def schedule_threshold(conf, tau, out=None, dev_status=None):
+    """Fixed-threshold verify length: the longest prefix with every
+    confidence >= tau."""
+    _need_cuda(conf)
+    R, g = conf.shape
+    dev = conf.device
+    if out is None:
+        out = dict(budget=torch.empty((R,), dtype=torch.int32, device=dev),
+                   total_tokens=torch.empty((1,), dtype=torch.int32, device=dev))
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_schedule_threshold(_ptr(conf), R, g, float(tau), _ptr(out["budget"]), _ptr(out["total_tokens"]),
+                                      _ptr(dev_status), _stream())
+    _check(st, "sdm_schedule_threshold")
+    return out
+
+
+def threshold_sweep(conf, taus, ceiling=None, out=None, dev_status=None):
+    """Drafts verified, drafts accepted (given whole-block ceilings) and
+    expected accepted drafts at every threshold in taus."""
+    _need_cuda(conf, taus, ceiling)
+    R, g = conf.shape
+    K = taus.numel()
+    dev = conf.device
+    if out is None:
+        out = dict(drafts=torch.empty((K,), dtype=torch.int32, device=dev),
+                   accepted=torch.empty((K,), dtype=torch.int32, device=dev),
+                   expected=torch.empty((K,), dtype=torch.float64, device=dev))
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_threshold_sweep(_ptr(conf), _ptr(ceiling), R, g, _ptr(taus), K, _ptr(out["drafts"]),
+                                   _ptr(out["accepted"]), _ptr(out["expected"]), _ptr(dev_status), _stream())
+    _check(st, "sdm_threshold_sweep")
     return out
 
 

@@ -458,6 +458,29 @@ sdm_status sdm_schedule_dynamic(const float* conf, const float* conf_stale, int 
     return SDM_OK;
 }
 
+sdm_status sdm_schedule_threshold(const float* conf, int R, int gamma, float tau, int32_t* budget,
+                                  int32_t* total_tokens, int32_t* dev_status, void* stream) {
+    (void)dev_status;
+    if (!conf || !budget || !total_tokens || R <= 0 || gamma <= 0) return SDM_ERR_INVALID_ARG;
+    if (static_cast<long long>(R) * gamma > (1LL << 30)) return SDM_ERR_UNSUPPORTED;
+    SDM_CHECK_CUDA(launch_schedule_threshold(conf, R, gamma, tau, budget, total_tokens,
+                                             static_cast<cudaStream_t>(stream)));
+    return SDM_OK;
+}
+
+sdm_status sdm_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int gamma, const float* taus, int K,
+                               int32_t* drafts, int32_t* accepted, double* expected, int32_t* dev_status,
+                               void* stream) {
+    (void)dev_status;
+    if (!conf || !taus || !drafts || !accepted || !expected || R <= 0 || gamma <= 0 || K <= 0)
+        return SDM_ERR_INVALID_ARG;
+    // the exact expected-count sum holds R gamma terms of at most 2^48 units
+    if (static_cast<long long>(R) * gamma > 32768 || K > 65535) return SDM_ERR_UNSUPPORTED;
+    SDM_CHECK_CUDA(launch_threshold_sweep(conf, ceiling, R, gamma, taus, K, drafts, accepted, expected,
+                                          static_cast<cudaStream_t>(stream)));
+    return SDM_OK;
+}
+
 sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
                            const int32_t* tiers, int n_tiers, int32_t* cu_seqlens, int32_t* packed_tok,
                            int32_t* packed_req, int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,
@@ -715,8 +738,9 @@ sdm_status sdm_tv_label(float temperature, const void* target, sdm_dtype dtT, in
         SDM_CHECK_CUDA(launch_markov_gemm(MODE_QLSE, tmW, tmW, p, gx, gy, s));
         SDM_CHECK_CUDA(launch_label_lse_q(part, n_part, slots, res_tok, row_lse_q, s));
     }
-    gemm_pick_stages(p, MODE_TVMIN);
-    SDM_CHECK_CUDA(launch_markov_gemm(MODE_TVMIN, tmW, tmW, p, gx, gy, s));
+    const int tv_mode = p.l_fp32 ? MODE_TVMIN : (p.t_fp32 ? MODE_TVMIN_B32 : MODE_TVMIN_B16);
+    gemm_pick_stages(p, tv_mode);
+    SDM_CHECK_CUDA(launch_markov_gemm(tv_mode, tmW, tmW, p, gx, gy, s));
     SDM_CHECK_CUDA(launch_label_finalize(part, n_part, slots, res_tok, res_req, res_pos, gamma, label, s));
     return SDM_OK;
 }

@@ -48,7 +48,9 @@ enum GemmMode {
     MODE_RESID = 3,
     MODE_ABSMAX = 4,
     MODE_QLSE = 5,    // soft label pass 1: log-sum-exp of the draft logits of listed rows
-    MODE_TVMIN = 6    // soft label pass 2: sum_v min(q_v, p_v) of listed rows
+    MODE_TVMIN = 6,   // soft label pass 2: sum_v min(q_v, p_v) of listed rows
+    MODE_TVMIN_B16 = 7,   // the same for bf16 L and bf16 target rows, loads a tile ahead of use
+    MODE_TVMIN_B32 = 8    // the same for bf16 L and fp32 target rows
 };
 
 // Modes that stage a tile of L beside each W tile (the others read their L
@@ -57,7 +59,14 @@ __host__ __device__ constexpr bool mode_reads_l(int mode) {
     return mode == MODE_CHAIN_GREEDY || mode == MODE_CHAIN_SAMPLE || mode == MODE_TREE;
 }
 // Modes whose GEMM rows come from an explicit row list (res_tok / res_req).
-__host__ __device__ constexpr bool mode_row_list(int mode) { return mode == MODE_QLSE || mode == MODE_TVMIN; }
+__host__ __device__ constexpr bool mode_row_list(int mode) {
+    return mode == MODE_QLSE || mode == MODE_TVMIN || mode == MODE_TVMIN_B16 || mode == MODE_TVMIN_B32;
+}
+// Modes whose epilogue issues a whole tile's global loads before reading the
+// accumulator, one slice at a time.
+__host__ __device__ constexpr bool mode_loads_first(int mode) {
+    return mode == MODE_QLSE || mode == MODE_TVMIN_B16 || mode == MODE_TVMIN_B32;
+}
 
 struct GemmParams {
     int rows;            // GEMM rows in use
@@ -309,5 +318,11 @@ cudaError_t launch_observe(const float* conf, const int32_t* cu, const int32_t* 
                            int gamma, int n_class, int n_bins, int32_t* hist, int32_t* reached, int32_t* hits,
                            int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece, int32_t* dev_status,
                            cudaStream_t s);
+
+// Fixed-threshold verify length and its sweep (threshold.cu)
+cudaError_t launch_schedule_threshold(const float* conf, int R, int gamma, float tau, int32_t* budget,
+                                      int32_t* total_tokens, cudaStream_t s);
+cudaError_t launch_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int gamma, const float* taus,
+                                   int K, int32_t* drafts, int32_t* accepted, double* expected, cudaStream_t s);
 
 }  // namespace sdm

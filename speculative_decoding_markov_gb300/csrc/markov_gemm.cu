@@ -19,7 +19,9 @@
 //                      rows, one partial (max, sum) per row, CTA and group
 //   MODE_TVMIN         sum_v min(q_v, p_v) of listed rows (the soft label
 //                      1 - TV, DSpark notes sec. 5.1), one partial sum per
-//                      row, CTA and column group
+//                      row, CTA and column group; MODE_TVMIN_B16 / _B32 are
+//                      the same for bf16 L and bf16 / fp32 target rows with
+//                      a tile's loads issued before its accumulator is read
 //
 // Data path (one CTA = 128 GEMM rows x a contiguous range of 64-wide vocab
 // tiles, K = r):
@@ -180,6 +182,33 @@ __device__ __forceinline__ void load_g(const void* base, int fp32, size_t off, i
             out[c * 4 + 1] = v.y;
             out[c * 4 + 2] = v.z;
             out[c * 4 + 3] = v.w;
+        }
+    }
+}
+
+// C elements of a global row as raw 16-byte words (bf16: r[0..1], fp32:
+// r[0..3]), issued now and unpacked when used; words at or past V read 0.
+__device__ __forceinline__ void load_raw(const void* base, int fp32, size_t off, int v0, int V, uint4 (&r)[4]) {
+    const int per = fp32 ? 4 : 8;
+    const uint8_t* p = static_cast<const uint8_t*>(base) + (off + v0) * (fp32 ? 4 : 2);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+        r[c] = ((fp32 || c < 2) && v0 + c * per < V) ? __ldg(reinterpret_cast<const uint4*>(p + c * 16))
+                                                      : make_uint4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ void unpack_raw(int fp32, const uint4 (&r)[4], float (&out)[C]) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint32_t w[4] = {r[c].x, r[c].y, r[c].z, r[c].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            if (fp32) {
+                out[c * 4 + k] = __uint_as_float(w[k]);
+            } else if (c < 2) {
+                out[c * 8 + 2 * k] = bf_lo(w[k]);
+                out[c * 8 + 2 * k + 1] = bf_hi(w[k]);
+            }
         }
     }
 }
@@ -370,17 +399,22 @@ struct Epi<MODE_QLSE> {
     int group;
     size_t l_off, t_off;
     float sc, m, s;
+    uint4 lr[2][4];   // a tile's L words (bf16: [0..1] of each slice)
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         valid = list_row(p, grow, l_off, t_off);
         sc = p.inv_t * kLog2e;
         m = -INFINITY;
         s = 0.f;
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int vbase, int,
-                                            const uint32_t (&acc)[C]) {
+    __device__ __forceinline__ void issue(const GemmParams& p, const int (&vbase)[2]) {
+        if (!valid) return;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) load_raw(p.L, p.l_fp32, l_off, vbase[h], p.V, lr[h]);
+    }
+    __device__ __forceinline__ void consume_slice(const GemmParams& p, int vbase, int h, const uint32_t (&acc)[C]) {
         if (!valid || vbase >= p.V) return;
         float z[C];
-        load_g(p.L, p.l_fp32, l_off, vbase, p.V, z);
+        unpack_raw(p.l_fp32, lr[h], z);
 #pragma unroll
         for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * sc;
         mask_tail(z, vbase, p.V);
@@ -434,6 +468,94 @@ struct Epi<MODE_TVMIN> {
         if (valid) *part_slot(p, grow, group) = make_float2(0.f, s);
     }
 };
+
+// Typed soft-label pass (L bf16; target bf16 or fp32 by TF32): the loads of
+// both 16-column slices of a tile are issued before the first is used, so a
+// warp keeps a whole tile's rows in flight (the row-per-lane loads are
+// latency-bound otherwise).
+template <int TF32>
+struct EpiTvTyped {
+    static constexpr int kT = TF32 ? 4 : 2;   // 16-byte words of target per slice
+    bool valid;
+    int group;
+    size_t l_off, t_off;
+    float lse_q, lse_p, s;
+    uint4 lr[2][2], tr[2][kT];
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
+        valid = list_row(p, grow, l_off, t_off);
+        s = 0.f;
+        if (valid) {
+            lse_q = p.row_lse_q[grow];
+            lse_p = p.res_lse_p[grow];
+        }
+    }
+    __device__ __forceinline__ void issue(const GemmParams& p, const int (&vbase)[2]) {
+        if (!valid) return;
+        const uint16_t* L = static_cast<const uint16_t*>(p.L) + l_off;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+                lr[h][c] = vbase[h] + c * 8 < p.V ? __ldg(reinterpret_cast<const uint4*>(L + vbase[h] + c * 8))
+                                                  : make_uint4(0, 0, 0, 0);
+            if (TF32) {
+                const float* T = static_cast<const float*>(p.target) + t_off;
+#pragma unroll
+                for (int c = 0; c < kT; ++c)
+                    tr[h][c] = vbase[h] + c * 4 < p.V ? __ldg(reinterpret_cast<const uint4*>(T + vbase[h] + c * 4))
+                                                      : make_uint4(0, 0, 0, 0);
+            } else {
+                const uint16_t* T = static_cast<const uint16_t*>(p.target) + t_off;
+#pragma unroll
+                for (int c = 0; c < kT; ++c)
+                    tr[h][c] = vbase[h] + c * 8 < p.V ? __ldg(reinterpret_cast<const uint4*>(T + vbase[h] + c * 8))
+                                                      : make_uint4(0, 0, 0, 0);
+            }
+        }
+    }
+    __device__ __forceinline__ void consume_slice(const GemmParams& p, int vbase, int h, const uint32_t (&acc)[C]) {
+        if (!valid || vbase >= p.V) return;
+        float lv[C], tv[C];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const uint32_t w[4] = {lr[h][c].x, lr[h][c].y, lr[h][c].z, lr[h][c].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                lv[c * 8 + 2 * k] = bf_lo(w[k]);
+                lv[c * 8 + 2 * k + 1] = bf_hi(w[k]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kT; ++c) {
+            const uint32_t w[4] = {tr[h][c].x, tr[h][c].y, tr[h][c].z, tr[h][c].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (TF32) {
+                    tv[c * 4 + k] = __uint_as_float(w[k]);
+                } else {
+                    tv[c * 8 + 2 * k] = bf_lo(w[k]);
+                    tv[c * 8 + 2 * k + 1] = bf_hi(w[k]);
+                }
+            }
+        }
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < C; ++j) {
+            const float q = __expf((lv[j] + __uint_as_float(acc[j])) * p.inv_t - lse_q);
+            const float pv = __expf(tv[j] * p.inv_t - lse_p);
+            ps[j & 3] += (vbase + j < p.V) ? fminf(pv, q) : 0.f;
+        }
+        s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    }
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
+        if (valid) *part_slot(p, grow, group) = make_float2(0.f, s);
+    }
+};
+
+template <>
+struct Epi<MODE_TVMIN_B16> : EpiTvTyped<0> {};
+template <>
+struct Epi<MODE_TVMIN_B32> : EpiTvTyped<1> {};
 
 template <>
 struct Epi<MODE_ABSMAX> {
@@ -650,6 +772,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         int t = 0, lap = 0;   // L ring slot and wraps
         for (int i = 0; i < nt; ++i) {
             const int b = i & 1;
+            if constexpr (mode_loads_first(MODE)) {
+                // the tile's L and target loads first (they do not wait on
+                // the MMA), then one accumulator slice at a time
+                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+                const int vb[2] = {v0 + g * C, v0 + kBoxN + g * C};
+                st.issue(p, vb);
+                bool ok = mbar_wait(&tfull[b], (i >> 1) & 1);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) {
+                    if (lane == 0) fail_timeout(p);
+                    break;
+                }
+                if (warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);
+                tc_fence_after();
+                uint32_t acc[C];
+                tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + g * C), acc);
+                tmem_ld_wait();
+                st.consume_slice(p, vb[0], 0, acc);
+                tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + kBoxN + g * C), acc);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[b]);
+                st.consume_slice(p, vb[1], 1, acc);
+                continue;
+            } else {
             bool ok = mbar_wait(&tfull[b], (i >> 1) & 1);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
@@ -689,6 +837,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!ok) {
                 if (lane == 0) fail_timeout(p);
                 break;
+            }
             }
         }
         st.flush(p, grow);
@@ -746,6 +895,8 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
         case MODE_ABSMAX: return launch_mode<MODE_ABSMAX>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_QLSE: return launch_mode<MODE_QLSE>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TVMIN: return launch_mode<MODE_TVMIN>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TVMIN_B16: return launch_mode<MODE_TVMIN_B16>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TVMIN_B32: return launch_mode<MODE_TVMIN_B32>(tmW, tmL, p, grid_x, grid_y, s);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -55,20 +55,24 @@ def grid_table(shape, r: int, seed: int, stream: int, device) -> torch.Tensor:
     return q.to(torch.bfloat16)
 
 
-def request_sigma(w: Workload, seed: int, device) -> torch.Tensor:
-    """Per-request target-noise std (fp32 [R])."""
+def request_class(w: Workload, seed: int) -> torch.Tensor:
+    """Traffic class of every request (int64 [R], CPU): its target-noise std
+    is w.sigma[class]."""
     nc = len(w.sigma)
     if nc == 1:
-        cls = torch.zeros(w.R, dtype=torch.int64)
-    elif w.class_mix == "alternate":
-        cls = torch.arange(w.R) % nc
-    else:
-        # equal class shares (rounded up), shuffled, truncated to R
-        per = -(-w.R // nc)
-        pool = torch.arange(nc).repeat_interleave(per)
-        perm = torch.randperm(pool.numel(), generator=_gen(seed, _S_CLASS, "cpu"))
-        cls = pool[perm][: w.R]
-    s = torch.tensor(w.sigma, dtype=torch.float32)[cls]
+        return torch.zeros(w.R, dtype=torch.int64)
+    if w.class_mix == "alternate":
+        return torch.arange(w.R) % nc
+    # equal class shares (rounded up), shuffled, truncated to R
+    per = -(-w.R // nc)
+    pool = torch.arange(nc).repeat_interleave(per)
+    perm = torch.randperm(pool.numel(), generator=_gen(seed, _S_CLASS, "cpu"))
+    return pool[perm][: w.R]
+
+
+def request_sigma(w: Workload, seed: int, device) -> torch.Tensor:
+    """Per-request target-noise std (fp32 [R])."""
+    s = torch.tensor(w.sigma, dtype=torch.float32)[request_class(w, seed)]
     return s.to(device)
 
 

@@ -154,3 +154,13 @@ def test_observability_host_validation(lib):
     bad = list(o)
     bad[6], bad[5] = 1000, 16                   # counters beyond 48 KB of shared memory
     assert ob(*bad) == 2
+
+
+def test_threshold_host_validation(lib):
+    st = lib.sdm_schedule_threshold
+    assert st(None, 4, 7, 0.5, FAKE, FAKE, None, None) == 1
+    assert st(FAKE, 0, 7, 0.5, FAKE, FAKE, None, None) == 1
+    sw = lib.sdm_threshold_sweep
+    assert sw(FAKE, None, 4, 7, None, 3, FAKE, FAKE, FAKE, None, None) == 1      # thresholds missing
+    assert sw(FAKE, None, 4, 7, FAKE, 0, FAKE, FAKE, FAKE, None, None) == 1      # K = 0
+    assert sw(FAKE, None, 4096, 9, FAKE, 3, FAKE, FAKE, FAKE, None, None) == 2   # R gamma > 32768
