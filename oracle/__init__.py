@@ -242,3 +242,29 @@ def threshold_sweep(conf, taus, ceiling=None):
     lib().orc_threshold_sweep(_p(_c(conf, np.float32)), _p(None if ceiling is None else _c(ceiling, np.int32)), R, g,
                               _p(taus), K, _p(drafts), _p(accepted), _p(expected))
     return dict(drafts=drafts, accepted=accepted, expected=expected)
+
+
+def rnn_memo(A, U, X, anchor, tokens):
+    """Memo trajectory [R, B, r] (float64) of the RNN head along tokens."""
+    R, B, r = X.shape
+    memo = np.zeros((R, B, r), np.float64)
+    lib().orc_rnn_memo(_p(_c(A, np.uint16)), _p(_c(U, np.uint16)), _p(_c(X, np.uint16)), _p(_c(anchor, np.int32)),
+                       _p(_c(tokens, np.int32)), R, B, r, _p(memo))
+    return memo
+
+
+def draft_chain_rnn(L, U, W, A, X, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0, req_ids=None):
+    """Chain draft with the RNN head; outputs as draft_chain."""
+    R, B, V = L.shape
+    r = U.shape[1]
+    L = np.ascontiguousarray(L)
+    tokens = np.zeros((R, B), np.int32)
+    logq = np.zeros((R, B), np.float64)
+    lse = np.zeros((R, B), np.float64)
+    margin = np.zeros((R, B), np.float64)
+    ids = None if req_ids is None else _c(req_ids, np.int32)
+    flags = lib().orc_draft_chain_rnn(
+        _p(L), _dt(L), _p(_c(U, np.uint16)), _p(_c(W, np.uint16)), _p(_c(A, np.uint16)), _p(_c(X, np.uint16)),
+        _p(_c(anchor, np.int32)), _p(ids), R, B, V, r, decode, ctypes.c_double(temperature), ctypes.c_uint64(seed),
+        ctypes.c_uint64(cycle), _p(tokens), _p(logq), _p(lse), _p(margin))
+    return dict(tokens=tokens, logq=logq, lse=lse, margin=margin, flags=flags)

@@ -830,3 +830,119 @@ int orc_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int ga
     }
     return 0;
 }
+
+/* ------------------------------------------------------------------ */
+/* RNN head ([DSpark notes] sec. 4, "RNN head": a memo that carries the */
+/* whole draft so far, updated once per step from the previous memo,    */
+/* the previous word and the current backbone state).  The update's    */
+/* formula is not legible on the page; the reading taken here:          */
+/*   m_0 = 0,  m_d = tanh(A m_{d-1} + U[y_{d-1}] + x_d)                 */
+/*   z_d = L_d + bf16(m_d) . W                                          */
+/* with U the Markov head's token table (the previous word's input),    */
+/* x_d the backbone state at position d projected to the memo's size r  */
+/* (an input), and the memo entering the vocabulary projection in bf16  */
+/* like U does.  With A = 0 and x = 0 this is the Markov head on the    */
+/* table bf16(tanh(U)).                                                 */
+/* ------------------------------------------------------------------ */
+
+/* IEEE round-to-nearest-even of a binary32 to its upper 16 bits. */
+static uint16_t float_to_bf16(float f) {
+    uint32_t b;
+    memcpy(&b, &f, sizeof b);
+    if ((b & 0x7F800000u) == 0x7F800000u && (b & 0x007FFFFFu)) return (uint16_t)((b >> 16) | 0x40u);   /* NaN */
+    b += 0x7FFFu + ((b >> 16) & 1u);
+    return (uint16_t)(b >> 16);
+}
+
+/* m_out = tanh(A m_prev + U[prev] + x), all in double; A is [r, r] row-major
+ * (output index first). */
+static void rnn_update(const uint16_t* A, const uint16_t* U, const uint16_t* x, int prev, int r,
+                       const double* m_prev, double* m_out) {
+    for (int j = 0; j < r; ++j) {
+        double v = 0.0;
+        for (int k = 0; k < r; ++k) v += (double)bf16_to_float(A[(size_t)j * r + (size_t)k]) * m_prev[k];
+        v += (double)bf16_to_float(U[(size_t)prev * r + (size_t)j]) + (double)bf16_to_float(x[j]);
+        m_out[j] = tanh(v);
+    }
+}
+
+/* M[v] = sum_j bf16(m_j) W[j, v] in double. */
+static void memo_times_w(const double* m, const uint16_t* W, int r, int V, double* M) {
+    for (int v = 0; v < V; ++v) M[v] = 0.0;
+    for (int j = 0; j < r; ++j) {
+        double a = (double)bf16_to_float(float_to_bf16((float)m[j]));
+        if (a == 0.0) continue;
+        const uint16_t* wrow = W + (size_t)j * V;
+        for (int v = 0; v < V; ++v) M[v] += a * (double)bf16_to_float(wrow[v]);
+    }
+}
+
+/* The memo trajectory along a given token sequence: memo[i, d-1, :] = m_d
+ * for d = 1..B (y_0 = anchor[i], y_d = tokens[i, d-1]). */
+int orc_rnn_memo(const uint16_t* A, const uint16_t* U, const uint16_t* X, const int32_t* anchor,
+                 const int32_t* tokens, int R, int B, int r, double* memo) {
+    double* m = (double*)calloc((size_t)r, sizeof(double));
+    for (int i = 0; i < R; ++i) {
+        for (int j = 0; j < r; ++j) m[j] = 0.0;
+        for (int d = 1; d <= B; ++d) {
+            int prev = d == 1 ? anchor[i] : tokens[(size_t)i * B + (size_t)(d - 2)];
+            double* out = memo + ((size_t)i * B + (size_t)(d - 1)) * r;
+            rnn_update(A, U, X + ((size_t)i * B + (size_t)(d - 1)) * r, prev, r, m, out);
+            memcpy(m, out, sizeof(double) * (size_t)r);
+        }
+    }
+    free(m);
+    return 0;
+}
+
+/* The chain draft with the RNN head: as orc_draft_chain, with z_d formed
+ * from the memo.  X is [R, B, r] bf16, A [r, r] bf16. */
+int orc_draft_chain_rnn(const void* L, int dtL, const uint16_t* U, const uint16_t* W, const uint16_t* A,
+                        const uint16_t* X, const int32_t* anchor, const int32_t* req_ids, int R, int B, int V, int r,
+                        int decode, double temperature, uint64_t seed, uint64_t cycle,
+                        int32_t* tokens, double* logq, double* lse, double* margin) {
+    double* M = (double*)malloc(sizeof(double) * (size_t)V);
+    double* wts = (double*)malloc(sizeof(double) * (size_t)V);
+    float* z = (float*)malloc(sizeof(float) * (size_t)V);
+    double* m = (double*)malloc(sizeof(double) * (size_t)r);
+    double* m_next = (double*)malloc(sizeof(double) * (size_t)r);
+    double inv_t = 1.0 / temperature;
+    for (int i = 0; i < R; ++i) {
+        uint32_t gid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
+        int prev = anchor[i];
+        for (int j = 0; j < r; ++j) m[j] = 0.0;
+        for (int d = 1; d <= B; ++d) {
+            size_t o = (size_t)i * B + (size_t)(d - 1);
+            rnn_update(A, U, X + o * (size_t)r, prev, r, m, m_next);
+            memcpy(m, m_next, sizeof(double) * (size_t)r);
+            memo_times_w(m, W, r, V, M);
+            combine_logits(L, dtL, o * V, M, V, z);
+            int y;
+            double gap = 0.0;
+            if (decode == ORC_GREEDY) {
+                y = argmax_f32(z, V, &gap);
+                if (logq) logq[o] = 0.0;
+                if (lse) lse[o] = 0.0;
+            } else {
+                double zmax = -INFINITY;
+                for (int v = 0; v < V; ++v)
+                    if ((double)z[v] * inv_t > zmax) zmax = (double)z[v] * inv_t;
+                for (int v = 0; v < V; ++v) wts[v] = exp((double)z[v] * inv_t - zmax);
+                double u = orc_uniform(seed, cycle, ORC_STREAM_DRAFT, gid, (uint32_t)d, 0u);
+                y = icdf_draw(wts, V, u, &gap);
+                double l = logsumexp_scaled(z, V, inv_t);
+                if (lse) lse[o] = l;
+                if (logq) logq[o] = (double)z[y] * inv_t - l;
+            }
+            tokens[o] = y;
+            if (margin) margin[o] = gap;
+            prev = y;
+        }
+    }
+    free(M);
+    free(wts);
+    free(z);
+    free(m);
+    free(m_next);
+    return 0;
+}

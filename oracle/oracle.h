@@ -131,6 +131,17 @@ int orc_schedule_threshold(const float* conf, int R, int gamma, float tau, int32
 int orc_threshold_sweep(const float* conf, const int32_t* ceiling, int R, int gamma, const float* taus, int K,
                         int32_t* drafts, int32_t* accepted, double* expected);
 
+/* RNN head: memo m_d = tanh(A m_{d-1} + U[y_{d-1}] + x_d), m_0 = 0, and
+ * z_d = L_d + bf16(m_d) . W.  orc_rnn_memo gives the memo along a given
+ * token sequence ([R, B, r] double); orc_draft_chain_rnn drafts with it
+ * (outputs as orc_draft_chain).  A [r, r], X [R, B, r] bf16. */
+int orc_rnn_memo(const uint16_t* A, const uint16_t* U, const uint16_t* X, const int32_t* anchor,
+                 const int32_t* tokens, int R, int B, int r, double* memo);
+int orc_draft_chain_rnn(const void* L, int dtL, const uint16_t* U, const uint16_t* W, const uint16_t* A,
+                        const uint16_t* X, const int32_t* anchor, const int32_t* req_ids, int R, int B, int V, int r,
+                        int decode, double temperature, uint64_t seed, uint64_t cycle,
+                        int32_t* tokens, double* logq, double* lse, double* margin);
+
 #ifdef __cplusplus
 }
 #endif

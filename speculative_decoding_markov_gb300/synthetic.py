@@ -30,7 +30,7 @@ from .workloads import BF16, FP32, Workload
 _TORCH_DTYPE = {BF16: torch.bfloat16, FP32: torch.float32}
 
 # distinct generator streams per tensor (seed * 64 + stream)
-_S_L, _S_LB, _S_U, _S_W, _S_ANCHOR, _S_ETA, _S_CONF, _S_CLASS, _S_STALE = range(16, 25)
+_S_L, _S_LB, _S_U, _S_W, _S_ANCHOR, _S_ETA, _S_CONF, _S_CLASS, _S_STALE, _S_ARNN, _S_XRNN = range(16, 27)
 
 
 def torch_dtype(code: int) -> torch.dtype:
@@ -105,6 +105,17 @@ def stale_confidences(conf: torch.Tensor, seed: int) -> torch.Tensor:
     noise = torch.randn(conf.shape, generator=_gen(seed, _S_STALE, conf.device), device=conf.device,
                         dtype=torch.float64) * 0.5
     return torch.sigmoid(x + noise).to(torch.float32)
+
+
+def rnn_inputs(w: Workload, seed: int = 0, device="cpu", a_scale: float = 0.9, x_std: float = 0.5) -> dict:
+    """Weights and inputs of the RNN head (bf16): the memo recurrence A
+    [r, r] with entries N(0, a_scale^2 / r) (spectral radius near a_scale),
+    and the backbone state projected to the memo's size, X [R, B, r] ~
+    N(0, x_std^2)."""
+    R, B, r = w.R, w.B, w.r
+    A = torch.randn((r, r), generator=_gen(seed, _S_ARNN, device), device=device) * (a_scale / math.sqrt(r))
+    X = torch.randn((R, B, r), generator=_gen(seed, _S_XRNN, device), device=device) * x_std
+    return dict(A_rnn=A.to(torch.bfloat16), X_rnn=X.to(torch.bfloat16))
 
 
 def generate(w: Workload, seed: int = 0, device="cpu") -> dict:

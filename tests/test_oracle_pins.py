@@ -935,3 +935,109 @@ def test_threshold_expected_matches_rejection_sampling():
         var += m2 - s.sum() ** 2
     assert abs(sw["accepted"][0] - sw["expected"][0]) < 4.5 * math.sqrt(var)
     assert abs(sw["expected"][0] - S.sum()) < 1e-6 * S.sum()
+
+
+# ---------------------------------------------------------------------------
+# RNN head
+# ---------------------------------------------------------------------------
+def _bf16_bits(x64):
+    """Round doubles to bf16 bits through binary32, nearest-even (numpy)."""
+    f = np.asarray(x64, np.float64).astype(np.float32)
+    b = f.view(np.uint32).astype(np.uint64)
+    b = (b + 0x7FFF + ((b >> 16) & 1)) >> 16
+    return b.astype(np.uint16)
+
+
+def _f64_of_bf16(bits):
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("decode", [oracle.GREEDY, oracle.SAMPLE])
+def test_rnn_without_memory_is_the_markov_head_on_tanh_table(decode):
+    """A = 0 and x = 0 leave m_d = tanh(U[y_{d-1}]): the RNN draft is the
+    Markov head's draft on the table bf16(tanh(U))."""
+    w = small(R=12, B=5, V=300, r=16, sigma=(0.5,), l_std=1.0)
+    inp = _inputs(w, seed=3)
+    L, U, W, an = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"])
+    A = np.zeros((w.r, w.r), np.uint16)
+    X = np.zeros((w.R, w.B, w.r), np.uint16)
+    U3 = _bf16_bits(_f64_of_bf16(U) * 4.0)                    # exact (a power of two), tanh well away from identity
+    assert np.array_equal(_f64_of_bf16(U3), _f64_of_bf16(U) * 4.0)
+    Ut = _bf16_bits(np.tanh(_f64_of_bf16(U3)))
+    rnn = oracle.draft_chain_rnn(L, U3, W, A, X, an, decode=decode, temperature=0.9, seed=4, cycle=1)
+    mk = oracle.draft_chain(L, Ut, W, an, decode=decode, temperature=0.9, seed=4, cycle=1)
+    np.testing.assert_array_equal(rnn["tokens"], mk["tokens"])
+    np.testing.assert_allclose(rnn["lse"], mk["lse"], rtol=0, atol=1e-12)
+
+
+def test_rnn_zero_tables_draft_the_backbone_argmax():
+    w = small(R=6, B=4, V=200, r=16, sigma=(0.5,))
+    inp = _inputs(w, seed=5)
+    L = np_of(inp["L"])
+    rng = np.random.default_rng(0)
+    A = _bf16_bits(rng.normal(0, 0.3, (w.r, w.r)))
+    zero_u = np.zeros_like(np_of(inp["U"]))
+    out = oracle.draft_chain_rnn(L, zero_u, np_of(inp["W"]), A, np.zeros((w.R, w.B, w.r), np.uint16),
+                                 np_of(inp["anchor"]))
+    np.testing.assert_array_equal(out["tokens"], L.argmax(-1))
+
+
+def test_rnn_memo_small_signal_closed_form():
+    """For small inputs tanh(v) = v - v^3/3 + ..., so the memo is the linear
+    recurrence's closed form m_d = sum_k A^k (U[y_{d-1-k}] + x_{d-k}) to
+    within the cubic terms carried through the recurrence (|A| < 1: at most
+    d of them, each below max|v|^3 / 3)."""
+    R, B, r, V = 5, 6, 16, 40
+    rng = np.random.default_rng(7)
+    eps = 2.0 ** -10
+    A = _bf16_bits(rng.normal(0, 0.8 / math.sqrt(r), (r, r)))
+    U = _bf16_bits(rng.normal(0, eps, (V, r)))
+    X = _bf16_bits(rng.normal(0, eps, (R, B, r)))
+    an = rng.integers(0, V, R).astype(np.int32)
+    toks = rng.integers(0, V, (R, B)).astype(np.int32)
+    memo = oracle.rnn_memo(A, U, X, an, toks)
+    Af, Uf, Xf = _f64_of_bf16(A), _f64_of_bf16(U), _f64_of_bf16(X)
+    powers = [np.eye(r)]
+    for _ in range(B):
+        powers.append(powers[-1] @ Af)
+    for i in range(R):
+        ys = np.concatenate([[an[i]], toks[i]])
+        for d in range(1, B + 1):
+            ref = sum(powers[k] @ (Uf[ys[d - 1 - k]] + Xf[i, d - 1 - k]) for k in range(d))
+            err = np.abs(memo[i, d - 1] - ref).max()
+            vmax = max(np.abs(memo[i, k]).max() for k in range(d)) * 1.01
+            assert err <= d * vmax ** 3 / 3 + 1e-15, (i, d, err)
+            assert err <= 1e-4 * np.abs(ref).max()
+
+
+def test_rnn_memo_remembers_earlier_tokens():
+    """With A != 0, m_3 depends on y_1; with A = 0 it depends only on y_2
+    and x_3 (the Markov head's reach)."""
+    R, B, r, V = 2, 3, 16, 30
+    rng = np.random.default_rng(9)
+    A = _bf16_bits(rng.normal(0, 0.5, (r, r)))
+    U = _bf16_bits(rng.normal(0, 0.5, (V, r)))
+    X = np.repeat(_bf16_bits(rng.normal(0, 0.5, (1, B, r))), R, axis=0)
+    an = np.array([3, 3], np.int32)
+    toks = np.array([[5, 7, 1], [6, 7, 1]], np.int32)          # differ at y_1 only
+    m = oracle.rnn_memo(A, U, X, an, toks)
+    assert np.abs(m[0, 2] - m[1, 2]).max() > 1e-3
+    m0 = oracle.rnn_memo(np.zeros_like(A), U, X, an, toks)
+    np.testing.assert_array_equal(m0[0, 2], m0[1, 2])
+    np.testing.assert_array_equal(m0[0, 0], m0[1, 0])
+
+
+def test_rnn_draft_follows_its_memo():
+    """Every greedy draft token is the argmax of L_d + bf16(m_d) W with m_d
+    the memo along the drafted tokens (the pinned recurrence above)."""
+    w = small(R=8, B=5, V=120, r=16, sigma=(0.5,), l_std=0.5)
+    inp = _inputs(w, seed=11)
+    rnn = synthetic.rnn_inputs(w, seed=11)
+    L, U, W, an = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"])
+    A, X = np_of(rnn["A_rnn"]), np_of(rnn["X_rnn"])
+    out = oracle.draft_chain_rnn(L, U, W, A, X, an)
+    memo = oracle.rnn_memo(A, U, X, an, out["tokens"])
+    mb = _f64_of_bf16(_bf16_bits(memo))
+    z = L.astype(np.float32) + np.einsum("idr,rv->idv", mb, _f64_of_bf16(W)).astype(np.float32)
+    np.testing.assert_array_equal(out["tokens"], z.argmax(-1))
+    assert np.abs(memo).max() < 1.0 and np.abs(memo).max() > 0.3      # tanh range, not saturated away
