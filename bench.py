@@ -50,6 +50,9 @@ def parse():
                          "scheduler (capacity from the confidences of two steps before, global search over the "
                          "tier-stepped table)")
     ap.add_argument("--tau", type=float, default=0.5, help="confidence threshold of --scheduler threshold")
+    ap.add_argument("--head", default="markov", choices=["markov", "rnn"],
+                    help="sequential head of the chain draft: the Markov head, or the RNN head (memo recurrence; "
+                         "dense tensor-core projection per step)")
     ap.add_argument("--requests", type=int, default=0,
                     help="run the workload with this many requests instead (smaller cases for profiler captures)")
     ap.add_argument("--observe", action="store_true",
@@ -175,7 +178,7 @@ class ClockSampler:
 class Cycle:
     """Preallocated buffers and the launch sequence of one decode cycle."""
 
-    def __init__(self, w, seed, device, dynamic=False, observe=False, tau=None):
+    def __init__(self, w, seed, device, dynamic=False, observe=False, tau=None, rnn=False):
         import torch
 
         from speculative_decoding_markov_gb300 import binding as sdm
@@ -190,6 +193,7 @@ class Cycle:
         self.tree = w.decode == "tree"
         self.dynamic = dynamic
         self.tau = tau
+        self.rnn = rnn and not self.tree
         self.obs = observe and not self.tree
         i32 = dict(dtype=torch.int32, device=device)
         self.status = sdm.new_status(device)
@@ -213,7 +217,10 @@ class Cycle:
         self.packed = torch.empty((cap, V), dtype=tdt, device=device)
         self.vr = dict(accept=torch.empty((R,), **i32), ceiling=torch.empty((R,), **i32),
                        out_tok=torch.empty((R, B + 1), **i32), n_out=torch.empty((R,), **i32))
-        self.ws_draft = sdm.workspace(sdm.OP_DRAFT_CHAIN, R, B, V, r, device=device)
+        self.ws_draft = sdm.workspace(sdm.OP_DRAFT_CHAIN_RNN if self.rnn else sdm.OP_DRAFT_CHAIN, R, B, V, r,
+                                      device=device)
+        if self.rnn:
+            self.inp.update(synthetic.rnn_inputs(w, seed=seed, device=device))
         self.ws_verify = sdm.workspace(sdm.OP_VERIFY, R, B, V, r, cap, device=device)
         if self.obs:
             self.n_class, self.n_bins = len(w.sigma), 10
@@ -229,7 +236,7 @@ class Cycle:
             self.side2 = torch.cuda.Stream(device=device)
         # greedy drafting uses the Markov head's prepared tables, built once
         # per weights (model-load time, outside the timed cycle)
-        self.prepared = None if self.sample else sdm.markov_prepare(self.inp["U"], self.inp["W"])
+        self.prepared = None if (self.sample or self.rnn) else sdm.markov_prepare(self.inp["U"], self.inp["W"])
         # one untimed cycle fixes the drafted prefix; the stand-in target model
         # then provides every window row along it
         self.draft()
@@ -272,6 +279,11 @@ class Cycle:
             w = self.w
             sdm.draft_tree(i["L"], i["U"], i["W"], i["anchor"], w.k, w.P, w.N, out=self.tr, ws=self.ws_draft,
                            dev_status=self.status)
+            return
+        if self.rnn:
+            sdm.draft_chain_rnn(i["L"], i["U"], i["W"], i["A_rnn"], i["X_rnn"], i["anchor"],
+                                decode=sdm.SAMPLE if self.sample else sdm.GREEDY, temperature=self.w.temperature,
+                                seed=0, cycle=0, out=self.dr, ws=self.ws_draft, dev_status=self.status)
             return
         sdm.draft_chain(i["L"], i["U"], i["W"], i["anchor"], decode=sdm.SAMPLE if self.sample else sdm.GREEDY,
                         temperature=self.w.temperature, seed=0, cycle=0, out=self.dr, ws=self.ws_draft,
@@ -352,7 +364,10 @@ class Cycle:
     def launches_per_step(self):
         if self.tree:
             return (2 * self.w.B + 2) + 2
-        draft = 2 if self.prepared is not None else self.w.B + 2
+        if self.rnn:   # per step the memo update and the GEMM (+ the select when sampling); greedy: fill, finalize
+            draft = self.w.B * (3 if self.sample else 2) + (0 if self.sample else 2)
+        else:
+            draft = 2 if self.prepared is not None else self.w.B + 2
         verify = 5 if self.sample else 2
         if self.obs:   # row stream, row list, [draft log-sum-exp pass + reduction], label pass + reduction, stats
             verify += 5 if self.sample else 7
@@ -378,7 +393,7 @@ def run_ours(args, w, world, rank, local):
     dev = torch.device("cuda", local)
     dynamic = args.scheduler == "dynamic"
     tau = args.tau if args.scheduler == "threshold" else None
-    cyc = Cycle(w, seed=rank, device=dev, dynamic=dynamic, observe=args.observe, tau=tau)
+    cyc = Cycle(w, seed=rank, device=dev, dynamic=dynamic, observe=args.observe, tau=tau, rnn=args.head == "rnn")
     R, B, V = w.R, w.B, w.V
     committed = int(cyc.vr["n_out"].sum().item())
     accepted = int(cyc.vr["accept"].sum().item())
@@ -480,10 +495,11 @@ def run_ours(args, w, world, rank, local):
         draft_alg, draft_launches, bound = float(R * B * V * s_l), 1, "hbm"
         dname = "chain_scan_kernel+chain_pick_kernel"
     else:
-        # one GEMM + one inverse-CDF select per step: that step's rows of L
-        # and all of W
+        # one GEMM (+ one inverse-CDF select) per step: that step's rows of L
+        # and all of W (the RNN head's memo update reads A and U rows only)
         draft_alg, draft_launches, bound = float(R * V * s_l + w.r * V * 2), B, "hbm"
-        dname = "markov_gemm_kernel<sample>+draft_select_kernel"
+        dname = ("rnn_step_kernel+" if cyc.rnn else "") + (
+            "markov_gemm_kernel<sample>+draft_select_kernel" if cyc.sample else "markov_gemm_kernel<greedy>")
     if t_draft >= t_verify:
         kname = dname
         per_launch_s = t_draft / args.steps / draft_launches
@@ -528,6 +544,7 @@ def run_ours(args, w, world, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "R": R, "B": B, "V": V, "r": w.r, "decode": w.decode, "mode": w.modes[0],
                    "scheduler": None if cyc.tree else args.scheduler, "tau": tau, "observe": cyc.obs,
+                   "head": None if cyc.tree else args.head,
                    "parallelism": f"replicas{world}" if world > 1 else "single",
                    "l2": "flushed by a 256 MB write before every step",
                    "timed": "draft+schedule+pack+verify (CUDA events); target stand-in row gather excluded"},
@@ -598,7 +615,7 @@ def run_e2e(cyc, args, committed):
     import torch
 
     i = cyc.inp
-    keys = ("L", "anchor", "conf") + (("conf_stale",) if cyc.dynamic else ())
+    keys = ("L", "anchor", "conf") + (("conf_stale",) if cyc.dynamic else ()) + (("X_rnn",) if cyc.rnn else ())
     host = {k: i[k].cpu().pin_memory() for k in keys}
     host["target"] = cyc.target.cpu().pin_memory()
     out_h = torch.empty_like(cyc.vr["out_tok"], device="cpu").pin_memory()
@@ -614,6 +631,8 @@ def run_e2e(cyc, args, committed):
         i["conf"].copy_(host["conf"], non_blocking=True)
         if cyc.dynamic:
             i["conf_stale"].copy_(host["conf_stale"], non_blocking=True)
+        if cyc.rnn:
+            i["X_rnn"].copy_(host["X_rnn"], non_blocking=True)
         cyc.target.copy_(host["target"], non_blocking=True)
         if graphs:
             cyc.g_draft.replay()
@@ -644,6 +663,7 @@ def run_e2e(cyc, args, committed):
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False, observe=False, tau=None):
+    """(the RNN head drafts when inp holds its weights)"""
     """One oracle cycle for the requests idx (schedule over all requests);
     returns (seconds of oracle work, committed tokens)."""
     import numpy as np
@@ -678,8 +698,14 @@ def oracle_cycle(w, inp, idx, cycle_seed=0, dynamic=False, observe=False, tau=No
     sample = w.decode == "sample"
     ids = np.asarray(idx, np.int32)
     t0 = time.perf_counter()
-    dr = oracle.draft_chain(L, U, W, an, decode=oracle.SAMPLE if sample else oracle.GREEDY,
-                            temperature=w.temperature, seed=cycle_seed, req_ids=ids)
+    if "A_rnn" in inp:
+        X = np_of(inp["X_rnn"].index_select(0, idx_t.to(inp["X_rnn"].device)))
+        dr = oracle.draft_chain_rnn(L, U, W, np_of(inp["A_rnn"]), X, an,
+                                    decode=oracle.SAMPLE if sample else oracle.GREEDY, temperature=w.temperature,
+                                    seed=cycle_seed, req_ids=ids)
+    else:
+        dr = oracle.draft_chain(L, U, W, an, decode=oracle.SAMPLE if sample else oracle.GREEDY,
+                                temperature=w.temperature, seed=cycle_seed, req_ids=ids)
     if tau is not None:
         sc = oracle.schedule_threshold(conf, tau)
     elif dynamic:
@@ -729,6 +755,8 @@ def run_reference(args, w):
     from speculative_decoding_markov_gb300 import synthetic
 
     inp = synthetic.generate(w, seed=0, device="cpu")
+    if args.head == "rnn" and w.decode != "tree":
+        inp.update(synthetic.rnn_inputs(w, seed=0))
     dynamic = args.scheduler == "dynamic" and w.decode != "tree"
     observe = args.observe and w.decode != "tree"
     tau = args.tau if args.scheduler == "threshold" and w.decode != "tree" else None
@@ -748,7 +776,7 @@ def run_reference(args, w):
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
             "config": {"workload": w.name, "R": w.R, "B": w.B, "V": w.V, "r": w.r, "decode": w.decode,
                        "mode": w.modes[0], "scheduler": None if w.decode == "tree" else args.scheduler,
-                       "tau": tau, "observe": observe},
+                       "tau": tau, "observe": observe, "head": None if w.decode == "tree" else args.head},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 

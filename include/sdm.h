@@ -93,7 +93,8 @@ enum {
     SDM_OP_PACK = 3,
     SDM_OP_VERIFY = 4,
     SDM_OP_VERIFY_TREE = 5,
-    SDM_OP_TV_LABEL = 6
+    SDM_OP_TV_LABEL = 6,
+    SDM_OP_DRAFT_CHAIN_RNN = 7
 };
 
 /* Bytes of scratch the operation needs for these sizes (0 if none).  Pass the
@@ -159,6 +160,33 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
                            sdm_decode decode, float temperature, sdm_rng rng,
                            int32_t* tokens, float* logq, float* lse,
                            void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
+ * draft_chain_rnn: the chain draft with the RNN sequential head ([DSpark
+ * notes] sec. 4, "RNN head": a memo that carries the whole draft so far,
+ * updated once per step from the previous memo, the previous word and the
+ * current backbone state; the page's formula is not legible, the reading
+ * taken is)
+ *     m_0 = 0,  m_d = tanh(A m_{d-1} + U[y_{d-1}] + x_d)
+ *     z_d = L_d + bf16(m_d) . W
+ * then y_d as in draft_chain (greedy argmax, or the inverse-CDF draw of
+ * softmax(z_d / T) with the same random stream).  With A = 0 and x = 0 this
+ * is the Markov head on the table bf16(tanh(U)).
+ * In:  L [R, B, V] (dtL), U [V, r], W [r, V], A [r, r] (row j = output j),
+ *      X [R, B, r] (x_d: the backbone state at position d projected to r),
+ *      all bf16 but L; anchor [R].  Shapes and alignment as draft_chain.
+ * Out: tokens [R, B]; logq, lse [R, B] fp32 (sampling; may be NULL);
+ *      memo [R, B, r] fp32 = m_d per position (may be NULL).  The memo is
+ *      formed in fp32 (tanhf); the projection on the tensor cores with fp32
+ *      accumulation.
+ * ws:  sdm_workspace_size(SDM_OP_DRAFT_CHAIN_RNN, R, B, V, r, 0, 0, 0).
+ * Device checks as draft_chain (a token id outside [0, V) sets
+ * SDM_DEV_BAD_TOKEN and is read as 0).
+ */
+sdm_status sdm_draft_chain_rnn(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, const uint16_t* A,
+                               const uint16_t* X, const int32_t* anchor, int R, int B, int V, int r, sdm_decode decode,
+                               float temperature, sdm_rng rng, int32_t* tokens, float* logq, float* lse, float* memo,
+                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
  * draft_tree: PCTree drafting ([PCTree]: per parent p, z_d(p) = L_d +

@@ -20,13 +20,13 @@ LIB_PATH = os.path.join(HERE, "libsdm.so")
 BF16, FP32 = 0, 1
 GREEDY, SAMPLE = 0, 1
 STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
-OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE, OP_TV_LABEL = range(7)
+OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE, OP_TV_LABEL, OP_DRAFT_CHAIN_RNN = range(8)
 DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY, DEV_BAD_CLASS = 1, 2, 4, 8, 16, 32
 
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
            "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_schedule_threshold",
-           "sdm_threshold_sweep", "sdm_status_str",
+           "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str",
            "sdm_version")
 
 
@@ -65,6 +65,9 @@ def _declare(lib):
                                _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_verify_greedy_static.restype = _I
     lib.sdm_verify_greedy_static.argtypes = [_I, _VP, _I, _I, _VP, _VP, _VP, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP]
+    lib.sdm_draft_chain_rnn.restype = _I
+    lib.sdm_draft_chain_rnn.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, SdmRng, _VP, _VP, _VP,
+                                        _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_schedule_threshold.restype = _I
     lib.sdm_schedule_threshold.argtypes = [_VP, _I, _I, _F, _VP, _VP, _VP, _VP]
     lib.sdm_threshold_sweep.restype = _I
@@ -169,6 +172,31 @@ def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0
                                float(temperature), SdmRng(seed, cycle), _ptr(out["tokens"]), _ptr(out["logq"]),
                                _ptr(out["lse"]), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
     _check(st, "sdm_draft_chain")
+    out["dev_status"] = dev_status
+    return out
+
+
+def draft_chain_rnn(L, U, W, A, X, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0, out=None, ws=None,
+                    dev_status=None, memo=False):
+    """Chain draft with the RNN head (memo m_d = tanh(A m_{d-1} + U[y_{d-1}]
+    + x_d), logits L_d + bf16(m_d) W); memo=True also returns the memo."""
+    _need_cuda(L, U, W, A, X, anchor)
+    R, B, V = L.shape
+    r = U.shape[1]
+    dev = L.device
+    if out is None:
+        out = dict(tokens=torch.empty((R, B), dtype=torch.int32, device=dev),
+                   logq=torch.zeros((R, B), dtype=torch.float32, device=dev),
+                   lse=torch.zeros((R, B), dtype=torch.float32, device=dev))
+        if memo:
+            out["memo"] = torch.empty((R, B, r), dtype=torch.float32, device=dev)
+    ws = workspace(OP_DRAFT_CHAIN_RNN, R, B, V, r, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_draft_chain_rnn(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(_u16(A)), _ptr(_u16(X)),
+                                   _ptr(anchor), R, B, V, r, decode, float(temperature), SdmRng(seed, cycle),
+                                   _ptr(out["tokens"]), _ptr(out.get("logq")), _ptr(out.get("lse")),
+                                   _ptr(out.get("memo")), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_draft_chain_rnn")
     out["dev_status"] = dev_status
     return out
 

@@ -107,6 +107,11 @@ size_t ws_chain_pruned(int R, int B, int V) {
 
 size_t ws_chain(int R, int B, int V) { return std::max(ws_chain_dense(R, B, V), ws_chain_pruned(R, B, V)); }
 
+// RNN head: the dense chain's scratch, then the fp32 memo and its bf16 rows
+size_t ws_chain_rnn(int R, int B, int V, int r) {
+    return ws_chain_dense(R, B, V) + align256(static_cast<size_t>(R) * r * 4) + align256(static_cast<size_t>(R) * r * 2);
+}
+
 // block records [rows][nb], per-row top-k and log-sum-exp, frontier and pool
 size_t ws_tree(int R, int B, int P, int V) {
     const size_t rows = static_cast<size_t>(R) * P;
@@ -136,6 +141,116 @@ size_t ws_tv_label(int R, int gamma, int V, int row_capacity) {
            align256(slots * label_n_part(R, gamma, V) * 8);
 }
 
+// The dense chain draft: per step one tensor-core GEMM over all requests
+// (argmax keys, or block records and an inverse-CDF select).  With rnn set,
+// each step first updates the RNN head's memo and the GEMM's A rows are the
+// memo's (scratch after the chain's: fp32 memo [R, r], bf16 rows [R, r]).
+sdm_status draft_chain_dense(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                             const RnnStepParams* rnn, const int32_t* anchor, int R, int B, int V, int r,
+                             sdm_decode decode, float temperature, sdm_rng rng, int32_t* tokens, float* logq,
+                             float* lse, void* ws, int32_t* dev_status, cudaStream_t s) {
+    Carver c{static_cast<uint8_t*>(ws)};
+    auto* keys = c.take<unsigned long long>(static_cast<size_t>(B) * R);
+    const int nb = n_blocks16(V);
+    auto* blk = c.take<float2>(static_cast<size_t>(R) * nb);
+
+    RnnStepParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    if (rnn) {   // the memo state and its bf16 rows follow the chain's scratch
+        rp = *rnn;
+        rp.m = c.take<float>(static_cast<size_t>(R) * r);
+        rp.a_rows = c.take<uint16_t>(static_cast<size_t>(R) * r);
+        rp.R = R;
+        rp.B = B;
+        rp.V = V;
+        rp.r = r;
+        rp.anchor = anchor;
+        rp.keys = decode == SDM_GREEDY ? keys : nullptr;
+        rp.tokens = tokens;
+        rp.dev_status = dev_status;
+    }
+    const int fp32 = dtL == SDM_FP32;
+    const int l_rows = std::min(R, kTileM);
+    CUtensorMap tmW, tmL;
+    if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
+    const int mode = decode == SDM_GREEDY ? MODE_CHAIN_GREEDY : MODE_CHAIN_SAMPLE;
+    const int n_tiles = (V + kTileN - 1) / kTileN;
+    const int gy = (R + kTileM - 1) / kTileM;
+    const int gx = gemm_grid_x(n_tiles, gy);
+
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = R;
+    p.R = R;
+    p.B = B;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = n_tiles;
+    p.l_fp32 = fp32;
+    p.l_rows = l_rows;
+    p.P = 1;
+    p.k = 1;
+    gemm_pick_stages(p, mode);
+    p.inv_t = decode == SDM_SAMPLE ? 1.0f / temperature : 1.0f;
+    p.U = U;
+    p.a_rows = rnn ? rp.a_rows : nullptr;
+    p.anchor = anchor;
+    p.keys = keys;
+    p.tok_in = tokens;
+    p.blk = blk;
+    p.nb = nb;
+    p.dev_status = dev_status;
+
+    if (decode == SDM_GREEDY) {
+        SDM_CHECK_CUDA(launch_fill_u64(keys, static_cast<size_t>(B) * R, 0ull, s));
+        for (int d = 1; d <= B; ++d) {
+            p.d = d;
+            if (rnn) {
+                rp.d = d;
+                SDM_CHECK_CUDA(launch_rnn_step(rp, s));
+            }
+            SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
+        }
+        SDM_CHECK_CUDA(launch_chain_finalize(keys, R, B, V, tokens, dev_status, s));
+        return SDM_OK;
+    }
+    // sampling: per step the GEMM writes the block records, then one CTA per
+    // request draws y_d by the inverse CDF (the next step's GEMM reads it)
+    DraftSelectParams sp;
+    std::memset(&sp, 0, sizeof sp);
+    sp.blk = blk;
+    sp.nb = nb;
+    sp.R = R;
+    sp.B = B;
+    sp.V = V;
+    sp.r = r;
+    sp.L = L;
+    sp.l_fp32 = fp32;
+    sp.U = U;
+    sp.W = W;
+    sp.a_rows = p.a_rows;
+    sp.anchor = anchor;
+    sp.inv_t = p.inv_t;
+    sp.k0 = static_cast<uint32_t>(rng.seed);
+    sp.k1 = static_cast<uint32_t>(rng.seed >> 32);
+    sp.cycle = static_cast<uint32_t>(rng.cycle);
+    sp.tokens = tokens;
+    sp.logq = logq;
+    sp.lse = lse;
+    sp.dev_status = dev_status;
+    for (int d = 1; d <= B; ++d) {
+        p.d = d;
+        sp.d = d;
+        if (rnn) {
+            rp.d = d;
+            SDM_CHECK_CUDA(launch_rnn_step(rp, s));
+        }
+        SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
+        SDM_CHECK_CUDA(launch_draft_select(sp, s));
+    }
+    return SDM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -149,6 +264,7 @@ size_t sdm_workspace_size(int op, int R, int B, int V, int r, int P, int k, int 
         case SDM_OP_DRAFT_TREE: return ws_tree(R, B, P, V);
         case SDM_OP_VERIFY: return ws_verify(R, P, V);
         case SDM_OP_TV_LABEL: return ws_tv_label(R, B, V, P);
+        case SDM_OP_DRAFT_CHAIN_RNN: return ws_chain_rnn(R, B, V, r);
         case SDM_OP_VERIFY_TREE:
             return align256(static_cast<size_t>(R) * (N + 1) * 8 * std::max(n_chunks_of(V, 0), n_chunks_of(V, 1)));
         default: return 0;
@@ -263,81 +379,31 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
         SDM_CHECK_CUDA(launch_chain_pruned(pp, s));
         return SDM_OK;
     }
-    Carver c{static_cast<uint8_t*>(ws)};
-    auto* keys = c.take<unsigned long long>(static_cast<size_t>(B) * R);
-    const int nb = n_blocks16(V);
-    auto* blk = c.take<float2>(static_cast<size_t>(R) * nb);
+    return draft_chain_dense(L, dtL, U, W, nullptr, anchor, R, B, V, r, decode, temperature, rng, tokens, logq, lse,
+                             ws, dev_status, s);
+}
 
-    const int fp32 = dtL == SDM_FP32;
-    const int l_rows = std::min(R, kTileM);
-    CUtensorMap tmW, tmL;
-    if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
-    const int mode = decode == SDM_GREEDY ? MODE_CHAIN_GREEDY : MODE_CHAIN_SAMPLE;
-    const int n_tiles = (V + kTileN - 1) / kTileN;
-    const int gy = (R + kTileM - 1) / kTileM;
-    const int gx = gemm_grid_x(n_tiles, gy);
-
-    GemmParams p;
-    std::memset(&p, 0, sizeof p);
-    p.rows = R;
-    p.R = R;
-    p.B = B;
-    p.V = V;
-    p.r = r;
-    p.n_tiles = n_tiles;
-    p.l_fp32 = fp32;
-    p.l_rows = l_rows;
-    p.P = 1;
-    p.k = 1;
-    gemm_pick_stages(p, mode);
-    p.inv_t = decode == SDM_SAMPLE ? 1.0f / temperature : 1.0f;
-    p.U = U;
-    p.anchor = anchor;
-    p.keys = keys;
-    p.tok_in = tokens;
-    p.blk = blk;
-    p.nb = nb;
-    p.dev_status = dev_status;
-
-    if (decode == SDM_GREEDY) {
-        SDM_CHECK_CUDA(launch_fill_u64(keys, static_cast<size_t>(B) * R, 0ull, s));
-        for (int d = 1; d <= B; ++d) {
-            p.d = d;
-            SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
-        }
-        SDM_CHECK_CUDA(launch_chain_finalize(keys, R, B, V, tokens, dev_status, s));
-        return SDM_OK;
-    }
-    // sampling: per step the GEMM writes the block records, then one CTA per
-    // request draws y_d by the inverse CDF (the next step's GEMM reads it)
-    DraftSelectParams sp;
-    std::memset(&sp, 0, sizeof sp);
-    sp.blk = blk;
-    sp.nb = nb;
-    sp.R = R;
-    sp.B = B;
-    sp.V = V;
-    sp.r = r;
-    sp.L = L;
-    sp.l_fp32 = fp32;
-    sp.U = U;
-    sp.W = W;
-    sp.anchor = anchor;
-    sp.inv_t = p.inv_t;
-    sp.k0 = static_cast<uint32_t>(rng.seed);
-    sp.k1 = static_cast<uint32_t>(rng.seed >> 32);
-    sp.cycle = static_cast<uint32_t>(rng.cycle);
-    sp.tokens = tokens;
-    sp.logq = logq;
-    sp.lse = lse;
-    sp.dev_status = dev_status;
-    for (int d = 1; d <= B; ++d) {
-        p.d = d;
-        sp.d = d;
-        SDM_CHECK_CUDA(launch_markov_gemm(mode, tmW, tmL, p, gx, gy, s));
-        SDM_CHECK_CUDA(launch_draft_select(sp, s));
-    }
-    return SDM_OK;
+sdm_status sdm_draft_chain_rnn(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, const uint16_t* A,
+                               const uint16_t* X, const int32_t* anchor, int R, int B, int V, int r, sdm_decode decode,
+                               float temperature, sdm_rng rng, int32_t* tokens, float* logq, float* lse, float* memo,
+                               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!L || !U || !W || !A || !X || !anchor || !tokens || R <= 0 || B <= 0 || V <= 0 || r <= 0)
+        return SDM_ERR_INVALID_ARG;
+    if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (decode != SDM_GREEDY && decode != SDM_SAMPLE) return SDM_ERR_INVALID_ARG;
+    if (decode == SDM_SAMPLE && !(temperature > 0.f)) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W) || !aligned16(A))
+        return SDM_ERR_UNSUPPORTED;
+    if (decode == SDM_SAMPLE && V > kMaxSampleV) return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_chain_rnn(R, B, V, r)) return SDM_ERR_WORKSPACE;
+    RnnStepParams rp;
+    std::memset(&rp, 0, sizeof rp);
+    rp.A = A;
+    rp.U = U;
+    rp.X = X;
+    rp.memo_out = memo;
+    return draft_chain_dense(L, dtL, U, W, &rp, anchor, R, B, V, r, decode, temperature, rng, tokens, logq, lse, ws,
+                             dev_status, static_cast<cudaStream_t>(stream));
 }
 
 sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,

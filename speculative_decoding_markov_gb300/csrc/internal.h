@@ -81,6 +81,7 @@ struct GemmParams {
     int d;               // 1-based draft position / tree level
     float inv_t;         // 1 / temperature
     const uint16_t* U;   // [V, r]
+    const uint16_t* a_rows;     // chain modes: [R, r] bf16 A row of GEMM row m in place of U[tok(m)] (RNN memo), or NULL
     const int32_t* anchor;
     // chain
     unsigned long long* keys;   // greedy: [B][R] argmax keys
@@ -188,6 +189,7 @@ struct DraftSelectParams {
     int l_fp32;
     const uint16_t* U;       // [V, r]
     const uint16_t* W;       // [r, V]
+    const uint16_t* a_rows;  // [R, r] bf16 row of request i in place of U[prev] (RNN memo), or NULL
     const int32_t* anchor;
     float inv_t;
     uint32_t k0, k1, cycle;  // Philox key and cycle
@@ -318,6 +320,22 @@ cudaError_t launch_observe(const float* conf, const int32_t* cu, const int32_t* 
                            int gamma, int n_class, int n_bins, int32_t* hist, int32_t* reached, int32_t* hits,
                            int32_t* bin_n, int32_t* bin_hit, double* bin_conf, double* ece, int32_t* dev_status,
                            cudaStream_t s);
+
+// RNN head memo update (rnn.cu): m_d = tanh(A m_{d-1} + U[y_{d-1}] + x_d)
+struct RnnStepParams {
+    const uint16_t* A;                 // [r, r] bf16, row j = output j
+    const uint16_t* U;                 // [V, r] bf16 token table
+    const uint16_t* X;                 // [R, B, r] bf16 projected backbone states
+    const int32_t* anchor;             // [R] y_0
+    const unsigned long long* keys;    // greedy: [B][R] argmax keys (y_{d-1} from keys[d-2]), else NULL
+    const int32_t* tokens;             // sampling: [R, B] drawn tokens (y_{d-1} = column d-2)
+    int R, B, V, r, d;
+    float* m;                          // [R, r] fp32 memo: m_{d-1} in, m_d out
+    uint16_t* a_rows;                  // [R, r] bf16(m_d)
+    float* memo_out;                   // [R, B, r] fp32 trajectory, or NULL
+    int32_t* dev_status;
+};
+cudaError_t launch_rnn_step(const RnnStepParams& p, cudaStream_t s);
 
 // Fixed-threshold verify length and its sweep (threshold.cu)
 cudaError_t launch_schedule_threshold(const float* conf, int R, int gamma, float tau, int32_t* budget,

@@ -643,7 +643,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int kchunks = p.r >> 3;
     for (int rr = warp; rr < kTileM; rr += kGemmThreads / 32) {
         const int tok = gemm_row_token<MODE>(p, row0 + rr);
-        const uint16_t* src = p.U + static_cast<size_t>(tok < 0 ? 0 : tok) * p.r;
+        const uint16_t* src = (p.a_rows && tok >= 0) ? p.a_rows + static_cast<size_t>(row0 + rr) * p.r
+                                                     : p.U + static_cast<size_t>(tok < 0 ? 0 : tok) * p.r;
         for (int q = lane; q < kchunks; q += 32) {
             uint8_t* dst = sA + (q >> 3) * (kTileM * 128) + rr * 128 + (((q & 7) ^ (rr & 7)) << 4);
             cp_async_16(dst, src + q * 8, tok < 0 ? 0u : 16u);

@@ -392,7 +392,10 @@ __global__ void __launch_bounds__(kSelThreads) draft_select_kernel(const DraftSe
     const int v0 = b * kBlockCols;
     const int v = v0 + tid;
     const float lv = (tid < kBlockCols && v < p.V) ? load_elem(p.L, p.l_fp32, o * p.V + v) : 0.f;
-    markov16(p.U, p.W, prev, p.r, p.V, v0, sh);
+    if (p.a_rows)   // RNN head: the request's memo row stands where U[prev] does
+        markov16(p.a_rows, p.W, i, p.r, p.V, v0, sh);
+    else
+        markov16(p.U, p.W, prev, p.r, p.V, v0, sh);
     if (tid < 32) {
         float zt = -INFINITY, w = 0.f;
         if (tid < kBlockCols && v < p.V) {
