@@ -609,8 +609,8 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     if (decode == SDM_GREEDY) {
         sp.keys = row_keys;
         SDM_CHECK_CUDA(launch_stream(STREAM_ARGMAX, sp, row_capacity, s));
-        SDM_CHECK_CUDA(launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, row_keys, sp.n_chunks, R, gamma, V, accept,
-                                                     ceiling, out_tok, n_out, dev_status, s));
+        SDM_CHECK_CUDA(launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, row_keys, sp.n_chunks, R, gamma,
+                                                     V, row_capacity, accept, ceiling, out_tok, n_out, dev_status, s));
         return SDM_OK;
     }
     // rejection sampling

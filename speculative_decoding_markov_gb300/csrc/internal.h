@@ -161,10 +161,11 @@ cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32
                         const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
                         int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s);
 
+// rows_avail: the packed rows the keys cover (a window past them is flagged)
 cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
                                           const unsigned long long* row_keys, int n_chunks, int R, int gamma, int V,
-                                          int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
-                                          int32_t* dev_status, cudaStream_t s);
+                                          int rows_avail, int32_t* accept, int32_t* ceiling, int32_t* out_tok,
+                                          int32_t* n_out, int32_t* dev_status, cudaStream_t s);
 
 // Sample verify, step 2: per request, merge row LSE partials, run the
 // left-to-right accept tests and choose the final row (residual or bonus).

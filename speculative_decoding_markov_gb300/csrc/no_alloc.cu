@@ -79,8 +79,8 @@ extern "C" sdm_status sdm_verify_greedy_static(sdm_vmode mode, const void* targe
     sp.inv_t = 1.0f;
     sp.keys = keys;   // every (row, chunk) partial read below is written first in this call
     if (launch_stream(STREAM_ARGMAX, sp, row_capacity, s) != cudaSuccess) return SDM_ERR_CUDA;
-    if (launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, keys, n_chunks, R, gamma, V, accept, ceiling,
-                                      out_tok, n_out, dev_status, s) != cudaSuccess)
+    if (launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, keys, n_chunks, R, gamma, V, row_capacity,
+                                      accept, ceiling, out_tok, n_out, dev_status, s) != cudaSuccess)
         return SDM_ERR_CUDA;
     return SDM_OK;
 }

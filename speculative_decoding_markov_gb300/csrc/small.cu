@@ -3,6 +3,7 @@
 // and PCTree's per-level merge/prune and final top-N selection.
 #include "device.cuh"
 #include "internal.h"
+#include "verify_greedy.cuh"
 
 namespace sdm {
 namespace {
@@ -482,78 +483,23 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
     }
 }
 
-// Argmax token of a row from its per-chunk partial keys (eight loads in
-// flight at a time).
-__device__ __forceinline__ int row_token(const unsigned long long* part, size_t row, int n_chunks) {
-    const unsigned long long* q = part + row * n_chunks;
-    unsigned long long k[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
-    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (c0 + j < n_chunks) k[j] = umax64(k[j], q[c0 + j]);
-    }
-#pragma unroll
-    for (int j = 1; j < 8; ++j) k[0] = umax64(k[0], k[j]);
-    return static_cast<int>(key_token(k[0]));
-}
 
 // ---------------------------------------------------------------------------
 // greedy verification: first mismatch per request
 // ---------------------------------------------------------------------------
 __global__ void verify_greedy_finalize_kernel(int mode, const int32_t* cu, const int32_t* draft,
                                               const int32_t* budget, const unsigned long long* row_keys, int n_chunks,
-                                              int R, int gamma, int V, int32_t* accept, int32_t* ceiling,
-                                              int32_t* out_tok, int32_t* n_out, int32_t* dev_status) {
+                                              int R, int gamma, int V, int rows_avail, int32_t* accept,
+                                              int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+                                              int32_t* dev_status) {
     // one warp per request: lane p resolves window rows p, p + 32, ...
     pdl_wait();
     pdl_trigger();
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= R) return;
-    const int row0 = cu[i];
-    int w = cu[i + 1] - row0 - 1;
-    if (w < 0 || w > gamma) {
-        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
-        w = w < 0 ? 0 : gamma;
-    }
-    int cap = w;
-    if (mode == SDM_CAP_ACCEPT) {
-        cap = budget[i];
-        if (cap < 0 || cap > w) {
-            if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
-            cap = cap < 0 ? 0 : w;
-        }
-    }
-    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
-    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
-    // A = first p < w with y_{p+1} != argmax of row p, else w
-    int A = w;
-    for (int base = 0; base < w && A == w; base += 32) {
-        const int p = base + lane;
-        const bool mism = p < w && y[p] != row_token(row_keys, static_cast<size_t>(row0 + p), n_chunks);
-        const unsigned bal = __ballot_sync(0xffffffffu, mism);
-        if (bal) A = base + __ffs(bal) - 1;
-    }
-    const int a = A < cap ? A : cap;
-    for (int p = lane; p <= gamma; p += 32) {
-        if (p < a) {
-            o[p] = y[p];
-        } else if (p == a) {
-            int t = row_token(row_keys, static_cast<size_t>(row0 + a), n_chunks);
-            if (t < 0 || t >= V) {
-                set_status(dev_status, SDM_DEV_BAD_TOKEN);
-                t = 0;
-            }
-            o[p] = t;
-        } else {
-            o[p] = -1;
-        }
-    }
-    if (lane == 0) {
-        accept[i] = a;
-        n_out[i] = a + 1;
-        if (ceiling) ceiling[i] = A;
-    }
+    greedy_resolve(i, lane, mode, cu, draft, budget, row_keys, n_chunks, gamma, V, rows_avail, accept, ceiling, out_tok,
+                   n_out, dev_status);
 }
 
 // ---------------------------------------------------------------------------
@@ -931,11 +877,11 @@ cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32
 
 cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,
                                           const unsigned long long* row_keys, int n_chunks, int R, int gamma, int V,
-                                          int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
-                                          int32_t* dev_status, cudaStream_t s) {
+                                          int rows_avail, int32_t* accept, int32_t* ceiling, int32_t* out_tok,
+                                          int32_t* n_out, int32_t* dev_status, cudaStream_t s) {
     return launch_pdl(verify_greedy_finalize_kernel, dim3(blocks_for(static_cast<long long>(R) * 32, 128)), dim3(128),
-                      0, s, mode, cu, draft, budget, row_keys, n_chunks, R, gamma, V, accept, ceiling, out_tok, n_out,
-                      dev_status);
+                      0, s, mode, cu, draft, budget, row_keys, n_chunks, R, gamma, V, rows_avail, accept, ceiling,
+                      out_tok, n_out, dev_status);
 }
 
 cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t* anchor, const int32_t* draft,

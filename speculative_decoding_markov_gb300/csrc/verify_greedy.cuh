@@ -1,0 +1,95 @@
+// verify_greedy.cuh - greedy verification of one request from the per-chunk
+// argmax keys of its window rows ([DSpark notes] sec. 1: left-to-right
+// acceptance, discard after the first mismatch, one bonus token; [SGLang]
+// "three verify modes").  Shared by the stand-alone finalize kernel and the
+// argmax stream that resolves a request as soon as its last row is done.
+#pragma once
+#include "device.cuh"
+#include "internal.h"
+
+namespace sdm {
+
+// Argmax token of a row from its per-chunk partial keys (eight loads in
+// flight at a time, through L2).
+__device__ __forceinline__ int row_token(const unsigned long long* part, size_t row, int n_chunks) {
+    const unsigned long long* q = part + row * n_chunks;
+    unsigned long long k[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (c0 + j < n_chunks) k[j] = umax64(k[j], __ldcg(q + c0 + j));
+    }
+#pragma unroll
+    for (int j = 1; j < 8; ++j) k[0] = umax64(k[0], k[j]);
+    return static_cast<int>(key_token(k[0]));
+}
+
+// Request i, resolved by one warp (lane p checks window rows p, p + 32, ...):
+//   A = the first p < w with y_{p+1} != argmax of row p, else w;
+//   commit a = A (min(A, budget) in CAP_ACCEPT) drafts and the target token
+//   of row a; ceiling = A.
+// A request without rows, or with rows past the rows_avail the keys cover,
+// is flagged and commits one token (0) with accept 0; a window longer than
+// gamma is flagged and cut to gamma.
+__device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const int32_t* cu, const int32_t* draft,
+                                               const int32_t* budget, const unsigned long long* row_keys,
+                                               int n_chunks, int gamma, int V, int rows_avail, int32_t* accept,
+                                               int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+                                               int32_t* dev_status) {
+    const int row0 = cu[i];
+    const int row1 = cu[i + 1];
+    int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
+    if (row1 <= row0 || row0 < 0 || row1 > rows_avail) {
+        for (int p = lane; p <= gamma; p += 32) o[p] = p == 0 ? 0 : -1;
+        if (lane == 0) {
+            set_status(dev_status, row1 > rows_avail ? SDM_DEV_CAPACITY : SDM_DEV_BAD_WINDOW);
+            accept[i] = 0;
+            n_out[i] = 1;
+            if (ceiling) ceiling[i] = 0;
+        }
+        return;
+    }
+    int w = row1 - row0 - 1;
+    if (w > gamma) {
+        if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
+        w = gamma;
+    }
+    int cap = w;
+    if (mode == SDM_CAP_ACCEPT) {
+        cap = budget[i];
+        if (cap < 0 || cap > w) {
+            if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
+            cap = cap < 0 ? 0 : w;
+        }
+    }
+    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    int A = w;
+    for (int base = 0; base < w && A == w; base += 32) {
+        const int p = base + lane;
+        const bool mism = p < w && y[p] != row_token(row_keys, static_cast<size_t>(row0 + p), n_chunks);
+        const unsigned bal = __ballot_sync(0xffffffffu, mism);
+        if (bal) A = base + __ffs(bal) - 1;
+    }
+    const int a = A < cap ? A : cap;
+    for (int p = lane; p <= gamma; p += 32) {
+        if (p < a) {
+            o[p] = y[p];
+        } else if (p == a) {
+            int t = row_token(row_keys, static_cast<size_t>(row0 + a), n_chunks);
+            if (t < 0 || t >= V) {
+                set_status(dev_status, SDM_DEV_BAD_TOKEN);
+                t = 0;
+            }
+            o[p] = t;
+        } else {
+            o[p] = -1;
+        }
+    }
+    if (lane == 0) {
+        accept[i] = a;
+        n_out[i] = a + 1;
+        if (ceiling) ceiling[i] = A;
+    }
+}
+
+}  // namespace sdm

@@ -394,6 +394,41 @@ def test_verify_greedy_empty_windows():
     np.testing.assert_array_equal(host(out["out_tok"]), ref["out_tok"])
 
 
+def test_verify_greedy_flags_bad_windows_without_waiting():
+    """A window without rows and a window past the packed rows are resolved
+    as flagged failures (accept 0, one token 0); the other requests are
+    verified as usual."""
+    w = small(R=6, B=4, V=1024, r=64, l_dtype=BF16, target_dtype=BF16)
+    inp = synthetic.generate(w, seed=4)
+    an = np_of(inp["anchor"])
+    dr = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), an)
+    pk = oracle.pack_ragged(an, dr["tokens"], None, np.array([64], np.int32))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    rows = int(pk["cu_seqlens"][-1])
+    packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"][:rows]),
+                                     torch.as_tensor(pk["packed_pos"][:rows]))
+    ref = oracle.verify(oracle.STATIC, oracle.GREEDY, np_of(packed), pk["cu_seqlens"], an, dr["tokens"])
+    for bad, bit in (("inverted", sdm.DEV_BAD_WINDOW), ("past", sdm.DEV_CAPACITY)):
+        cu = pk["cu_seqlens"].copy()
+        if bad == "inverted":
+            cu[3] = cu[2] - 1                    # request 2 inverted; request 3 grows
+        else:
+            cu[-1] = rows + 3                    # the last request runs past the buffer
+        st = sdm.new_status(DEV)
+        out = sdm.verify(sdm.STATIC, sdm.GREEDY, dev(packed), dev(torch.from_numpy(cu)), dev(inp["anchor"]),
+                         dev(torch.from_numpy(dr["tokens"])), dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) & bit
+        flagged = 2 if bad == "inverted" else w.R - 1
+        assert host(out["accept"])[flagged] == 0 and host(out["n_out"])[flagged] == 1
+        assert host(out["out_tok"])[flagged, 0] == 0
+        for i in range(w.R - 1):
+            if bad == "inverted" and i in (2, 3):   # request 3 took request 2's rows
+                continue
+            assert host(out["accept"])[i] == ref["accept"][i]
+            np.testing.assert_array_equal(host(out["out_tok"])[i], ref["out_tok"][i])
+
+
 # ---------------------------------------------------------------------------
 # verify (rejection sampling)
 # ---------------------------------------------------------------------------
