@@ -819,7 +819,8 @@ sdm_status sdm_observe(const float* conf, const int32_t* cu_seqlens, const int32
         !ece)
         return SDM_ERR_INVALID_ARG;
     if (R <= 0 || gamma <= 0 || n_class <= 0 || n_bins <= 0) return SDM_ERR_INVALID_ARG;
-    if (n_class > 4096 || n_bins > 4096 || gamma > 4096 || observe_smem_bytes(gamma, n_class, n_bins) > 49152)
+    if (n_class > 4096 || n_bins > 4096 || gamma > 4096 || observe_smem_bytes(gamma, n_class, n_bins) > 49152 ||
+        static_cast<long long>(R) * gamma > (1LL << 30))
         return SDM_ERR_UNSUPPORTED;
     SDM_CHECK_CUDA(launch_observe(conf, cu_seqlens, ceiling, cls, R, gamma, n_class, n_bins, hist, reached, hits,
                                   bin_n, bin_hit, bin_conf, ece, dev_status, static_cast<cudaStream_t>(stream)));
