@@ -9,18 +9,20 @@
 
 namespace sdm {
 
-// Argmax token of a row from its per-chunk partial keys (eight loads in
+// Argmax token of a row from its per-chunk partial keys (sixteen loads in
 // flight at a time, through L2).
 __device__ __forceinline__ int row_token(const unsigned long long* part, size_t row, int n_chunks) {
     const unsigned long long* q = part + row * n_chunks;
-    unsigned long long k[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
-    for (int c0 = 0; c0 < n_chunks; c0 += 8) {
+    unsigned long long k[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+    for (int j = 0; j < 16; ++j) k[j] = 0ull;
+    for (int c0 = 0; c0 < n_chunks; c0 += 16) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
             if (c0 + j < n_chunks) k[j] = umax64(k[j], __ldcg(q + c0 + j));
     }
 #pragma unroll
-    for (int j = 1; j < 8; ++j) k[0] = umax64(k[0], k[j]);
+    for (int j = 1; j < 16; ++j) k[0] = umax64(k[0], k[j]);
     return static_cast<int>(key_token(k[0]));
 }
 
@@ -63,19 +65,24 @@ __device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const 
         }
     }
     const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    // the first 32 window rows (the row after the last draft included) in
+    // one round: lane p holds row p's target token
+    const int t0 = lane <= w ? row_token(row_keys, static_cast<size_t>(row0 + lane), n_chunks) : -1;
     int A = w;
     for (int base = 0; base < w && A == w; base += 32) {
         const int p = base + lane;
-        const bool mism = p < w && y[p] != row_token(row_keys, static_cast<size_t>(row0 + p), n_chunks);
+        const int tp = base == 0 ? t0 : (p < w ? row_token(row_keys, static_cast<size_t>(row0 + p), n_chunks) : -1);
+        const bool mism = p < w && y[p] != tp;
         const unsigned bal = __ballot_sync(0xffffffffu, mism);
         if (bal) A = base + __ffs(bal) - 1;
     }
     const int a = A < cap ? A : cap;
+    const int ta = __shfl_sync(0xffffffffu, t0, a & 31);
     for (int p = lane; p <= gamma; p += 32) {
         if (p < a) {
             o[p] = y[p];
         } else if (p == a) {
-            int t = row_token(row_keys, static_cast<size_t>(row0 + a), n_chunks);
+            int t = a < 32 ? ta : row_token(row_keys, static_cast<size_t>(row0 + a), n_chunks);
             if (t < 0 || t >= V) {
                 set_status(dev_status, SDM_DEV_BAD_TOKEN);
                 t = 0;
