@@ -269,11 +269,13 @@ def _tiered_cost(R, g, rng):
     return float(rng.uniform(0.5, 3.0)) + float(rng.uniform(0.001, 0.02)) * t
 
 
-@pytest.mark.parametrize("R,g,seed", [(1, 4, 0), (4, 7, 1), (64, 7, 2), (256, 8, 3), (450, 8, 4), (37, 3, 5)])
+@pytest.mark.parametrize("R,g,seed", [(1, 4, 0), (4, 7, 1), (64, 7, 2), (256, 8, 3), (450, 8, 4), (37, 3, 5),
+                                      (256, 16, 6), (512, 16, 7)])   # the rejection-sampling shape; R gamma = 8192
 def test_schedule_dynamic(R, g, seed):
     """Capacity, budgets, survivals, E and N bit-exact against the oracle on a
-    tiered cost table (R * (gamma + 1) < 4096: fp64 sums exact in any order);
-    450 x 8 sorts 4096 keys, several per thread."""
+    tiered cost table (E stays below 4096 at these shapes, so the fp64 sums of
+    survivals >= 2^-18 are exact in any order); 450 x 8 sorts 4096 keys and
+    512 x 16 the largest supported set, several per thread."""
     rng = np.random.default_rng(seed)
     now = rng.uniform(0.02, 1.0, (R, g)).astype(np.float32)
     stale = np.clip(now + rng.normal(0, 0.2, (R, g)), 0.02, 1.0).astype(np.float32)
