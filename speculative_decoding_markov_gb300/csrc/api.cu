@@ -620,7 +620,8 @@ sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_
     SDM_CHECK_CUDA(launch_stream(STREAM_LSE, sp, row_capacity, s));
     SDM_CHECK_CUDA(launch_verify_sample_scan(mode, cu_seqlens, anchor, draft, budget, logq, target, t_fp32, V, lse_part,
                                              sp.n_chunks, sp.inv_t, k0, k1, cyc, R, gamma, accept, ceiling, res_tok,
-                                             res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, dev_status, s));
+                                             res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, row_capacity,
+                                             dev_status, s));
     // residual rows: recompute q with the Markov head; records of max(0, p - q)
     CUtensorMap tmW;
     if (!map_w(&tmW, W, r, V)) return SDM_ERR_CUDA;

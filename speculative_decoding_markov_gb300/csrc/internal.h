@@ -174,8 +174,8 @@ cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t
                                       int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
                                       uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
                                       int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
-                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int32_t* dev_status,
-                                      cudaStream_t s);
+                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int rows_avail,
+                                      int32_t* dev_status, cudaStream_t s);
 
 // ---------------------------------------------------------------------------
 // Inverse-CDF draws (select.cu).  A draw walks a row's (m, s) records, whose

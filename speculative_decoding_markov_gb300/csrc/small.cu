@@ -511,7 +511,7 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
                                           uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
                                           int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
                                           float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos,
-                                          int32_t* dev_status) {
+                                          int rows_avail, int32_t* dev_status) {
     // one warp per request; lane p runs the accept test of window row p (all
     // rows at once, each from its own partials), the first failure wins
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -519,10 +519,27 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
     if (i >= R) return;
     const RngKey rk{k0, k1, cycle};
     const int row0 = cu[i];
-    int w = cu[i + 1] - row0 - 1;
-    if (w < 0 || w > gamma) {
+    const int row1 = cu[i + 1];
+    if (row1 <= row0 || row0 < 0 || row1 > rows_avail) {
+        // no rows, or rows past the packed buffer: flagged, and neither a
+        // residual nor a bonus draw (the resample kernel commits token 0)
+        if (lane == 0) {
+            set_status(dev_status, row1 > rows_avail ? SDM_DEV_CAPACITY : SDM_DEV_BAD_WINDOW);
+            accept[i] = 0;
+            if (ceiling) ceiling[i] = 0;
+            res_tok[i] = -1;
+            res_pos[i] = 0;
+            res_trow[i] = 0;
+            res_lse_p[i] = 0.f;
+            bonus_row[i] = -1;
+            bonus_pos[i] = 0;
+        }
+        return;
+    }
+    int w = row1 - row0 - 1;
+    if (w > gamma) {
         if (lane == 0) set_status(dev_status, SDM_DEV_BAD_WINDOW);
-        w = w < 0 ? 0 : gamma;
+        w = gamma;
     }
     int cap = w;
     if (mode == SDM_CAP_ACCEPT) {
@@ -889,11 +906,11 @@ cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t
                                       int V, const float2* lse_part, int n_chunks, float inv_t, uint32_t k0,
                                       uint32_t k1, uint32_t cycle, int R, int gamma, int32_t* accept,
                                       int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
-                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int32_t* dev_status,
-                                      cudaStream_t s) {
+                                      float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int rows_avail,
+                                      int32_t* dev_status, cudaStream_t s) {
     verify_sample_scan_kernel<<<blocks_for(static_cast<long long>(R) * 32, 128), 128, 0, s>>>(
         mode, cu, anchor, draft, budget, logq, target, t_fp32, V, lse_part, n_chunks, inv_t, k0, k1, cycle, R, gamma,
-        accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, dev_status);
+        accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, rows_avail, dev_status);
     return cudaGetLastError();
 }
 

@@ -469,6 +469,39 @@ def test_verify_sample(mode, case, T):
         np.testing.assert_array_equal(host(out["ceiling"]), ref["ceiling"])
 
 
+def test_verify_sample_flags_windows_past_the_buffer():
+    """A window whose rows run past the packed buffer is flagged and commits
+    one token (0) with accept 0; the other requests are verified as usual."""
+    w = small(R=8, B=4, V=2048, r=64, l_dtype=BF16, target_dtype=FP32, sigma=(0.5,), temperature=1.0)
+    inp = synthetic.generate(w, seed=13)
+    an = np_of(inp["anchor"])
+    U, W = np_of(inp["U"]), np_of(inp["W"])
+    dr = oracle.draft_chain(np_of(inp["L"]), U, W, an, decode=oracle.SAMPLE, seed=2, cycle=0)
+    logq32, lse32 = dr["logq"].astype(np.float32), dr["lse"].astype(np.float32)
+    pk = oracle.pack_ragged(an, dr["tokens"], None, np.array([64], np.int32))
+    rows = int(pk["cu_seqlens"][-1])
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    packed = synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"][:rows]),
+                                     torch.as_tensor(pk["packed_pos"][:rows]))
+    ref = oracle.verify(oracle.STATIC, oracle.SAMPLE, np_of(packed), pk["cu_seqlens"], an, dr["tokens"],
+                        logq=logq32.astype(np.float64), lse_q=lse32.astype(np.float64), L=np_of(inp["L"]), U=U, W=W,
+                        seed=2, cycle=0)
+    cu = pk["cu_seqlens"].copy()
+    cu[-1] = rows + 5                            # the last request runs past the buffer
+    st = sdm.new_status(DEV)
+    out = sdm.verify(sdm.STATIC, sdm.SAMPLE, dev(packed), dev(torch.from_numpy(cu)), dev(inp["anchor"]),
+                     dev(torch.from_numpy(dr["tokens"])), logq=dev(torch.from_numpy(logq32)),
+                     lse_q=dev(torch.from_numpy(lse32)), L=dev(inp["L"]), U=dev(inp["U"]), W=dev(inp["W"]),
+                     seed=2, cycle=0, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & sdm.DEV_CAPACITY
+    last = w.R - 1
+    assert host(out["accept"])[last] == 0 and host(out["n_out"])[last] == 1 and host(out["out_tok"])[last, 0] == 0
+    for i in range(w.R - 1):
+        assert host(out["accept"])[i] == ref["accept"][i] or ref["margin"][i] < TIE
+        np.testing.assert_array_equal(host(out["out_tok"])[i], ref["out_tok"][i])
+
+
 # ---------------------------------------------------------------------------
 # PCTree
 # ---------------------------------------------------------------------------
