@@ -312,10 +312,10 @@ sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const in
  *      allocated in target (an upper bound on cu[R]).
  * Out: accept [R], ceiling [R] (may be NULL), out_tok [R, gamma+1] (-1
  *      padded), n_out [R] = accept + 1.
- * Greedy: a request without rows (cu[i+1] <= cu[i]) sets SDM_DEV_BAD_WINDOW,
- * one whose rows run past row_capacity sets SDM_DEV_CAPACITY; such a request
- * commits one token (0) with accept 0.  A window longer than gamma is
- * flagged (SDM_DEV_BAD_WINDOW) and cut to gamma.
+ * A request without rows (cu[i+1] <= cu[i]) sets SDM_DEV_BAD_WINDOW, one
+ * whose rows run past row_capacity sets SDM_DEV_CAPACITY; such a request
+ * commits one token (0) with accept 0 (greedy and sample).  A window longer
+ * than gamma is flagged (SDM_DEV_BAD_WINDOW) and cut to gamma.
  */
 sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_rng rng,
                       const void* target, sdm_dtype dtT, int row_capacity, const int32_t* cu_seqlens,
