@@ -83,7 +83,7 @@ def measured_peaks():
 KERNEL_SOURCES = {   # the files whose text fixes each reported kernel's code
     "chain_scan_kernel+chain_pick_kernel": ("chain_pruned.cu", "device.cuh", "internal.h"),
     "markov_gemm_kernel<sample>+draft_select_kernel": ("markov_gemm.cu", "select.cu", "device.cuh", "internal.h"),
-    "markov_gemm_kernel<tree>": ("markov_gemm.cu", "device.cuh", "internal.h"),
+    "markov_gemm_kernel<tree>+tree_select_kernel": ("markov_gemm.cu", "select.cu", "device.cuh", "internal.h"),
     "row_stream_kernel<argmax>": ("stream.cu", "device.cuh", "internal.h"),
 }
 
@@ -486,9 +486,12 @@ def run_ours(args, w, world, rank, local):
     s_t = 2 if w.target_dtype == 0 else 4
     verify_bytes = windows * V * s_t                            # every verified target row once
     if cyc.tree:
-        # one tensor-core launch per level: 2 * (R * P rows) * r * V flops
-        draft_alg, draft_launches, bound = 2.0 * R * w.P * w.r * V, B, "tensor"
-        dname = "markov_gemm_kernel<tree>"
+        # one tensor-core launch per level: 2 (R P) r V flops over W (2 r V
+        # bytes) and the level's L rows (R V s_L): about 227 flop per byte at
+        # R = 32, P = 8, r = 256, below the measured ridge (~255), so the
+        # level is HBM-bound; its algorithmic bytes are W and the L rows
+        draft_alg, draft_launches, bound = float(R * V * s_l + w.r * V * 2), B, "hbm"
+        dname = "markov_gemm_kernel<tree>+tree_select_kernel"
     elif cyc.prepared is not None:
         # the pruned greedy chain must read every element of L once (the few
         # W^T rows it scores are not counted)
@@ -564,7 +567,7 @@ def run_ours(args, w, world, rank, local):
         "roofline": {"bound": bound, "kernel": kname, "achieved": achieved, "peak": peak, "unit": unit,
                      "frac": achieved / peak, "peak_source": peak_kind, "traffic": traffic,
                      "algorithmic": {"draft_per_launch": draft_alg, "draft_launches_per_cycle": draft_launches,
-                                     "draft_unit": "flop" if cyc.tree else "byte",
+                                     "draft_unit": "byte",
                                      "verify_bytes_per_cycle": verify_bytes, "L_bytes_per_cycle": draft_bytes}},
         "gpu_launches": cyc.launches_per_step() * args.steps,
         "device_status": status,
