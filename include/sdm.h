@@ -60,9 +60,11 @@ typedef enum {
     SDM_OK = 0,
     SDM_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, bad enum */
     SDM_ERR_UNSUPPORTED = 2,   /* shape or alignment outside the constraints */
-    SDM_ERR_TIER_OVERFLOW = 3, /* reserved: strict tier mode */
+    SDM_ERR_TIER_OVERFLOW = 3, /* strict tier mode: packed total above every tier (from sdm_status_of_device) */
     SDM_ERR_CUDA = 4,          /* a CUDA runtime or driver call failed */
-    SDM_ERR_WORKSPACE = 5      /* ws is NULL or smaller than required */
+    SDM_ERR_WORKSPACE = 5,     /* ws is NULL or smaller than required */
+    SDM_ERR_DEVICE = 6,        /* a device-side input check failed (from sdm_status_of_device) */
+    SDM_ERR_TIMEOUT = 7        /* a bounded device wait ran out (from sdm_status_of_device) */
 } sdm_status;
 
 typedef enum { SDM_BF16 = 0, SDM_FP32 = 1 } sdm_dtype;
@@ -76,8 +78,16 @@ enum {
     SDM_DEV_TIMEOUT = 4,          /* a bounded pipeline wait ran out */
     SDM_DEV_BAD_WINDOW = 8,       /* budget or cu_seqlens window outside [0, gamma] */
     SDM_DEV_CAPACITY = 16,        /* packed rows would exceed the given capacity */
-    SDM_DEV_BAD_CLASS = 32        /* a request class id outside [0, n_class) */
+    SDM_DEV_BAD_CLASS = 32,       /* a request class id outside [0, n_class) */
+    SDM_DEV_TIER_OVERFLOW = 64    /* strict pack: packed total above every tier */
 };
+
+/* The status a caller reports for the device bits it read back after
+ * synchronising: SDM_OK for 0 or SDM_DEV_TIER_UNCAPTURED alone (informational:
+ * the caller runs that cycle uncaptured); else, by precedence,
+ * SDM_ERR_TIMEOUT (SDM_DEV_TIMEOUT), SDM_ERR_TIER_OVERFLOW
+ * (SDM_DEV_TIER_OVERFLOW), SDM_ERR_DEVICE (any other bit). */
+sdm_status sdm_status_of_device(int32_t dev_status_bits);
 
 /* Philox key material: key = seed, counter word 3 = cycle. */
 typedef struct {
@@ -270,9 +280,12 @@ sdm_status sdm_schedule_dynamic(const float* conf, const float* conf_stale, int 
  *   rows cu[i] .. cu[i] + n_i hold y_0 (anchor), y_1 .. y_{n_i}, with
  *   packed_req = i and packed_pos = 0..n_i; rows total .. capacity-1 hold -1.
  *   tier = smallest tiers[q] >= total; above every tier: tier = total and
- *   SDM_DEV_TIER_UNCAPTURED is set (the caller runs uncaptured).
+ *   SDM_DEV_TIER_UNCAPTURED is set (the caller runs uncaptured), or, with
+ *   strict != 0, SDM_DEV_TIER_OVERFLOW instead (a caller that only runs
+ *   captured tiers maps it to SDM_ERR_TIER_OVERFLOW with
+ *   sdm_status_of_device; the rows are packed the same way).
  * In:  anchor [R], draft [R, gamma], budget [R] or NULL, tiers [n_tiers]
- *      int32 (device).
+ *      int32 (device), strict (0 or 1).
  * Out: cu_seqlens [R+1], packed_tok/req/pos [capacity], tier [1] (device);
  *      tier_host (host, may be NULL): if non-NULL it must be pinned host
  *      memory and receives the tier by an async copy on `stream`.
@@ -280,7 +293,7 @@ sdm_status sdm_schedule_dynamic(const float* conf, const float* conf_stale, int 
  * capacity are dropped and SDM_DEV_CAPACITY is set.
  */
 sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,
-                           int R, int gamma, const int32_t* tiers, int n_tiers,
+                           int R, int gamma, const int32_t* tiers, int n_tiers, int strict,
                            int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
                            int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,
                            int32_t* dev_status, void* stream);
@@ -312,10 +325,12 @@ sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const in
  *      allocated in target (an upper bound on cu[R]).
  * Out: accept [R], ceiling [R] (may be NULL), out_tok [R, gamma+1] (-1
  *      padded), n_out [R] = accept + 1.
- * A request without rows (cu[i+1] <= cu[i]) sets SDM_DEV_BAD_WINDOW, one
- * whose rows run past row_capacity sets SDM_DEV_CAPACITY; such a request
- * commits one token (0) with accept 0 (greedy and sample).  A window longer
- * than gamma is flagged (SDM_DEV_BAD_WINDOW) and cut to gamma.
+ * Only rows below min(cu[R], row_capacity) are read.  A request without
+ * rows (cu[i+1] <= cu[i]) or whose rows end past cu[R] (a non-monotone
+ * cu_seqlens) sets SDM_DEV_BAD_WINDOW, one whose rows run past row_capacity
+ * sets SDM_DEV_CAPACITY; such a request commits one token (0) with accept 0
+ * (greedy and sample).  A window longer than gamma is flagged
+ * (SDM_DEV_BAD_WINDOW) and cut to gamma.
  */
 sdm_status sdm_verify(sdm_vmode mode, sdm_decode decode, float temperature, sdm_rng rng,
                       const void* target, sdm_dtype dtT, int row_capacity, const int32_t* cu_seqlens,
@@ -354,10 +369,12 @@ sdm_status sdm_verify_tree(const void* target, sdm_dtype dtT, const int32_t* tok
  * ceil(V / 16384) (bf16 target) or row_capacity * ceil(V / 8192) (fp32) must
  * be <= 131072, else SDM_ERR_WORKSPACE and nothing is launched.
  * The first call on a device looks the array's device address up (once per
- * device, with that device current); make that first call before any stream
- * capture.  All calls share the one array and each call fully rewrites what it
- * reads, so nothing carries over between calls, but calls that overlap on the
- * GPU (concurrent streams) race on it: serialise them.
+ * device, with that device current, and again if the device's context has
+ * changed since, e.g. after a device reset); make that first call before any
+ * stream capture.  All calls share the one array and each call rewrites every
+ * partial it reads (rows below min(cu[R], row_capacity); a window past them is
+ * flagged as in sdm_verify), so nothing carries over between calls, but calls
+ * that overlap on the GPU (concurrent streams) race on it: serialise them.
  * Arguments and outputs are those of sdm_verify.
  */
 sdm_status sdm_verify_greedy_static(sdm_vmode mode, const void* target, sdm_dtype dtT, int row_capacity,

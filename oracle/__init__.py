@@ -23,6 +23,7 @@ GREEDY, SAMPLE = 0, 1
 STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
 STREAM_DRAFT, STREAM_ACCEPT, STREAM_RESID, STREAM_BONUS = 0, 1, 2, 3
 FLAG_TIER_UNCAPTURED = 2
+FLAG_TIER_OVERFLOW = 64
 FLAG_INEXACT_MARKOV = 16
 
 _lib = None
@@ -137,7 +138,7 @@ def schedule_dynamic(conf, conf_stale, cost):
                 capacity=int(capacity[0]))
 
 
-def pack_ragged(anchor, draft, budget, tiers):
+def pack_ragged(anchor, draft, budget, tiers, strict=False):
     R, g = draft.shape
     tiers = _c(tiers, np.int32)
     cap = max(int(tiers.max()) if tiers.size else 0, R * (g + 1))
@@ -149,7 +150,8 @@ def pack_ragged(anchor, draft, budget, tiers):
     flags = np.zeros(1, np.int32)
     b = None if budget is None else _c(budget, np.int32)
     rc = lib().orc_pack_ragged(_p(_c(anchor, np.int32)), _p(_c(draft, np.int32)), _p(b), R, g,
-                               _p(tiers), tiers.size, _p(cu), _p(ptok), _p(preq), _p(ppos), _p(tier), _p(flags))
+                               _p(tiers), tiers.size, 1 if strict else 0, _p(cu), _p(ptok), _p(preq), _p(ppos),
+                               _p(tier), _p(flags))
     if rc != 0:
         raise ValueError("pack_ragged: budget out of range")
     t = int(tier[0])

@@ -481,7 +481,7 @@ int orc_schedule_dynamic(const float* conf, const float* conf_stale, int R, int 
 /* pack_ragged ([SGLang] "ragged verify")                               */
 /* ------------------------------------------------------------------ */
 int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,
-                    int R, int gamma, const int32_t* tiers, int n_tiers,
+                    int R, int gamma, const int32_t* tiers, int n_tiers, int strict,
                     int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
                     int32_t* packed_pos, int32_t* tier, int32_t* flags) {
     *flags = 0;
@@ -497,7 +497,7 @@ int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* 
         if (tiers[q] >= total && (t < 0 || tiers[q] < t)) t = tiers[q];
     if (t < 0) {
         t = total;                                                /* above every captured tier */
-        *flags |= ORC_FLAG_TIER_UNCAPTURED;
+        *flags |= strict ? ORC_FLAG_TIER_OVERFLOW : ORC_FLAG_TIER_UNCAPTURED;
     }
     *tier = t;
     for (int i = 0; i < R; ++i) {

@@ -44,7 +44,7 @@ enum { ORC_GREEDY = 0, ORC_SAMPLE = 1 };
 enum { ORC_STATIC = 0, ORC_COMPACT = 1, ORC_CAP_ACCEPT = 2 };
 enum { ORC_STREAM_DRAFT = 0, ORC_STREAM_ACCEPT = 1, ORC_STREAM_RESID = 2, ORC_STREAM_BONUS = 3 };
 /* flag bits returned through *flags */
-enum { ORC_FLAG_TIER_UNCAPTURED = 2, ORC_FLAG_INEXACT_MARKOV = 16 };
+enum { ORC_FLAG_TIER_UNCAPTURED = 2, ORC_FLAG_INEXACT_MARKOV = 16, ORC_FLAG_TIER_OVERFLOW = 64 };
 
 /* Philox4x32-10 block function, straight from its published definition. */
 void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
@@ -81,9 +81,12 @@ int orc_schedule_dynamic(const float* conf, const float* conf_stale, int R, int 
                          int32_t* capacity);
 
 /* Ragged front-pack of the verify windows.  budget == NULL means the full
- * block (n_i = gamma).  Packed arrays need max(tiers[-1], R*(gamma+1)) slots. */
+ * block (n_i = gamma).  Packed arrays need max(tiers[-1], R*(gamma+1)) slots.
+ * A total above every tier is run uncaptured (tier = total,
+ * ORC_FLAG_TIER_UNCAPTURED), or with strict != 0 reported as an overflow
+ * (ORC_FLAG_TIER_OVERFLOW; the rows are packed the same way). */
 int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget,
-                    int R, int gamma, const int32_t* tiers, int n_tiers,
+                    int R, int gamma, const int32_t* tiers, int n_tiers, int strict,
                     int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
                     int32_t* packed_pos, int32_t* tier, int32_t* flags);
 

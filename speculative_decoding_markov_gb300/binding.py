@@ -22,11 +22,12 @@ GREEDY, SAMPLE = 0, 1
 STATIC, COMPACT, CAP_ACCEPT = 0, 1, 2
 OP_DRAFT_CHAIN, OP_DRAFT_TREE, OP_SCHEDULE, OP_PACK, OP_VERIFY, OP_VERIFY_TREE, OP_TV_LABEL, OP_DRAFT_CHAIN_RNN = range(8)
 DEV_BAD_TOKEN, DEV_TIER_UNCAPTURED, DEV_TIMEOUT, DEV_BAD_WINDOW, DEV_CAPACITY, DEV_BAD_CLASS = 1, 2, 4, 8, 16, 32
+DEV_TIER_OVERFLOW = 64
 
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
            "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_schedule_threshold",
-           "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str",
+           "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str", "sdm_status_of_device",
            "sdm_version")
 
 
@@ -59,7 +60,9 @@ def _declare(lib):
     lib.sdm_schedule_dynamic.restype = _I
     lib.sdm_schedule_dynamic.argtypes = [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_pack_ragged.restype = _I
-    lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
+    lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
+    lib.sdm_status_of_device.restype = _I
+    lib.sdm_status_of_device.argtypes = [ctypes.c_int32]
     lib.sdm_verify.restype = _I
     lib.sdm_verify.argtypes = [_I, _I, _F, SdmRng, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _I,
                                _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
@@ -305,7 +308,8 @@ def pack_capacity(R, gamma, tiers) -> int:
     return max(max(tiers) if len(tiers) else 0, R * (gamma + 1))
 
 
-def pack_ragged(anchor, draft, budget, tiers, capacity=None, out=None, dev_status=None, tier_host=None):
+def pack_ragged(anchor, draft, budget, tiers, capacity=None, out=None, dev_status=None, tier_host=None,
+                strict=False):
     _need_cuda(anchor, draft, budget, tiers)
     R, g = draft.shape
     dev = draft.device
@@ -319,7 +323,7 @@ def pack_ragged(anchor, draft, budget, tiers, capacity=None, out=None, dev_statu
     cap = out["packed_tok"].numel()
     dev_status = new_status(dev) if dev_status is None else dev_status
     st = lib().sdm_pack_ragged(_ptr(anchor), _ptr(draft), _ptr(budget), R, g, _ptr(tiers), tiers.numel(),
-                               _ptr(out["cu_seqlens"]), _ptr(out["packed_tok"]), _ptr(out["packed_req"]),
+                               1 if strict else 0, _ptr(out["cu_seqlens"]), _ptr(out["packed_tok"]), _ptr(out["packed_req"]),
                                _ptr(out["packed_pos"]), cap, _ptr(out["tier"]), _ptr(tier_host), _ptr(dev_status),
                                _stream())
     _check(st, "sdm_pack_ragged")

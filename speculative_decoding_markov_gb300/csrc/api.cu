@@ -13,8 +13,6 @@ namespace {
 using namespace sdm;
 
 constexpr int kMaxGx = 256;           // upper bound of vocab splits per GEMM launch
-constexpr int kChunkBf16 = 16384;     // ids per streaming work item (32 KB)
-constexpr int kChunkFp32 = 8192;
 constexpr int kMaxSampleV = 524288;   // 32768 records of 16 ids: the select kernels' chunk tables
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -79,10 +77,6 @@ inline int gemm_grid_x(int n_tiles, int grid_y) {
 
 inline bool vocab_ok(int V) { return V >= 8 && V % 8 == 0; }
 inline bool rank_ok(int r) { return r >= 64 && r <= 256 && r % 64 == 0; }
-inline int n_chunks_of(int V, int fp32) {
-    const int c = fp32 ? kChunkFp32 : kChunkBf16;
-    return (V + c - 1) / c;
-}
 
 #define SDM_CHECK_CUDA(x)                          \
     do {                                           \
@@ -279,8 +273,17 @@ const char* sdm_status_str(sdm_status st) {
         case SDM_ERR_TIER_OVERFLOW: return "packed total above every tier";
         case SDM_ERR_CUDA: return "CUDA error";
         case SDM_ERR_WORKSPACE: return "workspace missing or too small";
+        case SDM_ERR_DEVICE: return "device-side input check failed";
+        case SDM_ERR_TIMEOUT: return "a bounded device wait ran out";
         default: return "unknown status";
     }
+}
+
+sdm_status sdm_status_of_device(int32_t bits) {
+    if (bits & SDM_DEV_TIMEOUT) return SDM_ERR_TIMEOUT;
+    if (bits & SDM_DEV_TIER_OVERFLOW) return SDM_ERR_TIER_OVERFLOW;
+    if (bits & ~static_cast<int32_t>(SDM_DEV_TIER_UNCAPTURED)) return SDM_ERR_DEVICE;
+    return SDM_OK;
 }
 
 int sdm_version(void) { return 100; }
@@ -548,14 +551,15 @@ sdm_status sdm_threshold_sweep(const float* conf, const int32_t* ceiling, int R,
 }
 
 sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
-                           const int32_t* tiers, int n_tiers, int32_t* cu_seqlens, int32_t* packed_tok,
+                           const int32_t* tiers, int n_tiers, int strict, int32_t* cu_seqlens, int32_t* packed_tok,
                            int32_t* packed_req, int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,
                            int32_t* dev_status, void* stream) {
     if (!anchor || !draft || !cu_seqlens || !packed_tok || !packed_req || !packed_pos || !tier) return SDM_ERR_INVALID_ARG;
     if (R <= 0 || gamma < 0 || n_tiers < 0 || capacity <= 0 || (n_tiers > 0 && !tiers)) return SDM_ERR_INVALID_ARG;
+    if (strict != 0 && strict != 1) return SDM_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    SDM_CHECK_CUDA(launch_pack(anchor, draft, budget, R, gamma, tiers, n_tiers, cu_seqlens, packed_tok, packed_req,
-                               packed_pos, capacity, tier, dev_status, s));
+    SDM_CHECK_CUDA(launch_pack(anchor, draft, budget, R, gamma, tiers, n_tiers, strict, cu_seqlens, packed_tok,
+                               packed_req, packed_pos, capacity, tier, dev_status, s));
     if (tier_host) SDM_CHECK_CUDA(cudaMemcpyAsync(tier_host, tier, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
     return SDM_OK;
 }

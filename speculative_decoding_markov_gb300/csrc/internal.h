@@ -122,6 +122,14 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
 // ---------------------------------------------------------------------------
 // Vocab-row streaming kernels (argmax / log-sum-exp partials over target rows)
 // ---------------------------------------------------------------------------
+constexpr int kChunkBf16 = 16384;     // ids per streaming work item (32 KB of bf16)
+constexpr int kChunkFp32 = 8192;      // (32 KB of fp32)
+// Streaming work items (and partials) per row of V elements.
+inline int n_chunks_of(int V, int fp32) {
+    const int c = fp32 ? kChunkFp32 : kChunkBf16;
+    return (V + c - 1) / c;
+}
+
 enum StreamOp { STREAM_ARGMAX = 0, STREAM_LSE = 1 };
 
 struct StreamParams {
@@ -158,7 +166,7 @@ cudaError_t launch_schedule_dynamic(const float* conf, const float* conf_stale, 
                                     int32_t* capacity, cudaStream_t s);
 
 cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
-                        const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
+                        const int32_t* tiers, int n_tiers, int strict, int32_t* cu, int32_t* ptok, int32_t* preq,
                         int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s);
 
 // rows_avail: the packed rows the keys cover (a window past them is flagged)

@@ -23,20 +23,22 @@
 //                      the same for bf16 L and bf16 / fp32 target rows with
 //                      a tile's loads issued before its accumulator is read
 //
-// Data path (one CTA = 128 GEMM rows x a contiguous range of 64-wide vocab
+// Data path (one CTA = 128 GEMM rows x a round-robin set of 128-wide vocab
 // tiles, K = r):
 //   * all threads gather the 128 rows U[tok(m)] (bf16, K-major) into shared
 //     memory once, in the 128-byte swizzled layout tcgen05 reads;
-//   * warp 0 streams W tiles [r x 64] (MN-major, TMA 2-D, 128-byte swizzle,
-//     L2 evict_last: W is re-read by every draft step) and the matching L tile
-//     [rows x 64] (TMA 3-D, evict_first) through an S-stage mbarrier ring;
+//   * warp 0 streams W tiles [r x 128] as two 64-id boxes per 64-row K block
+//     (MN-major, TMA 2-D, 128-byte swizzle, L2 evict_last) through a ring of
+//     tile slots; warp 2 streams the matching L boxes [rows x 64] (TMA 3-D,
+//     evict_first) through their own ring (modes that stage L);
 //   * warp 1 first copies A into tensor memory (tcgen05.cp, r/16 blocks of
-//     128 rows x 16 bf16), then issues r/16 tcgen05.mma (M=128, N=64, K=16,
-//     bf16 -> fp32, A from tensor memory, B from shared memory) per tile into
-//     one of two 64-column TMEM accumulators, with precomputed descriptors;
-//   * warps 2-17 drain the accumulator with tcgen05.ld (thread = GEMM row of
+//     128 rows x 16 bf16), then issues r/16 tcgen05.mma per tile (M=128,
+//     N=128 over the two boxes, K=16, bf16 -> fp32, A from tensor memory, B
+//     from shared memory) into one of two 128-column TMEM accumulators, with
+//     precomputed descriptors, and commits once per tile;
+//   * warps 3-18 drain the accumulator with tcgen05.ld (thread = GEMM row of
 //     its TMEM sub-partition; four warps per sub-partition, one per 16-column
-//     group of every tile), add L and run the mode's reduction in registers;
+//     group of each box), add L and run the mode's reduction in registers;
 //     one result per row, CTA and column group is written at the end (the
 //     sampling modes write one record per row and 16-column block instead).
 // The grid is (vocab splits) x (M tiles), one CTA per SM; vocab tiles are

@@ -14,7 +14,12 @@
 // library holds kStaticScratchBytes of it until the process exits.  Host code
 // cannot use the array's name as a device address: the address is looked up
 // with cudaGetSymbolAddress once per device, with that device current, on the
-// first call made on that device.
+// first call made on that device.  The lookup is kept together with the CUDA
+// context it was made in; a call made in another context (the device was
+// reset, or its primary context released and created again, which loads the
+// module again and may move the array) looks it up again.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -23,25 +28,46 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = 1u << 20;                       // 1 MiB
 constexpr size_t kStaticKeys = kStaticScratchBytes / sizeof(unsigned long long);
-constexpr int kChunkBf16 = 16384;   // the streaming work-item sizes of sdm_verify
-constexpr int kChunkFp32 = 8192;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned long long g_verify_scratch[kStaticKeys];
 
 std::mutex g_setup_mutex;
 unsigned long long* g_scratch_ptr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the scratch array for the current device (set-up on the
-// first call per device).  Returns nullptr on failure.
+// cuCtxGetCurrent through the runtime's driver entry point (the library does
+// not link the driver library itself).
+CUresult current_context(CUcontext* ctx) {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !p)
+            return CUDA_ERROR_NOT_FOUND;
+        fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }
+    return fn(ctx);
+}
+
+// Device address of the scratch array for the current device and context
+// (set-up on the first call per device, again after a context change).
+// Returns nullptr on failure.
 unsigned long long* scratch_for_current_device() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    // NULL until the runtime has made a context current on this thread
+    CUcontext ctx = nullptr;
+    if (current_context(&ctx) != CUDA_SUCCESS) return nullptr;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
+        // the lookup makes the device's primary context current if it is not
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_verify_scratch) != cudaSuccess || !p) return nullptr;
+        if (current_context(&ctx) != CUDA_SUCCESS || !ctx) return nullptr;
         g_scratch_ptr[dev] = static_cast<unsigned long long*>(p);
+        g_scratch_ctx[dev] = ctx;
     }
     return g_scratch_ptr[dev];
 }
@@ -61,8 +87,8 @@ extern "C" sdm_status sdm_verify_greedy_static(sdm_vmode mode, const void* targe
     if (mode == SDM_CAP_ACCEPT && !budget) return SDM_ERR_INVALID_ARG;
     if (V < 8 || V % 8 != 0 || (reinterpret_cast<uintptr_t>(target) & 15u) != 0) return SDM_ERR_UNSUPPORTED;
     const int fp32 = dtT == SDM_FP32;
-    const int chunk = fp32 ? kChunkFp32 : kChunkBf16;
-    const int n_chunks = (V + chunk - 1) / chunk;
+    const int chunk = fp32 ? kChunkFp32 : kChunkBf16;   // the streaming work items of sdm_verify
+    const int n_chunks = n_chunks_of(V, fp32);
     // one partial key per (row, chunk) must fit the fixed array
     if (static_cast<size_t>(row_capacity) * static_cast<size_t>(n_chunks) > kStaticKeys) return SDM_ERR_WORKSPACE;
     unsigned long long* keys = scratch_for_current_device();
@@ -77,7 +103,7 @@ extern "C" sdm_status sdm_verify_greedy_static(sdm_vmode mode, const void* targe
     sp.count = cu_seqlens + R;
     sp.n_items = row_capacity;
     sp.inv_t = 1.0f;
-    sp.keys = keys;   // every (row, chunk) partial read below is written first in this call
+    sp.keys = keys;   // every (row, chunk) partial read below is written first in this call (rows below cu[R])
     if (launch_stream(STREAM_ARGMAX, sp, row_capacity, s) != cudaSuccess) return SDM_ERR_CUDA;
     if (launch_verify_greedy_finalize(mode, cu_seqlens, draft, budget, keys, n_chunks, R, gamma, V, row_capacity,
                                       accept, ceiling, out_tok, n_out, dev_status, s) != cudaSuccess)

@@ -47,8 +47,11 @@ __global__ void label_prep_kernel(const int32_t* __restrict__ cu, const int32_t*
     }
     const int trow = c0 + p;
     const int prev = p == 0 ? anchor[i] : draft[static_cast<size_t>(i) * gamma + p - 1];
-    if (trow < 0 || trow >= row_capacity || prev < 0 || prev >= V) {
-        set_status(dev_status, (trow < 0 || trow >= row_capacity) ? SDM_DEV_CAPACITY : SDM_DEV_BAD_TOKEN);
+    // the log-sum-exp stream wrote partials for rows below min(cu[R], row_capacity) only
+    const int total = cu[R];
+    if (trow < 0 || trow >= row_capacity || trow >= total || prev < 0 || prev >= V) {
+        set_status(dev_status, trow >= row_capacity ? SDM_DEV_CAPACITY
+                               : (trow < 0 || trow >= total) ? SDM_DEV_BAD_WINDOW : SDM_DEV_BAD_TOKEN);
         res_tok[g] = -1;
         return;
     }

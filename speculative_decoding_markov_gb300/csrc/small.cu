@@ -388,7 +388,7 @@ constexpr int kPackThreads = 256;
 
 __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* anchor, const int32_t* draft,
                                                             const int32_t* budget, int R, int gamma,
-                                                            const int32_t* tiers, int n_tiers, int32_t* cu,
+                                                            const int32_t* tiers, int n_tiers, int strict, int32_t* cu,
                                                             int32_t* ptok, int32_t* preq, int32_t* ppos,
                                                             int capacity, int32_t* tier, int32_t* dev_status) {
     __shared__ int warp_sum[32];
@@ -465,9 +465,9 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
     if (tid == 0) {
         cu[R] = carry;
         int t = s_tier;
-        if (t == 0x7fffffff) {
+        if (t == 0x7fffffff) {   // above every tier: run uncaptured, or an error in strict mode
             t = carry;
-            set_status(dev_status, SDM_DEV_TIER_UNCAPTURED);
+            set_status(dev_status, strict ? SDM_DEV_TIER_OVERFLOW : SDM_DEV_TIER_UNCAPTURED);
         }
         s_total = carry;
         s_tier = t;
@@ -498,8 +498,8 @@ __global__ void verify_greedy_finalize_kernel(int mode, const int32_t* cu, const
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= R) return;
-    greedy_resolve(i, lane, mode, cu, draft, budget, row_keys, n_chunks, gamma, V, rows_avail, accept, ceiling, out_tok,
-                   n_out, dev_status);
+    greedy_resolve(i, lane, mode, cu, draft, budget, row_keys, n_chunks, gamma, V, rows_avail, cu[R], accept, ceiling,
+                   out_tok, n_out, dev_status);
 }
 
 // ---------------------------------------------------------------------------
@@ -520,9 +520,12 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
     const RngKey rk{k0, k1, cycle};
     const int row0 = cu[i];
     const int row1 = cu[i + 1];
-    if (row1 <= row0 || row0 < 0 || row1 > rows_avail) {
-        // no rows, or rows past the packed buffer: flagged, and neither a
-        // residual nor a bonus draw (the resample kernel commits token 0)
+    // the log-sum-exp stream wrote partials for rows below min(cu[R],
+    // rows_avail) only
+    if (row1 <= row0 || row0 < 0 || row1 > rows_avail || row1 > cu[R]) {
+        // no rows, rows past the packed buffer or past cu[R]: flagged, and
+        // neither a residual nor a bonus draw (the resample kernel commits
+        // token 0)
         if (lane == 0) {
             set_status(dev_status, row1 > rows_avail ? SDM_DEV_CAPACITY : SDM_DEV_BAD_WINDOW);
             accept[i] = 0;
@@ -886,10 +889,10 @@ cudaError_t launch_schedule_dynamic(const float* conf, const float* conf_stale, 
 }
 
 cudaError_t launch_pack(const int32_t* anchor, const int32_t* draft, const int32_t* budget, int R, int gamma,
-                        const int32_t* tiers, int n_tiers, int32_t* cu, int32_t* ptok, int32_t* preq,
+                        const int32_t* tiers, int n_tiers, int strict, int32_t* cu, int32_t* ptok, int32_t* preq,
                         int32_t* ppos, int capacity, int32_t* tier, int32_t* dev_status, cudaStream_t s) {
     return launch_pdl(pack_kernel, dim3(1), dim3(kPackThreads), 0, s, anchor, draft, budget, R, gamma, tiers, n_tiers,
-                      cu, ptok, preq, ppos, capacity, tier, dev_status);
+                      strict, cu, ptok, preq, ppos, capacity, tier, dev_status);
 }
 
 cudaError_t launch_verify_greedy_finalize(int mode, const int32_t* cu, const int32_t* draft, const int32_t* budget,

@@ -30,18 +30,21 @@ __device__ __forceinline__ int row_token(const unsigned long long* part, size_t 
 //   A = the first p < w with y_{p+1} != argmax of row p, else w;
 //   commit a = A (min(A, budget) in CAP_ACCEPT) drafts and the target token
 //   of row a; ceiling = A.
-// A request without rows, or with rows past the rows_avail the keys cover,
-// is flagged and commits one token (0) with accept 0; a window longer than
-// gamma is flagged and cut to gamma.
+// The argmax stream wrote keys for rows [0, min(cu[R], rows_avail)) only
+// (rows_avail: the rows the key buffer holds; total: cu[R]).  A request
+// without rows, with rows past the buffer (SDM_DEV_CAPACITY) or past cu[R]
+// (a non-monotone cu_seqlens, SDM_DEV_BAD_WINDOW) is flagged and commits one
+// token (0) with accept 0, so no key this call did not write is read; a
+// window longer than gamma is flagged and cut to gamma.
 __device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const int32_t* cu, const int32_t* draft,
                                                const int32_t* budget, const unsigned long long* row_keys,
-                                               int n_chunks, int gamma, int V, int rows_avail, int32_t* accept,
-                                               int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
+                                               int n_chunks, int gamma, int V, int rows_avail, int total,
+                                               int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
                                                int32_t* dev_status) {
     const int row0 = cu[i];
     const int row1 = cu[i + 1];
     int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
-    if (row1 <= row0 || row0 < 0 || row1 > rows_avail) {
+    if (row1 <= row0 || row0 < 0 || row1 > rows_avail || row1 > total) {
         for (int p = lane; p <= gamma; p += 32) o[p] = p == 0 ? 0 : -1;
         if (lane == 0) {
             set_status(dev_status, row1 > rows_avail ? SDM_DEV_CAPACITY : SDM_DEV_BAD_WINDOW);

@@ -45,6 +45,19 @@ def test_status_strings_and_version(lib):
     assert lib.sdm_version() >= 100
 
 
+def test_device_bits_map_to_a_status(lib):
+    f = lib.sdm_status_of_device
+    assert f(0) == 0
+    assert f(binding.DEV_TIER_UNCAPTURED) == 0                     # informational: run uncaptured
+    assert f(binding.DEV_TIER_OVERFLOW) == 3                       # SDM_ERR_TIER_OVERFLOW (strict pack)
+    assert f(binding.DEV_TIER_OVERFLOW | binding.DEV_TIER_UNCAPTURED) == 3
+    assert f(binding.DEV_TIMEOUT | binding.DEV_TIER_OVERFLOW) == 7   # a timed-out wait comes first
+    for bit in (binding.DEV_BAD_TOKEN, binding.DEV_BAD_WINDOW, binding.DEV_CAPACITY, binding.DEV_BAD_CLASS):
+        assert f(bit) == 6                                         # SDM_ERR_DEVICE
+    assert lib.sdm_status_str(3) == b"packed total above every tier"
+    assert lib.sdm_status_str(7) == b"a bounded device wait ran out"
+
+
 def test_workspace_sizes_are_host_computable(lib):
     assert lib.sdm_workspace_size(binding.OP_DRAFT_CHAIN, 64, 7, 151936, 256, 0, 0, 0) > 0
     assert lib.sdm_workspace_size(binding.OP_DRAFT_TREE, 32, 16, 151936, 256, 8, 4, 64) > 0
@@ -118,8 +131,10 @@ def test_tree_and_verify_host_validation(lib):
     sd = lib.sdm_schedule_dynamic
     assert sd(FAKE, None, 4, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 1   # no stale confidences
     assert sd(FAKE, FAKE, 2000, 8, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 2   # R * gamma > 8192
-    assert lib.sdm_pack_ragged(FAKE, FAKE, None, 4, 7, None, 2, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None, None,
+    assert lib.sdm_pack_ragged(FAKE, FAKE, None, 4, 7, None, 2, 0, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None, None,
                                None) == 1       # tiers missing
+    assert lib.sdm_pack_ragged(FAKE, FAKE, None, 4, 7, FAKE, 2, 2, FAKE, FAKE, FAKE, FAKE, 64, FAKE, None, None,
+                               None) == 1       # strict is 0 or 1
 
 
 def test_observability_host_validation(lib):

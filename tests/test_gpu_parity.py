@@ -318,26 +318,32 @@ def test_schedule_dynamic_cliff_fixture_and_additive_agreement():
 # ---------------------------------------------------------------------------
 # pack_ragged
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("strict", [False, True], ids=["uncaptured", "strict"])
 @pytest.mark.parametrize("R,g,seed,static", [(1, 1, 0, False), (37, 8, 1, False), (256, 8, 2, False),
                                              (256, 8, 3, True), (1500, 2, 4, False)])
-def test_pack_ragged(R, g, seed, static):
+def test_pack_ragged(R, g, seed, static, strict):
     rng = np.random.default_rng(seed)
     anchor = rng.integers(0, 5000, R).astype(np.int32)
     draft = rng.integers(0, 5000, (R, g)).astype(np.int32)
     budget = rng.integers(0, g + 1, R).astype(np.int32)
     budget[: max(1, R // 5)] = 0
     tiers = np.array([64, 128, 256, 512, 1024, 2048], np.int32)
-    ref = oracle.pack_ragged(anchor, draft, None if static else budget, tiers)
+    ref = oracle.pack_ragged(anchor, draft, None if static else budget, tiers, strict=strict)
     out = sdm.pack_ragged(dev(torch.from_numpy(anchor)), dev(torch.from_numpy(draft)),
-                          None if static else dev(torch.from_numpy(budget)), dev(torch.from_numpy(tiers)))
+                          None if static else dev(torch.from_numpy(budget)), dev(torch.from_numpy(tiers)),
+                          strict=strict)
     torch.cuda.synchronize()
     t = ref["tier"]
     assert int(host(out["tier"])[0]) == t
     np.testing.assert_array_equal(host(out["cu_seqlens"]), ref["cu_seqlens"])
     for k in ("packed_tok", "packed_req", "packed_pos"):
         np.testing.assert_array_equal(host(out[k])[:t], ref[k])
-    flag = int(out["dev_status"].item()) & sdm.DEV_TIER_UNCAPTURED
-    assert bool(flag) == bool(ref["flags"] & oracle.FLAG_TIER_UNCAPTURED)
+    bits = int(out["dev_status"].item())
+    assert bits == ref["flags"]                 # the same bit from both sides, nothing else
+    # the status a caller maps the bits to: strict overflow is an error, uncaptured is not
+    assert sdm.lib().sdm_status_of_device(bits) == (3 if ref["flags"] & oracle.FLAG_TIER_OVERFLOW else 0)
+    if static and R * (g + 1) > 2048:
+        assert ref["flags"] == (oracle.FLAG_TIER_OVERFLOW if strict else oracle.FLAG_TIER_UNCAPTURED)
 
 
 # ---------------------------------------------------------------------------
@@ -429,6 +435,63 @@ def test_verify_greedy_flags_bad_windows_without_waiting():
                 continue
             assert host(out["accept"])[i] == ref["accept"][i]
             np.testing.assert_array_equal(host(out["out_tok"])[i], ref["out_tok"][i])
+
+
+def _non_monotone_cu(cu):
+    """cu[R] moved down to cu[2]: requests 2 .. R-2 end past cu[R] (the
+    streams write rows below cu[R] only) and request R-1 has no rows."""
+    bad = cu.copy()
+    bad[-1] = bad[2]
+    return bad
+
+
+@pytest.mark.parametrize("decode", ["greedy", "sample"])
+def test_verify_flags_windows_past_the_packed_total(decode):
+    """A non-monotone cu_seqlens whose total cu[R] lies below a request's
+    end: that request is flagged (SDM_DEV_BAD_WINDOW) and commits one token
+    (0) instead of reading partials this call never wrote; requests inside
+    the total are verified as usual.  Run after a larger call on the same
+    workspace, so stale partials would be there to read."""
+    w = small(R=6, B=4, V=2048, r=64, l_dtype=BF16, target_dtype=BF16, sigma=(0.5,), temperature=1.0)
+    inp = synthetic.generate(w, seed=17)
+    an = np_of(inp["anchor"])
+    U, W = np_of(inp["U"]), np_of(inp["W"])
+    samp = decode == "sample"
+    dr = oracle.draft_chain(np_of(inp["L"]), U, W, an, decode=oracle.SAMPLE if samp else oracle.GREEDY, seed=4,
+                            cycle=1)
+    pk = oracle.pack_ragged(an, dr["tokens"], None, np.array([64], np.int32))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), w.target_dtype)
+    packed = dev(synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"])))
+    kw = {}
+    okw = {}
+    if samp:
+        logq32, lse32 = dr["logq"].astype(np.float32), dr["lse"].astype(np.float32)
+        kw = dict(logq=dev(torch.from_numpy(logq32)), lse_q=dev(torch.from_numpy(lse32)), L=dev(inp["L"]),
+                  U=dev(inp["U"]), W=dev(inp["W"]), seed=4, cycle=1)
+        okw = dict(logq=logq32.astype(np.float64), lse_q=lse32.astype(np.float64), L=np_of(inp["L"]), U=U, W=W,
+                   seed=4, cycle=1)
+    dec = sdm.SAMPLE if samp else sdm.GREEDY
+    ref = oracle.verify(oracle.STATIC, oracle.SAMPLE if samp else oracle.GREEDY, np_of(packed.cpu()),
+                        pk["cu_seqlens"], an, dr["tokens"], **okw)
+    tokens = dev(torch.from_numpy(dr["tokens"]))
+    ws = sdm.workspace(sdm.OP_VERIFY, w.R, w.B, w.V, w.r, packed.shape[0], device=DEV)
+    full = sdm.verify(sdm.STATIC, dec, packed, dev(torch.from_numpy(pk["cu_seqlens"])), dev(inp["anchor"]), tokens,
+                      ws=ws, **kw)
+    st = sdm.new_status(DEV)
+    cu = _non_monotone_cu(pk["cu_seqlens"])
+    out = sdm.verify(sdm.STATIC, dec, packed, dev(torch.from_numpy(cu)), dev(inp["anchor"]), tokens,
+                     ws=ws, dev_status=st, **kw)
+    torch.cuda.synchronize()
+    assert int(full["dev_status"].item()) == 0
+    assert int(st.item()) & sdm.DEV_BAD_WINDOW
+    assert not int(st.item()) & sdm.DEV_CAPACITY
+    for i in range(w.R):
+        if i < 2:
+            assert host(out["accept"])[i] == ref["accept"][i] or ref["margin"][i] < TIE
+            np.testing.assert_array_equal(host(out["out_tok"])[i], ref["out_tok"][i])
+        else:
+            assert host(out["accept"])[i] == 0 and host(out["n_out"])[i] == 1, i
+            assert host(out["out_tok"])[i, 0] == 0 and np.all(host(out["out_tok"])[i, 1:] == -1), i
 
 
 # ---------------------------------------------------------------------------

@@ -347,7 +347,14 @@ def test_pack_round_trip_and_tier():
     assert np.all(pk["packed_tok"][T:] == -1) and np.all(pk["packed_req"][T:] == -1)
     # static (budget = None) above every tier: uncaptured, tier = total
     pk = oracle.pack_ragged(anchor, draft, None, tiers[:3])
-    assert pk["tier"] == R * (g + 1) and pk["flags"] & oracle.FLAG_TIER_UNCAPTURED
+    assert pk["tier"] == R * (g + 1) and pk["flags"] == oracle.FLAG_TIER_UNCAPTURED
+    # strict mode ([SGLang] ragged verify: only captured tiers run): the same
+    # rows, reported as an overflow instead; a total inside a tier is no error
+    st = oracle.pack_ragged(anchor, draft, None, tiers[:3], strict=True)
+    assert st["flags"] == oracle.FLAG_TIER_OVERFLOW and st["tier"] == pk["tier"]
+    for k in ("cu_seqlens", "packed_tok", "packed_req", "packed_pos"):
+        np.testing.assert_array_equal(st[k], pk[k])
+    assert oracle.pack_ragged(anchor, draft, budget, tiers, strict=True)["flags"] == 0
 
 
 def test_pack_empty_windows():

@@ -78,3 +78,31 @@ def test_static_scratch_rejects_what_does_not_fit():
     torch.cuda.synchronize()
     assert st == 5                                       # SDM_ERR_WORKSPACE, nothing launched
     assert torch.all(out["accept"] == -9)
+
+
+def test_static_scratch_never_reads_partials_of_an_earlier_call():
+    """The array keeps the last call's partial keys.  A later call whose
+    cu_seqlens ends (cu[R]) before one of its requests' windows must not read
+    them: such a request is flagged and commits one token (0), the requests
+    inside the total match the workspace entry point."""
+    w = Workload(name="no_alloc", R=6, B=4, V=2048, r=64, l_dtype=BF16, l_std=2.0, sigma=(0.5,),
+                 target_dtype=BF16)
+    inp = {k: v.cuda() for k, v in synthetic.generate(w, seed=9).items()}
+    dr = sdm.draft_chain(inp["L"], inp["U"], inp["W"], inp["anchor"])
+    pk = sdm.pack_ragged(inp["anchor"], dr["tokens"], None, inp["tiers"])
+    target = synthetic.chain_target(inp, dr["tokens"], BF16)
+    packed = synthetic.gather_packed(target, pk["packed_req"], pk["packed_pos"])
+    ref = sdm.verify(sdm.STATIC, sdm.GREEDY, packed, pk["cu_seqlens"], inp["anchor"], dr["tokens"])
+    st, first = _static_verify(sdm.STATIC, packed, pk["cu_seqlens"], dr["tokens"], None, w.R, w.B, w.V)
+    torch.cuda.synchronize()
+    assert st == 0 and int(first["dev_status"].item()) == 0
+    bad = pk["cu_seqlens"].clone()
+    bad[-1] = bad[2]                          # requests 2 .. R-1 end past the packed total
+    st, out = _static_verify(sdm.STATIC, packed, bad, dr["tokens"], None, w.R, w.B, w.V)
+    torch.cuda.synchronize()
+    assert st == 0
+    assert int(out["dev_status"].item()) & sdm.DEV_BAD_WINDOW
+    for k in ("accept", "out_tok", "n_out"):
+        assert torch.equal(out[k][:2], ref[k][:2]), k
+    assert torch.all(out["accept"][2:] == 0) and torch.all(out["n_out"][2:] == 1)
+    assert torch.all(out["out_tok"][2:, 0] == 0) and torch.all(out["out_tok"][2:, 1:] == -1)
