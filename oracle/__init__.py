@@ -102,7 +102,7 @@ def draft_tree(L, U, W, anchor, k, P, N):
     score = np.zeros((R, S), np.float64)
     mask = np.zeros((R, S, words), np.uint32)
     n_nodes = np.zeros(R, np.int32)
-    margin = np.zeros(R, np.float64)
+    margin = np.zeros((R, B + 2), np.float64)
     flags = lib().orc_draft_tree(
         _p(L), _dt(L), _p(_c(U, np.uint16)), _p(_c(W, np.uint16)), _p(_c(anchor, np.int32)),
         R, B, V, r, k, P, N, _p(tok), _p(parent), _p(depth), _p(score), _p(mask), _p(n_nodes), _p(margin))
@@ -169,7 +169,7 @@ def verify(mode, decode, target, cu_seqlens, anchor, draft, budget=None, logq=No
     ceiling = np.zeros(R, np.int32)
     out_tok = np.zeros((R, g + 1), np.int32)
     n_out = np.zeros(R, np.int32)
-    margin = np.zeros(R, np.float64)
+    margin = np.zeros((R, g + 1), np.float64)
     r = 0 if U is None else U.shape[1]
     Lc = None if L is None else np.ascontiguousarray(L)
     flags = lib().orc_verify(
@@ -270,3 +270,21 @@ def draft_chain_rnn(L, U, W, A, X, anchor, decode=GREEDY, temperature=1.0, seed=
         _p(_c(anchor, np.int32)), _p(ids), R, B, V, r, decode, ctypes.c_double(temperature), ctypes.c_uint64(seed),
         ctypes.c_uint64(cycle), _p(tokens), _p(logq), _p(lse), _p(margin))
     return dict(tokens=tokens, logq=logq, lse=lse, margin=margin, flags=flags)
+
+
+def rnn_project(L, W, memo, decode=GREEDY, temperature=1.0, seed=0, cycle=0, req_ids=None):
+    """The RNN head's projection and decision for a given fp32 memo [R, B, r]
+    (z_d = L_d + bf16(memo_d) W); outputs as draft_chain, each margin that of
+    its own position's decision."""
+    R, B, V = L.shape
+    r = memo.shape[2]
+    L = np.ascontiguousarray(L)
+    tokens = np.zeros((R, B), np.int32)
+    logq = np.zeros((R, B), np.float64)
+    lse = np.zeros((R, B), np.float64)
+    margin = np.zeros((R, B), np.float64)
+    ids = None if req_ids is None else _c(req_ids, np.int32)
+    lib().orc_rnn_project(_p(L), _dt(L), _p(_c(W, np.uint16)), _p(_c(memo, np.float32)), _p(ids), R, B, V, r, decode,
+                          ctypes.c_double(temperature), ctypes.c_uint64(seed), ctypes.c_uint64(cycle), _p(tokens),
+                          _p(logq), _p(lse), _p(margin))
+    return dict(tokens=tokens, logq=logq, lse=lse, margin=margin)

@@ -250,7 +250,13 @@ int orc_draft_tree(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
     int* out_slot = (int*)malloc(sizeof(int) * (size_t)pool_cap);
 
     for (int i = 0; i < R; ++i) {
-        double min_gap = INFINITY;
+        /* one margin per decision: [i, d-1] the prune boundary of level d,
+         * [i, B] the top-N boundary, [i, B+1] the smallest score gap between
+         * neighbours of the output ranking (their order); INFINITY where no
+         * boundary was crossed */
+        double* mg = margin ? margin + (size_t)i * (size_t)(B + 2) : NULL;
+        if (mg)
+            for (int q = 0; q < B + 2; ++q) mg[q] = INFINITY;
         int n_pool = 0;
         pool[n_pool++] = (tree_node){anchor[i], -1, 0, 0, 0.0};   /* root = anchor */
         int n_front = 1;
@@ -292,10 +298,7 @@ int orc_draft_tree(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
                 cand[b] = t;
             }
             int keep = n_cand < P ? n_cand : P;
-            if (n_cand > keep) {
-                double g = cand[keep - 1].s - cand[keep].s;
-                if (g < min_gap) min_gap = g;
-            }
+            if (n_cand > keep && mg) mg[d - 1] = cand[keep - 1].s - cand[keep].s;
             for (int c = 0; c < keep; ++c) {
                 pool[n_pool] = (tree_node){cand[c].tok, cand[c].parent, d, n_pool, cand[c].s};
                 next_frontier[c] = n_pool;
@@ -316,9 +319,10 @@ int orc_draft_tree(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
             ++n_order;
         }
         int take = n_order < N ? n_order : N;
-        if (n_order > take) {
-            double g = pool[order[take - 1]].score - pool[order[take]].score;
-            if (g < min_gap) min_gap = g;
+        if (n_order > take && mg) mg[B] = pool[order[take - 1]].score - pool[order[take]].score;
+        for (int c = 1; c < take && mg; ++c) {
+            double g = pool[order[c - 1]].score - pool[order[c]].score;
+            if (g < mg[B + 1]) mg[B + 1] = g;
         }
         for (int p = 0; p < n_pool; ++p) out_slot[p] = -1;
         out_slot[0] = 0;
@@ -350,7 +354,6 @@ int orc_draft_tree(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
             if (c > take) continue;
             for (int a = c; a >= 0; a = parent[base + a]) row[a / 32] |= 1u << (a % 32);
         }
-        if (margin) margin[i] = min_gap;
     }
     free(M); free(z); free(pool); free(frontier); free(next_frontier);
     free(cand); free(top_id); free(order); free(out_slot);
@@ -565,7 +568,12 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
         int cap = (mode == ORC_CAP_ACCEPT) ? budget[i] : w;       /* drafts that may commit */
         if (cap > w) cap = w;
         const int32_t* y = draft + (size_t)i * gamma;             /* y[p] = y_{p+1} */
-        double min_gap = INFINITY;
+        /* one margin per decision: [i, p] the accept test of window row p,
+         * [i, gamma] the final draw (residual or bonus); INFINITY where no
+         * such decision was taken (and for every greedy decision) */
+        double* mg = margin ? margin + (size_t)i * (size_t)(gamma + 1) : NULL;
+        if (mg)
+            for (int p = 0; p <= gamma; ++p) mg[p] = INFINITY;
         int A, a, last;
         if (decode == ORC_GREEDY) {
             /* accept while the draft equals the target's argmax; the first
@@ -589,8 +597,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
                             - row_lse(target, dtT, row0 + (size_t)p, V, inv_t);
                 double lq = logq[(size_t)i * gamma + (size_t)p];
                 double lu = log(orc_uniform(seed, cycle, ORC_STREAM_ACCEPT, gid, (uint32_t)p, 0u));
-                double g = fabs(lu - (lp - lq));
-                if (g < min_gap) min_gap = g;
+                if (mg) mg[p] = fabs(lu - (lp - lq));
                 if (!(lu < lp - lq)) {
                     A = p;
                     break;
@@ -622,7 +629,7 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
                     wts[v] = exp((double)load_elem(target, dtT, (row0 + (size_t)row) * (size_t)V + (size_t)v) * inv_t - lse_p);
                 last = icdf_draw(wts, V, orc_uniform(seed, cycle, ORC_STREAM_BONUS, gid, (uint32_t)row, 0u), &gap);
             }
-            if (gap < min_gap) min_gap = gap;
+            if (mg) mg[gamma] = gap;
         }
         size_t ob = (size_t)i * (size_t)(gamma + 1);
         for (int p = 0; p < a; ++p) out_tok[ob + (size_t)p] = y[p];
@@ -631,7 +638,6 @@ int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t
         accept[i] = a;
         n_out[i] = a + 1;
         if (ceiling) ceiling[i] = A;
-        if (margin) margin[i] = min_gap;
     }
     free(M);
     free(wts);
@@ -944,5 +950,55 @@ int orc_draft_chain_rnn(const void* L, int dtL, const uint16_t* U, const uint16_
     free(z);
     free(m);
     free(m_next);
+    return 0;
+}
+
+/* The RNN head's projection and decision at every position for a memo that
+ * is given (fp32 [R, B, r], for instance the trajectory another
+ * implementation formed): z_d = L_d + bf16(memo_d) . W with the memo rounded
+ * to bf16 as in orc_draft_chain_rnn, then y_d, lse and logq exactly as there
+ * (greedy argmax, or the inverse-CDF draw of softmax(z_d / T) with the
+ * uniform of stream 0, row d).  Each position's decision depends on its own
+ * memo row only, so margin[i, d-1] is the margin of that one decision. */
+int orc_rnn_project(const void* L, int dtL, const uint16_t* W, const float* memo, const int32_t* req_ids,
+                    int R, int B, int V, int r, int decode, double temperature, uint64_t seed, uint64_t cycle,
+                    int32_t* tokens, double* logq, double* lse, double* margin) {
+    double* M = (double*)malloc(sizeof(double) * (size_t)V);
+    double* wts = (double*)malloc(sizeof(double) * (size_t)V);
+    float* z = (float*)malloc(sizeof(float) * (size_t)V);
+    double* m = (double*)malloc(sizeof(double) * (size_t)r);
+    double inv_t = 1.0 / temperature;
+    for (int i = 0; i < R; ++i) {
+        uint32_t gid = req_ids ? (uint32_t)req_ids[i] : (uint32_t)i;
+        for (int d = 1; d <= B; ++d) {
+            size_t o = (size_t)i * B + (size_t)(d - 1);
+            for (int j = 0; j < r; ++j) m[j] = (double)memo[o * (size_t)r + (size_t)j];
+            memo_times_w(m, W, r, V, M);
+            combine_logits(L, dtL, o * V, M, V, z);
+            int y;
+            double gap = 0.0;
+            if (decode == ORC_GREEDY) {
+                y = argmax_f32(z, V, &gap);
+                if (logq) logq[o] = 0.0;
+                if (lse) lse[o] = 0.0;
+            } else {
+                double zmax = -INFINITY;
+                for (int v = 0; v < V; ++v)
+                    if ((double)z[v] * inv_t > zmax) zmax = (double)z[v] * inv_t;
+                for (int v = 0; v < V; ++v) wts[v] = exp((double)z[v] * inv_t - zmax);
+                double u = orc_uniform(seed, cycle, ORC_STREAM_DRAFT, gid, (uint32_t)d, 0u);
+                y = icdf_draw(wts, V, u, &gap);
+                double l = logsumexp_scaled(z, V, inv_t);
+                if (lse) lse[o] = l;
+                if (logq) logq[o] = (double)z[y] * inv_t - l;
+            }
+            tokens[o] = y;
+            if (margin) margin[o] = gap;
+        }
+    }
+    free(M);
+    free(wts);
+    free(z);
+    free(m);
     return 0;
 }

@@ -60,8 +60,10 @@ int orc_draft_chain(const void* L, int dtL, const uint16_t* U, const uint16_t* W
                     int32_t* tokens, double* logq, double* lse, double* margin);
 
 /* PCTree drafting.  Outputs hold N+1 slots per request (slot 0 = root);
- * mask holds ceil((N+1)/32) words per node row.  margin[i] = smallest score
- * gap at a prune or top-N boundary of request i (may be NULL). */
+ * mask holds ceil((N+1)/32) words per node row.  margin [R, B+2] (may be
+ * NULL), one per decision: [i, d-1] the score gap at the prune boundary of
+ * level d, [i, B] at the top-N boundary, [i, B+1] the smallest gap between
+ * neighbours of the output ranking; INFINITY where nothing was cut. */
 int orc_draft_tree(const void* L, int dtL, const uint16_t* U, const uint16_t* W,
                    const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N,
                    int32_t* tok, int32_t* parent, int32_t* depth, double* score,
@@ -93,7 +95,10 @@ int orc_pack_ragged(const int32_t* anchor, const int32_t* draft, const int32_t* 
 /* Verification over packed target logits [rows, V].  budget is only read in
  * cap-accept mode; logq/lse_q/L/U/W/r only in sample mode.  req_ids (may be
  * NULL) maps local request i to the global request id of the random counters.
- * margin[i] = the smallest decision margin met for request i (may be NULL). */
+ * margin [R, gamma+1] (may be NULL), one per decision: [i, p] the margin
+ * |ln u - ln(p/q)| of the accept test of window row p, [i, gamma] that of the
+ * final residual or bonus draw; INFINITY where no such decision was taken
+ * (greedy decisions are exact: every entry INFINITY). */
 int orc_verify(int mode, int decode, double temperature, uint64_t seed, uint64_t cycle,
                const int32_t* req_ids, const void* target, int dtT, const int32_t* cu_seqlens,
                const int32_t* anchor, const int32_t* draft, const int32_t* budget,
@@ -144,6 +149,14 @@ int orc_draft_chain_rnn(const void* L, int dtL, const uint16_t* U, const uint16_
                         const uint16_t* X, const int32_t* anchor, const int32_t* req_ids, int R, int B, int V, int r,
                         int decode, double temperature, uint64_t seed, uint64_t cycle,
                         int32_t* tokens, double* logq, double* lse, double* margin);
+
+/* The RNN head's projection and decision for a given fp32 memo [R, B, r]:
+ * z_d = L_d + bf16(memo_d) . W, then y_d, lse and logq as
+ * orc_draft_chain_rnn forms them; margin[i, d-1] belongs to that position's
+ * decision alone. */
+int orc_rnn_project(const void* L, int dtL, const uint16_t* W, const float* memo, const int32_t* req_ids,
+                    int R, int B, int V, int r, int decode, double temperature, uint64_t seed, uint64_t cycle,
+                    int32_t* tokens, double* logq, double* lse, double* margin);
 
 #ifdef __cplusplus
 }

@@ -63,26 +63,21 @@ __global__ void label_prep_kernel(const int32_t* __restrict__ cu, const int32_t*
     const float2* part = lse_part + static_cast<size_t>(trow) * n_chunks;
     float m = -INFINITY;
     for (int c = 0; c < n_chunks; ++c) m = fmaxf(m, part[c].x);
-    float s = 0.f;
-    for (int c = 0; c < n_chunks; ++c) s += part[c].y * expf(part[c].x - m);
-    res_lse_p[g] = m + logf(s);
+    double s = 0.0;   // fp32 terms, summed in fp64
+    for (int c = 0; c < n_chunks; ++c) s += static_cast<double>(part[c].y * expf(part[c].x - m));
+    res_lse_p[g] = static_cast<float>(static_cast<double>(m) + log(s));
 }
 
-// One warp per listed row: lanes take partials lane, lane + 32, ... and a
-// fixed butterfly combines them (the order does not depend on timing).
-__device__ __forceinline__ float2 warp_lse_pair(float m, float s) {
+__device__ __forceinline__ double warp_sum_f64(double s) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-        const float so = __shfl_xor_sync(0xffffffffu, s, o);
-        const float mn = fmaxf(m, mo);
-        if (mn == -INFINITY) continue;   // both empty
-        s = s * expf(m - mn) + so * expf(mo - mn);
-        m = mn;
-    }
-    return make_float2(m, s);
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    return s;
 }
 
+// One warp per listed row: the row maximum of the partials first, then each
+// partial's sum rescaled to it (an fp32 exponential) and summed in fp64, lanes
+// taking partials lane, lane + 32, ... and a fixed butterfly combining them
+// (the order does not depend on timing).
 __global__ void label_lse_q_kernel(const float2* __restrict__ part, int n_part, int rows,
                                    const int32_t* __restrict__ res_tok, float* row_lse_q) {
     pdl_wait();
@@ -91,16 +86,20 @@ __global__ void label_lse_q_kernel(const float2* __restrict__ part, int n_part, 
     const int g = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
     if (g >= rows || res_tok[g] < 0) return;
     const float2* pr = part + static_cast<size_t>(g) * n_part;
-    float m = -INFINITY, s = 0.f;
+    float m = -INFINITY;
     for (int k = lane; k < n_part; k += 32) {
         const float2 x = pr[k];
-        if (x.y <= 0.f) continue;   // a thread that consumed no column
-        const float mn = fmaxf(m, x.x);
-        s = s * expf(m - mn) + x.y * expf(x.x - mn);
-        m = mn;
+        if (x.y > 0.f) m = fmaxf(m, x.x);   // a thread that consumed no column left (-inf, 0)
     }
-    const float2 r = warp_lse_pair(m, s);
-    if (lane == 0) row_lse_q[g] = r.x + logf(r.y);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    double s = 0.0;
+    for (int k = lane; k < n_part; k += 32) {
+        const float2 x = pr[k];
+        if (x.y > 0.f) s += static_cast<double>(x.y * expf(x.x - m));
+    }
+    s = warp_sum_f64(s);
+    if (lane == 0) row_lse_q[g] = static_cast<float>(static_cast<double>(m) + log(s));
 }
 
 __global__ void label_finalize_kernel(const float2* __restrict__ part, int n_part, int rows,
@@ -112,11 +111,10 @@ __global__ void label_finalize_kernel(const float2* __restrict__ part, int n_par
     const int g = blockIdx.x * kRowWarps + (threadIdx.x >> 5);
     if (g >= rows || res_tok[g] < 0) return;
     const float2* pr = part + static_cast<size_t>(g) * n_part;
-    float s = 0.f;
-    for (int k = lane; k < n_part; k += 32) s += pr[k].y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    if (lane == 0) label[static_cast<size_t>(res_req[g]) * gamma + res_pos[g]] = s;
+    double s = 0.0;   // the per-thread fp32 partial sums, added in fp64
+    for (int k = lane; k < n_part; k += 32) s += static_cast<double>(pr[k].y);
+    s = warp_sum_f64(s);
+    if (lane == 0) label[static_cast<size_t>(res_req[g]) * gamma + res_pos[g]] = static_cast<float>(s);
 }
 
 // ---------------------------------------------------------------------------

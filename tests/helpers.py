@@ -92,3 +92,70 @@ def oracle_greedy_decode(w: Workload, ab: dict, cycles: int, mode: str = "compac
         anchor = np.array([s[-1] for s in seqs], np.int32)
         records.append(dict(draft=dr, sched=sc, pack=pk, verify=vr))
     return seqs, records
+
+
+# ---------------------------------------------------------------------------
+# tie-zone events, localised to the first decision that differs
+# ---------------------------------------------------------------------------
+def verify_first_decision(ref: dict, j: int, accept: int, ceiling: int, out_tok: np.ndarray):
+    """For request j of an oracle verify result, the (position, margin) of
+    the first decision on which a GPU result (accept, ceiling, out_tok)
+    differs, or None when it agrees.  The accept tests run left to right, so
+    two ceilings first part at the test of row min(ceilings); equal ceilings
+    with a different final token part at the final draw (margin column
+    gamma)."""
+    g = ref["margin"].shape[1] - 1
+    if ceiling != ref["ceiling"][j]:
+        p = int(min(ceiling, ref["ceiling"][j]))
+        return p, float(ref["margin"][j, p])
+    if accept != ref["accept"][j] or not np.array_equal(out_tok, ref["out_tok"][j]):
+        return g, float(ref["margin"][j, g])
+    return None
+
+
+def tree_paths(tok: np.ndarray, parent: np.ndarray, depth: np.ndarray, n: int) -> dict:
+    """depth -> set of the token paths (root excluded) of the tree's nodes."""
+    out = {}
+    for c in range(1, n):
+        path, a = [], c
+        while a > 0:
+            path.append(int(tok[a]))
+            a = int(parent[a])
+        out.setdefault(int(depth[c]), set()).add(tuple(reversed(path)))
+    return out
+
+
+def tree_first_decision(ref: dict, j: int, tok, parent, depth, n_nodes: int, B: int):
+    """For request j of an oracle tree, the (kind, margin) of the first
+    decision on which a GPU tree differs, or None when it agrees: the first
+    depth whose set of nodes differs (its level's prune boundary, or the
+    top-N boundary, whichever is closer), else the order of the output
+    ranking."""
+    same = all(np.array_equal(a, ref[k][j]) for a, k in ((tok, "tok"), (parent, "parent"), (depth, "depth")))
+    if same and n_nodes == ref["n_nodes"][j]:
+        return None
+    gp = tree_paths(tok, parent, depth, n_nodes)
+    rp = tree_paths(ref["tok"][j], ref["parent"][j], ref["depth"][j], int(ref["n_nodes"][j]))
+    for d in range(1, B + 1):
+        if gp.get(d, set()) != rp.get(d, set()):
+            return f"level {d}", float(min(ref["margin"][j, d - 1], ref["margin"][j, B]))
+    return "ranking", float(ref["margin"][j, B + 1])
+
+
+def oracle_threads() -> int:
+    """Host cores this process may run on (the oracle's calls release the GIL)."""
+    import os
+
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+def oracle_map(fn, items):
+    """fn over items on a thread pool: each call is one single-threaded
+    oracle call (ctypes releases the GIL), results in order."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    items = list(items)
+    if len(items) <= 1:
+        return [fn(x) for x in items]
+    with ThreadPoolExecutor(max_workers=min(len(items), oracle_threads())) as ex:
+        return list(ex.map(fn, items))

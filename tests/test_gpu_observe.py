@@ -2,13 +2,14 @@
 1 - TV(q, p) of every verified window row (DSpark notes sec. 5.1) and the
 verify-cycle statistics (SGLang "observability").
 
-Label tolerance: the kernel forms q_v and p_v with fp32 exponentials of
-arguments within about 30 of zero (relative error a few 1e-6 each, plus the
-fp32 log-sum-exps it subtracts) and sums them in fp32 over 16-column blocks
-and then over vocabulary splits; over 152K columns the accumulated absolute
-error stays near 1e-5.  The oracle works in fp64.  The bar is 1e-4 absolute.
-Counts of the statistics are exact; the confidence sums per bin are fp64
-atomic adds (order not fixed), compared within 1e-12.
+Label tolerance: 1e-5 relative.  The label is a sum of positive terms
+min(q_v, p_v), so its relative error is at most the largest relative error of
+one term plus the summation's: each q_v and p_v is an fp32 exponential of an
+argument within about 30 of zero (relative error below 3e-6, the fp32
+log-sum-exp it subtracts included), a thread sums at most a few hundred terms
+in fp32 and the per-thread partials are added in fp64.  The oracle works in
+fp64.  Counts of the statistics are exact; the confidence sums per bin are
+fp64 atomic adds (order not fixed), compared within 1e-12.
 """
 from __future__ import annotations
 
@@ -26,7 +27,7 @@ from tests.helpers import np_of, small
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
-LABEL_TOL = 1e-4
+LABEL_TOL = 1e-5   # relative
 
 
 def dev(t):
@@ -56,8 +57,10 @@ def packed_rows(tgt, win, pad=0):
 def check_labels(gpu, ref):
     outside = ref == -1.0
     np.testing.assert_array_equal(gpu[outside], -1.0)
-    err = np.abs(gpu[~outside].astype(np.float64) - ref[~outside])
-    assert err.size == 0 or err.max() <= LABEL_TOL, f"max label error {err.max()}"
+    inside = ref[~outside]
+    assert np.all(inside > 0)
+    err = np.abs(gpu[~outside].astype(np.float64) - inside) / inside
+    assert err.size == 0 or err.max() <= LABEL_TOL, f"max relative label error {err.max()}"
     return err
 
 
@@ -122,7 +125,7 @@ def test_tv_label_given_and_computed_lse_agree():
     a = sdm.tv_label(*args, lse_q=dr["lse"], temperature=0.9)
     b = sdm.tv_label(*args, lse_q=None, temperature=0.9)
     torch.cuda.synchronize()
-    assert torch.max(torch.abs(a - b)).item() < 1e-5
+    assert torch.max(torch.abs(a - b) / b).item() < 2 * LABEL_TOL
     assert torch.all((a > 0) & (a <= 1 + 1e-5))
 
 
@@ -159,7 +162,7 @@ def test_tv_label_flags_bad_rows_without_faulting():
     assert out[1, 1] == -1.0
     keep = np.ones_like(out, bool)
     keep[1, 1] = False
-    assert np.abs(out[keep] - ref[keep]).max() <= LABEL_TOL
+    assert (np.abs(out[keep] - ref[keep]) / ref[keep]).max() <= LABEL_TOL
 
 
 def _full_label_case(name, idx, given_lse):

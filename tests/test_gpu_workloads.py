@@ -12,7 +12,7 @@ import oracle
 from speculative_decoding_markov_gb300 import binding as sdm
 from speculative_decoding_markov_gb300 import synthetic
 from speculative_decoding_markov_gb300.workloads import WORKLOADS
-from tests.helpers import np_of
+from tests.helpers import np_of, oracle_map, tree_first_decision, verify_first_decision
 
 pytestmark = pytest.mark.gpu
 TIE = 1e-5
@@ -55,9 +55,14 @@ def run_chain_workload(name, idx, modes=None):
     sub = sub_inputs(inp, idx)
     ids = np.asarray(idx, np.int32)
     U, W = np_of(sub["U"]), np_of(sub["W"])
-    odr = oracle.draft_chain(np_of(sub["L"]), U, W, np_of(sub["anchor"]),
-                             decode=oracle.SAMPLE if sample else oracle.GREEDY, temperature=w.temperature,
-                             seed=0, cycle=0, req_ids=ids)
+    Ls, ans = np_of(sub["L"]), np_of(sub["anchor"])
+
+    def one(j):   # one request per oracle call, the calls spread over the host cores
+        return oracle.draft_chain(Ls[j:j + 1], U, W, ans[j:j + 1], decode=oracle.SAMPLE if sample else oracle.GREEDY,
+                                  temperature=w.temperature, seed=0, cycle=0, req_ids=ids[j:j + 1])
+
+    parts = oracle_map(one, range(len(idx)))
+    odr = {k: np.concatenate([q[k] for q in parts]) for k in ("tokens", "logq", "lse", "margin")}
     gtok = host(dr["tokens"])[idx]
     for i in range(len(idx)):
         mism = np.nonzero(gtok[i] != odr["tokens"][i])[0]
@@ -115,12 +120,10 @@ def run_chain_workload(name, idx, modes=None):
         ovr = oracle.verify(om, oracle.SAMPLE if sample else oracle.GREEDY, np_of(opacked), opk["cu_seqlens"],
                             np_of(sub["anchor"]), odr["tokens"], budget=bsub, req_ids=ids, **okw)
         for j, i in enumerate(idx):
-            same = (host(vr["accept"])[i] == ovr["accept"][j] and
-                    np.array_equal(host(vr["out_tok"])[i], ovr["out_tok"][j]))
-            assert same or ovr["margin"][j] < TIE, f"{mode}: request {i} differs (margin {ovr['margin'][j]})"
-            assert same, f"{mode}: tie-zone event at request {i}"
-            if mode == "cap_accept":
-                assert host(vr["ceiling"])[i] == ovr["ceiling"][j]
+            first = verify_first_decision(ovr, j, host(vr["accept"])[i], host(vr["ceiling"])[i],
+                                          host(vr["out_tok"])[i])
+            assert first is None or first[1] < TIE, f"{mode}: request {i} differs at decision {first}"
+            assert first is None, f"{mode}: tie-zone event at request {i} ({first})"
         results[mode] = dict(accept=host(vr["accept"]), n_out=host(vr["n_out"]), out_tok=host(vr["out_tok"]),
                              ceiling=host(vr["ceiling"]))
     return w, results, osc
@@ -132,17 +135,18 @@ def test_tiny_chain_full():
 
 
 def test_qwen3_8b_chain():
-    w, res, _ = run_chain_workload("qwen3_8b_chain", [0, 1, 38, 63])
+    w, res, _ = run_chain_workload("qwen3_8b_chain", [0, 1, 17, 31, 38, 50, 62, 63])
     assert res["compact"]["n_out"].sum() > w.R          # some drafts accepted
 
 
 def test_rejection_sampling():
-    w, res, _ = run_chain_workload("rejection_sampling", [0, 131, 255])
+    # both M tiles of the GEMMs (requests 0-127 and 128-255), their edges included
+    w, res, _ = run_chain_workload("rejection_sampling", [0, 37, 100, 127, 128, 131, 200, 255])
     assert res["static"]["accept"].max() > 0
 
 
 def test_mixed_traffic_modes():
-    w, res, osc = run_chain_workload("mixed_traffic", [0, 100, 254])
+    w, res, osc = run_chain_workload("mixed_traffic", [0, 100, 127, 128, 200, 254])
     np.testing.assert_array_equal(res["cap_accept"]["out_tok"], res["compact"]["out_tok"])
     np.testing.assert_array_equal(res["cap_accept"]["ceiling"], res["static"]["accept"])
     np.testing.assert_array_equal(res["compact"]["accept"], np.minimum(res["static"]["accept"], osc["budget"]))
@@ -157,13 +161,21 @@ def test_pctree():
     torch.cuda.synchronize()
     assert int(tr["dev_status"].item()) == 0 and int(vt["dev_status"].item()) == 0
     assert np.all(host(tr["n_nodes"]) == w.N + 1)
-    idx = [5]
+    # frontier rows of requests 0-15 fill the level GEMM's first M tile, 16-31 its second
+    idx = [5, 15, 16, 30]
     sub = sub_inputs(inp, idx)
-    otr = oracle.draft_tree(np_of(sub["L"]), np_of(sub["U"]), np_of(sub["W"]), np_of(sub["anchor"]), w.k, w.P, w.N)
+    Ls, Us, Ws, ans = np_of(sub["L"]), np_of(sub["U"]), np_of(sub["W"]), np_of(sub["anchor"])
+    parts = oracle_map(lambda j: oracle.draft_tree(Ls[j:j + 1], Us, Ws, ans[j:j + 1], w.k, w.P, w.N),
+                       range(len(idx)))
+    otr = {k: np.concatenate([q[k] for q in parts]) for k in ("tok", "parent", "depth", "score", "mask", "n_nodes",
+                                                              "margin")}
+    for j, i in enumerate(idx):
+        first = tree_first_decision(otr, j, host(tr["tok"])[i], host(tr["parent"])[i], host(tr["depth"])[i],
+                                    int(host(tr["n_nodes"])[i]), w.B)
+        assert first is None or first[1] < TIE, f"tree of request {i} differs at {first}"
+        assert first is None, f"tie-zone event in the tree of request {i} ({first})"
     for key in ("tok", "parent", "depth", "n_nodes"):
-        same = np.array_equal(host(tr[key])[idx], otr[key])
-        assert same or otr["margin"][0] < TIE, f"tree {key} differs (margin {otr['margin'][0]})"
-        assert same
+        np.testing.assert_array_equal(host(tr[key])[idx], otr[key])
     np.testing.assert_array_equal(host(tr["mask"])[idx].view(np.uint32), otr["mask"])
     assert close(host(tr["score"])[idx], otr["score"]).all()
     otgt = synthetic.tree_target(sub, torch.as_tensor(otr["tok"]), torch.as_tensor(otr["depth"]),

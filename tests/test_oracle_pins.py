@@ -1048,3 +1048,124 @@ def test_rnn_draft_follows_its_memo():
     z = L.astype(np.float32) + np.einsum("idr,rv->idv", mb, _f64_of_bf16(W)).astype(np.float32)
     np.testing.assert_array_equal(out["tokens"], z.argmax(-1))
     assert np.abs(memo).max() < 1.0 and np.abs(memo).max() > 0.3      # tanh range, not saturated away
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_rnn_projection_of_a_given_memo_closed_forms(T):
+    """The projection of a given memo (the GPU's memo enters the parity
+    tests through it) reduces to library routines: a zero memo gives the
+    backbone row's argmax and log-sum-exp (scipy), and a memo row c e_j (c a
+    bf16 value) gives z = L + c W[j, :], whose argmax, log-sum-exp and
+    inverse-CDF draw numpy forms directly."""
+    R, B, V, r = 3, 4, 97 * 8, 16
+    rng = np.random.default_rng(4)
+    L = rng.normal(0, 1.5, (R, B, V)).astype(np.float32)
+    W = _bf16_bits(rng.normal(0, 0.25, (r, V)))
+    zero = np.zeros((R, B, r), np.float32)
+    g = oracle.rnn_project(L, W, zero)
+    np.testing.assert_array_equal(g["tokens"], L.argmax(-1))
+    s = oracle.rnn_project(L, W, zero, decode=oracle.SAMPLE, temperature=T, seed=2, cycle=5)
+    np.testing.assert_allclose(s["lse"], special.logsumexp(L.astype(np.float64) / T, axis=-1), rtol=1e-13)
+    memo = np.zeros((R, B, r), np.float32)
+    jj = rng.integers(0, r, (R, B))
+    cc = _f64_of_bf16(_bf16_bits(rng.normal(0, 2.0, (R, B)))).astype(np.float32)
+    for i in range(R):
+        for d in range(B):
+            memo[i, d, jj[i, d]] = cc[i, d]
+    z = (L.astype(np.float32) + (cc[..., None].astype(np.float64) *
+                                 _f64_of_bf16(W)[jj]).astype(np.float32)).astype(np.float32)
+    g = oracle.rnn_project(L, W, memo)
+    np.testing.assert_array_equal(g["tokens"], z.argmax(-1))
+    s = oracle.rnn_project(L, W, memo, decode=oracle.SAMPLE, temperature=T, seed=2, cycle=5)
+    zt = z.astype(np.float64) / T
+    np.testing.assert_allclose(s["lse"], special.logsumexp(zt, axis=-1), rtol=1e-13)
+    for i in range(R):
+        for d in range(B):
+            wts = np.exp(zt[i, d] - zt[i, d].max())
+            u = oracle.uniform(2, 5, oracle.STREAM_DRAFT, i, d + 1, 0)
+            y = int(np.searchsorted(np.cumsum(wts), u * wts.sum(), side="right"))
+            assert s["tokens"][i, d] == y
+            assert abs(s["logq"][i, d] - (zt[i, d, y] - s["lse"][i, d])) < 1e-12
+
+
+def test_rnn_projection_follows_the_rnn_draft():
+    """Fed the memo of the oracle's own RNN draft (rounded to fp32), the
+    projection takes the same decisions as the draft, position by position."""
+    w = small(R=6, B=5, V=400, r=32, sigma=(0.5,), l_std=1.0)
+    inp = _inputs(w, seed=12)
+    rnn = synthetic.rnn_inputs(w, seed=12)
+    L, U, W, an = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"])
+    A, X = np_of(rnn["A_rnn"]), np_of(rnn["X_rnn"])
+    for dec in (oracle.GREEDY, oracle.SAMPLE):
+        dr = oracle.draft_chain_rnn(L, U, W, A, X, an, decode=dec, temperature=0.8, seed=1, cycle=2)
+        memo = oracle.rnn_memo(A, U, X, an, dr["tokens"])
+        pj = oracle.rnn_project(L, W, memo.astype(np.float32), decode=dec, temperature=0.8, seed=1, cycle=2)
+        same_bf16 = np.all(_bf16_bits(memo) == _bf16_bits(memo.astype(np.float32)), axis=-1)
+        assert same_bf16.mean() > 0.9
+        np.testing.assert_array_equal(pj["tokens"][same_bf16], dr["tokens"][same_bf16])
+        np.testing.assert_allclose(pj["lse"][same_bf16], dr["lse"][same_bf16], rtol=1e-14)
+
+
+def test_verify_margins_belong_to_their_decisions():
+    """One margin per accept test and one for the final draw: the test of
+    row p reports |ln u - ln(p/q)| with u the accept uniform of that row,
+    rows past the rejection report none (infinity), and greedy decisions
+    report none at all."""
+    w = small(R=10, B=5, V=64, r=16, l_dtype=FP32, target_dtype=FP32, sigma=(0.8,), temperature=1.0)
+    inp = _inputs(w, seed=8)
+    an, U, W = np_of(inp["anchor"]), np_of(inp["U"]), np_of(inp["W"])
+    dr = oracle.draft_chain(np_of(inp["L"]), U, W, an, decode=oracle.SAMPLE, seed=3, cycle=0)
+    pk = oracle.pack_ragged(an, dr["tokens"], None, np.array([64], np.int32))
+    tgt = synthetic.chain_target(inp, torch.as_tensor(dr["tokens"]), FP32)
+    packed = np_of(synthetic.gather_packed(tgt, torch.as_tensor(pk["packed_req"]), torch.as_tensor(pk["packed_pos"])))
+    ref = oracle.verify(oracle.STATIC, oracle.SAMPLE, packed, pk["cu_seqlens"], an, dr["tokens"], logq=dr["logq"],
+                        lse_q=dr["lse"], L=np_of(inp["L"]), U=U, W=W, seed=3, cycle=0)
+    assert ref["margin"].shape == (w.R, w.B + 1)
+    cu = pk["cu_seqlens"]
+    for i in range(w.R):
+        A = ref["ceiling"][i]
+        for p in range(w.B):
+            if p > A or (p == A and A == w.B):
+                assert ref["margin"][i, p] == np.inf
+                continue
+            row = packed[cu[i] + p].astype(np.float64)
+            lp = row[dr["tokens"][i, p]] - special.logsumexp(row)
+            lu = math.log(oracle.uniform(3, 0, oracle.STREAM_ACCEPT, i, p, 0))
+            assert abs(ref["margin"][i, p] - abs(lu - (lp - dr["logq"][i, p]))) < 1e-9
+            assert (lu < lp - dr["logq"][i, p]) == (p < A)
+        assert 0 <= ref["margin"][i, w.B] < 1
+    gr = oracle.verify(oracle.STATIC, oracle.GREEDY, packed, cu, an, dr["tokens"])
+    assert np.all(gr["margin"] == np.inf)
+
+
+def test_tree_margins_belong_to_their_decisions():
+    """The tree's margins: level d's prune boundary gap equals the gap
+    between the P-th and (P+1)-th candidate of a brute-force replay of that
+    level (scores in double), the top-N gap and the ranking gap follow the
+    output scores."""
+    w = small(R=3, B=3, V=16, r=16, l_dtype=FP32, sigma=(0.5,), l_std=1.0)
+    inp = _inputs(w, seed=6)
+    L, U, W, an = np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"])
+    k, P, N = 3, 2, 5
+    out = oracle.draft_tree(L, U, W, an, k=k, P=P, N=N)
+    assert out["margin"].shape == (w.R, w.B + 2)
+    Wf, Uf = _f64_of_bf16(W), _f64_of_bf16(U)
+    for i in range(w.R):
+        front = [(an[i], 0.0)]
+        pool = []
+        for d in range(w.B):
+            cands = []
+            for slot, (tok, s) in enumerate(front):
+                z = (L[i, d].astype(np.float32) + (Uf[tok] @ Wf).astype(np.float32)).astype(np.float32)
+                lse = special.logsumexp(z.astype(np.float64))
+                order = sorted(range(w.V), key=lambda v: (-z[v], v))[:k]
+                cands += [(s + float(z[v]) - lse, slot, c, v) for c, v in enumerate(order)]
+            cands.sort(key=lambda c: (-c[0], c[1], c[2]))
+            gap = cands[P - 1][0] - cands[P][0] if len(cands) > P else np.inf
+            assert abs(out["margin"][i, d] - gap) < 1e-9 or gap == out["margin"][i, d]
+            front = [(c[3], c[0]) for c in cands[:P]]
+            pool += [c[0] for c in cands[:P]]
+        pool.sort(reverse=True)
+        assert abs(out["margin"][i, w.B] - (pool[N - 1] - pool[N])) < 1e-9
+        sc = out["score"][i, 1:out["n_nodes"][i]]
+        assert abs(out["margin"][i, w.B + 1] - np.min(sc[:-1] - sc[1:])) < 1e-12
