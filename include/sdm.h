@@ -382,6 +382,26 @@ sdm_status sdm_verify_greedy_static(sdm_vmode mode, const void* target, sdm_dtyp
                                     int R, int gamma, int V, int32_t* accept, int32_t* ceiling,
                                     int32_t* out_tok, int32_t* n_out, int32_t* dev_status, void* stream);
 
+/*
+ * check_timeout_path: exercises the device-side timeout path on purpose (no
+ * counterpart on the pages; a failure-detection check).  Every pipeline wait
+ * of the tensor-core kernels is bounded by a wall-clock limit (2 s in normal
+ * calls); when one runs out the kernel ORs SDM_DEV_TIMEOUT into *dev_status,
+ * waits (bounded) for the copies and tensor-core work it has in flight, frees
+ * its tensor memory and returns, so the context stays usable.  This call
+ * launches the greedy chain's Markov GEMM for step 1 on the given inputs with
+ * its loads withheld and every wait limited to wait_ns (1 us .. 1 s), so
+ * every wait runs out: afterwards *dev_status holds SDM_DEV_TIMEOUT and
+ * later calls on the stream run normally.  Nothing but the keys in ws is
+ * written.
+ * In:  as sdm_draft_chain (dense path); ws at least
+ *      sdm_workspace_size(SDM_OP_DRAFT_CHAIN, R, B, V, r, 0, 0, 0) bytes;
+ *      dev_status must not be NULL.
+ */
+sdm_status sdm_check_timeout_path(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                                  const int32_t* anchor, int R, int B, int V, int r, unsigned long long wait_ns,
+                                  void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* sdm_status_str(sdm_status status);
 

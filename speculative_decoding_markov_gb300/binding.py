@@ -27,7 +27,7 @@ DEV_TIER_OVERFLOW = 64
 EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare", "sdm_draft_chain",
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
            "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_schedule_threshold",
-           "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str", "sdm_status_of_device",
+           "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str", "sdm_status_of_device", "sdm_check_timeout_path",
            "sdm_version")
 
 
@@ -61,6 +61,9 @@ def _declare(lib):
     lib.sdm_schedule_dynamic.argtypes = [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_pack_ragged.restype = _I
     lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
+    lib.sdm_check_timeout_path.restype = _I
+    lib.sdm_check_timeout_path.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, ctypes.c_ulonglong, _VP, _SZ, _VP,
+                                           _VP]
     lib.sdm_status_of_device.restype = _I
     lib.sdm_status_of_device.argtypes = [ctypes.c_int32]
     lib.sdm_verify.restype = _I
@@ -177,6 +180,20 @@ def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0
     _check(st, "sdm_draft_chain")
     out["dev_status"] = dev_status
     return out
+
+
+def check_timeout_path(L, U, W, anchor, wait_ns, dev_status=None):
+    """One Markov GEMM launch with its loads withheld and every wait limited
+    to wait_ns: the kernel records DEV_TIMEOUT and winds down."""
+    _need_cuda(L, U, W, anchor)
+    R, B, V = L.shape
+    r = U.shape[1]
+    ws = workspace(OP_DRAFT_CHAIN, R, B, V, r, device=L.device)
+    dev_status = new_status(L.device) if dev_status is None else dev_status
+    st = lib().sdm_check_timeout_path(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(anchor), R, B, V, r,
+                                      int(wait_ns), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_check_timeout_path")
+    return dev_status
 
 
 def draft_chain_rnn(L, U, W, A, X, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0, out=None, ws=None,

@@ -501,6 +501,49 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     return SDM_OK;
 }
 
+sdm_status sdm_check_timeout_path(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                                  const int32_t* anchor, int R, int B, int V, int r, unsigned long long wait_ns,
+                                  void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!L || !U || !W || !anchor || !dev_status || R <= 0 || B <= 0 || V <= 0 || r <= 0) return SDM_ERR_INVALID_ARG;
+    if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (wait_ns < 1000ull || wait_ns > 1000000000ull) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W)) return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_chain_dense(R, B, V)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int fp32 = dtL == SDM_FP32;
+    const int l_rows = std::min(R, kTileM);
+    CUtensorMap tmW, tmL;
+    if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
+    const int n_tiles = (V + kTileN - 1) / kTileN;
+    const int gy = (R + kTileM - 1) / kTileM;
+    const int gx = gemm_grid_x(n_tiles, gy);
+    auto* keys = static_cast<unsigned long long*>(ws);
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    p.rows = R;
+    p.R = R;
+    p.B = B;
+    p.V = V;
+    p.r = r;
+    p.n_tiles = n_tiles;
+    p.l_fp32 = fp32;
+    p.l_rows = l_rows;
+    p.P = 1;
+    p.k = 1;
+    p.d = 1;
+    p.inv_t = 1.0f;
+    gemm_pick_stages(p, MODE_CHAIN_GREEDY);
+    p.U = U;
+    p.anchor = anchor;
+    p.keys = keys;
+    p.dev_status = dev_status;
+    p.wait_ns = wait_ns;
+    p.withhold_loads = 1;   // nothing is loaded: every pipeline wait runs out
+    SDM_CHECK_CUDA(launch_fill_u64(keys, static_cast<size_t>(B) * R, 0ull, s));
+    SDM_CHECK_CUDA(launch_markov_gemm(MODE_CHAIN_GREEDY, tmW, tmL, p, gx, gy, s));
+    return SDM_OK;
+}
+
 sdm_status sdm_schedule_budget(const float* conf, int R, int gamma, const double* cost, float* survival,
                                int32_t* budget, double* expected, int32_t* total_tokens, void* ws, size_t ws_bytes,
                                int32_t* dev_status, void* stream) {

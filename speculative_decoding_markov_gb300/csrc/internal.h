@@ -112,6 +112,10 @@ struct GemmParams {
     // absmax (prepared tables): GEMM row m = token m
     unsigned int* absmax_bits;      // [rows] max_v |U[m] . W[:, v]| as fp32 bits (atomic max)
     int32_t* dev_status;
+    // wind-down check: a limit on every pipeline wait (0: the default), and
+    // withheld loads (the producers arm nothing, so every wait runs out)
+    unsigned long long wait_ns;
+    int withhold_loads;
 };
 
 // Ring depths for the launch shape (written into p.w_stages / p.l_stages).

@@ -79,7 +79,7 @@ __host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32,
     s.l_box_bytes = (static_cast<uint32_t>(l_rows) * 128u + 1023u) & ~1023u;
     s.l_stage_bytes = mode_reads_l(mode) ? s.l_box_bytes * (l_fp32 ? 2u : 1u) : 0u;
     s.bar_off = s.l_off + static_cast<uint32_t>(l_stages) * s.l_stage_bytes;
-    s.total = s.bar_off + static_cast<uint32_t>(2 * w_stages + 2 * l_stages + 5) * 8u + 16u + 1024u;
+    s.total = s.bar_off + static_cast<uint32_t>(2 * w_stages + 2 * l_stages + 6) * 8u + 16u + 1024u;
     return s;
 }
 
@@ -604,7 +604,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* tfull = lempty + SL;
     uint64_t* tempty = tfull + 2;
     uint64_t* a_done = tempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(a_done + 1);
+    uint64_t* drain = a_done + 1;   // the MMA warp's own tensor-core work, before tensor memory is freed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    const uint64_t lim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -631,6 +633,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&tempty[b], kEpiWarps);
         }
         mbar_init(a_done, 1);
+        mbar_init(drain, 1);
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -671,13 +674,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         //     full, so the MMA warp commits once per tile (a commit waits for
         //     the MMA pipe to drain; one per stage would cost KB drains per
         //     tile).  The last slot holds A until it is in tensor memory.
-        if (lane == 0 && nt > 0) {
+        if (lane == 0 && nt > 0 && !p.withhold_loads) {
             const uint64_t pol_w = policy_evict_last();
             bool ok = true;
+            int issued = 0;   // tiles whose W loads were issued
             for (int i = 0; i < nt && ok; ++i) {
                 const int slot = i % NTS;
-                if (i >= NTS) ok = mbar_wait(&wdone[slot], ((i / NTS) - 1) & 1);
-                else if (slot == NTS - 1) ok = mbar_wait(a_done, 0);
+                if (i >= NTS) ok = mbar_wait(&wdone[slot], ((i / NTS) - 1) & 1, lim);
+                else if (slot == NTS - 1) ok = mbar_wait(a_done, 0, lim);
                 if (!ok) break;
                 const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -687,8 +691,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tma_load_2d(st, &tmW, &wfull[s], v0, kb * 64, pol_w);
                     tma_load_2d(st + kWBoxBytes, &tmW, &wfull[s], v0 + kBoxN, kb * 64, pol_w);
                 }
+                issued = i + 1;
             }
             if (!ok) fail_timeout(p);
+            // every copy issued has landed before the CTA may exit (a wait
+            // elsewhere may have run out while they were in flight): slot sl
+            // was armed by the tiles sl, sl + NTS, ... below `issued`
+            for (int sl = 0; sl < NTS && sl < issued; ++sl) {
+                const int arms = (issued - 1 - sl) / NTS + 1;
+                for (int kb = 0; kb < KB; ++kb) mbar_wait(&wfull[sl * KB + kb], (arms - 1) & 1, lim);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -715,7 +727,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         bool ok = true;
         for (int i = 0; i < nt && ok; ++i) {
             const int b = i & 1;
-            if (i >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[b], ((i >> 1) - 1) & 1));
+            if (i >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[b], ((i >> 1) - 1) & 1, lim));
             if (!ok) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
@@ -723,7 +735,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint32_t par = static_cast<uint32_t>(i / NTS) & 1u;
             for (int kb = 0; kb < KB; ++kb) {
                 const int s = slot * KB + kb;
-                ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par));
+                ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par, lim));
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
@@ -735,18 +747,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (ok) mma_commit_warp(&tfull[b]);
         }
         if (!ok && lane == 0) fail_timeout(p);
+        // every tensor-core operation this warp issued (the A copy, the
+        // MMAs) completes before tensor memory is freed, whether or not the
+        // epilogue waited for it
+        mma_commit_warp(drain);
+        mbar_wait(drain, 0, lim);
         __syncwarp();
     } else if (warp == 2) {
         // 2b. L producer: the tile's two 64-id boxes of L rows, one stage each
-        if (mode_reads_l(MODE) && lane == 0 && nt > 0) {
+        if (mode_reads_l(MODE) && lane == 0 && nt > 0 && !p.withhold_loads) {
             const uint64_t pol_l = policy_evict_first();
             const int lrow0 = (MODE == MODE_TREE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
             bool ok = true;
-            int t = 0, lap = 0;
+            int t = 0, lap = 0, issued = 0;   // boxes issued
             for (int i = 0; i < nt && ok; ++i) {
                 const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
                 for (int h = 0; h < 2; ++h, t = (t + 1 == SL) ? (++lap, 0) : t + 1) {
-                    if (lap > 0 && !mbar_wait(&lempty[t], (lap - 1) & 1)) {
+                    if (lap > 0 && !mbar_wait(&lempty[t], (lap - 1) & 1, lim)) {
                         ok = false;
                         break;
                     }
@@ -755,9 +772,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int vb = v0 + h * kBoxN;
                     tma_load_3d(sl, &tmL, &lfull[t], vb, p.d - 1, lrow0, pol_l);
                     if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &lfull[t], vb + 32, p.d - 1, lrow0, pol_l);
+                    ++issued;
                 }
             }
             if (!ok) fail_timeout(p);
+            // every box issued has landed before the CTA may exit: stage t
+            // was armed by the boxes t, t + SL, ... below `issued`
+            for (int st = 0; st < SL && st < issued; ++st) mbar_wait(&lfull[st], ((issued - 1 - st) / SL) & 1, lim);
         }
         __syncwarp();
     } else {
@@ -781,7 +802,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
                 const int vb[2] = {v0 + g * C, v0 + kBoxN + g * C};
                 st.issue(p, vb);
-                bool ok = mbar_wait(&tfull[b], (i >> 1) & 1);
+                bool ok = mbar_wait(&tfull[b], (i >> 1) & 1, lim);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) {
                     if (lane == 0) fail_timeout(p);
@@ -801,7 +822,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 st.consume_slice(p, vb[1], 1, acc);
                 continue;
             } else {
-            bool ok = mbar_wait(&tfull[b], (i >> 1) & 1);
+            bool ok = mbar_wait(&tfull[b], (i >> 1) & 1, lim);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) {
                 if (lane == 0) fail_timeout(p);
@@ -822,7 +843,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 if (mode_reads_l(MODE)) {
-                    bool lok = mbar_wait(&lfull[t], lap & 1);
+                    bool lok = mbar_wait(&lfull[t], lap & 1, lim);
                     lok = __all_sync(0xffffffffu, lok);
                     if (!lok) {
                         ok = false;

@@ -311,7 +311,11 @@ __device__ bool stage_bulk(void* dst, const void* src, uint32_t bytes, SelShared
                       bytes - off < kBulkChunk ? bytes - off : kBulkChunk, &sh.bar);
     }
     __syncthreads();
-    return mbar_wait(&sh.bar, 0);
+    if (mbar_wait(&sh.bar, 0)) return true;
+    // the copy did not land in time: wait once more (bounded) so that the
+    // CTA does not go on, or exit, while it may still write shared memory
+    mbar_wait(&sh.bar, 0);
+    return false;
 }
 
 // Markov logits of the 16 columns v0 .. v0 + 15 for token prev, without L:

@@ -45,6 +45,22 @@ def test_status_strings_and_version(lib):
     assert lib.sdm_version() >= 100
 
 
+def test_timeout_check_host_validation(lib):
+    f = lib.sdm_check_timeout_path
+    a = [FAKE, 0, FAKE, FAKE, FAKE, 4, 7, 1024, 64, 50_000, FAKE, 1 << 30, FAKE, None]
+    bad = list(a)
+    bad[9] = 10                                 # a limit below 1 us
+    assert f(*bad) == 1
+    bad[9] = 2_000_000_000                      # above 1 s
+    assert f(*bad) == 1
+    bad = list(a)
+    bad[12] = None                              # the status word is where the result goes
+    assert f(*bad) == 1
+    bad = list(a)
+    bad[11] = 16                                # workspace too small
+    assert f(*bad) == 5
+
+
 def test_device_bits_map_to_a_status(lib):
     f = lib.sdm_status_of_device
     assert f(0) == 0

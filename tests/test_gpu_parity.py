@@ -622,3 +622,31 @@ def test_verify_tree():
     for k in ("accept", "out_tok", "n_out"):
         np.testing.assert_array_equal(host(out[k]), ref[k])
     assert ref["accept"].max() >= 1
+
+
+# ---------------------------------------------------------------------------
+# failure detection: a bounded wait that runs out
+# ---------------------------------------------------------------------------
+def test_a_wait_that_runs_out_is_reported_and_the_stream_stays_usable():
+    """The Markov GEMM with its loads withheld and a 50 us limit on every
+    wait: every wait runs out, the kernel records SDM_DEV_TIMEOUT, drains
+    what it had in flight and returns; the next ordinary calls on the same
+    stream give the oracle's tokens."""
+    w = small(R=40, B=4, V=4160, r=128, l_dtype=BF16, sigma=(0.5,), l_std=2.0)
+    inp = synthetic.generate(w, seed=31)
+    L, U, W, an = dev(inp["L"]), dev(inp["U"]), dev(inp["W"]), dev(inp["anchor"])
+    st = sdm.check_timeout_path(L, U, W, an, 50_000)
+    torch.cuda.synchronize()
+    assert int(st.item()) == sdm.DEV_TIMEOUT
+    assert sdm.lib().sdm_status_of_device(int(st.item())) == 7           # SDM_ERR_TIMEOUT
+    ref = oracle.draft_chain(np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    for _ in range(2):
+        out = sdm.draft_chain(L, U, W, an)
+        torch.cuda.synchronize()
+        assert int(out["dev_status"].item()) == 0
+        np.testing.assert_array_equal(host(out["tokens"]), ref["tokens"])
+    st2 = sdm.check_timeout_path(L, U, W, an, 1_000_000)                  # a second run, a longer limit
+    out = sdm.draft_chain(L, U, W, an)
+    torch.cuda.synchronize()
+    assert int(st2.item()) == sdm.DEV_TIMEOUT and int(out["dev_status"].item()) == 0
+    np.testing.assert_array_equal(host(out["tokens"]), ref["tokens"])
