@@ -212,14 +212,28 @@ sdm_status sdm_draft_chain_rnn(const void* L, sdm_dtype dtL, const uint16_t* U, 
  *   tok, parent, depth [R, N+1] int32; score [R, N+1] fp32;
  *   mask [R, N+1, ceil((N+1)/32)] uint32, bit j of row c set iff slot j is c
  *   or an ancestor of c; n_nodes [R] int32 (root included).
- * Each level runs the tcgen05 GEMM for every frontier row with per-16-column
- * (max, sum of exp) records in its epilogue; the row's top-k ids lie in the
- * k blocks with the largest maxima, so one CTA per row ranks the records,
- * recomputes the logits of its 2k best blocks and ranks those.
+ * prepared: NULL, or the tables sdm_markov_prepare built from U and W.
+ * With prepared tables: since |U[y] . W[:, v]| <= c(y) for every v, the top
+ * k ids of parent y have L[v] >= L_(k) - 2 c(y), L_(k) the k-th largest
+ * backbone logit of the row.  One HBM-bound pass over L lists, per 32 KB
+ * chunk of every (request, level) row, the ids with L >= theta - 2 c_max
+ * (theta a lower bound on the chunk's k-th largest value); each level then
+ * runs the tcgen05 GEMM for every frontier row with only an online
+ * log-sum-exp in its epilogue, and one CTA per request scores the listed ids
+ * each parent can need exactly (z = L + U[y] . W^T[v]), takes each parent's
+ * top k, the children's scores and the prune.  A row whose lists overflow
+ * takes the exact top k over the whole vocabulary instead (slow).  Needs
+ * V <= 64 * 16384 (bf16 L) or 64 * 8192 (fp32 L), R B ceil(V / 16384 or
+ * 8192) <= 2^30.
+ * Without: each level runs the tcgen05 GEMM for every frontier row with
+ * per-16-column (max, sum of exp) records in its epilogue; the row's top-k
+ * ids lie in the k blocks with the largest maxima, so one CTA per row ranks
+ * the records, recomputes the logits of its 2k best blocks and ranks those.
+ * Both give the same tree.
  * Constraints: 1 <= k <= 8, 1 <= P, P*k <= 64, 128 % P == 0, N <= P*B,
  * P*B + 1 <= 8192, V <= 524288 (else SDM_ERR_UNSUPPORTED).
  */
-sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, const void* prepared,
                           const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N,
                           int32_t* tok, int32_t* parent, int32_t* depth, float* score,
                           uint32_t* mask, int32_t* n_nodes,

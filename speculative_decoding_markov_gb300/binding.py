@@ -53,8 +53,8 @@ def _declare(lib):
     lib.sdm_draft_chain.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _F, SdmRng, _VP, _VP, _VP, _VP,
                                     _SZ, _VP, _VP]
     lib.sdm_draft_tree.restype = _I
-    lib.sdm_draft_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP,
-                                   _VP, _SZ, _VP, _VP]
+    lib.sdm_draft_tree.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _VP, _VP, _VP, _VP,
+                                   _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_schedule_budget.restype = _I
     lib.sdm_schedule_budget.argtypes = [_VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_schedule_dynamic.restype = _I
@@ -221,7 +221,7 @@ def draft_chain_rnn(L, U, W, A, X, anchor, decode=GREEDY, temperature=1.0, seed=
     return out
 
 
-def draft_tree(L, U, W, anchor, k, P, N, out=None, ws=None, dev_status=None):
+def draft_tree(L, U, W, anchor, k, P, N, out=None, ws=None, dev_status=None, prepared=None):
     _need_cuda(L, U, W, anchor)
     R, B, V = L.shape
     r = U.shape[1]
@@ -237,7 +237,8 @@ def draft_tree(L, U, W, anchor, k, P, N, out=None, ws=None, dev_status=None):
                    n_nodes=torch.empty((R,), dtype=torch.int32, device=dev))
     ws = workspace(OP_DRAFT_TREE, R, B, V, r, P, k, N, device=dev) if ws is None else ws
     dev_status = new_status(dev) if dev_status is None else dev_status
-    st = lib().sdm_draft_tree(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(anchor), R, B, V, r, k, P, N,
+    st = lib().sdm_draft_tree(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(prepared), _ptr(anchor), R, B, V, r,
+                              k, P, N,
                               _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["score"]),
                               _ptr(out["mask"]), _ptr(out["n_nodes"]), _ptr(ws), ws.numel(), _ptr(dev_status),
                               _stream())

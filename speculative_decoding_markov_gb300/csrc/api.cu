@@ -106,12 +106,25 @@ size_t ws_chain_rnn(int R, int B, int V, int r) {
     return ws_chain_dense(R, B, V) + align256(static_cast<size_t>(R) * r * 4) + align256(static_cast<size_t>(R) * r * 2);
 }
 
-// block records [rows][nb], per-row top-k and log-sum-exp, frontier and pool
-size_t ws_tree(int R, int B, int P, int V) {
+// frontier and pool, then either the record path's block records [rows][nb],
+// per-row top-k and log-sum-exp, or the pruned path's scan lists (sized for
+// the larger fp32 chunk count) and the GEMM's log-sum-exp partials
+size_t ws_tree_common(int R, int B, int P) {
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
-    return align256(rows * n_blocks16(V) * 8) + align256(rows * kMaxTopK * 8) + align256(rows * 4) +
-           3 * align256(rows * 4) + align256(R * 4) + 4 * align256(pool * 4) + align256(R * 4);
+    return 3 * align256(rows * 4) + align256(R * 4) + 4 * align256(pool * 4) + align256(R * 4);
+}
+
+int tree_n_part(int R, int P, int V) {
+    const int gy = (R * P + kTileM - 1) / kTileM;
+    return gemm_grid_x((V + kTileN - 1) / kTileN, gy) * kColGroups;
+}
+
+size_t ws_tree(int R, int B, int P, int V) {
+    const size_t rows = static_cast<size_t>(R) * P;
+    const size_t records = align256(rows * n_blocks16(V) * 8) + align256(rows * kMaxTopK * 8) + align256(rows * 4);
+    const size_t pruned = ws_chain_pruned(R, B, V) + align256(rows * tree_n_part(R, P, V) * 8);
+    return ws_tree_common(R, B, P) + std::max(records, pruned);
 }
 
 size_t ws_verify(int R, int rows, int V) {
@@ -409,7 +422,7 @@ sdm_status sdm_draft_chain_rnn(const void* L, sdm_dtype dtL, const uint16_t* U, 
                              dev_status, static_cast<cudaStream_t>(stream));
 }
 
-sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, const void* prepared,
                           const int32_t* anchor, int R, int B, int V, int r, int k, int P, int N, int32_t* tok,
                           int32_t* parent, int32_t* depth, float* score, uint32_t* mask, int32_t* n_nodes, void* ws,
                           size_t ws_bytes, int32_t* dev_status, void* stream) {
@@ -420,15 +433,18 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     if (k > kMaxTopK || k > V || P * k > 64 || kTileM % P != 0 || N > P * B) return SDM_ERR_UNSUPPORTED;
     if (static_cast<long long>(P) * B + 1 > 8192) return SDM_ERR_UNSUPPORTED;   // the pool is ranked in shared memory
     if (V > kMaxSampleV) return SDM_ERR_UNSUPPORTED;   // the per-row chunk and candidate tables of the level select
+    const int fp32 = dtL == SDM_FP32;
+    const int n_chunks = pruned_chunks(V, fp32);
+    if (prepared) {
+        if (!aligned16(prepared)) return SDM_ERR_UNSUPPORTED;
+        if (n_chunks > kMaxPickChunks || static_cast<long long>(R) * B * n_chunks > (1LL << 30))
+            return SDM_ERR_UNSUPPORTED;
+    }
     if (!ws || ws_bytes < ws_tree(R, B, P, V)) return SDM_ERR_WORKSPACE;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t pool = static_cast<size_t>(R) * (1 + static_cast<size_t>(P) * B);
     Carver c{static_cast<uint8_t*>(ws)};
-    const int nb = n_blocks16(V);
-    auto* blk = c.take<float2>(rows * nb);
-    auto* row_top = c.take<float2>(rows * kMaxTopK);
-    float* row_lse = c.take<float>(rows);
     int32_t* front_tok = c.take<int32_t>(rows);
     int32_t* front_node = c.take<int32_t>(rows);
     float* front_score = c.take<float>(rows);
@@ -439,7 +455,6 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     float* pool_score = c.take<float>(pool);
     int32_t* pool_n = c.take<int32_t>(R);
 
-    const int fp32 = dtL == SDM_FP32;
     const int l_rows = std::min(kTileM / P, R);
     CUtensorMap tmW, tmL;
     if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
@@ -459,42 +474,118 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     p.l_rows = l_rows;
     p.P = P;
     p.k = k;
-    gemm_pick_stages(p, MODE_TREE);
     p.inv_t = 1.0f;
     p.U = U;
     p.anchor = anchor;
     p.front_tok = front_tok;
-    p.blk = blk;
-    p.nb = nb;
     p.dev_status = dev_status;
-    TreeSelectParams tp;
-    std::memset(&tp, 0, sizeof tp);
-    tp.blk = blk;
-    tp.nb = nb;
-    tp.rows = static_cast<int>(rows);
-    tp.P = P;
-    tp.B = B;
-    tp.V = V;
-    tp.r = r;
-    tp.k = k;
-    tp.front_tok = front_tok;
-    tp.L = L;
-    tp.l_fp32 = fp32;
-    tp.U = U;
-    tp.W = W;
-    tp.row_top = row_top;
-    tp.row_lse = row_lse;
-    tp.dev_status = dev_status;
-
     SDM_CHECK_CUDA(launch_tree_init(anchor, R, P, B, front_tok, front_node, front_score, n_front, pool_tok, pool_parent,
                                     pool_depth, pool_score, pool_n, dev_status, s));
-    for (int d = 1; d <= B; ++d) {
-        p.d = d;
-        tp.d = d;
-        SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE, tmW, tmL, p, gx, gy, s));
-        SDM_CHECK_CUDA(launch_tree_select(tp, s));
-        SDM_CHECK_CUDA(launch_tree_merge(row_top, row_lse, R, P, k, B, d, front_tok, front_node, front_score, n_front,
-                                         pool_tok, pool_parent, pool_depth, pool_score, pool_n, s));
+    if (prepared) {
+        // every (request, level) row of L listed once for the top k; per level
+        // the GEMM's log-sum-exp partials, then one CTA per request ranks the
+        // listed ids exactly and prunes
+        Carver pc{static_cast<uint8_t*>(const_cast<void*>(prepared))};
+        const uint16_t* Wt = pc.take<uint16_t>(static_cast<size_t>(V) * r);
+        const float* c_bound = pc.take<float>(V);
+        pc.take<float>(V);           // |U[v]|
+        pc.take<unsigned int>(V);    // A(v)
+        const float* c_max = pc.take<float>(1);
+        PrunedParams pp;
+        std::memset(&pp, 0, sizeof pp);
+        pp.L = L;
+        pp.l_fp32 = fp32;
+        pp.R = R;
+        pp.B = B;
+        pp.V = V;
+        pp.r = r;
+        pp.n_chunks = n_chunks;
+        pp.anchor = anchor;
+        pp.U = U;
+        pp.Wt = Wt;
+        pp.c_bound = c_bound;
+        pp.c_max = c_max;
+        const size_t segs = static_cast<size_t>(R) * B * pruned_chunks(V, 1);   // carved as ws_chain_pruned sizes it
+        pp.cand = c.take<uint2>(segs * kSegCap);
+        pp.cand_n = c.take<int32_t>(segs);
+        pp.cmax = c.take<float>(segs);
+        pp.dev_status = dev_status;
+        pp.kth = k;
+        const int n_part = gx * kColGroups;
+        auto* part = c.take<float2>(rows * n_part);
+        SDM_CHECK_CUDA(launch_chain_scan(pp, s));
+        p.part = part;
+        p.n_part = n_part;
+        gemm_pick_stages(p, MODE_TREE_LSE);
+        TreeLevelParams tl;
+        std::memset(&tl, 0, sizeof tl);
+        tl.cand = pp.cand;
+        tl.cand_n = pp.cand_n;
+        tl.n_chunks = n_chunks;
+        tl.L = L;
+        tl.l_fp32 = fp32;
+        tl.U = U;
+        tl.Wt = Wt;
+        tl.c_bound = c_bound;
+        tl.c_max = c_max;
+        tl.R = R;
+        tl.B = B;
+        tl.V = V;
+        tl.r = r;
+        tl.P = P;
+        tl.k = k;
+        tl.part = part;
+        tl.n_part = n_part;
+        tl.front_tok = front_tok;
+        tl.front_node = front_node;
+        tl.front_score = front_score;
+        tl.n_front = n_front;
+        tl.pool_tok = pool_tok;
+        tl.pool_parent = pool_parent;
+        tl.pool_depth = pool_depth;
+        tl.pool_score = pool_score;
+        tl.pool_n = pool_n;
+        tl.dev_status = dev_status;
+        for (int d = 1; d <= B; ++d) {
+            p.d = d;
+            tl.d = d;
+            SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE_LSE, tmW, tmL, p, gx, gy, s));
+            SDM_CHECK_CUDA(launch_tree_level(tl, s));
+        }
+    } else {
+        const int nb = n_blocks16(V);
+        auto* blk = c.take<float2>(rows * nb);
+        auto* row_top = c.take<float2>(rows * kMaxTopK);
+        float* row_lse = c.take<float>(rows);
+        p.blk = blk;
+        p.nb = nb;
+        gemm_pick_stages(p, MODE_TREE);
+        TreeSelectParams tp;
+        std::memset(&tp, 0, sizeof tp);
+        tp.blk = blk;
+        tp.nb = nb;
+        tp.rows = static_cast<int>(rows);
+        tp.P = P;
+        tp.B = B;
+        tp.V = V;
+        tp.r = r;
+        tp.k = k;
+        tp.front_tok = front_tok;
+        tp.L = L;
+        tp.l_fp32 = fp32;
+        tp.U = U;
+        tp.W = W;
+        tp.row_top = row_top;
+        tp.row_lse = row_lse;
+        tp.dev_status = dev_status;
+        for (int d = 1; d <= B; ++d) {
+            p.d = d;
+            tp.d = d;
+            SDM_CHECK_CUDA(launch_markov_gemm(MODE_TREE, tmW, tmL, p, gx, gy, s));
+            SDM_CHECK_CUDA(launch_tree_select(tp, s));
+            SDM_CHECK_CUDA(launch_tree_merge(row_top, row_lse, R, P, k, B, d, front_tok, front_node, front_score,
+                                             n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n, s));
+        }
     }
     SDM_CHECK_CUDA(launch_tree_finalize(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok, parent,
                                         depth, score, mask, n_nodes, s));

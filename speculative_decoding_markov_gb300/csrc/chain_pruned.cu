@@ -90,11 +90,8 @@ __device__ __forceinline__ const uint8_t* row_ptr(const PrunedParams& p, int row
     return static_cast<const uint8_t*>(p.L) + ((static_cast<size_t>(row) * p.B + (d - 1)) * p.V + v) * esz;
 }
 
-// The candidate threshold below a row maximum m for a Markov bound c, with
-// slack for the fp32 rounding of fp32(L) + Markov.
-__device__ __forceinline__ float threshold(float m, float c) {
-    return m - 2.0f * c - fabsf(m) * 9.765625e-4f - 9.5367431640625e-7f;
-}
+// The candidate threshold below a row maximum m for a Markov bound c.
+__device__ __forceinline__ float threshold(float m, float c) { return markov_cut(m, c); }
 
 // ---------------------------------------------------------------------------
 // A: candidate lists of every (request, step, chunk)
@@ -113,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
     constexpr int VPT = kChunkBytes / 16 / kThreads;        // vectors per thread
     constexpr int CHUNK_IDS = kChunkBytes / ESZ;
     __shared__ float s_wmax[kWarps];
+    __shared__ uint32_t s_ladder[kWarps][2];
     __shared__ int s_cnt[2];   // by item parity: a slot is reset two items after its last read
     pdl_wait();
     pdl_trigger();
@@ -155,16 +153,50 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
         float mc = s_wmax[0];
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) mc = fmaxf(mc, s_wmax[w]);
-        const float T = threshold(mc, cmax);
+        // the value the list is cut below: the chunk maximum for the argmax;
+        // for a top-k a lower bound theta on the chunk's k-th largest value,
+        // the first step of the ladder mc - {1/2, 1, 2, 4} reached by at least
+        // k vectors' maxima (each such vector holds a value >= theta, so at
+        // least k values are), -inf when none is
+        float theta = mc;
+        if (p.kth > 1) {
+            uint32_t ca = 0u, cb = 0u;   // two 16-bit counters each
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const float vm = vec_max<FP32>(x[k]);
+                ca += (vm >= mc - 0.5f ? 1u : 0u) + (vm >= mc - 1.0f ? 0x10000u : 0u);
+                cb += (vm >= mc - 2.0f ? 1u : 0u) + (vm >= mc - 4.0f ? 0x10000u : 0u);
+            }
+            ca = __reduce_add_sync(0xffffffffu, ca);
+            cb = __reduce_add_sync(0xffffffffu, cb);
+            if (lane == 0) {
+                s_ladder[warp][0] = ca;
+                s_ladder[warp][1] = cb;
+            }
+            __syncthreads();
+            uint32_t ta = 0u, tb = 0u;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                ta += s_ladder[w][0];
+                tb += s_ladder[w][1];
+            }
+            const uint32_t k = static_cast<uint32_t>(p.kth);
+            theta = (ta & 0xffffu) >= k ? mc - 0.5f
+                    : (ta >> 16) >= k   ? mc - 1.0f
+                    : (tb & 0xffffu) >= k ? mc - 2.0f
+                    : (tb >> 16) >= k   ? mc - 4.0f
+                                        : -INFINITY;
+        }
+        const float T = threshold(theta, cmax);
         const int seg = rs * nc + c;
         uint2* out = p.cand + static_cast<size_t>(seg) * kSegCap;
         if (tmax >= T) {   // only threads holding a candidate
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                if (vec_max<FP32>(x[k]) < T) continue;
+                const int i = threadIdx.x + k * kThreads;
+                if (i >= n_vec || vec_max<FP32>(x[k]) < T) continue;   // (a padded vector is never listed)
                 float v[VEC];
                 unpack<FP32>(x[k], v);
-                const int i = threadIdx.x + k * kThreads;
 #pragma unroll
                 for (int q = 0; q < VEC; ++q) {
                     if (v[q] >= T) {
@@ -830,14 +862,18 @@ int pruned_chunks(int V, int l_fp32) {
     return (V + per - 1) / per;
 }
 
-cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
+cudaError_t launch_chain_scan(const PrunedParams& p, cudaStream_t s) {
     const long long items = static_cast<long long>(p.R) * p.B * p.n_chunks;
     if (items > (1LL << 30)) return cudaErrorInvalidValue;
     // two CTAs per resident slot: a CTA that finishes early is replaced, which
     // evens out the tail better than one wave of equal shares
     const int grid = static_cast<int>(items < 8LL * num_sms() ? items : 8LL * num_sms());
-    cudaError_t e = p.l_fp32 ? launch_pdl(chain_scan_kernel<1>, dim3(grid), dim3(kThreads), 0, s, p)
-                             : launch_pdl(chain_scan_kernel<0>, dim3(grid), dim3(kThreads), 0, s, p);
+    return p.l_fp32 ? launch_pdl(chain_scan_kernel<1>, dim3(grid), dim3(kThreads), 0, s, p)
+                    : launch_pdl(chain_scan_kernel<0>, dim3(grid), dim3(kThreads), 0, s, p);
+}
+
+cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
+    cudaError_t e = launch_chain_scan(p, s);
     if (e != cudaSuccess) return e;
     const PickLayout lay = pick_layout(p.B, p.n_chunks, p.r);
     if (lay.cap < 1) return cudaErrorInvalidValue;

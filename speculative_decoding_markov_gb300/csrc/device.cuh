@@ -88,6 +88,14 @@ __device__ __forceinline__ Lse warp_lse(Lse v) {
     return v;
 }
 
+// Pruning by the Markov bound: with |U[y] . W[:, v]| <= c for every v, no id
+// whose backbone logit L_v lies below the returned value can reach a logit
+// z = fp32(L_v) + Markov that some id with L >= m reaches (m - 2 c, less
+// slack for the fp32 rounding of the sum).
+__device__ __forceinline__ float markov_cut(float m, float c) {
+    return m - 2.0f * c - fabsf(m) * 9.765625e-4f - 9.5367431640625e-7f;
+}
+
 __device__ __forceinline__ void set_status(int32_t* dev_status, int bits) {
     if (dev_status) atomicOr(dev_status, bits);
 }

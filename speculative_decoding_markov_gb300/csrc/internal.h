@@ -50,14 +50,17 @@ enum GemmMode {
     MODE_QLSE = 5,    // soft label pass 1: log-sum-exp of the draft logits of listed rows
     MODE_TVMIN = 6,   // soft label pass 2: sum_v min(q_v, p_v) of listed rows
     MODE_TVMIN_B16 = 7,   // the same for bf16 L and bf16 target rows, loads a tile ahead of use
-    MODE_TVMIN_B32 = 8    // the same for bf16 L and fp32 target rows
+    MODE_TVMIN_B32 = 8,   // the same for bf16 L and fp32 target rows
+    MODE_TREE_LSE = 9     // PCTree level, log-sum-exp only: one (max, sum) partial per frontier row, CTA and group
 };
 
 // Modes that stage a tile of L beside each W tile (the others read their L
 // rows, if any, straight from global memory).
 __host__ __device__ constexpr bool mode_reads_l(int mode) {
-    return mode == MODE_CHAIN_GREEDY || mode == MODE_CHAIN_SAMPLE || mode == MODE_TREE;
+    return mode == MODE_CHAIN_GREEDY || mode == MODE_CHAIN_SAMPLE || mode == MODE_TREE || mode == MODE_TREE_LSE;
 }
+// PCTree modes: GEMM row = (request, frontier slot), L row = the request's.
+__host__ __device__ constexpr bool mode_tree(int mode) { return mode == MODE_TREE || mode == MODE_TREE_LSE; }
 // Modes whose GEMM rows come from an explicit row list (res_tok / res_req).
 __host__ __device__ constexpr bool mode_row_list(int mode) {
     return mode == MODE_QLSE || mode == MODE_TVMIN || mode == MODE_TVMIN_B16 || mode == MODE_TVMIN_B32;
@@ -261,6 +264,38 @@ struct TreeSelectParams {
 };
 cudaError_t launch_tree_select(const TreeSelectParams& p, cudaStream_t s);
 
+// PCTree level by bound pruning (tree_pruned.cu): per request, the top-k
+// children of every frontier parent from the scan's lists and the prepared
+// tables, their scores from the MODE_TREE_LSE partials, the per-level prune.
+constexpr int kMaxTreeSlots = 64;   // frontier slots P (P k <= 64, k >= 1)
+
+struct TreeLevelParams {
+    const uint2* cand;          // the scan's lists [R * B][n_chunks][kSegCap]
+    const int32_t* cand_n;      // [R * B][n_chunks]
+    int n_chunks;
+    const void* L;              // [R, B, V]
+    int l_fp32;
+    const uint16_t* U;          // [V, r]
+    const uint16_t* Wt;         // [V, r] (prepared)
+    const float* c_bound;       // [V] (prepared)
+    const float* c_max;         // [1] (prepared)
+    int R, B, V, r, P, k, d;
+    const float2* part;         // [R * P][n_part] (max, sum) partials of MODE_TREE_LSE
+    int n_part;
+    int32_t* front_tok;
+    int32_t* front_node;
+    float* front_score;
+    int32_t* n_front;
+    int32_t* pool_tok;
+    int32_t* pool_parent;
+    int32_t* pool_depth;
+    float* pool_score;
+    int32_t* pool_n;
+    int32_t* dev_status;
+};
+size_t tree_level_smem(int P, int k, int r);
+cudaError_t launch_tree_level(const TreeLevelParams& p, cudaStream_t s);
+
 // PCTree
 cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
                              float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
@@ -302,10 +337,14 @@ struct PrunedParams {
     float* cmax;            // [R * B][n_chunks] chunk maxima
     int32_t* tokens;        // [R, B]
     int32_t* dev_status;
+    int kth;                // lists for the k-th largest (PCTree, k > 1); 0 or 1: the chain's argmax
 };
 
 int pruned_chunks(int V, int l_fp32);
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s);
+// The candidate lists alone (every (request, step) row), for a top-k of
+// kth > 1 (PCTree levels).
+cudaError_t launch_chain_scan(const PrunedParams& p, cudaStream_t s);
 // Prepared tables, step 1: W^T, |U[v]|, max |W[:, v]| and max |U[v]|; zeroes
 // absmax_bits for the absmax GEMM.  Step 2 (after that GEMM): the bounds.
 cudaError_t launch_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, uint16_t* Wt, float* u_norm,

@@ -95,7 +95,7 @@ __device__ __forceinline__ int gemm_row_token(const GemmParams& p, int grow) {
     } else if (MODE == MODE_CHAIN_SAMPLE) {
         if (grow >= p.R) return -1;
         t = (p.d == 1) ? p.anchor[grow] : p.tok_in[static_cast<size_t>(grow) * p.B + (p.d - 2)];
-    } else if (MODE == MODE_TREE) {
+    } else if (mode_tree(MODE)) {
         if (grow >= p.rows) return -1;
         t = p.front_tok[grow];
         if (t < 0) return -1;
@@ -391,6 +391,44 @@ __device__ __forceinline__ bool list_row(const GemmParams& p, int grow, size_t& 
 __device__ __forceinline__ float2* part_slot(const GemmParams& p, int grow, int group) {
     return p.part + static_cast<size_t>(grow) * p.n_part + blockIdx.x * kColGroups + group;
 }
+
+// Online (max, sum) of the logits z of a frontier row over every column this
+// thread consumes: the partial (m, s) = (max z, sum exp(z - m)), each
+// exponential one fma and one ex2 (2^(z log2(e) - m log2(e))).  A thread that
+// consumed nothing leaves (-inf, 0).
+template <>
+struct Epi<MODE_TREE_LSE> {
+    bool valid;
+    int group;
+    float m, s;
+    __device__ __forceinline__ void init(const GemmParams& p, int grow) {
+        valid = grow < p.rows && p.front_tok[grow] >= 0;
+        m = -INFINITY;
+        s = 0.f;
+    }
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+                                            int g, const uint32_t (&acc)[C]) {
+        if (!valid || vbase >= p.V) return;
+        float z[C];
+        load_l(sl, lbb, p.l_fp32, lrow / p.P, g, z);
+#pragma unroll
+        for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
+        mask_tail(z, vbase, p.V);
+        const float mb = maxc(z);   // finite: column vbase < V
+        if (mb > m) {
+            s *= fast_exp2((m - mb) * kLog2e);   // 0 while m = -inf
+            m = mb;
+        }
+        const float mo = m * kLog2e;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(fmaf(z[j], kLog2e, -mo));   // 2^-inf = 0 on the tail
+        s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+    }
+    __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
+        if (valid) *part_slot(p, grow, group) = make_float2(m, s);
+    }
+};
 
 // Online (max, sum) of x = z log2(e) / T over every column this thread
 // consumes; the partial is (max x ln 2, sum 2^(x - max x)) = (max z / T, sum
@@ -757,7 +795,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // 2b. L producer: the tile's two 64-id boxes of L rows, one stage each
         if (mode_reads_l(MODE) && lane == 0 && nt > 0 && !p.withhold_loads) {
             const uint64_t pol_l = policy_evict_first();
-            const int lrow0 = (MODE == MODE_TREE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
+            const int lrow0 = mode_tree(MODE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
             bool ok = true;
             int t = 0, lap = 0, issued = 0;   // boxes issued
             for (int i = 0; i < nt && ok; ++i) {
@@ -921,6 +959,7 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
         case MODE_TVMIN: return launch_mode<MODE_TVMIN>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TVMIN_B16: return launch_mode<MODE_TVMIN_B16>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TVMIN_B32: return launch_mode<MODE_TVMIN_B32>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TREE_LSE: return launch_mode<MODE_TREE_LSE>(tmW, tmL, p, grid_x, grid_y, s);
         default: return cudaErrorInvalidValue;
     }
 }

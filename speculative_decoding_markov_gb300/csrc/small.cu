@@ -3,6 +3,7 @@
 // and PCTree's per-level merge/prune and final top-N selection.
 #include "device.cuh"
 #include "internal.h"
+#include "tree_common.cuh"
 #include "verify_greedy.cuh"
 
 namespace sdm {
@@ -621,21 +622,6 @@ __global__ void tree_init_kernel(const int32_t* anchor, int R, int P, int B, int
     n_front[i] = 1;
 }
 
-struct Cand {
-    float s;
-    int slot, rank, tok;
-};
-
-// (s desc, slot asc, rank asc), with s compared through its order-preserving
-// bits: a strict total order even when a score is NaN, so that parallel ranks
-// form a permutation.
-__device__ __forceinline__ bool cand_before(const Cand& a, const Cand& b) {
-    const uint32_t oa = ordered_bits(a.s), ob = ordered_bits(b.s);
-    if (oa != ob) return oa > ob;
-    if (a.slot != b.slot) return a.slot < b.slot;
-    return a.rank < b.rank;
-}
-
 // One CTA per request: the children of every frontier slot (its top-k by z,
 // from the level's select kernel) get s(c) = s(p) + z - lse; they are ranked
 // in parallel and the best P kept.
@@ -660,40 +646,8 @@ __global__ void tree_merge_kernel(const float2* row_top, const float* row_lse, i
         cand[t] = Cand{front_score[grow] + (e.x - row_lse[grow]), f, q, __float_as_int(e.y)};
     }
     __syncthreads();
-    // rank of every child by (s desc, slot asc, rank asc): a strict total order
-    const int nc = nf * k;
-    for (int t = threadIdx.x; t < nc; t += blockDim.x) {
-        const Cand me = cand[t];
-        int rk = 0;
-        for (int u = 0; u < nc; ++u) rk += cand_before(cand[u], me) ? 1 : 0;
-        sorted[rk] = me;
-    }
-    __syncthreads();
-    const int keep = nc < P ? nc : P;
-    const int pool_cap = 1 + P * B;
-    const size_t pb = static_cast<size_t>(i) * pool_cap;
-    const int np = pool_n[i];
-    for (int c = threadIdx.x; c < P; c += blockDim.x) {
-        const size_t fo = static_cast<size_t>(i) * P + c;
-        if (c < keep) {
-            const Cand cd = sorted[c];
-            pool_tok[pb + np + c] = cd.tok;
-            pool_parent[pb + np + c] = parent_node[cd.slot];
-            pool_depth[pb + np + c] = d;
-            pool_score[pb + np + c] = cd.s;
-            front_tok[fo] = cd.tok;
-            front_node[fo] = np + c;
-            front_score[fo] = cd.s;
-        } else {
-            front_tok[fo] = -1;
-            front_node[fo] = -1;
-        }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        n_front[i] = keep;
-        pool_n[i] = np + keep;
-    }
+    tree_keep_children(i, P, B, d, nf * k, cand, sorted, parent_node, pool_n[i], front_tok, front_node, front_score,
+                       n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n);
 }
 
 // One CTA per request: rank the pool by (score desc, depth asc, creation asc),

@@ -117,23 +117,32 @@ def test_prepare_host_validation(lib):
 
 def test_tree_and_verify_host_validation(lib):
     f = lib.sdm_draft_tree
-    args = [FAKE, 0, FAKE, FAKE, FAKE, 32, 16, 1024, 64, 4, 8, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30,
-            None, None]
+    # L, dtL, U, W, prepared, anchor, R, B, V, r, k, P, N, outputs x 6, ws, ws_bytes, dev_status, stream
+    args = [FAKE, 0, FAKE, FAKE, None, FAKE, 32, 16, 1024, 64, 4, 8, 64, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+            1 << 30, None, None]
     bad_k = list(args)
-    bad_k[9] = 9                                # k > 8
+    bad_k[10] = 9                               # k > 8
     assert f(*bad_k) == 2
     bad_p = list(args)
-    bad_p[10] = 3                               # 128 % P != 0
+    bad_p[11] = 3                               # 128 % P != 0
     assert f(*bad_p) == 2
     bad_n = list(args)
-    bad_n[11] = 8 * 16 + 1                      # N > P * B
+    bad_n[12] = 8 * 16 + 1                      # N > P * B
     assert f(*bad_n) == 2
     big_pool = list(args)
-    big_pool[6], big_pool[10], big_pool[9] = 128, 64, 1   # P * B + 1 > 8192 (pool ranked in shared memory)
+    big_pool[7], big_pool[11], big_pool[10] = 128, 64, 1   # P * B + 1 > 8192 (pool ranked in shared memory)
     assert f(*big_pool) == 2
     big_v = list(args)
-    big_v[7] = 524288 + 8                       # V beyond the level select's chunk and candidate tables
+    big_v[8] = 524288 + 8                       # V beyond the level select's chunk and candidate tables
     assert f(*big_v) == 2
+    small_ws = list(args)
+    small_ws[20] = 1024                         # the workspace holds the scan lists or the records
+    assert f(*small_ws) == 5
+    bad_prep = list(args)
+    bad_prep[4] = ctypes.c_void_p(0x1008)       # prepared tables must be 16-byte aligned
+    assert f(*bad_prep) == 2
+    # the tree's workspace covers both level paths
+    assert lib.sdm_workspace_size(binding.OP_DRAFT_TREE, 32, 16, 151936, 256, 8, 4, 64) >= 32 * 16 * 10 * 512 * 8
     vt = lib.sdm_verify_tree
     assert vt(FAKE, 0, FAKE, FAKE, FAKE, 4, 16384, 7, 1024, FAKE, FAKE, FAKE, FAKE, 1 << 30, None, None) == 2
     v = lib.sdm_verify

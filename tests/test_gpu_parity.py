@@ -579,6 +579,76 @@ TREE_CASES = [dict(R=4, B=4, V=1000, r=64, k=4, P=8, N=16),
               dict(R=2, B=6, V=520, r=64, k=1, P=2, N=6)]         # k = 1: the chain
 
 
+def check_tree(out, ref, w, what):
+    """GPU tree against the oracle: identical trees (a differing one only at a
+    tie-zone decision, and none is expected), masks bit for bit, scores within
+    1e-5 relative."""
+    events = 0
+    for i in range(w.R):
+        first = tree_first_decision(ref, i, host(out["tok"])[i], host(out["parent"])[i], host(out["depth"])[i],
+                                    int(host(out["n_nodes"])[i]), w.B)
+        if first is not None:
+            assert first[1] < TIE, f"{what}: request {i} tree differs at {first[0]}, margin {first[1]}"
+            events += 1
+            continue
+        assert host(out["n_nodes"])[i] == ref["n_nodes"][i]
+        np.testing.assert_array_equal(host(out["mask"])[i].view(np.uint32), ref["mask"][i])
+        assert close(host(out["score"])[i], ref["score"][i]).all(), what
+    assert events == 0, f"{what}: {events} tie-zone events"
+
+
+@pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"R{c['R']}B{c['B']}k{c['k']}P{c['P']}N{c['N']}")
+def test_draft_tree_bound_pruned(case):
+    """The level by bound pruning (prepared tables): the scan's lists, the
+    GEMM's log-sum-exp partials and the per-request exact top-k give the
+    oracle's tree, and the same tree as the record path."""
+    w = small(R=case["R"], B=case["B"], V=case["V"], r=case["r"], l_dtype=BF16, sigma=(0.5,), l_std=2.0)
+    inp = synthetic.generate(w, seed=case["V"])
+    args = (np_of(inp["L"]), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    ref = oracle.draft_tree(*args, k=case["k"], P=case["P"], N=case["N"])
+    U, W = dev(inp["U"]), dev(inp["W"])
+    prep = sdm.markov_prepare(U, W)
+    out = sdm.draft_tree(dev(inp["L"]), U, W, dev(inp["anchor"]), case["k"], case["P"], case["N"], prepared=prep)
+    rec = sdm.draft_tree(dev(inp["L"]), U, W, dev(inp["anchor"]), case["k"], case["P"], case["N"])
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0
+    check_tree(out, ref, w, "pruned")
+    for k in ("tok", "parent", "depth", "n_nodes", "mask"):
+        assert torch.equal(out[k], rec[k]), k
+    assert close(host(out["score"]), host(rec["score"]), 2e-6).all()
+
+
+@pytest.mark.parametrize("kind", ["constant_rows", "few_large", "fp32_L"])
+def test_draft_tree_bound_pruned_adversarial(kind):
+    """Rows whose lists overflow (every logit equal: the chunk lists cannot
+    hold them) take the exhaustive top-k; rows with only a few large logits
+    test the k-th-largest ladder; fp32 L uses the 8192-id chunks.  Every
+    tree equals the oracle's."""
+    l_dtype = FP32 if kind == "fp32_L" else BF16
+    w = small(R=5, B=3, V=20000, r=64, l_dtype=l_dtype, sigma=(0.5,), l_std=2.0)
+    inp = synthetic.generate(w, seed=77)
+    L = inp["L"].clone()
+    if kind == "constant_rows":
+        L[1] = 0.5                                   # every logit of request 1 equal (ties by id)
+        L[3, 1] = -1.0                               # one level of request 3
+    elif kind == "few_large":
+        L[:] = -30.0
+        g = torch.Generator().manual_seed(3)
+        for i in range(w.R):
+            for d in range(w.B):
+                ids = torch.randperm(w.V, generator=g)[:3]   # fewer than k outstanding logits
+                L[i, d, ids] = torch.tensor([9.0, 8.5, 8.0]).to(L.dtype)
+    args = (np_of(L), np_of(inp["U"]), np_of(inp["W"]), np_of(inp["anchor"]))
+    k, P, N = 4, 4, 10
+    ref = oracle.draft_tree(*args, k=k, P=P, N=N)
+    U, W = dev(inp["U"]), dev(inp["W"])
+    prep = sdm.markov_prepare(U, W)
+    out = sdm.draft_tree(dev(L), U, W, dev(inp["anchor"]), k, P, N, prepared=prep)
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0
+    check_tree(out, ref, w, kind)
+
+
 @pytest.mark.parametrize("case", TREE_CASES, ids=lambda c: f"R{c['R']}B{c['B']}k{c['k']}P{c['P']}N{c['N']}")
 def test_draft_tree(case):
     w = small(R=case["R"], B=case["B"], V=case["V"], r=case["r"], l_dtype=BF16, sigma=(0.5,), l_std=2.0)

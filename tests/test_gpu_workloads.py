@@ -155,7 +155,13 @@ def test_mixed_traffic_modes():
 def test_pctree():
     w = WORKLOADS["pctree"]
     inp = synthetic.generate(w, seed=0, device="cuda")
-    tr = sdm.draft_tree(inp["L"], inp["U"], inp["W"], inp["anchor"], w.k, w.P, w.N)
+    prep = sdm.markov_prepare(inp["U"], inp["W"])
+    tr = sdm.draft_tree(inp["L"], inp["U"], inp["W"], inp["anchor"], w.k, w.P, w.N, prepared=prep)
+    rec = sdm.draft_tree(inp["L"], inp["U"], inp["W"], inp["anchor"], w.k, w.P, w.N)   # the record path
+    torch.cuda.synchronize()
+    for key in ("tok", "parent", "depth", "n_nodes", "mask"):   # the two level paths agree on every request
+        assert torch.equal(tr[key], rec[key]), key
+    assert close(host(tr["score"]), host(rec["score"]), 2e-6).all()
     tgt = synthetic.tree_target(inp, tr["tok"], tr["depth"], tr["n_nodes"], w.target_dtype)
     vt = sdm.verify_tree(tgt, tr["tok"], tr["parent"], tr["n_nodes"], w.B)
     torch.cuda.synchronize()
