@@ -552,7 +552,7 @@ def run_ours(args, w, world, rank, local):
     traffic = recorded_traffic(kname, w.name)
     draft_bytes = R * B * V * s_l
     extra = {}
-    if kname == dname and cyc.prepared is not None:
+    if kname == dname and cyc.prepared is not None and not cyc.tree:
         extra["achieved_l_only"] = draft_bytes / per_launch_s / 1e9
         extra["frac_l_only"] = extra["achieved_l_only"] / hbm_peak
     if kname == dname and cyc.tree:

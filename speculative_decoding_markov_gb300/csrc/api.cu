@@ -115,15 +115,19 @@ size_t ws_tree_common(int R, int B, int P) {
     return 3 * align256(rows * 4) + align256(R * 4) + 4 * align256(pool * 4) + align256(R * 4);
 }
 
-int tree_n_part(int R, int P, int V) {
+int tree_n_part(int R, int P, int V) {   // the most partials either sub-tile layout gives
     const int gy = (R * P + kTileM - 1) / kTileM;
-    return gemm_grid_x((V + kTileN - 1) / kTileN, gy) * kColGroups;
+    const int gy2 = (R * P + 2 * kTileM - 1) / (2 * kTileM);
+    return std::max(gemm_grid_x((V + kTileN - 1) / kTileN, gy), gemm_grid_x((V + kTileN - 1) / kTileN, gy2)) *
+           kColGroups;
 }
 
 size_t ws_tree(int R, int B, int P, int V) {
     const size_t rows = static_cast<size_t>(R) * P;
     const size_t records = align256(rows * n_blocks16(V) * 8) + align256(rows * kMaxTopK * 8) + align256(rows * 4);
-    const size_t pruned = ws_chain_pruned(R, B, V) + align256(rows * tree_n_part(R, P, V) * 8);
+    const size_t lrows = static_cast<size_t>(R) * B;
+    const size_t pruned = ws_chain_pruned(R, B, V) + align256(rows * tree_n_part(R, P, V) * 8) +
+                          align256(lrows * kTreeKeep * 8) + 3 * align256(lrows * 4);
     return ws_tree_common(R, B, P) + std::max(records, pruned);
 }
 
@@ -455,15 +459,19 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
     float* pool_score = c.take<float>(pool);
     int32_t* pool_n = c.take<int32_t>(R);
 
-    const int l_rows = std::min(kTileM / P, R);
+    // the bound-pruned level's GEMM takes two 128-row sub-tiles per CTA when
+    // there are more than 128 frontier rows (every W tile feeds 256 rows)
+    const int m_sub = (prepared && rows > static_cast<size_t>(kTileM)) ? 2 : 1;
+    const int l_rows = std::min(kTileM * m_sub / P, R);
     CUtensorMap tmW, tmL;
     if (!map_w(&tmW, W, r, V) || !map_l(&tmL, L, fp32, R, B, V, l_rows)) return SDM_ERR_CUDA;
     const int n_tiles = (V + kTileN - 1) / kTileN;
-    const int gy = static_cast<int>((rows + kTileM - 1) / kTileM);
+    const int gy = static_cast<int>((rows + kTileM * m_sub - 1) / (kTileM * m_sub));
     const int gx = gemm_grid_x(n_tiles, gy);
 
     GemmParams p;
     std::memset(&p, 0, sizeof p);
+    p.m_sub = m_sub;
     p.rows = static_cast<int>(rows);
     p.R = R;
     p.B = B;
@@ -513,21 +521,37 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
         pp.kth = k;
         const int n_part = gx * kColGroups;
         auto* part = c.take<float2>(rows * n_part);
+        TreeRowsParams rp;
+        std::memset(&rp, 0, sizeof rp);
+        rp.cand = pp.cand;
+        rp.cand_n = pp.cand_n;
+        rp.n_chunks = n_chunks;
+        rp.rows = R * B;
+        rp.V = V;
+        rp.k = k;
+        rp.c_max = c_max;
+        rp.keep = c.take<uint2>(static_cast<size_t>(R) * B * kTreeKeep);
+        rp.n_keep = c.take<int32_t>(static_cast<size_t>(R) * B);
+        rp.lk = c.take<float>(static_cast<size_t>(R) * B);
+        rp.cmax = pp.cmax;
+        rp.lmax = c.take<float>(static_cast<size_t>(R) * B);
         SDM_CHECK_CUDA(launch_chain_scan(pp, s));
+        SDM_CHECK_CUDA(launch_tree_rows(rp, s));
         p.part = part;
         p.n_part = n_part;
+        p.row_lmax = rp.lmax;
+        p.c_bound = c_bound;
         gemm_pick_stages(p, MODE_TREE_LSE);
         TreeLevelParams tl;
         std::memset(&tl, 0, sizeof tl);
-        tl.cand = pp.cand;
-        tl.cand_n = pp.cand_n;
-        tl.n_chunks = n_chunks;
+        tl.keep = rp.keep;
+        tl.n_keep = rp.n_keep;
+        tl.lk = rp.lk;
         tl.L = L;
         tl.l_fp32 = fp32;
         tl.U = U;
         tl.Wt = Wt;
         tl.c_bound = c_bound;
-        tl.c_max = c_max;
         tl.R = R;
         tl.B = B;
         tl.V = V;

@@ -34,6 +34,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+static_assert(kMaxTopK <= kWarps, "the scan's k-th threshold ranks the warps' maxima");
 constexpr int kListHead = 32;   // list entries the pick kernel loads with the list length
 
 template <int FP32>
@@ -110,7 +111,6 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
     constexpr int VPT = kChunkBytes / 16 / kThreads;        // vectors per thread
     constexpr int CHUNK_IDS = kChunkBytes / ESZ;
     __shared__ float s_wmax[kWarps];
-    __shared__ uint32_t s_ladder[kWarps][2];
     __shared__ int s_cnt[2];   // by item parity: a slot is reset two items after its last read
     pdl_wait();
     pdl_trigger();
@@ -154,38 +154,24 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
 #pragma unroll
         for (int w = 1; w < kWarps; ++w) mc = fmaxf(mc, s_wmax[w]);
         // the value the list is cut below: the chunk maximum for the argmax;
-        // for a top-k a lower bound theta on the chunk's k-th largest value,
-        // the first step of the ladder mc - {1/2, 1, 2, 4} reached by at least
-        // k vectors' maxima (each such vector holds a value >= theta, so at
-        // least k values are), -inf when none is
+        // for a top-k the k-th largest of the warps' maxima (k <= kWarps: the
+        // k warps with the largest maxima hold k distinct values at or above
+        // it, so it is a lower bound on the chunk's k-th largest value; -inf
+        // when fewer than k warps hold a value)
         float theta = mc;
         if (p.kth > 1) {
-            uint32_t ca = 0u, cb = 0u;   // two 16-bit counters each
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const float vm = vec_max<FP32>(x[k]);
-                ca += (vm >= mc - 0.5f ? 1u : 0u) + (vm >= mc - 1.0f ? 0x10000u : 0u);
-                cb += (vm >= mc - 2.0f ? 1u : 0u) + (vm >= mc - 4.0f ? 0x10000u : 0u);
-            }
-            ca = __reduce_add_sync(0xffffffffu, ca);
-            cb = __reduce_add_sync(0xffffffffu, cb);
-            if (lane == 0) {
-                s_ladder[warp][0] = ca;
-                s_ladder[warp][1] = cb;
-            }
-            __syncthreads();
-            uint32_t ta = 0u, tb = 0u;
+            theta = -INFINITY;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) {
-                ta += s_ladder[w][0];
-                tb += s_ladder[w][1];
+                const float x0 = s_wmax[w];
+                int gt = 0, ge = 0;
+#pragma unroll
+                for (int u = 0; u < kWarps; ++u) {
+                    gt += s_wmax[u] > x0 ? 1 : 0;
+                    ge += s_wmax[u] >= x0 ? 1 : 0;
+                }
+                if (gt < p.kth && ge >= p.kth) theta = x0;
             }
-            const uint32_t k = static_cast<uint32_t>(p.kth);
-            theta = (ta & 0xffffu) >= k ? mc - 0.5f
-                    : (ta >> 16) >= k   ? mc - 1.0f
-                    : (tb & 0xffffu) >= k ? mc - 2.0f
-                    : (tb >> 16) >= k   ? mc - 4.0f
-                                        : -INFINITY;
         }
         const float T = threshold(theta, cmax);
         const int seg = rs * nc + c;

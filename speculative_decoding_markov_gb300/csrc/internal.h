@@ -119,6 +119,13 @@ struct GemmParams {
     // withheld loads (the producers arm nothing, so every wait runs out)
     unsigned long long wait_ns;
     int withhold_loads;
+    // 128-row sub-tiles per CTA: 1, or 2 for PCTree levels (MODE_TREE_LSE)
+    // of more than 128 frontier rows (every W tile then feeds 256 rows)
+    int m_sub;
+    // MODE_TREE_LSE with prepared tables: the bound max_v L_v + c(y) >= z
+    // serves as the exponent reference (row_lmax [R * B], c_bound [V]), or NULL
+    const float* row_lmax;
+    const float* c_bound;
 };
 
 // Ring depths for the launch shape (written into p.w_stages / p.l_stages).
@@ -264,21 +271,36 @@ struct TreeSelectParams {
 };
 cudaError_t launch_tree_select(const TreeSelectParams& p, cudaStream_t s);
 
-// PCTree level by bound pruning (tree_pruned.cu): per request, the top-k
-// children of every frontier parent from the scan's lists and the prepared
-// tables, their scores from the MODE_TREE_LSE partials, the per-level prune.
+// PCTree level by bound pruning (tree_pruned.cu): once per cycle, per
+// (request, level) row, the ids any parent can need (from the scan's lists
+// and the prepared tables); per level and request, the top-k children of
+// every frontier parent, their scores from the MODE_TREE_LSE partials, the
+// per-level prune.
 constexpr int kMaxTreeSlots = 64;   // frontier slots P (P k <= 64, k >= 1)
+constexpr int kTreeKeep = 192;      // ids kept per row (more: the exhaustive path)
+
+struct TreeRowsParams {
+    const uint2* cand;          // the scan's lists [rows][n_chunks][kSegCap]
+    const int32_t* cand_n;      // [rows][n_chunks]
+    int n_chunks, rows, V, k;
+    const float* c_max;         // [1] (prepared)
+    uint2* keep;                // [rows][kTreeKeep] (id, L bits), (L desc, id asc)
+    int32_t* n_keep;            // [rows]; -1: the row takes the exhaustive path
+    float* lk;                  // [rows] the row's k-th largest backbone logit
+    const float* cmax;          // the scan's chunk maxima [rows][n_chunks]
+    float* lmax;                // [rows] the row's largest backbone logit
+};
+cudaError_t launch_tree_rows(const TreeRowsParams& p, cudaStream_t s);
 
 struct TreeLevelParams {
-    const uint2* cand;          // the scan's lists [R * B][n_chunks][kSegCap]
-    const int32_t* cand_n;      // [R * B][n_chunks]
-    int n_chunks;
+    const uint2* keep;          // tree_rows_kernel's outputs
+    const int32_t* n_keep;
+    const float* lk;
     const void* L;              // [R, B, V]
     int l_fp32;
     const uint16_t* U;          // [V, r]
     const uint16_t* Wt;         // [V, r] (prepared)
     const float* c_bound;       // [V] (prepared)
-    const float* c_max;         // [1] (prepared)
     int R, B, V, r, P, k, d;
     const float2* part;         // [R * P][n_part] (max, sum) partials of MODE_TREE_LSE
     int n_part;
@@ -293,7 +315,7 @@ struct TreeLevelParams {
     int32_t* pool_n;
     int32_t* dev_status;
 };
-size_t tree_level_smem(int P, int k, int r);
+size_t tree_level_smem(int P, int r);
 cudaError_t launch_tree_level(const TreeLevelParams& p, cudaStream_t s);
 
 // PCTree

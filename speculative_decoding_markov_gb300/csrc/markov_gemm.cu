@@ -65,21 +65,23 @@ constexpr int kTmemCols = 512;
 // into the last r / 64 W stages and copied to tensor memory before those
 // stages are first loaded.
 struct SmemLayout {
-    uint32_t a_off, l_off, l_box_bytes, l_stage_bytes, bar_off, total;
+    uint32_t a_off, l_off, l_box_bytes, l_stage_bytes, bar_off, tok_off, total;
 };
 
 __host__ __device__ inline SmemLayout make_layout(int r, int l_rows, int l_fp32, int w_stages, int l_stages,
-                                                  int mode) {
+                                                  int mode, int ms = 1) {
     SmemLayout s;
     const uint32_t w_bytes = static_cast<uint32_t>(w_stages) * kWStageBytes;
-    // A fills the last tile slot (KB = r / 64 stages of 16 KB = 128 x r x 2 bytes)
+    // A fills the last ms tile slots (a slot is KB = r / 64 stages of 16 KB =
+    // 128 x r x 2 bytes: one 128-row sub-tile of A)
     const int kb = r >> 6;
-    s.a_off = static_cast<uint32_t>((w_stages / kb - 1) * kb) * kWStageBytes;
+    s.a_off = static_cast<uint32_t>((w_stages / kb - ms) * kb) * kWStageBytes;
     s.l_off = w_bytes;
     s.l_box_bytes = (static_cast<uint32_t>(l_rows) * 128u + 1023u) & ~1023u;
     s.l_stage_bytes = mode_reads_l(mode) ? s.l_box_bytes * (l_fp32 ? 2u : 1u) : 0u;
     s.bar_off = s.l_off + static_cast<uint32_t>(l_stages) * s.l_stage_bytes;
-    s.total = s.bar_off + static_cast<uint32_t>(2 * w_stages + 2 * l_stages + 6) * 8u + 16u + 1024u;
+    s.tok_off = s.bar_off + static_cast<uint32_t>(2 * w_stages + 2 * l_stages + 6) * 8u + 16u;   // the rows' tokens
+    s.total = s.tok_off + static_cast<uint32_t>(kTileM * ms) * 4u + 1024u;
     return s;
 }
 
@@ -392,19 +394,32 @@ __device__ __forceinline__ float2* part_slot(const GemmParams& p, int grow, int 
     return p.part + static_cast<size_t>(grow) * p.n_part + blockIdx.x * kColGroups + group;
 }
 
-// Online (max, sum) of the logits z of a frontier row over every column this
-// thread consumes: the partial (m, s) = (max z, sum exp(z - m)), each
-// exponential one fma and one ex2 (2^(z log2(e) - m log2(e))).  A thread that
-// consumed nothing leaves (-inf, 0).
+// (max, sum) of the logits z of a frontier row over every column this thread
+// consumes, each exponential one fma and one ex2 (2^(z log2(e) - m log2(e))).
+// The reference m is, where the prepared tables give it, the row's bound
+// m = max_v L_v + c(y) >= every z (no maximum is tracked: the largest term is
+// at least exp(-2 c(y)) and none exceeds 1; used while c(y) <= 16), else the
+// running maximum.  A thread that consumed nothing leaves (-inf, 0).
 template <>
 struct Epi<MODE_TREE_LSE> {
-    bool valid;
+    bool valid, bounded;
     int group;
-    float m, s;
+    float m, s, mo;
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
-        valid = grow < p.rows && p.front_tok[grow] >= 0;
+        const int t = grow < p.rows ? p.front_tok[grow] : -1;
+        valid = t >= 0 && t < p.V;
         m = -INFINITY;
         s = 0.f;
+        bounded = false;
+        if (valid && p.row_lmax && p.c_bound) {
+            const float cy = p.c_bound[t];
+            const float lmax = p.row_lmax[(grow / p.P) * p.B + (p.d - 1)];
+            if (cy <= 16.f && lmax > -INFINITY && lmax < INFINITY) {
+                bounded = true;
+                m = lmax + cy;
+            }
+        }
+        mo = m * kLog2e;
     }
     __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
                                             int g, const uint32_t (&acc)[C]) {
@@ -414,19 +429,21 @@ struct Epi<MODE_TREE_LSE> {
 #pragma unroll
         for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
         mask_tail(z, vbase, p.V);
-        const float mb = maxc(z);   // finite: column vbase < V
-        if (mb > m) {
-            s *= fast_exp2((m - mb) * kLog2e);   // 0 while m = -inf
-            m = mb;
+        if (!bounded) {
+            const float mb = maxc(z);   // finite: column vbase < V
+            if (mb > m) {
+                s *= fast_exp2((m - mb) * kLog2e);   // 0 while m = -inf
+                m = mb;
+                mo = m * kLog2e;
+            }
         }
-        const float mo = m * kLog2e;
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(fmaf(z[j], kLog2e, -mo));   // 2^-inf = 0 on the tail
         s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     }
     __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
-        if (valid) *part_slot(p, grow, group) = make_float2(m, s);
+        if (valid) *part_slot(p, grow, group) = make_float2(s > 0.f ? m : -INFINITY, s);
     }
 };
 
@@ -626,14 +643,46 @@ struct Epi<MODE_ABSMAX> {
     }
 };
 
-template <int MODE>
+// W tile i (vocab ids from (blockIdx.x + i gridDim.x) 128) into tile slot
+// `slot`: KB stages of [64 K rows x 128 ids], two 64-id boxes each.
+__device__ __forceinline__ void issue_w_tile(const CUtensorMap& tmW, uint8_t* smem, uint64_t* wfull, int i, int slot,
+                                             int KB, uint64_t pol) {
+    const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+    for (int kb = 0; kb < KB; ++kb) {
+        const int s = slot * KB + kb;
+        uint8_t* st = smem + static_cast<uint32_t>(s) * kWStageBytes;
+        mbar_arrive_expect_tx(&wfull[s], kWStageBytes);
+        tma_load_2d(st, &tmW, &wfull[s], v0, kb * 64, pol);
+        tma_load_2d(st + kWBoxBytes, &tmW, &wfull[s], v0 + kBoxN, kb * 64, pol);
+    }
+}
+
+// L box bi (tile bi / 2, 64-id half bi % 2) of the CTA's L rows into stage t.
+__device__ __forceinline__ void issue_l_box(const CUtensorMap& tmL, uint8_t* smem, const SmemLayout& lay,
+                                            uint64_t* lfull, const GemmParams& p, int bi, int t, int mode, int ms,
+                                            uint64_t pol) {
+    const int lrow0 = mode_tree(mode) ? static_cast<int>(blockIdx.y) * (kTileM * ms / p.P)
+                                      : static_cast<int>(blockIdx.y) * kTileM * ms;
+    const int vb = (static_cast<int>(blockIdx.x) + (bi >> 1) * static_cast<int>(gridDim.x)) * kTileN + (bi & 1) * kBoxN;
+    uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(t) * lay.l_stage_bytes;
+    mbar_arrive_expect_tx(&lfull[t], static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u));
+    tma_load_3d(sl, &tmL, &lfull[t], vb, p.d - 1, lrow0, pol);
+    if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &lfull[t], vb + 32, p.d - 1, lrow0, pol);
+}
+
+// MS = 128-row sub-tiles of GEMM rows per CTA.  MS = 2 (PCTree levels of
+// more than 128 frontier rows): both sub-tiles' A rows sit in tensor memory
+// and every W tile feeds both, one accumulator per sub-tile, the epilogue of
+// one sub-tile overlapping the MMAs of the other; the W stream per row halves.
+template <int MODE, int MS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     markov_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmL,
                        const GemmParams p) {
+    static_assert(MS == 1 || (MS == 2 && mode_tree(MODE) && !mode_loads_first(MODE)), "two sub-tiles: PCTree modes");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int SW = p.w_stages, SL = p.l_stages;
-    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, SW, SL, MODE);
+    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, SW, SL, MODE, MS);
     uint8_t* sA = smem + lay.a_off;
     uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + lay.bar_off);
     uint64_t* wdone = wfull + SW;   // per tile slot: the slot's last tile has completed
@@ -644,11 +693,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* a_done = tempty + 2;
     uint64_t* drain = a_done + 1;   // the MMA warp's own tensor-core work, before tensor memory is freed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    int* s_rowtok = reinterpret_cast<int*>(smem + lay.tok_off);   // [kTileM * MS]
     const uint64_t lim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int row0 = blockIdx.y * kTileM;
+    const int row0 = blockIdx.y * kTileM * MS;
     const int KB = p.r >> 6;   // K blocks of 64 per tile
     const int NTS = SW / KB;   // W tile slots: tile i takes stages (i % NTS) * KB .. + KB - 1
     // vocab tiles are dealt round-robin (tile = blockIdx.x + i * gridDim.x) so
@@ -678,18 +728,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_prefetch_desc(&tmW);
         if (mode_reads_l(MODE)) tma_prefetch_desc(&tmL);
     }
+    __syncthreads();   // the barriers are initialised for every warp
+
+    // 0. loads that read nothing a previous kernel writes (W, and L, are
+    //    inputs), issued before the wait on the previous kernel: the first W
+    //    tiles (the slots that do not hold A) and the first L boxes
+    const int w_pre = nt < NTS - MS ? nt : NTS - MS;
+    const int l_pre = mode_reads_l(MODE) ? (2 * nt < SL ? 2 * nt : SL) : 0;
+    if (warp == 0 && lane == 0 && !p.withhold_loads) {
+        const uint64_t pol_w = policy_evict_last();
+        for (int i = 0; i < w_pre; ++i) issue_w_tile(tmW, smem, wfull, i, i % NTS, KB, pol_w);
+    }
+    if (warp == 2 && lane == 0 && !p.withhold_loads) {
+        const uint64_t pol_l = policy_evict_first();
+        for (int bi = 0; bi < l_pre; ++bi) issue_l_box(tmL, smem, lay, lfull, p, bi, bi % SL, MODE, MS, pol_l);
+    }
     pdl_wait();   // tokens (and every buffer this launch writes) belong to the previous kernel until here
     pdl_trigger();
 
-    // 1. gather A = U[tok(m)] for the 128 rows (K-major, 128-byte swizzle:
-    //    16-byte chunk c of row m in K block kb sits at chunk c ^ (m & 7)).
+    // 1. the rows' tokens, every load in flight at once, then A = U[tok(m)]
+    //    for the 128 MS rows (K-major, 128-byte swizzle: 16-byte chunk c of
+    //    row m in K block kb sits at chunk c ^ (m & 7)); sub-tile h occupies
+    //    its own slot (128 x r x 2 bytes).
+    for (int rr = threadIdx.x; rr < kTileM * MS; rr += kGemmThreads) s_rowtok[rr] = gemm_row_token<MODE>(p, row0 + rr);
+    __syncthreads();
     const int kchunks = p.r >> 3;
-    for (int rr = warp; rr < kTileM; rr += kGemmThreads / 32) {
-        const int tok = gemm_row_token<MODE>(p, row0 + rr);
+    for (int rr = warp; rr < kTileM * MS; rr += kGemmThreads / 32) {
+        const int tok = s_rowtok[rr];
         const uint16_t* src = (p.a_rows && tok >= 0) ? p.a_rows + static_cast<size_t>(row0 + rr) * p.r
                                                      : p.U + static_cast<size_t>(tok < 0 ? 0 : tok) * p.r;
+        const int rm = rr & (kTileM - 1);
+        uint8_t* sub = sA + (rr / kTileM) * (kTileM * p.r * 2);
         for (int q = lane; q < kchunks; q += 32) {
-            uint8_t* dst = sA + (q >> 3) * (kTileM * 128) + rr * 128 + (((q & 7) ^ (rr & 7)) << 4);
+            uint8_t* dst = sub + (q >> 3) * (kTileM * 128) + rm * 128 + (((q & 7) ^ (rm & 7)) << 4);
             cp_async_16(dst, src + q * 8, tok < 0 ? 0u : 16u);
         }
     }
@@ -715,20 +786,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (lane == 0 && nt > 0 && !p.withhold_loads) {
             const uint64_t pol_w = policy_evict_last();
             bool ok = true;
-            int issued = 0;   // tiles whose W loads were issued
-            for (int i = 0; i < nt && ok; ++i) {
+            int issued = w_pre;   // tiles whose W loads were issued (the first before the wait)
+            for (int i = w_pre; i < nt && ok; ++i) {
                 const int slot = i % NTS;
                 if (i >= NTS) ok = mbar_wait(&wdone[slot], ((i / NTS) - 1) & 1, lim);
-                else if (slot == NTS - 1) ok = mbar_wait(a_done, 0, lim);
+                else if (slot >= NTS - MS) ok = mbar_wait(a_done, 0, lim);
                 if (!ok) break;
-                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int s = slot * KB + kb;
-                    uint8_t* st = smem + static_cast<uint32_t>(s) * kWStageBytes;
-                    mbar_arrive_expect_tx(&wfull[s], kWStageBytes);
-                    tma_load_2d(st, &tmW, &wfull[s], v0, kb * 64, pol_w);
-                    tma_load_2d(st + kWBoxBytes, &tmW, &wfull[s], v0 + kBoxN, kb * 64, pol_w);
-                }
+                issue_w_tile(tmW, smem, wfull, i, slot, KB, pol_w);
                 issued = i + 1;
             }
             if (!ok) fail_timeout(p);
@@ -754,35 +818,45 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // A steps 32 bytes within a 128-byte swizzle row and 128 x 128
         // bytes per K block of 64; B steps 16 rows of 128 bytes, and its
         // second 64-id box (the MN-atom stride) is kWBoxBytes further.
-        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), 16, 1024);
         const int ksteps = p.r >> 4;
-        const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA);
-        for (int ks = 0; ks < ksteps; ++ks)
-            tmem_cp_128x256b_warp(a_tmem + static_cast<uint32_t>(ks * 8),
-                                  a_desc0 + static_cast<uint64_t>((ks >> 2) * ((kTileM * 128) >> 4) + (ks & 3) * 2));
+        for (int h = 0; h < MS; ++h) {   // sub-tile h's A at columns kTmemA + h r / 2
+            const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA + h * (kTileM * p.r * 2)), 16, 1024);
+            const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA + h * (p.r >> 1));
+            for (int ks = 0; ks < ksteps; ++ks)
+                tmem_cp_128x256b_warp(a_tmem + static_cast<uint32_t>(ks * 8),
+                                      a_desc0 + static_cast<uint64_t>((ks >> 2) * ((kTileM * 128) >> 4) + (ks & 3) * 2));
+        }
         mma_commit_warp(a_done);   // the A stages may be loaded once the copy has read them
         const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem), kWBoxBytes, 1024);
         bool ok = true;
         for (int i = 0; i < nt && ok; ++i) {
-            const int b = i & 1;
-            if (i >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[b], ((i >> 1) - 1) & 1, lim));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
             const int slot = i % NTS;
             const uint32_t par = static_cast<uint32_t>(i / NTS) & 1u;
-            for (int kb = 0; kb < KB; ++kb) {
-                const int s = slot * KB + kb;
-                ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par, lim));
+            for (int h = 0; h < MS && ok; ++h) {
+                // accumulator b (one of two in turn, or sub-tile h's own) and
+                // its use count
+                const int b = MS == 1 ? (i & 1) : h;
+                const int use = MS == 1 ? (i >> 1) : i;
+                if (use >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[b], (use - 1) & 1, lim));
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
+                const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA + h * (p.r >> 1));
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int s = slot * KB + kb;
+                    if (h == 0) {   // the later sub-tiles reuse the stages the first waited for
+                        ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par, lim));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    mma_bf16_ts_warp(d_tmem, a_tmem + static_cast<uint32_t>((kb * 4 + j) * 8),
-                                     bd0 + static_cast<uint64_t>(j * (2048 >> 4)), idesc, (kb | j) ? 1u : 0u);
+                    for (int j = 0; j < 4; ++j)
+                        mma_bf16_ts_warp(d_tmem, a_tmem + static_cast<uint32_t>((kb * 4 + j) * 8),
+                                         bd0 + static_cast<uint64_t>(j * (2048 >> 4)), idesc, (kb | j) ? 1u : 0u);
+                }
+                if (ok) mma_commit_warp(&tfull[b]);
             }
-            if (ok) mma_commit_warp(&tfull[b]);
         }
         if (!ok && lane == 0) fail_timeout(p);
         // every tensor-core operation this warp issued (the A copy, the
@@ -795,23 +869,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         // 2b. L producer: the tile's two 64-id boxes of L rows, one stage each
         if (mode_reads_l(MODE) && lane == 0 && nt > 0 && !p.withhold_loads) {
             const uint64_t pol_l = policy_evict_first();
-            const int lrow0 = mode_tree(MODE) ? static_cast<int>(blockIdx.y) * (kTileM / p.P) : row0;
             bool ok = true;
-            int t = 0, lap = 0, issued = 0;   // boxes issued
-            for (int i = 0; i < nt && ok; ++i) {
-                const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
-                for (int h = 0; h < 2; ++h, t = (t + 1 == SL) ? (++lap, 0) : t + 1) {
-                    if (lap > 0 && !mbar_wait(&lempty[t], (lap - 1) & 1, lim)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(t) * lay.l_stage_bytes;
-                    mbar_arrive_expect_tx(&lfull[t], static_cast<uint32_t>(p.l_rows) * 128u * (p.l_fp32 ? 2u : 1u));
-                    const int vb = v0 + h * kBoxN;
-                    tma_load_3d(sl, &tmL, &lfull[t], vb, p.d - 1, lrow0, pol_l);
-                    if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &lfull[t], vb + 32, p.d - 1, lrow0, pol_l);
-                    ++issued;
+            int issued = l_pre;   // boxes issued (the first before the wait)
+            for (int bi = l_pre; bi < 2 * nt; ++bi) {   // box bi = (tile bi / 2, half bi % 2) in stage bi % SL
+                const int t = bi % SL, lap = bi / SL;
+                if (lap > 0 && !mbar_wait(&lempty[t], (lap - 1) & 1, lim)) {
+                    ok = false;
+                    break;
                 }
+                issue_l_box(tmL, smem, lay, lfull, p, bi, t, MODE, MS, pol_l);
+                ++issued;
             }
             if (!ok) fail_timeout(p);
             // every box issued has landed before the CTA may exit: stage t
@@ -827,9 +894,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const int g = (warp - 3) >> 2;
         const int lrow = q * 32 + lane;
         const int grow = row0 + lrow;
-        Epi<MODE> st;
-        st.init(p, grow);
-        st.group = g;
+        Epi<MODE> sts[MS];   // one row of each sub-tile
+#pragma unroll
+        for (int h = 0; h < MS; ++h) {
+            sts[h].init(p, grow + h * kTileM);
+            sts[h].group = g;
+        }
+        Epi<MODE>& st = sts[0];
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         int t = 0, lap = 0;   // L ring slot and wraps
         for (int i = 0; i < nt; ++i) {
@@ -860,41 +931,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 st.consume_slice(p, vb[1], 1, acc);
                 continue;
             } else {
-            bool ok = mbar_wait(&tfull[b], (i >> 1) & 1, lim);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) {
-                if (lane == 0) fail_timeout(p);
-                break;
-            }
-            if (warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);   // the tile's W stages are free
-            tc_fence_after();
-            // both 16-column slices of the tile into registers, then the
-            // accumulator goes back to the MMA warp before any arithmetic
-            uint32_t acc[2][C];
-            tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + g * C), acc[0]);
-            tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + kBoxN + g * C), acc[1]);
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty[b]);
+            // the tile's two L stages (one per 64-id box), shared by the sub-tiles
+            const int t0 = t, lap0 = lap;
+            const int t1 = (t0 + 1 == SL) ? 0 : t0 + 1, lap1 = (t0 + 1 == SL) ? lap0 + 1 : lap0;
+            const int ts[2] = {t0, t1}, laps[2] = {lap0, lap1};
             const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
+            bool ok = true;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                if (mode_reads_l(MODE)) {
-                    bool lok = mbar_wait(&lfull[t], lap & 1, lim);
-                    lok = __all_sync(0xffffffffu, lok);
-                    if (!lok) {
-                        ok = false;
-                        break;
+            for (int h = 0; h < MS; ++h) {
+                const int ab = MS == 1 ? b : h;                 // accumulator
+                const int use = MS == 1 ? (i >> 1) : i;          // its use count
+                ok = mbar_wait(&tfull[ab], use & 1, lim);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                // the tile's W stages are free once its last sub-tile's MMAs are done
+                if (h == MS - 1 && warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);
+                tc_fence_after();
+                // both 16-column slices of the tile into registers, then the
+                // accumulator goes back to the MMA warp before any arithmetic
+                uint32_t acc[2][C];
+                tmem_ld16(lane_addr + static_cast<uint32_t>(ab * kTileN + g * C), acc[0]);
+                tmem_ld16(lane_addr + static_cast<uint32_t>(ab * kTileN + kBoxN + g * C), acc[1]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&tempty[ab]);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (mode_reads_l(MODE) && h == 0) {
+                        bool lok = mbar_wait(&lfull[ts[hh]], laps[hh] & 1, lim);
+                        lok = __all_sync(0xffffffffu, lok);
+                        if (!lok) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    const uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(ts[hh]) * lay.l_stage_bytes;
+                    sts[h].consume(p, sl, lay.l_box_bytes, lrow + h * kTileM, v0 + hh * kBoxN + g * C, g, acc[hh]);
+                    if (mode_reads_l(MODE) && h == MS - 1) {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&lempty[ts[hh]]);
                     }
                 }
-                const uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(t) * lay.l_stage_bytes;
-                st.consume(p, sl, lay.l_box_bytes, lrow, v0 + h * kBoxN + g * C, g, acc[h]);
-                if (mode_reads_l(MODE)) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&lempty[t]);
-                    t = (t + 1 == SL) ? (++lap, 0) : t + 1;
-                }
+                if (!ok) break;
+            }
+            if (mode_reads_l(MODE)) {
+                t = (t1 + 1 == SL) ? 0 : t1 + 1;
+                lap = (t1 + 1 == SL) ? lap1 + 1 : lap1;
             }
             if (!ok) {
                 if (lane == 0) fail_timeout(p);
@@ -902,7 +985,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             }
         }
-        st.flush(p, grow);
+#pragma unroll
+        for (int h = 0; h < MS; ++h) sts[h].flush(p, grow + h * kTileM);
     }
 
     tc_fence_before();
@@ -913,19 +997,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int MODE>
+template <int MODE, int MS = 1>
 cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p, int gx, int gy,
                         cudaStream_t s) {
-    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.w_stages, p.l_stages, MODE);
+    const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.w_stages, p.l_stages, MODE, MS);
+    // every sub-tile's A needs a W slot of its own, and the ring at least two
     if (lay.total > static_cast<uint32_t>(kSmemLimit) || p.w_stages < 2 * (p.r >> 6)) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemLimit);
+        cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE, MS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl(markov_gemm_kernel<MODE>, dim3(gx, gy), dim3(kGemmThreads), lay.total, s, tmW, tmL, p);
+    return launch_pdl(markov_gemm_kernel<MODE, MS>, dim3(gx, gy), dim3(kGemmThreads), lay.total, s, tmW, tmL, p);
 }
 
 }  // namespace
@@ -935,8 +1020,9 @@ void gemm_pick_stages(GemmParams& p, int mode) {
     // L boxes as fit up to kMaxLStages (three tiles ahead: L comes from HBM
     // in scattered rows); then more W slots with what is left.
     const int kb = p.r >> 6;
+    const int ms = p.m_sub > 1 ? p.m_sub : 1;
     const auto fits = [&](int ws, int ls) {
-        return make_layout(p.r, p.l_rows, p.l_fp32, ws, ls, mode).total <= static_cast<uint32_t>(kSmemLimit);
+        return make_layout(p.r, p.l_rows, p.l_fp32, ws, ls, mode, ms).total <= static_cast<uint32_t>(kSmemLimit);
     };
     int ws = 2 * kb, ls = 0;
     if (mode_reads_l(mode))
@@ -959,7 +1045,9 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
         case MODE_TVMIN: return launch_mode<MODE_TVMIN>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TVMIN_B16: return launch_mode<MODE_TVMIN_B16>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TVMIN_B32: return launch_mode<MODE_TVMIN_B32>(tmW, tmL, p, grid_x, grid_y, s);
-        case MODE_TREE_LSE: return launch_mode<MODE_TREE_LSE>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TREE_LSE:
+            return p.m_sub == 2 ? launch_mode<MODE_TREE_LSE, 2>(tmW, tmL, p, grid_x, grid_y, s)
+                                : launch_mode<MODE_TREE_LSE, 1>(tmW, tmL, p, grid_x, grid_y, s);
         default: return cudaErrorInvalidValue;
     }
 }

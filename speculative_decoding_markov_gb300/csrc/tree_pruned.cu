@@ -14,17 +14,16 @@
 //     with L >= theta - 2 c_max, theta a lower bound on the chunk's k-th
 //     largest value, so the lists hold every chunk's top k (hence the row's top
 //     k and L_(k)) and every id any parent can need.
-// tree_level_kernel, one CTA per request:
-//   1. (before the GEMM has finished) gathers the row's lists, finds L_(k),
-//      keeps the ids with L >= L_(k) - 2 c_max and copies their W^T rows into
-//      shared memory;
-//   2. (after) the parents' U rows and log-sum-exps, then z for every (parent,
-//      kept id) with L >= L_(k) - 2 c(y), exactly (fp32 products summed in
-//      fp32: exact on the grid tables), the top k of each parent, the children's
-//      scores and the per-level prune.
-// A row whose lists overflowed, or whose kept ids do not fit, takes every
-// parent's top k over the whole vocabulary from global memory instead
-// (exhaustive; slow, but exact).
+// tree_rows_kernel (once per cycle, one CTA per (request, level) row): the
+//   row's lists, L_(k), and the ids with L >= L_(k) - 2 c_max in (L desc, id
+//   asc) order; a row whose lists overflowed or whose ids do not fit is
+//   marked for the exhaustive path.
+// tree_level_kernel (per level, one CTA per request): the parents' U rows and
+//   log-sum-exps, the row's ids' W^T rows, z for every (parent, id) with
+//   L >= L_(k) - 2 c(y), exactly (fp32 products summed in fp32: exact on the
+//   grid tables), each parent's top k, the children's scores and the
+//   per-level prune.  A marked row takes every parent's top k over the whole
+//   vocabulary from global memory instead (slow, but exact).
 #include "device.cuh"
 #include "internal.h"
 #include "tree_common.cuh"
@@ -34,33 +33,8 @@ namespace {
 
 constexpr int kLvThreads = 256;
 constexpr int kLvWarps = kLvThreads / 32;
-constexpr int kGather = 2048;    // listed entries of a row held in shared memory
-constexpr int kStageCap = 192;   // kept ids (W^T rows staged)
-
-struct LevelLayout {
-    uint32_t w, u, g, z, cand, sorted, total;
-    int rs;   // staged row stride (elements): r + 8 (16 bytes apart in the banks)
-};
-
-// Dynamic shared memory: staged W^T rows [kStageCap][rs] bf16, parents' U
-// rows [P][rs] bf16, then the gathered list entries [kGather] (id, L bits),
-// which the logits [P][kStageCap] fp32 reuse once the ids are staged, then the
-// children [P k] and their rank order.
-__host__ __device__ inline LevelLayout level_layout(int P, int k, int r) {
-    LevelLayout l;
-    l.rs = r + 8;
-    const uint32_t row = 2u * static_cast<uint32_t>(l.rs);
-    l.w = 0;
-    l.u = l.w + static_cast<uint32_t>(kStageCap) * row;
-    l.g = l.u + static_cast<uint32_t>(P) * row;
-    const uint32_t gz = static_cast<uint32_t>(kGather) * 8u;
-    const uint32_t zz = static_cast<uint32_t>(P) * kStageCap * 4u;
-    l.z = l.g;
-    l.cand = l.g + ((gz > zz ? gz : zz) + 15u) / 16u * 16u;
-    l.sorted = l.cand + static_cast<uint32_t>(P * k) * 16u;
-    l.total = l.sorted + static_cast<uint32_t>(P * k) * 16u;
-    return l;
-}
+constexpr int kGather = 2048;   // listed entries of a row held in shared memory
+constexpr int kMaxPartLane = 24;   // GEMM partials per lane a warp loads at once (n_part <= 768)
 
 // Segment holding entry t of the row's concatenated lists.
 __device__ __forceinline__ int list_of(const int* pref, int nc, int t) {
@@ -109,39 +83,28 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
     return m;
 }
 
-__global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLevelParams p) {
-    extern __shared__ __align__(16) uint8_t s_dyn[];
-    const LevelLayout lay = level_layout(p.P, p.k, p.r);
-    const int RS = lay.rs;
-    uint16_t* s_w = reinterpret_cast<uint16_t*>(s_dyn + lay.w);     // [kStageCap][RS]
-    uint16_t* s_u = reinterpret_cast<uint16_t*>(s_dyn + lay.u);     // [P][RS]
-    uint2* s_g = reinterpret_cast<uint2*>(s_dyn + lay.g);           // [kGather] (id, L bits)
-    float* s_z = reinterpret_cast<float*>(s_dyn + lay.z);           // [P][kStageCap] (after staging)
-    Cand* s_cand = reinterpret_cast<Cand*>(s_dyn + lay.cand);       // [P k]
-    Cand* s_sorted = reinterpret_cast<Cand*>(s_dyn + lay.sorted);   // [P k]
+// ---------------------------------------------------------------------------
+// Once per cycle: the ids each (request, level) row can need
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kLvThreads) tree_rows_kernel(const TreeRowsParams p) {
     __shared__ int s_pref[kMaxPickChunks + 1];
-    __shared__ uint2 s_keep[kStageCap];    // kept (id, L bits), in (L desc, id asc) order
-    __shared__ int s_nkeep, s_exhaust, s_over;
-    __shared__ float s_lk;                 // L_(k) of the row
-    __shared__ int s_tok[kMaxTreeSlots], s_node[kMaxTreeSlots], s_cnt[kMaxTreeSlots];
-    __shared__ float s_score[kMaxTreeSlots], s_lse[kMaxTreeSlots], s_thr[kMaxTreeSlots];
-    __shared__ float2 s_top[kMaxTreeSlots][kMaxTopK];   // per parent: (z, id bits) in rank order
-    __shared__ unsigned long long s_red[kLvWarps];
-    const int i = blockIdx.x;
+    __shared__ uint2 s_g[kGather];
+    __shared__ uint2 s_keep[kTreeKeep];
+    __shared__ int s_nkeep, s_bad;
+    __shared__ float s_lk;
+    pdl_wait();
+    pdl_trigger();
+    const int row = blockIdx.x;   // request * B + (level - 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nc = p.n_chunks, P = p.P, K = p.k, r = p.r;
-    const int seg0 = (i * p.B + (p.d - 1)) * nc;
-    const float cmax = __ldcg(p.c_max);
-
-    // 1. the row's lists (written by the scan at the cycle's start, not by the
-    //    kernel this launch follows)
+    const int nc = p.n_chunks, K = p.k;
+    const int seg0 = row * nc;
     if (warp == 0) {
         int run = 0, over = 0;
         for (int c0 = 0; c0 < nc; c0 += 32) {
             const int c = c0 + lane;
             int n = 0;
             if (c < nc) {
-                const int cn = __ldcg(p.cand_n + seg0 + c);
+                const int cn = p.cand_n[seg0 + c];
                 over |= cn > kSegCap;
                 n = min(cn, kSegCap);
             }
@@ -155,20 +118,24 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
             run += __shfl_sync(0xffffffffu, x, 31);
         }
         over = __any_sync(0xffffffffu, over);
+        float lm = -INFINITY;   // the row's largest logit: the largest chunk maximum
+        for (int c = lane; c < nc; c += 32) lm = fmaxf(lm, p.cmax[seg0 + c]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lm = fmaxf(lm, __shfl_xor_sync(0xffffffffu, lm, o));
         if (lane == 0) {
+            p.lmax[row] = lm;
             s_pref[nc] = run;
-            s_over = over;
-            s_exhaust = over || run > kGather;
+            s_bad = over || run > kGather;
             s_nkeep = 0;
             s_lk = -INFINITY;
         }
     }
     __syncthreads();
     const int total = s_pref[nc];
-    if (!s_exhaust) {
+    if (!s_bad) {
         for (int t = tid; t < total; t += kLvThreads) {
             const int c = list_of(s_pref, nc, t);
-            s_g[t] = __ldcg(p.cand + static_cast<size_t>(seg0 + c) * kSegCap + (t - s_pref[c]));
+            s_g[t] = p.cand[static_cast<size_t>(seg0 + c) * kSegCap + (t - s_pref[c])];
         }
         __syncthreads();
         // L_(k): the entry with fewer than k entries above it and at least k
@@ -187,110 +154,175 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
         __syncthreads();
         const float lk = s_lk;
         if (lk == -INFINITY) {
-            if (tid == 0) s_exhaust = 1;       // fewer than k listed values
+            if (tid == 0) s_bad = 1;           // fewer than k listed values
         } else {
-            // the ids any parent can need: L >= L_(k) - 2 c_max
-            const float tu = markov_cut(lk, cmax);
+            const float tu = markov_cut(lk, *p.c_max);   // the ids any parent can need
             for (int t = tid; t < total; t += kLvThreads) {
                 const uint2 e = s_g[t];
                 if (e.x < static_cast<uint32_t>(p.V) && __uint_as_float(e.y) >= tu) {
                     const int slot = atomicAdd(&s_nkeep, 1);
-                    if (slot < kStageCap) s_keep[slot] = e;
+                    if (slot < kTreeKeep) s_keep[slot] = e;
                 }
             }
         }
         __syncthreads();
-        if (s_nkeep > kStageCap && tid == 0) s_exhaust = 1;
+        if (s_nkeep > kTreeKeep && tid == 0) s_bad = 1;
         __syncthreads();
-        if (!s_exhaust) {
-            // order the kept ids by (L desc, id asc): a parent's ids are then a prefix
-            const int nk = s_nkeep;
-            uint2 mine = make_uint2(0u, 0u);
-            int rk = -1;
-            if (tid < nk) {   // nk <= kStageCap < kLvThreads: one id per thread
-                mine = s_keep[tid];
-                const float x = __uint_as_float(mine.y);
-                rk = 0;
-                for (int u = 0; u < nk; ++u) {
-                    const uint2 o = s_keep[u];
-                    const float y = __uint_as_float(o.y);
-                    rk += (y > x || (y == x && o.x < mine.x)) ? 1 : 0;
-                }
-            }
-            __syncthreads();
-            if (rk >= 0) s_keep[rk] = mine;
-            __syncthreads();
-            // their W^T rows into shared memory (16 bytes per lane)
-            for (int j = warp; j < nk; j += kLvWarps) {
-                const uint16_t* src = p.Wt + static_cast<size_t>(s_keep[j].x) * r;
-                for (int q = lane * 8; q < r; q += 256) cp_async_16(s_w + static_cast<size_t>(j) * RS + q, src + q, 16u);
-            }
-        }
     }
+    uint2* out = p.keep + static_cast<size_t>(row) * kTreeKeep;
+    if (s_bad) {
+        if (tid == 0) {
+            p.n_keep[row] = -1;
+            p.lk[row] = -INFINITY;
+        }
+        return;
+    }
+    // (L desc, id asc): a parent's ids are then a prefix
+    const int nk = s_nkeep;
+    if (tid < nk) {   // nk <= kTreeKeep <= kLvThreads: one id per thread
+        const uint2 mine = s_keep[tid];
+        const float x = __uint_as_float(mine.y);
+        int rk = 0;
+        for (int u = 0; u < nk; ++u) {
+            const uint2 o = s_keep[u];
+            const float y = __uint_as_float(o.y);
+            rk += (y > x || (y == x && o.x < mine.x)) ? 1 : 0;
+        }
+        out[rk] = mine;
+    }
+    if (tid == 0) {
+        p.n_keep[row] = nk;
+        p.lk[row] = s_lk;
+    }
+}
 
-    // 2. the parents, once the GEMM (and the level before it) has finished
+// ---------------------------------------------------------------------------
+// Per level: every parent's top k, the children's scores, the prune
+// ---------------------------------------------------------------------------
+struct LevelLayout {
+    uint32_t w, u, z, total;
+    int rs;   // staged row stride (elements): r + 8 (16 bytes apart in the banks)
+};
+
+// Dynamic shared memory: the row's ids' W^T rows [kTreeKeep][rs] bf16, the
+// parents' U rows [P][rs] bf16, the logits [P][kTreeKeep] fp32.
+__host__ __device__ inline LevelLayout level_layout(int P, int r) {
+    LevelLayout l;
+    l.rs = r + 8;
+    const uint32_t row = 2u * static_cast<uint32_t>(l.rs);
+    l.w = 0;
+    l.u = l.w + static_cast<uint32_t>(kTreeKeep) * row;
+    l.z = l.u + static_cast<uint32_t>(P) * row;
+    l.total = l.z + static_cast<uint32_t>(P) * kTreeKeep * 4u;
+    return l;
+}
+
+__global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLevelParams p) {
+    extern __shared__ __align__(16) uint8_t s_dyn[];
+    const LevelLayout lay = level_layout(p.P, p.r);
+    const int RS = lay.rs;
+    uint16_t* s_w = reinterpret_cast<uint16_t*>(s_dyn + lay.w);     // [kTreeKeep][RS]
+    uint16_t* s_u = reinterpret_cast<uint16_t*>(s_dyn + lay.u);     // [P][RS]
+    float* s_z = reinterpret_cast<float*>(s_dyn + lay.z);           // [P][kTreeKeep]
+    __shared__ uint2 s_keep[kTreeKeep];    // the row's ids (id, L bits), (L desc, id asc)
+    __shared__ int s_nk;
+    __shared__ float s_lk;
+    __shared__ int s_tok[kMaxTreeSlots], s_node[kMaxTreeSlots], s_cnt[kMaxTreeSlots];
+    __shared__ float s_score[kMaxTreeSlots], s_lse[kMaxTreeSlots];
+    __shared__ float2 s_top[kMaxTreeSlots][kMaxTopK];   // per parent: (z, id bits) in rank order
+    __shared__ Cand s_cand[kMaxTreeSlots], s_sorted[kMaxTreeSlots];   // P k <= 64 children
+    __shared__ unsigned long long s_red[kLvWarps];
+    __shared__ int s_nf;
     pdl_wait();
     pdl_trigger();
-    const int nf = min(p.n_front[i], P);
+    const int i = blockIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int P = p.P, K = p.k, r = p.r;
+    const int row = i * p.B + (p.d - 1);
+    // 1. one round of independent loads: the frontier, the row's ids, the
+    //    GEMM's partials of every parent (each warp keeps its own in registers)
+    if (tid == 0) {
+        s_nf = min(max(p.n_front[i], 0), P);
+        s_nk = p.n_keep[row];
+        s_lk = p.lk[row];
+    }
     for (int f = tid; f < P; f += kLvThreads) {
         const size_t fr = static_cast<size_t>(i) * P + f;
-        int t = f < nf ? p.front_tok[fr] : -1;
-        if (t >= p.V) {
-            set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
-            t = -1;
-        }
-        s_tok[f] = t;
+        s_tok[f] = p.front_tok[fr];
         s_node[f] = p.front_node[fr];
         s_score[f] = p.front_score[fr];
-        s_thr[f] = t >= 0 ? markov_cut(s_lk, p.c_bound[t]) : INFINITY;
     }
+    for (int t = tid; t < kTreeKeep; t += kLvThreads) s_keep[t] = p.keep[static_cast<size_t>(row) * kTreeKeep + t];
     __syncthreads();
+    const int nf = s_nf, nk = s_nk;
+    const bool exhaust = nk < 0;
+    // 2. one more round, every load independent of the others: the parents'
+    //    U rows and the ids' W^T rows (copies into shared memory), each
+    //    parent's bound c(y) and the GEMM's partials of its row (registers)
     for (int f = warp; f < nf; f += kLvWarps) {
         const int t = s_tok[f];
-        if (t >= 0)
+        if (t >= 0 && t < p.V)
             for (int q = lane * 8; q < r; q += 256)
                 cp_async_16(s_u + static_cast<size_t>(f) * RS + q, p.U + static_cast<size_t>(t) * r + q, 16u);
-        // lse of the parent's logits from the GEMM's partials: the largest
-        // maximum, then every partial's sum rescaled to it (fp32 exponential,
-        // fp64 sum)
-        const float2* pr = p.part + (static_cast<size_t>(i) * P + f) * p.n_part;
-        float m = -INFINITY;
-        for (int q = lane; q < p.n_part; q += 32) {
-            const float2 x = pr[q];
-            if (x.y > 0.f) m = fmaxf(m, x.x);
+    }
+    if (!exhaust)
+        for (int j = warp; j < nk; j += kLvWarps) {
+            const uint16_t* src = p.Wt + static_cast<size_t>(s_keep[j].x) * r;
+            for (int q = lane * 8; q < r; q += 256) cp_async_16(s_w + static_cast<size_t>(j) * RS + q, src + q, 16u);
         }
+    for (int f = warp; f < nf; f += kLvWarps) {
+        int t = s_tok[f];
+        if (t >= p.V) {
+            if (lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
+            t = -1;
+        }
+        const float cy = (t >= 0 && !exhaust) ? p.c_bound[t] : 0.f;
+        const float2* pr = p.part + (static_cast<size_t>(i) * P + f) * p.n_part;
+        float2 x[kMaxPartLane];
+#pragma unroll
+        for (int e = 0; e < kMaxPartLane; ++e) {
+            const int q = lane + e * 32;
+            x[e] = q < p.n_part ? pr[q] : make_float2(-INFINITY, 0.f);
+        }
+        // lse of the parent's logits: the largest maximum, then every
+        // partial's sum rescaled to it, summed in fp32 (a lane's terms, then
+        // the butterfly)
+        float m = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < kMaxPartLane; ++e)
+            if (x[e].y > 0.f) m = fmaxf(m, x[e].x);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        double sum = 0.0;
-        for (int q = lane; q < p.n_part; q += 32) {
-            const float2 x = pr[q];
-            if (x.y > 0.f) sum += static_cast<double>(x.y * expf(x.x - m));
-        }
+        float sum = 0.f;
+#pragma unroll
+        for (int e = 0; e < kMaxPartLane; ++e)
+            if (x[e].y > 0.f) sum += x[e].y * expf(x[e].x - m);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        if (lane == 0) s_lse[f] = static_cast<float>(static_cast<double>(m) + log(sum));
+        // the parent's ids: the prefix with L >= L_(k) - 2 c(y)
+        int n = 0;
+        if (t >= 0 && !exhaust) {
+            const float thr = markov_cut(s_lk, cy);
+            for (int j0 = 0; j0 < nk; j0 += 32) {
+                const int j = j0 + lane;
+                n += __popc(__ballot_sync(0xffffffffu, j < nk && __uint_as_float(s_keep[j].y) >= thr));
+            }
+        }
+        if (lane == 0) {
+            s_lse[f] = m + logf(sum);
+            s_cnt[f] = n;
+            if (t < 0) s_tok[f] = -1;
+        }
     }
     cp_async_wait_all();
     __syncthreads();
 
-    if (!s_exhaust) {
-        const int nk = s_nkeep;
-        // each parent's ids: the kept prefix with L >= L_(k) - 2 c(y)
-        for (int f = warp; f < nf; f += kLvWarps) {
-            int n = 0;
-            for (int j0 = 0; j0 < nk; j0 += 32) {
-                const int j = j0 + lane;
-                const bool in = j < nk && __uint_as_float(s_keep[j].y) >= s_thr[f];
-                n += __popc(__ballot_sync(0xffffffffu, in));
-            }
-            if (lane == 0) s_cnt[f] = s_tok[f] >= 0 ? n : 0;
-        }
-        __syncthreads();
-        // z for every (parent, id) pair: fp32(L) + U[y] . W^T[v]
+    if (!exhaust) {
+        // 2. z for every (parent, id) pair: fp32(L) + U[y] . W^T[v]
         for (int t = tid; t < nf * nk; t += kLvThreads) {
             const int f = t / nk, j = t - f * nk;
             if (j < s_cnt[f])
-                s_z[f * kStageCap + j] = __uint_as_float(s_keep[j].y) +
+                s_z[f * kTreeKeep + j] = __uint_as_float(s_keep[j].y) +
                                          dot_rows(s_u + static_cast<size_t>(f) * RS, s_w + static_cast<size_t>(j) * RS, r);
         }
         __syncthreads();
@@ -299,17 +331,17 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
             const int f = t / nk, j = t - f * nk;
             const int n = s_cnt[f];
             if (j >= n) continue;
-            const unsigned long long me = argmax_key(s_z[f * kStageCap + j], s_keep[j].x);
+            const unsigned long long me = argmax_key(s_z[f * kTreeKeep + j], s_keep[j].x);
             int rk = 0;
             for (int u = 0; u < n && rk < K; ++u)
-                rk += argmax_key(s_z[f * kStageCap + u], s_keep[u].x) > me ? 1 : 0;
-            if (rk < K) s_top[f][rk] = make_float2(s_z[f * kStageCap + j], __int_as_float(static_cast<int>(s_keep[j].x)));
+                rk += argmax_key(s_z[f * kTreeKeep + u], s_keep[u].x) > me ? 1 : 0;
+            if (rk < K) s_top[f][rk] = make_float2(s_z[f * kTreeKeep + j], __int_as_float(static_cast<int>(s_keep[j].x)));
         }
     } else {
         // every id of the vocabulary for every parent, W^T rows from global
         // memory; per thread a sorted list of its k best keys, then k rounds
         // of the block maximum
-        const size_t lrow = (static_cast<size_t>(i) * p.B + (p.d - 1)) * p.V;
+        const size_t lrow = static_cast<size_t>(row) * p.V;
         for (int f = 0; f < nf; ++f) {
             if (s_tok[f] < 0) continue;
             unsigned long long best[kMaxTopK];
@@ -341,7 +373,7 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
         }
     }
     __syncthreads();
-    // children s = s(p) + (z - lse(p)), the P best kept
+    // 3. children s = s(p) + (z - lse(p)), the P best kept
     const int ncand = nf * K;
     for (int t = tid; t < ncand; t += kLvThreads) {
         const int f = t / K, q = t - f * K;
@@ -356,11 +388,16 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
 
 }  // namespace
 
-size_t tree_level_smem(int P, int k, int r) { return level_layout(P, k, r).total; }
+size_t tree_level_smem(int P, int r) { return level_layout(P, r).total; }
+
+cudaError_t launch_tree_rows(const TreeRowsParams& p, cudaStream_t s) {
+    if (p.k > kMaxTopK || p.n_chunks > kMaxPickChunks) return cudaErrorInvalidValue;
+    return launch_pdl(tree_rows_kernel, dim3(p.rows), dim3(kLvThreads), 0, s, p);
+}
 
 cudaError_t launch_tree_level(const TreeLevelParams& p, cudaStream_t s) {
-    if (p.P > kMaxTreeSlots || p.k > kMaxTopK || p.n_chunks > kMaxPickChunks) return cudaErrorInvalidValue;
-    const size_t smem = tree_level_smem(p.P, p.k, p.r);
+    if (p.P > kMaxTreeSlots || p.k > kMaxTopK || p.n_part > 32 * kMaxPartLane) return cudaErrorInvalidValue;
+    const size_t smem = tree_level_smem(p.P, p.r);
     static size_t configured = 0;   // the dynamic shared memory allowed so far
     if (smem > configured) {
         const cudaError_t e =
