@@ -219,6 +219,7 @@ class Cycle:
         i32 = dict(dtype=torch.int32, device=device)
         self.status = sdm.new_status(device)
         self.side = torch.cuda.Stream(device=device)
+        self.layout_ready = torch.cuda.Event()
         self.prepared = None
         if self.tree:
             self._init_tree(R, B, V, r, i32)
@@ -335,16 +336,31 @@ class Cycle:
 
     def front(self):
         """Draft, schedule and pack.  The budget needs only the confidences,
-        so the scheduler runs on a side stream while the draft runs; the
-        pack joins both."""
+        so the scheduler runs on a side stream while the draft runs.  With the
+        greedy chain's prepared tables the side stream also lays out the
+        ragged windows from the budgets, and the draft's pick writes its
+        tokens into them (no pack pass after the draft); otherwise the pack
+        joins both."""
         if self.tree:
             self.draft()
             return
-        torch = self.torch
+        torch, sdm, i = self.torch, self.sdm, self.inp
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
+        fused = self.prepared is not None and not self.rnn
         with torch.cuda.stream(self.side):
             self.schedule()
+            if fused:
+                budget = self.sc["budget"] if self.mode == sdm.COMPACT else None
+                sdm.pack_ragged(i["anchor"], None, budget, i["tiers"], out=self.pk, dev_status=self.status,
+                                gamma=self.w.B)
+                self.layout_ready.record(self.side)
+        if fused:
+            sdm.draft_chain_packed(i["L"], i["U"], i["W"], i["anchor"], self.prepared, self.pk["cu_seqlens"],
+                                   self.pk["packed_tok"], tokens=self.dr["tokens"], layout_ready=self.layout_ready,
+                                   ws=self.ws_draft, dev_status=self.status)
+            main.wait_stream(self.side)
+            return
         self.draft()
         main.wait_stream(self.side)
         self.pack()

@@ -172,6 +172,28 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
                            void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * draft_chain_packed: the greedy chain of sdm_draft_chain with prepared
+ * tables, writing its drafts also into the ragged verify layout (the pack of
+ * [SGLang] "ragged verify" without a pass of its own after the draft).  The
+ * layout is sdm_pack_ragged's with draft = NULL (cu_seqlens, the tier, the
+ * row maps and the anchors, made from the budgets alone, e.g. on a second
+ * stream while this draft runs); this call fills rows cu[i] + 1 .. cu[i] +
+ * n_i of packed_tok with y_1 .. y_{n_i}, n_i = cu[i+1] - cu[i] - 1, so that
+ * packed_tok ends as sdm_pack_ragged with the drafts would leave it.
+ * layout_ready (a cudaEvent_t, may be NULL): recorded after the layout's
+ * producer; the scan of L starts at once, the pass that writes the drafts
+ * waits for the event on `stream`.  NULL: the layout is ordered before this
+ * call on `stream`.
+ * In/out as sdm_draft_chain (prepared required); cu_seqlens [R+1],
+ * packed_tok [capacity] (device).  A window longer than B sets
+ * SDM_DEV_BAD_WINDOW (cut to B); rows past capacity SDM_DEV_CAPACITY.
+ */
+sdm_status sdm_draft_chain_packed(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                                  const void* prepared, const int32_t* anchor, int R, int B, int V, int r,
+                                  const int32_t* cu_seqlens, int32_t* packed_tok, int capacity, void* layout_ready,
+                                  int32_t* tokens, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
  * draft_chain_rnn: the chain draft with the RNN sequential head ([DSpark
  * notes] sec. 4, "RNN head": a memo that carries the whole draft so far,
  * updated once per step from the previous memo, the previous word and the
@@ -298,8 +320,9 @@ sdm_status sdm_schedule_dynamic(const float* conf, const float* conf_stale, int 
  *   strict != 0, SDM_DEV_TIER_OVERFLOW instead (a caller that only runs
  *   captured tiers maps it to SDM_ERR_TIER_OVERFLOW with
  *   sdm_status_of_device; the rows are packed the same way).
- * In:  anchor [R], draft [R, gamma], budget [R] or NULL, tiers [n_tiers]
- *      int32 (device), strict (0 or 1).
+ * In:  anchor [R], draft [R, gamma] or NULL (the layout alone: every draft
+ *      row holds -1, for sdm_draft_chain_packed to fill), budget [R] or
+ *      NULL, tiers [n_tiers] int32 (device), strict (0 or 1).
  * Out: cu_seqlens [R+1], packed_tok/req/pos [capacity], tier [1] (device);
  *      tier_host (host, may be NULL): if non-NULL it must be pinned host
  *      memory and receives the tier by an async copy on `stream`.

@@ -28,6 +28,7 @@ EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
            "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_schedule_threshold",
            "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str", "sdm_status_of_device", "sdm_check_timeout_path",
+           "sdm_draft_chain_packed",
            "sdm_version")
 
 
@@ -61,6 +62,9 @@ def _declare(lib):
     lib.sdm_schedule_dynamic.argtypes = [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_pack_ragged.restype = _I
     lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
+    lib.sdm_draft_chain_packed.restype = _I
+    lib.sdm_draft_chain_packed.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _I, _VP, _VP, _VP,
+                                           _SZ, _VP, _VP]
     lib.sdm_check_timeout_path.restype = _I
     lib.sdm_check_timeout_path.argtypes = [_VP, _I, _VP, _VP, _VP, _I, _I, _I, _I, ctypes.c_ulonglong, _VP, _SZ, _VP,
                                            _VP]
@@ -180,6 +184,26 @@ def draft_chain(L, U, W, anchor, decode=GREEDY, temperature=1.0, seed=0, cycle=0
     _check(st, "sdm_draft_chain")
     out["dev_status"] = dev_status
     return out
+
+
+def draft_chain_packed(L, U, W, anchor, prepared, cu_seqlens, packed_tok, tokens=None, layout_ready=None, ws=None,
+                       dev_status=None):
+    """Greedy chain draft (prepared tables) that also fills its drafts into a
+    ragged layout made by pack_ragged(draft=None); layout_ready: a
+    torch.cuda.Event recorded after that layout's producer (or None)."""
+    _need_cuda(L, U, W, anchor, cu_seqlens, packed_tok)
+    R, B, V = L.shape
+    r = U.shape[1]
+    dev = L.device
+    tokens = torch.empty((R, B), dtype=torch.int32, device=dev) if tokens is None else tokens
+    ws = workspace(OP_DRAFT_CHAIN, R, B, V, r, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    ev = None if layout_ready is None else ctypes.c_void_p(layout_ready.cuda_event)
+    st = lib().sdm_draft_chain_packed(_ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(prepared), _ptr(anchor), R,
+                                      B, V, r, _ptr(cu_seqlens), _ptr(packed_tok), packed_tok.numel(), ev,
+                                      _ptr(tokens), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_draft_chain_packed")
+    return dict(tokens=tokens, dev_status=dev_status)
 
 
 def check_timeout_path(L, U, W, anchor, wait_ns, dev_status=None):
@@ -327,10 +351,13 @@ def pack_capacity(R, gamma, tiers) -> int:
 
 
 def pack_ragged(anchor, draft, budget, tiers, capacity=None, out=None, dev_status=None, tier_host=None,
-                strict=False):
+                strict=False, gamma=None):
+    """Ragged front-pack; draft=None (give gamma) lays out the windows alone,
+    every draft row -1, for draft_chain_packed to fill."""
     _need_cuda(anchor, draft, budget, tiers)
-    R, g = draft.shape
-    dev = draft.device
+    R = anchor.numel()
+    g = draft.shape[1] if draft is not None else int(gamma)
+    dev = anchor.device
     if out is None:
         cap = capacity if capacity else pack_capacity(R, g, tiers.tolist())
         out = dict(cu_seqlens=torch.empty((R + 1,), dtype=torch.int32, device=dev),

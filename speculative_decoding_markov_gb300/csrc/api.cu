@@ -403,6 +403,56 @@ sdm_status sdm_draft_chain(const void* L, sdm_dtype dtL, const uint16_t* U, cons
                              ws, dev_status, s);
 }
 
+sdm_status sdm_draft_chain_packed(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                                  const void* prepared, const int32_t* anchor, int R, int B, int V, int r,
+                                  const int32_t* cu_seqlens, int32_t* packed_tok, int capacity, void* layout_ready,
+                                  int32_t* tokens, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!L || !U || !W || !prepared || !anchor || !cu_seqlens || !packed_tok || !tokens || R <= 0 || B <= 0 ||
+        V <= 0 || r <= 0 || capacity <= 0)
+        return SDM_ERR_INVALID_ARG;
+    if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W) || !aligned16(prepared))
+        return SDM_ERR_UNSUPPORTED;
+    const int n_chunks = pruned_chunks(V, dtL == SDM_FP32);
+    if (B > kMaxPickSteps || n_chunks > kMaxPickChunks || static_cast<long long>(R) * B * n_chunks > (1LL << 30))
+        return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_chain(R, B, V)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Carver pc{static_cast<uint8_t*>(const_cast<void*>(prepared))};
+    PrunedParams pp;
+    std::memset(&pp, 0, sizeof pp);
+    pp.L = L;
+    pp.l_fp32 = dtL == SDM_FP32;
+    pp.R = R;
+    pp.B = B;
+    pp.V = V;
+    pp.r = r;
+    pp.n_chunks = n_chunks;
+    pp.anchor = anchor;
+    pp.U = U;
+    pp.Wt = pc.take<uint16_t>(static_cast<size_t>(V) * r);
+    pp.c_bound = pc.take<float>(V);
+    pc.take<float>(V);           // |U[v]|
+    pc.take<unsigned int>(V);    // A(v)
+    pp.c_max = pc.take<float>(1);
+    Carver wc{static_cast<uint8_t*>(ws)};
+    const size_t segs = static_cast<size_t>(R) * B * n_chunks;
+    pp.cand = wc.take<uint2>(segs * kSegCap);
+    pp.cand_n = wc.take<int32_t>(segs);
+    pp.cmax = wc.take<float>(segs);
+    pp.tokens = tokens;
+    pp.dev_status = dev_status;
+    pp.pack_cu = cu_seqlens;
+    pp.pack_tok = packed_tok;
+    pp.pack_cap = capacity;
+    // the scan reads only L: it runs before the layout is ready; the pick
+    // writes into the layout, so it waits for it
+    SDM_CHECK_CUDA(launch_chain_scan(pp, s));
+    if (layout_ready) SDM_CHECK_CUDA(cudaStreamWaitEvent(s, static_cast<cudaEvent_t>(layout_ready), 0));
+    SDM_CHECK_CUDA(launch_chain_pick(pp, s));
+    return SDM_OK;
+}
+
 sdm_status sdm_draft_chain_rnn(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, const uint16_t* A,
                                const uint16_t* X, const int32_t* anchor, int R, int B, int V, int r, sdm_decode decode,
                                float temperature, sdm_rng rng, int32_t* tokens, float* logq, float* lse, float* memo,
@@ -712,7 +762,7 @@ sdm_status sdm_pack_ragged(const int32_t* anchor, const int32_t* draft, const in
                            const int32_t* tiers, int n_tiers, int strict, int32_t* cu_seqlens, int32_t* packed_tok,
                            int32_t* packed_req, int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tier_host,
                            int32_t* dev_status, void* stream) {
-    if (!anchor || !draft || !cu_seqlens || !packed_tok || !packed_req || !packed_pos || !tier) return SDM_ERR_INVALID_ARG;
+    if (!anchor || !cu_seqlens || !packed_tok || !packed_req || !packed_pos || !tier) return SDM_ERR_INVALID_ARG;
     if (R <= 0 || gamma < 0 || n_tiers < 0 || capacity <= 0 || (n_tiers > 0 && !tiers)) return SDM_ERR_INVALID_ARG;
     if (strict != 0 && strict != 1) return SDM_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);

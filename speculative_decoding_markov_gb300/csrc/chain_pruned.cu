@@ -325,6 +325,20 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Draft token y of position d0 + 1 (0-based d0) of request `row`: the
+// tokens array and, when a ragged layout is given, its row cu[row] + 1 + d0
+// if the request's window holds it (pk0 = cu[row], pkn = its window).
+__device__ __forceinline__ void emit_token(const PrunedParams& p, int row, int d0, int y, int pk0, int pkn) {
+    p.tokens[static_cast<size_t>(row) * p.B + d0] = y;
+    if (p.pack_tok && d0 < pkn) {
+        const int prow = pk0 + 1 + d0;
+        if (prow >= 0 && prow < p.pack_cap)
+            p.pack_tok[prow] = y;
+        else
+            set_status(p.dev_status, SDM_DEV_CAPACITY);
+    }
+}
+
 template <int FP32>
 __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedParams p) {
     constexpr int VEC = FP32 ? 4 : 8;
@@ -360,9 +374,24 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     __shared__ uint2 s_ids[kPickCap];
     __shared__ int s_m;
     __shared__ unsigned long long s_best[2];
+    __shared__ int s_pk0, s_pkn;                                    // the request's ragged window, if any
     const float cmax = *p.c_max;
     const int seg0 = row * B * nc;
-    if (threadIdx.x == 0) s_alloc = 0;
+    if (threadIdx.x == 0) {
+        s_alloc = 0;
+        s_pk0 = 0;
+        s_pkn = -1;
+        if (p.pack_tok) {
+            const int c0 = p.pack_cu[row], c1 = p.pack_cu[row + 1];
+            int n = c1 - c0 - 1;
+            if (n > B || n < 0) {
+                if (n > B) set_status(p.dev_status, SDM_DEV_BAD_WINDOW);
+                n = n > B ? B : -1;
+            }
+            s_pk0 = c0;
+            s_pkn = n;
+        }
+    }
     for (int t = threadIdx.x; t <= kRowCapMax; t += kThreads) s_rowkey[t] = 0ull;
     __syncthreads();
 
@@ -641,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
                         set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
                         tokv = 0;
                     }
-                    p.tokens[static_cast<size_t>(row) * B + d] = tokv;
+                    emit_token(p, row, d, tokv, s_pk0, s_pkn);
                 }
             }
             return;
@@ -707,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
                 y = 0;
                 bslot = -1;
             }
-            if (lane == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
+            if (lane == 0) emit_token(p, row, d - 1, y, s_pk0, s_pkn);
             if (bslot >= 0) {   // the winner's U row and bound were staged with it
                 urow = st_u + static_cast<size_t>(bslot) * RS;
                 cprev = st_c[bslot];
@@ -779,7 +808,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
             if (threadIdx.x == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
             y = 0;
         }
-        if (threadIdx.x == 0) p.tokens[static_cast<size_t>(row) * B + (d - 1)] = y;
+        if (threadIdx.x == 0) emit_token(p, row, d - 1, y, s_pk0, s_pkn);
         urow = p.U + static_cast<size_t>(y) * r;
         cprev = p.c_bound[y];
         pidx = -1;
@@ -861,6 +890,11 @@ cudaError_t launch_chain_scan(const PrunedParams& p, cudaStream_t s) {
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {
     cudaError_t e = launch_chain_scan(p, s);
     if (e != cudaSuccess) return e;
+    return launch_chain_pick(p, s);
+}
+
+cudaError_t launch_chain_pick(const PrunedParams& p, cudaStream_t s) {
+    cudaError_t e = cudaSuccess;
     const PickLayout lay = pick_layout(p.B, p.n_chunks, p.r);
     if (lay.cap < 1) return cudaErrorInvalidValue;
     static bool configured = false;

@@ -360,7 +360,15 @@ struct PrunedParams {
     int32_t* tokens;        // [R, B]
     int32_t* dev_status;
     int kth;                // lists for the k-th largest (PCTree, k > 1); 0 or 1: the chain's argmax
+    // the pick's drafts also into a ragged layout (NULL: none): rows
+    // pack_cu[i] + 1 .. pack_cu[i] + n_i of pack_tok, n_i = pack_cu[i+1] - pack_cu[i] - 1
+    const int32_t* pack_cu;
+    int32_t* pack_tok;
+    int pack_cap;
 };
+// The scan alone, then (after the caller's dependency, e.g. an event wait)
+// the pick alone.
+cudaError_t launch_chain_pick(const PrunedParams& p, cudaStream_t s);
 
 int pruned_chunks(int V, int l_fp32);
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s);

@@ -447,7 +447,8 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(const int32_t* ancho
                 continue;
             }
             const int ig = base + il;
-            ptok[row] = (p == 0) ? anchor[ig] : draft[static_cast<size_t>(ig) * gamma + p - 1];
+            // without drafts (a layout for sdm_draft_chain_packed to fill) the draft rows hold -1
+            ptok[row] = (p == 0) ? anchor[ig] : (draft ? draft[static_cast<size_t>(ig) * gamma + p - 1] : -1);
             preq[row] = ig;
             ppos[row] = p;
         }

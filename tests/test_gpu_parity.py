@@ -720,3 +720,59 @@ def test_a_wait_that_runs_out_is_reported_and_the_stream_stays_usable():
     torch.cuda.synchronize()
     assert int(st2.item()) == sdm.DEV_TIMEOUT and int(out["dev_status"].item()) == 0
     np.testing.assert_array_equal(host(out["tokens"]), ref["tokens"])
+
+
+# ---------------------------------------------------------------------------
+# the draft that fills the ragged layout
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", [dict(R=64, B=7, V=151936, r=256), dict(R=37, B=5, V=4104, r=64)],
+                         ids=["headline_shape", "ragged"])
+def test_draft_chain_packed_fills_the_layout(case):
+    """The layout made from the budgets alone (pack_ragged without drafts, on
+    a second stream) and filled by the draft's pick equals pack_ragged with
+    the drafts; the drafts equal sdm_draft_chain's."""
+    w = small(l_dtype=BF16, sigma=(0.5,), l_std=2.0, **case)
+    inp = {k: dev(v) for k, v in synthetic.generate(w, seed=case["R"]).items()}
+    prep = sdm.markov_prepare(inp["U"], inp["W"])
+    ref = sdm.draft_chain(inp["L"], inp["U"], inp["W"], inp["anchor"], prepared=prep)
+    budget = dev(torch.from_numpy(np.random.default_rng(3).integers(0, w.B + 1, w.R).astype(np.int32)))
+    tiers = dev(torch.tensor([64, 128, 256, 512, 1024], dtype=torch.int32))
+    full = sdm.pack_ragged(inp["anchor"], ref["tokens"], budget, tiers)
+    side = torch.cuda.Stream()
+    ready = torch.cuda.Event()
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        lay = sdm.pack_ragged(inp["anchor"], None, budget, tiers, gamma=w.B)
+        ready.record(side)
+    out = sdm.draft_chain_packed(inp["L"], inp["U"], inp["W"], inp["anchor"], prep, lay["cu_seqlens"],
+                                 lay["packed_tok"], layout_ready=ready)
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) == 0 and int(lay["dev_status"].item()) & ~sdm.DEV_TIER_UNCAPTURED == 0
+    assert torch.equal(out["tokens"], ref["tokens"])
+    for k in ("cu_seqlens", "packed_tok", "packed_req", "packed_pos", "tier"):
+        assert torch.equal(lay[k], full[k]), k
+
+
+def test_pack_layout_alone_holds_the_anchors():
+    """Without drafts the layout's window rows hold the anchor first and -1
+    where the drafts go; the offsets and row maps are those of the full pack."""
+    R, g = 9, 4
+    rng = np.random.default_rng(5)
+    anchor = rng.integers(0, 1000, R).astype(np.int32)
+    draft = rng.integers(0, 1000, (R, g)).astype(np.int32)
+    budget = rng.integers(0, g + 1, R).astype(np.int32)
+    tiers = np.array([16, 32, 64], np.int32)
+    ref = oracle.pack_ragged(anchor, draft, budget, tiers)
+    out = sdm.pack_ragged(dev(torch.from_numpy(anchor)), None, dev(torch.from_numpy(budget)), dev(torch.from_numpy(tiers)),
+                          gamma=g)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(host(out["cu_seqlens"]), ref["cu_seqlens"])
+    t = ref["tier"]
+    np.testing.assert_array_equal(host(out["packed_req"])[:t], ref["packed_req"])
+    np.testing.assert_array_equal(host(out["packed_pos"])[:t], ref["packed_pos"])
+    tok = host(out["packed_tok"])[:t]
+    pos = ref["packed_pos"]
+    np.testing.assert_array_equal(tok[pos == 0], anchor)
+    assert np.all(tok[pos > 0] == -1)
