@@ -115,11 +115,10 @@ size_t ws_tree_common(int R, int B, int P) {
     return 3 * align256(rows * 4) + align256(R * 4) + 4 * align256(pool * 4) + align256(R * 4);
 }
 
-int tree_n_part(int R, int P, int V) {   // the most partials either sub-tile layout gives
+int tree_n_part(int R, int P, int V) {   // one partial per GEMM CTA column: the most either sub-tile layout gives
     const int gy = (R * P + kTileM - 1) / kTileM;
     const int gy2 = (R * P + 2 * kTileM - 1) / (2 * kTileM);
-    return std::max(gemm_grid_x((V + kTileN - 1) / kTileN, gy), gemm_grid_x((V + kTileN - 1) / kTileN, gy2)) *
-           kColGroups;
+    return std::max(gemm_grid_x((V + kTileN - 1) / kTileN, gy), gemm_grid_x((V + kTileN - 1) / kTileN, gy2));
 }
 
 size_t ws_tree(int R, int B, int P, int V) {
@@ -569,7 +568,7 @@ sdm_status sdm_draft_tree(const void* L, sdm_dtype dtL, const uint16_t* U, const
         pp.cmax = c.take<float>(segs);
         pp.dev_status = dev_status;
         pp.kth = k;
-        const int n_part = gx * kColGroups;
+        const int n_part = gx;   // one partial per frontier row and GEMM CTA
         auto* part = c.take<float2>(rows * n_part);
         TreeRowsParams rp;
         std::memset(&rp, 0, sizeof rp);

@@ -111,7 +111,7 @@ struct GemmParams {
     const int32_t* res_req;
     const float* row_lse_q;
     float2* part;               // [rows][n_part]
-    int n_part;                 // gridDim.x * kColGroups
+    int n_part;                 // gridDim.x * kColGroups (MODE_TREE_LSE: gridDim.x, the groups merged)
     // absmax (prepared tables): GEMM row m = token m
     unsigned int* absmax_bits;      // [rows] max_v |U[m] . W[:, v]| as fp32 bits (atomic max)
     int32_t* dev_status;

@@ -442,8 +442,10 @@ struct Epi<MODE_TREE_LSE> {
         for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(fmaf(z[j], kLog2e, -mo));   // 2^-inf = 0 on the tail
         s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     }
+    // this thread's (m, s): (-inf, 0) when it consumed nothing
+    __device__ __forceinline__ float2 partial() const { return make_float2(s > 0.f ? m : -INFINITY, s); }
     __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
-        if (valid) *part_slot(p, grow, group) = make_float2(s > 0.f ? m : -INFINITY, s);
+        if (valid) *part_slot(p, grow, group) = partial();
     }
 };
 
@@ -985,8 +987,35 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             }
         }
+        if constexpr (MODE == MODE_TREE_LSE) {
+            // one partial per row and CTA: the column groups' pairs meet in
+            // shared memory (the rings are idle once every epilogue warp has
+            // consumed its last tile), the first group merges and writes them
+            float2* cmb = reinterpret_cast<float2*>(smem);   // [kColGroups][MS][kTileM]
 #pragma unroll
-        for (int h = 0; h < MS; ++h) sts[h].flush(p, grow + h * kTileM);
+            for (int h = 0; h < MS; ++h) cmb[(g * MS + h) * kTileM + lrow] = sts[h].partial();
+            asm volatile("bar.sync 1, %0;" ::"r"(kEpiWarps * 32) : "memory");
+            if (g == 0) {
+#pragma unroll
+                for (int h = 0; h < MS; ++h) {
+                    float mm = -INFINITY;
+#pragma unroll
+                    for (int gg = 0; gg < kColGroups; ++gg) mm = fmaxf(mm, cmb[(gg * MS + h) * kTileM + lrow].x);
+                    float ss = 0.f;
+#pragma unroll
+                    for (int gg = 0; gg < kColGroups; ++gg) {
+                        const float2 x = cmb[(gg * MS + h) * kTileM + lrow];
+                        if (x.y > 0.f) ss += x.y * fast_exp2((x.x - mm) * kLog2e);
+                    }
+                    if (sts[h].valid)
+                        p.part[static_cast<size_t>(grow + h * kTileM) * p.n_part + blockIdx.x] =
+                            make_float2(ss > 0.f ? mm : -INFINITY, ss);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int h = 0; h < MS; ++h) sts[h].flush(p, grow + h * kTileM);
+        }
     }
 
     tc_fence_before();

@@ -34,7 +34,7 @@ namespace {
 constexpr int kLvThreads = 256;
 constexpr int kLvWarps = kLvThreads / 32;
 constexpr int kGather = 2048;   // listed entries of a row held in shared memory
-constexpr int kMaxPartLane = 24;   // GEMM partials per lane a warp loads at once (n_part <= 768)
+constexpr int kMaxPartLane = 8;    // GEMM partials per lane a warp loads at once (n_part <= 256 CTA columns)
 
 // Segment holding entry t of the row's concatenated lists.
 __device__ __forceinline__ int list_of(const int* pref, int nc, int t) {
@@ -232,19 +232,34 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
     __shared__ float2 s_top[kMaxTreeSlots][kMaxTopK];   // per parent: (z, id bits) in rank order
     __shared__ Cand s_cand[kMaxTreeSlots], s_sorted[kMaxTreeSlots];   // P k <= 64 children
     __shared__ unsigned long long s_red[kLvWarps];
-    __shared__ int s_nf;
-    pdl_wait();
-    pdl_trigger();
+    __shared__ int s_nf, s_np;
     const int i = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = p.P, K = p.k, r = p.r;
     const int row = i * p.B + (p.d - 1);
-    // 1. one round of independent loads: the frontier, the row's ids, the
-    //    GEMM's partials of every parent (each warp keeps its own in registers)
+    // 0. before the wait on the level's GEMM: the row's ids (made once per
+    //    cycle, before the first level) and the copies of their W^T rows
+    //    (read through L2: written by an earlier kernel than the one this
+    //    launch waits for)
+    if (tid == 0) {
+        s_nk = __ldcg(p.n_keep + row);
+        s_lk = __ldcg(p.lk + row);
+    }
+    for (int t = tid; t < kTreeKeep; t += kLvThreads) s_keep[t] = __ldcg(p.keep + static_cast<size_t>(row) * kTreeKeep + t);
+    __syncthreads();
+    const int nk = s_nk;
+    const bool exhaust = nk < 0;
+    if (!exhaust)
+        for (int j = warp; j < nk; j += kLvWarps) {
+            const uint16_t* src = p.Wt + static_cast<size_t>(s_keep[j].x) * r;
+            for (int q = lane * 8; q < r; q += 256) cp_async_16(s_w + static_cast<size_t>(j) * RS + q, src + q, 16u);
+        }
+    pdl_wait();
+    pdl_trigger();
+    // 1. one round of independent loads: the frontier and the pool's size
     if (tid == 0) {
         s_nf = min(max(p.n_front[i], 0), P);
-        s_nk = p.n_keep[row];
-        s_lk = p.lk[row];
+        s_np = p.pool_n[i];
     }
     for (int f = tid; f < P; f += kLvThreads) {
         const size_t fr = static_cast<size_t>(i) * P + f;
@@ -252,24 +267,17 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
         s_node[f] = p.front_node[fr];
         s_score[f] = p.front_score[fr];
     }
-    for (int t = tid; t < kTreeKeep; t += kLvThreads) s_keep[t] = p.keep[static_cast<size_t>(row) * kTreeKeep + t];
     __syncthreads();
-    const int nf = s_nf, nk = s_nk;
-    const bool exhaust = nk < 0;
+    const int nf = s_nf;
     // 2. one more round, every load independent of the others: the parents'
-    //    U rows and the ids' W^T rows (copies into shared memory), each
-    //    parent's bound c(y) and the GEMM's partials of its row (registers)
+    //    U rows (copies into shared memory), each parent's bound c(y) and the
+    //    GEMM's partials of its row (registers)
     for (int f = warp; f < nf; f += kLvWarps) {
         const int t = s_tok[f];
         if (t >= 0 && t < p.V)
             for (int q = lane * 8; q < r; q += 256)
                 cp_async_16(s_u + static_cast<size_t>(f) * RS + q, p.U + static_cast<size_t>(t) * r + q, 16u);
     }
-    if (!exhaust)
-        for (int j = warp; j < nk; j += kLvWarps) {
-            const uint16_t* src = p.Wt + static_cast<size_t>(s_keep[j].x) * r;
-            for (int q = lane * 8; q < r; q += 256) cp_async_16(s_w + static_cast<size_t>(j) * RS + q, src + q, 16u);
-        }
     for (int f = warp; f < nf; f += kLvWarps) {
         int t = s_tok[f];
         if (t >= p.V) {
@@ -382,7 +390,7 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
                                   : Cand{-INFINITY, f, q, -1};
     }
     __syncthreads();
-    tree_keep_children(i, P, p.B, p.d, ncand, s_cand, s_sorted, s_node, p.pool_n[i], p.front_tok, p.front_node,
+    tree_keep_children(i, P, p.B, p.d, ncand, s_cand, s_sorted, s_node, s_np, p.front_tok, p.front_node,
                        p.front_score, p.n_front, p.pool_tok, p.pool_parent, p.pool_depth, p.pool_score, p.pool_n);
 }
 
