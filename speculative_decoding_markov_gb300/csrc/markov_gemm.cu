@@ -55,7 +55,7 @@ constexpr uint32_t kWBoxBytes = 64u * kBoxN * 2u;      // 8 KB
 constexpr int kMaxWStages = 12;
 constexpr int kMaxLStages = 6;
 // Tensor memory: two 128-column fp32 accumulators, then A (128 rows x r
-// bf16, two per 32-bit column: r / 2 <= 128 columns).
+// bf16 per sub-tile, two per 32-bit column: r / 2 <= 128 columns each).
 constexpr int kTmemA = 2 * kTileN;
 constexpr int kTmemCols = 512;
 
@@ -128,7 +128,7 @@ constexpr int C = kEpiCols;   // columns per epilogue thread and tile
 // swizzle: 16-byte chunk c of a row sits at c ^ (lr & 7)).
 __device__ __forceinline__ void load_l(const uint8_t* sl, uint32_t l_box_bytes, int l_fp32, int lr, int g,
                                        float (&out)[C]) {
-    if (!l_fp32) {
+    if (!l_fp32) {   // a constant where the kernel is instantiated per L dtype
         const uint8_t* rowp = sl + lr * 128;
 #pragma unroll
         for (int c = 0; c < C / 8; ++c) {
@@ -261,11 +261,12 @@ struct Epi<MODE_CHAIN_GREEDY> {
         best = -INFINITY;
         best_v = 0;
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lf, int lrow,
+                                            int vbase,
                                             int g, const uint32_t (&acc)[C]) {
         if (!valid) return;
         float z[C];
-        load_l(sl, lbb, p.l_fp32, lrow, g, z);
+        load_l(sl, lbb, lf, lrow, g, z);
 #pragma unroll
         for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
         mask_tail(z, vbase, p.V);
@@ -296,11 +297,12 @@ struct Epi<MODE_CHAIN_SAMPLE> {
         sc = p.inv_t * kLog2e;
         rec = p.blk + static_cast<size_t>(valid ? grow : 0) * p.nb;
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lf, int lrow,
+                                            int vbase,
                                             int g, const uint32_t (&acc)[C]) {
         if (!valid || vbase >= p.V) return;
         float z[C];
-        load_l(sl, lbb, p.l_fp32, lrow, g, z);
+        load_l(sl, lbb, lf, lrow, g, z);
 #pragma unroll
         for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * sc;
         mask_tail(z, vbase, p.V);
@@ -324,11 +326,12 @@ struct Epi<MODE_TREE> {
         valid = grow < p.rows && p.front_tok[grow] >= 0;
         rec = p.blk + static_cast<size_t>(grow < p.rows ? grow : 0) * p.nb;
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lf, int lrow,
+                                            int vbase,
                                             int g, const uint32_t (&acc)[C]) {
         if (!valid || vbase >= p.V) return;
         float z[C];
-        load_l(sl, lbb, p.l_fp32, lrow / p.P, g, z);
+        load_l(sl, lbb, lf, lrow, g, z);   // lrow: the request's L row
 #pragma unroll
         for (int j = 0; j < C; ++j) z[j] = (z[j] + __uint_as_float(acc[j])) * kLog2e;
         mask_tail(z, vbase, p.V);
@@ -361,7 +364,7 @@ struct Epi<MODE_RESID> {
             lse_p = p.res_lse_p[grow];
         }
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int vbase, int,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int, int vbase, int,
                                             const uint32_t (&acc)[C]) {
         if (!valid || vbase >= p.V) return;
         float lv[C], tv[C];
@@ -394,6 +397,40 @@ __device__ __forceinline__ float2* part_slot(const GemmParams& p, int grow, int 
     return p.part + static_cast<size_t>(grow) * p.n_part + blockIdx.x * kColGroups + group;
 }
 
+// Two fp32 values in one 64-bit register, the operand of the f32x2
+// instructions (sm_100 and later).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t x) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+    return r;
+}
+
+// Two columns of the bounded tree step: z = fp32(L) + a for the bf16 pair in
+// w (the mixed-precision add: the exact conversion and one rounding, as
+// fp32(L) + a), then acc += 2^(z log2(e) - m log2(e)) lane-wise, the scaling
+// one paired fma, the sum one paired add.
+__device__ __forceinline__ void lse2_bf16(uint32_t w, uint32_t a0, uint32_t a1, uint64_t sc2, uint64_t mo2,
+                                          uint64_t& acc) {
+    asm("{\n\t.reg .b16 lo, hi;\n\t.reg .f32 z0, z1, e0, e1;\n\t.reg .b64 zz, xx, ee;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "add.rn.f32.bf16 z0, lo, %2;\n\t"
+        "add.rn.f32.bf16 z1, hi, %3;\n\t"
+        "mov.b64 zz, {z0, z1};\n\t"
+        "fma.rn.f32x2 xx, zz, %4, %5;\n\t"
+        "mov.b64 {z0, z1}, xx;\n\t"
+        "ex2.approx.ftz.f32 e0, z0;\n\t"
+        "ex2.approx.ftz.f32 e1, z1;\n\t"
+        "mov.b64 ee, {e0, e1};\n\t"
+        "add.rn.f32x2 %0, %0, ee;\n\t}"
+        : "+l"(acc)
+        : "r"(w), "f"(__uint_as_float(a0)), "f"(__uint_as_float(a1)), "l"(sc2), "l"(mo2));
+}
+
 // (max, sum) of the logits z of a frontier row over every column this thread
 // consumes, each exponential one fma and one ex2 (2^(z log2(e) - m log2(e))).
 // The reference m is, where the prepared tables give it, the row's bound
@@ -405,6 +442,7 @@ struct Epi<MODE_TREE_LSE> {
     bool valid, bounded;
     int group;
     float m, s, mo;
+    uint64_t pa, pb, sc2, mo2;   // bounded bf16 path: two paired sums, (log2 e, log2 e), (-mo, -mo)
     __device__ __forceinline__ void init(const GemmParams& p, int grow) {
         const int t = grow < p.rows ? p.front_tok[grow] : -1;
         valid = t >= 0 && t < p.V;
@@ -420,12 +458,29 @@ struct Epi<MODE_TREE_LSE> {
             }
         }
         mo = m * kLog2e;
+        pa = pb = 0;   // the bits of (0.f, 0.f)
+        sc2 = f2_pack(kLog2e, kLog2e);
+        mo2 = f2_pack(-mo, -mo);
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lrow, int vbase,
-                                            int g, const uint32_t (&acc)[C]) {
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t* sl, uint32_t lbb, int lf, int lrow,
+                                            int vbase, int g, const uint32_t (&acc)[C]) {
         if (!valid || vbase >= p.V) return;
+        if (bounded && !lf && vbase + C <= p.V) {
+            // the common case (fixed reference, bf16 L, no vocabulary tail):
+            // the 16 L values of row lrow, column group g, two per 32-bit word
+            const uint8_t* rowp = sl + lrow * 128;
+#pragma unroll
+            for (int c = 0; c < C / 8; ++c) {
+                const uint4 v = *reinterpret_cast<const uint4*>(rowp + (((g * (C / 8) + c) ^ (lrow & 7)) << 4));
+                lse2_bf16(v.x, acc[c * 8 + 0], acc[c * 8 + 1], sc2, mo2, pa);
+                lse2_bf16(v.y, acc[c * 8 + 2], acc[c * 8 + 3], sc2, mo2, pb);
+                lse2_bf16(v.z, acc[c * 8 + 4], acc[c * 8 + 5], sc2, mo2, pa);
+                lse2_bf16(v.w, acc[c * 8 + 6], acc[c * 8 + 7], sc2, mo2, pb);
+            }
+            return;
+        }
         float z[C];
-        load_l(sl, lbb, p.l_fp32, lrow / p.P, g, z);
+        load_l(sl, lbb, lf, lrow, g, z);   // lrow: the request's L row
 #pragma unroll
         for (int j = 0; j < C; ++j) z[j] = z[j] + __uint_as_float(acc[j]);   // fp32(L) + Markov, one rounding
         mask_tail(z, vbase, p.V);
@@ -442,8 +497,13 @@ struct Epi<MODE_TREE_LSE> {
         for (int j = 0; j < C; ++j) ps[j & 3] += fast_exp2(fmaf(z[j], kLog2e, -mo));   // 2^-inf = 0 on the tail
         s += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     }
-    // this thread's (m, s): (-inf, 0) when it consumed nothing
-    __device__ __forceinline__ float2 partial() const { return make_float2(s > 0.f ? m : -INFINITY, s); }
+    // this thread's (m, s): (-inf, 0) when it consumed nothing (the paired
+    // sums share the fixed reference m with s)
+    __device__ __forceinline__ float2 partial() const {
+        const float2 a = f2_unpack(pa), b = f2_unpack(pb);
+        const float t = s + ((a.x + a.y) + (b.x + b.y));
+        return make_float2(t > 0.f ? m : -INFINITY, t);
+    }
     __device__ __forceinline__ void flush(const GemmParams& p, int grow) {
         if (valid) *part_slot(p, grow, group) = partial();
     }
@@ -508,7 +568,7 @@ struct Epi<MODE_TVMIN> {
             lse_p = p.res_lse_p[grow];
         }
     }
-    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int vbase, int,
+    __device__ __forceinline__ void consume(const GemmParams& p, const uint8_t*, uint32_t, int, int, int vbase, int,
                                             const uint32_t (&acc)[C]) {
         if (!valid || vbase >= p.V) return;
         float lv[C], tv[C];
@@ -627,7 +687,7 @@ struct Epi<MODE_ABSMAX> {
     }
     // Columns past V hold 0 (the W tile's out-of-range fill), which never
     // raises a maximum of absolute values.
-    __device__ __forceinline__ void consume(const GemmParams&, const uint8_t*, uint32_t, int, int, int,
+    __device__ __forceinline__ void consume(const GemmParams&, const uint8_t*, uint32_t, int, int, int, int,
                                             const uint32_t (&acc)[C]) {
         float t[C / 2];
 #pragma unroll
@@ -672,11 +732,12 @@ __device__ __forceinline__ void issue_l_box(const CUtensorMap& tmL, uint8_t* sme
     if (p.l_fp32) tma_load_3d(sl + lay.l_box_bytes, &tmL, &lfull[t], vb + 32, p.d - 1, lrow0, pol);
 }
 
-// MS = 128-row sub-tiles of GEMM rows per CTA.  MS = 2 (PCTree levels of
+// MS = 128-row sub-tiles of GEMM rows per CTA; LF = the L dtype (0 bf16, 1
+// fp32) where the mode stages L in shared memory, -1 (read from p) otherwise.  MS = 2 (PCTree levels of
 // more than 128 frontier rows): both sub-tiles' A rows sit in tensor memory
 // and every W tile feeds both, one accumulator per sub-tile, the epilogue of
 // one sub-tile overlapping the MMAs of the other; the W stream per row halves.
-template <int MODE, int MS>
+template <int MODE, int MS, int LF>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     markov_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmL,
                        const GemmParams p) {
@@ -690,9 +751,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     uint64_t* wdone = wfull + SW;   // per tile slot: the slot's last tile has completed
     uint64_t* lfull = wdone + SW;
     uint64_t* lempty = lfull + SL;
+    constexpr int NACC = 2;   // accumulators: one per sub-tile, or two used in turn
     uint64_t* tfull = lempty + SL;
-    uint64_t* tempty = tfull + 2;
-    uint64_t* a_done = tempty + 2;
+    uint64_t* tempty = tfull + NACC;
+    uint64_t* a_done = tempty + NACC;
     uint64_t* drain = a_done + 1;   // the MMA warp's own tensor-core work, before tensor memory is freed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     int* s_rowtok = reinterpret_cast<int*>(smem + lay.tok_off);   // [kTileM * MS]
@@ -718,7 +780,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&lfull[s], 1);
             mbar_init(&lempty[s], kEpiWarps);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NACC; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], kEpiWarps);
         }
@@ -831,26 +893,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mma_commit_warp(a_done);   // the A stages may be loaded once the copy has read them
         const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem), kWBoxBytes, 1024);
         bool ok = true;
-        for (int i = 0; i < nt && ok; ++i) {
-            const int slot = i % NTS;
-            const uint32_t par = static_cast<uint32_t>(i / NTS) & 1u;
-            for (int h = 0; h < MS && ok; ++h) {
-                // accumulator b (one of two in turn, or sub-tile h's own) and
-                // its use count
-                const int b = MS == 1 ? (i & 1) : h;
-                const int use = MS == 1 ? (i >> 1) : i;
+        if constexpr (MS == 2) {
+            // one 128 x 128 accumulator per sub-tile: each W stage feeds both
+            // sub-tiles' MMAs, the epilogue of one sub-tile overlapping the
+            // MMAs of the other (four 128 x 64 accumulators, which let the
+            // MMAs run further ahead, measured slower)
+            for (int i = 0; i < nt && ok; ++i) {
+                const int slot = i % NTS;
+                const uint32_t par = static_cast<uint32_t>(i / NTS) & 1u;
+                for (int h = 0; h < MS && ok; ++h) {
+                    if (i >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[h], (i - 1) & 1, lim));
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(h * kTileN);
+                    const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA + h * (p.r >> 1));
+                    for (int kb = 0; kb < KB; ++kb) {
+                        const int s = slot * KB + kb;
+                        if (h == 0) {   // the second sub-tile reuses the stages the first waited for
+                            ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par, lim));
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint64_t bd0 =
+                            b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            mma_bf16_ts_warp(d_tmem, a_tmem + static_cast<uint32_t>((kb * 4 + j) * 8),
+                                             bd0 + static_cast<uint64_t>(j * (2048 >> 4)), idesc, (kb | j) ? 1u : 0u);
+                    }
+                    if (ok) mma_commit_warp(&tfull[h]);
+                }
+            }
+        } else {
+            // two 128 x 128 accumulators, used in turn
+            for (int i = 0; i < nt && ok; ++i) {
+                const int slot = i % NTS;
+                const uint32_t par = static_cast<uint32_t>(i / NTS) & 1u;
+                const int b = i & 1, use = i >> 1;
                 if (use >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&tempty[b], (use - 1) & 1, lim));
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(b * kTileN);
-                const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA + h * (p.r >> 1));
+                const uint32_t a_tmem = tmem_base + static_cast<uint32_t>(kTmemA);
                 for (int kb = 0; kb < KB; ++kb) {
                     const int s = slot * KB + kb;
-                    if (h == 0) {   // the later sub-tiles reuse the stages the first waited for
-                        ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par, lim));
-                        if (!ok) break;
-                        tc_fence_after();
-                    }
+                    ok = __all_sync(0xffffffffu, mbar_wait(&wfull[s], par, lim));
+                    if (!ok) break;
+                    tc_fence_after();
                     const uint64_t bd0 = b_desc0 + static_cast<uint64_t>((static_cast<uint32_t>(s) * kWStageBytes) >> 4);
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
@@ -903,6 +992,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             sts[h].group = g;
         }
         Epi<MODE>& st = sts[0];
+        // the L row of each sub-tile's row in the staged L boxes (PCTree: one
+        // per request, shared by its P frontier rows) and the L dtype
+        int lr[MS];
+#pragma unroll
+        for (int h = 0; h < MS; ++h) lr[h] = mode_tree(MODE) ? (lrow + h * kTileM) / p.P : lrow + h * kTileM;
+        const int lf = LF >= 0 ? LF : p.l_fp32;
         const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
         int t = 0, lap = 0;   // L ring slot and wraps
         for (int i = 0; i < nt; ++i) {
@@ -939,43 +1034,68 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const int ts[2] = {t0, t1}, laps[2] = {lap0, lap1};
             const int v0 = (static_cast<int>(blockIdx.x) + i * static_cast<int>(gridDim.x)) * kTileN;
             bool ok = true;
+            if constexpr (MS == 2) {
+                // sub-tile h's accumulator: both 16-column slices into
+                // registers, handed back to the MMA warp before the arithmetic
 #pragma unroll
-            for (int h = 0; h < MS; ++h) {
-                const int ab = MS == 1 ? b : h;                 // accumulator
-                const int use = MS == 1 ? (i >> 1) : i;          // its use count
-                ok = mbar_wait(&tfull[ab], use & 1, lim);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                // the tile's W stages are free once its last sub-tile's MMAs are done
-                if (h == MS - 1 && warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);
-                tc_fence_after();
-                // both 16-column slices of the tile into registers, then the
-                // accumulator goes back to the MMA warp before any arithmetic
-                uint32_t acc[2][C];
-                tmem_ld16(lane_addr + static_cast<uint32_t>(ab * kTileN + g * C), acc[0]);
-                tmem_ld16(lane_addr + static_cast<uint32_t>(ab * kTileN + kBoxN + g * C), acc[1]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[ab]);
+                for (int h = 0; h < MS; ++h) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&tfull[h], i & 1, lim));
+                    if (!ok) break;
+                    // the tile's W stages are free once its last sub-tile's MMAs are done
+                    if (h == MS - 1 && warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);
+                    tc_fence_after();
+                    uint32_t acc[2][C];
+                    tmem_ld16(lane_addr + static_cast<uint32_t>(h * kTileN + g * C), acc[0]);
+                    tmem_ld16(lane_addr + static_cast<uint32_t>(h * kTileN + kBoxN + g * C), acc[1]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[h]);
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (mode_reads_l(MODE) && h == 0) {
-                        bool lok = mbar_wait(&lfull[ts[hh]], laps[hh] & 1, lim);
-                        lok = __all_sync(0xffffffffu, lok);
-                        if (!lok) {
-                            ok = false;
-                            break;
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (mode_reads_l(MODE) && h == 0) {
+                            ok = __all_sync(0xffffffffu, mbar_wait(&lfull[ts[hh]], laps[hh] & 1, lim));
+                            if (!ok) break;
+                        }
+                        const uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(ts[hh]) * lay.l_stage_bytes;
+                        sts[h].consume(p, sl, lay.l_box_bytes, lf, lr[h], v0 + hh * kBoxN + g * C, g, acc[hh]);
+                        if (mode_reads_l(MODE) && h == MS - 1) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&lempty[ts[hh]]);
                         }
                     }
-                    const uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(ts[hh]) * lay.l_stage_bytes;
-                    sts[h].consume(p, sl, lay.l_box_bytes, lrow + h * kTileM, v0 + hh * kBoxN + g * C, g, acc[hh]);
-                    if (mode_reads_l(MODE) && h == MS - 1) {
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&lempty[ts[hh]]);
+                    if (!ok) break;
+                }
+            } else {
+                ok = __all_sync(0xffffffffu, mbar_wait(&tfull[b], (i >> 1) & 1, lim));
+                if (ok) {
+                    // the tile's W stages are free once its MMAs are done
+                    if (warp == 3 && lane == 0) mbar_arrive(&wdone[i % NTS]);
+                    tc_fence_after();
+                    // both 16-column slices of the tile into registers, then
+                    // the accumulator goes back to the MMA warp before any
+                    // arithmetic
+                    uint32_t acc[2][C];
+                    tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + g * C), acc[0]);
+                    tmem_ld16(lane_addr + static_cast<uint32_t>(b * kTileN + kBoxN + g * C), acc[1]);
+                    tmem_ld_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[b]);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (mode_reads_l(MODE)) {
+                            ok = __all_sync(0xffffffffu, mbar_wait(&lfull[ts[hh]], laps[hh] & 1, lim));
+                            if (!ok) break;
+                        }
+                        const uint8_t* sl = smem + lay.l_off + static_cast<uint32_t>(ts[hh]) * lay.l_stage_bytes;
+                        st.consume(p, sl, lay.l_box_bytes, lf, lr[0], v0 + hh * kBoxN + g * C, g, acc[hh]);
+                        if (mode_reads_l(MODE)) {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&lempty[ts[hh]]);
+                        }
                     }
                 }
-                if (!ok) break;
             }
             if (mode_reads_l(MODE)) {
                 t = (t1 + 1 == SL) ? 0 : t1 + 1;
@@ -1026,7 +1146,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
-template <int MODE, int MS = 1>
+template <int MODE, int MS = 1, int LF = -1>
 cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p, int gx, int gy,
                         cudaStream_t s) {
     const SmemLayout lay = make_layout(p.r, p.l_rows, p.l_fp32, p.w_stages, p.l_stages, MODE, MS);
@@ -1034,12 +1154,12 @@ cudaError_t launch_mode(const CUtensorMap& tmW, const CUtensorMap& tmL, const Ge
     if (lay.total > static_cast<uint32_t>(kSmemLimit) || p.w_stages < 2 * (p.r >> 6)) return cudaErrorInvalidValue;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE, MS>,
+        cudaError_t e = cudaFuncSetAttribute(markov_gemm_kernel<MODE, MS, LF>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    return launch_pdl(markov_gemm_kernel<MODE, MS>, dim3(gx, gy), dim3(kGemmThreads), lay.total, s, tmW, tmL, p);
+    return launch_pdl(markov_gemm_kernel<MODE, MS, LF>, dim3(gx, gy), dim3(kGemmThreads), lay.total, s, tmW, tmL, p);
 }
 
 }  // namespace
@@ -1065,9 +1185,16 @@ void gemm_pick_stages(GemmParams& p, int mode) {
 cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorMap& tmL, const GemmParams& p,
                                int grid_x, int grid_y, cudaStream_t s) {
     switch (mode) {
-        case MODE_CHAIN_GREEDY: return launch_mode<MODE_CHAIN_GREEDY>(tmW, tmL, p, grid_x, grid_y, s);
-        case MODE_CHAIN_SAMPLE: return launch_mode<MODE_CHAIN_SAMPLE>(tmW, tmL, p, grid_x, grid_y, s);
-        case MODE_TREE: return launch_mode<MODE_TREE>(tmW, tmL, p, grid_x, grid_y, s);
+        // the modes that stage L in shared memory: one kernel per L dtype
+        case MODE_CHAIN_GREEDY:
+            return p.l_fp32 ? launch_mode<MODE_CHAIN_GREEDY, 1, 1>(tmW, tmL, p, grid_x, grid_y, s)
+                            : launch_mode<MODE_CHAIN_GREEDY, 1, 0>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_CHAIN_SAMPLE:
+            return p.l_fp32 ? launch_mode<MODE_CHAIN_SAMPLE, 1, 1>(tmW, tmL, p, grid_x, grid_y, s)
+                            : launch_mode<MODE_CHAIN_SAMPLE, 1, 0>(tmW, tmL, p, grid_x, grid_y, s);
+        case MODE_TREE:
+            return p.l_fp32 ? launch_mode<MODE_TREE, 1, 1>(tmW, tmL, p, grid_x, grid_y, s)
+                            : launch_mode<MODE_TREE, 1, 0>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_RESID: return launch_mode<MODE_RESID>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_ABSMAX: return launch_mode<MODE_ABSMAX>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_QLSE: return launch_mode<MODE_QLSE>(tmW, tmL, p, grid_x, grid_y, s);
@@ -1075,8 +1202,11 @@ cudaError_t launch_markov_gemm(int mode, const CUtensorMap& tmW, const CUtensorM
         case MODE_TVMIN_B16: return launch_mode<MODE_TVMIN_B16>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TVMIN_B32: return launch_mode<MODE_TVMIN_B32>(tmW, tmL, p, grid_x, grid_y, s);
         case MODE_TREE_LSE:
-            return p.m_sub == 2 ? launch_mode<MODE_TREE_LSE, 2>(tmW, tmL, p, grid_x, grid_y, s)
-                                : launch_mode<MODE_TREE_LSE, 1>(tmW, tmL, p, grid_x, grid_y, s);
+            if (p.m_sub == 2)
+                return p.l_fp32 ? launch_mode<MODE_TREE_LSE, 2, 1>(tmW, tmL, p, grid_x, grid_y, s)
+                                : launch_mode<MODE_TREE_LSE, 2, 0>(tmW, tmL, p, grid_x, grid_y, s);
+            return p.l_fp32 ? launch_mode<MODE_TREE_LSE, 1, 1>(tmW, tmL, p, grid_x, grid_y, s)
+                            : launch_mode<MODE_TREE_LSE, 1, 0>(tmW, tmL, p, grid_x, grid_y, s);
         default: return cudaErrorInvalidValue;
     }
 }

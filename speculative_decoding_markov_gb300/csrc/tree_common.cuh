@@ -32,11 +32,21 @@ __device__ __forceinline__ void tree_keep_children(int i, int P, int B, int d, i
                                                    int32_t* front_node, float* front_score, int32_t* n_front,
                                                    int32_t* pool_tok, int32_t* pool_parent, int32_t* pool_depth,
                                                    float* pool_score, int32_t* pool_n) {
-    for (int t = threadIdx.x; t < nc; t += blockDim.x) {
-        const Cand me = cand[t];
+    // a child's rank = the children before it, four threads per child each
+    // counting a quarter (blockDim is a multiple of 32: every lane of a warp
+    // runs each round)
+    for (int t0 = 0; t0 < 4 * nc; t0 += blockDim.x) {
+        const int t = t0 + static_cast<int>(threadIdx.x);
+        const int c = t >> 2;
         int rk = 0;
-        for (int u = 0; u < nc; ++u) rk += cand_before(cand[u], me) ? 1 : 0;
-        sorted[rk] = me;
+        Cand me{};
+        if (c < nc) {
+            me = cand[c];
+            for (int u = t & 3; u < nc; u += 4) rk += cand_before(cand[u], me) ? 1 : 0;
+        }
+        rk += __shfl_xor_sync(0xffffffffu, rk, 1);
+        rk += __shfl_xor_sync(0xffffffffu, rk, 2);
+        if (c < nc && (t & 3) == 0) sorted[rk] = me;
     }
     __syncthreads();
     const int keep = nc < P ? nc : P;

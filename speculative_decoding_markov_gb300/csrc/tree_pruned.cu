@@ -71,6 +71,27 @@ __device__ __forceinline__ float dot_rows(const uint16_t* a, const uint16_t* b, 
     return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
+// Warp-wide tensor-core step for the level's dots: D[16 x 8] += A[16 x 16] B,
+// A = 16 W^T rows (ids x K, K contiguous), B = 8 U rows (parents x K, K
+// contiguous): bf16 in, fp32 accumulate.  Fragments by ldmatrix from rows
+// 16-byte aligned; lane l addresses A row (l % 16), K offset 8 (l / 16), and
+// B row (l % 8), K offset 8 ((l / 8) % 2).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&a)[4], const uint16_t* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&b)[2], const uint16_t* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(b[0]), "=r"(b[1]) : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void mma_16816_bf16(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v, unsigned long long* red) {
     v = warp_max_u64(v);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -326,24 +347,55 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
     __syncthreads();
 
     if (!exhaust) {
-        // 2. z for every (parent, id) pair: fp32(L) + U[y] . W^T[v]
-        for (int t = tid; t < nf * nk; t += kLvThreads) {
-            const int f = t / nk, j = t - f * nk;
-            if (j < s_cnt[f])
-                s_z[f * kTreeKeep + j] = __uint_as_float(s_keep[j].y) +
-                                         dot_rows(s_u + static_cast<size_t>(f) * RS, s_w + static_cast<size_t>(j) * RS, r);
+        // 2. z for every (parent, id) pair: fp32(L) + U[y] . W^T[v], one warp
+        //    per 16 ids x 8 parents on the tensor cores (m16n8k16); rows past
+        //    the staged ids or parents give values nobody reads
+        int nmax = 0;
+        for (int f = 0; f < nf; ++f) nmax = max(nmax, s_cnt[f]);
+        const int nb16 = (nmax + 15) >> 4, nb8 = (nf + 7) >> 3;
+        for (int tb = warp; tb < nb16 * nb8; tb += kLvWarps) {
+            const int jb = (tb % nb16) * 16, fb = (tb / nb16) * 8;
+            const uint16_t* arow = s_w + static_cast<size_t>(jb + (lane & 15)) * RS + ((lane >> 4) << 3);
+            const uint16_t* brow = s_u + static_cast<size_t>(min(fb + (lane & 7), P - 1)) * RS + (((lane >> 3) & 1) << 3);
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k0 = 0; k0 < r; k0 += 16) {
+                uint32_t a[4], b[2];
+                ldsm_x4(a, arow + k0);
+                ldsm_x2(b, brow + k0);
+                mma_16816_bf16(d, a, b);
+            }
+            // lane (g, t) = (lane / 4, lane % 4) holds ids jb + g, jb + g + 8
+            // and parents fb + 2 t, fb + 2 t + 1
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = jb + (lane >> 2) + (e >> 1) * 8, f = fb + 2 * (lane & 3) + (e & 1);
+                if (f < nf && j < s_cnt[f]) s_z[f * kTreeKeep + j] = __uint_as_float(s_keep[j].y) + d[e];
+            }
         }
         __syncthreads();
-        // each parent's top k by (z desc, id asc)
-        for (int t = tid; t < nf * nk; t += kLvThreads) {
-            const int f = t / nk, j = t - f * nk;
+        // each parent's top k by (z desc, id asc): one warp per parent, k
+        // rounds of the warp's largest remaining key (keys are distinct: the
+        // ids differ)
+        for (int f = warp; f < nf; f += kLvWarps) {
             const int n = s_cnt[f];
-            if (j >= n) continue;
-            const unsigned long long me = argmax_key(s_z[f * kTreeKeep + j], s_keep[j].x);
-            int rk = 0;
-            for (int u = 0; u < n && rk < K; ++u)
-                rk += argmax_key(s_z[f * kTreeKeep + u], s_keep[u].x) > me ? 1 : 0;
-            if (rk < K) s_top[f][rk] = make_float2(s_z[f * kTreeKeep + j], __int_as_float(static_cast<int>(s_keep[j].x)));
+            unsigned long long key[kTreeKeep / 32];
+#pragma unroll
+            for (int e = 0; e < kTreeKeep / 32; ++e) {
+                const int j = lane + 32 * e;
+                key[e] = j < n ? argmax_key(s_z[f * kTreeKeep + j], s_keep[j].x) : 0ull;
+            }
+            for (int q = 0; q < K; ++q) {
+                unsigned long long best = 0ull;
+#pragma unroll
+                for (int e = 0; e < kTreeKeep / 32; ++e) best = umax64(best, key[e]);
+                const unsigned long long m = warp_max_u64(best);
+#pragma unroll
+                for (int e = 0; e < kTreeKeep / 32; ++e)
+                    if (key[e] == m) key[e] = 0ull;
+                if (lane == 0)
+                    s_top[f][q] = m ? make_float2(key_value(m), __int_as_float(static_cast<int>(key_token(m))))
+                                    : make_float2(-INFINITY, __int_as_float(-1));
+            }
         }
     } else {
         // every id of the vocabulary for every parent, W^T rows from global
