@@ -258,54 +258,66 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int P = p.P, K = p.k, r = p.r;
     const int row = i * p.B + (p.d - 1);
-    // 0. before the wait on the level's GEMM: the row's ids (made once per
-    //    cycle, before the first level) and the copies of their W^T rows
-    //    (read through L2: written by an earlier kernel than the one this
-    //    launch waits for)
+    // 0. before the wait on the level's GEMM, everything but its partials:
+    //    the row's ids (made once per cycle, before the first level) and the
+    //    copies of their W^T rows; the frontier and the pool's size, written
+    //    by the previous level's kernel (complete before the GEMM passed its
+    //    own wait, and this launch begins only after every GEMM CTA did), the
+    //    parents' U rows, bounds and id counts.  Loads through L2.
     if (tid == 0) {
         s_nk = __ldcg(p.n_keep + row);
         s_lk = __ldcg(p.lk + row);
+        s_nf = min(max(__ldcg(p.n_front + i), 0), P);
+        s_np = __ldcg(p.pool_n + i);
     }
     for (int t = tid; t < kTreeKeep; t += kLvThreads) s_keep[t] = __ldcg(p.keep + static_cast<size_t>(row) * kTreeKeep + t);
+    for (int f = tid; f < P; f += kLvThreads) {
+        const size_t fr = static_cast<size_t>(i) * P + f;
+        s_tok[f] = __ldcg(p.front_tok + fr);
+        s_node[f] = __ldcg(p.front_node + fr);
+        s_score[f] = __ldcg(p.front_score + fr);
+    }
     __syncthreads();
-    const int nk = s_nk;
+    const int nk = s_nk, nf = s_nf;
     const bool exhaust = nk < 0;
     if (!exhaust)
         for (int j = warp; j < nk; j += kLvWarps) {
             const uint16_t* src = p.Wt + static_cast<size_t>(s_keep[j].x) * r;
             for (int q = lane * 8; q < r; q += 256) cp_async_16(s_w + static_cast<size_t>(j) * RS + q, src + q, 16u);
         }
-    pdl_wait();
-    pdl_trigger();
-    // 1. one round of independent loads: the frontier and the pool's size
-    if (tid == 0) {
-        s_nf = min(max(p.n_front[i], 0), P);
-        s_np = p.pool_n[i];
-    }
-    for (int f = tid; f < P; f += kLvThreads) {
-        const size_t fr = static_cast<size_t>(i) * P + f;
-        s_tok[f] = p.front_tok[fr];
-        s_node[f] = p.front_node[fr];
-        s_score[f] = p.front_score[fr];
-    }
-    __syncthreads();
-    const int nf = s_nf;
-    // 2. one more round, every load independent of the others: the parents'
-    //    U rows (copies into shared memory), each parent's bound c(y) and the
-    //    GEMM's partials of its row (registers)
     for (int f = warp; f < nf; f += kLvWarps) {
         const int t = s_tok[f];
         if (t >= 0 && t < p.V)
             for (int q = lane * 8; q < r; q += 256)
                 cp_async_16(s_u + static_cast<size_t>(f) * RS + q, p.U + static_cast<size_t>(t) * r + q, 16u);
     }
+    // each parent's ids: the prefix of the row's list with L >= L_(k) - 2 c(y)
     for (int f = warp; f < nf; f += kLvWarps) {
         int t = s_tok[f];
         if (t >= p.V) {
             if (lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
             t = -1;
         }
-        const float cy = (t >= 0 && !exhaust) ? p.c_bound[t] : 0.f;
+        int n = 0;
+        if (t >= 0 && !exhaust) {
+            const float thr = markov_cut(s_lk, p.c_bound[t]);
+            for (int j0 = 0; j0 < nk; j0 += 32) {
+                const int j = j0 + lane;
+                n += __popc(__ballot_sync(0xffffffffu, j < nk && __uint_as_float(s_keep[j].y) >= thr));
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            s_cnt[f] = n;
+            if (t < 0) s_tok[f] = -1;
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+    // 1. the log-sum-exp of each parent's logits from the GEMM's partials:
+    //    the largest maximum, then every partial's sum rescaled to it, summed
+    //    in fp32 (a lane's terms, then the butterfly)
+    for (int f = warp; f < nf; f += kLvWarps) {
         const float2* pr = p.part + (static_cast<size_t>(i) * P + f) * p.n_part;
         float2 x[kMaxPartLane];
 #pragma unroll
@@ -313,9 +325,6 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
             const int q = lane + e * 32;
             x[e] = q < p.n_part ? pr[q] : make_float2(-INFINITY, 0.f);
         }
-        // lse of the parent's logits: the largest maximum, then every
-        // partial's sum rescaled to it, summed in fp32 (a lane's terms, then
-        // the butterfly)
         float m = -INFINITY;
 #pragma unroll
         for (int e = 0; e < kMaxPartLane; ++e)
@@ -328,20 +337,7 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
             if (x[e].y > 0.f) sum += x[e].y * expf(x[e].x - m);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-        // the parent's ids: the prefix with L >= L_(k) - 2 c(y)
-        int n = 0;
-        if (t >= 0 && !exhaust) {
-            const float thr = markov_cut(s_lk, cy);
-            for (int j0 = 0; j0 < nk; j0 += 32) {
-                const int j = j0 + lane;
-                n += __popc(__ballot_sync(0xffffffffu, j < nk && __uint_as_float(s_keep[j].y) >= thr));
-            }
-        }
-        if (lane == 0) {
-            s_lse[f] = m + logf(sum);
-            s_cnt[f] = n;
-            if (t < 0) s_tok[f] = -1;
-        }
+        if (lane == 0) s_lse[f] = m + logf(sum);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -357,13 +353,20 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
             const int jb = (tb % nb16) * 16, fb = (tb / nb16) * 8;
             const uint16_t* arow = s_w + static_cast<size_t>(jb + (lane & 15)) * RS + ((lane >> 4) << 3);
             const uint16_t* brow = s_u + static_cast<size_t>(min(fb + (lane & 7), P - 1)) * RS + (((lane >> 3) & 1) << 3);
-            float d[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int k0 = 0; k0 < r; k0 += 16) {
-                uint32_t a[4], b[2];
+            // two accumulators over alternate K steps (r / 16 is even): half
+            // the dependent chain
+            float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int k0 = 0; k0 < r; k0 += 32) {
+                uint32_t a[4], b[2], a2[4], b2[2];
                 ldsm_x4(a, arow + k0);
                 ldsm_x2(b, brow + k0);
+                ldsm_x4(a2, arow + k0 + 16);
+                ldsm_x2(b2, brow + k0 + 16);
                 mma_16816_bf16(d, a, b);
+                mma_16816_bf16(d2, a2, b2);
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d[e] += d2[e];
             // lane (g, t) = (lane / 4, lane % 4) holds ids jb + g, jb + g + 8
             // and parents fb + 2 t, fb + 2 t + 1
 #pragma unroll
@@ -388,7 +391,12 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
                 unsigned long long best = 0ull;
 #pragma unroll
                 for (int e = 0; e < kTreeKeep / 32; ++e) best = umax64(best, key[e]);
-                const unsigned long long m = warp_max_u64(best);
+                // the warp's largest key: its high word, then the low word
+                // among the lanes that hold that high word
+                const uint32_t hi = __reduce_max_sync(0xffffffffu, static_cast<uint32_t>(best >> 32));
+                const uint32_t lo = __reduce_max_sync(
+                    0xffffffffu, static_cast<uint32_t>(best >> 32) == hi ? static_cast<uint32_t>(best) : 0u);
+                const unsigned long long m = (static_cast<unsigned long long>(hi) << 32) | lo;
 #pragma unroll
                 for (int e = 0; e < kTreeKeep / 32; ++e)
                     if (key[e] == m) key[e] = 0ull;
@@ -433,11 +441,18 @@ __global__ void __launch_bounds__(kLvThreads, 1) tree_level_kernel(const TreeLev
         }
     }
     __syncthreads();
-    // 3. children s = s(p) + (z - lse(p)), the P best kept
+    // 3. children s = s(p) + (z - lse(p)), the P best kept; every child's U
+    //    row is asked into L2 for the next level's GEMM, which gathers the
+    //    kept ones
     const int ncand = nf * K;
     for (int t = tid; t < ncand; t += kLvThreads) {
         const int f = t / K, q = t - f * K;
         const float2 e = s_top[f][q];
+        const int ct = __float_as_int(e.y);
+        if (s_tok[f] >= 0 && ct >= 0 && ct < p.V)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.U + static_cast<size_t>(ct) * r),
+                         "r"(r * 2)
+                         : "memory");
         s_cand[t] = s_tok[f] >= 0 ? Cand{s_score[f] + (e.x - s_lse[f]), f, q, __float_as_int(e.y)}
                                   : Cand{-INFINITY, f, q, -1};
     }
