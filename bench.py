@@ -39,6 +39,15 @@ FLUSH_BYTES = 256 << 20
 OTHER_WORKLOADS = ("tiny_chain", "rejection_sampling", "pctree", "mixed_traffic")
 
 
+def status_bits(status):
+    """Names of the device status bits set (the informational tier bit included)."""
+    from speculative_decoding_markov_gb300 import binding as sdm
+    names = {sdm.DEV_BAD_TOKEN: "bad_token", sdm.DEV_TIER_UNCAPTURED: "tier_uncaptured (informational)",
+             sdm.DEV_TIMEOUT: "timeout", sdm.DEV_BAD_WINDOW: "bad_window", sdm.DEV_CAPACITY: "capacity",
+             sdm.DEV_BAD_CLASS: "bad_class", sdm.DEV_TIER_OVERFLOW: "tier_overflow"}
+    return [n for b, n in names.items() if status & b]
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -627,10 +636,11 @@ def run_ours(args, w, world, rank, local):
                      "traffic_unit": "DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      **extra,
                      "algorithmic": {"draft_per_launch": draft_alg, "draft_launches_per_cycle": draft_launches,
-                                     "draft_unit": "byte",
+                                     "draft_unit": "flop" if bound == "tensor" else "byte",
                                      "verify_bytes_per_cycle": verify_bytes, "L_bytes_per_cycle": draft_bytes}},
         "gpu_launches": cyc.launches_per_step() * args.steps,
         "device_status": status,
+        "device_status_bits": status_bits(status),
         "clocks": clk,
     }
     if e2e is not None:

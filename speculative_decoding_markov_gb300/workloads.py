@@ -16,7 +16,8 @@ Readings fixed here (the pages leave them open):
   * The target LLM is replaced by T_d(prev) = L_d + U[prev] W + eta_d, i.e.
     "draft logits plus noise" along any drafted prefix.
   * Seed 0 everywhere; the additive table 2.0 + 0.004 N (ms) and the tiers
-    {64, ..., 2048} are reused where a workload names none.
+    {64, ..., 2048} are reused where a workload names none (the two batches
+    of 256 requests add 4096 and 8192, so that their totals fall in a tier).
 """
 from __future__ import annotations
 
@@ -26,6 +27,8 @@ BF16 = 0
 FP32 = 1
 
 TIERS = (64, 128, 256, 512, 1024, 2048)
+# batches of 256 requests verify up to 256 (gamma + 1) rows: two more tiers
+TIERS_LARGE = TIERS + (4096, 8192)
 
 
 @dataclass(frozen=True)
@@ -64,7 +67,7 @@ WORKLOADS = {
     "rejection_sampling": Workload(
         name="rejection_sampling", R=256, B=16, V=151936, r=256, l_dtype=BF16, l_std=2.0,
         sigma=(0.7,), target_dtype=FP32, decode="sample", modes=("static",),
-        temperature=1.0, conf="sigmoid"),
+        temperature=1.0, conf="sigmoid", tiers=TIERS_LARGE),
     "pctree": Workload(
         name="pctree", R=32, B=16, V=151936, r=256, l_dtype=BF16, l_std=2.0,
         sigma=(0.5,), target_dtype=BF16, decode="tree", modes=("tree",),
@@ -73,7 +76,7 @@ WORKLOADS = {
         name="mixed_traffic", R=256, B=8, V=129280, r=256, l_dtype=BF16, l_std=2.0,
         sigma=(0.2, 0.8, 1.5), target_dtype=BF16, decode="greedy",
         modes=("static", "compact", "cap_accept"), conf="one_minus_tv",
-        cost=(2.0, 0.004), class_mix="shuffle"),
+        cost=(2.0, 0.004), class_mix="shuffle", tiers=TIERS_LARGE),
 }
 
 # the order the workloads are listed in (the second is the headline one)
