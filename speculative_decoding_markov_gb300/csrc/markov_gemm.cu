@@ -22,6 +22,10 @@
 //                      row, CTA and column group; MODE_TVMIN_B16 / _B32 are
 //                      the same for bf16 L and bf16 / fp32 target rows with
 //                      a tile's loads issued before its accumulator is read
+//   MODE_TREE_LSE      PCTree level with the bound-pruned children: only the
+//                      log-sum-exp of each frontier row, one partial (max,
+//                      sum) per row and CTA (tree_pruned.cu scores the
+//                      children)
 //
 // Data path (one CTA = 128 GEMM rows x a round-robin set of 128-wide vocab
 // tiles, K = r):
