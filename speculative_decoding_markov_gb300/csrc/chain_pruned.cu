@@ -159,19 +159,16 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
         // it, so it is a lower bound on the chunk's k-th largest value; -inf
         // when fewer than k warps hold a value)
         float theta = mc;
-        if (p.kth > 1) {
-            theta = -INFINITY;
+        if (p.kth > 1) {   // lane w < kWarps ranks warp w's maximum
+            const float x0 = s_wmax[lane & (kWarps - 1)];
+            int gt = 0, ge = 0;
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float x0 = s_wmax[w];
-                int gt = 0, ge = 0;
-#pragma unroll
-                for (int u = 0; u < kWarps; ++u) {
-                    gt += s_wmax[u] > x0 ? 1 : 0;
-                    ge += s_wmax[u] >= x0 ? 1 : 0;
-                }
-                if (gt < p.kth && ge >= p.kth) theta = x0;
+            for (int u = 0; u < kWarps; ++u) {
+                gt += s_wmax[u] > x0 ? 1 : 0;
+                ge += s_wmax[u] >= x0 ? 1 : 0;
             }
+            const unsigned at = __ballot_sync(0xffffffffu, lane < kWarps && gt < p.kth && ge >= p.kth);
+            theta = at ? __shfl_sync(0xffffffffu, x0, __ffs(at) - 1) : -INFINITY;
         }
         const float T = threshold(theta, cmax);
         const int seg = rs * nc + c;

@@ -104,6 +104,31 @@ __device__ __forceinline__ unsigned long long block_max_u64(unsigned long long v
     return m;
 }
 
+// The warp's largest value among every lane's v[] (-inf when all are -inf),
+// one occurrence of it removed (from the lowest lane holding it); every lane
+// gets the value.
+template <int N>
+__device__ __forceinline__ float warp_take_max(float (&v)[N]) {
+    const int lane = threadIdx.x & 31;
+    float m = v[0];
+#pragma unroll
+    for (int e = 1; e < N; ++e) m = fmaxf(m, v[e]);
+    float wm = m;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+    const unsigned holders = __ballot_sync(0xffffffffu, m == wm && wm > -INFINITY);
+    if (holders && lane == __ffs(holders) - 1) {
+        bool done = false;
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            if (!done && v[e] == wm) {
+                v[e] = -INFINITY;
+                done = true;
+            }
+    }
+    return wm;
+}
+
 // ---------------------------------------------------------------------------
 // Once per cycle: the ids each (request, level) row can need
 // ---------------------------------------------------------------------------
@@ -113,6 +138,7 @@ __global__ void __launch_bounds__(kLvThreads) tree_rows_kernel(const TreeRowsPar
     __shared__ uint2 s_keep[kTreeKeep];
     __shared__ int s_nkeep, s_bad;
     __shared__ float s_lk;
+    __shared__ float s_wtop[kLvWarps][kMaxTopK];   // each warp's k largest listed values, in order
     pdl_wait();
     pdl_trigger();
     const int row = blockIdx.x;   // request * B + (level - 1)
@@ -159,18 +185,32 @@ __global__ void __launch_bounds__(kLvThreads) tree_rows_kernel(const TreeRowsPar
             s_g[t] = p.cand[static_cast<size_t>(seg0 + c) * kSegCap + (t - s_pref[c])];
         }
         __syncthreads();
-        // L_(k): the entry with fewer than k entries above it and at least k
-        // at or above it (the lists hold every chunk's top k, so the row's
-        // top k are among them)
-        for (int t = tid; t < total; t += kLvThreads) {
-            const float x = __uint_as_float(s_g[t].y);
-            int gt = 0, ge = 0;
-            for (int u = 0; u < total; ++u) {
-                const float y = __uint_as_float(s_g[u].y);
-                gt += y > x ? 1 : 0;
-                ge += y >= x ? 1 : 0;
+        // L_(k), the k-th largest listed value counted with multiplicity (the
+        // lists hold every chunk's top k, so the row's top k are among
+        // them): k rounds per warp of taking its largest remaining value
+        // (one occurrence), then the same over the warps' k values
+        constexpr int kPer = kGather / kLvThreads;
+        float v[kPer];
+#pragma unroll
+        for (int e = 0; e < kPer; ++e) {
+            const int t = tid + e * kLvThreads;
+            v[e] = t < total ? __uint_as_float(s_g[t].y) : -INFINITY;
+        }
+        for (int q = 0; q < K; ++q) {
+            const float top = warp_take_max<kPer>(v);
+            if (lane == 0) s_wtop[warp][q] = top;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float w2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = lane + 32 * e;   // (warp t / k, rank t % k) of the warps' lists
+                w2[e] = t < kLvWarps * K ? s_wtop[t / K][t % K] : -INFINITY;
             }
-            if (gt < K && ge >= K) s_lk = x;   // one value, whoever writes it
+            float top = -INFINITY;
+            for (int q = 0; q < K; ++q) top = warp_take_max<2>(w2);
+            if (lane == 0) s_lk = top;   // -inf when fewer than k values are listed
         }
         __syncthreads();
         const float lk = s_lk;
