@@ -658,13 +658,14 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
                                      const int32_t* pool_depth, const float* pool_score, const int32_t* pool_n,
                                      int32_t* tok, int32_t* parent, int32_t* depth, float* score, uint32_t* mask,
                                      int32_t* n_nodes) {
-    extern __shared__ int tf_smem[];
+    extern __shared__ unsigned long long tf_smem[];
     const int pool_cap = 1 + P * B;
-    int* slot_of = tf_smem;               // pool index -> output slot (-1: not selected)
+    unsigned long long* s_key = tf_smem;   // pool rank keys: larger = earlier in the output order
+    int* slot_of = reinterpret_cast<int*>(s_key + pool_cap);   // pool index -> output slot (-1: not selected)
     int* node_at = slot_of + pool_cap;    // output slot -> pool index
     int* s_par = node_at + (N + 1);       // pool parents
-    int* s_dep = s_par + pool_cap;        // pool depths
-    float* s_sc = reinterpret_cast<float*>(s_dep + pool_cap);   // pool scores
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x;
     const size_t pb = static_cast<size_t>(i) * pool_cap;
     const int np = pool_n[i];
@@ -674,23 +675,30 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
         slot_of[j] = -1;
         if (j < np) {
             s_par[j] = pool_parent[pb + j];
-            s_dep[j] = pool_depth[pb + j];
-            s_sc[j] = pool_score[pb + j];
+            // (score desc, depth asc, creation asc) as one key; scores through
+            // their order-preserving bits, a strict total order even for NaN
+            // (depth <= B < 2^15, creation < 2^16); depth and score are read
+            // back from the key
+            s_key[j] = (static_cast<unsigned long long>(ordered_bits(pool_score[pb + j])) << 32) |
+                       (static_cast<unsigned long long>(0x7fffu - static_cast<uint32_t>(pool_depth[pb + j])) << 16) |
+                       static_cast<unsigned long long>(0xffffu - static_cast<uint32_t>(j));
         }
     }
     __syncthreads();
-    // ranks by (score desc, depth asc, creation asc); scores compared through
-    // their order-preserving bits, a strict total order even for NaN
-    for (int j = 1 + threadIdx.x; j < np; j += blockDim.x) {
-        const uint32_t sj = ordered_bits(s_sc[j]);
-        const int dj = s_dep[j];
+    // the rank of pool node j >= 1: the nodes before it, four threads per node
+    // each counting a quarter (blockDim is a multiple of 32: every lane of a
+    // warp runs each round)
+    for (int t0 = 0; t0 < 4 * (np - 1); t0 += blockDim.x) {
+        const int t = t0 + static_cast<int>(threadIdx.x);
+        const int j = 1 + (t >> 2);
         int rank = 0;
-        for (int q = 1; q < np; ++q) {
-            const uint32_t sq = ordered_bits(s_sc[q]);
-            const int dq = s_dep[q];
-            rank += (q != j && (sq > sj || (sq == sj && (dq < dj || (dq == dj && q < j))))) ? 1 : 0;
+        if (j < np) {
+            const unsigned long long kj = s_key[j];
+            for (int q = 1 + (t & 3); q < np; q += 4) rank += s_key[q] > kj ? 1 : 0;
         }
-        if (rank < take) {
+        rank += __shfl_xor_sync(0xffffffffu, rank, 1);
+        rank += __shfl_xor_sync(0xffffffffu, rank, 2);
+        if (j < np && (t & 3) == 0 && rank < take) {
             slot_of[j] = rank + 1;
             node_at[rank + 1] = j;
         }
@@ -708,8 +716,8 @@ __global__ void tree_finalize_kernel(int R, int P, int B, int N, const int32_t* 
             const int j = node_at[c];
             tok[ob + c] = pool_tok[pb + j];
             parent[ob + c] = (c == 0) ? -1 : slot_of[s_par[j]];
-            depth[ob + c] = s_dep[j];
-            score[ob + c] = (c == 0) ? 0.f : s_sc[j];
+            depth[ob + c] = 0x7fff - static_cast<int>((s_key[j] >> 16) & 0xffffu);
+            score[ob + c] = (c == 0) ? 0.f : key_value(s_key[j]);
             for (int w = 0; w < words; ++w) {   // bit sa of the row: ancestors (and the node) in word w
                 uint32_t bits = 0u;
                 for (int a = j; a >= 0; a = (a == 0 ? -1 : s_par[a])) {
@@ -904,9 +912,8 @@ cudaError_t launch_tree_finalize(int R, int P, int B, int N, const int32_t* pool
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    tree_finalize_kernel<<<R, 128, smem, s>>>(R, P, B, N, pool_tok, pool_parent, pool_depth, pool_score, pool_n, tok,
-                                              parent, depth, score, mask, n_nodes);
-    return cudaGetLastError();
+    return launch_pdl(tree_finalize_kernel, dim3(R), dim3(256), smem, s, R, P, B, N, pool_tok, pool_parent, pool_depth,
+                      pool_score, pool_n, tok, parent, depth, score, mask, n_nodes);
 }
 
 cudaError_t launch_tree_verify_walk(const unsigned long long* row_keys, int n_chunks, const int32_t* tok, const int32_t* parent,
