@@ -516,6 +516,8 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
                                           int rows_avail, int32_t* dev_status) {
     // one warp per request; lane p runs the accept test of window row p (all
     // rows at once, each from its own partials), the first failure wins
+    pdl_wait();
+    pdl_trigger();
     const int i = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (i >= R) return;
@@ -606,6 +608,8 @@ __global__ void verify_sample_scan_kernel(int mode, const int32_t* cu, const int
 __global__ void tree_init_kernel(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
                                  float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
                                  int32_t* pool_depth, float* pool_score, int32_t* pool_n, int32_t* dev_status) {
+    pdl_wait();
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= R) return;
     const int pool_cap = 1 + P * B;
@@ -874,20 +878,19 @@ cudaError_t launch_verify_sample_scan(int mode, const int32_t* cu, const int32_t
                                       int32_t* ceiling, int32_t* res_tok, int32_t* res_pos, int32_t* res_trow,
                                       float* res_lse_p, int32_t* bonus_row, int32_t* bonus_pos, int rows_avail,
                                       int32_t* dev_status, cudaStream_t s) {
-    verify_sample_scan_kernel<<<blocks_for(static_cast<long long>(R) * 32, 128), 128, 0, s>>>(
-        mode, cu, anchor, draft, budget, logq, target, t_fp32, V, lse_part, n_chunks, inv_t, k0, k1, cycle, R, gamma,
-        accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos, rows_avail, dev_status);
-    return cudaGetLastError();
+    return launch_pdl(verify_sample_scan_kernel, dim3(blocks_for(static_cast<long long>(R) * 32, 128)), dim3(128), 0,
+                      s, mode, cu, anchor, draft, budget, logq, target, t_fp32, V, lse_part, n_chunks, inv_t, k0, k1,
+                      cycle, R, gamma, accept, ceiling, res_tok, res_pos, res_trow, res_lse_p, bonus_row, bonus_pos,
+                      rows_avail, dev_status);
 }
 
 cudaError_t launch_tree_init(const int32_t* anchor, int R, int P, int B, int32_t* front_tok, int32_t* front_node,
                              float* front_score, int32_t* n_front, int32_t* pool_tok, int32_t* pool_parent,
                              int32_t* pool_depth, float* pool_score, int32_t* pool_n, int32_t* dev_status,
                              cudaStream_t s) {
-    tree_init_kernel<<<blocks_for(R, 128), 128, 0, s>>>(anchor, R, P, B, front_tok, front_node, front_score, n_front,
-                                                        pool_tok, pool_parent, pool_depth, pool_score, pool_n,
-                                                        dev_status);
-    return cudaGetLastError();
+    return launch_pdl(tree_init_kernel, dim3(blocks_for(R, 128)), dim3(128), 0, s, anchor, R, P, B, front_tok,
+                      front_node, front_score, n_front, pool_tok, pool_parent, pool_depth, pool_score, pool_n,
+                      dev_status);
 }
 
 cudaError_t launch_tree_merge(const float2* row_top, const float* row_lse, int R, int P, int k, int B, int d,
