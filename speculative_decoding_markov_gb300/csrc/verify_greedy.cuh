@@ -41,6 +41,9 @@ __device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const 
                                                int n_chunks, int gamma, int V, int rows_avail, int total,
                                                int32_t* accept, int32_t* ceiling, int32_t* out_tok, int32_t* n_out,
                                                int32_t* dev_status) {
+    // the first 32 drafts load with the window's bounds (independent loads)
+    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
+    const int y0 = lane < gamma ? y[lane] : -1;
     const int row0 = cu[i];
     const int row1 = cu[i + 1];
     int32_t* o = out_tok + static_cast<size_t>(i) * (gamma + 1);
@@ -67,7 +70,6 @@ __device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const 
             cap = cap < 0 ? 0 : w;
         }
     }
-    const int32_t* y = draft + static_cast<size_t>(i) * gamma;
     // the first 32 window rows (the row after the last draft included) in
     // one round: lane p holds row p's target token
     const int t0 = lane <= w ? row_token(row_keys, static_cast<size_t>(row0 + lane), n_chunks) : -1;
@@ -75,7 +77,7 @@ __device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const 
     for (int base = 0; base < w && A == w; base += 32) {
         const int p = base + lane;
         const int tp = base == 0 ? t0 : (p < w ? row_token(row_keys, static_cast<size_t>(row0 + p), n_chunks) : -1);
-        const bool mism = p < w && y[p] != tp;
+        const bool mism = p < w && (base == 0 ? y0 : y[p]) != tp;
         const unsigned bal = __ballot_sync(0xffffffffu, mism);
         if (bal) A = base + __ffs(bal) - 1;
     }
@@ -83,7 +85,7 @@ __device__ __forceinline__ void greedy_resolve(int i, int lane, int mode, const 
     const int ta = __shfl_sync(0xffffffffu, t0, a & 31);
     for (int p = lane; p <= gamma; p += 32) {
         if (p < a) {
-            o[p] = y[p];
+            o[p] = p < 32 ? y0 : y[p];   // p < 32: p is this lane
         } else if (p == a) {
             int t = a < 32 ? ta : row_token(row_keys, static_cast<size_t>(row0 + a), n_chunks);
             if (t < 0 || t >= V) {
