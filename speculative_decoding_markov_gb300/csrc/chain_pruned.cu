@@ -374,19 +374,15 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     __shared__ int s_pk0, s_pkn;                                    // the request's ragged window, if any
     const float cmax = *p.c_max;
     const int seg0 = row * B * nc;
+    // the request's ragged window (if the drafts go into one): loaded now,
+    // used only when the tokens are written, so its latency hides under the
+    // staging below
+    int pk_c0 = 0, pk_c1 = -1;
     if (threadIdx.x == 0) {
         s_alloc = 0;
-        s_pk0 = 0;
-        s_pkn = -1;
         if (p.pack_tok) {
-            const int c0 = p.pack_cu[row], c1 = p.pack_cu[row + 1];
-            int n = c1 - c0 - 1;
-            if (n > B || n < 0) {
-                if (n > B) set_status(p.dev_status, SDM_DEV_BAD_WINDOW);
-                n = n > B ? B : -1;
-            }
-            s_pk0 = c0;
-            s_pkn = n;
+            pk_c0 = p.pack_cu[row];
+            pk_c1 = p.pack_cu[row + 1];
         }
     }
     for (int t = threadIdx.x; t <= kRowCapMax; t += kThreads) s_rowkey[t] = 0ull;
@@ -535,6 +531,19 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
         if (lane == 0) s_cprev0 = p.c_bound[a];
     }
     cp_async_wait_all();
+    if (threadIdx.x == 0) {
+        s_pk0 = 0;
+        s_pkn = -1;
+        if (p.pack_tok) {
+            int n = pk_c1 - pk_c0 - 1;
+            if (n > B || n < 0) {
+                if (n > B) set_status(p.dev_status, SDM_DEV_BAD_WINDOW);
+                n = n > B ? B : -1;
+            }
+            s_pk0 = pk_c0;
+            s_pkn = n;
+        }
+    }
     __syncthreads();
 
     // Pair scores: for every step d whose ids are staged and whose possible
