@@ -357,6 +357,13 @@ class Cycle:
         main = torch.cuda.current_stream()
         self.side.wait_stream(main)
         fused = self.prepared is not None and not self.rnn
+        if fused and self.front_one_launch():
+            # the scheduler and the layout in the draft's own first launch
+            # (one extra CTA of the scan), the pick filling the layout
+            sdm.draft_chain_front(i["L"], i["U"], i["W"], i["anchor"], self.prepared, i["conf"], i["cost"],
+                                  i["tiers"], use_budget=self.mode == sdm.COMPACT, tokens=self.dr["tokens"],
+                                  sched=self.sc, pk=self.pk, ws=self.ws_draft, dev_status=self.status)
+            return
         with torch.cuda.stream(self.side):
             self.schedule()
             if fused:
@@ -410,6 +417,26 @@ class Cycle:
         self.sdm.observe(self.inp["conf"], self.pk["cu_seqlens"], self.vr["ceiling"], self.cls, self.n_class,
                          self.n_bins, out=self.st, dev_status=self.status)
 
+    def front_one_launch(self):
+        """Whether the budget scheduler and the layout ride in the draft's scan
+        (sdm_draft_chain_front): the budget scheduler, its shared memory within
+        the 48 KB the scan is launched with, and a scan that fills every SM
+        (four 32 KB items per SM or more).  Only then does a side-stream
+        scheduler wait for the scan to drain; on a smaller scan it runs beside
+        it at once, with four times the threads of the scan's extra CTA."""
+        if self.tau is not None or self.dynamic or self.prepared is None or self.rnn or self.tree:
+            return False
+        esz = 4 if self.w.l_dtype == self.sdm.FP32 else 2
+        items = self.w.R * self.w.B * -(-self.w.V * esz // (32 * 1024))
+        if items < 4 * self.torch.cuda.get_device_properties(0).multi_processor_count:
+            return False
+        n = self.w.R * self.w.B
+        n_pad = 1
+        while n_pad < n:
+            n_pad <<= 1
+        smem = n_pad * 8 + 256 * 8 + self.w.R * 4 + n * 4 + (n_pad + 1) * 4
+        return n <= 8192 and smem <= 48 * 1024
+
     def launches_per_step(self):
         if self.tree:   # init, scan, per level the GEMM and the level kernel, finalize; verify stream and walk
             return (2 * self.w.B + 3) + 2
@@ -420,7 +447,8 @@ class Cycle:
         verify = 5 if self.sample else 2
         if self.obs:   # row stream, row list, [draft log-sum-exp pass + reduction], label pass + reduction, stats
             verify += 5 if self.sample else 7
-        return draft + 1 + 1 + verify
+        schedule_pack = 0 if self.front_one_launch() else 2   # inside the draft's scan, or two launches
+        return draft + schedule_pack + verify
 
     def capture(self):
         """CUDA graphs of the two timed segments (the stand-in gather between

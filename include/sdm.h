@@ -194,6 +194,40 @@ sdm_status sdm_draft_chain_packed(const void* L, sdm_dtype dtL, const uint16_t* 
                                   int32_t* tokens, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /*
+ * draft_chain_front: the greedy chain draft together with the budget
+ * scheduler and the ragged layout of its windows, in one call whose outputs
+ * equal, bit for bit, those of
+ *     sdm_schedule_budget(conf, R, B, cost, survival, budget, expected,
+ *                         total_tokens)
+ *     sdm_pack_ragged(anchor, NULL, use_budget ? budget : NULL, R, B, tiers,
+ *                     n_tiers, strict, cu_seqlens, packed_tok, packed_req,
+ *                     packed_pos, capacity, tier)
+ *     sdm_draft_chain_packed(L, ..., prepared, anchor, R, B, V, r,
+ *                            cu_seqlens, packed_tok, capacity, NULL, tokens)
+ * ([DSpark notes] sec. 4, 5.1-5.2; [SGLang] "ragged verify").  The scheduler
+ * and the layout need only the confidences, so they run in one extra CTA of
+ * the draft's first (vocabulary-streaming) launch, beside its other CTAs,
+ * and the pick writes the drafts into the layout; nothing runs on a second
+ * stream.  It pays when the scan fills every SM (a side-stream scheduler
+ * then waits for the scan to drain: 67.4 against 70.5 us per decode cycle
+ * of 64 requests, B 7, V 151936); on a scan of a few CTAs the scheduler's
+ * CTA is the longer path, and the three calls with the scheduler on a second
+ * stream are faster.  Requires the prepared tables and R * B <= 8192 with the
+ * scheduler's shared memory (about 16 (R B) bytes rounded up) within 48 KB,
+ * else SDM_ERR_UNSUPPORTED (use the three calls).  Arguments as in those
+ * calls; use_budget 1 packs budget[i] drafts per request (compact), 0 all B
+ * (static); the tier's host copy is not offered.  Workspace: as
+ * SDM_OP_DRAFT_CHAIN.
+ */
+sdm_status sdm_draft_chain_front(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                                 const void* prepared, const int32_t* anchor, int R, int B, int V, int r,
+                                 const float* conf, const double* cost, int use_budget, const int32_t* tiers,
+                                 int n_tiers, int strict, float* survival, int32_t* budget, double* expected,
+                                 int32_t* total_tokens, int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
+                                 int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tokens, void* ws,
+                                 size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/*
  * draft_chain_rnn: the chain draft with the RNN sequential head ([DSpark
  * notes] sec. 4, "RNN head": a memo that carries the whole draft so far,
  * updated once per step from the previous memo, the previous word and the

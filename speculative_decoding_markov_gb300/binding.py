@@ -28,7 +28,7 @@ EXPORTS = ("sdm_workspace_size", "sdm_markov_prepared_size", "sdm_markov_prepare
            "sdm_draft_tree", "sdm_schedule_budget", "sdm_pack_ragged", "sdm_verify", "sdm_verify_tree",
            "sdm_verify_greedy_static", "sdm_schedule_dynamic", "sdm_tv_label", "sdm_observe", "sdm_schedule_threshold",
            "sdm_threshold_sweep", "sdm_draft_chain_rnn", "sdm_status_str", "sdm_status_of_device", "sdm_check_timeout_path",
-           "sdm_draft_chain_packed",
+           "sdm_draft_chain_packed", "sdm_draft_chain_front",
            "sdm_version")
 
 
@@ -62,6 +62,9 @@ def _declare(lib):
     lib.sdm_schedule_dynamic.argtypes = [_VP, _VP, _I, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]
     lib.sdm_pack_ragged.restype = _I
     lib.sdm_pack_ragged.argtypes = [_VP, _VP, _VP, _I, _I, _VP, _I, _I, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP]
+    lib.sdm_draft_chain_front.restype = _I
+    lib.sdm_draft_chain_front.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _I, _VP, _I, _I,
+                                          _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _SZ, _VP, _VP]
     lib.sdm_draft_chain_packed.restype = _I
     lib.sdm_draft_chain_packed.argtypes = [_VP, _I, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _VP, _VP, _I, _VP, _VP, _VP,
                                            _SZ, _VP, _VP]
@@ -204,6 +207,41 @@ def draft_chain_packed(L, U, W, anchor, prepared, cu_seqlens, packed_tok, tokens
                                       _ptr(tokens), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
     _check(st, "sdm_draft_chain_packed")
     return dict(tokens=tokens, dev_status=dev_status)
+
+
+def draft_chain_front(L, U, W, anchor, prepared, conf, cost, tiers, use_budget=True, strict=False, tokens=None,
+                      sched=None, pk=None, capacity=None, ws=None, dev_status=None):
+    """Greedy chain draft (prepared tables) with the budget scheduler and the
+    ragged layout in the same launches: the outputs of schedule_budget,
+    pack_ragged(draft=None) and draft_chain_packed.  sched / pk: output dicts
+    as those calls return (made here when None)."""
+    _need_cuda(L, U, W, anchor, conf, cost, tiers)
+    R, B, V = L.shape
+    r = U.shape[1]
+    dev = L.device
+    tokens = torch.empty((R, B), dtype=torch.int32, device=dev) if tokens is None else tokens
+    if sched is None:
+        sched = dict(survival=torch.empty((R, B), dtype=torch.float32, device=dev),
+                     budget=torch.empty((R,), dtype=torch.int32, device=dev),
+                     expected=torch.empty((1,), dtype=torch.float64, device=dev),
+                     total_tokens=torch.empty((1,), dtype=torch.int32, device=dev))
+    if pk is None:
+        cap = capacity if capacity else pack_capacity(R, B, tiers.tolist())
+        pk = dict(cu_seqlens=torch.empty((R + 1,), dtype=torch.int32, device=dev),
+                  packed_tok=torch.empty((cap,), dtype=torch.int32, device=dev),
+                  packed_req=torch.empty((cap,), dtype=torch.int32, device=dev),
+                  packed_pos=torch.empty((cap,), dtype=torch.int32, device=dev),
+                  tier=torch.empty((1,), dtype=torch.int32, device=dev))
+    ws = workspace(OP_DRAFT_CHAIN, R, B, V, r, device=dev) if ws is None else ws
+    dev_status = new_status(dev) if dev_status is None else dev_status
+    st = lib().sdm_draft_chain_front(
+        _ptr(L), _dt(L), _ptr(_u16(U)), _ptr(_u16(W)), _ptr(prepared), _ptr(anchor), R, B, V, r, _ptr(conf),
+        _ptr(cost), 1 if use_budget else 0, _ptr(tiers), tiers.numel(), 1 if strict else 0, _ptr(sched["survival"]),
+        _ptr(sched["budget"]), _ptr(sched["expected"]), _ptr(sched["total_tokens"]), _ptr(pk["cu_seqlens"]),
+        _ptr(pk["packed_tok"]), _ptr(pk["packed_req"]), _ptr(pk["packed_pos"]), pk["packed_tok"].numel(),
+        _ptr(pk["tier"]), _ptr(tokens), _ptr(ws), ws.numel(), _ptr(dev_status), _stream())
+    _check(st, "sdm_draft_chain_front")
+    return dict(tokens=tokens, sched=sched, pk=pk, dev_status=dev_status)
 
 
 def check_timeout_path(L, U, W, anchor, wait_ns, dev_status=None):

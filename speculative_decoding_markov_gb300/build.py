@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libsdm.so")
 SOURCES = ("markov_gemm.cu", "chain_pruned.cu", "stream.cu", "select.cu", "small.cu", "api.cu", "no_alloc.cu", "observe.cu", "threshold.cu", "rnn.cu", "tree_pruned.cu")
-HEADERS = ("device.cuh", "internal.h", "verify_greedy.cuh", "tree_common.cuh")
+HEADERS = ("device.cuh", "internal.h", "verify_greedy.cuh", "tree_common.cuh", "schedule_pack.cuh")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -452,6 +452,82 @@ sdm_status sdm_draft_chain_packed(const void* L, sdm_dtype dtL, const uint16_t* 
     return SDM_OK;
 }
 
+sdm_status sdm_draft_chain_front(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W,
+                                 const void* prepared, const int32_t* anchor, int R, int B, int V, int r,
+                                 const float* conf, const double* cost, int use_budget, const int32_t* tiers,
+                                 int n_tiers, int strict, float* survival, int32_t* budget, double* expected,
+                                 int32_t* total_tokens, int32_t* cu_seqlens, int32_t* packed_tok, int32_t* packed_req,
+                                 int32_t* packed_pos, int capacity, int32_t* tier, int32_t* tokens, void* ws,
+                                 size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!L || !U || !W || !prepared || !anchor || !conf || !cost || !survival || !budget || !expected ||
+        !total_tokens || !cu_seqlens || !packed_tok || !packed_req || !packed_pos || !tier || !tokens || R <= 0 ||
+        B <= 0 || V <= 0 || r <= 0 || capacity <= 0 || n_tiers < 0 || (n_tiers > 0 && !tiers))
+        return SDM_ERR_INVALID_ARG;
+    if (dtL != SDM_BF16 && dtL != SDM_FP32) return SDM_ERR_INVALID_ARG;
+    if ((strict != 0 && strict != 1) || (use_budget != 0 && use_budget != 1)) return SDM_ERR_INVALID_ARG;
+    if (!vocab_ok(V) || !rank_ok(r) || !aligned16(L) || !aligned16(U) || !aligned16(W) || !aligned16(prepared))
+        return SDM_ERR_UNSUPPORTED;
+    const int n_chunks = pruned_chunks(V, dtL == SDM_FP32);
+    if (B > kMaxPickSteps || n_chunks > kMaxPickChunks || static_cast<long long>(R) * B * n_chunks > (1LL << 30))
+        return SDM_ERR_UNSUPPORTED;
+    if (static_cast<long long>(R) * B > 8192 || chain_front_smem(R, B) > kFrontSmemMax) return SDM_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < ws_chain(R, B, V)) return SDM_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    Carver pc{static_cast<uint8_t*>(const_cast<void*>(prepared))};
+    PrunedParams pp;
+    std::memset(&pp, 0, sizeof pp);
+    pp.L = L;
+    pp.l_fp32 = dtL == SDM_FP32;
+    pp.R = R;
+    pp.B = B;
+    pp.V = V;
+    pp.r = r;
+    pp.n_chunks = n_chunks;
+    pp.anchor = anchor;
+    pp.U = U;
+    pp.Wt = pc.take<uint16_t>(static_cast<size_t>(V) * r);
+    pp.c_bound = pc.take<float>(V);
+    pc.take<float>(V);           // |U[v]|
+    pc.take<unsigned int>(V);    // A(v)
+    pp.c_max = pc.take<float>(1);
+    Carver wc{static_cast<uint8_t*>(ws)};
+    const size_t segs = static_cast<size_t>(R) * B * n_chunks;
+    pp.cand = wc.take<uint2>(segs * kSegCap);
+    pp.cand_n = wc.take<int32_t>(segs);
+    pp.cmax = wc.take<float>(segs);
+    pp.tokens = tokens;
+    pp.dev_status = dev_status;
+    pp.pack_cu = cu_seqlens;
+    pp.pack_tok = packed_tok;
+    pp.pack_cap = capacity;
+    FrontParams& fr = pp.fr;
+    fr.on = 1;
+    fr.conf = conf;
+    fr.cost = cost;
+    fr.survival = survival;
+    fr.budget = budget;
+    fr.expected = expected;
+    fr.total_tokens = total_tokens;
+    int n_pad = 1;
+    while (n_pad < R * B) n_pad <<= 1;
+    fr.n_pad = n_pad;
+    fr.use_budget = use_budget;
+    fr.tiers = tiers;
+    fr.n_tiers = n_tiers;
+    fr.strict = strict;
+    fr.cu = cu_seqlens;
+    fr.ptok = packed_tok;
+    fr.preq = packed_req;
+    fr.ppos = packed_pos;
+    fr.capacity = capacity;
+    fr.tier = tier;
+    // one launch lists the candidates and, in its first CTA, schedules and
+    // lays out the windows; the pick (programmatic launch) waits for all of it
+    SDM_CHECK_CUDA(launch_chain_scan(pp, s));
+    SDM_CHECK_CUDA(launch_chain_pick(pp, s));
+    return SDM_OK;
+}
+
 sdm_status sdm_draft_chain_rnn(const void* L, sdm_dtype dtL, const uint16_t* U, const uint16_t* W, const uint16_t* A,
                                const uint16_t* X, const int32_t* anchor, int R, int B, int V, int r, sdm_decode decode,
                                float temperature, sdm_rng rng, int32_t* tokens, float* logq, float* lse, float* memo,

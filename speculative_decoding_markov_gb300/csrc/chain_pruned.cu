@@ -28,6 +28,7 @@
 
 #include "device.cuh"
 #include "internal.h"
+#include "schedule_pack.cuh"
 
 namespace sdm {
 namespace {
@@ -35,6 +36,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 static_assert(kMaxTopK <= kWarps, "the scan's k-th threshold ranks the warps' maxima");
+static_assert(kThreads == kPackThreads, "the scan's front CTA runs the pack block");
 constexpr int kListHead = 32;   // list entries the pick kernel loads with the list length
 
 template <int FP32>
@@ -112,17 +114,31 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
     constexpr int CHUNK_IDS = kChunkBytes / ESZ;
     __shared__ float s_wmax[kWarps];
     __shared__ int s_cnt[2];   // by item parity: a slot is reset two items after its last read
+    extern __shared__ unsigned long long s_front[];   // the scheduler's arrays (the front CTA's only)
     pdl_wait();
     pdl_trigger();
+    if (p.fr.on && blockIdx.x == 0) {
+        // the front CTA (dispatched first): budgets, then the windows' layout
+        // from them (the block barrier orders the budgets' global writes
+        // before the pack reads them)
+        schedule_block(p.fr.conf, p.R, p.B, p.fr.cost, p.fr.survival, p.fr.budget, p.fr.expected,
+                       p.fr.total_tokens, p.fr.n_pad, s_front, kThreads);
+        __syncthreads();
+        pack_block(p.anchor, nullptr, p.fr.use_budget ? p.fr.budget : nullptr, p.R, p.B, p.fr.tiers, p.fr.n_tiers,
+                   p.fr.strict, p.fr.cu, p.fr.ptok, p.fr.preq, p.fr.ppos, p.fr.capacity, p.fr.tier, p.dev_status);
+        return;
+    }
+    const int g0 = p.fr.on ? 1 : 0;
+    const int G = static_cast<int>(gridDim.x) - g0;   // the scanning CTAs
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nc = p.n_chunks;
     const int items = p.R * p.B * nc;       // <= 2^30 (checked by the host)
     const float cmax = *p.c_max;
     // item it = rs * nc + c, rs = request * B + (d - 1): walk (rs, c) by the
     // grid stride without dividing per item
-    int it = blockIdx.x;
+    int it = static_cast<int>(blockIdx.x) - g0;
     int rs = it / nc, c = it - rs * nc;
-    const int srs = gridDim.x / nc, sc = gridDim.x - srs * nc;
+    const int srs = G / nc, sc = G - srs * nc;
     const uint8_t* L = static_cast<const uint8_t*>(p.L);
     for (int par = 0; it < items; par ^= 1) {
         int nrs = rs + srs, ncc = c + sc;
@@ -199,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 4) chain_scan_kernel(const PrunedPar
         // the head of the list (kListHead entries) is always written, so that
         // the pick kernel's speculative head loads hit L2
         if (threadIdx.x >= cnt && threadIdx.x < kListHead) out[threadIdx.x] = make_uint2(0xffffffffu, 0u);
-        it += gridDim.x;
+        it += G;
         rs = nrs;
         c = ncc;
     }
@@ -889,8 +905,16 @@ cudaError_t launch_chain_scan(const PrunedParams& p, cudaStream_t s) {
     // two CTAs per resident slot: a CTA that finishes early is replaced, which
     // evens out the tail better than one wave of equal shares
     const int grid = static_cast<int>(items < 8LL * num_sms() ? items : 8LL * num_sms());
-    return p.l_fp32 ? launch_pdl(chain_scan_kernel<1>, dim3(grid), dim3(kThreads), 0, s, p)
-                    : launch_pdl(chain_scan_kernel<0>, dim3(grid), dim3(kThreads), 0, s, p);
+    const size_t smem = p.fr.on ? chain_front_smem(p.R, p.B) : 0;
+    if (smem > kFrontSmemMax) return cudaErrorInvalidValue;
+    return p.l_fp32 ? launch_pdl(chain_scan_kernel<1>, dim3(grid + (p.fr.on ? 1 : 0)), dim3(kThreads), smem, s, p)
+                    : launch_pdl(chain_scan_kernel<0>, dim3(grid + (p.fr.on ? 1 : 0)), dim3(kThreads), smem, s, p);
+}
+
+size_t chain_front_smem(int R, int B) {
+    int n_pad = 1;
+    while (n_pad < R * B) n_pad <<= 1;
+    return schedule_smem_bytes(R, B, n_pad, kThreads);
 }
 
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s) {

@@ -344,6 +344,30 @@ constexpr int kSegCap = 512;                   // listed ids per chunk
 constexpr int kMaxPickSteps = 64;              // B limit of the pruned chain
 constexpr int kMaxPickChunks = 64;             // chunks-per-row limit of the pruned chain
 
+// The budget scheduler and the ragged layout run by one extra CTA of the
+// greedy chain's scan (on != 0): from the confidences, costs and tiers alone,
+// while the scan's other CTAs list the candidates; the pick then writes its
+// drafts into that layout.
+struct FrontParams {
+    int on;
+    const float* conf;        // [R, B] confidences
+    const double* cost;       // [R (B + 1) + 1] step costs
+    float* survival;          // [R, B]
+    int32_t* budget;          // [R]
+    double* expected;         // [1]
+    int32_t* total_tokens;    // [1]
+    int n_pad;                // R B rounded up to a power of two
+    int use_budget;           // pack budget[i] drafts (compact) or all B (static)
+    const int32_t* tiers;
+    int n_tiers, strict;
+    int32_t* cu;              // [R + 1]
+    int32_t* ptok;            // [capacity]
+    int32_t* preq;
+    int32_t* ppos;
+    int capacity;
+    int32_t* tier;            // [1]
+};
+
 struct PrunedParams {
     const void* L;
     int l_fp32;
@@ -365,6 +389,7 @@ struct PrunedParams {
     const int32_t* pack_cu;
     int32_t* pack_tok;
     int pack_cap;
+    FrontParams fr;         // the scan's extra CTA (fr.on): scheduler and layout
 };
 // The scan alone, then (after the caller's dependency, e.g. an event wait)
 // the pick alone.
@@ -373,8 +398,13 @@ cudaError_t launch_chain_pick(const PrunedParams& p, cudaStream_t s);
 int pruned_chunks(int V, int l_fp32);
 cudaError_t launch_chain_pruned(const PrunedParams& p, cudaStream_t s);
 // The candidate lists alone (every (request, step) row), for a top-k of
-// kth > 1 (PCTree levels).
+// kth > 1 (PCTree levels); with p.fr.on one more CTA runs the scheduler and
+// the ragged layout.
 cudaError_t launch_chain_scan(const PrunedParams& p, cudaStream_t s);
+// Dynamic shared memory of the scan's scheduler CTA (0 when off); the fused
+// front is offered up to kFrontSmemMax.
+size_t chain_front_smem(int R, int B);
+constexpr size_t kFrontSmemMax = 48 * 1024;
 // Prepared tables, step 1: W^T, |U[v]|, max |W[:, v]| and max |U[v]|; zeroes
 // absmax_bits for the absmax GEMM.  Step 2 (after that GEMM): the bounds.
 cudaError_t launch_markov_prepare(const uint16_t* U, const uint16_t* W, int V, int r, uint16_t* Wt, float* u_norm,

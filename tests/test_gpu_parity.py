@@ -755,6 +755,32 @@ def test_draft_chain_packed_fills_the_layout(case):
         assert torch.equal(lay[k], full[k]), k
 
 
+@pytest.mark.parametrize("case", [dict(R=64, B=7, V=8200, r=128), dict(R=5, B=3, V=2056, r=64),
+                                  dict(R=300, B=6, V=4104, r=64), dict(R=37, B=16, V=8200, r=256)])
+@pytest.mark.parametrize("use_budget", [True, False])
+def test_draft_chain_front_equals_the_three_calls(case, use_budget):
+    """The greedy draft with the scheduler and the layout in its own launches
+    (the scan's extra CTA) gives, bit for bit, schedule_budget, then
+    pack_ragged with the drafts (budgets for compact, all B for static), and
+    sdm_draft_chain's tokens."""
+    w = small(l_dtype=BF16, sigma=(0.5,), l_std=2.0, conf="sigmoid", cost=(2.0, 0.004), **case)
+    inp = {k: dev(v) for k, v in synthetic.generate(w, seed=case["R"] + 1).items()}
+    prep = sdm.markov_prepare(inp["U"], inp["W"])
+    ref = sdm.draft_chain(inp["L"], inp["U"], inp["W"], inp["anchor"], prepared=prep)
+    sc = sdm.schedule_budget(inp["conf"], inp["cost"])
+    full = sdm.pack_ragged(inp["anchor"], ref["tokens"], sc["budget"] if use_budget else None, inp["tiers"])
+    out = sdm.draft_chain_front(inp["L"], inp["U"], inp["W"], inp["anchor"], prep, inp["conf"], inp["cost"],
+                                inp["tiers"], use_budget=use_budget, capacity=full["packed_tok"].numel())
+    torch.cuda.synchronize()
+    assert int(out["dev_status"].item()) & ~sdm.DEV_TIER_UNCAPTURED == 0
+    assert int(out["dev_status"].item()) == int(full["dev_status"].item()) | int(ref["dev_status"].item())
+    assert torch.equal(out["tokens"], ref["tokens"])
+    for k in ("survival", "budget", "expected", "total_tokens"):
+        assert torch.equal(out["sched"][k], sc[k]), k
+    for k in ("cu_seqlens", "packed_tok", "packed_req", "packed_pos", "tier"):
+        assert torch.equal(out["pk"][k], full[k]), k
+
+
 def test_pack_layout_alone_holds_the_anchors():
     """Without drafts the layout's window rows hold the anchor first and -1
     where the drafts go; the offsets and row maps are those of the full pack."""
