@@ -108,11 +108,12 @@ def measured_burst_tflops(default):
 
 
 KERNEL_SOURCES = {   # the files whose text fixes each reported kernel's code
-    "chain_scan_kernel+chain_pick_kernel": ("chain_pruned.cu", "device.cuh", "internal.h"),
+    "chain_scan_kernel+chain_pick_kernel": ("chain_pruned.cu", "schedule_pack.cuh", "device.cuh", "internal.h"),
     "markov_gemm_kernel<sample>+draft_select_kernel": ("markov_gemm.cu", "select.cu", "device.cuh", "internal.h"),
     "markov_gemm_kernel<tree>+tree_select_kernel": ("markov_gemm.cu", "select.cu", "device.cuh", "internal.h"),
     "markov_gemm_kernel<tree_lse>+tree_level_kernel": ("markov_gemm.cu", "tree_pruned.cu", "tree_common.cuh",
-                                                       "chain_pruned.cu", "device.cuh", "internal.h"),
+                                                       "chain_pruned.cu", "schedule_pack.cuh", "device.cuh",
+                                                       "internal.h"),
     "row_stream_kernel<argmax>": ("stream.cu", "device.cuh", "internal.h"),
 }
 
