@@ -357,8 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     constexpr int VEC = FP32 ? 4 : 8;
     constexpr int kBatch = 4;   // list entries a lane loads at once (second round)
     constexpr int kHead = kListHead;
-    pdl_wait();
-    pdl_trigger();
     const int row = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nc = p.n_chunks, B = p.B, r = p.r;
@@ -388,7 +386,21 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
     __shared__ int s_m;
     __shared__ unsigned long long s_best[2];
     __shared__ int s_pk0, s_pkn;                                    // the request's ragged window, if any
+    // Before the wait, only what the scan does not write (the anchor and the
+    // prepared tables), so that its latency hides under the scan's tail:
+    // c_max, and U[anchor] and c(anchor) into shared memory (last warp).
     const float cmax = *p.c_max;
+    bool bad_anchor = false;
+    if (warp == kWarps - 1) {
+        int a = p.anchor[row];
+        bad_anchor = a < 0 || a >= p.V;
+        if (bad_anchor) a = 0;
+        if (lane * 8 < r) cp_async_16(u_anchor + lane * 8, p.U + static_cast<size_t>(a) * r + lane * 8, 16u);
+        if (lane == 0) s_cprev0 = p.c_bound[a];
+    }
+    pdl_wait();
+    pdl_trigger();
+    if (bad_anchor && lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
     const int seg0 = row * B * nc;
     // the request's ragged window (if the drafts go into one): loaded now,
     // used only when the tokens are written, so its latency hides under the
@@ -526,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
                     cp_async_16(st_u + static_cast<size_t>(slot) * RS + lane * 8, p.U + static_cast<size_t>(v) * r + lane * 8, 16u);
                 }
             }
-            for (int j = lane; j < kept; j += 32) st_c[off + j] = p.c_bound[st_key[off + j].x];
+            for (int j = lane; j < kept; j += 32) cp_async_4(st_c + off + j, p.c_bound + st_key[off + j].x);
         }
         if (lane == 0) {
             s_lmax[d] = m;
@@ -536,17 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) chain_pick_kernel(const PrunedPar
             s_staged[d] = fits;
         }
     }
-    // the anchor: U[anchor] as the pool's last U row, and its bound
-    if (warp == kWarps - 1) {
-        int a = p.anchor[row];
-        if (a < 0 || a >= p.V) {
-            if (lane == 0) set_status(p.dev_status, SDM_DEV_BAD_TOKEN);
-            a = 0;
-        }
-        if (lane * 8 < r) cp_async_16(u_anchor + lane * 8, p.U + static_cast<size_t>(a) * r + lane * 8, 16u);
-        if (lane == 0) s_cprev0 = p.c_bound[a];
-    }
-    cp_async_wait_all();
+    cp_async_wait_all();   // the staged rows and bounds, and U[anchor]
     if (threadIdx.x == 0) {
         s_pk0 = 0;
         s_pkn = -1;

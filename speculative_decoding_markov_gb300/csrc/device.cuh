@@ -261,6 +261,12 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src, uint32_t
                  : "memory");
 }
 
+// 4-byte asynchronous copy global -> shared (the .ca form: the only one that
+// takes sizes below 16 bytes); both addresses 4-byte aligned.
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
