@@ -153,7 +153,8 @@ def test_markov_prepare_bounds_full_vocab():
     assert float(t["c_max"]) < float(t["u_max"]) * float(t["n_max"])   # tighter than Cauchy-Schwarz
 
 
-@pytest.mark.parametrize("kind", ["all_equal", "outlier", "ties", "wide_markov", "crowded", "crowded_long"])
+@pytest.mark.parametrize("kind", ["all_equal", "outlier", "ties", "wide_markov", "crowded", "crowded_mid",
+                                  "crowded_long"])
 def test_draft_chain_prepared_adversarial(kind):
     """Inputs that defeat the pruning bound (every id a candidate: many batches),
     exact ties (lowest id wins), a dominant Markov term, and crowded rows whose
@@ -175,6 +176,8 @@ def test_draft_chain_prepared_adversarial(kind):
         L = torch.round(L.float() * 2).to(torch.bfloat16) / 2          # many exact ties
     elif kind == "wide_markov":
         L = (L.float() * 0.01).to(torch.bfloat16)                      # the Markov term decides
+    elif kind == "crowded_mid":
+        L = (L.float() * 0.5).to(torch.bfloat16)                       # lists around the pick's loaded head
     else:
         L = (L.float() * 0.3).to(torch.bfloat16)                       # ~60 candidates per step
     d = {k: dev(v) for k, v in inp.items()}
