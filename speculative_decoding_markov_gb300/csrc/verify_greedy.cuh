@@ -1,8 +1,8 @@
 // verify_greedy.cuh - greedy verification of one request from the per-chunk
 // argmax keys of its window rows ([DSpark notes] sec. 1: left-to-right
 // acceptance, discard after the first mismatch, one bonus token; [SGLang]
-// "three verify modes").  Shared by the stand-alone finalize kernel and the
-// argmax stream that resolves a request as soon as its last row is done.
+// "three verify modes").  Run by the finalize kernel, one warp per request,
+// after the argmax stream has written every row's per-chunk keys.
 #pragma once
 #include "device.cuh"
 #include "internal.h"
