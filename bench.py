@@ -345,11 +345,13 @@ class Cycle:
         self.pack()
 
     def front(self):
-        """Draft, schedule and pack.  The budget needs only the confidences,
-        so the scheduler runs on a side stream while the draft runs.  With the
-        greedy chain's prepared tables the side stream also lays out the
-        ragged windows from the budgets, and the draft's pick writes its
-        tokens into them (no pack pass after the draft); otherwise the pack
+        """Draft, schedule and pack.  The budget needs only the confidences.
+        With the greedy chain's prepared tables and a scan that fills the GPU,
+        the scheduler and the ragged layout run in one extra CTA of the draft's
+        scan and the pick writes its tokens into the layout (one call).
+        Otherwise the scheduler runs on a side stream while the draft runs;
+        with the prepared tables the side stream also lays out the windows and
+        the pick fills them (no pack pass after the draft), else the pack
         joins both."""
         if self.tree:
             self.draft()
