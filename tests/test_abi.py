@@ -108,6 +108,30 @@ def test_draft_chain_host_validation(lib):
     assert _chain(lib, dec=1, V=524288 + 8) == 2   # sampling: the draw's chunk table holds 32768 records
 
 
+def _front(lib, **kw):
+    a = dict(L=FAKE, dtL=0, prepared=FAKE, R=64, B=7, V=1024, r=64, use_budget=1, tiers=FAKE, n_tiers=2, strict=0,
+             capacity=1024, ws=FAKE, ws_bytes=1 << 30)
+    a.update(kw)
+    return lib.sdm_draft_chain_front(a["L"], a["dtL"], FAKE, FAKE, a["prepared"], FAKE, a["R"], a["B"], a["V"], a["r"],
+                                     FAKE, FAKE, a["use_budget"], a["tiers"], a["n_tiers"], a["strict"], FAKE, FAKE,
+                                     FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, a["capacity"], FAKE, FAKE, a["ws"],
+                                     a["ws_bytes"], None, None)
+
+
+def test_draft_chain_front_host_validation(lib):
+    assert _front(lib, prepared=None) == 1      # the bound-pruned chain needs the prepared tables
+    assert _front(lib, strict=2) == 1
+    assert _front(lib, use_budget=2) == 1
+    assert _front(lib, tiers=None) == 1         # tiers missing
+    assert _front(lib, capacity=0) == 1
+    assert _front(lib, V=1001) == 2             # V % 8 != 0
+    assert _front(lib, R=2000, B=8) == 2        # R * B > 8192: the scheduler ranks in shared memory
+    assert _front(lib, R=512, B=8) == 2         # R * B = 4096: the scheduler's arrays exceed 48 KB
+    assert _front(lib, B=65) == 2               # more steps than the pick walks
+    assert _front(lib, ws_bytes=16) == 5
+    assert lib.sdm_workspace_size(binding.OP_DRAFT_CHAIN, 64, 7, 1024, 64, 0, 0, 0) <= 1 << 30
+
+
 def test_prepare_host_validation(lib):
     assert lib.sdm_markov_prepared_size(151936, 256) >= 151936 * 256 * 2 + 3 * 151936 * 4
     assert lib.sdm_markov_prepare(None, FAKE, 1024, 64, FAKE, 1 << 30, None, None) == 1
