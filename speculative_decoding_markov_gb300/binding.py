@@ -137,6 +137,13 @@ def _need_cuda(*ts):
             raise ValueError("inputs must be contiguous CUDA tensors")
 
 
+def _need_cost(cost, R, gamma):
+    """The step-cost table the schedulers index up to cost[R * (gamma + 1)]:
+    fp64 with at least R * (gamma + 1) + 1 entries."""
+    if cost.dtype != torch.float64 or cost.numel() < R * (gamma + 1) + 1:
+        raise ValueError(f"cost must be fp64 with at least R*(gamma+1)+1 = {R * (gamma + 1) + 1} entries")
+
+
 def _u16(t):
     """bf16 tensors are passed by pointer; this only checks the dtype."""
     if t.dtype != torch.bfloat16:
@@ -217,6 +224,7 @@ def draft_chain_front(L, U, W, anchor, prepared, conf, cost, tiers, use_budget=T
     as those calls return (made here when None)."""
     _need_cuda(L, U, W, anchor, conf, cost, tiers)
     R, B, V = L.shape
+    _need_cost(cost, R, B)
     r = U.shape[1]
     dev = L.device
     tokens = torch.empty((R, B), dtype=torch.int32, device=dev) if tokens is None else tokens
@@ -312,6 +320,7 @@ def draft_tree(L, U, W, anchor, k, P, N, out=None, ws=None, dev_status=None, pre
 def schedule_budget(conf, cost, out=None, dev_status=None):
     _need_cuda(conf, cost)
     R, g = conf.shape
+    _need_cost(cost, R, g)
     dev = conf.device
     if out is None:
         out = dict(survival=torch.empty((R, g), dtype=torch.float32, device=dev),
@@ -333,6 +342,7 @@ def schedule_dynamic(conf, conf_stale, cost, out=None, dev_status=None):
     survivals."""
     _need_cuda(conf, conf_stale, cost)
     R, g = conf.shape
+    _need_cost(cost, R, g)
     assert tuple(conf_stale.shape) == (R, g)
     dev = conf.device
     if out is None:

@@ -228,3 +228,12 @@ def test_threshold_host_validation(lib):
     assert sw(FAKE, None, 4, 7, None, 3, FAKE, FAKE, FAKE, None, None) == 1      # thresholds missing
     assert sw(FAKE, None, 4, 7, FAKE, 0, FAKE, FAKE, FAKE, None, None) == 1      # K = 0
     assert sw(FAKE, None, 4096, 9, FAKE, 3, FAKE, FAKE, FAKE, None, None) == 2   # R gamma > 32768
+
+
+def test_binding_checks_the_cost_table():
+    import torch
+    binding._need_cost(torch.zeros(2 * 4 + 1, dtype=torch.float64), 2, 3)          # R (gamma + 1) + 1 entries
+    with pytest.raises(ValueError):
+        binding._need_cost(torch.zeros(2 * 4, dtype=torch.float64), 2, 3)          # one short
+    with pytest.raises(ValueError):
+        binding._need_cost(torch.zeros(2 * 4 + 1, dtype=torch.float32), 2, 3)      # not fp64
